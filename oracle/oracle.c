@@ -1,0 +1,453 @@
+/*
+ * oracle.c -- plain CPU reference of the gradient-averaging hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY (see oracle.h).  Single-threaded, no SIMD, no
+ * blocking or reordering beyond what the cited definitions state.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ===================================================================== */
+/* Philox4x32 [S]: a 4-word counter and a 2-word key; each round multiplies
+ * words 0 and 2 by the two round multipliers, mixes the high halves with
+ * words 1 and 3 and the key, and the key is advanced by the two Weyl
+ * increments between rounds.  The constants are the ones the SC'11 paper
+ * publishes for the 4x32 variant.                                          */
+/* ===================================================================== */
+#define PHILOX_MUL_A 0xD2511F53u
+#define PHILOX_MUL_B 0xCD9E8D57u
+#define PHILOX_WEYL_A 0x9E3779B9u
+#define PHILOX_WEYL_B 0xBB67AE85u
+
+void oracle_philox4x32(const uint32_t ctr[4], const uint32_t key[2], int rounds,
+                       uint32_t out[4]) {
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < rounds; ++r) {
+        if (r > 0) {
+            k0 += PHILOX_WEYL_A;
+            k1 += PHILOX_WEYL_B;
+        }
+        uint64_t prod_a = (uint64_t)PHILOX_MUL_A * (uint64_t)c0;
+        uint64_t prod_b = (uint64_t)PHILOX_MUL_B * (uint64_t)c2;
+        uint32_t hi_a = (uint32_t)(prod_a >> 32), lo_a = (uint32_t)prod_a;
+        uint32_t hi_b = (uint32_t)(prod_b >> 32), lo_b = (uint32_t)prod_b;
+        uint32_t n0 = hi_b ^ c1 ^ k0;
+        uint32_t n1 = lo_b;
+        uint32_t n2 = hi_a ^ c3 ^ k1;
+        uint32_t n3 = lo_a;
+        c0 = n0;
+        c1 = n1;
+        c2 = n2;
+        c3 = n3;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+/* ===================================================================== */
+/* Ring all-reduce [H] "The Ring-Allreduce Algorithm", [R] sections 4, 5, 7 */
+/* ===================================================================== */
+
+/* The buffer is cut into p chunks.  The pages only give the case where p
+ * divides n; for other n every chunk but the trailing ones has ceil(n/p)
+ * elements and the trailing chunks are short or empty.                    */
+int64_t oracle_ring_chunk_len(int64_t n, int p) { return (n + p - 1) / p; }
+
+static int64_t chunk_begin(int64_t n, int p, int c) {
+    int64_t b = (int64_t)c * oracle_ring_chunk_len(n, p);
+    return b < n ? b : n;
+}
+static int64_t chunk_end(int64_t n, int p, int c) { return chunk_begin(n, p, c + 1); }
+static int ring_mod(int a, int p) { return ((a % p) + p) % p; }
+
+int oracle_ring_schedule_f32(float *const *bufs, int p, int64_t n, int op, int phases,
+                             int64_t *sent_elems, int *steps) {
+    if (p < 1 || n < 0 || (op != ORACLE_SUM && op != ORACLE_AVG)) return -1;
+    int64_t clen = oracle_ring_chunk_len(n, p);
+    /* one chunk-sized "wire" slot per sender, so that every worker's send of
+     * a step is taken before any worker's receive of that step is applied */
+    float *wire = (float *)malloc(sizeof(float) * (size_t)(clen > 0 ? clen : 1) * (size_t)p);
+    if (!wire) return -1;
+    for (int w = 0; w < p; ++w)
+        if (sent_elems) sent_elems[w] = 0;
+    int nsteps = 0;
+
+    /* Phase 1, scatter-reduce: at step s worker i sends chunk (i - s) mod p
+     * to worker i + 1, which adds it into its own copy of that chunk. */
+    for (int s = 0; s < p - 1; ++s) {
+        for (int i = 0; i < p; ++i) {
+            int c = ring_mod(i - s, p);
+            int64_t b = chunk_begin(n, p, c), e = chunk_end(n, p, c);
+            memcpy(wire + (size_t)i * (size_t)clen, bufs[i] + b, sizeof(float) * (size_t)(e - b));
+            if (sent_elems) sent_elems[i] += e - b;
+        }
+        for (int i = 0; i < p; ++i) {
+            int from = ring_mod(i - 1, p);
+            int c = ring_mod(i - s - 1, p);
+            int64_t b = chunk_begin(n, p, c), e = chunk_end(n, p, c);
+            const float *recv = wire + (size_t)from * (size_t)clen;
+            for (int64_t k = b; k < e; ++k) bufs[i][k] = bufs[i][k] + recv[k - b];
+        }
+        ++nsteps;
+    }
+    if (phases == 2) {
+        /* Phase 2, all-gather: at step s worker i sends its finished chunk
+         * (i - s + 1) mod p to worker i + 1, which overwrites its copy. */
+        for (int s = 0; s < p - 1; ++s) {
+            for (int i = 0; i < p; ++i) {
+                int c = ring_mod(i - s + 1, p);
+                int64_t b = chunk_begin(n, p, c), e = chunk_end(n, p, c);
+                memcpy(wire + (size_t)i * (size_t)clen, bufs[i] + b,
+                       sizeof(float) * (size_t)(e - b));
+                if (sent_elems) sent_elems[i] += e - b;
+            }
+            for (int i = 0; i < p; ++i) {
+                int from = ring_mod(i - 1, p);
+                int c = ring_mod(i - s, p);
+                int64_t b = chunk_begin(n, p, c), e = chunk_end(n, p, c);
+                memcpy(bufs[i] + b, wire + (size_t)from * (size_t)clen,
+                       sizeof(float) * (size_t)(e - b));
+            }
+            ++nsteps;
+        }
+        /* The average is the sum divided element-wise by the worker count. */
+        if (op == ORACLE_AVG) {
+            float fp = (float)p;
+            for (int i = 0; i < p; ++i)
+                for (int64_t k = 0; k < n; ++k) bufs[i][k] = bufs[i][k] / fp;
+        }
+    }
+    free(wire);
+    if (steps) *steps = nsteps;
+    return 0;
+}
+
+/* Chunk c leaves worker c at step 0 and picks up one addend per hop, so an
+ * element of chunk c is x_c + x_{c+1} + ... + x_{c+p-1} (indices mod p),
+ * added left to right in fp32.  IEEE addition is commutative, so this is
+ * bit for bit the value the literal schedule produces. */
+static float fold_one_f32(const float *const *x, int p, int64_t n, int op, int64_t k) {
+    int c = (int)(k / oracle_ring_chunk_len(n, p));
+    float s = x[c][k];
+    for (int j = 1; j < p; ++j) s = s + x[(c + j) % p][k];
+    if (op == ORACLE_AVG) s = s / (float)p;
+    return s;
+}
+
+int oracle_ring_fold_f32(const float *const *x, int p, int64_t n, int op, float *out) {
+    if (p < 1 || n < 0) return -1;
+    for (int64_t k = 0; k < n; ++k) out[k] = fold_one_f32(x, p, n, op, k);
+    return 0;
+}
+
+int oracle_ring_fold_f32_at(const float *const *x, int p, int64_t n, int op,
+                            const int64_t *idx, int64_t count, float *out) {
+    if (p < 1 || n < 0) return -1;
+    for (int64_t k = 0; k < count; ++k) {
+        if (idx[k] < 0 || idx[k] >= n) return -1;
+        out[k] = fold_one_f32(x, p, n, op, idx[k]);
+    }
+    return 0;
+}
+
+/* bf16 is the top 16 bits of an IEEE binary32: widening is a shift. */
+float oracle_bf16_to_f32(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* Round a binary32 to the nearest bf16, ties to even.  NaN stays NaN (its
+ * payload is not specified here). */
+uint16_t oracle_f32_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u); /* quiet NaN */
+    uint32_t upper = u >> 16;
+    uint32_t lower = u & 0xFFFFu;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;
+    return (uint16_t)upper;
+}
+
+static float fold_one_bf16(const uint16_t *const *x, int p, int64_t n, int op, int64_t k) {
+    int c = (int)(k / oracle_ring_chunk_len(n, p));
+    float s = oracle_bf16_to_f32(x[c][k]);
+    for (int j = 1; j < p; ++j) s = s + oracle_bf16_to_f32(x[(c + j) % p][k]);
+    if (op == ORACLE_AVG) s = s / (float)p;
+    return s;
+}
+
+int oracle_ring_fold_bf16(const uint16_t *const *x, int p, int64_t n, int op, uint16_t *out,
+                          float *out_f32) {
+    if (p < 1 || n < 0) return -1;
+    for (int64_t k = 0; k < n; ++k) {
+        float s = fold_one_bf16(x, p, n, op, k);
+        if (out_f32) out_f32[k] = s;
+        out[k] = oracle_f32_to_bf16(s);
+    }
+    return 0;
+}
+
+int oracle_ring_fold_bf16_at(const uint16_t *const *x, int p, int64_t n, int op,
+                             const int64_t *idx, int64_t count, uint16_t *out) {
+    if (p < 1 || n < 0) return -1;
+    for (int64_t k = 0; k < count; ++k) {
+        if (idx[k] < 0 || idx[k] >= n) return -1;
+        out[k] = oracle_f32_to_bf16(fold_one_bf16(x, p, n, op, idx[k]));
+    }
+    return 0;
+}
+
+/* bf16 buffers on the literal schedule: the values on the wire are the fp32
+ * partial sums; the result is rounded to bf16 once, at the end. */
+int oracle_ring_schedule_bf16(uint16_t *const *bufs, int p, int64_t n, int op,
+                              int64_t *sent_elems, int *steps) {
+    if (p < 1 || n < 0) return -1;
+    float **work = (float **)calloc((size_t)p, sizeof(float *));
+    if (!work) return -1;
+    int rc = 0;
+    for (int i = 0; i < p; ++i) {
+        work[i] = (float *)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
+        if (!work[i]) rc = -1;
+    }
+    if (rc == 0) {
+        for (int i = 0; i < p; ++i)
+            for (int64_t k = 0; k < n; ++k) work[i][k] = oracle_bf16_to_f32(bufs[i][k]);
+        rc = oracle_ring_schedule_f32(work, p, n, op, 2, sent_elems, steps);
+        if (rc == 0)
+            for (int i = 0; i < p; ++i)
+                for (int64_t k = 0; k < n; ++k) bufs[i][k] = oracle_f32_to_bf16(work[i][k]);
+    }
+    for (int i = 0; i < p; ++i) free(work[i]);
+    free(work);
+    return rc;
+}
+
+/* ===================================================================== */
+/* Tensor Fusion [H] "Tensor Fusion", steps 1-6                           */
+/* ===================================================================== */
+static int dtype_bytes(int32_t dt) {
+    if (dt == ORACLE_F32) return 4;
+    if (dt == ORACLE_BF16) return 2;
+    return -1;
+}
+
+/* Tensors are taken in list (ready) order.  A tensor joins the open buffer
+ * when it has the buffer's dtype and fits in the room left (its start
+ * rounded up to align_bytes); otherwise the open buffer is closed and a new
+ * one starts with this tensor.  A tensor larger than the capacity gets a
+ * buffer to itself.                                                         */
+int oracle_fusion_plan(const int64_t *numel, const int32_t *dtype, int count,
+                       int64_t capacity_bytes, int align_bytes, int32_t *seg_buffer,
+                       int64_t *seg_offset, int64_t *buf_numel) {
+    if (count < 0 || capacity_bytes <= 0 || align_bytes <= 0) return -1;
+    int nbuf = 0;
+    int32_t open_dtype = -1;
+    int64_t used = 0; /* bytes used in the open buffer */
+    for (int i = 0; i < count; ++i) {
+        int es = dtype_bytes(dtype[i]);
+        if (es < 0 || numel[i] < 0 || align_bytes % es != 0) return -1;
+        int64_t bytes = numel[i] * es;
+        int64_t start = (used + align_bytes - 1) / align_bytes * align_bytes;
+        int fits = nbuf > 0 && dtype[i] == open_dtype && start + bytes <= capacity_bytes;
+        if (!fits) {
+            ++nbuf;
+            open_dtype = dtype[i];
+            start = 0;
+        }
+        seg_buffer[i] = nbuf - 1;
+        seg_offset[i] = start / es;
+        used = start + bytes;
+        buf_numel[nbuf - 1] = used / es;
+    }
+    return nbuf;
+}
+
+int oracle_fusion_pack(const void *const *src, const int32_t *seg_buffer,
+                       const int64_t *seg_offset, const int64_t *numel, int count, int buffer,
+                       void *fusion_buf, int64_t buf_numel, int elem_bytes) {
+    if (elem_bytes <= 0 || buf_numel < 0) return -1;
+    unsigned char *dst = (unsigned char *)fusion_buf;
+    memset(dst, 0, (size_t)(buf_numel * elem_bytes));
+    for (int i = 0; i < count; ++i) {
+        if (seg_buffer[i] != buffer) continue;
+        if (seg_offset[i] + numel[i] > buf_numel) return -1;
+        memcpy(dst + seg_offset[i] * elem_bytes, src[i], (size_t)(numel[i] * elem_bytes));
+    }
+    return 0;
+}
+
+int oracle_fusion_unpack(const void *fusion_buf, const int32_t *seg_buffer,
+                         const int64_t *seg_offset, const int64_t *numel, int count, int buffer,
+                         void *const *dst, int elem_bytes) {
+    if (elem_bytes <= 0) return -1;
+    const unsigned char *src = (const unsigned char *)fusion_buf;
+    for (int i = 0; i < count; ++i) {
+        if (seg_buffer[i] != buffer) continue;
+        memcpy(dst[i], src + seg_offset[i] * elem_bytes, (size_t)(numel[i] * elem_bytes));
+    }
+    return 0;
+}
+
+/* ===================================================================== */
+/* Uniform THC [T] section 4, Algorithm 1                                 */
+/* ===================================================================== */
+
+/* Preliminary round: the global smallest and largest entry over all
+ * workers.  NaN entries are skipped. */
+void oracle_thc_range(const float *const *x, int p, int64_t n, float *m, float *M) {
+    float lo = INFINITY, hi = -INFINITY;
+    for (int w = 0; w < p; ++w)
+        for (int64_t k = 0; k < n; ++k) {
+            float v = x[w][k];
+            if (v < lo) lo = v;
+            if (v > hi) hi = v;
+        }
+    *m = lo;
+    *M = hi;
+}
+
+/* The 2^b quantization values are q_j = m + j (M - m) / L, L = 2^b - 1.
+ * The position of a value on that grid, in fp32: (x - m) times the fp32
+ * scale L / (M - m), clamped to [0, L]. */
+float oracle_thc_position(float x, float m, float M, int b) {
+    const float L = (float)((1u << b) - 1u);
+    if (M == m) return 0.0f;
+    float range = M - m;
+    float scale = L / range;
+    float d = x - m;
+    float t = d * scale;
+    if (t < 0.0f) t = 0.0f;
+    if (t > L) t = L;
+    return t;
+}
+
+/* Stochastic quantization: a value between q_j and q_{j+1} goes up to
+ * q_{j+1} with probability equal to its fractional position f and down to
+ * q_j otherwise, which makes it unbiased.  The uniform draw u comes from
+ * the Philox4x32-10 stream keyed by the 64-bit seed: counter
+ * (e/4 low word, e/4 high word, worker, 0), output word e mod 4, of which
+ * the low 23 bits are read as u = bits / 2^23 in [0, 1).  Up iff u < f. */
+uint32_t oracle_thc_index(float x, float m, float M, int b, uint64_t seed, int worker,
+                          int64_t e) {
+    float t = oracle_thc_position(x, m, M, b);
+    float j = floorf(t);
+    float f = t - j;
+    uint64_t q = (uint64_t)e >> 2;
+    uint32_t ctr[4] = {(uint32_t)q, (uint32_t)(q >> 32), (uint32_t)worker, 0u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t r[4];
+    oracle_philox4x32(ctr, key, 10, r);
+    uint32_t bits = r[e & 3] & 0x7FFFFFu;
+    float u = (float)bits / 8388608.0f; /* exact: bits < 2^23 */
+    return (uint32_t)j + (u < f ? 1u : 0u);
+}
+
+static int valid_bits(int b) { return b == 1 || b == 2 || b == 4 || b == 8; }
+
+/* Indices are packed least significant bits first: element e sits in
+ * word e / (32 / b) at bit (e mod (32 / b)) * b; the last word is padded
+ * with zero indices. */
+int oracle_thc_encode(const float *x, int64_t n, float m, float M, int b, uint64_t seed,
+                      int worker, uint32_t *packed) {
+    if (!valid_bits(b) || n < 0) return -1;
+    int per_word = 32 / b;
+    int64_t nwords = (n + per_word - 1) / per_word;
+    for (int64_t k = 0; k < nwords; ++k) packed[k] = 0u;
+    for (int64_t e = 0; e < n; ++e) {
+        uint32_t idx = oracle_thc_index(x[e], m, M, b, seed, worker, e);
+        packed[e / per_word] |= idx << ((e % per_word) * b);
+    }
+    return 0;
+}
+
+int oracle_thc_unpack(const uint32_t *packed, int64_t n, int b, uint8_t *idx) {
+    if (!valid_bits(b) || n < 0) return -1;
+    int per_word = 32 / b;
+    uint32_t mask = (1u << b) - 1u;
+    for (int64_t e = 0; e < n; ++e)
+        idx[e] = (uint8_t)((packed[e / per_word] >> ((e % per_word) * b)) & mask);
+    return 0;
+}
+
+/* The PS sums the workers' index vectors as integers; nothing is decoded. */
+int oracle_thc_aggregate(const uint32_t *const *packed, int p, int64_t n, int b,
+                         uint16_t *sums) {
+    if (!valid_bits(b) || n < 0 || p < 1) return -1;
+    if ((int64_t)p * ((1 << b) - 1) > 65535) return -1;
+    int per_word = 32 / b;
+    uint32_t mask = (1u << b) - 1u;
+    for (int64_t e = 0; e < n; ++e) {
+        uint32_t s = 0;
+        for (int w = 0; w < p; ++w) s += (packed[w][e / per_word] >> ((e % per_word) * b)) & mask;
+        sums[e] = (uint16_t)s;
+    }
+    return 0;
+}
+
+/* Each worker divides the index sum by the number of workers and maps the
+ * average index back onto the grid: avg = m + (S / p) (M - m) / L, in fp64. */
+int oracle_thc_decode(const uint16_t *sums, int64_t n, float m, float M, int b, int p,
+                      double *avg) {
+    if (!valid_bits(b) || n < 0 || p < 1) return -1;
+    double L = (double)((1 << b) - 1);
+    double step = ((double)M - (double)m) / L;
+    for (int64_t e = 0; e < n; ++e) avg[e] = (double)m + ((double)sums[e] / (double)p) * step;
+    return 0;
+}
+
+int oracle_thc_allreduce(const float *const *x, int p, int64_t n, int b, uint64_t seed,
+                         float m, float M, double *avg, uint32_t *const *packed) {
+    if (!valid_bits(b) || n < 0 || p < 1) return -1;
+    int per_word = 32 / b;
+    int64_t nwords = (n + per_word - 1) / per_word;
+    uint32_t **pk = (uint32_t **)calloc((size_t)p, sizeof(uint32_t *));
+    uint16_t *sums = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(n > 0 ? n : 1));
+    int rc = (pk && sums) ? 0 : -1;
+    for (int w = 0; w < p && rc == 0; ++w) {
+        pk[w] = packed ? packed[w]
+                       : (uint32_t *)malloc(sizeof(uint32_t) * (size_t)(nwords > 0 ? nwords : 1));
+        if (!pk[w]) rc = -1;
+        else rc = oracle_thc_encode(x[w], n, m, M, b, seed, w, pk[w]);
+    }
+    if (rc == 0) rc = oracle_thc_aggregate((const uint32_t *const *)pk, p, n, b, sums);
+    if (rc == 0) rc = oracle_thc_decode(sums, n, m, M, b, p, avg);
+    if (pk && !packed)
+        for (int w = 0; w < p; ++w) free(pk[w]);
+    free(pk);
+    free(sums);
+    return rc;
+}
+
+/* ===================================================================== */
+/* NMSE [T] section 2: ||x - x_hat||^2 / ||x||^2, accumulated in fp64.     */
+/* ===================================================================== */
+double oracle_nmse(const float *x, const float *x_hat, int64_t n) {
+    double num = 0.0, den = 0.0;
+    for (int64_t k = 0; k < n; ++k) {
+        double d = (double)x[k] - (double)x_hat[k];
+        num += d * d;
+        den += (double)x[k] * (double)x[k];
+    }
+    if (den == 0.0) return NAN;
+    return num / den;
+}
+
+double oracle_nmse_f64(const double *x, const double *x_hat, int64_t n) {
+    double num = 0.0, den = 0.0;
+    for (int64_t k = 0; k < n; ++k) {
+        double d = x[k] - x_hat[k];
+        num += d * d;
+        den += x[k] * x[k];
+    }
+    if (den == 0.0) return NAN;
+    return num / den;
+}

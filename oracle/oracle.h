@@ -1,0 +1,117 @@
+/*
+ * oracle.h -- plain, slow CPU reference of the gradient-averaging hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load this code.  It shares nothing
+ * with the CUDA library (no header, helper, table or constant generator):
+ * every function below is written straight from the pages it cites.
+ *
+ * Sources (cited by page title and section):
+ *  [H]  "Horovod: Fast and Easy Distributed Deep Learning in TensorFlow"
+ *       (explainer page), section "The Ring-Allreduce Algorithm" and
+ *       section "Tensor Fusion: Why Small Tensors Break Ring-Allreduce".
+ *  [R]  "Collective Communication: Ring All-Reduce" tutorial, section 4
+ *       (step-by-step schedule), section 5 (data volume), section 7
+ *       (ring simulator).
+ *  [T]  "THC: Accelerating Distributed Deep Learning Using Tensor
+ *       Homomorphic Compression", section 2 (NMSE definition), section 4
+ *       (stochastic quantization, uniform SQ, Uniform THC / Algorithm 1).
+ *  [S]  Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
+ *       1, 2, 3", SC'11 -- definition of the Philox4x32 generator.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math), so
+ * every float expression is evaluated as written, one IEEE rounding per op.
+ */
+#ifndef GAR_ORACLE_H
+#define GAR_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtype codes and reduction ops used by the oracle's own interface */
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+#define ORACLE_SUM 0
+#define ORACLE_AVG 1
+
+/* ---------------- Philox4x32 [S] ---------------- */
+void oracle_philox4x32(const uint32_t ctr[4], const uint32_t key[2], int rounds,
+                       uint32_t out[4]);
+
+/* ---------------- ring all-reduce [H], [R] ---------------- */
+/* chunk length used for a buffer of n elements split over p workers */
+int64_t oracle_ring_chunk_len(int64_t n, int p);
+
+/* Literal schedule: p-1 scatter-reduce steps then (if phases == 2) p-1
+ * all-gather steps, run in place on p fp32 host buffers.  sent_elems[w]
+ * receives the number of elements worker w put on the wire; *steps the
+ * number of synchronous ring steps executed.  Returns 0 or -1 (bad args). */
+int oracle_ring_schedule_f32(float *const *bufs, int p, int64_t n, int op, int phases,
+                             int64_t *sent_elems, int *steps);
+
+/* Closed form of the same schedule: every element's ring-order fp32 fold,
+ * written to out[n] (all workers receive this value). */
+int oracle_ring_fold_f32(const float *const *x, int p, int64_t n, int op, float *out);
+/* the same, only for the element indices idx[k], k < count */
+int oracle_ring_fold_f32_at(const float *const *x, int p, int64_t n, int op,
+                            const int64_t *idx, int64_t count, float *out);
+
+/* bf16 variants: inputs are bf16 bit patterns, partial sums are fp32, the
+ * averaged value is rounded to bf16 (nearest-even) on output.
+ * out_f32 (may be NULL) receives the fp32 value before that rounding. */
+float oracle_bf16_to_f32(uint16_t h);
+uint16_t oracle_f32_to_bf16(float f);
+int oracle_ring_fold_bf16(const uint16_t *const *x, int p, int64_t n, int op, uint16_t *out,
+                          float *out_f32);
+int oracle_ring_fold_bf16_at(const uint16_t *const *x, int p, int64_t n, int op,
+                             const int64_t *idx, int64_t count, uint16_t *out);
+int oracle_ring_schedule_bf16(uint16_t *const *bufs, int p, int64_t n, int op,
+                              int64_t *sent_elems, int *steps);
+
+/* ---------------- Tensor Fusion [H] ---------------- */
+/* Next-fit plan.  dtype[i] is ORACLE_F32 or ORACLE_BF16.  Outputs per tensor:
+ * seg_buffer[i], seg_offset[i] (elements from the buffer start); per buffer:
+ * buf_numel[b] (elements, from 0 to the end of the last tensor).  buf_numel
+ * must have room for count entries.  Returns the number of buffers or -1. */
+int oracle_fusion_plan(const int64_t *numel, const int32_t *dtype, int count,
+                       int64_t capacity_bytes, int align_bytes, int32_t *seg_buffer,
+                       int64_t *seg_offset, int64_t *buf_numel);
+/* Copy the tensors of `buffer` into fusion_buf; every other byte of
+ * fusion_buf[0, buf_numel) is set to zero. */
+int oracle_fusion_pack(const void *const *src, const int32_t *seg_buffer,
+                       const int64_t *seg_offset, const int64_t *numel, int count, int buffer,
+                       void *fusion_buf, int64_t buf_numel, int elem_bytes);
+int oracle_fusion_unpack(const void *fusion_buf, const int32_t *seg_buffer,
+                         const int64_t *seg_offset, const int64_t *numel, int count, int buffer,
+                         void *const *dst, int elem_bytes);
+
+/* ---------------- uniform THC [T] ---------------- */
+void oracle_thc_range(const float *const *x, int p, int64_t n, float *m, float *M);
+/* fp32 position t = (x - m) * (L / (M - m)) clamped to [0, L] */
+float oracle_thc_position(float x, float m, float M, int b);
+/* index of one coordinate of worker `worker` at element index e */
+uint32_t oracle_thc_index(float x, float m, float M, int b, uint64_t seed, int worker,
+                          int64_t e);
+int oracle_thc_encode(const float *x, int64_t n, float m, float M, int b, uint64_t seed,
+                      int worker, uint32_t *packed);
+int oracle_thc_unpack(const uint32_t *packed, int64_t n, int b, uint8_t *idx);
+int oracle_thc_aggregate(const uint32_t *const *packed, int p, int64_t n, int b,
+                         uint16_t *sums);
+int oracle_thc_decode(const uint16_t *sums, int64_t n, float m, float M, int b, int p,
+                      double *avg);
+/* encode every worker, aggregate, decode; packed may be NULL */
+int oracle_thc_allreduce(const float *const *x, int p, int64_t n, int b, uint64_t seed,
+                         float m, float M, double *avg, uint32_t *const *packed);
+
+/* ---------------- NMSE [T] ---------------- */
+double oracle_nmse(const float *x, const float *x_hat, int64_t n);
+double oracle_nmse_f64(const double *x, const double *x_hat, int64_t n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
