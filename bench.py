@@ -1,0 +1,482 @@
+"""Benchmark of the gradient-averaging hot path on GB300.
+
+One step = one pass of the whole path over the ResNet-101-like Tensor
+Fusion workload: P = 8 workers, 300 fp32 gradient tensors (~45M parameters,
+log-uniform sizes 256..2.4M, N(0, 0.01)), 64 MB fusion buffers:
+
+  1. fusion plan (host)                                  gar_fusion_plan
+  2. ring all-reduce average, pack + ring + unpack fused gar_fused_allreduce
+  3. pack every worker's tensors into its fusion buffers gar_fusion_pack
+  4. per fusion buffer: THC shared range, then encode +  gar_thc_range,
+     aggregate + decode (b = 4, fresh seed each step)    gar_thc_allreduce_fused
+  5. THC average back into the tensors                   gar_fusion_unpack
+  6. NMSE of the THC estimate against the ring average   gar_fusion_pack, gar_nmse
+
+Metric: gradient bytes reduced per second = P x 45M x 4 B per step / step
+time (each step averages those bytes twice: exactly by the ring and
+compressed by THC).  ``value`` is device-timed with inputs resident in HBM
+(1.44 GB of inputs per step, larger than L2, so no L2 flush is needed);
+``e2e`` adds, every step, the host->device copy of the workers' gradients
+from pinned memory and the device->host read of both averages and the NMSE.
+
+``--impl reference`` times the CPU oracle (plain C, one core) on a bounded
+sample of the same workload.  Under torchrun with N > 1 GPUs every rank runs
+an independent replica (the path does not shard across GPUs).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "gradient GB/s reduced (P-worker ring + THC) and % of GB300 HBM peak"
+UNIT = "GB/s"
+P = 8
+B_THC = 4
+CAPACITY = 64 << 20
+ALIGN = 16
+WORKLOAD = "resnet_fusion"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _config(n_params, n_buffers, **extra):
+    c = {"workload": "ResNet-101-like Tensor Fusion: P=8 workers x 300 fp32 tensors "
+                     f"({n_params} params, log-uniform 256..2.4M, N(0,0.01)), 64 MB fusion buffers "
+                     f"({n_buffers} buffers), ring average + uniform THC b=4 + NMSE",
+         "P": P, "tensors": 300, "params_per_worker": int(n_params), "fusion_buffer_bytes": CAPACITY,
+         "thc_bits": B_THC, "l2": "inputs larger than L2 (P x params x 4 B per step); no flush"}
+    c.update(extra)
+    return c
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, _, flags in rows for n, f in zip(names, flags) if f.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[0] for r in rows])), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ GPU (ours)
+class Step:
+    """Device-resident state and the per-step call sequence."""
+
+    def __init__(self, torch, g, dev):
+        self.torch, self.g, self.dev = torch, g, dev
+        sizes = workloads.resnet_fusion_sizes()
+        self.sizes = sizes
+        self.n_params = int(sizes.sum())
+        self.dtype = np.zeros(sizes.size, np.int32)
+        # each worker's gradients live in one flat allocation, every tensor
+        # starting on a 16-byte line (4 fp32), as a framework's flat grad buffer
+        self.offs = np.concatenate([[0], np.cumsum((sizes + 3) // 4 * 4)])
+        self.flat_len = int(self.offs[-1])
+        cfg = workloads.CONFIG_IDS[WORKLOAD]
+        self.flat = [workloads.device_normal(self.flat_len, 0.01, 1000 * cfg + w, torch.float32, dev) for w in range(P)]
+        self.src = [self._views(f) for f in self.flat]
+        self.ring_flat = [torch.empty(self.flat_len, dtype=torch.float32, device=dev) for _ in range(P)]
+        self.ring = [self._views(f) for f in self.ring_flat]
+        self.thc_flat = torch.empty(self.flat_len, dtype=torch.float32, device=dev)
+        self.thc = self._views(self.thc_flat)
+        self.plan = g.gar_fusion_plan(sizes, self.dtype, CAPACITY, ALIGN)
+        self.nb = self.plan.n_buffers
+        bn = self.plan.buf_numel
+        self.fusion = [[torch.empty(int(bn[b]), dtype=torch.float32, device=dev) for b in range(self.nb)]
+                       for _ in range(P)]
+        self.ring_fb = [torch.empty(int(bn[b]), dtype=torch.float32, device=dev) for b in range(self.nb)]
+        self.thc_avg = [torch.empty(int(bn[b]), dtype=torch.float32, device=dev) for b in range(self.nb)]
+        self.words = [g.gar_thc_words(int(bn[b]), B_THC) for b in range(self.nb)]
+        self.packed = [[torch.empty(self.words[b], dtype=torch.int32, device=dev) for b in range(self.nb)]
+                       for _ in range(P)]
+        self.mM = torch.empty((self.nb, 2), dtype=torch.float32, device=dev)
+        self.nmse = torch.empty(self.nb, dtype=torch.float64, device=dev)
+        self.ws = torch.empty(max(g.gar_nmse_workspace_bytes(int(x)) for x in bn) // 8 + 1, dtype=torch.float64,
+                              device=dev)
+        # host pointer tables built once (the tensors do not move between steps)
+        self.tables = g.fused_pointer_tables(self.src, self.ring)
+        self.src_tab = [g.pointer_table(self.src[w]) for w in range(P)]
+        self.ring0_tab = g.pointer_table(self.ring[0])
+        self.thc_tab = g.pointer_table(self.thc)
+        self.fusion_col = [g.pointer_table([self.fusion[w][b] for w in range(P)]) for b in range(self.nb)]
+        self.packed_col = [g.pointer_table([self.packed[w][b] for w in range(P)]) for b in range(self.nb)]
+        self.buf_total = int(bn.sum())
+        self.stages = ["fused_ring", "pack", "thc_range", "thc_fused", "unpack", "nmse"]
+
+    def _views(self, flat):
+        return [flat[int(self.offs[i]):int(self.offs[i]) + int(s)] for i, s in enumerate(self.sizes)]
+
+    def algorithmic_bytes(self):
+        n, bt, nb = self.n_params * 4, self.buf_total * 4, self.nb
+        words = 4 * sum(self.words)
+        return {
+            "fused_ring": 2 * P * n,                       # read P x n, write P x n
+            "pack": P * n + P * bt,                        # read tensors, write buffers (gaps zeroed)
+            "thc_range": P * bt,                           # read P buffers
+            "thc_fused": P * bt + bt + P * words,          # read P buffers, write avg + wire vectors
+            "unpack": 2 * n,                               # THC average back into one tensor set
+            "nmse": n + bt + 2 * bt,                       # pack ring average, read both buffers
+        }
+
+    def run(self, step_idx, events=None):
+        g, torch = self.g, self.torch
+        seed = workloads.THC_SEED + step_idx
+
+        def mark(i):
+            if events is not None:
+                events[i].record()
+
+        plan = g.gar_fusion_plan(self.sizes, self.dtype, CAPACITY, ALIGN)
+        mark(0)
+        g.gar_fused_allreduce(self.src, self.ring, plan, op=g.GAR_AVG, tables=self.tables)
+        mark(1)
+        for w in range(P):
+            for b in range(self.nb):
+                g.gar_fusion_pack(self.src_tab[w], plan, b, self.fusion[w][b])
+        mark(2)
+        for b in range(self.nb):
+            g.gar_thc_range(self.fusion_col[b], self.mM[b])
+        mark(3)
+        for b in range(self.nb):
+            g.gar_thc_allreduce_fused(self.fusion_col[b], B_THC, seed, self.mM[b], self.thc_avg[b],
+                                      self.packed_col[b])
+        mark(4)
+        for b in range(self.nb):
+            g.gar_fusion_unpack(self.thc_avg[b], plan, b, self.thc_tab)
+        mark(5)
+        for b in range(self.nb):
+            g.gar_fusion_pack(self.ring0_tab, plan, b, self.ring_fb[b])
+            g.gar_nmse(self.ring_fb[b], self.thc_avg[b], self.nmse[b:b + 1], self.ws)
+        mark(6)
+
+
+KERNEL_OF_STAGE = {"fused_ring": "ring_fold_kernel", "pack": "copy_jobs_kernel", "thc_range": "thc_range_kernel",
+                   "thc_fused": "thc_fused_kernel", "unpack": "copy_jobs_kernel",
+                   "nmse": "copy_jobs_kernel + nmse_partial_kernel + nmse_final_kernel"}
+PER_OF_STAGE = {
+    "fused_ring": "all launches of one step's gar_fused_allreduce (3 launches, 300 tensors x 8 workers)",
+    "pack": "all launches of one step's 24 gar_fusion_pack calls (8 workers x 3 fusion buffers, one launch each)",
+    "thc_range": "all launches of one step's 3 gar_thc_range calls",
+    "thc_fused": "all launches of one step's 3 gar_thc_allreduce_fused calls",
+    "unpack": "all launches of one step's 3 gar_fusion_unpack calls",
+    "nmse": "one step's NMSE stage",
+}
+# stage -> committed ncu summary holding its per-step DRAM traffic
+PROFILE_OF_STAGE = {"fused_ring": ("ring_fold_kernel_resnet_fusion", "ring.cu"),
+                    "pack": ("copy_jobs_kernel_resnet_fusion", "fusion.cu"),
+                    "thc_fused": ("thc_fused_kernel_resnet_fusion", "thc.cu")}
+
+
+def _profile_traffic(stage):
+    """Per-step DRAM traffic of a stage from its committed ncu summary, only if
+    the summary was taken on the current kernel source (else None)."""
+    if stage not in PROFILE_OF_STAGE:
+        return None
+    tag, src_name = PROFILE_OF_STAGE[stage]
+    path = os.path.join(ROOT, "profiles", f"{tag}.md")
+    src = os.path.join(ROOT, "gradient_allreduce_homomorphic_gb300", "csrc", src_name)
+    if not os.path.exists(path) or not os.path.exists(src):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_step:\s*([0-9]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return int(m.group(1)) if cur == h.group(1) else None
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+
+    import gradient_allreduce_homomorphic_gb300 as g
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    g.load()
+    st = Step(torch, g, dev)
+    nbytes = P * st.n_params * 4
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for i in range(args.warmup):
+        st.run(i)
+    torch.cuda.synchronize()
+
+    # ---- device-timed region: inputs resident in HBM
+    nst = len(st.stages)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    launches0 = g.gar_launch_count()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(args.steps):
+        st.run(args.warmup + i, evs[i])
+    stop.record()
+    torch.cuda.synchronize()
+    launches = g.gar_launch_count() - launches0
+    barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(stop) / args.steps
+    stage_ms = {s: float(np.mean([evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(args.steps)]))
+                for k, s in enumerate(st.stages)}
+    if dist is not None:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end: pinned host gradients in, both averages and the NMSE out
+    host_in = [torch.empty(st.flat_len, dtype=torch.float32, pin_memory=True) for _ in range(P)]
+    for w in range(P):
+        host_in[w].copy_(st.flat[w])
+    host_ring = torch.empty(st.flat_len, dtype=torch.float32, pin_memory=True)
+    host_thc = torch.empty(st.flat_len, dtype=torch.float32, pin_memory=True)
+    host_nmse = torch.empty(st.nb, dtype=torch.float64, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step(i):
+        for w in range(P):
+            st.flat[w].copy_(host_in[w], non_blocking=True)
+        st.run(10_000 + i)
+        host_ring.copy_(st.ring_flat[0], non_blocking=True)
+        host_thc.copy_(st.thc_flat, non_blocking=True)
+        host_nmse.copy_(st.nmse, non_blocking=True)
+
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(e2e_steps):
+        e2e_step(2 + i)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    nmse_vals = host_nmse.numpy().tolist()
+    assert all(np.isfinite(nmse_vals)), nmse_vals
+
+    if rank != 0:
+        return None
+    peak, peak_kind = _peaks()
+    algo = st.algorithmic_bytes()
+    dom = max(stage_ms, key=lambda s: stage_ms[s])
+    achieved = algo[dom] / (stage_ms[dom] * 1e-3) / 1e9
+    traffic = _profile_traffic(dom)
+    value = world * nbytes / (ms * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded N(0,0.01) gradients drawn on the device)",
+        "config": _config(st.n_params, st.nb, parallelism=f"{world} independent replicas" if world > 1 else "single GPU"),
+        "elements_per_s": round(world * P * st.n_params / (ms * 1e-3), 1),
+        "hbm_fraction_of_step": round(sum(algo.values()) / (ms * 1e-3) / 1e9 / peak, 4),
+        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "stage_gbs": {k: round(algo[k] / (stage_ms[k] * 1e-3) / 1e9, 1) for k in stage_ms},
+        "roofline": {"kernel": KERNEL_OF_STAGE[dom],
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                     "per": PER_OF_STAGE[dom], "stage": dom},
+        "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": P * st.flat_len * 4,
+                "d2h_bytes_per_step": 2 * st.flat_len * 4 + 8 * st.nb},
+        "gpu_launches": int(launches),
+        "nmse_thc_b4": [round(v, 6) for v in nmse_vals],
+        "clocks": clk,
+    }
+    return out
+
+
+# --------------------------------------------------------- CPU (oracle)
+def oracle_step(sample_sizes, host, seed):
+    """The same pass with the CPU oracle on a sample of the workload."""
+    import oracle
+
+    dt = np.zeros(sample_sizes.size, np.int32)
+    sb, so, bn = oracle.fusion_plan(sample_sizes, dt, CAPACITY, ALIGN)
+    nmses = []
+    for b in range(len(bn)):
+        fbs = [oracle.fusion_pack(host[w], sb, so, b, bn[b]) for w in range(P)]
+        ring = oracle.ring_fold(fbs, op=oracle.AVG)
+        oracle.fusion_unpack(ring, sb, so, sample_sizes, b)
+        m, M = oracle.thc_range(fbs)
+        avg = oracle.thc_allreduce(fbs, B_THC, seed, m, M)
+        nmses.append(oracle.nmse(ring, avg.astype(np.float32)))
+    return nmses
+
+
+def sample_workload(target_params):
+    sizes = workloads.resnet_fusion_sizes()
+    take = []
+    total = 0
+    for s in sizes:  # a prefix of the tensor list, in ready order
+        if total >= target_params and take:
+            break
+        take.append(int(s))
+        total += int(s)
+    ss = np.array(take, np.int64)
+    cfg = workloads.CONFIG_IDS[WORKLOAD]
+    host = [workloads.tensors_normal(ss, 0.01, cfg, w) for w in range(P)]
+    return ss, host
+
+
+def time_oracle(budget_s: float, reps: int):
+    """Calibrate a sample so `reps` oracle steps take about budget_s seconds."""
+    ss, host = sample_workload(600_000)  # larger than the host caches, so the rate holds
+    t0 = time.perf_counter()
+    oracle_step(ss, host, 1)
+    rate = ss.sum() / max(time.perf_counter() - t0, 1e-6)  # params per second per step
+    target = int(np.clip(0.8 * rate * budget_s / reps, 50_000, 45_000_000))
+    ss, host = sample_workload(target)
+    return ss, host
+
+
+def cpu_baseline(budget_s=15.0):
+    ss, host = time_oracle(budget_s, 1)
+    t0 = time.perf_counter()
+    oracle_step(ss, host, workloads.THC_SEED)
+    dt = time.perf_counter() - t0
+    n = int(ss.sum())
+    return {"value": round(P * n * 4 / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {ss.size} of the 300 tensors ({n} params per worker, P=8), one full step "
+                      f"(plan, pack, ring fold, unpack, THC range + encode/aggregate/decode, NMSE), {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+
+    oracle.build()
+    budget = 100.0  # seconds of oracle work for the whole --steps/--warmup run
+    reps = args.steps + args.warmup
+    ss, host = time_oracle(budget, reps)
+    for i in range(args.warmup):
+        oracle_step(ss, host, workloads.THC_SEED + i)
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(ss, host, workloads.THC_SEED + args.warmup + i)
+        times.append(time.perf_counter() - t0)
+    ms = float(np.mean(times)) * 1e3
+    n = int(ss.sum())
+    value = P * n * 4 / (ms * 1e-3) / 1e9
+    sample = (f"first {ss.size} of the 300 tensors ({n} params per worker, P=8) per step, sized so "
+              f"{reps} steps fit in ~{budget:.0f} s")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy N(0,0.01))",
+            "config": _config(45_000_465, 3, reference="CPU oracle (plain C, single thread)"),
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as tdist
+
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+            tdist.init_process_group("nccl")
+            dist = tdist
+        out = run_ours(args, rank, world, dist)
+        if out is not None and world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline()
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

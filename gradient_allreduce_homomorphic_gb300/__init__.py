@@ -1,0 +1,274 @@
+"""Python binding of libgar.so, the GB300 gradient-averaging library.
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch supplies device memory and streams.  The functions carry
+the names of the C entry points declared in ``include/gar.h``; they take
+torch tensors (and lists of them) in place of raw pointers, enqueue on the
+current CUDA stream unless ``stream`` is given, and raise ``GarError`` on a
+non-zero status.  There is no fallback: if the library is not built, or the
+tensors are not on a CUDA device, the call fails.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgar.so")
+
+GAR_OK, GAR_EINVAL, GAR_EDTYPE, GAR_EALIGN, GAR_EOVERFLOW, GAR_ECUDA = 0, -1, -2, -3, -4, -5
+GAR_F32, GAR_BF16 = 0, 1
+GAR_SUM, GAR_AVG = 0, 1
+GAR_MAX_WORKERS = 64
+
+
+class GarError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"gar status {status}: {message}")
+        self.status = status
+
+
+class gar_seg(C.Structure):
+    _fields_ = [("buffer", C.c_int32), ("reserved", C.c_int32), ("offset", C.c_int64), ("numel", C.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+_vp, _pp = C.c_void_p, C.POINTER(C.c_void_p)
+_i32, _i64, _u64 = C.c_int32, C.c_int64, C.c_uint64
+_SIGNATURES = {
+    "gar_version": (C.c_int, []),
+    "gar_last_error": (C.c_char_p, []),
+    "gar_launch_count": (C.c_uint64, []),
+    "gar_fusion_plan": (C.c_int, [_vp, _vp, _i32, _i64, _i32, _vp, C.POINTER(_i32), _vp]),
+    "gar_fusion_pack": (C.c_int, [_pp, _vp, _vp, _i32, _i32, _vp, _i64, _vp]),
+    "gar_fusion_unpack": (C.c_int, [_vp, _vp, _vp, _i32, _i32, _pp, _vp]),
+    "gar_fused_allreduce": (C.c_int, [_pp, _pp, _i32, _vp, _vp, _i32, _vp, _i32, _i32, _vp]),
+    "gar_ring_allreduce_sim": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _vp]),
+    "gar_ring_allreduce_sim_out": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _pp, _i32, _vp]),
+    "gar_ring_allreduce_steps": (C.c_int, [_pp, _i32, _i64, _i32, C.POINTER(_i32), _vp, _vp]),
+    "gar_thc_words": (_i64, [_i64, _i32]),
+    "gar_thc_range": (C.c_int, [_pp, _i32, _i64, _vp, _vp]),
+    "gar_thc_encode": (C.c_int, [_vp, _i64, _vp, _i32, _u64, _i32, _vp, _vp]),
+    "gar_thc_aggregate": (C.c_int, [_pp, _i32, _i64, _i32, _vp, _vp]),
+    "gar_thc_decode": (C.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _vp]),
+    "gar_thc_allreduce_fused": (C.c_int, [_pp, _i32, _i64, _i32, _u64, _vp, _vp, _pp, _vp]),
+    "gar_nmse_workspace_bytes": (C.c_size_t, [_i64]),
+    "gar_nmse": (C.c_int, [_vp, _vp, _i64, _vp, _vp, C.c_size_t, _vp]),
+}
+
+
+def load(path: str = LIB_PATH):
+    """Load libgar.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with gradient_allreduce_homomorphic_gb300.build.build() "
+                    "(there is no CPU fallback)")
+            lib = C.CDLL(path)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _call(name, *args):
+    rc = getattr(load(), name)(*args)
+    if rc != GAR_OK:
+        raise GarError(rc, load().gar_last_error().decode(errors="replace"))
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t):
+    if not t.is_cuda:
+        raise GarError(GAR_EINVAL, "tensor is not on a CUDA device (the library has no CPU path)")
+    return t.data_ptr()
+
+
+class PtrTable:
+    """A host array of device pointers built once from a list of tensors, so
+    that repeated calls skip the per-call marshalling.  Keeps the tensors
+    alive; numel and dtype describe the first tensor."""
+
+    def __init__(self, tensors, allow_none: bool = False):
+        self.tensors = list(tensors)
+        ptrs = [(_dev(t) if t is not None else None) if allow_none else _dev(t) for t in self.tensors]
+        self.array = (C.c_void_p * len(ptrs))(*ptrs)
+        first = next((t for t in self.tensors if t is not None), None)
+        self.numel = first.numel() if first is not None else 0
+        self.first = first
+
+    def __len__(self):
+        return len(self.tensors)
+
+
+def pointer_table(tensors, allow_none: bool = False) -> PtrTable:
+    return tensors if isinstance(tensors, PtrTable) else PtrTable(tensors, allow_none)
+
+
+def _ptr_array(tensors):
+    return pointer_table(tensors).array
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.float32:
+        return GAR_F32
+    if t.dtype == torch.bfloat16:
+        return GAR_BF16
+    raise GarError(GAR_EDTYPE, f"unsupported dtype {t.dtype}")
+
+
+def gar_version() -> int:
+    return int(load().gar_version())
+
+
+def gar_last_error() -> str:
+    return load().gar_last_error().decode(errors="replace")
+
+
+def gar_launch_count() -> int:
+    return int(load().gar_launch_count())
+
+
+# ------------------------------------------------------------ Tensor Fusion
+@dataclass
+class FusionPlan:
+    segs: C.Array           # gar_seg[count]
+    dtype: np.ndarray       # int32[count]
+    buf_numel: np.ndarray   # int64[n_buffers]
+
+    @property
+    def count(self) -> int:
+        return len(self.dtype)
+
+    @property
+    def n_buffers(self) -> int:
+        return len(self.buf_numel)
+
+    def buffers(self) -> np.ndarray:
+        return np.array([s.buffer for s in self.segs], np.int32)
+
+    def offsets(self) -> np.ndarray:
+        return np.array([s.offset for s in self.segs], np.int64)
+
+
+def gar_fusion_plan(numel, dtype, capacity_bytes: int = 64 << 20, align_bytes: int = 16) -> FusionPlan:
+    numel = np.ascontiguousarray(numel, np.int64)
+    dtype = np.ascontiguousarray(dtype, np.int32)
+    count = int(numel.size)
+    segs = (gar_seg * max(count, 1))()
+    bn = np.zeros(max(count, 1), np.int64)
+    nb = _i32(0)
+    _call("gar_fusion_plan", numel.ctypes.data, dtype.ctypes.data, count, capacity_bytes, align_bytes,
+          C.addressof(segs), C.byref(nb), bn.ctypes.data)
+    return FusionPlan(segs, dtype, bn[:nb.value].copy())
+
+
+def gar_fusion_pack(src, plan: FusionPlan, buffer: int, fusion_buf, stream=None):
+    """src: one worker's tensors (list or PtrTable; entries of other buffers may be None)."""
+    ptrs = pointer_table(src, allow_none=True).array
+    _call("gar_fusion_pack", ptrs, C.addressof(plan.segs), plan.dtype.ctypes.data, plan.count, buffer,
+          _dev(fusion_buf), int(plan.buf_numel[buffer]), _stream(stream))
+
+
+def gar_fusion_unpack(fusion_buf, plan: FusionPlan, buffer: int, dst, stream=None):
+    ptrs = pointer_table(dst, allow_none=True).array
+    _call("gar_fusion_unpack", _dev(fusion_buf), C.addressof(plan.segs), plan.dtype.ctypes.data, plan.count,
+          buffer, ptrs, _stream(stream))
+
+
+def fused_pointer_tables(src, dst):
+    """Host pointer tables for gar_fused_allreduce (reuse them across steps)."""
+    return (PtrTable([t for row in src for t in row]), PtrTable([t for row in dst for t in row]))
+
+
+def gar_fused_allreduce(src, dst, plan: FusionPlan, op: int = GAR_AVG, stream=None, tables=None):
+    """src[w][i], dst[w][i]: worker w's tensor i (dst may be src)."""
+    P = len(src)
+    s, d = tables if tables is not None else fused_pointer_tables(src, dst)
+    _call("gar_fused_allreduce", s.array, d.array, P, C.addressof(plan.segs), plan.dtype.ctypes.data, plan.count,
+          plan.buf_numel.ctypes.data, plan.n_buffers, op, _stream(stream))
+
+
+# ----------------------------------------------------------- ring all-reduce
+def gar_ring_allreduce_sim(bufs, op: int = GAR_AVG, stream=None):
+    t = pointer_table(bufs)
+    _call("gar_ring_allreduce_sim", t.array, len(t), t.numel, _dtype_code(t.first), op, _stream(stream))
+
+
+def gar_ring_allreduce_sim_out(bufs, out, op: int = GAR_AVG, stream=None):
+    t, o = pointer_table(bufs), pointer_table(out)
+    _call("gar_ring_allreduce_sim_out", t.array, len(t), t.numel, _dtype_code(t.first), op,
+          o.array, len(o), _stream(stream))
+
+
+def gar_ring_allreduce_steps(bufs, op: int = GAR_AVG, stream=None):
+    """Literal schedule (fp32, in place); returns (steps, sent_elems[P])."""
+    P = len(bufs)
+    steps = _i32(0)
+    sent = np.zeros(P, np.int64)
+    _call("gar_ring_allreduce_steps", _ptr_array(bufs), P, bufs[0].numel(), op, C.byref(steps),
+          sent.ctypes.data, _stream(stream))
+    return steps.value, sent
+
+
+# --------------------------------------------------------------------- THC
+def gar_thc_words(N: int, b: int) -> int:
+    return int(load().gar_thc_words(N, b))
+
+
+def gar_thc_range(x, d_mM, stream=None):
+    t = pointer_table(x)
+    _call("gar_thc_range", t.array, len(t), t.numel, _dev(d_mM), _stream(stream))
+
+
+def gar_thc_encode(x, d_mM, b: int, seed: int, worker: int, packed, stream=None):
+    _call("gar_thc_encode", _dev(x), x.numel(), _dev(d_mM), b, seed, worker, _dev(packed), _stream(stream))
+
+
+def gar_thc_aggregate(packed, N: int, b: int, sums, stream=None):
+    t = pointer_table(packed)
+    _call("gar_thc_aggregate", t.array, len(t), N, b, _dev(sums), _stream(stream))
+
+
+def gar_thc_decode(sums, d_mM, b: int, P: int, avg, stream=None):
+    _call("gar_thc_decode", _dev(sums), sums.numel(), _dev(d_mM), b, P, _dev(avg), _stream(stream))
+
+
+def gar_thc_allreduce_fused(x, b: int, seed: int, d_mM, avg, packed=None, stream=None):
+    t = pointer_table(x)
+    pk = pointer_table(packed).array if packed is not None else None
+    _call("gar_thc_allreduce_fused", t.array, len(t), t.numel, b, seed, _dev(d_mM), _dev(avg), pk,
+          _stream(stream))
+
+
+# -------------------------------------------------------------------- NMSE
+def gar_nmse_workspace_bytes(N: int) -> int:
+    return int(load().gar_nmse_workspace_bytes(N))
+
+
+def gar_nmse(x, x_hat, d_out, workspace, stream=None):
+    nbytes = workspace.numel() * workspace.element_size()
+    _call("gar_nmse", _dev(x), _dev(x_hat), x.numel(), _dev(d_out), _dev(workspace), nbytes, _stream(stream))
+
+
+__all__ = [n for n in dir() if n.startswith(("gar_", "GAR_"))] + ["GarError", "FusionPlan", "PtrTable", "load",
+                                                                    "pointer_table", "fused_pointer_tables"]

@@ -1,0 +1,48 @@
+// common.cu -- error reporting, launch checks and device queries.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+
+#include "common.cuh"
+
+namespace gar {
+
+namespace {
+thread_local char g_last_error[512] = "";
+std::atomic<unsigned long long> g_launches{0};
+}
+
+int fail(int status, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int check_launch(const char *what) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(GAR_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+    return GAR_OK;
+}
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+}  // namespace gar
+
+extern "C" int gar_version(void) { return 100; }
+
+extern "C" const char *gar_last_error(void) { return gar::g_last_error; }
+
+extern "C" uint64_t gar_launch_count(void) { return gar::g_launches.load(std::memory_order_relaxed); }

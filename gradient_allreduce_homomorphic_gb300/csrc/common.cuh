@@ -1,0 +1,77 @@
+// common.cuh -- internal helpers shared by the library's translation units.
+//
+// Host side: error reporting (thread-local message + status), launch checks,
+// SM count.  Device side: 16-byte streaming loads/stores, bf16 <-> fp32
+// conversion, and the Philox4x32-10 counter-based generator.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gar.h"
+
+namespace gar {
+
+// ------------------------------------------------------------------ host
+// Record `msg` as this thread's last error and return `status`.
+int fail(int status, const char *fmt, ...);
+// GAR_ECUDA (with the runtime's message) if the last launch failed, else GAR_OK.
+int check_launch(const char *what);
+// Multiprocessor count of the current device (cached per device).
+int sm_count();
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+inline int elem_bytes(int32_t dtype) { return dtype == GAR_F32 ? 4 : (dtype == GAR_BF16 ? 2 : -1); }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------- device
+// 16-byte loads and stores with the streaming ("evict first") cache hint:
+// every byte of the hot path is touched once per pass.
+__device__ __forceinline__ uint4 ld16(const void *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }
+__device__ __forceinline__ void st16(void *p, uint4 v) { __stcs(reinterpret_cast<uint4 *>(p), v); }
+
+// bf16 is the upper half of an IEEE binary32: widening is exact.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_one(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
+// Two fp32 values rounded to nearest-even bf16 and packed (lo in bits 0-15).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ uint16_t to_bf16(float v) { return static_cast<uint16_t>(pack_bf16x2(v, 0.0f) & 0xFFFFu); }
+
+// Philox4x32 round keys for a 64-bit seed: round r uses
+// (seed_lo + r * 0x9E3779B9, seed_hi + r * 0xBB67AE85) (mod 2^32), [S].
+struct PhiloxKeys {
+    uint32_t lo[10];
+    uint32_t hi[10];
+};
+inline PhiloxKeys philox_keys(uint64_t seed) {
+    PhiloxKeys k;
+    uint32_t a = static_cast<uint32_t>(seed), b = static_cast<uint32_t>(seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        k.lo[r] = a;
+        k.hi[r] = b;
+        a += 0x9E3779B9u;
+        b += 0xBB67AE85u;
+    }
+    return k;
+}
+
+// Philox4x32-10 [S]: ten rounds; each multiplies counter words 0 and 2 by
+// the two round constants (full 64-bit products), then the next counter is
+// (hi(B*c2) ^ c1 ^ k_lo, lo(B*c2), hi(A*c0) ^ c3 ^ k_hi, lo(A*c0)).
+__device__ __forceinline__ uint4 philox10(uint4 c, const PhiloxKeys &k) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t a_lo = 0xD2511F53u * c.x, a_hi = __umulhi(0xD2511F53u, c.x);
+        const uint32_t b_lo = 0xCD9E8D57u * c.z, b_hi = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(b_hi ^ c.y ^ k.lo[r], b_lo, a_hi ^ c.w ^ k.hi[r], a_lo);
+    }
+    return c;
+}
+
+}  // namespace gar

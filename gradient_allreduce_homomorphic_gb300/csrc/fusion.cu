@@ -1,0 +1,300 @@
+// fusion.cu -- Tensor Fusion ([H] "Tensor Fusion: Why Small Tensors Break
+// Ring-Allreduce", steps 1-6): the fusion plan (host), the copy into and out
+// of fusion buffers (steps 3 and 5) and the plan-driven one-pass all-reduce.
+//
+// Copies run as a list of byte-range jobs (a tensor into its slot, a slot
+// back into a tensor, or a zero fill of an alignment gap).  Jobs are cut
+// into tiles of 512 x 16-byte vectors and CTAs stride over the tiles, so a
+// launch moves hundreds of tensors of any size mix at streaming bandwidth.
+#include <cstring>
+#include <vector>
+
+#include "common.cuh"
+#include "ring.cuh"
+
+namespace gar {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 2;
+constexpr int kTileUnits = kThreads * kUnroll;
+constexpr int kMaxJobs = 256;
+
+struct CopyJob {
+    const unsigned char *src;  // NULL: zero fill
+    unsigned char *dst;
+    int64_t bytes;
+    int32_t unit;  // 16, 4, 2 or 1: the widest access both addresses allow
+    int32_t pad;
+};
+
+struct CopyParams {
+    int32_t njobs;
+    int32_t pad;
+    int64_t total_tiles;
+    int64_t tile_start[kMaxJobs + 1];
+    CopyJob job[kMaxJobs];
+};
+static_assert(sizeof(CopyParams) <= 32000, "copy parameters exceed the launch limit");
+
+template <int U>
+struct Word;
+template <>
+struct Word<16> {
+    using T = uint4;
+};
+template <>
+struct Word<4> {
+    using T = uint32_t;
+};
+template <>
+struct Word<2> {
+    using T = uint16_t;
+};
+template <>
+struct Word<1> {
+    using T = unsigned char;
+};
+
+template <int U>
+__device__ __forceinline__ void copy_units(const CopyJob &j, int64_t lt) {
+    using T = typename Word<U>::T;
+    const int64_t n = j.bytes / U;
+    const T *s = reinterpret_cast<const T *>(j.src);
+    T *d = reinterpret_cast<T *>(j.dst);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const int64_t i = lt * kTileUnits + u * kThreads + threadIdx.x;
+        if (i < n) {
+            T v;
+            if (s) {
+                if constexpr (U == 16) v = __ldcs(s + i);
+                else v = s[i];
+            } else {
+                v = T{};
+            }
+            if constexpr (U == 16) __stcs(d + i, v);
+            else d[i] = v;
+        }
+    }
+    if (lt == 0) {  // bytes past the last whole unit
+        const int64_t rem = j.bytes - n * U;
+        if (threadIdx.x < rem) {
+            const int64_t k = n * U + threadIdx.x;
+            j.dst[k] = j.src ? j.src[k] : static_cast<unsigned char>(0);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) copy_jobs_kernel(const __grid_constant__ CopyParams p) {
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        int lo = 0, hi = p.njobs - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.tile_start[mid] <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        const CopyJob &j = p.job[lo];
+        const int64_t lt = t - p.tile_start[lo];
+        switch (j.unit) {
+            case 16: copy_units<16>(j, lt); break;
+            case 4: copy_units<4>(j, lt); break;
+            case 2: copy_units<2>(j, lt); break;
+            default: copy_units<1>(j, lt); break;
+        }
+    }
+}
+
+int widest_unit(const void *s, const void *d) {
+    for (int u : {16, 4, 2}) {
+        if ((!s || aligned(s, u)) && aligned(d, u)) return u;
+    }
+    return 1;
+}
+
+class CopyBatch {
+  public:
+    explicit CopyBatch(cudaStream_t s) : stream_(s), p_(new CopyParams) { std::memset(p_, 0, sizeof(CopyParams)); }
+    ~CopyBatch() { delete p_; }
+    int add(const void *src, void *dst, int64_t bytes) {
+        if (bytes <= 0) return GAR_OK;
+        if (p_->njobs == kMaxJobs) {
+            const int rc = flush();
+            if (rc) return rc;
+        }
+        CopyJob &j = p_->job[p_->njobs++];
+        j.src = static_cast<const unsigned char *>(src);
+        j.dst = static_cast<unsigned char *>(dst);
+        j.bytes = bytes;
+        j.unit = widest_unit(src, dst);
+        j.pad = 0;
+        return GAR_OK;
+    }
+    int flush() {
+        if (p_->njobs == 0) return GAR_OK;
+        int64_t tiles = 0;
+        for (int i = 0; i < p_->njobs; ++i) {
+            p_->tile_start[i] = tiles;
+            const int64_t t = ceil_div(p_->job[i].bytes / p_->job[i].unit, kTileUnits);
+            tiles += t > 0 ? t : 1;
+        }
+        p_->tile_start[p_->njobs] = tiles;
+        p_->total_tiles = tiles;
+        static int occ = 0;
+        if (occ == 0) {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, copy_jobs_kernel, kThreads, 0) != cudaSuccess || n <= 0)
+                n = 4;
+            occ = n;
+        }
+        int64_t grid = static_cast<int64_t>(sm_count()) * occ;
+        if (grid > tiles) grid = tiles;
+        copy_jobs_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream_>>>(*p_);
+        p_->njobs = 0;
+        return check_launch("copy_jobs_kernel");
+    }
+
+  private:
+    cudaStream_t stream_;
+    CopyParams *p_;
+};
+
+// Checks shared by pack / unpack: the buffer's tensors, their common dtype.
+int buffer_members(const gar_seg *segs, const int32_t *dtype, int32_t count, int32_t buffer,
+                   std::vector<int> &members, int &es) {
+    if (!segs || !dtype || count < 0) return fail(GAR_EINVAL, "segs/dtype NULL or count < 0");
+    if (buffer < 0) return fail(GAR_EINVAL, "buffer id %d < 0", buffer);
+    int dt = -1;
+    for (int i = 0; i < count; ++i) {
+        if (segs[i].buffer != buffer) continue;
+        if (elem_bytes(dtype[i]) < 0) return fail(GAR_EDTYPE, "tensor %d has unknown dtype %d", i, dtype[i]);
+        if (dt >= 0 && dtype[i] != dt) return fail(GAR_EDTYPE, "buffer %d mixes dtypes", buffer);
+        if (segs[i].offset < 0 || segs[i].numel < 0) return fail(GAR_EINVAL, "tensor %d has a negative offset/numel", i);
+        dt = dtype[i];
+        members.push_back(i);
+    }
+    es = dt >= 0 ? elem_bytes(dt) : 4;
+    return GAR_OK;
+}
+
+}  // namespace
+}  // namespace gar
+
+using namespace gar;
+
+extern "C" int gar_fusion_plan(const int64_t *numel, const int32_t *dtype, int32_t count, int64_t capacity_bytes,
+                               int32_t align_bytes, gar_seg *segs, int32_t *n_buffers, int64_t *buf_numel) {
+    if (count < 0) return fail(GAR_EINVAL, "count %d < 0", count);
+    if (count > 0 && (!numel || !dtype || !segs || !buf_numel)) return fail(GAR_EINVAL, "NULL plan array");
+    if (!n_buffers) return fail(GAR_EINVAL, "n_buffers is NULL");
+    if (capacity_bytes <= 0) return fail(GAR_EINVAL, "capacity %lld <= 0", static_cast<long long>(capacity_bytes));
+    if (align_bytes <= 0) return fail(GAR_EINVAL, "alignment %d <= 0", align_bytes);
+    int32_t open = -1;       // id of the open buffer
+    int32_t open_dtype = -1;
+    int64_t fill = 0;        // bytes used in the open buffer
+    for (int32_t i = 0; i < count; ++i) {
+        const int es = elem_bytes(dtype[i]);
+        if (es < 0) return fail(GAR_EDTYPE, "tensor %d has unknown dtype %d", i, dtype[i]);
+        if (numel[i] < 0) return fail(GAR_EINVAL, "tensor %d has numel < 0", i);
+        if (align_bytes % es) return fail(GAR_EINVAL, "alignment %d is not a multiple of %d", align_bytes, es);
+        const int64_t bytes = numel[i] * es;
+        const int64_t at = ceil_div(fill, align_bytes) * align_bytes;
+        const bool joins = open >= 0 && dtype[i] == open_dtype && at + bytes <= capacity_bytes;
+        int64_t start = at;
+        if (!joins) {  // close the open buffer (if any), open the next one
+            ++open;
+            open_dtype = dtype[i];
+            start = 0;
+        }
+        segs[i].buffer = open;
+        segs[i].reserved = 0;
+        segs[i].offset = start / es;
+        segs[i].numel = numel[i];
+        fill = start + bytes;
+        buf_numel[open] = fill / es;
+    }
+    *n_buffers = open + 1;
+    return GAR_OK;
+}
+
+extern "C" int gar_fusion_pack(const void *const *src, const gar_seg *segs, const int32_t *dtype, int32_t count,
+                               int32_t buffer, void *fusion_buf, int64_t buf_numel, gar_stream_t stream) {
+    std::vector<int> members;
+    int es = 4;
+    int rc = buffer_members(segs, dtype, count, buffer, members, es);
+    if (rc) return rc;
+    if (buf_numel < 0) return fail(GAR_EINVAL, "buf_numel < 0");
+    if (buf_numel > 0 && !fusion_buf) return fail(GAR_EINVAL, "fusion_buf is NULL");
+    if (!members.empty() && !src) return fail(GAR_EINVAL, "src is NULL");
+    if (fusion_buf && !aligned(fusion_buf, es)) return fail(GAR_EALIGN, "fusion_buf not aligned to %d bytes", es);
+    CopyBatch batch(reinterpret_cast<cudaStream_t>(stream));
+    unsigned char *base = static_cast<unsigned char *>(fusion_buf);
+    int64_t cursor = 0;  // element where the next zero gap starts
+    for (int i : members) {
+        const gar_seg &s = segs[i];
+        if (s.offset < cursor || s.offset + s.numel > buf_numel)
+            return fail(GAR_EINVAL, "tensor %d does not lie in order inside buffer %d", i, buffer);
+        if (s.numel > 0 && !src[i]) return fail(GAR_EINVAL, "source tensor %d is NULL", i);
+        if (s.numel > 0 && !aligned(src[i], es)) return fail(GAR_EALIGN, "source tensor %d not aligned", i);
+    }
+    for (int i : members) {
+        const gar_seg &s = segs[i];
+        if ((rc = batch.add(nullptr, base + cursor * es, (s.offset - cursor) * es))) return rc;
+        if ((rc = batch.add(src[i], base + s.offset * es, s.numel * es))) return rc;
+        cursor = s.offset + s.numel;
+    }
+    if ((rc = batch.add(nullptr, base + cursor * es, (buf_numel - cursor) * es))) return rc;
+    return batch.flush();
+}
+
+extern "C" int gar_fusion_unpack(const void *fusion_buf, const gar_seg *segs, const int32_t *dtype, int32_t count,
+                                 int32_t buffer, void *const *dst, gar_stream_t stream) {
+    std::vector<int> members;
+    int es = 4;
+    int rc = buffer_members(segs, dtype, count, buffer, members, es);
+    if (rc) return rc;
+    if (members.empty()) return GAR_OK;
+    if (!fusion_buf || !dst) return fail(GAR_EINVAL, "fusion_buf or dst is NULL");
+    if (!aligned(fusion_buf, es)) return fail(GAR_EALIGN, "fusion_buf not aligned to %d bytes", es);
+    for (int i : members) {
+        if (segs[i].numel > 0 && !dst[i]) return fail(GAR_EINVAL, "destination tensor %d is NULL", i);
+        if (segs[i].numel > 0 && !aligned(dst[i], es)) return fail(GAR_EALIGN, "destination tensor %d not aligned", i);
+    }
+    CopyBatch batch(reinterpret_cast<cudaStream_t>(stream));
+    const unsigned char *base = static_cast<const unsigned char *>(fusion_buf);
+    for (int i : members)
+        if ((rc = batch.add(base + segs[i].offset * es, dst[i], segs[i].numel * es))) return rc;
+    return batch.flush();
+}
+
+extern "C" int gar_fused_allreduce(const void *const *src, void *const *dst, int32_t P, const gar_seg *segs,
+                                   const int32_t *dtype, int32_t count, const int64_t *buf_numel, int32_t n_buffers,
+                                   int32_t op, gar_stream_t stream) {
+    if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
+    if (op != GAR_SUM && op != GAR_AVG) return fail(GAR_EINVAL, "unknown op %d", op);
+    if (count < 0 || n_buffers < 0) return fail(GAR_EINVAL, "count or n_buffers < 0");
+    if (count == 0) return GAR_OK;
+    if (!src || !dst || !segs || !dtype || !buf_numel) return fail(GAR_EINVAL, "NULL argument");
+    std::vector<int32_t> buf_dt(n_buffers, -1);
+    std::vector<int64_t> cursor(n_buffers, 0);
+    for (int i = 0; i < count; ++i) {
+        const gar_seg &s = segs[i];
+        const int es = elem_bytes(dtype[i]);
+        if (es < 0) return fail(GAR_EDTYPE, "tensor %d has unknown dtype %d", i, dtype[i]);
+        if (s.buffer < 0 || s.buffer >= n_buffers) return fail(GAR_EINVAL, "tensor %d has buffer id %d", i, s.buffer);
+        if (buf_dt[s.buffer] >= 0 && buf_dt[s.buffer] != dtype[i]) return fail(GAR_EDTYPE, "buffer %d mixes dtypes", s.buffer);
+        buf_dt[s.buffer] = dtype[i];
+        if (s.numel < 0 || s.offset < cursor[s.buffer] || s.offset + s.numel > buf_numel[s.buffer])
+            return fail(GAR_EINVAL, "tensor %d does not lie in order inside buffer %d", i, s.buffer);
+        cursor[s.buffer] = s.offset + s.numel;
+        if (s.numel == 0) continue;
+        for (int w = 0; w < P; ++w) {
+            const void *sp = src[static_cast<int64_t>(w) * count + i];
+            const void *dp = dst[static_cast<int64_t>(w) * count + i];
+            if (!sp || !dp) return fail(GAR_EINVAL, "worker %d tensor %d pointer is NULL", w, i);
+            if (!aligned(sp, es) || !aligned(dp, es)) return fail(GAR_EALIGN, "worker %d tensor %d not aligned", w, i);
+        }
+    }
+    return fused_allreduce_impl(src, dst, P, segs, dtype, count, buf_numel, n_buffers, op,
+                                reinterpret_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,120 @@
+// nmse.cu -- NMSE(x, x_hat) = ||x - x_hat||^2 / ||x||^2 ([T] section 2).
+//
+// Two launches, deterministic: (1) each CTA folds its grid-stride slice into
+// one (sum (x - x_hat)^2, sum x^2) pair of doubles in the caller's
+// workspace; (2) one CTA adds the pairs in a fixed order and divides.
+// Per-element terms are formed in fp32 (four at a time) and accumulated in
+// fp64: fp64 throughput on this part is a small fraction of fp32, and one
+// fp32 rounding per term keeps the result within 2e-6 of an all-fp64 sum.
+#include <cstring>
+
+#include "common.cuh"
+
+namespace gar {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxBlocks = 1024;
+
+int nmse_blocks(int64_t N) {
+    int64_t g = ceil_div(ceil_div(N, 4), kThreads);
+    if (g > kMaxBlocks) g = kMaxBlocks;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// Block-wide sum of two doubles in a fixed order; result valid in thread 0.
+__device__ __forceinline__ void block_sum2(double &a, double &b) {
+    __shared__ double s_a[kThreads / 32], s_b[kThreads / 32];
+    a = warp_sum(a);
+    b = warp_sum(b);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        s_a[warp] = a;
+        s_b[warp] = b;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        a = lane < kThreads / 32 ? s_a[lane] : 0.0;
+        b = lane < kThreads / 32 ? s_b[lane] : 0.0;
+        a = warp_sum(a);
+        b = warp_sum(b);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+nmse_partial_kernel(const float *__restrict__ x, const float *__restrict__ xh, int64_t N, int vec, double *ws) {
+    double num = 0.0, den = 0.0;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    int64_t first = 0;
+    if (vec) {
+        const int64_t nv = N / 4;
+        for (int64_t i = tid; i < nv; i += stride) {
+            const float4 a = __ldcs(reinterpret_cast<const float4 *>(x) + i);
+            const float4 b = __ldcs(reinterpret_cast<const float4 *>(xh) + i);
+            const float d0 = __fsub_rn(a.x, b.x), d1 = __fsub_rn(a.y, b.y);
+            const float d2 = __fsub_rn(a.z, b.z), d3 = __fsub_rn(a.w, b.w);
+            const float e = __fadd_rn(__fadd_rn(__fmul_rn(d0, d0), __fmul_rn(d1, d1)),
+                                      __fadd_rn(__fmul_rn(d2, d2), __fmul_rn(d3, d3)));
+            const float s = __fadd_rn(__fadd_rn(__fmul_rn(a.x, a.x), __fmul_rn(a.y, a.y)),
+                                      __fadd_rn(__fmul_rn(a.z, a.z), __fmul_rn(a.w, a.w)));
+            num += static_cast<double>(e);
+            den += static_cast<double>(s);
+        }
+        first = nv * 4;
+    }
+    for (int64_t k = first + tid; k < N; k += stride) {
+        const float a = x[k], d = __fsub_rn(a, xh[k]);
+        num += static_cast<double>(__fmul_rn(d, d));
+        den += static_cast<double>(__fmul_rn(a, a));
+    }
+    block_sum2(num, den);
+    if (threadIdx.x == 0) {
+        ws[2 * blockIdx.x] = num;
+        ws[2 * blockIdx.x + 1] = den;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) nmse_final_kernel(const double *ws, int nblocks, double *out) {
+    double num = 0.0, den = 0.0;
+    for (int i = threadIdx.x; i < nblocks; i += kThreads) {
+        num += ws[2 * i];
+        den += ws[2 * i + 1];
+    }
+    block_sum2(num, den);
+    if (threadIdx.x == 0) *out = den == 0.0 ? __longlong_as_double(0x7FF8000000000000ll) : num / den;
+}
+
+}  // namespace
+}  // namespace gar
+
+using namespace gar;
+
+extern "C" size_t gar_nmse_workspace_bytes(int64_t N) {
+    return static_cast<size_t>(nmse_blocks(N < 0 ? 0 : N)) * 2 * sizeof(double);
+}
+
+extern "C" int gar_nmse(const float *x, const float *x_hat, int64_t N, double *d_out, void *d_workspace,
+                        size_t workspace_bytes, gar_stream_t stream_) {
+    if (N < 0 || !d_out || !d_workspace) return fail(GAR_EINVAL, "N < 0 or NULL argument");
+    if (N > 0 && (!x || !x_hat)) return fail(GAR_EINVAL, "x or x_hat is NULL");
+    if (workspace_bytes < gar_nmse_workspace_bytes(N))
+        return fail(GAR_EINVAL, "workspace of %zu bytes < %zu needed", workspace_bytes, gar_nmse_workspace_bytes(N));
+    if (!aligned(d_workspace, 8) || !aligned(d_out, 8)) return fail(GAR_EALIGN, "workspace or d_out not 8-byte aligned");
+    if ((x && !aligned(x, 4)) || (x_hat && !aligned(x_hat, 4))) return fail(GAR_EALIGN, "x or x_hat not 4-byte aligned");
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const int g = nmse_blocks(N);
+    const int vec = aligned(x, 16) && aligned(x_hat, 16);
+    double *ws = static_cast<double *>(d_workspace);
+    nmse_partial_kernel<<<g, kThreads, 0, stream>>>(x, x_hat, N, vec, ws);
+    int rc = check_launch("nmse_partial_kernel");
+    if (rc) return rc;
+    nmse_final_kernel<<<1, kThreads, 0, stream>>>(ws, g, d_out);
+    return check_launch("nmse_final_kernel");
+}

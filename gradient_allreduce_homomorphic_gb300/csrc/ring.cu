@@ -1,0 +1,469 @@
+// ring.cu -- ring all-reduce of P worker buffers held in one GPU's HBM.
+//
+// Ring all-reduce ([H] "The Ring-Allreduce Algorithm"; [R] sections 4, 5, 7):
+// the buffer is cut into P chunks; in P-1 scatter-reduce steps chunk c
+// travels c -> c+1 -> ... gaining each worker's addend, and in P-1
+// all-gather steps the finished chunk is copied around the ring.  On one
+// GPU the "wire" is HBM, so the whole schedule collapses into one pass: for
+// every element, load the P workers' values, fold them in fp32 in the ring
+// order of the element's chunk (x_c, x_{c+1}, ..., x_{c+P-1}, indices mod P)
+// and store the result to every destination.  IEEE addition is commutative,
+// so this matches the literal schedule bit for bit; its traffic is the
+// minimum (each input read once, each output written once).
+//
+// Work decomposition: the element range is cut into "pieces" -- runs of one
+// tensor that lie in one ring chunk -- so the chunk (the fold's starting
+// worker) is uniform over a piece and never computed per element.  Pieces are
+// cut into tiles of 512 x 16-byte vectors; CTAs stride over the flattened
+// tile list.  The same kernel serves a single buffer (one tensor, P pieces)
+// and a whole Tensor Fusion plan (every tensor of every fusion buffer, split
+// at that buffer's chunk boundaries), where it reads the workers' tensors and
+// writes their results directly: pack, all-reduce and unpack in one pass.
+#include <cstring>
+#include <vector>
+
+#include "common.cuh"
+#include "ring.cuh"
+
+namespace gar {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 2;
+constexpr int kTileUnits = kThreads * kUnroll;
+constexpr int kLoadBatch = 8;  // worker vectors in flight per thread before folding
+
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+    static constexpr int kVec = 4;  // elements per 16 bytes
+    __device__ static void unpack(const uint4 &r, float (&v)[4]) {
+        v[0] = __uint_as_float(r.x);
+        v[1] = __uint_as_float(r.y);
+        v[2] = __uint_as_float(r.z);
+        v[3] = __uint_as_float(r.w);
+    }
+    __device__ static uint4 pack(const float (&v)[4]) {
+        return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                          __float_as_uint(v[3]));
+    }
+    __device__ static float load1(const void *p, int64_t e) { return __ldcs(static_cast<const float *>(p) + e); }
+    __device__ static void store1(void *p, int64_t e, float v) { __stcs(static_cast<float *>(p) + e, v); }
+};
+template <>
+struct Elem<uint16_t> {  // bf16 storage
+    static constexpr int kVec = 8;
+    __device__ static void unpack(const uint4 &r, float (&v)[8]) {
+        v[0] = bf16_lo(r.x);
+        v[1] = bf16_hi(r.x);
+        v[2] = bf16_lo(r.y);
+        v[3] = bf16_hi(r.y);
+        v[4] = bf16_lo(r.z);
+        v[5] = bf16_hi(r.z);
+        v[6] = bf16_lo(r.w);
+        v[7] = bf16_hi(r.w);
+    }
+    __device__ static uint4 pack(const float (&v)[8]) {
+        return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                          pack_bf16x2(v[6], v[7]));
+    }
+    __device__ static float load1(const void *p, int64_t e) {
+        return bf16_one(__ldcs(reinterpret_cast<const unsigned short *>(p) + e));
+    }
+    __device__ static void store1(void *p, int64_t e, float v) {
+        __stcs(reinterpret_cast<unsigned short *>(p) + e, static_cast<unsigned short>(to_bf16(v)));
+    }
+};
+
+template <class Prm>
+__device__ __forceinline__ float finish(const Prm &p, float s) {
+    if (p.mode == kModeMulInv) return __fmul_rn(s, p.inv_p);  // exact: P is a power of two
+    if (p.mode == kModeDiv) return __fdiv_rn(s, p.fp);
+    return s;
+}
+
+// Fold one 16-byte vector at element e of row `row`, ring order from worker c.
+template <typename T, class Prm>
+__device__ __forceinline__ void fold_vec(const Prm &p, int row, int c, int64_t e) {
+    constexpr int V = Elem<T>::kVec;
+    const int P = p.P;
+    const void *const *src = p.src + static_cast<int64_t>(row) * P;
+    float acc[V];
+    for (int k0 = 0; k0 < P; k0 += kLoadBatch) {
+        uint4 raw[kLoadBatch];
+#pragma unroll
+        for (int j = 0; j < kLoadBatch; ++j) {
+            if (k0 + j < P) {
+                int w = c + k0 + j;
+                w -= (w >= P) ? P : 0;
+                raw[j] = ld16(static_cast<const T *>(src[w]) + e);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kLoadBatch; ++j) {
+            if (k0 + j < P) {
+                float v[V];
+                Elem<T>::unpack(raw[j], v);
+                if (k0 + j == 0) {
+#pragma unroll
+                    for (int q = 0; q < V; ++q) acc[q] = v[q];
+                } else {
+#pragma unroll
+                    for (int q = 0; q < V; ++q) acc[q] = __fadd_rn(acc[q], v[q]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < V; ++q) acc[q] = finish(p, acc[q]);
+    const uint4 out = Elem<T>::pack(acc);
+    void *const *dst = p.dst + static_cast<int64_t>(row) * p.n_out;
+    for (int k = 0; k < p.n_out; ++k) st16(static_cast<T *>(dst[k]) + e, out);
+}
+
+template <typename T, class Prm>
+__device__ __forceinline__ void fold_one(const Prm &p, int row, int c, int64_t e) {
+    const int P = p.P;
+    const void *const *src = p.src + static_cast<int64_t>(row) * P;
+    float acc = Elem<T>::load1(src[c], e);
+    for (int k = 1; k < P; ++k) {
+        int w = c + k;
+        w -= (w >= P) ? P : 0;
+        acc = __fadd_rn(acc, Elem<T>::load1(src[w], e));
+    }
+    acc = finish(p, acc);
+    void *const *dst = p.dst + static_cast<int64_t>(row) * p.n_out;
+    for (int k = 0; k < p.n_out; ++k) Elem<T>::store1(dst[k], e, acc);
+}
+
+template <typename T, class Prm>
+__global__ void __launch_bounds__(kThreads) ring_fold_kernel(const __grid_constant__ Prm p) {
+    constexpr int V = Elem<T>::kVec;
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        // the piece that owns tile t: largest i with tile_start[i] <= t (uniform per CTA)
+        int lo = 0, hi = p.npieces - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.tile_start[mid] <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        const Piece pc = p.piece[lo];
+        const int64_t lt = t - p.tile_start[lo];
+        if (pc.vec) {
+            int64_t vb = (pc.begin + V - 1) / V * V;
+            if (vb > pc.end) vb = pc.end;
+            int64_t ve = pc.end / V * V;
+            if (ve < vb) ve = vb;
+            const int64_t nvec = (ve - vb) / V;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t i = lt * kTileUnits + u * kThreads + threadIdx.x;
+                if (i < nvec) fold_vec<T>(p, pc.row, pc.chunk, vb + i * V);
+            }
+            if (lt == 0) {  // ragged head and tail of the piece (fewer than V each)
+                const int head = static_cast<int>(vb - pc.begin);
+                const int tail = static_cast<int>(pc.end - ve);
+                if (threadIdx.x < head) fold_one<T>(p, pc.row, pc.chunk, pc.begin + threadIdx.x);
+                else if (threadIdx.x >= 32 && threadIdx.x < 32 + tail)
+                    fold_one<T>(p, pc.row, pc.chunk, ve + (threadIdx.x - 32));
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t e = pc.begin + lt * kTileUnits + u * kThreads + threadIdx.x;
+                if (e < pc.end) fold_one<T>(p, pc.row, pc.chunk, e);
+            }
+        }
+    }
+}
+
+// Launch configuration: enough CTAs to fill every SM at full occupancy,
+// striding over the tiles.
+template <typename T, class Prm>
+int launch_fold(const Prm &p, cudaStream_t stream) {
+    if (p.total_tiles <= 0) return GAR_OK;
+    static int per_sm[2] = {0, 0};
+    int &occ = per_sm[sizeof(T) == 4 ? 0 : 1];
+    if (occ == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ring_fold_kernel<T, Prm>, kThreads, 0) != cudaSuccess ||
+            n <= 0)
+            n = 4;
+        occ = n;
+    }
+    int64_t grid = static_cast<int64_t>(sm_count()) * occ;
+    if (grid > p.total_tiles) grid = p.total_tiles;
+    ring_fold_kernel<T, Prm><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+    return check_launch("ring_fold_kernel");
+}
+
+template <class Prm>
+void set_mode(Prm &p, int op, int P) {
+    p.fp = static_cast<float>(P);
+    p.inv_p = 1.0f / static_cast<float>(P);
+    if (op == GAR_SUM || P == 1) p.mode = kModeSum;
+    else if ((P & (P - 1)) == 0) p.mode = kModeMulInv;
+    else p.mode = kModeDiv;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ host
+// Number of tiles a piece needs (at least one: tile 0 also folds the ragged
+// head and tail).
+static int64_t piece_tiles(const Piece &pc, int V) {
+    if (!pc.vec) {
+        const int64_t t = ceil_div(pc.end - pc.begin, kTileUnits);
+        return t > 0 ? t : 1;
+    }
+    int64_t vb = (pc.begin + V - 1) / V * V;
+    if (vb > pc.end) vb = pc.end;
+    int64_t ve = pc.end / V * V;
+    if (ve < vb) ve = vb;
+    const int64_t t = ceil_div((ve - vb) / V, kTileUnits);
+    return t > 0 ? t : 1;
+}
+
+template <class Prm>
+static void finalize_tiles(Prm &p, int V) {
+    int64_t tiles = 0;
+    for (int i = 0; i < p.npieces; ++i) {
+        p.tile_start[i] = tiles;
+        tiles += piece_tiles(p.piece[i], V);
+    }
+    p.tile_start[p.npieces] = tiles;
+    p.total_tiles = tiles;
+}
+
+template <class Prm>
+static int launch_dtype(const Prm &p, int32_t dtype, cudaStream_t stream) {
+    return dtype == GAR_F32 ? launch_fold<float>(p, stream) : launch_fold<uint16_t>(p, stream);
+}
+
+static int check_common(int32_t P, int64_t N, int32_t dtype, int32_t op) {
+    if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
+    if (N < 0) return fail(GAR_EINVAL, "N=%lld < 0", static_cast<long long>(N));
+    if (elem_bytes(dtype) < 0) return fail(GAR_EDTYPE, "unknown dtype %d", dtype);
+    if (op != GAR_SUM && op != GAR_AVG) return fail(GAR_EINVAL, "unknown op %d", op);
+    return GAR_OK;
+}
+
+// Ring all-reduce of one buffer per worker: n_out destinations.
+static int ring_single(const void *const *src, void *const *dst, int n_out, int32_t P, int64_t N,
+                       int32_t dtype, int32_t op, cudaStream_t stream) {
+    using Prm = FoldParamsSmall;
+    Prm p;
+    std::memset(&p, 0, sizeof(p));
+    p.P = P;
+    p.n_out = n_out;
+    set_mode(p, op, P);
+    const int es = elem_bytes(dtype);
+    if (N == 0) return GAR_OK;  // nothing is read or written: pointers may be NULL
+    bool vec = true;
+    for (int w = 0; w < P; ++w) {
+        if (!src[w]) return fail(GAR_EINVAL, "input buffer %d is NULL", w);
+        if (!aligned(src[w], es)) return fail(GAR_EALIGN, "input buffer %d not aligned to %d bytes", w, es);
+        vec = vec && aligned(src[w], 16);
+        p.src[w] = src[w];
+    }
+    for (int k = 0; k < n_out; ++k) {
+        if (!dst[k]) return fail(GAR_EINVAL, "output buffer %d is NULL", k);
+        if (!aligned(dst[k], es)) return fail(GAR_EALIGN, "output buffer %d not aligned to %d bytes", k, es);
+        vec = vec && aligned(dst[k], 16);
+        p.dst[k] = dst[k];
+    }
+    if (N == 0) return GAR_OK;
+    const int64_t clen = ceil_div(N, P);
+    for (int c = 0; c < P; ++c) {
+        const int64_t b = static_cast<int64_t>(c) * clen;
+        if (b >= N) break;
+        const int64_t e = b + clen < N ? b + clen : N;
+        Piece &pc = p.piece[p.npieces++];
+        pc.row = 0;
+        pc.chunk = c;
+        pc.vec = vec ? 1 : 0;
+        pc.pad = 0;
+        pc.begin = b;
+        pc.end = e;
+    }
+    finalize_tiles(p, 16 / es);
+    return launch_dtype(p, dtype, stream);
+}
+
+extern "C" int gar_ring_allreduce_sim(void *const *bufs, int32_t P, int64_t N, int32_t dtype, int32_t op,
+                                      gar_stream_t stream) {
+    int rc = check_common(P, N, dtype, op);
+    if (rc) return rc;
+    if (!bufs) return fail(GAR_EINVAL, "bufs is NULL");
+    for (int a = 0; a < P && N > 0; ++a)
+        for (int b = a + 1; b < P; ++b)
+            if (bufs[a] == bufs[b]) return fail(GAR_EINVAL, "workers %d and %d share a buffer", a, b);
+    return ring_single(reinterpret_cast<const void *const *>(bufs), bufs, P, P, N, dtype, op,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gar_ring_allreduce_sim_out(const void *const *bufs, int32_t P, int64_t N, int32_t dtype, int32_t op,
+                                          void *const *out, int32_t n_out, gar_stream_t stream) {
+    int rc = check_common(P, N, dtype, op);
+    if (rc) return rc;
+    if (!bufs || !out) return fail(GAR_EINVAL, "bufs or out is NULL");
+    if (n_out < 1 || n_out > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "n_out=%d outside [1, %d]", n_out, GAR_MAX_WORKERS);
+    return ring_single(bufs, out, n_out, P, N, dtype, op, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------- plan-driven (fused) launch
+int fused_allreduce_impl(const void *const *src, void *const *dst, int32_t P, const gar_seg *segs,
+                         const int32_t *dtype, int32_t count, const int64_t *buf_numel, int32_t n_buffers,
+                         int32_t op, cudaStream_t stream) {
+    using Prm = FoldParamsLarge;
+    Prm *p = new Prm;  // ~25 KB: keep it off the stack
+    int rc = GAR_OK;
+    for (int pass_dtype = 0; pass_dtype < 2 && rc == GAR_OK; ++pass_dtype) {
+        const int es = elem_bytes(pass_dtype);
+        std::memset(p, 0, sizeof(Prm));
+        p->P = P;
+        p->n_out = P;
+        set_mode(*p, op, P);
+        int rows = 0;
+        auto flush = [&]() -> int {
+            if (p->npieces == 0) return GAR_OK;
+            finalize_tiles(*p, 16 / es);
+            const int r = launch_dtype(*p, pass_dtype, stream);
+            p->npieces = 0;
+            rows = 0;
+            return r;
+        };
+        for (int i = 0; i < count && rc == GAR_OK; ++i) {
+            if (dtype[i] != pass_dtype || segs[i].numel == 0) continue;
+            const int b = segs[i].buffer;
+            const int64_t clen = ceil_div(buf_numel[b], P);
+            const int64_t first_chunk = segs[i].offset / clen;
+            const int64_t last_chunk = (segs[i].offset + segs[i].numel - 1) / clen;
+            const int need = static_cast<int>(last_chunk - first_chunk + 1);
+            if ((rows + 1) * P > kLargePtrs || p->npieces + need > kLargePieces) rc = flush();
+            if (rc) break;
+            bool vec = true;
+            for (int w = 0; w < P; ++w) {
+                const void *s = src[static_cast<int64_t>(w) * count + i];
+                void *d = dst[static_cast<int64_t>(w) * count + i];
+                vec = vec && aligned(s, 16) && aligned(d, 16);
+                p->src[rows * P + w] = s;
+                p->dst[rows * P + w] = d;
+            }
+            int64_t pos = 0;
+            const int64_t off = segs[i].offset, n = segs[i].numel;
+            while (pos < n) {
+                const int64_t c = (off + pos) / clen;
+                int64_t stop = (c + 1) * clen - off;
+                if (stop > n) stop = n;
+                Piece &pc = p->piece[p->npieces++];
+                pc.row = rows;
+                pc.chunk = static_cast<int32_t>(c);
+                pc.vec = vec ? 1 : 0;
+                pc.pad = 0;
+                pc.begin = pos;
+                pc.end = stop;
+                pos = stop;
+            }
+            ++rows;
+        }
+        if (rc == GAR_OK) rc = flush();
+    }
+    delete p;
+    return rc;
+}
+
+// ------------------------------------------------- literal step schedule
+namespace {
+
+__global__ void ring_step_kernel(const __grid_constant__ StepParams p) {
+    // worker i = blockIdx.y receives from i - 1 into chunk (i - s - 1) mod P
+    // (scatter-reduce) or (i - s) mod P (all-gather)
+    const int P = p.P;
+    const int i = blockIdx.y;
+    const int from = (i - 1 + P) % P;
+    const int c = p.gather ? ((i - p.step) % P + P) % P : ((i - p.step - 1) % P + 2 * P) % P;
+    const int64_t b = static_cast<int64_t>(c) * p.clen;
+    int64_t e = b + p.clen;
+    if (e > p.N) e = p.N;
+    float *mine = p.buf[i];
+    const float *recv = p.buf[from];
+    for (int64_t k = b + blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < e;
+         k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        mine[k] = p.gather ? recv[k] : __fadd_rn(mine[k], recv[k]);
+    }
+}
+
+__global__ void ring_divide_kernel(const __grid_constant__ StepParams p) {
+    float *x = p.buf[blockIdx.y];
+    const float fp = static_cast<float>(p.P);
+    for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < p.N;
+         k += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        x[k] = __fdiv_rn(x[k], fp);
+}
+
+}  // namespace
+
+extern "C" int gar_ring_allreduce_steps(void *const *bufs, int32_t P, int64_t N, int32_t op, int32_t *steps,
+                                        int64_t *sent_elems, gar_stream_t stream_) {
+    int rc = check_common(P, N, GAR_F32, op);
+    if (rc) return rc;
+    if (!bufs) return fail(GAR_EINVAL, "bufs is NULL");
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    StepParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.P = P;
+    p.N = N;
+    p.clen = N > 0 ? ceil_div(N, P) : 0;
+    for (int w = 0; w < P; ++w) {
+        if (!bufs[w] && N > 0) return fail(GAR_EINVAL, "buffer %d is NULL", w);
+        if (!aligned(bufs[w], 4)) return fail(GAR_EALIGN, "buffer %d not 4-byte aligned", w);
+        p.buf[w] = static_cast<float *>(bufs[w]);
+    }
+    for (int a = 0; a < P && N > 0; ++a)
+        for (int b = a + 1; b < P; ++b)
+            if (bufs[a] == bufs[b]) return fail(GAR_EINVAL, "workers %d and %d share a buffer", a, b);
+    std::vector<int64_t> sent(P, 0);
+    auto chunk_len = [&](int c) -> int64_t {
+        const int64_t b = static_cast<int64_t>(c) * p.clen;
+        if (b >= N) return 0;
+        return (b + p.clen < N ? b + p.clen : N) - b;
+    };
+    const int64_t per_block = 256 * 8;
+    int64_t gx = p.clen > 0 ? ceil_div(p.clen, per_block) : 1;
+    if (gx > 65535) gx = 65535;
+    const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(P));
+    int nsteps = 0;
+    for (int phase = 0; phase < 2; ++phase) {
+        for (int s = 0; s < P - 1; ++s) {
+            p.step = s;
+            p.gather = phase;
+            if (N > 0) {
+                ring_step_kernel<<<grid, 256, 0, stream>>>(p);
+                rc = check_launch("ring_step_kernel");
+                if (rc) return rc;
+            }
+            for (int i = 0; i < P; ++i) {
+                // worker i sends chunk (i - s) mod P, or (i - s + 1) mod P while gathering
+                const int c = phase ? ((i - s + 1) % P + P) % P : ((i - s) % P + P) % P;
+                sent[i] += chunk_len(c);
+            }
+            ++nsteps;
+        }
+    }
+    if (op == GAR_AVG && P > 1 && N > 0) {
+        int64_t gd = ceil_div(N, per_block);
+        if (gd > 65535) gd = 65535;
+        ring_divide_kernel<<<dim3(static_cast<unsigned>(gd), static_cast<unsigned>(P)), 256, 0, stream>>>(p);
+        rc = check_launch("ring_divide_kernel");
+        if (rc) return rc;
+    }
+    if (steps) *steps = nsteps;
+    if (sent_elems)
+        for (int i = 0; i < P; ++i) sent_elems[i] = sent[i];
+    return GAR_OK;
+}
+
+}  // namespace gar

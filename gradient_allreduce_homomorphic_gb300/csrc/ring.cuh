@@ -1,0 +1,58 @@
+// ring.cuh -- kernel-parameter layouts of the ring all-reduce kernels.
+#pragma once
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace gar {
+
+// A run of one tensor's elements that lies inside one ring chunk: the fold
+// of every element of the run starts at worker `chunk`.
+struct Piece {
+    int32_t row;    // row of the pointer tables (one tensor)
+    int32_t chunk;  // ring chunk id = first worker of the fold
+    int32_t vec;    // 1: all of the row's pointers are 16-byte aligned
+    int32_t pad;
+    int64_t begin;  // first element, in the tensor's own indexing
+    int64_t end;    // one past the last element
+};
+
+enum { kModeSum = 0, kModeMulInv = 1, kModeDiv = 2 };
+
+// Passed by value (kernel parameter space): no device-side tables to upload.
+template <int NPTR, int NPIECE>
+struct FoldParams {
+    int32_t P;        // workers
+    int32_t n_out;    // destinations per row
+    int32_t npieces;
+    int32_t mode;     // kMode*
+    float inv_p;      // 1/P (exact when P is a power of two)
+    float fp;         // P
+    int32_t pad0, pad1;
+    int64_t total_tiles;
+    int64_t tile_start[NPIECE + 1];  // first tile of each piece; [npieces] = total
+    Piece piece[NPIECE];
+    const void *src[NPTR];  // src[row * P + w]
+    void *dst[NPTR];        // dst[row * n_out + k]
+};
+
+constexpr int kSmallPtrs = 64, kSmallPieces = 64;
+constexpr int kLargePtrs = 1024, kLargePieces = 256;
+using FoldParamsSmall = FoldParams<kSmallPtrs, kSmallPieces>;  // < 4 KB
+using FoldParamsLarge = FoldParams<kLargePtrs, kLargePieces>;  // < 32 KB (large-parameter launch)
+static_assert(sizeof(FoldParamsSmall) <= 4096, "small fold parameters exceed 4 KB");
+static_assert(sizeof(FoldParamsLarge) <= 32000, "large fold parameters exceed the 32 KB launch limit");
+
+struct StepParams {
+    int32_t P, step, gather, pad;
+    int64_t N, clen;
+    float *buf[GAR_MAX_WORKERS];
+};
+
+// Plan-driven all-reduce over the workers' tensors (validated by the caller).
+int fused_allreduce_impl(const void *const *src, void *const *dst, int32_t P, const gar_seg *segs,
+                         const int32_t *dtype, int32_t count, const int64_t *buf_numel, int32_t n_buffers,
+                         int32_t op, cudaStream_t stream);
+
+}  // namespace gar

@@ -1,0 +1,576 @@
+// thc.cu -- uniform Tensor Homomorphic Compression ([T] section 4, Uniform
+// THC / Algorithm 1; section 5 for the index vectors the PS sums).
+//
+//   range      the preliminary round: global min / max over all workers
+//   encode     Philox-driven stochastic quantization to packed b-bit indices
+//   aggregate  integer sum of the workers' indices, never decoded (the PS)
+//   decode     index sum / P mapped back onto the grid (each worker)
+//   fused      encode (all workers) -> aggregate -> decode in one pass
+//
+// Index decision in fp32 (shared by encode and fused; one rounding per op):
+//   t = clamp((x - m) * sc, 0, L),  sc = L / (M - m)  (0 when M == m)
+//   floor: jm = t + 2^23 rounded down  ->  bits(jm) = 0x4B000000 + floor(t)
+//   f = t - (jm - 2^23)                  (exact)
+//   up iff u < f with u = (r mod 2^23) / 2^23; tested as
+//        1 + u  <  (1 + f) rounded up to the 2^-23 grid
+//   (both sides are exact: 1 + u is the float with mantissa r mod 2^23).
+// No integer<->float conversion is needed per element.
+#include <cstring>
+
+#include "common.cuh"
+
+namespace gar {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float range_scale(float m, float M, float L) {
+    return (M == m) ? 0.0f : __fdiv_rn(L, __fsub_rn(M, m));
+}
+
+// Index of x given the Philox word r; returns bits(jm) + up, i.e. the index
+// plus 0x4B000000 (the caller subtracts the constant once per sum).
+__device__ __forceinline__ uint32_t index_biased(float x, float m, float sc, float L, uint32_t r) {
+    float t = __fmul_rn(__fsub_rn(x, m), sc);
+    t = fminf(fmaxf(t, 0.0f), L);
+    const float jm = __fadd_rd(t, 8388608.0f);
+    const float f = __fsub_rn(t, __fsub_rn(jm, 8388608.0f));
+    const float f1 = __fadd_ru(f, 1.0f);
+    const float one_u = __uint_as_float((r & 0x007FFFFFu) | 0x3F800000u);
+    return __float_as_uint(jm) + (one_u < f1 ? 1u : 0u);
+}
+
+__device__ __forceinline__ uint4 philox_block(int64_t q, int worker, const PhiloxKeys &k) {
+    return philox10(make_uint4(static_cast<uint32_t>(q), static_cast<uint32_t>(static_cast<uint64_t>(q) >> 32),
+                               static_cast<uint32_t>(worker), 0u),
+                    k);
+}
+
+__device__ __forceinline__ uint32_t pick(const uint4 &r, int i) {
+    return i == 0 ? r.x : (i == 1 ? r.y : (i == 2 ? r.z : r.w));
+}
+
+// ------------------------------------------------------------------ range
+__device__ __forceinline__ void atomic_min_float(float *a, float v) {
+    if ((__float_as_uint(v) >> 31) == 0u) atomicMin(reinterpret_cast<int *>(a), __float_as_int(v));
+    else atomicMax(reinterpret_cast<unsigned int *>(a), __float_as_uint(v));
+}
+__device__ __forceinline__ void atomic_max_float(float *a, float v) {
+    if ((__float_as_uint(v) >> 31) == 0u) atomicMax(reinterpret_cast<int *>(a), __float_as_int(v));
+    else atomicMin(reinterpret_cast<unsigned int *>(a), __float_as_uint(v));
+}
+
+__global__ void thc_range_init(float *mM) {
+    mM[0] = __int_as_float(0x7F800000);   // +inf
+    mM[1] = __int_as_float(0xFF800000u);  // -inf
+}
+
+struct RangeParams {
+    const float *x[GAR_MAX_WORKERS];
+    int64_t N;
+    float *mM;
+    int32_t vec;  // all inputs 16-byte aligned
+    int32_t pad;
+};
+
+__global__ void __launch_bounds__(kThreads) thc_range_kernel(const __grid_constant__ RangeParams p) {
+    const float *x = p.x[blockIdx.y];
+    float lo = __int_as_float(0x7F800000), hi = __int_as_float(0xFF800000u);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    int64_t scalar_from = 0;
+    if (p.vec) {
+        const int64_t nv = p.N / 4;
+        const float4 *xv = reinterpret_cast<const float4 *>(x);
+        int64_t i = tid;
+        for (; i + stride < nv; i += 2 * stride) {  // two loads in flight
+            const float4 a = __ldcs(xv + i), b = __ldcs(xv + i + stride);
+            lo = fminf(lo, fminf(fminf(a.x, a.y), fminf(a.z, a.w)));
+            hi = fmaxf(hi, fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)));
+            lo = fminf(lo, fminf(fminf(b.x, b.y), fminf(b.z, b.w)));
+            hi = fmaxf(hi, fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w)));
+        }
+        if (i < nv) {
+            const float4 a = __ldcs(xv + i);
+            lo = fminf(lo, fminf(fminf(a.x, a.y), fminf(a.z, a.w)));
+            hi = fmaxf(hi, fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)));
+        }
+        scalar_from = nv * 4;
+    }
+    for (int64_t k = scalar_from + tid; k < p.N; k += stride) {
+        const float v = __ldcs(x + k);
+        lo = fminf(lo, v);
+        hi = fmaxf(hi, v);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+        hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
+    }
+    __shared__ float s_lo[kThreads / 32], s_hi[kThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        s_lo[warp] = lo;
+        s_hi[warp] = hi;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        lo = lane < kThreads / 32 ? s_lo[lane] : __int_as_float(0x7F800000);
+        hi = lane < kThreads / 32 ? s_hi[lane] : __int_as_float(0xFF800000u);
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) {
+            lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+            hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
+        }
+        if (lane == 0) {
+            if (lo == lo) atomic_min_float(p.mM, lo);  // NaN only if the slice was empty of numbers
+            if (hi == hi) atomic_max_float(p.mM + 1, hi);
+        }
+    }
+}
+
+// ----------------------------------------------------------------- encode
+struct EncodeParams {
+    PhiloxKeys keys;
+    const float *x;
+    const float *mM;
+    uint32_t *packed;
+    int64_t N;
+    int64_t nwords;
+    int32_t worker;
+    int32_t vec;
+    float L;
+    int32_t pad;
+};
+
+template <int B>
+__global__ void __launch_bounds__(kThreads) thc_encode_kernel(const __grid_constant__ EncodeParams p) {
+    constexpr int E = 32 / B;  // elements per packed word
+    const float m = p.mM[0], M = p.mM[1];
+    const float sc = range_scale(m, M, p.L);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < p.nwords; w += stride) {
+        const int64_t e0 = w * E;
+        uint32_t word = 0;
+        if (p.vec && e0 + E <= p.N) {
+            float4 v[E / 4];
+#pragma unroll
+            for (int g = 0; g < E / 4; ++g) v[g] = __ldcs(reinterpret_cast<const float4 *>(p.x + e0) + g);
+#pragma unroll
+            for (int g = 0; g < E / 4; ++g) {
+                const uint4 r = philox_block((e0 >> 2) + g, p.worker, p.keys);
+                const uint32_t i0 = index_biased(v[g].x, m, sc, p.L, r.x) - 0x4B000000u;
+                const uint32_t i1 = index_biased(v[g].y, m, sc, p.L, r.y) - 0x4B000000u;
+                const uint32_t i2 = index_biased(v[g].z, m, sc, p.L, r.z) - 0x4B000000u;
+                const uint32_t i3 = index_biased(v[g].w, m, sc, p.L, r.w) - 0x4B000000u;
+                word |= (i0 | (i1 << B) | (i2 << (2 * B)) | (i3 << (3 * B))) << (4 * g * B);
+            }
+        } else {
+            for (int g = 0; g < E / 4; ++g) {
+                const int64_t eb = e0 + 4 * g;
+                if (eb >= p.N) break;
+                const uint4 r = philox_block(eb >> 2, p.worker, p.keys);
+                for (int i = 0; i < 4 && eb + i < p.N; ++i) {
+                    const uint32_t idx = index_biased(p.x[eb + i], m, sc, p.L, pick(r, i)) - 0x4B000000u;
+                    word |= idx << ((4 * g + i) * B);
+                }
+            }
+        }
+        __stcs(p.packed + w, word);
+    }
+}
+
+// -------------------------------------------------------------- aggregate
+struct AggParams {
+    const uint32_t *packed[GAR_MAX_WORKERS];
+    uint16_t *sums;
+    int64_t N;
+    int64_t nwords;
+    int32_t P;
+    int32_t vec;  // every packed vector and sums 16-byte aligned
+};
+
+// Sixteen-bit lanes: word bits [B*i, B*i + B) hold element i and bits
+// [16 + B*i, ...) element i + 16/B, so masking with the pair mask and
+// adding sums two elements per 32-bit add without carries (P*L <= 65535).
+template <int B>
+__global__ void __launch_bounds__(kThreads) thc_aggregate_kernel(const __grid_constant__ AggParams p) {
+    constexpr int E = 32 / B;
+    constexpr int K = 16 / B;  // lane-pair accumulators per word
+    constexpr uint32_t kPair = ((1u << B) - 1u) | (((1u << B) - 1u) << 16);
+    const int64_t ngroups = p.nwords / 4;  // whole 16-byte groups of words
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    if (p.vec) {
+        for (int64_t g = tid; g < ngroups; g += stride) {
+            if ((g + 1) * 4 * E > p.N) break;  // the group holding the tail is done below
+            uint32_t acc[4][K];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int i = 0; i < K; ++i) acc[j][i] = 0;
+            for (int w = 0; w < p.P; ++w) {
+                const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(p.packed[w]) + g);
+                const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int i = 0; i < K; ++i) acc[j][i] += (words[j] >> (B * i)) & kPair;
+            }
+            // element j*E + i is the low half of acc[j][i], element j*E + K + i the high half
+            uint32_t out[4 * E / 2];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int i = 0; i < K; i += 2) {
+                    out[(j * E + i) / 2] = __byte_perm(acc[j][i], acc[j][i + 1], 0x5410);
+                    out[(j * E + K + i) / 2] = __byte_perm(acc[j][i], acc[j][i + 1], 0x7632);
+                }
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(p.sums + g * 4 * E);
+#pragma unroll
+            for (int q = 0; q < 4 * E / 8; ++q)
+                __stcs(dst + q, make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]));
+        }
+    }
+    // elements not covered above: one element per thread
+    int64_t first = 0;
+    if (p.vec) {
+        first = (p.N / (4 * E)) * 4 * E;
+        if (first > ngroups * 4 * E) first = ngroups * 4 * E;
+    }
+    const uint32_t L = (1u << B) - 1u;
+    for (int64_t e = first + tid; e < p.N; e += stride) {
+        uint32_t s = 0;
+        for (int w = 0; w < p.P; ++w) s += (p.packed[w][e / E] >> ((e % E) * B)) & L;
+        p.sums[e] = static_cast<uint16_t>(s);
+    }
+}
+
+// ----------------------------------------------------------------- decode
+struct DecodeParams {
+    const uint16_t *sums;
+    const float *mM;
+    float *avg;
+    int64_t N;
+    float L;
+    float fp;  // P
+    int32_t vec;
+    int32_t pad;
+};
+
+__device__ __forceinline__ float decode_step(const float *mM, float L, float fp, float &m) {
+    m = mM[0];
+    const float delta = __fdiv_rn(__fsub_rn(mM[1], m), L);
+    return __fdiv_rn(delta, fp);
+}
+// S < 2^23: the float with mantissa S, minus 2^23, is S exactly
+__device__ __forceinline__ float small_to_float(uint32_t s) {
+    return __fsub_rn(__uint_as_float(0x4B000000u | s), 8388608.0f);
+}
+
+__global__ void __launch_bounds__(kThreads) thc_decode_kernel(const __grid_constant__ DecodeParams p) {
+    float m;
+    const float k = decode_step(p.mM, p.L, p.fp, m);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    int64_t first = 0;
+    if (p.vec) {
+        const int64_t n8 = p.N / 8;
+        for (int64_t i = tid; i < n8; i += stride) {
+            const uint4 s = __ldcs(reinterpret_cast<const uint4 *>(p.sums) + i);
+            const uint32_t w[4] = {s.x, s.y, s.z, s.w};
+            float o[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                o[2 * q] = __fmaf_rn(small_to_float(w[q] & 0xFFFFu), k, m);
+                o[2 * q + 1] = __fmaf_rn(small_to_float(w[q] >> 16), k, m);
+            }
+            float4 *dst = reinterpret_cast<float4 *>(p.avg) + 2 * i;
+            __stcs(dst, make_float4(o[0], o[1], o[2], o[3]));
+            __stcs(dst + 1, make_float4(o[4], o[5], o[6], o[7]));
+        }
+        first = n8 * 8;
+    }
+    for (int64_t e = first + tid; e < p.N; e += stride)
+        p.avg[e] = __fmaf_rn(small_to_float(p.sums[e]), k, m);
+}
+
+// ------------------------------------------------------------------ fused
+struct FusedParams {
+    PhiloxKeys keys;
+    const float *x[GAR_MAX_WORKERS];
+    uint32_t *packed[GAR_MAX_WORKERS];  // all NULL when the wire vectors are not wanted
+    const float *mM;
+    float *avg;
+    int64_t N;
+    int64_t nwords;
+    int32_t P;
+    int32_t vec;  // inputs and avg 16-byte aligned
+    float L;
+    float fp;
+};
+
+template <int B, bool kPacked>
+__global__ void __launch_bounds__(kThreads) thc_fused_kernel(const __grid_constant__ FusedParams p) {
+    constexpr int E = 32 / B;
+    constexpr int G = E / 4;  // float4 groups (and Philox blocks) per word
+    const float m = p.mM[0], M = p.mM[1];
+    const float sc = range_scale(m, M, p.L);
+    float km;
+    const float k = decode_step(p.mM, p.L, p.fp, km);
+    const uint32_t bias = static_cast<uint32_t>(p.P) * 0x4B000000u;  // mod 2^32
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < p.nwords; w += stride) {
+        const int64_t e0 = w * E;
+        uint32_t s[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i) s[i] = 0;
+        if (p.vec && e0 + E <= p.N) {
+            float4 cur[G], nxt[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) cur[g] = __ldcs(reinterpret_cast<const float4 *>(p.x[0] + e0) + g);
+            for (int wk = 0; wk < p.P; ++wk) {
+                if (wk + 1 < p.P) {  // next worker's loads in flight while this one is quantized
+#pragma unroll
+                    for (int g = 0; g < G; ++g) nxt[g] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk + 1] + e0) + g);
+                }
+                uint32_t word = 0;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const uint4 r = philox_block((e0 >> 2) + g, wk, p.keys);
+                    const uint32_t a0 = index_biased(cur[g].x, m, sc, p.L, r.x);
+                    const uint32_t a1 = index_biased(cur[g].y, m, sc, p.L, r.y);
+                    const uint32_t a2 = index_biased(cur[g].z, m, sc, p.L, r.z);
+                    const uint32_t a3 = index_biased(cur[g].w, m, sc, p.L, r.w);
+                    s[4 * g] += a0;
+                    s[4 * g + 1] += a1;
+                    s[4 * g + 2] += a2;
+                    s[4 * g + 3] += a3;
+                    if (kPacked) {
+                        word |= ((a0 - 0x4B000000u) | ((a1 - 0x4B000000u) << B) | ((a2 - 0x4B000000u) << (2 * B)) |
+                                 ((a3 - 0x4B000000u) << (3 * B)))
+                                << (4 * g * B);
+                    }
+                }
+                if (kPacked) __stcs(p.packed[wk] + w, word);
+#pragma unroll
+                for (int g = 0; g < G; ++g) cur[g] = nxt[g];
+            }
+            float4 *dst = reinterpret_cast<float4 *>(p.avg + e0);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                __stcs(dst + g, make_float4(__fmaf_rn(small_to_float(s[4 * g] - bias), k, km),
+                                            __fmaf_rn(small_to_float(s[4 * g + 1] - bias), k, km),
+                                            __fmaf_rn(small_to_float(s[4 * g + 2] - bias), k, km),
+                                            __fmaf_rn(small_to_float(s[4 * g + 3] - bias), k, km)));
+            }
+        } else {  // ragged last word, or unaligned inputs: element by element
+            for (int wk = 0; wk < p.P; ++wk) {
+                uint32_t word = 0;
+                for (int g = 0; g < G; ++g) {
+                    const int64_t eb = e0 + 4 * g;
+                    if (eb >= p.N) break;
+                    const uint4 r = philox_block(eb >> 2, wk, p.keys);
+                    for (int i = 0; i < 4 && eb + i < p.N; ++i) {
+                        const uint32_t a = index_biased(p.x[wk][eb + i], m, sc, p.L, pick(r, i));
+                        s[4 * g + i] += a;
+                        word |= (a - 0x4B000000u) << ((4 * g + i) * B);
+                    }
+                }
+                if (kPacked) p.packed[wk][w] = word;
+            }
+            for (int i = 0; i < E && e0 + i < p.N; ++i) {
+                // elements never visited above kept s = 0; only in-range ones are stored
+                p.avg[e0 + i] = __fmaf_rn(small_to_float(s[i] - bias), k, km);
+            }
+        }
+    }
+}
+
+template <typename K>
+int grid_for(K kernel, int64_t work_items) {
+    if (work_items <= 0) return 0;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess || occ <= 0) occ = 2;
+    int64_t g = static_cast<int64_t>(sm_count()) * occ;
+    const int64_t need = ceil_div(work_items, kThreads);
+    if (g > need) g = need;
+    return static_cast<int>(g > 0 ? g : 1);
+}
+
+bool valid_b(int b) { return b == 1 || b == 2 || b == 4 || b == 8; }
+
+}  // namespace
+}  // namespace gar
+
+using namespace gar;
+
+extern "C" int64_t gar_thc_words(int64_t N, int32_t b) {
+    if (!valid_b(b) || N < 0) return 0;
+    const int64_t per = 32 / b;
+    return (N + per - 1) / per;
+}
+
+extern "C" int gar_thc_range(const float *const *x, int32_t P, int64_t N, float *d_mM, gar_stream_t stream_) {
+    if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
+    if (N < 0 || !x || !d_mM) return fail(GAR_EINVAL, "N < 0 or NULL argument");
+    if (!aligned(d_mM, 4)) return fail(GAR_EALIGN, "d_mM not 4-byte aligned");
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    RangeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.N = N;
+    p.mM = d_mM;
+    p.vec = 1;
+    for (int w = 0; w < P; ++w) {
+        if (!x[w] && N > 0) return fail(GAR_EINVAL, "input %d is NULL", w);
+        if (!aligned(x[w], 4)) return fail(GAR_EALIGN, "input %d not 4-byte aligned", w);
+        p.x[w] = x[w];
+        p.vec = p.vec && aligned(x[w], 16);
+    }
+    thc_range_init<<<1, 1, 0, stream>>>(d_mM);
+    int rc = check_launch("thc_range_init");
+    if (rc || N == 0) return rc;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, thc_range_kernel, kThreads, 0) != cudaSuccess || occ <= 0)
+        occ = 4;
+    int64_t per_worker = static_cast<int64_t>(sm_count()) * occ / P;
+    const int64_t need = ceil_div(ceil_div(N, 8), kThreads);  // two float4 per thread
+    if (per_worker > need) per_worker = need;
+    if (per_worker < 1) per_worker = 1;
+    thc_range_kernel<<<dim3(static_cast<unsigned>(per_worker), static_cast<unsigned>(P)), kThreads, 0, stream>>>(p);
+    return check_launch("thc_range_kernel");
+}
+
+extern "C" int gar_thc_encode(const float *x, int64_t N, const float *d_mM, int32_t b, uint64_t seed, int32_t worker,
+                              uint32_t *packed, gar_stream_t stream_) {
+    if (!valid_b(b)) return fail(GAR_EINVAL, "b=%d not in {1, 2, 4, 8}", b);
+    if (N < 0 || !d_mM) return fail(GAR_EINVAL, "N < 0 or d_mM NULL");
+    if (N == 0) return GAR_OK;
+    if (!x || !packed) return fail(GAR_EINVAL, "x or packed is NULL");
+    if (worker < 0) return fail(GAR_EINVAL, "worker %d < 0", worker);
+    if (!aligned(x, 4) || !aligned(packed, 4) || !aligned(d_mM, 4)) return fail(GAR_EALIGN, "misaligned pointer");
+    EncodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.keys = philox_keys(seed);
+    p.x = x;
+    p.mM = d_mM;
+    p.packed = packed;
+    p.N = N;
+    p.nwords = gar_thc_words(N, b);
+    p.worker = worker;
+    p.vec = aligned(x, 16) ? 1 : 0;
+    p.L = static_cast<float>((1 << b) - 1);
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    switch (b) {
+        case 1: thc_encode_kernel<1><<<grid_for(thc_encode_kernel<1>, p.nwords), kThreads, 0, stream>>>(p); break;
+        case 2: thc_encode_kernel<2><<<grid_for(thc_encode_kernel<2>, p.nwords), kThreads, 0, stream>>>(p); break;
+        case 4: thc_encode_kernel<4><<<grid_for(thc_encode_kernel<4>, p.nwords), kThreads, 0, stream>>>(p); break;
+        default: thc_encode_kernel<8><<<grid_for(thc_encode_kernel<8>, p.nwords), kThreads, 0, stream>>>(p); break;
+    }
+    return check_launch("thc_encode_kernel");
+}
+
+extern "C" int gar_thc_aggregate(const uint32_t *const *packed, int32_t P, int64_t N, int32_t b, uint16_t *sums,
+                                 gar_stream_t stream_) {
+    if (!valid_b(b)) return fail(GAR_EINVAL, "b=%d not in {1, 2, 4, 8}", b);
+    if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
+    if (static_cast<int64_t>(P) * ((1 << b) - 1) > 65535) return fail(GAR_EOVERFLOW, "P * (2^b - 1) > 65535");
+    if (N < 0) return fail(GAR_EINVAL, "N < 0");
+    if (N == 0) return GAR_OK;
+    if (!packed || !sums) return fail(GAR_EINVAL, "packed or sums is NULL");
+    if (!aligned(sums, 2)) return fail(GAR_EALIGN, "sums not 2-byte aligned");
+    AggParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.sums = sums;
+    p.N = N;
+    p.nwords = gar_thc_words(N, b);
+    p.P = P;
+    p.vec = aligned(sums, 16) ? 1 : 0;
+    for (int w = 0; w < P; ++w) {
+        if (!packed[w]) return fail(GAR_EINVAL, "packed vector %d is NULL", w);
+        if (!aligned(packed[w], 4)) return fail(GAR_EALIGN, "packed vector %d not 4-byte aligned", w);
+        p.packed[w] = packed[w];
+        p.vec = p.vec && aligned(packed[w], 16);
+    }
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const int64_t items = p.vec ? p.nwords / 4 + 4 * (32 / b) : N;
+    switch (b) {
+        case 1: thc_aggregate_kernel<1><<<grid_for(thc_aggregate_kernel<1>, items), kThreads, 0, stream>>>(p); break;
+        case 2: thc_aggregate_kernel<2><<<grid_for(thc_aggregate_kernel<2>, items), kThreads, 0, stream>>>(p); break;
+        case 4: thc_aggregate_kernel<4><<<grid_for(thc_aggregate_kernel<4>, items), kThreads, 0, stream>>>(p); break;
+        default: thc_aggregate_kernel<8><<<grid_for(thc_aggregate_kernel<8>, items), kThreads, 0, stream>>>(p); break;
+    }
+    return check_launch("thc_aggregate_kernel");
+}
+
+extern "C" int gar_thc_decode(const uint16_t *sums, int64_t N, const float *d_mM, int32_t b, int32_t P, float *avg,
+                              gar_stream_t stream_) {
+    if (!valid_b(b)) return fail(GAR_EINVAL, "b=%d not in {1, 2, 4, 8}", b);
+    if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
+    if (N < 0 || !d_mM) return fail(GAR_EINVAL, "N < 0 or d_mM NULL");
+    if (N == 0) return GAR_OK;
+    if (!sums || !avg) return fail(GAR_EINVAL, "sums or avg is NULL");
+    if (!aligned(sums, 2) || !aligned(avg, 4) || !aligned(d_mM, 4)) return fail(GAR_EALIGN, "misaligned pointer");
+    DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.sums = sums;
+    p.mM = d_mM;
+    p.avg = avg;
+    p.N = N;
+    p.L = static_cast<float>((1 << b) - 1);
+    p.fp = static_cast<float>(P);
+    p.vec = aligned(sums, 16) && aligned(avg, 16);
+    const int64_t items = p.vec ? ceil_div(N, 8) : N;
+    thc_decode_kernel<<<grid_for(thc_decode_kernel, items), kThreads, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(p);
+    return check_launch("thc_decode_kernel");
+}
+
+extern "C" int gar_thc_allreduce_fused(const float *const *x, int32_t P, int64_t N, int32_t b, uint64_t seed,
+                                       const float *d_mM, float *avg, uint32_t *const *packed, gar_stream_t stream_) {
+    if (!valid_b(b)) return fail(GAR_EINVAL, "b=%d not in {1, 2, 4, 8}", b);
+    if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
+    if (static_cast<int64_t>(P) * ((1 << b) - 1) > 65535) return fail(GAR_EOVERFLOW, "P * (2^b - 1) > 65535");
+    if (N < 0 || !d_mM || !x) return fail(GAR_EINVAL, "N < 0 or NULL argument");
+    if (N == 0) return GAR_OK;
+    if (!avg) return fail(GAR_EINVAL, "avg is NULL");
+    if (!aligned(avg, 4) || !aligned(d_mM, 4)) return fail(GAR_EALIGN, "misaligned pointer");
+    FusedParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.keys = philox_keys(seed);
+    p.mM = d_mM;
+    p.avg = avg;
+    p.N = N;
+    p.nwords = gar_thc_words(N, b);
+    p.P = P;
+    p.L = static_cast<float>((1 << b) - 1);
+    p.fp = static_cast<float>(P);
+    p.vec = aligned(avg, 16) ? 1 : 0;
+    for (int w = 0; w < P; ++w) {
+        if (!x[w]) return fail(GAR_EINVAL, "input %d is NULL", w);
+        if (!aligned(x[w], 4)) return fail(GAR_EALIGN, "input %d not 4-byte aligned", w);
+        p.x[w] = x[w];
+        p.vec = p.vec && aligned(x[w], 16);
+        if (packed) {
+            if (!packed[w]) return fail(GAR_EINVAL, "packed vector %d is NULL", w);
+            if (!aligned(packed[w], 4)) return fail(GAR_EALIGN, "packed vector %d not 4-byte aligned", w);
+            p.packed[w] = packed[w];
+        }
+    }
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+#define GAR_FUSED_CASE(BB)                                                                                  \
+    case BB:                                                                                                \
+        if (packed)                                                                                         \
+            thc_fused_kernel<BB, true><<<grid_for(thc_fused_kernel<BB, true>, p.nwords), kThreads, 0, stream>>>(p); \
+        else                                                                                                \
+            thc_fused_kernel<BB, false><<<grid_for(thc_fused_kernel<BB, false>, p.nwords), kThreads, 0, stream>>>(p); \
+        break;
+    switch (b) {
+        GAR_FUSED_CASE(1)
+        GAR_FUSED_CASE(2)
+        GAR_FUSED_CASE(4)
+        GAR_FUSED_CASE(8)
+    }
+#undef GAR_FUSED_CASE
+    return check_launch("thc_fused_kernel");
+}

@@ -1,0 +1,143 @@
+"""Per-kernel microbenchmark of libgar.so on one GPU.
+
+    python -m gradient_allreduce_homomorphic_gb300.microbench <case> [--P 8] [--N 16777216]
+           [--b 4] [--iters 20] [--warmup 3] [--dtype f32|bf16]
+
+Cases: ring (in-place ring all-reduce of P buffers), ring_out (reduce to one
+output), fused (plan-driven all-reduce of the 300-tensor ResNet-like model),
+pack, unpack, thc_range, thc_encode, thc_aggregate, thc_decode, thc_fused,
+thc_fused_packed, nmse.  Inputs are seeded N(0, 1) draws made on the device;
+every size is chosen by the caller, so a case can be kept small enough for a
+profiler capture.  Prints one JSON line: time per call (CUDA events on the
+launching stream, after warm-up) and algorithmic GB/s.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import sys
+
+import numpy as np
+
+_ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if _ROOT not in sys.path:
+    sys.path.insert(0, _ROOT)
+
+
+def main(argv=None):
+    import torch
+
+    import gradient_allreduce_homomorphic_gb300 as g
+    import workloads
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case")
+    ap.add_argument("--P", type=int, default=8)
+    ap.add_argument("--N", type=int, default=1 << 24)
+    ap.add_argument("--b", type=int, default=4)
+    ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--dtype", default="f32")
+    a = ap.parse_args(argv)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g.load()
+    P, N, b = a.P, a.N, a.b
+    tdt = torch.float32 if a.dtype == "f32" else torch.bfloat16
+    es = 4 if a.dtype == "f32" else 2
+
+    def bufs(n, k, dt=tdt, seed=0):
+        return [workloads.device_normal(n, 1.0, 77_000 + seed + i, dt, dev) for i in range(k)]
+
+    if a.case in ("ring", "ring_out"):
+        x = bufs(N, P)
+        if a.case == "ring":
+            t = g.pointer_table(x)
+            fn = lambda: g.gar_ring_allreduce_sim(t)  # noqa: E731
+            nbytes = 2 * P * N * es
+        else:
+            out = [torch.empty(N, dtype=tdt, device=dev)]
+            t, o = g.pointer_table(x), g.pointer_table(out)
+            fn = lambda: g.gar_ring_allreduce_sim_out(t, o)  # noqa: E731
+            nbytes = P * N * es + N * es
+    elif a.case in ("fused", "pack", "unpack"):
+        sizes = workloads.resnet_fusion_sizes()
+        dt = np.zeros(sizes.size, np.int32)
+        plan = g.gar_fusion_plan(sizes, dt, 64 << 20, 16)
+        n = int(sizes.sum())
+        src = [[workloads.device_normal(int(s), 1.0, 1000 * w + i, torch.float32, dev) for i, s in enumerate(sizes)]
+               for w in range(P)]
+        if a.case == "fused":
+            tables = g.fused_pointer_tables(src, src)
+            fn = lambda: g.gar_fused_allreduce(src, src, plan, tables=tables)  # noqa: E731
+            nbytes = 2 * P * n * 4
+        else:
+            fbs = [[torch.empty(int(k), device=dev) for k in plan.buf_numel] for _ in range(P)]
+            tabs = [g.pointer_table(src[w]) for w in range(P)]
+
+            def fn():
+                for w in range(P):
+                    for bb in range(plan.n_buffers):
+                        if a.case == "pack":
+                            g.gar_fusion_pack(tabs[w], plan, bb, fbs[w][bb])
+                        else:
+                            g.gar_fusion_unpack(fbs[w][bb], plan, bb, tabs[w])
+
+            nbytes = P * (n + int(plan.buf_numel.sum())) * 4 if a.case == "pack" else 2 * P * n * 4
+    elif a.case.startswith("thc") or a.case == "nmse":
+        x = bufs(N, P, torch.float32)
+        mM = torch.empty(2, device=dev)
+        g.gar_thc_range(x, mM)
+        words = g.gar_thc_words(N, b)
+        packed = [torch.zeros(words, dtype=torch.int32, device=dev) for _ in range(P)]
+        sums = torch.zeros(N, dtype=torch.int16, device=dev)
+        avg = torch.empty(N, device=dev)
+        xt, pt = g.pointer_table(x), g.pointer_table(packed)
+        if a.case == "thc_range":
+            fn = lambda: g.gar_thc_range(xt, mM)  # noqa: E731
+            nbytes = P * N * 4
+        elif a.case == "thc_encode":
+            fn = lambda: g.gar_thc_encode(x[0], mM, b, 5, 0, packed[0])  # noqa: E731
+            nbytes = N * 4 + words * 4
+        elif a.case == "thc_aggregate":
+            fn = lambda: g.gar_thc_aggregate(pt, N, b, sums)  # noqa: E731
+            nbytes = P * words * 4 + 2 * N
+        elif a.case == "thc_decode":
+            fn = lambda: g.gar_thc_decode(sums, mM, b, P, avg)  # noqa: E731
+            nbytes = 2 * N + 4 * N
+        elif a.case == "thc_fused":
+            fn = lambda: g.gar_thc_allreduce_fused(xt, b, 5, mM, avg)  # noqa: E731
+            nbytes = P * N * 4 + N * 4
+        elif a.case == "thc_fused_packed":
+            fn = lambda: g.gar_thc_allreduce_fused(xt, b, 5, mM, avg, pt)  # noqa: E731
+            nbytes = P * N * 4 + N * 4 + P * words * 4
+        else:
+            ws = torch.empty(g.gar_nmse_workspace_bytes(N) // 8, dtype=torch.float64, device=dev)
+            out = torch.empty(1, dtype=torch.float64, device=dev)
+            fn = lambda: g.gar_nmse(x[0], x[1], out, ws)  # noqa: E731
+            nbytes = 2 * N * 4
+    else:
+        raise SystemExit(f"unknown case {a.case}")
+
+    for _ in range(a.warmup):
+        fn()
+    torch.cuda.synchronize()
+    launches0 = g.gar_launch_count()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(a.iters):
+        s.record()
+        fn()
+        e.record()
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    launches = (g.gar_launch_count() - launches0) // max(a.iters, 1)
+    ms = float(np.median(times))
+    print(json.dumps({"case": a.case, "P": P, "N": N, "b": b, "dtype": a.dtype, "ms": round(ms, 4),
+                      "ms_min": round(float(np.min(times)), 4), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                      "bytes": int(nbytes), "launches_per_call": int(launches)}))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,275 @@
+/*
+ * gar.h -- C ABI of the GB300 gradient-averaging library (libgar.so).
+ *
+ * The library averages the gradients of P data-parallel workers whose
+ * buffers all live in one GPU's HBM.  Three parts, each a hand-written
+ * sm_103a CUDA kernel family behind the calls below:
+ *
+ *   1. Tensor Fusion   -- many small gradient tensors packed into large
+ *                         fusion buffers and scattered back afterwards.
+ *   2. Ring all-reduce -- the reduce-scatter + all-gather chunk schedule,
+ *                         computed as one pass that reproduces, bit for bit,
+ *                         the fp32 sum order of the 2(P-1)-step ring.
+ *   3. Uniform THC     -- shared range, Philox-driven stochastic quantization
+ *                         to b-bit indices, integer summation of the indices
+ *                         without decompression, one decode to the average.
+ *
+ * Sources (cited by page title and section):
+ *   [H] "Horovod: Fast and Easy Distributed Deep Learning in TensorFlow"
+ *       (explainer page): "The Ring-Allreduce Algorithm"; "Tensor Fusion:
+ *       Why Small Tensors Break Ring-Allreduce" (steps 1-6).
+ *   [R] "Collective Communication: Ring All-Reduce" tutorial: section 4
+ *       (schedule), section 5 (per-worker volume 2(P-1)/P of the buffer),
+ *       section 7 (ring simulator).
+ *   [T] "THC: Accelerating Distributed Deep Learning Using Tensor
+ *       Homomorphic Compression": section 2 (NMSE), section 4 (stochastic
+ *       quantization, uniform SQ on a global range, Uniform THC /
+ *       Algorithm 1), section 5 (index vectors summed at the PS).
+ *   [S] Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3"
+ *       (SC'11): Philox4x32-10.
+ *
+ * Conventions shared by every call
+ *   - Ownership: the caller owns every buffer.  "device" pointers are CUDA
+ *     device (or managed) memory; "host" arrays (pointer tables, plans) are
+ *     read during the call only and may be freed when it returns.  No call
+ *     allocates device memory.
+ *   - Asynchrony: device work is enqueued on `stream` (a cudaStream_t; NULL
+ *     is the legacy default stream) and the call returns without waiting.
+ *     The status covers argument checks and the launch itself.
+ *   - Errors: every call returns GAR_OK (0) or a negative gar_status; nothing
+ *     exits, traps or prints.  gar_last_error() returns a message for the
+ *     last failing call on the calling thread.
+ *   - Limits: 1 <= P <= GAR_MAX_WORKERS; sizes are element counts (int64).
+ *   - Alignment: device buffers with 16-byte aligned base addresses take
+ *     the vectorised paths; other addresses are accepted and take scalar
+ *     paths (same results).  Element alignment (4 B for fp32 and uint32,
+ *     2 B for bf16 and uint16) is required: GAR_EALIGN otherwise.
+ */
+#ifndef GAR_H
+#define GAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *gar_stream_t;
+
+typedef enum {
+    GAR_OK = 0,
+    GAR_EINVAL = -1,    /* null pointer, bad size, P, b, op, buffer id ...      */
+    GAR_EDTYPE = -2,    /* unknown dtype, or mixed dtypes where one is required */
+    GAR_EALIGN = -3,    /* pointer not aligned to its element size              */
+    GAR_EOVERFLOW = -4, /* P * (2^b - 1) exceeds the 16-bit index sum           */
+    GAR_ECUDA = -5      /* the CUDA runtime reported an error at launch         */
+} gar_status;
+
+typedef enum { GAR_F32 = 0, GAR_BF16 = 1 } gar_dtype;
+typedef enum { GAR_SUM = 0, GAR_AVG = 1 } gar_op;
+
+#define GAR_MAX_WORKERS 64
+
+/* One tensor's place in a fusion plan. */
+typedef struct {
+    int32_t buffer;   /* fusion buffer id, 0-based                    */
+    int32_t reserved; /* 0                                            */
+    int64_t offset;   /* first element of the tensor inside the buffer */
+    int64_t numel;    /* number of elements                           */
+} gar_seg;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int gar_version(void);
+
+/* Message for the last non-OK status returned on this thread ("" if none).
+ * The string stays valid until the next failing call on the thread. */
+const char *gar_last_error(void);
+
+/* Number of CUDA kernels this library has launched in this process (all
+ * threads, all devices), for accounting; never reset. */
+uint64_t gar_launch_count(void);
+
+/* ===================================================================== */
+/* Tensor Fusion [H] "Tensor Fusion", steps 1-6                          */
+/* ===================================================================== */
+
+/* gar_fusion_plan -- host only, no device work.
+ * Plans the fusion of `count` tensors taken in list (= ready) order
+ * (step 1): a tensor joins the open buffer if it has that buffer's dtype
+ * and fits in the room left, its start rounded up to `align_bytes`;
+ * otherwise the open buffer is closed and the tensor opens the next one
+ * (next-fit).  A tensor larger than the capacity gets a buffer to itself.
+ * Step 2's buffer size is `capacity_bytes` (64 MB default in Horovod).
+ *   numel[count], dtype[count]  host, per tensor (gar_dtype)
+ *   capacity_bytes              > 0
+ *   align_bytes                 > 0, a multiple of every used element size
+ *                               (16 lets every tensor start on a 16-B line)
+ *   segs[count]                 host, out: the tensor's buffer and offset
+ *   n_buffers                   host, out: number of buffers
+ *   buf_numel[count]            host, out: elements of each buffer, from 0
+ *                               to the end of its last tensor (only the first
+ *                               *n_buffers entries are written)
+ * Errors: GAR_EINVAL (null, count < 0, numel < 0, bad capacity/alignment),
+ *         GAR_EDTYPE (unknown dtype). */
+int gar_fusion_plan(const int64_t *numel, const int32_t *dtype, int32_t count,
+                    int64_t capacity_bytes, int32_t align_bytes, gar_seg *segs,
+                    int32_t *n_buffers, int64_t *buf_numel);
+
+/* gar_fusion_pack -- step 3: copy the tensors that the plan puts in `buffer`
+ * into `fusion_buf` at their offsets; the alignment gaps between them are
+ * zero-filled.  One worker's tensors per call.
+ *   src[count]    host array of device pointers (entries of tensors in other
+ *                 buffers are ignored and may be NULL)
+ *   segs, dtype   the plan and the per-tensor dtypes given to the plan
+ *   fusion_buf    device, buf_numel elements of the buffer's dtype
+ * Errors: GAR_EINVAL (bad buffer id, a segment outside buf_numel, null
+ *         pointer), GAR_EDTYPE (dtypes differ within the buffer),
+ *         GAR_EALIGN, GAR_ECUDA. */
+int gar_fusion_pack(const void *const *src, const gar_seg *segs, const int32_t *dtype,
+                    int32_t count, int32_t buffer, void *fusion_buf, int64_t buf_numel,
+                    gar_stream_t stream);
+
+/* gar_fusion_unpack -- step 5: copy each tensor of `buffer` from `fusion_buf`
+ * back to dst[i] (host array of device pointers).  Errors as for pack. */
+int gar_fusion_unpack(const void *fusion_buf, const gar_seg *segs, const int32_t *dtype,
+                      int32_t count, int32_t buffer, void *const *dst, gar_stream_t stream);
+
+/* gar_fused_allreduce -- steps 3-5 in one pass: for every fusion buffer of
+ * the plan, the ring all-reduce (as gar_ring_allreduce_sim, over the
+ * buffer's buf_numel elements with its chunking) is applied, reading the
+ * workers' tensors directly and writing each worker's result tensors
+ * directly; the fusion buffers themselves are never materialised.  Results
+ * are bit-identical to pack -> ring all-reduce -> unpack.
+ *   src[P * count]  host array: src[w * count + i] = worker w's tensor i
+ *   dst[P * count]  host array, same layout; dst may equal src (in place)
+ *   segs, dtype     plan and per-tensor dtypes; buf_numel[n_buffers]
+ *   op              GAR_SUM or GAR_AVG
+ * Errors: GAR_EINVAL, GAR_EDTYPE, GAR_EALIGN, GAR_ECUDA. */
+int gar_fused_allreduce(const void *const *src, void *const *dst, int32_t P,
+                        const gar_seg *segs, const int32_t *dtype, int32_t count,
+                        const int64_t *buf_numel, int32_t n_buffers, int32_t op,
+                        gar_stream_t stream);
+
+/* ===================================================================== */
+/* Ring all-reduce [H] "The Ring-Allreduce Algorithm", [R] sections 4, 5, 7 */
+/* ===================================================================== */
+
+/* gar_ring_allreduce_sim -- the ring all-reduce of P worker buffers held in
+ * one GPU's memory, in place: afterwards every bufs[w] holds the result.
+ * The buffer is cut into P chunks of ceil(N / P) elements (the trailing
+ * chunks short or empty when P does not divide N).  Chunk c starts on worker
+ * c and gains one worker per scatter-reduce hop, so every element of chunk c
+ * becomes the fp32 fold x_c + x_{c+1} + ... + x_{c+P-1} (indices mod P),
+ * left to right; the all-gather hands that value to every worker.  GAR_AVG
+ * then divides by P (fp32, round to nearest even).  bf16 buffers are widened
+ * exactly, folded in fp32 and rounded to bf16 (nearest even) once, at the
+ * end.  The result equals the literal 2(P-1)-step schedule bit for bit.
+ *   bufs[P]  host array of device pointers, each N elements of `dtype`
+ * Errors: GAR_EINVAL, GAR_EDTYPE, GAR_EALIGN, GAR_ECUDA. */
+int gar_ring_allreduce_sim(void *const *bufs, int32_t P, int64_t N, int32_t dtype, int32_t op,
+                           gar_stream_t stream);
+
+/* gar_ring_allreduce_sim_out -- the same result written to n_out separate
+ * device buffers out[n_out] (1 = reduce to one output, P = one per worker);
+ * the inputs bufs[P] are only read.  Outputs must not overlap the inputs. */
+int gar_ring_allreduce_sim_out(const void *const *bufs, int32_t P, int64_t N, int32_t dtype,
+                               int32_t op, void *const *out, int32_t n_out,
+                               gar_stream_t stream);
+
+/* gar_ring_allreduce_steps -- the literal schedule, one launch per ring
+ * step: P-1 scatter-reduce steps (worker i adds worker i-1's chunk
+ * (i-s-1) mod P into its own), P-1 all-gather steps (worker i overwrites its
+ * chunk (i-s) mod P with worker i-1's), then, for GAR_AVG, one element-wise
+ * division by P.  In place, fp32 only (a bf16 schedule would round the
+ * partial sums held in the buffers).  A checking path, not a fast one.
+ *   steps       host, out (may be NULL): ring steps executed, 2(P-1)
+ *   sent_elems  host, out (may be NULL): [P] elements each worker sent
+ * Errors: GAR_EINVAL, GAR_EDTYPE (bf16), GAR_EALIGN, GAR_ECUDA. */
+int gar_ring_allreduce_steps(void *const *bufs, int32_t P, int64_t N, int32_t op,
+                             int32_t *steps, int64_t *sent_elems, gar_stream_t stream);
+
+/* ===================================================================== */
+/* Uniform THC [T] section 4 (Algorithm 1) and section 5                 */
+/* ===================================================================== */
+/* Encoding of one coordinate x of worker `worker` at element index e, with
+ * L = 2^b - 1 and the shared range [m, M] (all in fp32, one rounding each):
+ *     t = clamp((x - m) * (L / (M - m)), 0, L)       (t = 0 when M == m)
+ *     j = floor(t),  f = t - j
+ *     r = word (e mod 4) of Philox4x32-10 [S] with key (seed low 32 bits,
+ *         seed high 32 bits) and counter (e/4 low, e/4 high, worker, 0)
+ *     u = (r mod 2^23) / 2^23
+ *     index = j + (u < f ? 1 : 0)
+ * so the index rounds up with probability f (to within 2^-23) and the
+ * quantized value m + index (M - m) / L is unbiased.  Indices are packed
+ * least-significant-bits first: element e in word e / (32/b) at bit
+ * (e mod (32/b)) * b; the last word is zero-padded.  b in {1, 2, 4, 8}. */
+
+/* Number of uint32 words that hold N packed b-bit indices (0 if b is bad). */
+int64_t gar_thc_words(int64_t N, int32_t b);
+
+/* gar_thc_range -- the preliminary round: d_mM[0] = min, d_mM[1] = max over
+ * all P * N entries (NaN entries are skipped; N = 0 gives +inf, -inf).
+ *   x[P]  host array of device fp32 pointers;  d_mM  device, 2 floats.
+ * Errors: GAR_EINVAL, GAR_EALIGN, GAR_ECUDA. */
+int gar_thc_range(const float *const *x, int32_t P, int64_t N, float *d_mM,
+                  gar_stream_t stream);
+
+/* gar_thc_encode -- one worker's quantization to packed b-bit indices.
+ *   x       device, N fp32;  d_mM  device [m, M] (e.g. from gar_thc_range)
+ *   packed  device, gar_thc_words(N, b) uint32 words, fully written
+ * Errors: GAR_EINVAL, GAR_EALIGN, GAR_ECUDA. */
+int gar_thc_encode(const float *x, int64_t N, const float *d_mM, int32_t b, uint64_t seed,
+                   int32_t worker, uint32_t *packed, gar_stream_t stream);
+
+/* gar_thc_aggregate -- the PS step: sums[e] = sum over workers of their
+ * index e, as exact integers, without decoding anything.
+ *   packed[P]  host array of device pointers (gar_thc_words(N, b) words each)
+ *   sums       device, N uint16
+ * Errors: GAR_EINVAL, GAR_EOVERFLOW (P * (2^b - 1) > 65535), GAR_EALIGN,
+ *         GAR_ECUDA. */
+int gar_thc_aggregate(const uint32_t *const *packed, int32_t P, int64_t N, int32_t b,
+                      uint16_t *sums, gar_stream_t stream);
+
+/* gar_thc_decode -- each worker's last step: the index sum divided by the
+ * number of workers, mapped back onto the grid:
+ *     avg[e] = fma(sums[e], ((M - m) / L) / P, m)      (fp32, one rounding
+ * per operation; within 1e-6 (|m| + |M|) of the exact value).
+ *   sums  device, N uint16;  d_mM  device [m, M];  avg  device, N fp32
+ * Errors: GAR_EINVAL, GAR_EALIGN, GAR_ECUDA. */
+int gar_thc_decode(const uint16_t *sums, int64_t N, const float *d_mM, int32_t b, int32_t P,
+                   float *avg, gar_stream_t stream);
+
+/* gar_thc_allreduce_fused -- encode (every worker), aggregate and decode in
+ * one pass over the P inputs: avg equals gar_thc_decode(gar_thc_aggregate(
+ * gar_thc_encode(x[w]) for w < P)) bit for bit.  If packed is non-NULL,
+ * packed[w] (device, gar_thc_words(N, b) words) also receives worker w's
+ * packed indices, the vector THC puts on the wire.
+ * Errors: GAR_EINVAL, GAR_EOVERFLOW, GAR_EALIGN, GAR_ECUDA. */
+int gar_thc_allreduce_fused(const float *const *x, int32_t P, int64_t N, int32_t b,
+                            uint64_t seed, const float *d_mM, float *avg,
+                            uint32_t *const *packed, gar_stream_t stream);
+
+/* ===================================================================== */
+/* NMSE [T] section 2: ||x - x_hat||^2 / ||x||^2                          */
+/* ===================================================================== */
+
+/* Bytes of device workspace gar_nmse needs for N elements. */
+size_t gar_nmse_workspace_bytes(int64_t N);
+
+/* gar_nmse -- *d_out (device, one double) = sum (x - x_hat)^2 / sum x^2,
+ * NaN when sum x^2 = 0.  Per-element terms are formed in fp32 and summed in
+ * fp64 in a fixed order (deterministic; within 2e-6 relative of an all-fp64
+ * sum).  x, x_hat: device, N fp32.  d_workspace: device, at least
+ * gar_nmse_workspace_bytes(N) bytes, 8-byte aligned, caller-owned, not
+ * shared with a concurrent call.
+ * Errors: GAR_EINVAL (null, N < 0, workspace too small), GAR_EALIGN,
+ *         GAR_ECUDA. */
+int gar_nmse(const float *x, const float *x_hat, int64_t N, double *d_out, void *d_workspace,
+             size_t workspace_bytes, gar_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GAR_H */

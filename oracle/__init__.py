@@ -63,6 +63,10 @@ def _load():
                 "oracle_ring_fold_bf16": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, vp]),
                 "oracle_ring_fold_bf16_at": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, i64, vp]),
                 "oracle_ring_schedule_bf16": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, vp]),
+                "oracle_ring_fold_f32_samples": (C.c_int, [vp, C.c_int, i64, C.c_int, vp, i64, vp]),
+                "oracle_ring_fold_bf16_samples": (C.c_int, [vp, C.c_int, i64, C.c_int, vp, i64, vp]),
+                "oracle_thc_allreduce_samples": (C.c_int, [vp, C.c_int, vp, i64, C.c_int, u64, C.c_float,
+                                                           C.c_float, vp, vp]),
                 "oracle_fusion_plan": (C.c_int, [vp, vp, C.c_int, i64, C.c_int, vp, vp, vp]),
                 "oracle_fusion_pack": (C.c_int, [pp, vp, vp, vp, C.c_int, C.c_int, vp, i64, C.c_int]),
                 "oracle_fusion_unpack": (C.c_int, [vp, vp, vp, vp, C.c_int, C.c_int, pp, C.c_int]),
@@ -165,6 +169,22 @@ def ring_fold_at(xs, n: int, idx, op: int = AVG):
     return out
 
 
+def ring_fold_samples(vals, n: int, idx, op: int = AVG):
+    """vals[w, k] = worker w's value at element idx[k] of its n-element buffer
+    (fp32, or uint16 bf16 bits); returns the ring fold at those elements."""
+    vals = np.ascontiguousarray(vals)
+    idx = np.ascontiguousarray(idx, np.int64)
+    p = vals.shape[0]
+    lib = _load()
+    if vals.dtype == np.float32:
+        out = np.empty(idx.size, np.float32)
+        _check(lib.oracle_ring_fold_f32_samples(_ptr(vals), p, n, op, _ptr(idx), idx.size, _ptr(out)), "samples")
+    else:
+        out = np.empty(idx.size, np.uint16)
+        _check(lib.oracle_ring_fold_bf16_samples(_ptr(vals), p, n, op, _ptr(idx), idx.size, _ptr(out)), "samples")
+    return out
+
+
 def bf16_to_f32(h: int) -> float:
     return float(_load().oracle_bf16_to_f32(int(h)))
 
@@ -190,9 +210,11 @@ def fusion_plan(numel, dtype, capacity_bytes: int = 64 << 20, align_bytes: int =
 
 
 def fusion_pack(srcs, seg_buffer, seg_offset, buffer: int, buf_numel: int):
-    es = srcs[0].dtype.itemsize if srcs else 4
-    dt = srcs[0].dtype if srcs else np.float32
+    members = [i for i, b in enumerate(seg_buffer) if b == buffer]
+    dt = srcs[members[0]].dtype if members else np.dtype(np.float32)
+    es = dt.itemsize
     numel = np.array([s.size for s in srcs], np.int64)
+    srcs = [s if s.dtype == dt else np.zeros(0, dt) for s in srcs]  # other buffers' tensors are not read
     sb = np.ascontiguousarray(seg_buffer, np.int32)
     so = np.ascontiguousarray(seg_offset, np.int64)
     out = np.empty(int(buf_numel), dt)
@@ -260,6 +282,18 @@ def thc_decode(sums, m, M, b: int, p: int) -> np.ndarray:
     _check(_load().oracle_thc_decode(_ptr(sums), sums.size, float(m), float(M), b, p, _ptr(out)),
            "thc_decode")
     return out
+
+
+def thc_allreduce_samples(vals, idx, b: int, seed: int, m, M):
+    """vals[w, k] = worker w's value at element idx[k]; returns (indices[w, k], avg[k])."""
+    vals = np.ascontiguousarray(vals, np.float32)
+    idx = np.ascontiguousarray(idx, np.int64)
+    p, k = vals.shape
+    ind = np.empty((p, k), np.uint8)
+    avg = np.empty(k, np.float64)
+    _check(_load().oracle_thc_allreduce_samples(_ptr(vals), p, _ptr(idx), k, b, seed, float(m), float(M),
+                                                _ptr(ind), _ptr(avg)), "thc_samples")
+    return ind, avg
 
 
 def thc_allreduce(xs, b: int, seed: int, m=None, M=None, want_packed: bool = False):

@@ -231,6 +231,34 @@ int oracle_ring_schedule_bf16(uint16_t *const *bufs, int p, int64_t n, int op,
     return rc;
 }
 
+int oracle_ring_fold_f32_samples(const float *vals, int p, int64_t n, int op, const int64_t *e,
+                                 int64_t count, float *out) {
+    if (p < 1 || n < 0) return -1;
+    for (int64_t k = 0; k < count; ++k) {
+        if (e[k] < 0 || e[k] >= n) return -1;
+        int c = (int)(e[k] / oracle_ring_chunk_len(n, p));
+        float s = vals[(int64_t)c * count + k];
+        for (int j = 1; j < p; ++j) s = s + vals[(int64_t)((c + j) % p) * count + k];
+        if (op == ORACLE_AVG) s = s / (float)p;
+        out[k] = s;
+    }
+    return 0;
+}
+
+int oracle_ring_fold_bf16_samples(const uint16_t *vals, int p, int64_t n, int op,
+                                  const int64_t *e, int64_t count, uint16_t *out) {
+    if (p < 1 || n < 0) return -1;
+    for (int64_t k = 0; k < count; ++k) {
+        if (e[k] < 0 || e[k] >= n) return -1;
+        int c = (int)(e[k] / oracle_ring_chunk_len(n, p));
+        float s = oracle_bf16_to_f32(vals[(int64_t)c * count + k]);
+        for (int j = 1; j < p; ++j) s = s + oracle_bf16_to_f32(vals[(int64_t)((c + j) % p) * count + k]);
+        if (op == ORACLE_AVG) s = s / (float)p;
+        out[k] = oracle_f32_to_bf16(s);
+    }
+    return 0;
+}
+
 /* ===================================================================== */
 /* Tensor Fusion [H] "Tensor Fusion", steps 1-6                           */
 /* ===================================================================== */
@@ -401,6 +429,23 @@ int oracle_thc_decode(const uint16_t *sums, int64_t n, float m, float M, int b, 
     double L = (double)((1 << b) - 1);
     double step = ((double)M - (double)m) / L;
     for (int64_t e = 0; e < n; ++e) avg[e] = (double)m + ((double)sums[e] / (double)p) * step;
+    return 0;
+}
+
+int oracle_thc_allreduce_samples(const float *vals, int p, const int64_t *e, int64_t count, int b,
+                                 uint64_t seed, float m, float M, uint8_t *idx, double *avg) {
+    if (!valid_bits(b) || p < 1 || count < 0) return -1;
+    double L = (double)((1 << b) - 1);
+    double step = ((double)M - (double)m) / L;
+    for (int64_t k = 0; k < count; ++k) {
+        uint32_t s = 0;
+        for (int w = 0; w < p; ++w) {
+            uint32_t i = oracle_thc_index(vals[(int64_t)w * count + k], m, M, b, seed, w, e[k]);
+            if (idx) idx[(int64_t)w * count + k] = (uint8_t)i;
+            s += i;
+        }
+        avg[k] = (double)m + ((double)s / (double)p) * step;
+    }
     return 0;
 }
 

@@ -71,6 +71,12 @@ int oracle_ring_fold_bf16_at(const uint16_t *const *x, int p, int64_t n, int op,
                              const int64_t *idx, int64_t count, uint16_t *out);
 int oracle_ring_schedule_bf16(uint16_t *const *bufs, int p, int64_t n, int op,
                               int64_t *sent_elems, int *steps);
+/* Sampled forms for buffers too large to copy to the host: vals[w * count + k]
+ * is worker w's value at element e[k] of its n-element buffer. */
+int oracle_ring_fold_f32_samples(const float *vals, int p, int64_t n, int op, const int64_t *e,
+                                 int64_t count, float *out);
+int oracle_ring_fold_bf16_samples(const uint16_t *vals, int p, int64_t n, int op,
+                                  const int64_t *e, int64_t count, uint16_t *out);
 
 /* ---------------- Tensor Fusion [H] ---------------- */
 /* Next-fit plan.  dtype[i] is ORACLE_F32 or ORACLE_BF16.  Outputs per tensor:
@@ -103,6 +109,11 @@ int oracle_thc_aggregate(const uint32_t *const *packed, int p, int64_t n, int b,
                          uint16_t *sums);
 int oracle_thc_decode(const uint16_t *sums, int64_t n, float m, float M, int b, int p,
                       double *avg);
+/* Sampled THC round: vals[w * count + k] is worker w's value at element e[k];
+ * idx[w * count + k] (may be NULL) receives its index, avg[k] the decoded
+ * average of element e[k]. */
+int oracle_thc_allreduce_samples(const float *vals, int p, const int64_t *e, int64_t count, int b,
+                                 uint64_t seed, float m, float M, uint8_t *idx, double *avg);
 /* encode every worker, aggregate, decode; packed may be NULL */
 int oracle_thc_allreduce(const float *const *x, int p, int64_t n, int b, uint64_t seed,
                          float m, float M, double *avg, uint32_t *const *packed);

@@ -208,3 +208,17 @@ def test_all_chunk_rotations_seen():
             before = (w_big - c) % P
             expect = 2.0 ** 24 if before <= 1 else 2.0 ** 24 + 4
             np.testing.assert_array_equal(s[2 * c:2 * c + 2], np.full(2, expect, np.float32))
+
+
+def test_samples_match_full_fold():
+    torch = pytest.importorskip("torch")
+    P, N = 6, 5003
+    xs = [np.random.default_rng([71, w]).standard_normal(N, dtype=np.float32) for w in range(P)]
+    idx = np.array([0, 1, 833, 834, 835, 4000, 5002], np.int64)
+    full = oracle.ring_fold(xs, op=oracle.AVG)
+    vals = np.stack([x[idx] for x in xs])
+    np.testing.assert_array_equal(oracle.ring_fold_samples(vals, N, idx), full[idx])
+    hb = [torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16) for x in xs]
+    fullb = oracle.ring_fold(hb, op=oracle.AVG)
+    valsb = np.stack([h[idx] for h in hb])
+    np.testing.assert_array_equal(oracle.ring_fold_samples(valsb, N, idx), fullb[idx])

@@ -263,3 +263,15 @@ def test_nmse_definition():
     assert oracle.nmse(x, np.zeros_like(x)) == 1.0
     assert abs(oracle.nmse(x, (2 * x).astype(np.float32)) - 1.0) < 1e-15
     assert math.isnan(oracle.nmse(np.zeros(4, np.float32), np.ones(4, np.float32)))
+
+
+def test_samples_match_full_round():
+    P, N, b = 5, 3001, 4
+    xs = [np.random.default_rng([73, w]).standard_normal(N).astype(np.float32) for w in range(P)]
+    m, M = oracle.thc_range(xs)
+    avg, packed = oracle.thc_allreduce(xs, b, 17, m, M, want_packed=True)
+    idx = np.array([0, 3, 4, 1500, 2999, 3000], np.int64)
+    ind, savg = oracle.thc_allreduce_samples(np.stack([x[idx] for x in xs]), idx, b, 17, m, M)
+    np.testing.assert_array_equal(savg, avg[idx])
+    for w in range(P):
+        np.testing.assert_array_equal(ind[w], oracle.thc_unpack(packed[w], N, b)[idx])

@@ -103,3 +103,17 @@ def device_normal(shape, var: float, seed: int, dtype, device):
     if var != 1.0:
         x.mul_(math.sqrt(var))
     return x.to(dtype)
+
+
+def device_student_t(n: int, nu: int, scale: float, seed: int, device):
+    """Seeded Student-t(nu) draws (integer nu) made on the device:
+    Z / sqrt(chi2_nu / nu) with chi2_nu a sum of nu squared normals."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    z = torch.randn(n, generator=g, device=device, dtype=torch.float32)
+    chi2 = torch.zeros(n, device=device, dtype=torch.float32)
+    for _ in range(nu):
+        chi2.addcmul_(*(2 * [torch.randn(n, generator=g, device=device, dtype=torch.float32)]))
+    return (z / torch.sqrt(chi2 / nu) * scale).to(torch.float32)
