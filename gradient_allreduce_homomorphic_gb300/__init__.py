@@ -60,6 +60,7 @@ _SIGNATURES = {
     "gar_thc_allreduce_fused": (C.c_int, [_pp, _i32, _i64, _i32, _u64, _vp, _vp, _pp, _vp]),
     "gar_nmse_workspace_bytes": (C.c_size_t, [_i64]),
     "gar_nmse": (C.c_int, [_vp, _vp, _i64, _vp, _vp, C.c_size_t, _vp]),
+    "gar_nmse_noalloc": (C.c_int, [_vp, _vp, _i64, _vp, _vp]),
 }
 
 
@@ -268,6 +269,12 @@ def gar_nmse_workspace_bytes(N: int) -> int:
 def gar_nmse(x, x_hat, d_out, workspace, stream=None):
     nbytes = workspace.numel() * workspace.element_size()
     _call("gar_nmse", _dev(x), _dev(x_hat), x.numel(), _dev(d_out), _dev(workspace), nbytes, _stream(stream))
+
+
+def gar_nmse_noalloc(x, x_hat, d_out, stream=None):
+    """NMSE without a workspace, for callers that may not allocate device
+    memory: partial sums go to a fixed array inside the library (see gar.h)."""
+    _call("gar_nmse_noalloc", _dev(x), _dev(x_hat), x.numel(), _dev(d_out), _stream(stream))
 
 
 __all__ = [n for n in dir() if n.startswith(("gar_", "GAR_"))] + ["GarError", "FusionPlan", "PtrTable", "load",

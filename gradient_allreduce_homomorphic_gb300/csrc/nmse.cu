@@ -7,6 +7,7 @@
 // fp64: fp64 throughput on this part is a small fraction of fp32, and one
 // fp32 rounding per term keeps the result within 2e-6 of an all-fp64 sum.
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -114,6 +115,69 @@ extern "C" int gar_nmse(const float *x, const float *x_hat, int64_t N, double *d
     double *ws = static_cast<double *>(d_workspace);
     nmse_partial_kernel<<<g, kThreads, 0, stream>>>(x, x_hat, N, vec, ws);
     int rc = check_launch("nmse_partial_kernel");
+    if (rc) return rc;
+    nmse_final_kernel<<<1, kThreads, 0, stream>>>(ws, g, d_out);
+    return check_launch("nmse_final_kernel");
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free NMSE.  Some callers cannot hand this library a workspace:
+// they are given their input and output buffers by someone else and may not
+// call cudaMalloc themselves -- e.g. a plug-in inside a host framework whose
+// allocator owns all of the device's memory, or a latency-critical path that
+// must not pay cudaMalloc's implicit device-wide synchronisation.  For them the
+// per-block partial sums live in the fixed array below, which is part of the
+// library's image: every GPU that loads the library holds these 16 KiB until
+// the process exits.  The array is shared by every call on a device and keeps
+// the last call's contents; nothing in it needs to start at zero, because each
+// CTA of the first kernel overwrites its own pair before the second kernel
+// reads it.  Calls that overlap on the GPU (e.g. on two streams) race on it.
+namespace {
+
+constexpr int kStaticPairs = 1024;  // (sum (x - x_hat)^2, sum x^2) per CTA, at most 1024 CTAs
+static_assert(kStaticPairs >= kMaxBlocks, "the static scratch must hold one pair per CTA");
+static __device__ __align__(256) double g_nmse_scratch[2 * kStaticPairs];
+
+std::mutex g_scratch_mutex;
+double *g_scratch_addr[64] = {};
+
+// Device address of g_nmse_scratch on the current device, looked up once per
+// device (host code cannot use the symbol itself as a device pointer).
+int static_scratch(double **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(GAR_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(GAR_EINVAL, "device ordinal %d outside [0, 64)", dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_nmse_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(GAR_ECUDA, "cudaGetSymbolAddress(nmse scratch): %s", cudaGetErrorString(e));
+        g_scratch_addr[dev] = static_cast<double *>(p);
+    }
+    *out = g_scratch_addr[dev];
+    return GAR_OK;
+}
+
+}  // namespace
+
+extern "C" int gar_nmse_noalloc(const float *x, const float *x_hat, int64_t N, double *d_out, gar_stream_t stream_) {
+    if (N < 0 || !d_out) return fail(GAR_EINVAL, "N < 0 or d_out is NULL");
+    if (N > 0 && (!x || !x_hat)) return fail(GAR_EINVAL, "x or x_hat is NULL");
+    const int g = nmse_blocks(N);
+    if (g > kStaticPairs)  // cannot happen while nmse_blocks caps the grid at kMaxBlocks
+        return fail(GAR_EINVAL, "N=%lld needs %d partial sums, the static scratch holds %d",
+                    static_cast<long long>(N), g, kStaticPairs);
+    if (!aligned(d_out, 8)) return fail(GAR_EALIGN, "d_out not 8-byte aligned");
+    if ((x && !aligned(x, 4)) || (x_hat && !aligned(x_hat, 4))) return fail(GAR_EALIGN, "x or x_hat not 4-byte aligned");
+    double *ws = nullptr;
+    int rc = static_scratch(&ws);
+    if (rc) return rc;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const int vec = aligned(x, 16) && aligned(x_hat, 16);
+    nmse_partial_kernel<<<g, kThreads, 0, stream>>>(x, x_hat, N, vec, ws);
+    rc = check_launch("nmse_partial_kernel");
     if (rc) return rc;
     nmse_final_kernel<<<1, kThreads, 0, stream>>>(ws, g, d_out);
     return check_launch("nmse_final_kernel");

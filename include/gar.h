@@ -269,6 +269,27 @@ size_t gar_nmse_workspace_bytes(int64_t N);
 int gar_nmse(const float *x, const float *x_hat, int64_t N, double *d_out, void *d_workspace,
              size_t workspace_bytes, gar_stream_t stream);
 
+/* gar_nmse_noalloc -- no counterpart in the pages: a library convenience.
+ * The same NMSE as gar_nmse (same kernels, same summation order, same result)
+ * for callers that cannot provide a workspace because they may not allocate
+ * device memory themselves -- for instance a plug-in running inside a host
+ * framework whose allocator owns all of the device's memory, or a
+ * latency-critical path that must not pay cudaMalloc's implicit device-wide
+ * synchronisation.  The caller still passes x, x_hat (device, N fp32) and
+ * d_out (device, one double).  The call allocates nothing: the per-block
+ * partial sums go to a fixed 16 KiB array inside the library (1024 pairs of
+ * doubles; every GPU that loads the library holds it until the process
+ * exits).  Every N >= 0 fits, because the reduction never uses more than 1024
+ * blocks; a size needing more partial sums than the array holds would be
+ * rejected with GAR_EINVAL.  The first call on a device looks up that array's
+ * device address (cudaGetSymbolAddress) with the device current; make that
+ * first call before any stream capture.  All calls on a device share the
+ * array and it keeps the last call's contents (nothing in it needs to start
+ * at zero); calls that overlap on the GPU, e.g. on two streams, race.
+ * Errors: GAR_EINVAL (null, N < 0), GAR_EALIGN, GAR_ECUDA. */
+int gar_nmse_noalloc(const float *x, const float *x_hat, int64_t N, double *d_out,
+                     gar_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
