@@ -124,8 +124,11 @@ class ClockSampler:
 class Step:
     """Device-resident state and the per-step call sequence."""
 
-    def __init__(self, torch, g, dev):
+    STAGES = ["fused_ring", "pack", "thc_fused", "unpack", "nmse"]
+
+    def __init__(self, torch, g, dev, schedule="overlap"):
         self.torch, self.g, self.dev = torch, g, dev
+        self.schedule = schedule
         sizes = workloads.resnet_fusion_sizes()
         self.sizes = sizes
         self.n_params = int(sizes.sum())
@@ -137,96 +140,114 @@ class Step:
         cfg = workloads.CONFIG_IDS[WORKLOAD]
         self.flat = [workloads.device_normal(self.flat_len, 0.01, 1000 * cfg + w, torch.float32, dev) for w in range(P)]
         self.src = [self._views(f) for f in self.flat]
-        self.ring_flat = [torch.empty(self.flat_len, dtype=torch.float32, device=dev) for _ in range(P)]
+        # outputs: zeros, so the flat padding between tensors stays 0 and the
+        # NMSE over the flat buffers equals the NMSE over the tensors
+        self.ring_flat = [torch.zeros(self.flat_len, dtype=torch.float32, device=dev) for _ in range(P)]
         self.ring = [self._views(f) for f in self.ring_flat]
-        self.thc_flat = torch.empty(self.flat_len, dtype=torch.float32, device=dev)
+        self.thc_flat = torch.zeros(self.flat_len, dtype=torch.float32, device=dev)
         self.thc = self._views(self.thc_flat)
         self.plan = g.gar_fusion_plan(sizes, self.dtype, CAPACITY, ALIGN)
         self.nb = self.plan.n_buffers
         bn = self.plan.buf_numel
         self.fusion = [[torch.empty(int(bn[b]), dtype=torch.float32, device=dev) for b in range(self.nb)]
                        for _ in range(P)]
-        self.ring_fb = [torch.empty(int(bn[b]), dtype=torch.float32, device=dev) for b in range(self.nb)]
         self.thc_avg = [torch.empty(int(bn[b]), dtype=torch.float32, device=dev) for b in range(self.nb)]
         self.words = [g.gar_thc_words(int(bn[b]), B_THC) for b in range(self.nb)]
         self.packed = [[torch.empty(self.words[b], dtype=torch.int32, device=dev) for b in range(self.nb)]
                        for _ in range(P)]
         self.mM = torch.empty((self.nb, 2), dtype=torch.float32, device=dev)
-        self.nmse = torch.empty(self.nb, dtype=torch.float64, device=dev)
-        self.ws = torch.empty(max(g.gar_nmse_workspace_bytes(int(x)) for x in bn) // 8 + 1, dtype=torch.float64,
-                              device=dev)
+        self.nmse = torch.empty(1, dtype=torch.float64, device=dev)
+        self.ws = torch.empty(g.gar_nmse_workspace_bytes(self.flat_len) // 8 + 1, dtype=torch.float64, device=dev)
         # host pointer tables built once (the tensors do not move between steps)
-        self.tables = g.fused_pointer_tables(self.src, self.ring)
-        self.src_tab = [g.pointer_table(self.src[w]) for w in range(P)]
-        self.ring0_tab = g.pointer_table(self.ring[0])
+        self.ring_tables = g.fused_pointer_tables(self.src, self.ring)
+        self.pack_tables = g.pack_all_tables(self.src, self.fusion)
         self.thc_tab = g.pointer_table(self.thc)
         self.fusion_col = [g.pointer_table([self.fusion[w][b] for w in range(P)]) for b in range(self.nb)]
         self.packed_col = [g.pointer_table([self.packed[w][b] for w in range(P)]) for b in range(self.nb)]
         self.buf_total = int(bn.sum())
-        self.stages = ["fused_ring", "pack", "thc_range", "thc_fused", "unpack", "nmse"]
+        self.stream_r = torch.cuda.Stream(device=dev)
+        self.stream_t = torch.cuda.Stream(device=dev)
+        self.stages = list(self.STAGES)
 
     def _views(self, flat):
         return [flat[int(self.offs[i]):int(self.offs[i]) + int(s)] for i, s in enumerate(self.sizes)]
 
     def algorithmic_bytes(self):
-        n, bt, nb = self.n_params * 4, self.buf_total * 4, self.nb
+        n, bt = self.n_params * 4, self.buf_total * 4
         words = 4 * sum(self.words)
         return {
-            "fused_ring": 2 * P * n,                       # read P x n, write P x n
-            "pack": P * n + P * bt,                        # read tensors, write buffers (gaps zeroed)
-            "thc_range": P * bt,                           # read P buffers
-            "thc_fused": P * bt + bt + P * words,          # read P buffers, write avg + wire vectors
-            "unpack": 2 * n,                               # THC average back into one tensor set
-            "nmse": n + bt + 2 * bt,                       # pack ring average, read both buffers
+            "fused_ring": 2 * P * n,                  # read P x n, write P x n
+            "pack": P * n + P * bt,                   # read tensors, write buffers (gaps zeroed); range on the way
+            "thc_fused": P * bt + bt + P * words,     # read P buffers, write avg + wire vectors
+            "unpack": 2 * n,                          # THC average back into one tensor set
+            "nmse": 2 * self.flat_len * 4,            # read both flat averages
         }
 
     def run(self, step_idx, events=None):
+        """events: dict stage -> (start, end) CUDA events, or None."""
         g, torch = self.g, self.torch
         seed = workloads.THC_SEED + step_idx
+        main = torch.cuda.current_stream()
+        overlap = self.schedule == "overlap"
+        s_thc = self.stream_t if overlap else main
+        s_ring = self.stream_r if overlap else main
 
-        def mark(i):
+        def mark(stage, k, stream):
             if events is not None:
-                events[i].record()
+                events[stage][k].record(stream)
 
         plan = g.gar_fusion_plan(self.sizes, self.dtype, CAPACITY, ALIGN)
-        mark(0)
-        g.gar_fused_allreduce(self.src, self.ring, plan, op=g.GAR_AVG, tables=self.tables)
-        mark(1)
-        for w in range(P):
-            for b in range(self.nb):
-                g.gar_fusion_pack(self.src_tab[w], plan, b, self.fusion[w][b])
-        mark(2)
-        for b in range(self.nb):
-            g.gar_thc_range(self.fusion_col[b], self.mM[b])
-        mark(3)
+        if overlap:
+            s_thc.wait_stream(main)
+            s_ring.wait_stream(main)
+        # THC path: pack every worker (range fused in), encode/aggregate/decode, unpack
+        mark("pack", 0, s_thc)
+        g.gar_fusion_pack_all(self.src, plan, self.fusion, self.mM, stream=s_thc, tables=self.pack_tables)
+        mark("pack", 1, s_thc)
+        if overlap:  # the ring (HBM-bound) runs while THC quantizes (ALU-bound)
+            s_ring.wait_stream(s_thc)
+        mark("thc_fused", 0, s_thc)
         for b in range(self.nb):
             g.gar_thc_allreduce_fused(self.fusion_col[b], B_THC, seed, self.mM[b], self.thc_avg[b],
-                                      self.packed_col[b])
-        mark(4)
+                                      self.packed_col[b], stream=s_thc)
+        mark("thc_fused", 1, s_thc)
+        mark("unpack", 0, s_thc)
         for b in range(self.nb):
-            g.gar_fusion_unpack(self.thc_avg[b], plan, b, self.thc_tab)
-        mark(5)
-        for b in range(self.nb):
-            g.gar_fusion_pack(self.ring0_tab, plan, b, self.ring_fb[b])
-            g.gar_nmse(self.ring_fb[b], self.thc_avg[b], self.nmse[b:b + 1], self.ws)
-        mark(6)
+            g.gar_fusion_unpack(self.thc_avg[b], plan, b, self.thc_tab, stream=s_thc)
+        mark("unpack", 1, s_thc)
+        # exact path: Tensor Fusion + ring all-reduce average, one pass
+        mark("fused_ring", 0, s_ring)
+        g.gar_fused_allreduce(self.src, self.ring, plan, op=g.GAR_AVG, tables=self.ring_tables, stream=s_ring)
+        mark("fused_ring", 1, s_ring)
+        if overlap:
+            main.wait_stream(s_thc)
+            main.wait_stream(s_ring)
+        mark("nmse", 0, main)
+        g.gar_nmse(self.ring_flat[0], self.thc_flat, self.nmse, self.ws, stream=main)
+        mark("nmse", 1, main)
 
 
-KERNEL_OF_STAGE = {"fused_ring": "ring_fold_kernel", "pack": "copy_jobs_kernel", "thc_range": "thc_range_kernel",
-                   "thc_fused": "thc_fused_kernel", "unpack": "copy_jobs_kernel",
-                   "nmse": "copy_jobs_kernel + nmse_partial_kernel + nmse_final_kernel"}
+KERNEL_OF_STAGE = {"fused_ring": "ring_fold_kernel", "pack": "pack_all_kernel", "thc_fused": "thc_fused_kernel",
+                   "unpack": "copy_jobs_kernel", "nmse": "nmse_partial_kernel + nmse_final_kernel"}
 PER_OF_STAGE = {
     "fused_ring": "all launches of one step's gar_fused_allreduce (3 launches, 300 tensors x 8 workers)",
-    "pack": "all launches of one step's 24 gar_fusion_pack calls (8 workers x 3 fusion buffers, one launch each)",
-    "thc_range": "all launches of one step's 3 gar_thc_range calls",
+    "pack": "all launches of one step's gar_fusion_pack_all (8 workers x 3 fusion buffers, range fused in)",
     "thc_fused": "all launches of one step's 3 gar_thc_allreduce_fused calls",
     "unpack": "all launches of one step's 3 gar_fusion_unpack calls",
-    "nmse": "one step's NMSE stage",
+    "nmse": "one step's gar_nmse over the flat averages",
 }
 # stage -> committed ncu summary holding its per-step DRAM traffic
-PROFILE_OF_STAGE = {"fused_ring": ("ring_fold_kernel_resnet_fusion", "ring.cu"),
-                    "pack": ("copy_jobs_kernel_resnet_fusion", "fusion.cu"),
-                    "thc_fused": ("thc_fused_kernel_resnet_fusion", "thc.cu")}
+PROFILE_OF_STAGE = {"fused_ring": ("ring_fold_kernel_resnet_fusion", ["ring.cu", "ring.cuh", "common.cuh"]),
+                    "pack": ("pack_all_kernel_resnet_fusion", ["fusion.cu", "ring.cuh", "common.cuh"]),
+                    "thc_fused": ("thc_fused_kernel_resnet_fusion", ["thc.cu", "common.cuh"])}
+
+
+def kernel_source_hash(files):
+    """sha256 over the kernel's source files (the hash an ncu summary records)."""
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "gradient_allreduce_homomorphic_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
 
 
 def _profile_traffic(stage):
@@ -234,18 +255,16 @@ def _profile_traffic(stage):
     the summary was taken on the current kernel source (else None)."""
     if stage not in PROFILE_OF_STAGE:
         return None
-    tag, src_name = PROFILE_OF_STAGE[stage]
+    tag, files = PROFILE_OF_STAGE[stage]
     path = os.path.join(ROOT, "profiles", f"{tag}.md")
-    src = os.path.join(ROOT, "gradient_allreduce_homomorphic_gb300", "csrc", src_name)
-    if not os.path.exists(path) or not os.path.exists(src):
+    if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_step:\s*([0-9]+)", text)
     h = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
     if not m or not h:
         return None
-    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return int(m.group(1)) if cur == h.group(1) else None
+    return int(m.group(1)) if kernel_source_hash(files) == h.group(1) else None
 
 
 def run_ours(args, rank, world, dist):
@@ -257,7 +276,7 @@ def run_ours(args, rank, world, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     g.load()
-    st = Step(torch, g, dev)
+    st = Step(torch, g, dev, schedule=args.schedule)
     nbytes = P * st.n_params * 4
 
     def barrier():
@@ -269,8 +288,8 @@ def run_ours(args, rank, world, dist):
     torch.cuda.synchronize()
 
     # ---- device-timed region: inputs resident in HBM
-    nst = len(st.stages)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    evs = [{s: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for s in st.stages}
+           for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -287,12 +306,31 @@ def run_ours(args, rank, world, dist):
     barrier()
     clk = clocks.stop()
     ms = start.elapsed_time(stop) / args.steps
-    stage_ms = {s: float(np.mean([evs[i][k].elapsed_time(evs[i][k + 1]) for i in range(args.steps)]))
-                for k, s in enumerate(st.stages)}
+    stage_ms = {s: float(np.mean([evs[i][s][0].elapsed_time(evs[i][s][1]) for i in range(args.steps)]))
+                for s in st.stages}
     if dist is not None:
         t = torch.tensor([ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
+    overlap_evs = evs if args.schedule == "overlap" else None
+
+    # ---- the same steps with every kernel alone on one stream: per-kernel
+    # times for the roofline (in the two-stream schedule the ring and THC
+    # kernels share HBM, so their individual durations stretch)
+    serial_stage_ms = stage_ms
+    if args.schedule == "overlap":
+        st.schedule = "serial"
+        for i in range(3):
+            st.run(20_000 + i)
+        sevs = [{s: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for s in st.stages}
+                for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            st.run(20_003 + i, sevs[i])
+        torch.cuda.synchronize()
+        serial_stage_ms = {s: float(np.mean([sevs[i][s][0].elapsed_time(sevs[i][s][1]) for i in range(args.steps)]))
+                           for s in st.stages}
+        st.schedule = "overlap"
 
     # ---- end to end: pinned host gradients in, both averages and the NMSE out
     host_in = [torch.empty(st.flat_len, dtype=torch.float32, pin_memory=True) for _ in range(P)]
@@ -300,7 +338,7 @@ def run_ours(args, rank, world, dist):
         host_in[w].copy_(st.flat[w])
     host_ring = torch.empty(st.flat_len, dtype=torch.float32, pin_memory=True)
     host_thc = torch.empty(st.flat_len, dtype=torch.float32, pin_memory=True)
-    host_nmse = torch.empty(st.nb, dtype=torch.float64, pin_memory=True)
+    host_nmse = torch.empty(1, dtype=torch.float64, pin_memory=True)
     e2e_steps = max(3, min(args.steps, 20))
 
     def e2e_step(i):
@@ -333,29 +371,48 @@ def run_ours(args, rank, world, dist):
         return None
     peak, peak_kind = _peaks()
     algo = st.algorithmic_bytes()
-    dom = max(stage_ms, key=lambda s: stage_ms[s])
-    achieved = algo[dom] / (stage_ms[dom] * 1e-3) / 1e9
+    dom = max(serial_stage_ms, key=lambda s: serial_stage_ms[s])
+    achieved = algo[dom] / (serial_stage_ms[dom] * 1e-3) / 1e9
     traffic = _profile_traffic(dom)
     value = world * nbytes / (ms * 1e-3) / 1e9
+    overlap_region = None
+    if overlap_evs is not None:
+        # ring and THC quantization share HBM: their combined bytes over the
+        # span from the ring's start to the later of the two ends
+        evs = overlap_evs
+        span = float(np.mean([max(evs[i]["fused_ring"][0].elapsed_time(evs[i]["fused_ring"][1]),
+                                  evs[i]["fused_ring"][0].elapsed_time(evs[i]["thc_fused"][1]))
+                              for i in range(args.steps)]))
+        both = algo["fused_ring"] + algo["thc_fused"]
+        overlap_region = {"stages": ["fused_ring", "thc_fused"], "ms": round(span, 4),
+                          "gbs": round(both / (span * 1e-3) / 1e9, 1),
+                          "frac": round(both / (span * 1e-3) / 1e9 / peak, 4)}
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded N(0,0.01) gradients drawn on the device)",
-        "config": _config(st.n_params, st.nb, parallelism=f"{world} independent replicas" if world > 1 else "single GPU"),
+        "config": _config(st.n_params, st.nb, parallelism=f"{world} independent replicas" if world > 1 else "single GPU",
+                          schedule=("two streams: ring all-reduce overlapped with THC quantization"
+                                    if args.schedule == "overlap" else "one stream, stages in sequence")),
         "elements_per_s": round(world * P * st.n_params / (ms * 1e-3), 1),
         "hbm_fraction_of_step": round(sum(algo.values()) / (ms * 1e-3) / 1e9 / peak, 4),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
-        "stage_gbs": {k: round(algo[k] / (stage_ms[k] * 1e-3) / 1e9, 1) for k in stage_ms},
+        "stage_ms_alone": {k: round(v, 4) for k, v in serial_stage_ms.items()},
+        "stage_gbs_alone": {k: round(algo[k] / (serial_stage_ms[k] * 1e-3) / 1e9, 1) for k in serial_stage_ms},
+        "overlap_region": overlap_region,
         "roofline": {"kernel": KERNEL_OF_STAGE[dom],
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-                     "per": PER_OF_STAGE[dom], "stage": dom},
+                     "per": PER_OF_STAGE[dom], "stage": dom,
+                     "timed": ("alone: the same steps run once more on one stream in this run, so the kernel "
+                               "does not share HBM with a concurrent one" if args.schedule == "overlap"
+                               else "in the timed steps")},
         "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": P * st.flat_len * 4,
-                "d2h_bytes_per_step": 2 * st.flat_len * 4 + 8 * st.nb},
+                "d2h_bytes_per_step": 2 * st.flat_len * 4 + 8},
         "gpu_launches": int(launches),
-        "nmse_thc_b4": [round(v, 6) for v in nmse_vals],
+        "nmse_thc_b4": round(nmse_vals[0], 6),
         "clocks": clk,
     }
     return out
@@ -452,6 +509,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--schedule", choices=["overlap", "serial"], default="overlap")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

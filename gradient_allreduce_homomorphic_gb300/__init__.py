@@ -49,6 +49,7 @@ _SIGNATURES = {
     "gar_fusion_pack": (C.c_int, [_pp, _vp, _vp, _i32, _i32, _vp, _i64, _vp]),
     "gar_fusion_unpack": (C.c_int, [_vp, _vp, _vp, _i32, _i32, _pp, _vp]),
     "gar_fused_allreduce": (C.c_int, [_pp, _pp, _i32, _vp, _vp, _i32, _vp, _i32, _i32, _vp]),
+    "gar_fusion_pack_all": (C.c_int, [_pp, _i32, _vp, _vp, _i32, _pp, _vp, _i32, _vp, _vp]),
     "gar_ring_allreduce_sim": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _vp]),
     "gar_ring_allreduce_sim_out": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _pp, _i32, _vp]),
     "gar_ring_allreduce_steps": (C.c_int, [_pp, _i32, _i64, _i32, C.POINTER(_i32), _vp, _vp]),
@@ -194,6 +195,24 @@ def gar_fusion_unpack(fusion_buf, plan: FusionPlan, buffer: int, dst, stream=Non
     ptrs = pointer_table(dst, allow_none=True).array
     _call("gar_fusion_unpack", _dev(fusion_buf), C.addressof(plan.segs), plan.dtype.ctypes.data, plan.count,
           buffer, ptrs, _stream(stream))
+
+
+def gar_fusion_pack_all(src, plan: FusionPlan, fusion_bufs, d_mM=None, stream=None, tables=None):
+    """Pack every worker's tensors into its fusion buffers in one pass.
+
+    src[w][i]: worker w's tensor i; fusion_bufs[w][b]: worker w's buffer b;
+    d_mM (optional, fp32 plans): [n_buffers, 2] per-buffer min/max output."""
+    P = len(src)
+    if tables is None:
+        tables = pack_all_tables(src, fusion_bufs)
+    s, f = tables
+    _call("gar_fusion_pack_all", s.array, P, C.addressof(plan.segs), plan.dtype.ctypes.data, plan.count, f.array,
+          plan.buf_numel.ctypes.data, plan.n_buffers, _dev(d_mM) if d_mM is not None else None, _stream(stream))
+
+
+def pack_all_tables(src, fusion_bufs):
+    """Host pointer tables for gar_fusion_pack_all (reuse them across steps)."""
+    return (PtrTable([t for row in src for t in row]), PtrTable([t for row in fusion_bufs for t in row]))
 
 
 def fused_pointer_tables(src, dst):

@@ -67,9 +67,10 @@ inline PhiloxKeys philox_keys(uint64_t seed) {
 __device__ __forceinline__ uint4 philox10(uint4 c, const PhiloxKeys &k) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint32_t a_lo = 0xD2511F53u * c.x, a_hi = __umulhi(0xD2511F53u, c.x);
-        const uint32_t b_lo = 0xCD9E8D57u * c.z, b_hi = __umulhi(0xCD9E8D57u, c.z);
-        c = make_uint4(b_hi ^ c.y ^ k.lo[r], b_lo, a_hi ^ c.w ^ k.hi[r], a_lo);
+        const uint64_t pa = static_cast<uint64_t>(c.x) * 0xD2511F53ull;
+        const uint64_t pb = static_cast<uint64_t>(c.z) * 0xCD9E8D57ull;
+        c = make_uint4(static_cast<uint32_t>(pb >> 32) ^ c.y ^ k.lo[r], static_cast<uint32_t>(pb),
+                       static_cast<uint32_t>(pa >> 32) ^ c.w ^ k.hi[r], static_cast<uint32_t>(pa));
     }
     return c;
 }

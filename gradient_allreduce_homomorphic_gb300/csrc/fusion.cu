@@ -159,6 +159,199 @@ class CopyBatch {
     CopyParams *p_;
 };
 
+// ------------------------------------------------- all workers, one pass
+// One row per tensor: P source pointers (the workers' copies of the tensor)
+// and P destination pointers (each worker's fusion buffer at the tensor's
+// offset).  Tile 0 of a row also zero-fills the row's alignment gap.  With
+// a range output every tile folds its values (and the gap zeros) into the
+// buffer's global [min, max], THC's preliminary round, while copying.
+struct PackRow {
+    int32_t buffer;
+    int32_t vec;   // every pointer of the row 16-byte aligned
+    int32_t gap;   // zero elements after the tensor, up to the next one's offset
+    int32_t pad;
+    int64_t numel;
+};
+
+constexpr int kPackPtrs = 1024, kPackRows = 256;
+struct PackAllParams {
+    int32_t P;
+    int32_t nrows;
+    int32_t pad0;
+    int32_t pad1;
+    float *mM;  // [n_buffers][2] or NULL
+    int64_t total_tiles;
+    int64_t tile_start[kPackRows + 1];
+    PackRow row[kPackRows];
+    const void *src[kPackPtrs];  // src[row * P + w]
+    void *dst[kPackPtrs];        // dst[row * P + w]
+};
+static_assert(sizeof(PackAllParams) <= 32000, "pack parameters exceed the launch limit");
+
+constexpr int kPackBatch = 8;  // worker vectors in flight per thread
+
+template <typename T>
+struct PackElem;
+template <>
+struct PackElem<float> {
+    static constexpr int kVec = 4;
+    __device__ static void range(const uint4 &r, float &lo, float &hi) {
+        const float a = __uint_as_float(r.x), b = __uint_as_float(r.y), c = __uint_as_float(r.z),
+                    d = __uint_as_float(r.w);
+        lo = fminf(lo, fminf(fminf(a, b), fminf(c, d)));
+        hi = fmaxf(hi, fmaxf(fmaxf(a, b), fmaxf(c, d)));
+    }
+};
+template <>
+struct PackElem<uint16_t> {
+    static constexpr int kVec = 8;
+    __device__ static void range(const uint4 &, float &, float &) {}
+};
+
+__device__ __forceinline__ void atomic_min_f(float *a, float v) {
+    if ((__float_as_uint(v) >> 31) == 0u) atomicMin(reinterpret_cast<int *>(a), __float_as_int(v));
+    else atomicMax(reinterpret_cast<unsigned int *>(a), __float_as_uint(v));
+}
+__device__ __forceinline__ void atomic_max_f(float *a, float v) {
+    if ((__float_as_uint(v) >> 31) == 0u) atomicMax(reinterpret_cast<int *>(a), __float_as_int(v));
+    else atomicMin(reinterpret_cast<unsigned int *>(a), __float_as_uint(v));
+}
+
+__global__ void pack_range_init(float *mM, int n) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        mM[2 * i] = __int_as_float(0x7F800000);       // +inf
+        mM[2 * i + 1] = __int_as_float(0xFF800000u);  // -inf
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) pack_all_kernel(const __grid_constant__ PackAllParams p) {
+    constexpr int V = PackElem<T>::kVec;
+    const bool want_range = p.mM != nullptr;
+    __shared__ float s_lo[kThreads / 32], s_hi[kThreads / 32];
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        int lo_i = 0, hi_i = p.nrows - 1;
+        while (lo_i < hi_i) {
+            const int mid = (lo_i + hi_i + 1) >> 1;
+            if (p.tile_start[mid] <= t) lo_i = mid;
+            else hi_i = mid - 1;
+        }
+        const PackRow r = p.row[lo_i];
+        const int64_t lt = t - p.tile_start[lo_i];
+        const void *const *src = p.src + static_cast<int64_t>(lo_i) * p.P;
+        void *const *dst = p.dst + static_cast<int64_t>(lo_i) * p.P;
+        float lo = __int_as_float(0x7F800000), hi = __int_as_float(0xFF800000u);
+        const int64_t nvec = r.vec ? r.numel / V : 0;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = lt * kTileUnits + u * kThreads + threadIdx.x;
+            if (i < nvec) {
+                for (int w0 = 0; w0 < p.P; w0 += kPackBatch) {
+                    uint4 v[kPackBatch];
+#pragma unroll
+                    for (int j = 0; j < kPackBatch; ++j)
+                        if (w0 + j < p.P) v[j] = ld16(static_cast<const T *>(src[w0 + j]) + i * V);
+#pragma unroll
+                    for (int j = 0; j < kPackBatch; ++j) {
+                        if (w0 + j < p.P) {
+                            st16(static_cast<T *>(dst[w0 + j]) + i * V, v[j]);
+                            if (want_range) PackElem<T>::range(v[j], lo, hi);
+                        }
+                    }
+                }
+            }
+        }
+        if (!r.vec) {  // unaligned row: element by element
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t e = lt * kTileUnits + u * kThreads + threadIdx.x;
+                if (e < r.numel) {
+                    for (int w = 0; w < p.P; ++w) {
+                        const T v = static_cast<const T *>(src[w])[e];
+                        static_cast<T *>(dst[w])[e] = v;
+                        if constexpr (sizeof(T) == 4) {
+                            lo = fminf(lo, v);
+                            hi = fmaxf(hi, v);
+                        }
+                    }
+                }
+            }
+        }
+        if (lt == 0) {  // vector tail of the tensor, then the zero gap after it
+            // (an unaligned row has copied every element above: no tail, the gap starts at numel)
+            const int64_t tail0 = r.vec ? nvec * V : r.numel;
+            const int64_t ntail = r.numel - tail0;
+            for (int64_t k = threadIdx.x; k < ntail + r.gap; k += kThreads) {
+                for (int w = 0; w < p.P; ++w) {
+                    T v;
+                    if (k < ntail) {
+                        v = static_cast<const T *>(src[w])[tail0 + k];
+                    } else {
+                        v = T{};
+                    }
+                    static_cast<T *>(dst[w])[tail0 + k] = v;
+                    if constexpr (sizeof(T) == 4) {
+                        lo = fminf(lo, static_cast<float>(v));
+                        hi = fmaxf(hi, static_cast<float>(v));
+                    }
+                }
+            }
+        }
+        if (want_range) {  // uniform branch: one pair of atomics per tile
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+                hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
+            }
+            const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+            __syncthreads();  // the previous tile's readers are done with s_lo/s_hi
+            if (lane == 0) {
+                s_lo[warp] = lo;
+                s_hi[warp] = hi;
+            }
+            __syncthreads();
+            if (warp == 0) {
+                lo = lane < kThreads / 32 ? s_lo[lane] : __int_as_float(0x7F800000);
+                hi = lane < kThreads / 32 ? s_hi[lane] : __int_as_float(0xFF800000u);
+#pragma unroll
+                for (int o = 4; o > 0; o >>= 1) {
+                    lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+                    hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
+                }
+                if (lane == 0) {
+                    if (lo == lo) atomic_min_f(p.mM + 2 * r.buffer, lo);
+                    if (hi == hi) atomic_max_f(p.mM + 2 * r.buffer + 1, hi);
+                }
+            }
+        }
+    }
+}
+
+template <typename T>
+int launch_pack_all(PackAllParams &p, cudaStream_t stream) {
+    constexpr int V = PackElem<T>::kVec;
+    int64_t tiles = 0;
+    for (int i = 0; i < p.nrows; ++i) {
+        p.tile_start[i] = tiles;
+        const int64_t units = p.row[i].vec ? p.row[i].numel / V : p.row[i].numel;
+        const int64_t t = ceil_div(units, kTileUnits);
+        tiles += t > 0 ? t : 1;
+    }
+    p.tile_start[p.nrows] = tiles;
+    p.total_tiles = tiles;
+    static int occ = 0;
+    if (occ == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pack_all_kernel<T>, kThreads, 0) != cudaSuccess || n <= 0)
+            n = 4;
+        occ = n;
+    }
+    int64_t grid = static_cast<int64_t>(sm_count()) * occ;
+    if (grid > tiles) grid = tiles;
+    pack_all_kernel<T><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+    return check_launch("pack_all_kernel");
+}
+
 // Checks shared by pack / unpack: the buffer's tensors, their common dtype.
 int buffer_members(const gar_seg *segs, const int32_t *dtype, int32_t count, int32_t buffer,
                    std::vector<int> &members, int &es) {
@@ -265,6 +458,119 @@ extern "C" int gar_fusion_unpack(const void *fusion_buf, const gar_seg *segs, co
     for (int i : members)
         if ((rc = batch.add(base + segs[i].offset * es, dst[i], segs[i].numel * es))) return rc;
     return batch.flush();
+}
+
+extern "C" int gar_fusion_pack_all(const void *const *src, int32_t P, const gar_seg *segs, const int32_t *dtype,
+                                   int32_t count, void *const *fusion_bufs, const int64_t *buf_numel,
+                                   int32_t n_buffers, float *d_mM, gar_stream_t stream_) {
+    if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
+    if (count < 0 || n_buffers < 0) return fail(GAR_EINVAL, "count or n_buffers < 0");
+    if (count > 0 && (!src || !segs || !dtype || !fusion_bufs || !buf_numel)) return fail(GAR_EINVAL, "NULL argument");
+    if (d_mM && !aligned(d_mM, 4)) return fail(GAR_EALIGN, "d_mM not 4-byte aligned");
+    std::vector<int32_t> buf_dt(n_buffers, -1);
+    std::vector<int> last(n_buffers, -1);  // last tensor of each buffer so far
+    std::vector<int> first(n_buffers, -1);
+    for (int i = 0; i < count; ++i) {
+        const gar_seg &s = segs[i];
+        const int es = elem_bytes(dtype[i]);
+        if (es < 0) return fail(GAR_EDTYPE, "tensor %d has unknown dtype %d", i, dtype[i]);
+        if (s.buffer < 0 || s.buffer >= n_buffers) return fail(GAR_EINVAL, "tensor %d has buffer id %d", i, s.buffer);
+        if (buf_dt[s.buffer] >= 0 && buf_dt[s.buffer] != dtype[i]) return fail(GAR_EDTYPE, "buffer %d mixes dtypes", s.buffer);
+        if (d_mM && dtype[i] != GAR_F32) return fail(GAR_EDTYPE, "a range is only computed over fp32 buffers");
+        buf_dt[s.buffer] = dtype[i];
+        const int prev = last[s.buffer];
+        const int64_t cursor = prev < 0 ? 0 : segs[prev].offset + segs[prev].numel;
+        if (s.numel < 0 || s.offset < cursor || s.offset + s.numel > buf_numel[s.buffer])
+            return fail(GAR_EINVAL, "tensor %d does not lie in order inside buffer %d", i, s.buffer);
+        if (first[s.buffer] < 0) first[s.buffer] = i;
+        last[s.buffer] = i;
+        for (int w = 0; w < P; ++w) {
+            const void *sp = src[static_cast<int64_t>(w) * count + i];
+            if (s.numel > 0 && !sp) return fail(GAR_EINVAL, "worker %d tensor %d pointer is NULL", w, i);
+            if (!aligned(sp, es)) return fail(GAR_EALIGN, "worker %d tensor %d not aligned", w, i);
+        }
+    }
+    for (int b = 0; b < n_buffers; ++b) {
+        if (buf_numel[b] < 0) return fail(GAR_EINVAL, "buffer %d has negative length", b);
+        const int es = buf_dt[b] >= 0 ? elem_bytes(buf_dt[b]) : 4;
+        for (int w = 0; w < P; ++w) {
+            void *fb = fusion_bufs[static_cast<int64_t>(w) * n_buffers + b];
+            if (buf_numel[b] > 0 && !fb) return fail(GAR_EINVAL, "worker %d fusion buffer %d is NULL", w, b);
+            if (!aligned(fb, es)) return fail(GAR_EALIGN, "worker %d fusion buffer %d not aligned", w, b);
+        }
+    }
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (d_mM && n_buffers > 0) {
+        pack_range_init<<<1, 256, 0, stream>>>(d_mM, n_buffers);
+        const int rc = check_launch("pack_range_init");
+        if (rc) return rc;
+    }
+    PackAllParams *p = new PackAllParams;
+    int rc = GAR_OK;
+    for (int pass_dtype = 0; pass_dtype < 2 && rc == GAR_OK; ++pass_dtype) {
+        std::memset(p, 0, sizeof(PackAllParams));
+        p->P = P;
+        p->mM = d_mM;
+        const int es = elem_bytes(pass_dtype);
+        auto flush = [&]() -> int {
+            if (p->nrows == 0) return GAR_OK;
+            const int r = pass_dtype == GAR_F32 ? launch_pack_all<float>(*p, stream) : launch_pack_all<uint16_t>(*p, stream);
+            p->nrows = 0;
+            return r;
+        };
+        auto add_row = [&](int buffer, int64_t dst_elem, int64_t numel, int64_t gap, int tensor) -> int {
+            if ((p->nrows + 1) * P > kPackPtrs || p->nrows + 1 > kPackRows) {
+                const int r = flush();
+                if (r) return r;
+            }
+            PackRow &row = p->row[p->nrows];
+            row.buffer = buffer;
+            row.numel = numel;
+            row.gap = static_cast<int32_t>(gap);
+            row.pad = 0;
+            bool vec = true;
+            for (int w = 0; w < P; ++w) {
+                const void *sp = tensor >= 0 ? src[static_cast<int64_t>(w) * count + tensor] : nullptr;
+                unsigned char *fb = static_cast<unsigned char *>(fusion_bufs[static_cast<int64_t>(w) * n_buffers + buffer]);
+                void *dp = fb + dst_elem * es;
+                vec = vec && aligned(sp, 16) && aligned(dp, 16);
+                p->src[p->nrows * P + w] = sp;
+                p->dst[p->nrows * P + w] = dp;
+            }
+            row.vec = vec ? 1 : 0;
+            ++p->nrows;
+            return GAR_OK;
+        };
+        for (int b = 0; b < n_buffers && rc == GAR_OK; ++b) {
+            if (buf_dt[b] != pass_dtype && !(buf_dt[b] < 0 && pass_dtype == GAR_F32)) continue;
+            const int f = first[b];
+            const int64_t lead = f < 0 ? buf_numel[b] : segs[f].offset;
+            if (lead > 0) {  // zeros before the buffer's first tensor (none in plans from gar_fusion_plan)
+                for (int64_t z = 0; z < lead && rc == GAR_OK; z += (1 << 30))
+                    rc = add_row(b, z, 0, lead - z < (1 << 30) ? lead - z : (1 << 30), -1);
+            }
+        }
+        for (int i = 0; i < count && rc == GAR_OK; ++i) {
+            if (dtype[i] != pass_dtype) continue;
+            const gar_seg &s = segs[i];
+            // the gap runs to the next tensor of the same buffer, or to the buffer's end
+            int64_t next = buf_numel[s.buffer];
+            for (int j = i + 1; j < count; ++j)
+                if (segs[j].buffer == s.buffer) {
+                    next = segs[j].offset;
+                    break;
+                }
+            const int64_t gap = next - (s.offset + s.numel);
+            if (gap >= (1 << 30)) {
+                rc = fail(GAR_EINVAL, "gap after tensor %d too large", i);
+                break;
+            }
+            rc = add_row(s.buffer, s.offset, s.numel, gap, i);
+        }
+        if (rc == GAR_OK) rc = flush();
+    }
+    delete p;
+    return rc;
 }
 
 extern "C" int gar_fused_allreduce(const void *const *src, void *const *dst, int32_t P, const gar_seg *segs,

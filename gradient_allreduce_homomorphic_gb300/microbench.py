@@ -5,7 +5,8 @@
 
 Cases: ring (in-place ring all-reduce of P buffers), ring_out (reduce to one
 output), fused (plan-driven all-reduce of the 300-tensor ResNet-like model),
-pack, unpack, thc_range, thc_encode, thc_aggregate, thc_decode, thc_fused,
+pack, unpack (per worker and buffer), pack_all, pack_all_range (every worker
+in one call, with THC's range fused in), thc_range, thc_encode, thc_aggregate, thc_decode, thc_fused,
 thc_fused_packed, nmse.  Inputs are seeded N(0, 1) draws made on the device;
 every size is chosen by the caller, so a case can be kept small enough for a
 profiler capture.  Prints one JSON line: time per call (CUDA events on the
@@ -61,7 +62,7 @@ def main(argv=None):
             t, o = g.pointer_table(x), g.pointer_table(out)
             fn = lambda: g.gar_ring_allreduce_sim_out(t, o)  # noqa: E731
             nbytes = P * N * es + N * es
-    elif a.case in ("fused", "pack", "unpack"):
+    elif a.case in ("fused", "pack", "unpack", "pack_all", "pack_all_range"):
         sizes = workloads.resnet_fusion_sizes()
         dt = np.zeros(sizes.size, np.int32)
         plan = g.gar_fusion_plan(sizes, dt, 64 << 20, 16)
@@ -72,6 +73,12 @@ def main(argv=None):
             tables = g.fused_pointer_tables(src, src)
             fn = lambda: g.gar_fused_allreduce(src, src, plan, tables=tables)  # noqa: E731
             nbytes = 2 * P * n * 4
+        elif a.case.startswith("pack_all"):
+            fbs = [[torch.empty(int(k), device=dev) for k in plan.buf_numel] for _ in range(P)]
+            mM = torch.empty((plan.n_buffers, 2), device=dev) if a.case == "pack_all_range" else None
+            tables = g.pack_all_tables(src, fbs)
+            fn = lambda: g.gar_fusion_pack_all(src, plan, fbs, mM, tables=tables)  # noqa: E731
+            nbytes = P * (n + int(plan.buf_numel.sum())) * 4
         else:
             fbs = [[torch.empty(int(k), device=dev) for k in plan.buf_numel] for _ in range(P)]
             tabs = [g.pointer_table(src[w]) for w in range(P)]

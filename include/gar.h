@@ -136,6 +136,24 @@ int gar_fusion_pack(const void *const *src, const gar_seg *segs, const int32_t *
 int gar_fusion_unpack(const void *fusion_buf, const gar_seg *segs, const int32_t *dtype,
                       int32_t count, int32_t buffer, void *const *dst, gar_stream_t stream);
 
+/* gar_fusion_pack_all -- step 3 for every worker and every fusion buffer in
+ * one pass (the same bytes as P * n_buffers gar_fusion_pack calls, in a
+ * handful of launches).  Optionally also THC's preliminary round ([T] section
+ * 4, Algorithm 1): d_mM[2b], d_mM[2b+1] = min and max over all workers'
+ * fusion buffer b, its zero padding included -- the same values
+ * gar_thc_range gives on the packed buffers -- computed while copying.
+ *   src[P * count]          host array: src[w * count + i] = worker w's tensor i
+ *   segs, dtype, count      the plan and per-tensor dtypes
+ *   fusion_bufs[P * n_buffers]  host array: fusion_bufs[w * n_buffers + b] =
+ *                           worker w's buffer b (device, buf_numel[b] elements)
+ *   d_mM                    device, 2 * n_buffers floats, or NULL (no range);
+ *                           fp32 plans only
+ * Errors: GAR_EINVAL, GAR_EDTYPE (mixed dtypes in a buffer, or a range asked
+ *         of bf16 tensors), GAR_EALIGN, GAR_ECUDA. */
+int gar_fusion_pack_all(const void *const *src, int32_t P, const gar_seg *segs, const int32_t *dtype,
+                        int32_t count, void *const *fusion_bufs, const int64_t *buf_numel,
+                        int32_t n_buffers, float *d_mM, gar_stream_t stream);
+
 /* gar_fused_allreduce -- steps 3-5 in one pass: for every fusion buffer of
  * the plan, the ring all-reduce (as gar_ring_allreduce_sim, over the
  * buffer's buf_numel elements with its chunking) is applied, reading the

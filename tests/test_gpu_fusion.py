@@ -202,3 +202,62 @@ def test_vgg_fusion_full_size_sampled(env):
             assert torch.equal(src[w][i], src[0][i])
     del src
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("trial", range(8))
+@pytest.mark.parametrize("P", [1, 3, 8])
+def test_pack_all(env, trial, P):
+    # every worker, every buffer in one pass: the same bytes as per-worker packs;
+    # with a range, the min/max of the packed buffers (padding zeros included)
+    torch, g = env
+    mixed = trial % 4 == 3
+    sizes, dtype, host32 = _random_plan_inputs(trial, P, mixed=mixed)
+    host = [[_as_dtype(x, int(d), torch) for x, d in zip(row, dtype)] for row in host32]
+    cap, align = 16 << 10, (16 if trial % 2 == 0 else 4)
+    plan = g.gar_fusion_plan(sizes, dtype, cap, align)
+    sb, so, bn = oracle.fusion_plan(sizes, dtype, cap, align)
+    src = [[to_dev(h, torch) for h in row] for row in host]
+    fbs = []
+    for w in range(P):
+        row = []
+        for b in range(len(bn)):
+            members = [i for i in range(len(sizes)) if sb[i] == b]
+            tdt = torch.bfloat16 if (members and dtype[members[0]] == 1) else torch.float32
+            row.append(torch.full((int(bn[b]),), 9.0, dtype=tdt, device="cuda"))
+        fbs.append(row)
+    want_range = not mixed
+    mM = torch.empty((len(bn), 2), dtype=torch.float32, device="cuda") if want_range else None
+    g.gar_fusion_pack_all(src, plan, fbs, mM)
+    for b in range(len(bn)):
+        packed = [oracle.fusion_pack(host[w], sb, so, b, bn[b]) for w in range(P)]
+        for w in range(P):
+            same_bits(to_host(fbs[w][b]), packed[w])
+        if want_range and bn[b] > 0:
+            m, M = oracle.thc_range(packed)
+            assert to_host(mM[b]).tolist() == [m, M]
+
+
+def test_pack_all_unaligned_and_leading_gap(env):
+    torch, g = env
+    P = 3
+    sizes = np.array([5, 17, 0, 40], np.int64)
+    dtype = np.zeros(4, np.int32)
+    plan = g.gar_fusion_plan(sizes, dtype, 1 << 20, 16)
+    # a hand-made plan: the first tensor starts at offset 3 (zeros before it)
+    for s, off in zip(plan.segs, (3, 12, 32, 32)):
+        s.offset = off
+    plan.buf_numel[0] = 75
+    host = [[np.random.default_rng([96, w, i]).standard_normal(int(k)).astype(np.float32) for i, k in enumerate(sizes)]
+            for w in range(P)]
+    bases = [[to_dev(np.concatenate([[1.0], h]).astype(np.float32), torch) for h in row] for row in host]
+    src = [[b[1:] for b in row] for row in bases]  # 4-byte aligned views
+    fbs = [[torch.full((75,), 5.0, device="cuda")] for _ in range(P)]
+    mM = torch.empty((1, 2), device="cuda")
+    g.gar_fusion_pack_all(src, plan, fbs, mM)
+    for w in range(P):
+        ref = np.zeros(75, np.float32)
+        for k, off in zip(range(4), (3, 12, 32, 32)):
+            ref[off:off + sizes[k]] = host[w][k]
+        same_bits(to_host(fbs[w][0]), ref)
+    allv = np.concatenate([np.concatenate(r) for r in host] + [np.zeros(1, np.float32)])
+    assert to_host(mM[0]).tolist() == [allv.min(), allv.max()]
