@@ -171,6 +171,19 @@ class FusionPlan:
     def offsets(self) -> np.ndarray:
         return np.array([s.offset for s in self.segs], np.int64)
 
+    def subplan(self, first: int, count: int) -> "FusionPlan":
+        """The plan restricted to tensors first .. first+count-1 (a view of the
+        same segments; buffer ids and buffer lengths unchanged)."""
+        segs = (gar_seg * max(count, 1)).from_address(C.addressof(self.segs) + first * C.sizeof(gar_seg))
+        sub = FusionPlan(segs, self.dtype[first:first + count].copy(), self.buf_numel)
+        sub._parent = self  # keep the segment storage alive
+        return sub
+
+    def buffer_tensors(self, buffer: int):
+        """(first, count) of the tensors of one buffer (contiguous in plan order)."""
+        ids = np.nonzero(self.buffers() == buffer)[0]
+        return (int(ids[0]), int(ids.size)) if ids.size else (0, 0)
+
 
 def gar_fusion_plan(numel, dtype, capacity_bytes: int = 64 << 20, align_bytes: int = 16) -> FusionPlan:
     numel = np.ascontiguousarray(numel, np.int64)
@@ -202,10 +215,10 @@ def gar_fusion_pack_all(src, plan: FusionPlan, fusion_bufs, d_mM=None, stream=No
 
     src[w][i]: worker w's tensor i; fusion_bufs[w][b]: worker w's buffer b;
     d_mM (optional, fp32 plans): [n_buffers, 2] per-buffer min/max output."""
-    P = len(src)
     if tables is None:
         tables = pack_all_tables(src, fusion_bufs)
     s, f = tables
+    P = len(s) // max(plan.count, 1)
     _call("gar_fusion_pack_all", s.array, P, C.addressof(plan.segs), plan.dtype.ctypes.data, plan.count, f.array,
           plan.buf_numel.ctypes.data, plan.n_buffers, _dev(d_mM) if d_mM is not None else None, _stream(stream))
 

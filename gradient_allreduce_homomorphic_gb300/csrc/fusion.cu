@@ -217,10 +217,16 @@ __device__ __forceinline__ void atomic_max_f(float *a, float v) {
     else atomicMin(reinterpret_cast<unsigned int *>(a), __float_as_uint(v));
 }
 
-__global__ void pack_range_init(float *mM, int n) {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        mM[2 * i] = __int_as_float(0x7F800000);       // +inf
-        mM[2 * i + 1] = __int_as_float(0xFF800000u);  // -inf
+struct RangeInitParams {
+    float *mM;
+    int32_t n;
+    int32_t ids[255];  // buffers whose range entries are reset
+};
+
+__global__ void pack_range_init(const __grid_constant__ RangeInitParams p) {
+    for (int i = threadIdx.x; i < p.n; i += blockDim.x) {
+        p.mM[2 * p.ids[i]] = __int_as_float(0x7F800000);       // +inf
+        p.mM[2 * p.ids[i] + 1] = __int_as_float(0xFF800000u);  // -inf
     }
 }
 
@@ -500,10 +506,20 @@ extern "C" int gar_fusion_pack_all(const void *const *src, int32_t P, const gar_
         }
     }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    if (d_mM && n_buffers > 0) {
-        pack_range_init<<<1, 256, 0, stream>>>(d_mM, n_buffers);
-        const int rc = check_launch("pack_range_init");
-        if (rc) return rc;
+    if (d_mM) {  // reset the range entries of the buffers this call packs
+        RangeInitParams ip;
+        std::memset(&ip, 0, sizeof(ip));
+        ip.mM = d_mM;
+        for (int b = 0; b <= n_buffers; ++b) {
+            const bool last = b == n_buffers;
+            if (!last && first[b] >= 0) ip.ids[ip.n++] = b;
+            if (ip.n > 0 && (last || ip.n == 255)) {
+                pack_range_init<<<1, 256, 0, stream>>>(ip);
+                const int rc = check_launch("pack_range_init");
+                if (rc) return rc;
+                ip.n = 0;
+            }
+        }
     }
     PackAllParams *p = new PackAllParams;
     int rc = GAR_OK;
@@ -542,9 +558,11 @@ extern "C" int gar_fusion_pack_all(const void *const *src, int32_t P, const gar_
             return GAR_OK;
         };
         for (int b = 0; b < n_buffers && rc == GAR_OK; ++b) {
-            if (buf_dt[b] != pass_dtype && !(buf_dt[b] < 0 && pass_dtype == GAR_F32)) continue;
+            // buffers that none of the given tensors belong to are left untouched,
+            // so a caller can pack one buffer at a time with a slice of the plan
+            if (buf_dt[b] != pass_dtype || first[b] < 0) continue;
             const int f = first[b];
-            const int64_t lead = f < 0 ? buf_numel[b] : segs[f].offset;
+            const int64_t lead = segs[f].offset;
             if (lead > 0) {  // zeros before the buffer's first tensor (none in plans from gar_fusion_plan)
                 for (int64_t z = 0; z < lead && rc == GAR_OK; z += (1 << 30))
                     rc = add_row(b, z, 0, lead - z < (1 << 30) ? lead - z : (1 << 30), -1);

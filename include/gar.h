@@ -148,6 +148,9 @@ int gar_fusion_unpack(const void *fusion_buf, const gar_seg *segs, const int32_t
  *                           worker w's buffer b (device, buf_numel[b] elements)
  *   d_mM                    device, 2 * n_buffers floats, or NULL (no range);
  *                           fp32 plans only
+ * Only buffers that at least one of the `count` tensors belongs to are
+ * written (their range entries too), so a slice of a plan (e.g. one buffer's
+ * tensors) packs just those buffers.
  * Errors: GAR_EINVAL, GAR_EDTYPE (mixed dtypes in a buffer, or a range asked
  *         of bf16 tensors), GAR_EALIGN, GAR_ECUDA. */
 int gar_fusion_pack_all(const void *const *src, int32_t P, const gar_seg *segs, const int32_t *dtype,

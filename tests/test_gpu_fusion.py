@@ -261,3 +261,43 @@ def test_pack_all_unaligned_and_leading_gap(env):
         same_bits(to_host(fbs[w][0]), ref)
     allv = np.concatenate([np.concatenate(r) for r in host] + [np.zeros(1, np.float32)])
     assert to_host(mM[0]).tolist() == [allv.min(), allv.max()]
+
+
+def test_plan_slices(env):
+    # a slice of the plan (one buffer's tensors) packs, ranges and reduces only
+    # that buffer; every other buffer and range entry is left untouched
+    torch, g = env
+    P = 4
+    sizes, dtype, host = _random_plan_inputs(5, P, mixed=False)
+    plan = g.gar_fusion_plan(sizes, dtype, 16 << 10, 16)
+    sb, so, bn = oracle.fusion_plan(sizes, dtype, 16 << 10, 16)
+    assert plan.n_buffers >= 2
+    src = [[to_dev(h, torch) for h in row] for row in host]
+    fbs = [[torch.full((int(k),), 3.0, device="cuda") for k in bn] for _ in range(P)]
+    mM = torch.full((len(bn), 2), 7.0, device="cuda")
+    b = 1
+    first, cnt = plan.buffer_tensors(b)
+    assert list(range(first, first + cnt)) == [i for i in range(len(sizes)) if sb[i] == b]
+    sub = plan.subplan(first, cnt)
+    g.gar_fusion_pack_all([row[first:first + cnt] for row in src], sub, fbs, mM)
+    packed = [oracle.fusion_pack(host[w], sb, so, b, bn[b]) for w in range(P)]
+    m, M = oracle.thc_range(packed)
+    assert to_host(mM[b]).tolist() == [m, M]
+    for bb in range(len(bn)):
+        if bb != b:
+            assert np.all(to_host(mM[bb]) == 7.0)
+        for w in range(P):
+            if bb == b:
+                same_bits(to_host(fbs[w][bb]), packed[w])
+            else:
+                assert np.all(to_host(fbs[w][bb]) == 3.0)
+    # the fused all-reduce of the slice touches only that buffer's tensors
+    dst = [[torch.full_like(t, 5.0) for t in row] for row in src]
+    g.gar_fused_allreduce([row[first:first + cnt] for row in src], [row[first:first + cnt] for row in dst], sub)
+    ref = _oracle_fused(host, sizes, dtype, sb, so, bn, oracle.AVG)
+    for w in range(P):
+        for i in range(len(sizes)):
+            if first <= i < first + cnt:
+                same_bits(to_host(dst[w][i]), ref[w][i])
+            else:
+                assert np.all(to_host(dst[w][i]) == 5.0)
