@@ -78,6 +78,14 @@ def _load():
                 "oracle_thc_aggregate": (C.c_int, [pp, C.c_int, i64, C.c_int, vp]),
                 "oracle_thc_decode": (C.c_int, [vp, i64, C.c_float, C.c_float, C.c_int, C.c_int, vp]),
                 "oracle_thc_allreduce": (C.c_int, [pp, C.c_int, i64, C.c_int, u64, C.c_float, C.c_float, vp, pp]),
+                "oracle_nuhc_check_table": (C.c_int, [vp, C.c_int, C.c_int]),
+                "oracle_nuhc_position": (C.c_float, [C.c_float, C.c_float, C.c_float, C.c_int]),
+                "oracle_nuhc_index": (u32, [C.c_float, C.c_float, C.c_float, C.c_int, C.c_int, vp, u64, C.c_int,
+                                            i64]),
+                "oracle_nuhc_encode": (C.c_int, [vp, i64, C.c_float, C.c_float, C.c_int, C.c_int, vp, u64,
+                                                 C.c_int, vp]),
+                "oracle_nuhc_aggregate": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, vp]),
+                "oracle_nuhc_decode": (C.c_int, [vp, i64, C.c_float, C.c_float, C.c_int, C.c_int, vp]),
                 "oracle_nmse": (C.c_double, [vp, vp, i64]),
                 "oracle_nmse_f64": (C.c_double, [vp, vp, i64]),
             }
@@ -308,6 +316,54 @@ def thc_allreduce(xs, b: int, seed: int, m=None, M=None, want_packed: bool = Fal
     if want_packed:
         return avg, [pk[:thc_words(n, b)] for pk in packed]
     return avg
+
+
+# ----------------------------------------------------- non-uniform THC
+def _table(table):
+    return np.ascontiguousarray(table, np.uint16)
+
+
+def nuhc_table_ok(table, b: int, g: int) -> bool:
+    return _load().oracle_nuhc_check_table(_ptr(_table(table)), b, g) == 0
+
+
+def nuhc_position(x, m, M, g: int) -> np.float32:
+    return np.float32(_load().oracle_nuhc_position(float(x), float(m), float(M), g))
+
+
+def nuhc_index(x, m, M, b, g, table, seed, worker, e) -> int:
+    return int(_load().oracle_nuhc_index(float(np.float32(x)), float(m), float(M), b, g, _ptr(_table(table)), seed,
+                                         worker, e))
+
+
+def nuhc_encode(x, m, M, b: int, g: int, table, seed: int, worker: int) -> np.ndarray:
+    out = np.empty(max(thc_words(x.size, b), 1), np.uint32)
+    _check(_load().oracle_nuhc_encode(_ptr(x), x.size, float(m), float(M), b, g, _ptr(_table(table)), seed, worker,
+                                      _ptr(out)), "nuhc_encode")
+    return out[:thc_words(x.size, b)]
+
+
+def nuhc_aggregate(packed_list, n: int, b: int, table) -> np.ndarray:
+    out = np.empty(n, np.uint16)
+    _check(_load().oracle_nuhc_aggregate(_ptrs(packed_list), len(packed_list), n, b, _ptr(_table(table)),
+                                         _ptr(out)), "nuhc_aggregate")
+    return out
+
+
+def nuhc_decode(sums, m, M, g: int, p: int) -> np.ndarray:
+    sums = np.ascontiguousarray(sums, np.uint16)
+    out = np.empty(sums.size, np.float64)
+    _check(_load().oracle_nuhc_decode(_ptr(sums), sums.size, float(m), float(M), g, p, _ptr(out)), "nuhc_decode")
+    return out
+
+
+def nuhc_allreduce(xs, b: int, g: int, table, seed: int, m=None, M=None, want_packed: bool = False):
+    """Non-uniform THC round: encode every worker, look up and sum, decode."""
+    if m is None or M is None:
+        m, M = thc_range(xs)
+    packed = [nuhc_encode(x, m, M, b, g, table, seed, w) for w, x in enumerate(xs)]
+    avg = nuhc_decode(nuhc_aggregate(packed, xs[0].size, b, table), m, M, g, len(xs))
+    return (avg, packed) if want_packed else avg
 
 
 def nmse(x, x_hat) -> float:

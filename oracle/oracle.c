@@ -473,6 +473,91 @@ int oracle_thc_allreduce(const float *const *x, int p, int64_t n, int b, uint64_
 }
 
 /* ===================================================================== */
+/* Non-uniform THC [T] section 5, Algorithm 2                             */
+/* ===================================================================== */
+/* With granularity g >= 2^b - 1 the grid is m + k (M - m) / g, k = 0..g,
+ * but a worker may only send the 2^b grid points whose k is a table value
+ * T[z].  It rounds stochastically between the two neighbouring allowed
+ * points (unbiased), sends the table index z, the PS looks each index up in
+ * T and sums the looked-up values, and each worker divides that sum by the
+ * number of workers and maps it back: avg = m + (Y / p) (M - m) / g.  With
+ * g = 2^b - 1 and T the identity this is exactly uniform THC.            */
+int oracle_nuhc_check_table(const uint16_t *table, int b, int g) {
+    if (!valid_bits(b)) return -1;
+    int L = (1 << b) - 1;
+    if (g < L || table[0] != 0 || table[L] != g) return -1;
+    for (int z = 0; z < L; ++z)
+        if (table[z + 1] <= table[z]) return -1;
+    return 0;
+}
+
+float oracle_nuhc_position(float x, float m, float M, int g) {
+    const float G = (float)g;
+    if (M == m) return 0.0f;
+    float range = M - m;
+    float scale = G / range;
+    float d = x - m;
+    float t = d * scale;
+    if (t < 0.0f) t = 0.0f;
+    if (t > G) t = G;
+    return t;
+}
+
+uint32_t oracle_nuhc_index(float x, float m, float M, int b, int g, const uint16_t *table,
+                           uint64_t seed, int worker, int64_t e) {
+    int L = (1 << b) - 1;
+    float t = oracle_nuhc_position(x, m, M, g);
+    /* the allowed grid points around t: table[z] <= t <= table[z + 1] */
+    int z = 0;
+    while (z < L - 1 && t >= (float)table[z + 1]) ++z;
+    float lo = (float)table[z], hi = (float)table[z + 1];
+    float p = (t - lo) / (hi - lo); /* probability of rounding up to table[z + 1] */
+    uint64_t q = (uint64_t)e >> 2;
+    uint32_t ctr[4] = {(uint32_t)q, (uint32_t)(q >> 32), (uint32_t)worker, 0u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t r[4];
+    oracle_philox4x32(ctr, key, 10, r);
+    float u = (float)(r[e & 3] & 0x7FFFFFu) / 8388608.0f;
+    return (uint32_t)z + (u < p ? 1u : 0u);
+}
+
+int oracle_nuhc_encode(const float *x, int64_t n, float m, float M, int b, int g,
+                       const uint16_t *table, uint64_t seed, int worker, uint32_t *packed) {
+    if (oracle_nuhc_check_table(table, b, g) != 0 || n < 0) return -1;
+    int per_word = 32 / b;
+    int64_t nwords = (n + per_word - 1) / per_word;
+    for (int64_t k = 0; k < nwords; ++k) packed[k] = 0u;
+    for (int64_t e = 0; e < n; ++e) {
+        uint32_t idx = oracle_nuhc_index(x[e], m, M, b, g, table, seed, worker, e);
+        packed[e / per_word] |= idx << ((e % per_word) * b);
+    }
+    return 0;
+}
+
+int oracle_nuhc_aggregate(const uint32_t *const *packed, int p, int64_t n, int b,
+                          const uint16_t *table, uint16_t *sums) {
+    if (!valid_bits(b) || n < 0 || p < 1) return -1;
+    int L = (1 << b) - 1;
+    if ((int64_t)p * table[L] > 65535) return -1;
+    int per_word = 32 / b;
+    uint32_t mask = (1u << b) - 1u;
+    for (int64_t e = 0; e < n; ++e) {
+        uint32_t s = 0;
+        for (int w = 0; w < p; ++w) s += table[(packed[w][e / per_word] >> ((e % per_word) * b)) & mask];
+        sums[e] = (uint16_t)s;
+    }
+    return 0;
+}
+
+int oracle_nuhc_decode(const uint16_t *sums, int64_t n, float m, float M, int g, int p,
+                       double *avg) {
+    if (g < 1 || n < 0 || p < 1) return -1;
+    double step = ((double)M - (double)m) / (double)g;
+    for (int64_t e = 0; e < n; ++e) avg[e] = (double)m + ((double)sums[e] / (double)p) * step;
+    return 0;
+}
+
+/* ===================================================================== */
 /* NMSE [T] section 2: ||x - x_hat||^2 / ||x||^2, accumulated in fp64.     */
 /* ===================================================================== */
 double oracle_nmse(const float *x, const float *x_hat, int64_t n) {

@@ -118,6 +118,22 @@ int oracle_thc_allreduce_samples(const float *vals, int p, const int64_t *e, int
 int oracle_thc_allreduce(const float *const *x, int p, int64_t n, int b, uint64_t seed,
                          float m, float M, double *avg, uint32_t *const *packed);
 
+/* ---------------- non-uniform THC [T] section 5, Algorithm 2 ---------------- */
+/* table[0..L], L = 2^b - 1: strictly increasing integers, table[0] = 0,
+ * table[L] = g.  Returns 0 if valid, -1 otherwise. */
+int oracle_nuhc_check_table(const uint16_t *table, int b, int g);
+/* fp32 position on the granularity-g grid: clamp((x - m) * (g / (M - m)), 0, g) */
+float oracle_nuhc_position(float x, float m, float M, int g);
+uint32_t oracle_nuhc_index(float x, float m, float M, int b, int g, const uint16_t *table,
+                           uint64_t seed, int worker, int64_t e);
+int oracle_nuhc_encode(const float *x, int64_t n, float m, float M, int b, int g,
+                       const uint16_t *table, uint64_t seed, int worker, uint32_t *packed);
+/* the PS: sums[e] = sum over workers of table[index] */
+int oracle_nuhc_aggregate(const uint32_t *const *packed, int p, int64_t n, int b,
+                          const uint16_t *table, uint16_t *sums);
+int oracle_nuhc_decode(const uint16_t *sums, int64_t n, float m, float M, int g, int p,
+                       double *avg);
+
 /* ---------------- NMSE [T] ---------------- */
 double oracle_nmse(const float *x, const float *x_hat, int64_t n);
 double oracle_nmse_f64(const double *x, const double *x_hat, int64_t n);
