@@ -59,6 +59,10 @@ _SIGNATURES = {
     "gar_thc_aggregate": (C.c_int, [_pp, _i32, _i64, _i32, _vp, _vp]),
     "gar_thc_decode": (C.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _vp]),
     "gar_thc_allreduce_fused": (C.c_int, [_pp, _i32, _i64, _i32, _u64, _vp, _vp, _pp, _vp]),
+    "gar_nuhc_encode": (C.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _u64, _i32, _vp, _vp]),
+    "gar_nuhc_aggregate": (C.c_int, [_pp, _i32, _i64, _i32, _vp, _vp, _vp]),
+    "gar_nuhc_decode": (C.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _vp]),
+    "gar_nuhc_allreduce_fused": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _vp, _u64, _vp, _vp, _pp, _vp]),
     "gar_nmse_workspace_bytes": (C.c_size_t, [_i64]),
     "gar_nmse": (C.c_int, [_vp, _vp, _i64, _vp, _vp, C.c_size_t, _vp]),
     "gar_nmse_noalloc": (C.c_int, [_vp, _vp, _i64, _vp, _vp]),
@@ -290,6 +294,35 @@ def gar_thc_allreduce_fused(x, b: int, seed: int, d_mM, avg, packed=None, stream
     t = pointer_table(x)
     pk = pointer_table(packed).array if packed is not None else None
     _call("gar_thc_allreduce_fused", t.array, len(t), t.numel, b, seed, _dev(d_mM), _dev(avg), pk,
+          _stream(stream))
+
+
+# --------------------------------------------------------- non-uniform THC
+def _table(table):
+    t = np.ascontiguousarray(table, np.uint16)
+    return t, t.ctypes.data
+
+
+def gar_nuhc_encode(x, d_mM, b: int, g: int, table, seed: int, worker: int, packed, stream=None):
+    t, tp = _table(table)
+    _call("gar_nuhc_encode", _dev(x), x.numel(), _dev(d_mM), b, g, tp, seed, worker, _dev(packed), _stream(stream))
+
+
+def gar_nuhc_aggregate(packed, N: int, b: int, table, sums, stream=None):
+    t, tp = _table(table)
+    pt = pointer_table(packed)
+    _call("gar_nuhc_aggregate", pt.array, len(pt), N, b, tp, _dev(sums), _stream(stream))
+
+
+def gar_nuhc_decode(sums, d_mM, g: int, P: int, avg, stream=None):
+    _call("gar_nuhc_decode", _dev(sums), sums.numel(), _dev(d_mM), g, P, _dev(avg), _stream(stream))
+
+
+def gar_nuhc_allreduce_fused(x, b: int, g: int, table, seed: int, d_mM, avg, packed=None, stream=None):
+    t, tp = _table(table)
+    xt = pointer_table(x)
+    pk = pointer_table(packed).array if packed is not None else None
+    _call("gar_nuhc_allreduce_fused", xt.array, len(xt), xt.numel, b, g, tp, seed, _dev(d_mM), _dev(avg), pk,
           _stream(stream))
 
 

@@ -7,7 +7,8 @@ Cases: ring (in-place ring all-reduce of P buffers), ring_out (reduce to one
 output), fused (plan-driven all-reduce of the 300-tensor ResNet-like model),
 pack, unpack (per worker and buffer), pack_all, pack_all_range (every worker
 in one call, with THC's range fused in), thc_range, thc_encode, thc_aggregate, thc_decode, thc_fused,
-thc_fused_packed, nmse.  Inputs are seeded N(0, 1) draws made on the device;
+thc_fused_packed, nuhc_fused, nuhc_fused_packed (non-uniform THC with a
+table on a granularity-g grid), nmse.  Inputs are seeded N(0, 1) draws made on the device;
 every size is chosen by the caller, so a case can be kept small enough for a
 profiler capture.  Prints one JSON line: time per call (CUDA events on the
 launching stream, after warm-up) and algorithmic GB/s.
@@ -40,6 +41,7 @@ def main(argv=None):
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--dtype", default="f32")
+    ap.add_argument("--g", type=int, default=0, help="granularity for the nuhc cases")
     a = ap.parse_args(argv)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -119,6 +121,20 @@ def main(argv=None):
         elif a.case == "thc_fused_packed":
             fn = lambda: g.gar_thc_allreduce_fused(xt, b, 5, mM, avg, pt)  # noqa: E731
             nbytes = P * N * 4 + N * 4 + P * words * 4
+        elif a.case in ("nuhc_fused", "nuhc_fused_packed"):
+            # granularity 36 for b = 4, 2(2^b - 1) + 1 otherwise; a table denser near the middle
+            L = (1 << b) - 1
+            gr = a.g if a.g else (36 if b == 4 else 2 * L + 1)
+            zz = np.arange(L + 1) / L * 2 - 1
+            tab = np.rint(gr / 2 + gr / 2 * np.sign(zz) * np.abs(zz) ** 1.6).astype(np.int64)
+            tab[0], tab[-1] = 0, gr
+            for i in range(1, L):
+                tab[i] = max(tab[i], tab[i - 1] + 1)
+            for i in range(L - 1, -1, -1):
+                tab[i] = min(tab[i], tab[i + 1] - 1)
+            pk = pt if a.case == "nuhc_fused_packed" else None
+            fn = lambda: g.gar_nuhc_allreduce_fused(xt, b, gr, tab, 5, mM, avg, pk)  # noqa: E731
+            nbytes = P * N * 4 + N * 4 + (P * words * 4 if pk is not None else 0)
         else:
             ws = torch.empty(g.gar_nmse_workspace_bytes(N) // 8, dtype=torch.float64, device=dev)
             out = torch.empty(1, dtype=torch.float64, device=dev)

@@ -273,6 +273,46 @@ int gar_thc_allreduce_fused(const float *const *x, int32_t P, int64_t N, int32_t
                             uint32_t *const *packed, gar_stream_t stream);
 
 /* ===================================================================== */
+/* Non-uniform THC [T] section 5, Algorithm 2                            */
+/* ===================================================================== */
+/* With granularity g (2^b - 1 <= g <= 16383) the grid is m + k (M - m)/g,
+ * k = 0..g, but a worker may only send the 2^b points whose k is a value of
+ * the lookup table T (host array of 2^b uint16, strictly increasing,
+ * T[0] = 0, T[2^b - 1] = g; the pages give no optimal tables, so T is the
+ * caller's).  Encoding in fp32, one rounding per operation:
+ *     t = clamp((x - m) * (g / (M - m)), 0, g)        (t = 0 when M == m)
+ *     z = the largest z <= 2^b - 2 with T[z] <= t
+ *     p = (t - T[z]) / (T[z + 1] - T[z])
+ *     index = z + (u < p ? 1 : 0)    (u: the Philox draw of uniform THC)
+ * Packing as for uniform THC.  The PS looks every index up in T and sums the
+ * table values; each worker decodes avg = fma(S, ((M - m)/g)/P, m).  With
+ * g = 2^b - 1 and T the identity this is exactly uniform THC. */
+
+/* gar_nuhc_encode -- one worker's indices (see gar_thc_encode for layout).
+ * Errors: GAR_EINVAL (bad b, g or table, NULL), GAR_EALIGN, GAR_ECUDA. */
+int gar_nuhc_encode(const float *x, int64_t N, const float *d_mM, int32_t b, int32_t g,
+                    const uint16_t *table, uint64_t seed, int32_t worker, uint32_t *packed,
+                    gar_stream_t stream);
+
+/* gar_nuhc_aggregate -- sums[e] = sum over workers of T[index] (uint16).
+ * g is taken as T[2^b - 1].  Errors: GAR_EINVAL, GAR_EOVERFLOW (P * g >
+ * 65535), GAR_EALIGN (sums must be 4-byte aligned), GAR_ECUDA. */
+int gar_nuhc_aggregate(const uint32_t *const *packed, int32_t P, int64_t N, int32_t b,
+                       const uint16_t *table, uint16_t *sums, gar_stream_t stream);
+
+/* gar_nuhc_decode -- avg[e] = fma(sums[e], ((M - m)/g)/P, m) in fp32.
+ * Errors: GAR_EINVAL, GAR_EALIGN, GAR_ECUDA. */
+int gar_nuhc_decode(const uint16_t *sums, int64_t N, const float *d_mM, int32_t g, int32_t P,
+                    float *avg, gar_stream_t stream);
+
+/* gar_nuhc_allreduce_fused -- encode every worker, look up, sum and decode in
+ * one pass; equal bit for bit to decode(aggregate(encode)).  packed may be
+ * NULL.  Errors: GAR_EINVAL, GAR_EOVERFLOW, GAR_EALIGN, GAR_ECUDA. */
+int gar_nuhc_allreduce_fused(const float *const *x, int32_t P, int64_t N, int32_t b, int32_t g,
+                             const uint16_t *table, uint64_t seed, const float *d_mM, float *avg,
+                             uint32_t *const *packed, gar_stream_t stream);
+
+/* ===================================================================== */
 /* NMSE [T] section 2: ||x - x_hat||^2 / ||x||^2                          */
 /* ===================================================================== */
 

@@ -1,0 +1,169 @@
+"""GPU parity of non-uniform THC (THC section 5, Algorithm 2) against the oracle.
+
+Indices and table-value sums bit-exact; decoded averages within
+1e-6 * max(|m|, |M|) of the oracle's fp64 decode; the fused kernel equals
+decode(aggregate(encode)) bit for bit; the identity table with g = 2^b - 1
+equals the uniform THC kernels bit for bit; the page's T2 example; a
+full-size sampled run with the page's simulation setting (b = 4, g = 36).
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from helpers import need_cuda, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    return need_cuda()
+
+
+def s_curve_table(b, g):
+    """A valid table (strictly increasing, 0 .. g) denser near the middle."""
+    L = (1 << b) - 1
+    z = np.arange(L + 1) / L * 2 - 1
+    raw = np.rint(g / 2 + g / 2 * np.sign(z) * np.abs(z) ** 1.6).astype(np.int64)
+    raw[0], raw[-1] = 0, g
+    for i in range(1, L):  # repair ties from rounding; the ends stay 0 and g
+        raw[i] = max(raw[i], raw[i - 1] + 1)
+    for i in range(L - 1, -1, -1):
+        raw[i] = min(raw[i], raw[i + 1] - 1)
+    assert oracle.nuhc_table_ok(raw, b, g)
+    return raw.astype(np.uint16)
+
+
+def _xs(P, N, seed):
+    return [np.random.default_rng([seed, P, N, w]).standard_normal(N).astype(np.float32) for w in range(P)]
+
+
+def _words(g, N, b, P, torch):
+    return [torch.empty(max(g.gar_thc_words(N, b), 1), dtype=torch.int32, device="cuda") for _ in range(P)]
+
+
+CASES = [(1, 1), (1, 5), (2, 3), (2, 4), (2, 17), (4, 15), (4, 36), (4, 51), (8, 255), (8, 1000)]
+
+
+@pytest.mark.parametrize("b,g", CASES)
+@pytest.mark.parametrize("P,N", [(1, 77), (3, 1001), (8, 4096), (16, 2049)])
+def test_encode_aggregate_decode_fused(env, b, g, P, N):
+    torch, gar = env
+    if P * g > 65535:
+        pytest.skip("sum would overflow 16 bits")
+    T = s_curve_table(b, g)
+    seed = 0x5EED + g
+    xs = _xs(P, N, 121)
+    m, M = oracle.thc_range(xs)
+    xd = [to_dev(x, torch) for x in xs]
+    mM = torch.tensor([m, M], dtype=torch.float32, device="cuda")
+    packed = _words(gar, N, b, P, torch)
+    for w in range(P):
+        gar.gar_nuhc_encode(xd[w], mM, b, g, T, seed, w, packed[w])
+    sums = torch.empty(N + 1, dtype=torch.int16, device="cuda")[:N]
+    gar.gar_nuhc_aggregate(packed, N, b, T, sums)
+    avg = torch.empty(N, device="cuda")
+    gar.gar_nuhc_decode(sums, mM, g, P, avg)
+    ref_avg, ref_packed = oracle.nuhc_allreduce(xs, b, g, T, seed, m, M, want_packed=True)
+    for w in range(P):
+        np.testing.assert_array_equal(to_host(packed[w])[:ref_packed[w].size], ref_packed[w])
+    np.testing.assert_array_equal(to_host(sums), oracle.nuhc_aggregate(ref_packed, N, b, T))
+    assert np.max(np.abs(to_host(avg).astype(np.float64) - ref_avg)) <= 1e-6 * max(abs(m), abs(M))
+    favg = torch.empty(N, device="cuda")
+    fpk = _words(gar, N, b, P, torch)
+    gar.gar_nuhc_allreduce_fused(xd, b, g, T, seed, mM, favg, fpk)
+    for w in range(P):
+        np.testing.assert_array_equal(to_host(fpk[w])[:ref_packed[w].size], ref_packed[w])
+    np.testing.assert_array_equal(to_host(favg).view(np.uint32), to_host(avg).view(np.uint32))
+
+
+@pytest.mark.parametrize("b", [1, 2, 4, 8])
+def test_identity_table_equals_uniform_kernels(env, b):
+    torch, gar = env
+    L = (1 << b) - 1
+    T = np.arange(L + 1, dtype=np.uint16)
+    P, N, seed = 5, 10007, 99
+    xd = [to_dev(x, torch) for x in _xs(P, N, 122)]
+    mM = torch.empty(2, device="cuda")
+    gar.gar_thc_range(xd, mM)
+    u_avg, n_avg = torch.empty(N, device="cuda"), torch.empty(N, device="cuda")
+    u_pk, n_pk = _words(gar, N, b, P, torch), _words(gar, N, b, P, torch)
+    gar.gar_thc_allreduce_fused(xd, b, seed, mM, u_avg, u_pk)
+    gar.gar_nuhc_allreduce_fused(xd, b, L, T, seed, mM, n_avg, n_pk)
+    assert torch.equal(u_avg.view(torch.int32), n_avg.view(torch.int32))
+    for a, c in zip(u_pk, n_pk):
+        assert torch.equal(a, c)
+
+
+def test_t2_example(env, golden_dir):
+    torch, gar = env
+    d = json.load(open(os.path.join(golden_dir, "nuhc_t2_example.json")))
+    b, g, T = d["b"], d["g"], np.array(d["table"], np.uint16)
+    mM = torch.tensor([d["m"], d["M"]], device="cuda")
+    for case in d["cases"]:
+        xd = [torch.tensor([float(Fraction(q))], device="cuda") for q in case["quantized"]]
+        pk = _words(gar, 1, b, len(xd), torch)
+        avg = torch.empty(1, device="cuda")
+        gar.gar_nuhc_allreduce_fused(xd, b, g, T, 7, mM, avg, pk)
+        assert [int(to_host(p)[0]) for p in pk] == case["indices"]
+        sums = torch.empty(2, dtype=torch.int16, device="cuda")[:1]
+        gar.gar_nuhc_aggregate(pk, 1, b, T, sums)
+        assert int(to_host(sums)[0]) == case["table_sum"]
+        assert abs(to_host(avg)[0] - float(Fraction(d["average_for_table_sum_3"]))) <= 1e-6
+
+
+def test_degenerate_and_errors(env):
+    torch, gar = env
+    T = s_curve_table(4, 36)
+    x = np.full(50, 0.25, np.float32)
+    xd = [to_dev(x, torch) for _ in range(3)]
+    mM = torch.empty(2, device="cuda")
+    gar.gar_thc_range(xd, mM)
+    avg = torch.empty(50, device="cuda")
+    pk = _words(gar, 50, 4, 3, torch)
+    gar.gar_nuhc_allreduce_fused(xd, 4, 36, T, 1, mM, avg, pk)
+    assert np.all(to_host(avg) == 0.25) and all(np.all(to_host(p) == 0) for p in pk)
+    bad = T.copy()
+    bad[3] = bad[2]
+    with pytest.raises(gar.GarError):
+        gar.gar_nuhc_allreduce_fused(xd, 4, 36, bad, 1, mM, avg, pk)
+    with pytest.raises(gar.GarError):
+        gar.gar_nuhc_allreduce_fused(xd, 4, 40, T, 1, mM, avg, pk)  # T ends at 36, not 40
+
+
+@pytest.mark.parametrize("P", [4, 16])
+def test_sweep_shape_full_size_sampled(env, P):
+    # N = 2^24 Student-t(3) x 1e-3, b = 4 with granularity 36 (the page's simulation setting)
+    torch, gar = env
+    b, g, N, seed = 4, 36, 1 << 24, workloads.THC_SEED
+    T = s_curve_table(b, g)
+    xd = [workloads.device_student_t(N, 3, 1e-3, 50_000 + 100 * P + w, "cuda") for w in range(P)]
+    mM = torch.empty(2, device="cuda")
+    gar.gar_thc_range(xd, mM)
+    lo = min(float(x.min()) for x in xd)
+    hi = max(float(x.max()) for x in xd)
+    avg = torch.empty(N, device="cuda")
+    pk = _words(gar, N, b, P, torch)
+    gar.gar_nuhc_allreduce_fused(xd, b, g, T, seed, mM, avg, pk)
+    idx = np.unique(np.concatenate([np.random.default_rng([123, P]).integers(0, N, 1024), [0, N - 1]]))
+    it = torch.from_numpy(idx).cuda()
+    vals = np.stack([to_host(x.index_select(0, it)) for x in xd])
+    per = 32 // b
+    wsel = torch.from_numpy(idx // per).cuda()
+    ref_idx = np.stack([[oracle.nuhc_index(vals[w, k], lo, hi, b, g, T, seed, w, int(idx[k])) for k in range(idx.size)]
+                        for w in range(P)])
+    for w in range(P):
+        words = to_host(pk[w].index_select(0, wsel))
+        got = (words >> ((idx % per) * b).astype(np.uint32)) & np.uint32((1 << b) - 1)
+        np.testing.assert_array_equal(got, ref_idx[w])
+    Y = T[ref_idx].astype(np.int64).sum(0)
+    ref_avg = float(np.float32(lo)) + Y / P * ((float(np.float32(hi)) - float(np.float32(lo))) / g)
+    got = to_host(avg.index_select(0, it)).astype(np.float64)
+    assert np.max(np.abs(got - ref_avg)) <= 1e-6 * max(abs(lo), abs(hi))
+    del xd, pk
+    torch.cuda.empty_cache()
