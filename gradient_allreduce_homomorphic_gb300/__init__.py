@@ -52,6 +52,7 @@ _SIGNATURES = {
     "gar_fusion_pack_all": (C.c_int, [_pp, _i32, _vp, _vp, _i32, _pp, _vp, _i32, _vp, _vp]),
     "gar_ring_allreduce_sim": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _vp]),
     "gar_ring_allreduce_sim_out": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _pp, _i32, _vp]),
+    "gar_ring_allreduce_bidir": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _vp]),
     "gar_ring_allreduce_steps": (C.c_int, [_pp, _i32, _i64, _i32, C.POINTER(_i32), _vp, _vp]),
     "gar_thc_words": (_i64, [_i64, _i32]),
     "gar_thc_range": (C.c_int, [_pp, _i32, _i64, _vp, _vp]),
@@ -249,6 +250,12 @@ def gar_fused_allreduce(src, dst, plan: FusionPlan, op: int = GAR_AVG, stream=No
 def gar_ring_allreduce_sim(bufs, op: int = GAR_AVG, stream=None):
     t = pointer_table(bufs)
     _call("gar_ring_allreduce_sim", t.array, len(t), t.numel, _dtype_code(t.first), op, _stream(stream))
+
+
+def gar_ring_allreduce_bidir(bufs, op: int = GAR_AVG, stream=None):
+    """Bidirectional dual ring (in place): first half clockwise, second half counter-clockwise."""
+    t = pointer_table(bufs)
+    _call("gar_ring_allreduce_bidir", t.array, len(t), t.numel, _dtype_code(t.first), op, _stream(stream))
 
 
 def gar_ring_allreduce_sim_out(bufs, out, op: int = GAR_AVG, stream=None):

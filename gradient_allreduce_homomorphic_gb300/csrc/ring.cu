@@ -84,9 +84,18 @@ __device__ __forceinline__ float finish(const Prm &p, float s) {
     return s;
 }
 
+// Worker at position k of the fold that starts at worker c: c + k, or c - k
+// on the counter-clockwise ring (indices mod P).
+__device__ __forceinline__ int ring_worker(int c, int k, int ccw, int P) {
+    int w = ccw ? c - k : c + k;
+    w += (w < 0) ? P : 0;
+    w -= (w >= P) ? P : 0;
+    return w;
+}
+
 // Fold one 16-byte vector at element e of row `row`, ring order from worker c.
 template <typename T, class Prm>
-__device__ __forceinline__ void fold_vec(const Prm &p, int row, int c, int64_t e) {
+__device__ __forceinline__ void fold_vec(const Prm &p, int row, int c, int ccw, int64_t e) {
     constexpr int V = Elem<T>::kVec;
     const int P = p.P;
     const void *const *src = p.src + static_cast<int64_t>(row) * P;
@@ -96,8 +105,7 @@ __device__ __forceinline__ void fold_vec(const Prm &p, int row, int c, int64_t e
 #pragma unroll
         for (int j = 0; j < kLoadBatch; ++j) {
             if (k0 + j < P) {
-                int w = c + k0 + j;
-                w -= (w >= P) ? P : 0;
+                const int w = ring_worker(c, k0 + j, ccw, P);
                 raw[j] = ld16(static_cast<const T *>(src[w]) + e);
             }
         }
@@ -124,14 +132,12 @@ __device__ __forceinline__ void fold_vec(const Prm &p, int row, int c, int64_t e
 }
 
 template <typename T, class Prm>
-__device__ __forceinline__ void fold_one(const Prm &p, int row, int c, int64_t e) {
+__device__ __forceinline__ void fold_one(const Prm &p, int row, int c, int ccw, int64_t e) {
     const int P = p.P;
     const void *const *src = p.src + static_cast<int64_t>(row) * P;
     float acc = Elem<T>::load1(src[c], e);
     for (int k = 1; k < P; ++k) {
-        int w = c + k;
-        w -= (w >= P) ? P : 0;
-        acc = __fadd_rn(acc, Elem<T>::load1(src[w], e));
+        acc = __fadd_rn(acc, Elem<T>::load1(src[ring_worker(c, k, ccw, P)], e));
     }
     acc = finish(p, acc);
     void *const *dst = p.dst + static_cast<int64_t>(row) * p.n_out;
@@ -160,20 +166,20 @@ __global__ void __launch_bounds__(kThreads) ring_fold_kernel(const __grid_consta
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int64_t i = lt * kTileUnits + u * kThreads + threadIdx.x;
-                if (i < nvec) fold_vec<T>(p, pc.row, pc.chunk, vb + i * V);
+                if (i < nvec) fold_vec<T>(p, pc.row, pc.chunk, pc.ccw, vb + i * V);
             }
             if (lt == 0) {  // ragged head and tail of the piece (fewer than V each)
                 const int head = static_cast<int>(vb - pc.begin);
                 const int tail = static_cast<int>(pc.end - ve);
-                if (threadIdx.x < head) fold_one<T>(p, pc.row, pc.chunk, pc.begin + threadIdx.x);
+                if (threadIdx.x < head) fold_one<T>(p, pc.row, pc.chunk, pc.ccw, pc.begin + threadIdx.x);
                 else if (threadIdx.x >= 32 && threadIdx.x < 32 + tail)
-                    fold_one<T>(p, pc.row, pc.chunk, ve + (threadIdx.x - 32));
+                    fold_one<T>(p, pc.row, pc.chunk, pc.ccw, ve + (threadIdx.x - 32));
             }
         } else {
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int64_t e = pc.begin + lt * kTileUnits + u * kThreads + threadIdx.x;
-                if (e < pc.end) fold_one<T>(p, pc.row, pc.chunk, e);
+                if (e < pc.end) fold_one<T>(p, pc.row, pc.chunk, pc.ccw, e);
             }
         }
     }
@@ -250,11 +256,12 @@ static int check_common(int32_t P, int64_t N, int32_t dtype, int32_t op) {
     return GAR_OK;
 }
 
-// Ring all-reduce of one buffer per worker: n_out destinations.
-static int ring_single(const void *const *src, void *const *dst, int n_out, int32_t P, int64_t N,
-                       int32_t dtype, int32_t op, cudaStream_t stream) {
-    using Prm = FoldParamsSmall;
-    Prm p;
+// Ring all-reduce of one buffer per worker: n_out destinations.  rings = 1:
+// P chunks on the clockwise ring; rings = 2: 2P sub-chunks, the first P on
+// the clockwise ring, the last P on the counter-clockwise ring.
+template <class Prm>
+static int ring_single_impl(Prm &p, const void *const *src, void *const *dst, int n_out, int32_t P, int64_t N,
+                            int32_t dtype, int32_t op, int rings, cudaStream_t stream) {
     std::memset(&p, 0, sizeof(p));
     p.P = P;
     p.n_out = n_out;
@@ -275,21 +282,34 @@ static int ring_single(const void *const *src, void *const *dst, int n_out, int3
         p.dst[k] = dst[k];
     }
     if (N == 0) return GAR_OK;
-    const int64_t clen = ceil_div(N, P);
-    for (int c = 0; c < P; ++c) {
-        const int64_t b = static_cast<int64_t>(c) * clen;
+    const int nchunks = rings * P;
+    const int64_t clen = ceil_div(N, nchunks);
+    for (int k = 0; k < nchunks; ++k) {
+        const int64_t b = static_cast<int64_t>(k) * clen;
         if (b >= N) break;
         const int64_t e = b + clen < N ? b + clen : N;
         Piece &pc = p.piece[p.npieces++];
         pc.row = 0;
-        pc.chunk = c;
+        pc.chunk = k < P ? k : k - P;
         pc.vec = vec ? 1 : 0;
-        pc.pad = 0;
+        pc.ccw = k < P ? 0 : 1;
         pc.begin = b;
         pc.end = e;
     }
     finalize_tiles(p, 16 / es);
     return launch_dtype(p, dtype, stream);
+}
+
+static int ring_single(const void *const *src, void *const *dst, int n_out, int32_t P, int64_t N, int32_t dtype,
+                       int32_t op, int rings, cudaStream_t stream) {
+    if (rings * P <= kSmallPieces) {
+        FoldParamsSmall p;
+        return ring_single_impl(p, src, dst, n_out, P, N, dtype, op, rings, stream);
+    }
+    FoldParamsLarge *p = new FoldParamsLarge;  // ~25 KB: keep it off the stack
+    const int rc = ring_single_impl(*p, src, dst, n_out, P, N, dtype, op, rings, stream);
+    delete p;
+    return rc;
 }
 
 extern "C" int gar_ring_allreduce_sim(void *const *bufs, int32_t P, int64_t N, int32_t dtype, int32_t op,
@@ -300,7 +320,19 @@ extern "C" int gar_ring_allreduce_sim(void *const *bufs, int32_t P, int64_t N, i
     for (int a = 0; a < P && N > 0; ++a)
         for (int b = a + 1; b < P; ++b)
             if (bufs[a] == bufs[b]) return fail(GAR_EINVAL, "workers %d and %d share a buffer", a, b);
-    return ring_single(reinterpret_cast<const void *const *>(bufs), bufs, P, P, N, dtype, op,
+    return ring_single(reinterpret_cast<const void *const *>(bufs), bufs, P, P, N, dtype, op, 1,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gar_ring_allreduce_bidir(void *const *bufs, int32_t P, int64_t N, int32_t dtype, int32_t op,
+                                        gar_stream_t stream) {
+    int rc = check_common(P, N, dtype, op);
+    if (rc) return rc;
+    if (!bufs) return fail(GAR_EINVAL, "bufs is NULL");
+    for (int a = 0; a < P && N > 0; ++a)
+        for (int b = a + 1; b < P; ++b)
+            if (bufs[a] == bufs[b]) return fail(GAR_EINVAL, "workers %d and %d share a buffer", a, b);
+    return ring_single(reinterpret_cast<const void *const *>(bufs), bufs, P, P, N, dtype, op, 2,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -310,7 +342,7 @@ extern "C" int gar_ring_allreduce_sim_out(const void *const *bufs, int32_t P, in
     if (rc) return rc;
     if (!bufs || !out) return fail(GAR_EINVAL, "bufs or out is NULL");
     if (n_out < 1 || n_out > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "n_out=%d outside [1, %d]", n_out, GAR_MAX_WORKERS);
-    return ring_single(bufs, out, n_out, P, N, dtype, op, reinterpret_cast<cudaStream_t>(stream));
+    return ring_single(bufs, out, n_out, P, N, dtype, op, 1, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------- plan-driven (fused) launch
@@ -362,7 +394,7 @@ int fused_allreduce_impl(const void *const *src, void *const *dst, int32_t P, co
                 pc.row = rows;
                 pc.chunk = static_cast<int32_t>(c);
                 pc.vec = vec ? 1 : 0;
-                pc.pad = 0;
+                pc.ccw = 0;
                 pc.begin = pos;
                 pc.end = stop;
                 pos = stop;

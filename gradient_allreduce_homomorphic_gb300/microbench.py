@@ -4,7 +4,7 @@
            [--b 4] [--iters 20] [--warmup 3] [--dtype f32|bf16]
 
 Cases: ring (in-place ring all-reduce of P buffers), ring_out (reduce to one
-output), fused (plan-driven all-reduce of the 300-tensor ResNet-like model),
+output), bidir (bidirectional dual ring), fused (plan-driven all-reduce of the 300-tensor ResNet-like model),
 pack, unpack (per worker and buffer), pack_all, pack_all_range (every worker
 in one call, with THC's range fused in), thc_range, thc_encode, thc_aggregate, thc_decode, thc_fused,
 thc_fused_packed, nuhc_fused, nuhc_fused_packed (non-uniform THC with a
@@ -53,11 +53,15 @@ def main(argv=None):
     def bufs(n, k, dt=tdt, seed=0):
         return [workloads.device_normal(n, 1.0, 77_000 + seed + i, dt, dev) for i in range(k)]
 
-    if a.case in ("ring", "ring_out"):
+    if a.case in ("ring", "ring_out", "bidir"):
         x = bufs(N, P)
         if a.case == "ring":
             t = g.pointer_table(x)
             fn = lambda: g.gar_ring_allreduce_sim(t)  # noqa: E731
+            nbytes = 2 * P * N * es
+        elif a.case == "bidir":
+            t = g.pointer_table(x)
+            fn = lambda: g.gar_ring_allreduce_bidir(t)  # noqa: E731
             nbytes = 2 * P * N * es
         else:
             out = [torch.empty(N, dtype=tdt, device=dev)]

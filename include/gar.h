@@ -199,6 +199,17 @@ int gar_ring_allreduce_sim_out(const void *const *bufs, int32_t P, int64_t N, in
                                int32_t op, void *const *out, int32_t n_out,
                                gar_stream_t stream);
 
+/* gar_ring_allreduce_bidir -- the bidirectional dual ring ([R] section 11,
+ * exercise 1): the buffer is cut into 2P sub-chunks of ceil(N / 2P)
+ * elements; sub-chunks 0..P-1 travel the clockwise ring exactly as in
+ * gar_ring_allreduce_sim (sub-chunk c folds x_c + x_{c+1} + ...), sub-chunks
+ * P..2P-1 travel the counter-clockwise ring (sub-chunk P + c folds
+ * x_c + x_{c-1} + ..., indices mod P), in the same 2(P-1) steps.  In place,
+ * fp32 or bf16, GAR_SUM or GAR_AVG as gar_ring_allreduce_sim.
+ * Errors: GAR_EINVAL, GAR_EDTYPE, GAR_EALIGN, GAR_ECUDA. */
+int gar_ring_allreduce_bidir(void *const *bufs, int32_t P, int64_t N, int32_t dtype, int32_t op,
+                             gar_stream_t stream);
+
 /* gar_ring_allreduce_steps -- the literal schedule, one launch per ring
  * step: P-1 scatter-reduce steps (worker i adds worker i-1's chunk
  * (i-s-1) mod P into its own), P-1 all-gather steps (worker i overwrites its

@@ -63,6 +63,10 @@ def _load():
                 "oracle_ring_fold_bf16": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, vp]),
                 "oracle_ring_fold_bf16_at": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, i64, vp]),
                 "oracle_ring_schedule_bf16": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, vp]),
+                "oracle_bidir_subchunk_len": (i64, [i64, C.c_int]),
+                "oracle_bidir_schedule_f32": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, vp]),
+                "oracle_bidir_fold_f32": (C.c_int, [pp, C.c_int, i64, C.c_int, vp]),
+                "oracle_bidir_fold_f32_samples": (C.c_int, [vp, C.c_int, i64, C.c_int, vp, i64, vp]),
                 "oracle_ring_fold_f32_samples": (C.c_int, [vp, C.c_int, i64, C.c_int, vp, i64, vp]),
                 "oracle_ring_fold_bf16_samples": (C.c_int, [vp, C.c_int, i64, C.c_int, vp, i64, vp]),
                 "oracle_thc_allreduce_samples": (C.c_int, [vp, C.c_int, vp, i64, C.c_int, u64, C.c_float,
@@ -174,6 +178,31 @@ def ring_fold_at(xs, n: int, idx, op: int = AVG):
     else:
         out = np.empty(idx.size, np.uint16)
         _check(lib.oracle_ring_fold_bf16_at(_ptrs(xs), p, n, op, _ptr(idx), idx.size, _ptr(out)), "fold_at")
+    return out
+
+
+def bidir_schedule(bufs, op: int = AVG):
+    """Literal bidirectional dual-ring schedule in place (fp32); returns (steps, sent_elems[p])."""
+    p, n = len(bufs), bufs[0].size
+    sent = np.zeros(p, np.int64)
+    steps = C.c_int(0)
+    _check(_load().oracle_bidir_schedule_f32(_ptrs(bufs), p, n, op, _ptr(sent), C.byref(steps)), "bidir_schedule")
+    return steps.value, sent
+
+
+def bidir_fold(xs, op: int = AVG):
+    out = np.empty(xs[0].size, np.float32)
+    _check(_load().oracle_bidir_fold_f32(_ptrs(xs), len(xs), xs[0].size, op, _ptr(out)), "bidir_fold")
+    return out
+
+
+def bidir_fold_samples(vals, n: int, idx, op: int = AVG):
+    """vals[w, k] = worker w's fp32 value at element idx[k]; the two-ring fold there."""
+    vals = np.ascontiguousarray(vals, np.float32)
+    idx = np.ascontiguousarray(idx, np.int64)
+    out = np.empty(idx.size, np.float32)
+    _check(_load().oracle_bidir_fold_f32_samples(_ptr(vals), vals.shape[0], n, op, _ptr(idx), idx.size, _ptr(out)),
+           "bidir_samples")
     return out
 
 

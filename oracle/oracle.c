@@ -260,6 +260,108 @@ int oracle_ring_fold_bf16_samples(const uint16_t *vals, int p, int64_t n, int op
 }
 
 /* ===================================================================== */
+/* Bidirectional dual ring [R] section 11, exercise 1                     */
+/* ===================================================================== */
+/* 2p sub-chunks of ceil(n / 2p) elements (trailing ones short or empty).
+ * Clockwise ring (next = i + 1) on sub-chunks 0..p-1, exactly the single
+ * ring's schedule; counter-clockwise ring (next = i - 1) on p..2p-1: at
+ * scatter step s worker i sends sub-chunk p + (i + s) mod p to worker i - 1,
+ * which adds it into its own copy; at gather step s it sends
+ * p + (i + s - 1) mod p, which the receiver copies.                       */
+int64_t oracle_bidir_subchunk_len(int64_t n, int p) { return (n + 2 * (int64_t)p - 1) / (2 * (int64_t)p); }
+
+static int64_t sub_begin(int64_t n, int p, int k) {
+    int64_t b = (int64_t)k * oracle_bidir_subchunk_len(n, p);
+    return b < n ? b : n;
+}
+static int64_t sub_end(int64_t n, int p, int k) { return sub_begin(n, p, k + 1); }
+
+int oracle_bidir_schedule_f32(float *const *bufs, int p, int64_t n, int op, int64_t *sent_elems,
+                              int *steps) {
+    if (p < 1 || p > 64 || n < 0 || (op != ORACLE_SUM && op != ORACLE_AVG)) return -1;
+    int64_t slen = oracle_bidir_subchunk_len(n, p);
+    size_t slot = (size_t)(slen > 0 ? slen : 1);
+    float *cw = (float *)malloc(sizeof(float) * slot * (size_t)p);
+    float *ccw = (float *)malloc(sizeof(float) * slot * (size_t)p);
+    if (!cw || !ccw) {
+        free(cw);
+        free(ccw);
+        return -1;
+    }
+    for (int w = 0; w < p; ++w)
+        if (sent_elems) sent_elems[w] = 0;
+    int nsteps = 0;
+    for (int phase = 0; phase < 2; ++phase) {
+        for (int s = 0; s < p - 1; ++s) {
+            /* every worker's two sends of this step, taken before any receive */
+            int cw_send[64], ccw_send[64];
+            for (int i = 0; i < p; ++i) {
+                cw_send[i] = phase == 0 ? ring_mod(i - s, p) : ring_mod(i - s + 1, p);
+                ccw_send[i] = p + (phase == 0 ? ring_mod(i + s, p) : ring_mod(i + s - 1, p));
+                int64_t b0 = sub_begin(n, p, cw_send[i]), e0 = sub_end(n, p, cw_send[i]);
+                int64_t b1 = sub_begin(n, p, ccw_send[i]), e1 = sub_end(n, p, ccw_send[i]);
+                memcpy(cw + (size_t)i * slot, bufs[i] + b0, sizeof(float) * (size_t)(e0 - b0));
+                memcpy(ccw + (size_t)i * slot, bufs[i] + b1, sizeof(float) * (size_t)(e1 - b1));
+                if (sent_elems) sent_elems[i] += (e0 - b0) + (e1 - b1);
+            }
+            for (int i = 0; i < p; ++i) {
+                int from_cw = ring_mod(i - 1, p), from_ccw = ring_mod(i + 1, p);
+                int k0 = cw_send[from_cw], k1 = ccw_send[from_ccw];
+                int64_t b0 = sub_begin(n, p, k0), e0 = sub_end(n, p, k0);
+                int64_t b1 = sub_begin(n, p, k1), e1 = sub_end(n, p, k1);
+                const float *r0 = cw + (size_t)from_cw * slot, *r1 = ccw + (size_t)from_ccw * slot;
+                for (int64_t k = b0; k < e0; ++k) bufs[i][k] = phase == 0 ? bufs[i][k] + r0[k - b0] : r0[k - b0];
+                for (int64_t k = b1; k < e1; ++k) bufs[i][k] = phase == 0 ? bufs[i][k] + r1[k - b1] : r1[k - b1];
+            }
+            ++nsteps;
+        }
+    }
+    if (op == ORACLE_AVG) {
+        float fp = (float)p;
+        for (int i = 0; i < p; ++i)
+            for (int64_t k = 0; k < n; ++k) bufs[i][k] = bufs[i][k] / fp;
+    }
+    free(cw);
+    free(ccw);
+    if (steps) *steps = nsteps;
+    return 0;
+}
+
+/* Closed form: an element of clockwise sub-chunk c is x_c + x_{c+1} + ...;
+ * one of counter-clockwise sub-chunk p + c is x_c + x_{c-1} + ... (mod p). */
+int oracle_bidir_fold_f32(const float *const *x, int p, int64_t n, int op, float *out) {
+    if (p < 1 || n < 0 || p > 64) return -1;
+    int64_t slen = oracle_bidir_subchunk_len(n, p);
+    for (int64_t k = 0; k < n; ++k) {
+        int sub = (int)(k / slen);
+        int c = sub < p ? sub : sub - p;
+        int dir = sub < p ? 1 : -1;
+        float s = x[c][k];
+        for (int j = 1; j < p; ++j) s = s + x[ring_mod(c + dir * j, p)][k];
+        if (op == ORACLE_AVG) s = s / (float)p;
+        out[k] = s;
+    }
+    return 0;
+}
+
+int oracle_bidir_fold_f32_samples(const float *vals, int p, int64_t n, int op, const int64_t *e,
+                                  int64_t count, float *out) {
+    if (p < 1 || n < 0 || p > 64) return -1;
+    int64_t slen = oracle_bidir_subchunk_len(n, p);
+    for (int64_t k = 0; k < count; ++k) {
+        if (e[k] < 0 || e[k] >= n) return -1;
+        int sub = (int)(e[k] / slen);
+        int c = sub < p ? sub : sub - p;
+        int dir = sub < p ? 1 : -1;
+        float s = vals[(int64_t)c * count + k];
+        for (int j = 1; j < p; ++j) s = s + vals[(int64_t)ring_mod(c + dir * j, p) * count + k];
+        if (op == ORACLE_AVG) s = s / (float)p;
+        out[k] = s;
+    }
+    return 0;
+}
+
+/* ===================================================================== */
 /* Tensor Fusion [H] "Tensor Fusion", steps 1-6                           */
 /* ===================================================================== */
 static int dtype_bytes(int32_t dt) {

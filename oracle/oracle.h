@@ -78,6 +78,19 @@ int oracle_ring_fold_f32_samples(const float *vals, int p, int64_t n, int op, co
 int oracle_ring_fold_bf16_samples(const uint16_t *vals, int p, int64_t n, int op,
                                   const int64_t *e, int64_t count, uint16_t *out);
 
+/* Bidirectional dual ring ([R] section 11, exercise 1 and its worked
+ * solution): the buffer is cut into 2p sub-chunks; sub-chunks 0..p-1 go
+ * round the clockwise ring, p..2p-1 round the counter-clockwise ring, both
+ * in the same 2(p-1) steps.  Literal schedule (fp32, in place) and its
+ * closed form. */
+int64_t oracle_bidir_subchunk_len(int64_t n, int p);
+int oracle_bidir_schedule_f32(float *const *bufs, int p, int64_t n, int op, int64_t *sent_elems,
+                              int *steps);
+int oracle_bidir_fold_f32(const float *const *x, int p, int64_t n, int op, float *out);
+/* sampled form: vals[w * count + k] = worker w's value at element e[k] */
+int oracle_bidir_fold_f32_samples(const float *vals, int p, int64_t n, int op, const int64_t *e,
+                                  int64_t count, float *out);
+
 /* ---------------- Tensor Fusion [H] ---------------- */
 /* Next-fit plan.  dtype[i] is ORACLE_F32 or ORACLE_BF16.  Outputs per tensor:
  * seg_buffer[i], seg_offset[i] (elements from the buffer start); per buffer:
