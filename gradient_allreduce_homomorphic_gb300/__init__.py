@@ -60,6 +60,7 @@ _SIGNATURES = {
     "gar_thc_aggregate": (C.c_int, [_pp, _i32, _i64, _i32, _vp, _vp]),
     "gar_thc_decode": (C.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _vp]),
     "gar_thc_allreduce_fused": (C.c_int, [_pp, _i32, _i64, _i32, _u64, _vp, _vp, _pp, _vp]),
+    "gar_thc_allreduce_fused_masked": (C.c_int, [_pp, _i32, _u64, _i64, _i32, _u64, _vp, _vp, _pp, _vp]),
     "gar_nuhc_encode": (C.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _u64, _i32, _vp, _vp]),
     "gar_nuhc_aggregate": (C.c_int, [_pp, _i32, _i64, _i32, _vp, _vp, _vp]),
     "gar_nuhc_decode": (C.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _vp]),
@@ -302,6 +303,15 @@ def gar_thc_allreduce_fused(x, b: int, seed: int, d_mM, avg, packed=None, stream
     pk = pointer_table(packed).array if packed is not None else None
     _call("gar_thc_allreduce_fused", t.array, len(t), t.numel, b, seed, _dev(d_mM), _dev(avg), pk,
           _stream(stream))
+
+
+def gar_thc_allreduce_fused_masked(x, arrived: int, b: int, seed: int, d_mM, avg, packed=None, stream=None):
+    """THC round over the workers whose bit is set in `arrived` (stragglers
+    dropped); x[w] / packed[w] of the others may be None."""
+    xt = pointer_table(x, allow_none=True)
+    pk = pointer_table(packed, allow_none=True).array if packed is not None else None
+    _call("gar_thc_allreduce_fused_masked", xt.array, len(xt), arrived, xt.numel, b, seed, _dev(d_mM), _dev(avg),
+          pk, _stream(stream))
 
 
 # --------------------------------------------------------- non-uniform THC

@@ -299,13 +299,14 @@ __global__ void __launch_bounds__(kThreads) thc_decode_kernel(const __grid_const
 // ------------------------------------------------------------------ fused
 struct FusedParams {
     PhiloxKeys keys;
-    const float *x[GAR_MAX_WORKERS];
+    const float *x[GAR_MAX_WORKERS];    // the P contributing workers, slot by slot
     uint32_t *packed[GAR_MAX_WORKERS];  // all NULL when the wire vectors are not wanted
+    int32_t wid[GAR_MAX_WORKERS];       // worker id of each slot (keys its Philox stream)
     const float *mM;
     float *avg;
     int64_t N;
     int64_t nwords;
-    int32_t P;
+    int32_t P;    // contributing workers (the decode divides by this)
     int32_t vec;  // inputs and avg 16-byte aligned
     float L;
     float fp;
@@ -338,7 +339,7 @@ __global__ void __launch_bounds__(kThreads) thc_fused_kernel(const __grid_consta
                 uint32_t word = 0;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const uint4 r = philox_block((e0 >> 2) + g, wk, p.keys);
+                    const uint4 r = philox_block((e0 >> 2) + g, p.wid[wk], p.keys);
                     const uint32_t a0 = index_biased(cur[g].x, m, sc, p.L, r.x);
                     const uint32_t a1 = index_biased(cur[g].y, m, sc, p.L, r.y);
                     const uint32_t a2 = index_biased(cur[g].z, m, sc, p.L, r.z);
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(kThreads) thc_fused_kernel(const __grid_consta
                 for (int g = 0; g < G; ++g) {
                     const int64_t eb = e0 + 4 * g;
                     if (eb >= p.N) break;
-                    const uint4 r = philox_block(eb >> 2, wk, p.keys);
+                    const uint4 r = philox_block(eb >> 2, p.wid[wk], p.keys);
                     for (int i = 0; i < 4 && eb + i < p.N; ++i) {
                         const uint32_t a = index_biased(p.x[wk][eb + i], m, sc, p.L, pick(r, i));
                         s[4 * g + i] += a;
@@ -763,11 +764,16 @@ extern "C" int gar_thc_decode(const uint16_t *sums, int64_t N, const float *d_mM
     return check_launch("thc_decode_kernel");
 }
 
-extern "C" int gar_thc_allreduce_fused(const float *const *x, int32_t P, int64_t N, int32_t b, uint64_t seed,
-                                       const float *d_mM, float *avg, uint32_t *const *packed, gar_stream_t stream_) {
+// Shared by the plain and the straggler-masked fused entry points: the
+// workers whose bit is set in `arrived` contribute, each under its own id.
+static int thc_fused_entry(const float *const *x, int32_t P, uint64_t arrived, int64_t N, int32_t b, uint64_t seed,
+                           const float *d_mM, float *avg, uint32_t *const *packed, gar_stream_t stream_) {
     if (!valid_b(b)) return fail(GAR_EINVAL, "b=%d not in {1, 2, 4, 8}", b);
     if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
-    if (static_cast<int64_t>(P) * ((1 << b) - 1) > 65535) return fail(GAR_EOVERFLOW, "P * (2^b - 1) > 65535");
+    if (P < 64) arrived &= (uint64_t{1} << P) - 1u;
+    const int p_eff = __builtin_popcountll(arrived);
+    if (p_eff == 0) return fail(GAR_EINVAL, "no worker arrived");
+    if (static_cast<int64_t>(p_eff) * ((1 << b) - 1) > 65535) return fail(GAR_EOVERFLOW, "P * (2^b - 1) > 65535");
     if (N < 0 || !d_mM || !x) return fail(GAR_EINVAL, "N < 0 or NULL argument");
     if (N == 0) return GAR_OK;
     if (!avg) return fail(GAR_EINVAL, "avg is NULL");
@@ -779,20 +785,24 @@ extern "C" int gar_thc_allreduce_fused(const float *const *x, int32_t P, int64_t
     p.avg = avg;
     p.N = N;
     p.nwords = gar_thc_words(N, b);
-    p.P = P;
+    p.P = p_eff;
     p.L = static_cast<float>((1 << b) - 1);
-    p.fp = static_cast<float>(P);
+    p.fp = static_cast<float>(p_eff);
     p.vec = aligned(avg, 16) ? 1 : 0;
+    int slot = 0;
     for (int w = 0; w < P; ++w) {
+        if (!((arrived >> w) & 1u)) continue;
         if (!x[w]) return fail(GAR_EINVAL, "input %d is NULL", w);
         if (!aligned(x[w], 4)) return fail(GAR_EALIGN, "input %d not 4-byte aligned", w);
-        p.x[w] = x[w];
+        p.x[slot] = x[w];
+        p.wid[slot] = w;
         p.vec = p.vec && aligned(x[w], 16);
         if (packed) {
             if (!packed[w]) return fail(GAR_EINVAL, "packed vector %d is NULL", w);
             if (!aligned(packed[w], 4)) return fail(GAR_EALIGN, "packed vector %d not 4-byte aligned", w);
-            p.packed[w] = packed[w];
+            p.packed[slot] = packed[w];
         }
+        ++slot;
     }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 #define GAR_FUSED_CASE(BB)                                                                                  \
@@ -810,6 +820,17 @@ extern "C" int gar_thc_allreduce_fused(const float *const *x, int32_t P, int64_t
     }
 #undef GAR_FUSED_CASE
     return check_launch("thc_fused_kernel");
+}
+
+extern "C" int gar_thc_allreduce_fused(const float *const *x, int32_t P, int64_t N, int32_t b, uint64_t seed,
+                                       const float *d_mM, float *avg, uint32_t *const *packed, gar_stream_t stream) {
+    return thc_fused_entry(x, P, ~uint64_t{0}, N, b, seed, d_mM, avg, packed, stream);
+}
+
+extern "C" int gar_thc_allreduce_fused_masked(const float *const *x, int32_t P, uint64_t arrived, int64_t N,
+                                              int32_t b, uint64_t seed, const float *d_mM, float *avg,
+                                              uint32_t *const *packed, gar_stream_t stream) {
+    return thc_fused_entry(x, P, arrived, N, b, seed, d_mM, avg, packed, stream);
 }
 
 // ------------------------------------------------------- non-uniform THC

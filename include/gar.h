@@ -283,6 +283,20 @@ int gar_thc_allreduce_fused(const float *const *x, int32_t P, int64_t N, int32_t
                             uint64_t seed, const float *d_mM, float *avg,
                             uint32_t *const *packed, gar_stream_t stream);
 
+/* gar_thc_allreduce_fused_masked -- straggler dropping ([T] section 8,
+ * stragglers: the PS waits only for the workers that arrived).  Only the
+ * workers whose bit is set in `arrived` (bit w = worker w, w < P) are
+ * encoded, each under its own worker id, and summed; the decode divides by
+ * their number.  x[w] and packed[w] of the other workers are not read or
+ * written (they may be NULL).  With every bit set this is
+ * gar_thc_allreduce_fused bit for bit; it also equals gar_thc_encode of the
+ * arrived workers -> gar_thc_aggregate over their vectors -> gar_thc_decode
+ * with their number.  Errors: as gar_thc_allreduce_fused, and GAR_EINVAL when
+ * no worker arrived. */
+int gar_thc_allreduce_fused_masked(const float *const *x, int32_t P, uint64_t arrived, int64_t N,
+                                   int32_t b, uint64_t seed, const float *d_mM, float *avg,
+                                   uint32_t *const *packed, gar_stream_t stream);
+
 /* ===================================================================== */
 /* Non-uniform THC [T] section 5, Algorithm 2                            */
 /* ===================================================================== */

@@ -82,6 +82,8 @@ def _load():
                 "oracle_thc_aggregate": (C.c_int, [pp, C.c_int, i64, C.c_int, vp]),
                 "oracle_thc_decode": (C.c_int, [vp, i64, C.c_float, C.c_float, C.c_int, C.c_int, vp]),
                 "oracle_thc_allreduce": (C.c_int, [pp, C.c_int, i64, C.c_int, u64, C.c_float, C.c_float, vp, pp]),
+                "oracle_thc_allreduce_masked": (C.c_int, [pp, C.c_int, u64, i64, C.c_int, u64, C.c_float,
+                                                          C.c_float, vp, pp]),
                 "oracle_nuhc_check_table": (C.c_int, [vp, C.c_int, C.c_int]),
                 "oracle_nuhc_position": (C.c_float, [C.c_float, C.c_float, C.c_float, C.c_int]),
                 "oracle_nuhc_index": (u32, [C.c_float, C.c_float, C.c_float, C.c_int, C.c_int, vp, u64, C.c_int,
@@ -342,6 +344,18 @@ def thc_allreduce(xs, b: int, seed: int, m=None, M=None, want_packed: bool = Fal
     packed = [np.empty(max(thc_words(n, b), 1), np.uint32) for _ in range(p)]
     _check(_load().oracle_thc_allreduce(_ptrs(xs), p, n, b, seed, float(m), float(M), _ptr(avg),
                                         _ptrs(packed)), "thc_allreduce")
+    if want_packed:
+        return avg, [pk[:thc_words(n, b)] for pk in packed]
+    return avg
+
+
+def thc_allreduce_masked(xs, arrived: int, b: int, seed: int, m, M, want_packed: bool = False):
+    """THC round over the workers whose bit is set in `arrived` (stragglers dropped)."""
+    p, n = len(xs), xs[0].size
+    avg = np.empty(n, np.float64)
+    packed = [np.zeros(max(thc_words(n, b), 1), np.uint32) for _ in range(p)]
+    _check(_load().oracle_thc_allreduce_masked(_ptrs(xs), p, arrived, n, b, seed, float(m), float(M), _ptr(avg),
+                                               _ptrs(packed)), "thc_allreduce_masked")
     if want_packed:
         return avg, [pk[:thc_words(n, b)] for pk in packed]
     return avg

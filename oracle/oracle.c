@@ -551,6 +551,27 @@ int oracle_thc_allreduce_samples(const float *vals, int p, const int64_t *e, int
     return 0;
 }
 
+int oracle_thc_allreduce_masked(const float *const *x, int p, uint64_t arrived, int64_t n, int b,
+                                uint64_t seed, float m, float M, double *avg, uint32_t *const *packed) {
+    if (!valid_bits(b) || n < 0 || p < 1 || p > 64) return -1;
+    int p_eff = 0;
+    for (int w = 0; w < p; ++w) p_eff += (int)((arrived >> w) & 1u);
+    if (p_eff == 0) return -1;
+    double L = (double)((1 << b) - 1);
+    double step = ((double)M - (double)m) / L;
+    for (int w = 0; w < p; ++w) {
+        if (!((arrived >> w) & 1u) || !packed) continue;
+        if (oracle_thc_encode(x[w], n, m, M, b, seed, w, packed[w]) != 0) return -1;
+    }
+    for (int64_t e = 0; e < n; ++e) {
+        uint32_t s = 0;
+        for (int w = 0; w < p; ++w)
+            if ((arrived >> w) & 1u) s += oracle_thc_index(x[w][e], m, M, b, seed, w, e);
+        avg[e] = (double)m + ((double)s / (double)p_eff) * step;
+    }
+    return 0;
+}
+
 int oracle_thc_allreduce(const float *const *x, int p, int64_t n, int b, uint64_t seed,
                          float m, float M, double *avg, uint32_t *const *packed) {
     if (!valid_bits(b) || n < 0 || p < 1) return -1;

@@ -127,6 +127,12 @@ int oracle_thc_decode(const uint16_t *sums, int64_t n, float m, float M, int b, 
  * average of element e[k]. */
 int oracle_thc_allreduce_samples(const float *vals, int p, const int64_t *e, int64_t count, int b,
                                  uint64_t seed, float m, float M, uint8_t *idx, double *avg);
+/* Straggler dropping ([T] section 8, stragglers): only the workers whose bit
+ * is set in `arrived` are encoded (each with its own worker id) and summed;
+ * the decode divides by their number.  packed may be NULL; entries of
+ * workers that did not arrive are not written. */
+int oracle_thc_allreduce_masked(const float *const *x, int p, uint64_t arrived, int64_t n, int b,
+                                uint64_t seed, float m, float M, double *avg, uint32_t *const *packed);
 /* encode every worker, aggregate, decode; packed may be NULL */
 int oracle_thc_allreduce(const float *const *x, int p, int64_t n, int b, uint64_t seed,
                          float m, float M, double *avg, uint32_t *const *packed);

@@ -218,6 +218,43 @@ def test_thc_sweep_full_size_sampled(env, P, b):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("arrived", [0b11111111, 0b10110101, 0b00001000, 0b11111110])
+@pytest.mark.parametrize("b", [2, 4, 8])
+def test_straggler_masked(env, arrived, b):
+    # stragglers dropped: only arrived workers encode (own ids) and sum, decode by their count
+    torch, g = env
+    P, N, seed = 8, 20011, 4242
+    xs = _xs(P, N, 9)
+    ids = [w for w in range(P) if (arrived >> w) & 1]
+    m, M = oracle.thc_range([xs[w] for w in ids])
+    mM = torch.tensor([m, M], device="cuda")
+    xd = [to_dev(x, torch) if w in ids else None for w, x in enumerate(xs)]
+    pk = [torch.zeros(g.gar_thc_words(N, b), dtype=torch.int32, device="cuda") if w in ids else None for w in range(P)]
+    avg = torch.empty(N, device="cuda")
+    g.gar_thc_allreduce_fused_masked(xd, arrived, b, seed, mM, avg, pk)
+    ref_avg, ref_pk = oracle.thc_allreduce_masked(xs, arrived, b, seed, m, M, want_packed=True)
+    for w in ids:
+        np.testing.assert_array_equal(to_host(pk[w]), ref_pk[w])
+    assert np.max(np.abs(to_host(avg).astype(np.float64) - ref_avg)) <= 1e-6 * max(abs(m), abs(M))
+    # the same as the separate kernels over the arrived workers' vectors
+    sums = torch.empty(N, dtype=torch.int16, device="cuda")
+    g.gar_thc_aggregate([pk[w] for w in ids], N, b, sums)
+    avg2 = torch.empty(N, device="cuda")
+    g.gar_thc_decode(sums, mM, b, len(ids), avg2)
+    assert torch.equal(avg.view(torch.int32), avg2.view(torch.int32))
+    if arrived == (1 << P) - 1:  # everyone arrived: the unmasked kernel, bit for bit
+        avg3 = torch.empty(N, device="cuda")
+        g.gar_thc_allreduce_fused(xd, b, seed, mM, avg3)
+        assert torch.equal(avg.view(torch.int32), avg3.view(torch.int32))
+
+
+def test_straggler_mask_rejects_no_arrivals(env):
+    torch, g = env
+    x = [torch.zeros(8, device="cuda")]
+    with pytest.raises(g.GarError):
+        g.gar_thc_allreduce_fused_masked(x, 0, 4, 1, torch.zeros(2, device="cuda"), torch.empty(8, device="cuda"))
+
+
 @pytest.mark.parametrize("N", [1, 3, 4, 1000, 4097, 1 << 20])
 def test_nmse(env, N):
     torch, g = env

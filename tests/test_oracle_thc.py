@@ -265,6 +265,52 @@ def test_nmse_definition():
     assert math.isnan(oracle.nmse(np.zeros(4, np.float32), np.ones(4, np.float32)))
 
 
+def test_masked_round_all_arrived_is_the_full_round():
+    P, N, b = 6, 777, 4
+    xs = [np.random.default_rng([151, w]).standard_normal(N).astype(np.float32) for w in range(P)]
+    m, M = oracle.thc_range(xs)
+    full, pk_full = oracle.thc_allreduce(xs, b, 3, m, M, want_packed=True)
+    masked, pk_m = oracle.thc_allreduce_masked(xs, (1 << P) - 1, b, 3, m, M, want_packed=True)
+    np.testing.assert_array_equal(full, masked)
+    for a, c in zip(pk_full, pk_m):
+        np.testing.assert_array_equal(a, c)
+
+
+def test_masked_round_keeps_worker_ids_and_divides_by_arrivals():
+    # stragglers 1 and 4 dropped: the others are encoded with their own ids
+    # (not renumbered) and the decode divides by the 4 that arrived
+    P, N, b = 6, 500, 4
+    xs = [np.random.default_rng([152, w]).standard_normal(N).astype(np.float32) for w in range(P)]
+    m, M = oracle.thc_range(xs)
+    arrived = 0b101101
+    avg, pk = oracle.thc_allreduce_masked(xs, arrived, b, 11, m, M, want_packed=True)
+    ids = [w for w in range(P) if (arrived >> w) & 1]
+    for w in ids:
+        np.testing.assert_array_equal(pk[w], oracle.thc_encode(xs[w], m, M, b, 11, w))
+    idx = np.sum([oracle.thc_unpack(pk[w], N, b).astype(np.int64) for w in ids], axis=0)
+    np.testing.assert_allclose(avg, oracle.thc_decode(idx.astype(np.uint16), m, M, b, len(ids)), rtol=0, atol=0)
+    # a single arrival decodes to that worker's own quantized values
+    one = oracle.thc_allreduce_masked(xs, 1 << 3, b, 11, m, M)
+    q = oracle.thc_unpack(oracle.thc_encode(xs[3], m, M, b, 11, 3), N, b)
+    np.testing.assert_allclose(one, oracle.thc_decode(q.astype(np.uint16), m, M, b, 1), rtol=0, atol=0)
+
+
+def test_masked_round_unbiased_for_the_arrived_mean():
+    P, N, b = 5, 64, 2
+    xs = [np.random.default_rng([153, w]).standard_normal(N).astype(np.float32) for w in range(P)]
+    m, M = oracle.thc_range(xs)
+    arrived = 0b10110
+    ids = [w for w in range(P) if (arrived >> w) & 1]
+    target = np.mean(np.stack([xs[w] for w in ids]).astype(np.float64), axis=0)
+    K = 1500
+    acc = np.zeros(N)
+    for seed in range(K):
+        acc += oracle.thc_allreduce_masked(xs, arrived, b, seed, m, M)
+    step = (float(M) - float(m)) / 3
+    sigma = math.sqrt(step ** 2 / (4 * len(ids)) / K)
+    assert np.all(np.abs(acc / K - target) <= 5.5 * sigma + _bias_bound(m, M, b))
+
+
 def test_samples_match_full_round():
     P, N, b = 5, 3001, 4
     xs = [np.random.default_rng([73, w]).standard_normal(N).astype(np.float32) for w in range(P)]
