@@ -92,6 +92,9 @@ def _load():
                                                  C.c_int, vp]),
                 "oracle_nuhc_aggregate": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, vp]),
                 "oracle_nuhc_decode": (C.c_int, [vp, i64, C.c_float, C.c_float, C.c_int, C.c_int, vp]),
+                "oracle_rht_signs": (C.c_int, [i64, u64, vp]),
+                "oracle_rht": (C.c_int, [vp, i64, u64, C.c_int, vp]),
+                "oracle_rht_norm_range": (None, [pp, C.c_int, i64, C.c_double, vp, vp]),
                 "oracle_nmse": (C.c_double, [vp, vp, i64]),
                 "oracle_nmse_f64": (C.c_double, [vp, vp, i64]),
             }
@@ -407,6 +410,29 @@ def nuhc_allreduce(xs, b: int, g: int, table, seed: int, m=None, M=None, want_pa
     packed = [nuhc_encode(x, m, M, b, g, table, seed, w) for w, x in enumerate(xs)]
     avg = nuhc_decode(nuhc_aggregate(packed, xs[0].size, b, table), m, M, g, len(xs))
     return (avg, packed) if want_packed else avg
+
+
+# ----------------------------------------------------------------- RHT
+def rht_signs(n: int, seed: int) -> np.ndarray:
+    out = np.empty(n, np.int8)
+    _check(_load().oracle_rht_signs(n, seed, _ptr(out)), "rht_signs")
+    return out
+
+
+def rht(x, seed: int, inverse: bool = False) -> np.ndarray:
+    """(1/sqrt(n)) H D x, or its inverse (1/sqrt(n)) D H y, in fp64."""
+    v = np.ascontiguousarray(x, np.float64)
+    out = np.empty_like(v)
+    _check(_load().oracle_rht(_ptr(v), v.size, seed, 1 if inverse else 0, _ptr(out)), "rht")
+    return out
+
+
+def rht_norm_range(xs, t_p: float):
+    """m = -M, M = (t_p / sqrt(n)) max_w ||x_w||_2 (fp64)."""
+    vs = [np.ascontiguousarray(x, np.float64) for x in xs]
+    m, M = C.c_double(0), C.c_double(0)
+    _load().oracle_rht_norm_range(_ptrs(vs), len(vs), vs[0].size, float(t_p), C.byref(m), C.byref(M))
+    return m.value, M.value
 
 
 def nmse(x, x_hat) -> float:

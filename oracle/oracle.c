@@ -681,6 +681,63 @@ int oracle_nuhc_decode(const uint16_t *sums, int64_t n, float m, float M, int g,
 }
 
 /* ===================================================================== */
+/* Randomized Hadamard Transform [T] section 5                            */
+/* ===================================================================== */
+static int is_pow2(int64_t n) { return n > 0 && (n & (n - 1)) == 0; }
+
+int oracle_rht_signs(int64_t n, uint64_t seed, int8_t *d) {
+    if (n < 0) return -1;
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    for (int64_t i = 0; i < n; ++i) {
+        uint64_t q = (uint64_t)i >> 7;
+        uint32_t ctr[4] = {(uint32_t)q, (uint32_t)(q >> 32), 0xFFFFFFFFu, 0u};
+        uint32_t r[4];
+        oracle_philox4x32(ctr, key, 10, r);
+        uint32_t bit = (r[(i >> 5) & 3] >> (i & 31)) & 1u;
+        d[i] = bit ? (int8_t)-1 : (int8_t)1;
+    }
+    return 0;
+}
+
+/* In-place fast Walsh-Hadamard transform (unnormalised): for each stride h
+ * = 1, 2, 4, ..., pairs (a, b) at distance h become (a + b, a - b).  This is
+ * H_n x for the Sylvester construction H_2n = [[H_n, H_n], [H_n, -H_n]]. */
+static void fwht(double *v, int64_t n) {
+    for (int64_t h = 1; h < n; h <<= 1)
+        for (int64_t i = 0; i < n; i += 2 * h)
+            for (int64_t j = i; j < i + h; ++j) {
+                double a = v[j], b = v[j + h];
+                v[j] = a + b;
+                v[j + h] = a - b;
+            }
+}
+
+int oracle_rht(const double *in, int64_t n, uint64_t seed, int inverse, double *out) {
+    if (!is_pow2(n)) return -1;
+    int8_t *d = (int8_t *)malloc((size_t)n);
+    if (!d) return -1;
+    oracle_rht_signs(n, seed, d);
+    double scale = 1.0 / sqrt((double)n);
+    for (int64_t i = 0; i < n; ++i) out[i] = inverse ? in[i] : in[i] * d[i];
+    fwht(out, n);
+    for (int64_t i = 0; i < n; ++i) out[i] = (inverse ? out[i] * d[i] : out[i]) * scale;
+    free(d);
+    return 0;
+}
+
+void oracle_rht_norm_range(const double *const *x, int p, int64_t n, double t_p, double *m,
+                           double *M) {
+    double l = 0.0;
+    for (int w = 0; w < p; ++w) {
+        double s = 0.0;
+        for (int64_t i = 0; i < n; ++i) s += x[w][i] * x[w][i];
+        if (sqrt(s) > l) l = sqrt(s);
+    }
+    *M = t_p / sqrt((double)n) * l;
+    *m = -*M;
+}
+
+/* ===================================================================== */
 /* NMSE [T] section 2: ||x - x_hat||^2 / ||x||^2, accumulated in fp64.     */
 /* ===================================================================== */
 double oracle_nmse(const float *x, const float *x_hat, int64_t n) {

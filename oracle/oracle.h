@@ -153,6 +153,20 @@ int oracle_nuhc_aggregate(const uint32_t *const *packed, int p, int64_t n, int b
 int oracle_nuhc_decode(const uint16_t *sums, int64_t n, float m, float M, int g, int p,
                        double *avg);
 
+/* ---------------- RHT pre/post-processing [T] section 5 ---------------- */
+/* Rademacher diagonal D: d_i = -1 when bit (i mod 128) of the 128-bit
+ * Philox4x32-10 block with counter (i/128 low, i/128 high, 0xFFFFFFFF, 0)
+ * and key (seed low, seed high) is set (word (i/32) mod 4, bit i mod 32),
+ * else +1.  The worker slot 0xFFFFFFFF keeps this stream apart from the
+ * quantization draws; every worker uses the same D (same seed). */
+int oracle_rht_signs(int64_t n, uint64_t seed, int8_t *d);
+/* y = (1/sqrt(n)) H D x (inverse = 0) or x = (1/sqrt(n)) D H y (inverse = 1),
+ * n a power of two, H the Sylvester-Hadamard matrix, in fp64. */
+int oracle_rht(const double *in, int64_t n, uint64_t seed, int inverse, double *out);
+/* Norm-based range: l = max_w ||x_w||_2, M = (t_p / sqrt(n)) l, m = -M (fp64). */
+void oracle_rht_norm_range(const double *const *x, int p, int64_t n, double t_p, double *m,
+                           double *M);
+
 /* ---------------- NMSE [T] ---------------- */
 double oracle_nmse(const float *x, const float *x_hat, int64_t n);
 double oracle_nmse_f64(const double *x, const double *x_hat, int64_t n);
