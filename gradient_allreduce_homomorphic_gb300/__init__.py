@@ -65,6 +65,11 @@ _SIGNATURES = {
     "gar_nuhc_aggregate": (C.c_int, [_pp, _i32, _i64, _i32, _vp, _vp, _vp]),
     "gar_nuhc_decode": (C.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _vp]),
     "gar_nuhc_allreduce_fused": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _vp, _u64, _vp, _vp, _pp, _vp]),
+    "gar_rht": (C.c_int, [_vp, _vp, _i64, _u64, _i32, _vp]),
+    "gar_rht_norm_range_workspace_bytes": (C.c_size_t, [_i32, _i64]),
+    "gar_rht_norm_range": (C.c_int, [_pp, _i32, _i64, C.c_double, _vp, _vp, C.c_size_t, _vp]),
+    "gar_ef_apply": (C.c_int, [_vp, _vp, _vp, _i64, _vp]),
+    "gar_ef_update": (C.c_int, [_vp, _vp, _vp, _i64, _vp]),
     "gar_nmse_workspace_bytes": (C.c_size_t, [_i64]),
     "gar_nmse": (C.c_int, [_vp, _vp, _i64, _vp, _vp, C.c_size_t, _vp]),
     "gar_nmse_noalloc": (C.c_int, [_vp, _vp, _i64, _vp, _vp]),
@@ -341,6 +346,31 @@ def gar_nuhc_allreduce_fused(x, b: int, g: int, table, seed: int, d_mM, avg, pac
     pk = pointer_table(packed).array if packed is not None else None
     _call("gar_nuhc_allreduce_fused", xt.array, len(xt), xt.numel, b, g, tp, seed, _dev(d_mM), _dev(avg), pk,
           _stream(stream))
+
+
+# ------------------------------------------- RHT, range and error feedback
+def gar_rht(x, out, seed: int, inverse: bool = False, stream=None):
+    """out = (1/sqrt n) H D x, or (1/sqrt n) D H x with inverse=True; out may be x."""
+    _call("gar_rht", _dev(x), _dev(out), x.numel(), seed, int(bool(inverse)), _stream(stream))
+
+
+def gar_rht_norm_range_workspace_bytes(P: int, n: int) -> int:
+    return int(load().gar_rht_norm_range_workspace_bytes(P, n))
+
+
+def gar_rht_norm_range(x, t_p: float, d_mM, workspace, stream=None):
+    t = pointer_table(x)
+    nbytes = workspace.numel() * workspace.element_size()
+    _call("gar_rht_norm_range", t.array, len(t), t.numel, float(t_p), _dev(d_mM), _dev(workspace), nbytes,
+          _stream(stream))
+
+
+def gar_ef_apply(grad, e, x, stream=None):
+    _call("gar_ef_apply", _dev(grad), _dev(e), _dev(x), grad.numel(), _stream(stream))
+
+
+def gar_ef_update(e, x, x_hat, stream=None):
+    _call("gar_ef_update", _dev(e), _dev(x), _dev(x_hat), e.numel(), _stream(stream))
 
 
 # -------------------------------------------------------------------- NMSE

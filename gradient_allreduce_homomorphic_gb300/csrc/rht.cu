@@ -1,0 +1,443 @@
+// rht.cu -- THC's pre- and post-processing ([T] section 5): the randomized
+// Hadamard transform (1/sqrt(n)) H D x and its inverse (1/sqrt(n)) D H y,
+// the norm-based range M = (t_p / sqrt(n)) max_w ||x_w||, m = -M, and the
+// error-feedback updates x = grad + e and e = x - x_hat.
+//
+// The fast Walsh-Hadamard transform of n = 2^k elements is k butterfly
+// stages ((a, b) -> (a + b, a - b) between elements whose indices differ in
+// one bit); stages on different bits commute, so they may run in any order.
+//
+// Stages on index bits 0..11 run inside 4096-element tiles (one read and one
+// write of HBM): a thread holds 16 elements (coalesced float4 loads give it
+// bits 0, 1, 10, 11 in registers), does those four stages in registers, and
+// two swizzled shared-memory transposes bring bits 2..5 and then 6..9 into
+// its registers.  Higher bits go in passes of up to eight: a CTA holds 256
+// rows of 16 consecutive elements, the rows 2^s apart (64-byte segments:
+// whole DRAM sectors), and does the row bits in two register rounds around
+// one transpose.  n = 2^24 takes three kernels, n = 2^20 two.
+//
+// The Rademacher signs D come from their own Philox stream (worker slot
+// 0xFFFFFFFF): one 128-bit block per 128 elements, bit i mod 128 for
+// element i.  The forward transform applies them as the first tile kernel
+// loads; the inverse applies them as the last kernel stores.
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace gar {
+namespace {
+
+constexpr int kTile = 4096;  // elements per tile / per pass block
+constexpr int kThreads = 256;
+constexpr uint32_t kSignSlot = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint4 sign_block(int64_t q, const PhiloxKeys &k) {
+    return philox10(make_uint4(static_cast<uint32_t>(q), static_cast<uint32_t>(static_cast<uint64_t>(q) >> 32),
+                               kSignSlot, 0u),
+                    k);
+}
+__device__ __forceinline__ uint32_t word_of(const uint4 &b, int w) {
+    return w == 0 ? b.x : (w == 1 ? b.y : (w == 2 ? b.z : b.w));
+}
+
+// Butterfly stages over v[0..15] on the register-index bits >= lo_bit.
+__device__ __forceinline__ void butterfly16(float (&v)[16], int lo_bit = 0) {
+#pragma unroll
+    for (int bit = 0; bit < 4; ++bit) {
+        if (bit < lo_bit) continue;
+        const int h = 1 << bit;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            if ((r & h) == 0) {
+                const float a = v[r], b = v[r + h];
+                v[r] = __fadd_rn(a, b);
+                v[r + h] = __fsub_rn(a, b);
+            }
+        }
+    }
+}
+
+struct RhtParams {
+    PhiloxKeys keys;
+    const float *in;
+    float *out;
+    int64_t n;
+    int32_t inverse;  // 0: (1/sqrt n) H D x;  1: (1/sqrt n) D H y
+    int32_t last;     // this launch writes the final values (scale, inverse signs)
+    int32_t s;        // pass: log2 of the row stride
+    int32_t lo_bit;   // pass: row bits below this were done by an earlier launch
+    float scale;      // 1/sqrt(n) rounded to fp32
+};
+
+// Tile shared-memory layout: element i of the tile lives at i ^ (bits 6..8
+// of i moved to bits 2..4).  Every warp access below then hits 32 distinct
+// banks, and 16-byte groups stay whole for the float4 stores.
+__device__ __forceinline__ int tile_swz(int i) { return i ^ (((i >> 6) & 7) << 2); }
+
+// Index bits 0..11 of every 4096-element tile.
+__global__ void __launch_bounds__(kThreads) rht_tile_kernel(const __grid_constant__ RhtParams p) {
+    __shared__ __align__(16) float s[kTile];
+    __shared__ uint32_t s_sign[kTile / 32];  // bit i: sign of tile element i (1 = negative)
+    const int t = threadIdx.x;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kTile;
+    const float4 *src = reinterpret_cast<const float4 *>(p.in + base);
+    float v[16];
+    // v[4q + j] = tile element (q << 10) | (t << 2) | j
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 a = __ldcs(src + q * 256 + t);
+        v[4 * q] = a.x;
+        v[4 * q + 1] = a.y;
+        v[4 * q + 2] = a.z;
+        v[4 * q + 3] = a.w;
+    }
+    const bool signs_in = !p.inverse;
+    const bool signs_out = p.inverse && p.last;
+    if (signs_in || signs_out) {
+        if (t < kTile / 128) {
+            const uint4 r = sign_block((base >> 7) + t, p.keys);
+            s_sign[4 * t] = r.x;
+            s_sign[4 * t + 1] = r.y;
+            s_sign[4 * t + 2] = r.z;
+            s_sign[4 * t + 3] = r.w;
+        }
+        __syncthreads();
+    }
+    if (signs_in) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t bits = s_sign[32 * q + (t >> 3)] >> (4 * (t & 7));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if ((bits >> j) & 1u) v[4 * q + j] = -v[4 * q + j];
+        }
+    }
+    butterfly16(v);  // bits 0, 1, 10, 11
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<float4 *>(&s[tile_swz((q << 10) | (t << 2))]) =
+            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    __syncthreads();
+    // bits 2..5 in registers: element (t & 3) | (r << 2) | ((t >> 2) << 6)
+    const int b1 = (t & 3) | ((t >> 2) << 6);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) v[r] = s[tile_swz(b1 | (r << 2))];
+    butterfly16(v);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) s[tile_swz(b1 | (r << 2))] = v[r];
+    __syncthreads();
+    // bits 6..9 in registers: element (t & 63) | (r << 6) | ((t >> 6) << 10)
+    const int b2 = (t & 63) | ((t >> 6) << 10);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) v[r] = s[tile_swz(b2 | (r << 6))];
+    butterfly16(v);
+    float *dst = p.out + base;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        const int e = b2 | (r << 6);
+        float y = v[r];
+        if (p.last) {
+            if (signs_out && ((s_sign[e >> 5] >> (e & 31)) & 1u)) y = -y;
+            y = __fmul_rn(y, p.scale);
+        }
+        __stcs(dst + e, y);
+    }
+}
+
+// Row bits [lo_bit, 8) of 256 rows 2^s apart (s >= 4), 16 columns each, in
+// place on p.out.  Block -> (hi, column block cb): element of (row m, column
+// c) = (hi << (s + 8)) | (m << s) | (cb << 4) | c.  Shared layout: row-major
+// m * 16 + c with bit 8 folded into bit 4 (conflict-free both rounds).
+__device__ __forceinline__ int pass_swz(int i) { return i ^ (((i >> 8) & 1) << 4); }
+
+__global__ void __launch_bounds__(kThreads) rht_pass_kernel(const __grid_constant__ RhtParams p) {
+    __shared__ float s[kTile];
+    const int t = threadIdx.x;
+    const int c = t & 15, mh = t >> 4;
+    const int64_t bid = blockIdx.x;
+    const int cb_bits = p.s - 4;
+    const int64_t cb = bid & ((int64_t{1} << cb_bits) - 1);
+    const int64_t hi = bid >> cb_bits;
+    float *x = p.out + ((hi << (p.s + 8)) | (cb << 4) | c);
+    float v[16];
+    // round 1: rows (mh << 4) | j
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __ldcs(x + (static_cast<int64_t>((mh << 4) | j) << p.s));
+    butterfly16(v, p.lo_bit);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) s[pass_swz((mh << 8) | (j << 4) | c)] = v[j];
+    __syncthreads();
+    // round 2: rows (j << 4) | mh
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = s[pass_swz((j << 8) | (mh << 4) | c)];
+    butterfly16(v, p.lo_bit > 4 ? p.lo_bit - 4 : 0);
+    if (p.last) {
+        if (p.inverse) {
+            // a half-warp's 16 columns share one sign word; lane L draws the word
+            // of row ((L & 15) << 4) | mh for its half-warp, the others read it
+            const int lane = t & 31;
+            const int mh_lane = ((t & ~31) >> 4) | (lane >> 4);
+            const int64_t e_lane = (hi << (p.s + 8)) | (cb << 4) |
+                                   (static_cast<int64_t>(((lane & 15) << 4) | mh_lane) << p.s);
+            const uint32_t mine = word_of(sign_block(e_lane >> 7, p.keys), static_cast<int>((e_lane >> 5) & 3));
+            const int bit = static_cast<int>(((cb & 1) << 4) | c);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const uint32_t w = __shfl_sync(0xFFFFFFFFu, mine, j | (lane & 16));
+                if ((w >> bit) & 1u) v[j] = -v[j];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], p.scale);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) __stcs(x + (static_cast<int64_t>((j << 4) | mh) << p.s), v[j]);
+}
+
+// n < 4096: one CTA, every stage in shared memory.
+__global__ void __launch_bounds__(kThreads) rht_small_kernel(const __grid_constant__ RhtParams p) {
+    __shared__ float s[kTile];
+    const int n = static_cast<int>(p.n);
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        float x = p.in[i];
+        if (!p.inverse && ((word_of(sign_block(i >> 7, p.keys), (i >> 5) & 3) >> (i & 31)) & 1u)) x = -x;
+        s[i] = x;
+    }
+    __syncthreads();
+    for (int h = 1; h < n; h <<= 1) {
+        for (int j = threadIdx.x; j < n / 2; j += kThreads) {
+            const int i = (j / h) * 2 * h + (j % h);
+            const float a = s[i], b = s[i + h];
+            s[i] = __fadd_rn(a, b);
+            s[i + h] = __fsub_rn(a, b);
+        }
+        __syncthreads();
+    }
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        float y = s[i];
+        if (p.inverse && ((word_of(sign_block(i >> 7, p.keys), (i >> 5) & 3) >> (i & 31)) & 1u)) y = -y;
+        p.out[i] = __fmul_rn(y, p.scale);
+    }
+}
+
+// ------------------------------------------------------------ norm range
+constexpr int kNormBlocksMax = 256;  // per worker
+
+struct NormParams {
+    const float *x[GAR_MAX_WORKERS];
+    double *ws;  // [P][blocks] partial sums of squares
+    float *mM;
+    int64_t n;
+    int32_t P;
+    int32_t blocks;
+    double t_over_sqrt_n;
+};
+
+__device__ __forceinline__ double block_sum(double v) {
+    __shared__ double s_v[kThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();  // s_v may still be read by a previous call
+    if (lane == 0) s_v[warp] = v;
+    __syncthreads();
+    v = 0.0;
+    if (warp == 0) {
+        v = lane < kThreads / 32 ? s_v[lane] : 0.0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    }
+    return v;  // valid in thread 0
+}
+
+__device__ __forceinline__ float sq4(const float4 &a) {
+    return __fadd_rn(__fadd_rn(__fmul_rn(a.x, a.x), __fmul_rn(a.y, a.y)), __fadd_rn(__fmul_rn(a.z, a.z), __fmul_rn(a.w, a.w)));
+}
+
+// Partial sums of squares: grid (blocks, P).  Terms are formed in fp32 four
+// at a time and accumulated in fp64 in a fixed order (deterministic).
+__global__ void __launch_bounds__(kThreads) rht_norm_partial(const __grid_constant__ NormParams p) {
+    const float *x = p.x[blockIdx.y];
+    double acc = 0.0;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    int64_t first = 0;
+    if ((reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+        const int64_t nv = p.n / 4;
+        for (int64_t i = tid; i < nv; i += stride)
+            acc += static_cast<double>(sq4(__ldcs(reinterpret_cast<const float4 *>(x) + i)));
+        first = nv * 4;
+    }
+    for (int64_t i = first + tid; i < p.n; i += stride) {
+        const float a = x[i];
+        acc += static_cast<double>(__fmul_rn(a, a));
+    }
+    acc = block_sum(acc);
+    if (threadIdx.x == 0) p.ws[static_cast<int64_t>(blockIdx.y) * p.blocks + blockIdx.x] = acc;
+}
+
+// max over workers of the summed partials -> (m, M)
+__global__ void __launch_bounds__(kThreads) rht_norm_final(const __grid_constant__ NormParams p) {
+    double best = 0.0;
+    for (int w = 0; w < p.P; ++w) {
+        double acc = 0.0;
+        for (int b = threadIdx.x; b < p.blocks; b += kThreads) acc += p.ws[static_cast<int64_t>(w) * p.blocks + b];
+        acc = block_sum(acc);
+        if (threadIdx.x == 0 && acc > best) best = acc;
+    }
+    if (threadIdx.x == 0) {
+        const float M = static_cast<float>(p.t_over_sqrt_n * sqrt(best));
+        p.mM[0] = -M;
+        p.mM[1] = M;
+    }
+}
+
+int norm_blocks(int64_t n) {
+    int64_t b = ceil_div(n, 4 * 2048);
+    if (b > kNormBlocksMax) b = kNormBlocksMax;
+    return static_cast<int>(b < 1 ? 1 : b);
+}
+
+// ---------------------------------------------------------- error feedback
+// out = a + b (Sub = false) or a - b (Sub = true), one rounding each.
+template <bool Sub>
+__device__ __forceinline__ float ef_op(float a, float b) {
+    return Sub ? __fsub_rn(a, b) : __fadd_rn(a, b);
+}
+
+template <bool Sub>
+__global__ void __launch_bounds__(kThreads) ef_kernel(const float *a, const float *b, float *out, int64_t n, int vec) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    int64_t first = 0;
+    if (vec) {
+        const int64_t nv = n / 4;
+        for (int64_t i = tid; i < nv; i += stride) {
+            const float4 u = __ldcs(reinterpret_cast<const float4 *>(a) + i);
+            const float4 w = __ldcs(reinterpret_cast<const float4 *>(b) + i);
+            __stcs(reinterpret_cast<float4 *>(out) + i, make_float4(ef_op<Sub>(u.x, w.x), ef_op<Sub>(u.y, w.y),
+                                                                    ef_op<Sub>(u.z, w.z), ef_op<Sub>(u.w, w.w)));
+        }
+        first = nv * 4;
+    }
+    for (int64_t i = first + tid; i < n; i += stride) out[i] = ef_op<Sub>(a[i], b[i]);
+}
+
+int ew_grid(int64_t items) {
+    int64_t g = static_cast<int64_t>(sm_count()) * 8;
+    const int64_t need = ceil_div(items, kThreads);
+    if (g > need) g = need;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+bool overlaps(const void *a, const void *b, int64_t bytes) {
+    const char *x = static_cast<const char *>(a), *y = static_cast<const char *>(b);
+    return x < y + bytes && y < x + bytes;
+}
+
+}  // namespace
+}  // namespace gar
+
+using namespace gar;
+
+extern "C" int gar_rht(const float *in, float *out, int64_t n, uint64_t seed, int32_t inverse, gar_stream_t stream_) {
+    if (n < 1 || (n & (n - 1)) != 0) return fail(GAR_EINVAL, "n=%lld is not a power of two", static_cast<long long>(n));
+    if (n > (int64_t{1} << 31)) return fail(GAR_EINVAL, "n=%lld above 2^31", static_cast<long long>(n));
+    if (!in || !out) return fail(GAR_EINVAL, "in or out is NULL");
+    if (inverse != 0 && inverse != 1) return fail(GAR_EINVAL, "inverse must be 0 or 1");
+    if (!aligned(in, 16) || !aligned(out, 16)) return fail(GAR_EALIGN, "in and out must be 16-byte aligned");
+    if (in != out && overlaps(in, out, n * 4)) return fail(GAR_EINVAL, "in and out overlap without being equal");
+    RhtParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.keys = philox_keys(seed);
+    p.in = in;
+    p.out = out;
+    p.n = n;
+    p.inverse = inverse;
+    p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(n)));
+    int k = 0;
+    while ((int64_t{1} << k) < n) ++k;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (n < kTile) {
+        p.last = 1;
+        rht_small_kernel<<<1, kThreads, 0, stream>>>(p);
+        return check_launch("rht_small_kernel");
+    }
+    const unsigned blocks = static_cast<unsigned>(n / kTile);
+    p.last = k == 12 ? 1 : 0;
+    rht_tile_kernel<<<blocks, kThreads, 0, stream>>>(p);
+    int rc = check_launch("rht_tile_kernel");
+    // bits 12.. in passes of eight; a pass that would run past bit k-1 is
+    // moved down (s = k - 8) and skips the row bits already done
+    for (int done = 12; done < k && rc == GAR_OK;) {
+        p.s = done < k - 8 ? done : k - 8;
+        p.lo_bit = done - p.s;
+        p.last = p.s + 8 >= k ? 1 : 0;
+        rht_pass_kernel<<<blocks, kThreads, 0, stream>>>(p);
+        rc = check_launch("rht_pass_kernel");
+        done = p.s + 8;
+    }
+    return rc;
+}
+
+extern "C" size_t gar_rht_norm_range_workspace_bytes(int32_t P, int64_t n) {
+    if (P < 1 || P > GAR_MAX_WORKERS || n < 0) return 0;
+    return static_cast<size_t>(P) * static_cast<size_t>(norm_blocks(n)) * sizeof(double);
+}
+
+extern "C" int gar_rht_norm_range(const float *const *x, int32_t P, int64_t n, double t_p, float *d_mM,
+                                  void *d_workspace, size_t workspace_bytes, gar_stream_t stream_) {
+    if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
+    if (n < 1) return fail(GAR_EINVAL, "n=%lld < 1", static_cast<long long>(n));
+    if (!x || !d_mM || !d_workspace) return fail(GAR_EINVAL, "NULL argument");
+    if (!(t_p > 0.0) || !std::isfinite(t_p)) return fail(GAR_EINVAL, "t_p must be positive and finite");
+    const size_t need = gar_rht_norm_range_workspace_bytes(P, n);
+    if (workspace_bytes < need) return fail(GAR_EINVAL, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+    if (!aligned(d_workspace, 8) || !aligned(d_mM, 4)) return fail(GAR_EALIGN, "misaligned workspace or d_mM");
+    NormParams p;
+    std::memset(&p, 0, sizeof(p));
+    for (int w = 0; w < P; ++w) {
+        if (!x[w]) return fail(GAR_EINVAL, "input %d is NULL", w);
+        if (!aligned(x[w], 4)) return fail(GAR_EALIGN, "input %d not 4-byte aligned", w);
+        p.x[w] = x[w];
+    }
+    p.ws = static_cast<double *>(d_workspace);
+    p.mM = d_mM;
+    p.n = n;
+    p.P = P;
+    p.blocks = norm_blocks(n);
+    p.t_over_sqrt_n = t_p / std::sqrt(static_cast<double>(n));
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    rht_norm_partial<<<dim3(static_cast<unsigned>(p.blocks), static_cast<unsigned>(P)), kThreads, 0, stream>>>(p);
+    int rc = check_launch("rht_norm_partial");
+    if (rc) return rc;
+    rht_norm_final<<<1, kThreads, 0, stream>>>(p);
+    return check_launch("rht_norm_final");
+}
+
+static int ef_launch(const float *a, const float *b, float *out, int64_t n, int subtract, gar_stream_t stream_) {
+    if (n < 0) return fail(GAR_EINVAL, "n < 0");
+    if (n == 0) return GAR_OK;
+    if (!a || !b || !out) return fail(GAR_EINVAL, "NULL argument");
+    if (!aligned(a, 4) || !aligned(b, 4) || !aligned(out, 4)) return fail(GAR_EALIGN, "pointer not 4-byte aligned");
+    // out may be a or b exactly (each element is read before the same thread writes it)
+    if ((out != a && overlaps(out, a, n * 4)) || (out != b && overlaps(out, b, n * 4)))
+        return fail(GAR_EINVAL, "output overlaps an input without being equal to it");
+    const int vec = aligned(a, 16) && aligned(b, 16) && aligned(out, 16);
+    const int grid = ew_grid(vec ? ceil_div(n, 4) : n);
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (subtract)
+        ef_kernel<true><<<grid, kThreads, 0, stream>>>(a, b, out, n, vec);
+    else
+        ef_kernel<false><<<grid, kThreads, 0, stream>>>(a, b, out, n, vec);
+    return check_launch("ef_kernel");
+}
+
+extern "C" int gar_ef_apply(const float *grad, const float *e, float *x, int64_t n, gar_stream_t stream) {
+    return ef_launch(grad, e, x, n, 0, stream);
+}
+
+extern "C" int gar_ef_update(float *e, const float *x, const float *x_hat, int64_t n, gar_stream_t stream) {
+    return ef_launch(x, x_hat, e, n, 1, stream);
+}

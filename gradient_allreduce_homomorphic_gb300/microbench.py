@@ -144,6 +144,24 @@ def main(argv=None):
             out = torch.empty(1, dtype=torch.float64, device=dev)
             fn = lambda: g.gar_nmse(x[0], x[1], out, ws)  # noqa: E731
             nbytes = 2 * N * 4
+    elif a.case in ("rht", "rht_inv", "rht_inplace", "rht_norm", "ef_apply"):
+        # algorithmic bytes: one read and one write of the vector (rht), P reads (norm), 2 reads + 1 write (ef)
+        x = bufs(N, max(P, 2), torch.float32)
+        y = torch.empty(N, device=dev)
+        if a.case == "rht_norm":
+            ws = torch.empty(g.gar_rht_norm_range_workspace_bytes(P, N) // 8, dtype=torch.float64, device=dev)
+            mM = torch.empty(2, device=dev)
+            xt = g.pointer_table(x[:P])
+            fn = lambda: g.gar_rht_norm_range(xt, 2.15, mM, ws)  # noqa: E731
+            nbytes = P * N * 4
+        elif a.case == "ef_apply":
+            fn = lambda: g.gar_ef_apply(x[0], x[1], y)  # noqa: E731
+            nbytes = 3 * N * 4
+        else:
+            src, dst = (y, y) if a.case == "rht_inplace" else (x[0], y)
+            inv = a.case == "rht_inv"
+            fn = lambda: g.gar_rht(src, dst, 7, inverse=inv)  # noqa: E731
+            nbytes = 2 * N * 4
     else:
         raise SystemExit(f"unknown case {a.case}")
 

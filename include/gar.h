@@ -338,6 +338,60 @@ int gar_nuhc_allreduce_fused(const float *const *x, int32_t P, int64_t N, int32_
                              uint32_t *const *packed, gar_stream_t stream);
 
 /* ===================================================================== */
+/* Pre- and post-processing [T] section 5 (RHT, truncation, error feedback) */
+/* ===================================================================== */
+/* Before non-uniform THC each worker adds its error-feedback vector to its
+ * gradient (x = grad + e), rotates it with the randomized Hadamard transform
+ * and quantizes against the range [-M, M] set from the largest worker norm
+ * (values outside are clamped: the truncation).  After the decode each
+ * worker applies the inverse rotation to the average estimate and updates
+ * e.  Every worker draws the same D (same seed).  Vectors whose length is
+ * not a power of two are zero-padded to one by the caller. */
+
+/* gar_rht -- out = (1/sqrt(n)) H D in (inverse = 0) or
+ * out = (1/sqrt(n)) D H in (inverse = 1), H the n x n Sylvester-Hadamard
+ * matrix, D = diag(d), d_i = -1 when bit (i mod 128) of the Philox4x32-10
+ * block with key (seed low, seed high) and counter (i/128 low, i/128 high,
+ * 0xFFFFFFFF, 0) is set (word (i/32) mod 4, bit i mod 32), else +1.
+ * in, out: device, n fp32, 16-byte aligned, caller-owned; out == in runs in
+ * place, any other overlap is rejected.  n: a power of two, 1 <= n <= 2^31.
+ * fp32 butterflies (a + b, a - b), the 1/sqrt(n) factor (rounded to fp32)
+ * applied once at the end: each output is within about
+ * (log2 n + 2) 2^-24 ||in|| of the exact value.  Kernels: n < 4096 one CTA;
+ * else one 4096-element tile pass plus ceil((log2 n - 12) / 8) strided
+ * passes, each one read and one write of the vector.
+ * Errors: GAR_EINVAL (n not a power of two or above 2^31, NULL, bad inverse,
+ * partial overlap), GAR_EALIGN, GAR_ECUDA. */
+int gar_rht(const float *in, float *out, int64_t n, uint64_t seed, int32_t inverse,
+            gar_stream_t stream);
+
+/* Bytes of device workspace gar_rht_norm_range needs (0 for bad P or n). */
+size_t gar_rht_norm_range_workspace_bytes(int32_t P, int64_t n);
+
+/* gar_rht_norm_range -- the range of the rotated vectors without rotating
+ * them first (the rotation keeps norms): l = max over workers of ||x_w||_2,
+ * d_mM[0] = -M, d_mM[1] = M with M = (t_p / sqrt(n)) l, rounded to fp32.
+ * x: host array of P device pointers to n fp32 each (4-byte aligned).
+ * t_p > 0: the truncation threshold for a p fraction outside,
+ * Phi^-1(1 - p/2).  d_mM: device, two floats.  Squares are formed in fp32
+ * (four summed pairwise) and accumulated in fp64 in a fixed order
+ * (deterministic; relative error below 1e-6).  d_workspace: device, 8-byte
+ * aligned, caller-owned, not shared with a concurrent call.
+ * Errors: GAR_EINVAL (P outside [1, 64], n < 1, NULL, t_p not positive,
+ * workspace too small), GAR_EALIGN, GAR_ECUDA. */
+int gar_rht_norm_range(const float *const *x, int32_t P, int64_t n, double t_p, float *d_mM,
+                       void *d_workspace, size_t workspace_bytes, gar_stream_t stream);
+
+/* gar_ef_apply -- x = grad + e, elementwise fp32 (one rounding).
+ * gar_ef_update -- e = x - x_hat, elementwise fp32, where x_hat is the value
+ * this worker's x came back as (its own quantized vector, decoded and
+ * inverse-rotated).  Device pointers, n fp32 each, 4-byte aligned; the
+ * output may be one of the inputs exactly, any other overlap is rejected;
+ * n = 0 is a no-op.  Errors: GAR_EINVAL, GAR_EALIGN, GAR_ECUDA. */
+int gar_ef_apply(const float *grad, const float *e, float *x, int64_t n, gar_stream_t stream);
+int gar_ef_update(float *e, const float *x, const float *x_hat, int64_t n, gar_stream_t stream);
+
+/* ===================================================================== */
 /* NMSE [T] section 2: ||x - x_hat||^2 / ||x||^2                          */
 /* ===================================================================== */
 
