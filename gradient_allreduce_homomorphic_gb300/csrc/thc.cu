@@ -9,11 +9,11 @@
 //
 // Index decision in fp32 (shared by encode and fused; one rounding per op):
 //   t = clamp((x - m) * sc, 0, L),  sc = L / (M - m)  (0 when M == m)
-//   floor: jm = t + 2^23 rounded down  ->  bits(jm) = 0x4B000000 + floor(t)
-//   f = t - (jm - 2^23)                  (exact)
-//   up iff u < f with u = (r mod 2^23) / 2^23; tested as
-//        1 + u  <  (1 + f) rounded up to the 2^-23 grid
-//   (both sides are exact: 1 + u is the float with mantissa r mod 2^23).
+//   floor: jm = t + 2^23 rounded down  ->  bits(jm) = 0x4B000000 + j, j = floor(t)
+//   up iff u < f = t - j with u = (r mod 2^23) / 2^23.  Since t is a float,
+//   j + u < t exactly iff (j + u rounded down) < t; j + u is formed as
+//   (jm - (2^23 + 1)) + (1 + u), where jm - (2^23 + 1) = j - 1 is exact and
+//   1 + u is the float with mantissa r mod 2^23.
 // No integer<->float conversion is needed per element.
 #include <cstring>
 
@@ -34,16 +34,25 @@ __device__ __forceinline__ uint32_t index_biased(float x, float m, float sc, flo
     float t = __fmul_rn(__fsub_rn(x, m), sc);
     t = fminf(fmaxf(t, 0.0f), L);
     const float jm = __fadd_rd(t, 8388608.0f);
-    const float f = __fsub_rn(t, __fsub_rn(jm, 8388608.0f));
-    const float f1 = __fadd_ru(f, 1.0f);
+    const float j_minus_1 = __fsub_rn(jm, 8388609.0f);
     const float one_u = __uint_as_float((r & 0x007FFFFFu) | 0x3F800000u);
-    return __float_as_uint(jm) + (one_u < f1 ? 1u : 0u);
+    return __float_as_uint(jm) + (__fadd_rd(j_minus_1, one_u) < t ? 1u : 0u);
 }
 
 __device__ __forceinline__ uint4 philox_block(int64_t q, int worker, const PhiloxKeys &k) {
     return philox10(make_uint4(static_cast<uint32_t>(q), static_cast<uint32_t>(static_cast<uint64_t>(q) >> 32),
                                static_cast<uint32_t>(worker), 0u),
                     k);
+}
+
+// Sum over the 32/B fields of a packed word of (0x4B000000 << field shift),
+// mod 2^32: packing the biased indices with plain shifted adds and removing
+// this once leaves the exact word (the fields never overlap).
+template <int B>
+__host__ __device__ constexpr uint32_t pack_bias() {
+    uint32_t s = 0;
+    for (int i = 0; i < 32 / B; ++i) s += 0x4B000000u << (i * B);
+    return s;
 }
 
 __device__ __forceinline__ uint32_t pick(const uint4 &r, int i) {
@@ -312,6 +321,36 @@ struct FusedParams {
     float fp;
 };
 
+// One worker's contribution to a word of E = 4G elements: Philox draws,
+// indices added to the running sums s, the packed word stored if wanted.
+template <int B, bool kPacked, int G>
+__device__ __forceinline__ void fused_one_worker(const float4 (&v)[G], uint32_t (&s)[4 * G], int64_t e0, int64_t w,
+                                                 int wk, const FusedParams &p, float m, float sc) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const uint4 r = philox_block((e0 >> 2) + g, p.wid[wk], p.keys);
+        const uint32_t a0 = index_biased(v[g].x, m, sc, p.L, r.x);
+        const uint32_t a1 = index_biased(v[g].y, m, sc, p.L, r.y);
+        const uint32_t a2 = index_biased(v[g].z, m, sc, p.L, r.z);
+        const uint32_t a3 = index_biased(v[g].w, m, sc, p.L, r.w);
+        s[4 * g] += a0;
+        s[4 * g + 1] += a1;
+        s[4 * g + 2] += a2;
+        s[4 * g + 3] += a3;
+        if (kPacked)
+            word += (a0 << (4 * g * B)) + (a1 << ((4 * g + 1) * B)) + (a2 << ((4 * g + 2) * B)) +
+                    (a3 << ((4 * g + 3) * B));
+    }
+    if (kPacked) __stcs(p.packed[wk] + w, word - pack_bias<B>());
+}
+
+template <int G>
+__device__ __forceinline__ void load_worker(float4 (&v)[G], const FusedParams &p, int wk, int64_t e0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) v[g] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk] + e0) + g);
+}
+
 template <int B, bool kPacked>
 __global__ void __launch_bounds__(kThreads) thc_fused_kernel(const __grid_constant__ FusedParams p) {
     constexpr int E = 32 / B;
@@ -328,35 +367,16 @@ __global__ void __launch_bounds__(kThreads) thc_fused_kernel(const __grid_consta
 #pragma unroll
         for (int i = 0; i < E; ++i) s[i] = 0;
         if (p.vec && e0 + E <= p.N) {
-            float4 cur[G], nxt[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) cur[g] = __ldcs(reinterpret_cast<const float4 *>(p.x[0] + e0) + g);
-            for (int wk = 0; wk < p.P; ++wk) {
-                if (wk + 1 < p.P) {  // next worker's loads in flight while this one is quantized
-#pragma unroll
-                    for (int g = 0; g < G; ++g) nxt[g] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk + 1] + e0) + g);
-                }
-                uint32_t word = 0;
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const uint4 r = philox_block((e0 >> 2) + g, p.wid[wk], p.keys);
-                    const uint32_t a0 = index_biased(cur[g].x, m, sc, p.L, r.x);
-                    const uint32_t a1 = index_biased(cur[g].y, m, sc, p.L, r.y);
-                    const uint32_t a2 = index_biased(cur[g].z, m, sc, p.L, r.z);
-                    const uint32_t a3 = index_biased(cur[g].w, m, sc, p.L, r.w);
-                    s[4 * g] += a0;
-                    s[4 * g + 1] += a1;
-                    s[4 * g + 2] += a2;
-                    s[4 * g + 3] += a3;
-                    if (kPacked) {
-                        word |= ((a0 - 0x4B000000u) | ((a1 - 0x4B000000u) << B) | ((a2 - 0x4B000000u) << (2 * B)) |
-                                 ((a3 - 0x4B000000u) << (3 * B)))
-                                << (4 * g * B);
-                    }
-                }
-                if (kPacked) __stcs(p.packed[wk] + w, word);
-#pragma unroll
-                for (int g = 0; g < G; ++g) cur[g] = nxt[g];
+            // two register buffers, the worker loop unrolled by two: one worker's
+            // loads are in flight while the other is quantized, with no copies
+            float4 va[G], vb[G];
+            load_worker(va, p, 0, e0);
+            for (int wk = 0; wk < p.P; wk += 2) {
+                const bool has1 = wk + 1 < p.P;
+                if (has1) load_worker(vb, p, wk + 1, e0);
+                fused_one_worker<B, kPacked>(va, s, e0, w, wk, p, m, sc);
+                if (wk + 2 < p.P) load_worker(va, p, wk + 2, e0);
+                if (has1) fused_one_worker<B, kPacked>(vb, s, e0, w, wk + 1, p, m, sc);
             }
             float4 *dst = reinterpret_cast<float4 *>(p.avg + e0);
 #pragma unroll

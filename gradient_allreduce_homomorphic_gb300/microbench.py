@@ -98,7 +98,7 @@ def main(argv=None):
                             g.gar_fusion_unpack(fbs[w][bb], plan, bb, tabs[w])
 
             nbytes = P * (n + int(plan.buf_numel.sum())) * 4 if a.case == "pack" else 2 * P * n * 4
-    elif a.case.startswith("thc") or a.case == "nmse":
+    elif a.case.startswith(("thc", "nuhc")) or a.case == "nmse":
         x = bufs(N, P, torch.float32)
         mM = torch.empty(2, device=dev)
         g.gar_thc_range(x, mM)
