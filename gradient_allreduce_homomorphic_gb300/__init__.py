@@ -50,6 +50,7 @@ _SIGNATURES = {
     "gar_fusion_unpack": (C.c_int, [_vp, _vp, _vp, _i32, _i32, _pp, _vp]),
     "gar_fused_allreduce": (C.c_int, [_pp, _pp, _i32, _vp, _vp, _i32, _vp, _i32, _i32, _vp]),
     "gar_fusion_pack_all": (C.c_int, [_pp, _i32, _vp, _vp, _i32, _pp, _vp, _i32, _vp, _vp]),
+    "gar_fused_allreduce_range": (C.c_int, [_pp, _pp, _i32, _vp, _vp, _i32, _vp, _i32, _i32, _vp, _vp]),
     "gar_ring_allreduce_sim": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _vp]),
     "gar_ring_allreduce_sim_out": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _pp, _i32, _vp]),
     "gar_ring_allreduce_bidir": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _vp]),
@@ -61,6 +62,8 @@ _SIGNATURES = {
     "gar_thc_decode": (C.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _vp]),
     "gar_thc_allreduce_fused": (C.c_int, [_pp, _i32, _i64, _i32, _u64, _vp, _vp, _pp, _vp]),
     "gar_thc_allreduce_fused_masked": (C.c_int, [_pp, _i32, _u64, _i64, _i32, _u64, _vp, _vp, _pp, _vp]),
+    "gar_thc_allreduce_fused_plan": (C.c_int, [_pp, _i32, _vp, _vp, _i32, _vp, _i32, _i32, _u64, _vp, _pp, _pp,
+                                               _vp]),
     "gar_nuhc_encode": (C.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _u64, _i32, _vp, _vp]),
     "gar_nuhc_aggregate": (C.c_int, [_pp, _i32, _i64, _i32, _vp, _vp, _vp]),
     "gar_nuhc_decode": (C.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _vp]),
@@ -252,6 +255,15 @@ def gar_fused_allreduce(src, dst, plan: FusionPlan, op: int = GAR_AVG, stream=No
           plan.buf_numel.ctypes.data, plan.n_buffers, op, _stream(stream))
 
 
+def gar_fused_allreduce_range(src, dst, plan: FusionPlan, d_mM, op: int = GAR_AVG, stream=None, tables=None):
+    """gar_fused_allreduce that also writes each buffer's THC range [m, M]
+    (d_mM: [n_buffers, 2] fp32 device tensor) from the same reads."""
+    P = len(src)
+    s, d = tables if tables is not None else fused_pointer_tables(src, dst)
+    _call("gar_fused_allreduce_range", s.array, d.array, P, C.addressof(plan.segs), plan.dtype.ctypes.data,
+          plan.count, plan.buf_numel.ctypes.data, plan.n_buffers, op, _dev(d_mM), _stream(stream))
+
+
 # ----------------------------------------------------------- ring all-reduce
 def gar_ring_allreduce_sim(bufs, op: int = GAR_AVG, stream=None):
     t = pointer_table(bufs)
@@ -317,6 +329,26 @@ def gar_thc_allreduce_fused_masked(x, arrived: int, b: int, seed: int, d_mM, avg
     pk = pointer_table(packed, allow_none=True).array if packed is not None else None
     _call("gar_thc_allreduce_fused_masked", xt.array, len(xt), arrived, xt.numel, b, seed, _dev(d_mM), _dev(avg),
           pk, _stream(stream))
+
+
+def thc_plan_tables(src, out, packed=None):
+    """Host pointer tables for gar_thc_allreduce_fused_plan (reuse them across steps):
+    src[w][i] worker w's tensor i, out[i] output tensor i, packed[w][b] or None."""
+    return (PtrTable([t for row in src for t in row]), PtrTable(out),
+            PtrTable([t for row in packed for t in row]) if packed is not None else None)
+
+
+def gar_thc_allreduce_fused_plan(src, plan: FusionPlan, b: int, seed: int, d_mM, out, packed=None, stream=None,
+                                 tables=None):
+    """Uniform THC of every fusion buffer of `plan`, reading the workers'
+    tensors src[w][i] directly and writing the average to out[i]; d_mM is the
+    [n_buffers, 2] per-buffer range; packed[w][b] optionally receives worker
+    w's indices of buffer b."""
+    s, o, pk = tables if tables is not None else thc_plan_tables(src, out, packed)
+    P = len(s) // max(plan.count, 1)
+    _call("gar_thc_allreduce_fused_plan", s.array, P, C.addressof(plan.segs), plan.dtype.ctypes.data, plan.count,
+          plan.buf_numel.ctypes.data, plan.n_buffers, b, seed, _dev(d_mM), o.array,
+          pk.array if pk is not None else None, _stream(stream))
 
 
 # --------------------------------------------------------- non-uniform THC
@@ -390,4 +422,4 @@ def gar_nmse_noalloc(x, x_hat, d_out, stream=None):
 
 
 __all__ = [n for n in dir() if n.startswith(("gar_", "GAR_"))] + ["GarError", "FusionPlan", "PtrTable", "load",
-                                                                    "pointer_table", "fused_pointer_tables"]
+                                                                    "pointer_table", "fused_pointer_tables", "thc_plan_tables"]

@@ -591,9 +591,9 @@ extern "C" int gar_fusion_pack_all(const void *const *src, int32_t P, const gar_
     return rc;
 }
 
-extern "C" int gar_fused_allreduce(const void *const *src, void *const *dst, int32_t P, const gar_seg *segs,
-                                   const int32_t *dtype, int32_t count, const int64_t *buf_numel, int32_t n_buffers,
-                                   int32_t op, gar_stream_t stream) {
+static int fused_allreduce_entry(const void *const *src, void *const *dst, int32_t P, const gar_seg *segs,
+                                 const int32_t *dtype, int32_t count, const int64_t *buf_numel, int32_t n_buffers,
+                                 int32_t op, float *d_mM, gar_stream_t stream) {
     if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
     if (op != GAR_SUM && op != GAR_AVG) return fail(GAR_EINVAL, "unknown op %d", op);
     if (count < 0 || n_buffers < 0) return fail(GAR_EINVAL, "count or n_buffers < 0");
@@ -607,6 +607,7 @@ extern "C" int gar_fused_allreduce(const void *const *src, void *const *dst, int
         if (es < 0) return fail(GAR_EDTYPE, "tensor %d has unknown dtype %d", i, dtype[i]);
         if (s.buffer < 0 || s.buffer >= n_buffers) return fail(GAR_EINVAL, "tensor %d has buffer id %d", i, s.buffer);
         if (buf_dt[s.buffer] >= 0 && buf_dt[s.buffer] != dtype[i]) return fail(GAR_EDTYPE, "buffer %d mixes dtypes", s.buffer);
+        if (d_mM && dtype[i] != GAR_F32) return fail(GAR_EDTYPE, "a range is only computed over fp32 buffers");
         buf_dt[s.buffer] = dtype[i];
         if (s.numel < 0 || s.offset < cursor[s.buffer] || s.offset + s.numel > buf_numel[s.buffer])
             return fail(GAR_EINVAL, "tensor %d does not lie in order inside buffer %d", i, s.buffer);
@@ -619,6 +620,20 @@ extern "C" int gar_fused_allreduce(const void *const *src, void *const *dst, int
             if (!aligned(sp, es) || !aligned(dp, es)) return fail(GAR_EALIGN, "worker %d tensor %d not aligned", w, i);
         }
     }
-    return fused_allreduce_impl(src, dst, P, segs, dtype, count, buf_numel, n_buffers, op,
+    if (d_mM && !aligned(d_mM, 4)) return fail(GAR_EALIGN, "d_mM not 4-byte aligned");
+    return fused_allreduce_impl(src, dst, P, segs, dtype, count, buf_numel, n_buffers, op, d_mM,
                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gar_fused_allreduce(const void *const *src, void *const *dst, int32_t P, const gar_seg *segs,
+                                   const int32_t *dtype, int32_t count, const int64_t *buf_numel, int32_t n_buffers,
+                                   int32_t op, gar_stream_t stream) {
+    return fused_allreduce_entry(src, dst, P, segs, dtype, count, buf_numel, n_buffers, op, nullptr, stream);
+}
+
+extern "C" int gar_fused_allreduce_range(const void *const *src, void *const *dst, int32_t P, const gar_seg *segs,
+                                         const int32_t *dtype, int32_t count, const int64_t *buf_numel,
+                                         int32_t n_buffers, int32_t op, float *d_mM, gar_stream_t stream) {
+    if (!d_mM && count > 0) return fail(GAR_EINVAL, "d_mM is NULL");
+    return fused_allreduce_entry(src, dst, P, segs, dtype, count, buf_numel, n_buffers, op, d_mM, stream);
 }

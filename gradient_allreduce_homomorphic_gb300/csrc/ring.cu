@@ -33,6 +33,10 @@ constexpr int kThreads = 256;
 constexpr int kUnroll = 2;
 constexpr int kTileUnits = kThreads * kUnroll;
 constexpr int kLoadBatch = 8;  // worker vectors in flight per thread before folding
+#ifndef GAR_RING_RANGE_MIN_BLOCKS
+#define GAR_RING_RANGE_MIN_BLOCKS 4
+#endif
+constexpr int kRangeMinBlocks = GAR_RING_RANGE_MIN_BLOCKS;  // CTAs per SM the range variant is built for
 
 template <typename T>
 struct Elem;
@@ -93,9 +97,23 @@ __device__ __forceinline__ int ring_worker(int c, int k, int ccw, int P) {
     return w;
 }
 
+// min / max over every input value seen, for the THC range of a fusion buffer
+// (fminf / fmaxf: NaN inputs are skipped, as in the packing kernel)
+struct Range {
+    float lo, hi;
+    __device__ __forceinline__ Range() {
+        lo = __int_as_float(0x7F800000);   // +inf
+        hi = __int_as_float(0xFF800000u);  // -inf
+    }
+    __device__ __forceinline__ void add(float v) {
+        lo = fminf(lo, v);
+        hi = fmaxf(hi, v);
+    }
+};
+
 // Fold one 16-byte vector at element e of row `row`, ring order from worker c.
-template <typename T, class Prm>
-__device__ __forceinline__ void fold_vec(const Prm &p, int row, int c, int ccw, int64_t e) {
+template <typename T, bool kRange, class Prm>
+__device__ __forceinline__ void fold_vec(const Prm &p, int row, int c, int ccw, int64_t e, Range &rg) {
     constexpr int V = Elem<T>::kVec;
     const int P = p.P;
     const void *const *src = p.src + static_cast<int64_t>(row) * P;
@@ -114,6 +132,10 @@ __device__ __forceinline__ void fold_vec(const Prm &p, int row, int c, int ccw, 
             if (k0 + j < P) {
                 float v[V];
                 Elem<T>::unpack(raw[j], v);
+                if (kRange) {
+#pragma unroll
+                    for (int q = 0; q < V; ++q) rg.add(v[q]);
+                }
                 if (k0 + j == 0) {
 #pragma unroll
                     for (int q = 0; q < V; ++q) acc[q] = v[q];
@@ -131,22 +153,68 @@ __device__ __forceinline__ void fold_vec(const Prm &p, int row, int c, int ccw, 
     for (int k = 0; k < p.n_out; ++k) st16(static_cast<T *>(dst[k]) + e, out);
 }
 
-template <typename T, class Prm>
-__device__ __forceinline__ void fold_one(const Prm &p, int row, int c, int ccw, int64_t e) {
+template <typename T, bool kRange, class Prm>
+__device__ __forceinline__ void fold_one(const Prm &p, int row, int c, int ccw, int64_t e, Range &rg) {
     const int P = p.P;
     const void *const *src = p.src + static_cast<int64_t>(row) * P;
     float acc = Elem<T>::load1(src[c], e);
+    if (kRange) rg.add(acc);
     for (int k = 1; k < P; ++k) {
-        acc = __fadd_rn(acc, Elem<T>::load1(src[ring_worker(c, k, ccw, P)], e));
+        const float v = Elem<T>::load1(src[ring_worker(c, k, ccw, P)], e);
+        if (kRange) rg.add(v);
+        acc = __fadd_rn(acc, v);
     }
     acc = finish(p, acc);
     void *const *dst = p.dst + static_cast<int64_t>(row) * p.n_out;
     for (int k = 0; k < p.n_out; ++k) Elem<T>::store1(dst[k], e, acc);
 }
 
-template <typename T, class Prm>
-__global__ void __launch_bounds__(kThreads) ring_fold_kernel(const __grid_constant__ Prm p) {
+__device__ __forceinline__ void atomic_min_f(float *a, float v) {
+    if ((__float_as_uint(v) >> 31) == 0u) atomicMin(reinterpret_cast<int *>(a), __float_as_int(v));
+    else atomicMax(reinterpret_cast<unsigned int *>(a), __float_as_uint(v));
+}
+__device__ __forceinline__ void atomic_max_f(float *a, float v) {
+    if ((__float_as_uint(v) >> 31) == 0u) atomicMax(reinterpret_cast<int *>(a), __float_as_int(v));
+    else atomicMin(reinterpret_cast<unsigned int *>(a), __float_as_uint(v));
+}
+
+// Block-wide min / max of rg merged into range[slot] (one pair of atomics).
+__device__ __forceinline__ void flush_range(Range rg, float *range, int slot) {
+    __shared__ float s_lo[kThreads / 32], s_hi[kThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        rg.lo = fminf(rg.lo, __shfl_xor_sync(0xFFFFFFFFu, rg.lo, o));
+        rg.hi = fmaxf(rg.hi, __shfl_xor_sync(0xFFFFFFFFu, rg.hi, o));
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();  // an earlier flush's readers are done with s_lo / s_hi
+    if (lane == 0) {
+        s_lo[warp] = rg.lo;
+        s_hi[warp] = rg.hi;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        rg.lo = lane < kThreads / 32 ? s_lo[lane] : __int_as_float(0x7F800000);
+        rg.hi = lane < kThreads / 32 ? s_hi[lane] : __int_as_float(0xFF800000u);
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) {
+            rg.lo = fminf(rg.lo, __shfl_xor_sync(0xFFFFFFFFu, rg.lo, o));
+            rg.hi = fmaxf(rg.hi, __shfl_xor_sync(0xFFFFFFFFu, rg.hi, o));
+        }
+        if (lane == 0) {
+            if (rg.lo == rg.lo) atomic_min_f(range + 2 * slot, rg.lo);
+            if (rg.hi == rg.hi) atomic_max_f(range + 2 * slot + 1, rg.hi);
+        }
+    }
+}
+
+// kRange: also fold the inputs into their buffer's [min, max]; a CTA merges
+// its partial range when the buffer of its next tile differs, and at the end.
+template <typename T, class Prm, bool kRange>
+__global__ void __launch_bounds__(kThreads, kRange ? kRangeMinBlocks : 4) ring_fold_kernel(const __grid_constant__ Prm p) {
     constexpr int V = Elem<T>::kVec;
+    Range rg;
+    int slot = -1;
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         // the piece that owns tile t: largest i with tile_start[i] <= t (uniform per CTA)
         int lo = 0, hi = p.npieces - 1;
@@ -156,6 +224,11 @@ __global__ void __launch_bounds__(kThreads) ring_fold_kernel(const __grid_consta
             else hi = mid - 1;
         }
         const Piece pc = p.piece[lo];
+        if (kRange && p.slot[lo] != slot) {
+            if (slot >= 0) flush_range(rg, p.range, slot);
+            rg = Range();
+            slot = p.slot[lo];
+        }
         const int64_t lt = t - p.tile_start[lo];
         if (pc.vec) {
             int64_t vb = (pc.begin + V - 1) / V * V;
@@ -166,43 +239,66 @@ __global__ void __launch_bounds__(kThreads) ring_fold_kernel(const __grid_consta
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int64_t i = lt * kTileUnits + u * kThreads + threadIdx.x;
-                if (i < nvec) fold_vec<T>(p, pc.row, pc.chunk, pc.ccw, vb + i * V);
+                if (i < nvec) fold_vec<T, kRange>(p, pc.row, pc.chunk, pc.ccw, vb + i * V, rg);
             }
             if (lt == 0) {  // ragged head and tail of the piece (fewer than V each)
                 const int head = static_cast<int>(vb - pc.begin);
                 const int tail = static_cast<int>(pc.end - ve);
-                if (threadIdx.x < head) fold_one<T>(p, pc.row, pc.chunk, pc.ccw, pc.begin + threadIdx.x);
+                if (threadIdx.x < head) fold_one<T, kRange>(p, pc.row, pc.chunk, pc.ccw, pc.begin + threadIdx.x, rg);
                 else if (threadIdx.x >= 32 && threadIdx.x < 32 + tail)
-                    fold_one<T>(p, pc.row, pc.chunk, pc.ccw, ve + (threadIdx.x - 32));
+                    fold_one<T, kRange>(p, pc.row, pc.chunk, pc.ccw, ve + (threadIdx.x - 32), rg);
             }
         } else {
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int64_t e = pc.begin + lt * kTileUnits + u * kThreads + threadIdx.x;
-                if (e < pc.end) fold_one<T>(p, pc.row, pc.chunk, pc.ccw, e);
+                if (e < pc.end) fold_one<T, kRange>(p, pc.row, pc.chunk, pc.ccw, e, rg);
             }
         }
+    }
+    if (kRange && slot >= 0) flush_range(rg, p.range, slot);
+}
+
+// Range entries of the buffers a call covers start at (+inf, -inf), or at
+// (0, 0) when the packed buffer would hold zero gaps.
+struct RangeResetParams {
+    float *mM;
+    int32_t n;
+    int32_t ids[255];
+    uint8_t zero[256];
+};
+
+__global__ void range_reset_kernel(const __grid_constant__ RangeResetParams p) {
+    for (int i = threadIdx.x; i < p.n; i += blockDim.x) {
+        p.mM[2 * p.ids[i]] = p.zero[i] ? 0.0f : __int_as_float(0x7F800000);
+        p.mM[2 * p.ids[i] + 1] = p.zero[i] ? 0.0f : __int_as_float(0xFF800000u);
     }
 }
 
 // Launch configuration: enough CTAs to fill every SM at full occupancy,
 // striding over the tiles.
-template <typename T, class Prm>
-int launch_fold(const Prm &p, cudaStream_t stream) {
-    if (p.total_tiles <= 0) return GAR_OK;
-    static int per_sm[2] = {0, 0};
-    int &occ = per_sm[sizeof(T) == 4 ? 0 : 1];
+template <typename T, class Prm, bool kRange>
+int launch_fold_as(const Prm &p, cudaStream_t stream) {
+    static int occ = 0;  // per instantiation
     if (occ == 0) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ring_fold_kernel<T, Prm>, kThreads, 0) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ring_fold_kernel<T, Prm, kRange>, kThreads, 0) !=
+                cudaSuccess ||
             n <= 0)
             n = 4;
         occ = n;
     }
     int64_t grid = static_cast<int64_t>(sm_count()) * occ;
     if (grid > p.total_tiles) grid = p.total_tiles;
-    ring_fold_kernel<T, Prm><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+    ring_fold_kernel<T, Prm, kRange><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
     return check_launch("ring_fold_kernel");
+}
+
+template <typename T, class Prm>
+int launch_fold(const Prm &p, cudaStream_t stream) {
+    if (p.total_tiles <= 0) return GAR_OK;
+    if (p.range) return launch_fold_as<T, Prm, true>(p, stream);
+    return launch_fold_as<T, Prm, false>(p, stream);
 }
 
 template <class Prm>
@@ -245,7 +341,10 @@ static void finalize_tiles(Prm &p, int V) {
 
 template <class Prm>
 static int launch_dtype(const Prm &p, int32_t dtype, cudaStream_t stream) {
-    return dtype == GAR_F32 ? launch_fold<float>(p, stream) : launch_fold<uint16_t>(p, stream);
+    if (dtype == GAR_F32) return launch_fold<float>(p, stream);
+    Prm q = p;  // a range is only ever asked of fp32 buffers
+    q.range = nullptr;
+    return launch_fold<uint16_t>(q, stream);
 }
 
 static int check_common(int32_t P, int64_t N, int32_t dtype, int32_t op) {
@@ -346,17 +445,56 @@ extern "C" int gar_ring_allreduce_sim_out(const void *const *bufs, int32_t P, in
 }
 
 // ---------------------------------------------- plan-driven (fused) launch
+// Reset the range entries of the buffers the call covers.  A buffer starts at
+// (0, 0) when its packed form would hold zeros: an alignment gap after one of
+// the given tensors (up to the next given tensor of the buffer, or the end).
+static int reset_ranges(const gar_seg *segs, int32_t count, const int64_t *buf_numel, int32_t n_buffers,
+                        float *d_mM, cudaStream_t stream) {
+    std::vector<int8_t> state(n_buffers, -1);  // -1 not covered, 0 no zeros, 1 zeros
+    std::vector<int64_t> last_end(n_buffers, 0);
+    for (int i = 0; i < count; ++i) {
+        const gar_seg &s = segs[i];
+        if (state[s.buffer] < 0) state[s.buffer] = 0;
+        else if (s.offset > last_end[s.buffer]) state[s.buffer] = 1;  // gap before this tensor
+        last_end[s.buffer] = s.offset + s.numel;
+    }
+    for (int b = 0; b < n_buffers; ++b)
+        if (state[b] == 0 && last_end[b] < buf_numel[b]) state[b] = 1;  // gap up to the buffer's end
+    RangeResetParams rp;
+    std::memset(&rp, 0, sizeof(rp));
+    rp.mM = d_mM;
+    for (int b = 0; b <= n_buffers; ++b) {
+        if (b < n_buffers && state[b] >= 0) {
+            rp.ids[rp.n] = b;
+            rp.zero[rp.n] = static_cast<uint8_t>(state[b]);
+            ++rp.n;
+        }
+        if (rp.n > 0 && (rp.n == 255 || b == n_buffers)) {
+            range_reset_kernel<<<1, 256, 0, stream>>>(rp);
+            const int rc = check_launch("range_reset_kernel");
+            if (rc) return rc;
+            rp.n = 0;
+        }
+    }
+    return GAR_OK;
+}
+
 int fused_allreduce_impl(const void *const *src, void *const *dst, int32_t P, const gar_seg *segs,
                          const int32_t *dtype, int32_t count, const int64_t *buf_numel, int32_t n_buffers,
-                         int32_t op, cudaStream_t stream) {
+                         int32_t op, float *d_mM, cudaStream_t stream) {
     using Prm = FoldParamsLarge;
-    Prm *p = new Prm;  // ~25 KB: keep it off the stack
     int rc = GAR_OK;
+    if (d_mM) {
+        rc = reset_ranges(segs, count, buf_numel, n_buffers, d_mM, stream);
+        if (rc) return rc;
+    }
+    Prm *p = new Prm;  // ~25 KB: keep it off the stack
     for (int pass_dtype = 0; pass_dtype < 2 && rc == GAR_OK; ++pass_dtype) {
         const int es = elem_bytes(pass_dtype);
         std::memset(p, 0, sizeof(Prm));
         p->P = P;
         p->n_out = P;
+        p->range = pass_dtype == GAR_F32 ? d_mM : nullptr;
         set_mode(*p, op, P);
         int rows = 0;
         auto flush = [&]() -> int {
@@ -395,6 +533,7 @@ int fused_allreduce_impl(const void *const *src, void *const *dst, int32_t P, co
                 pc.chunk = static_cast<int32_t>(c);
                 pc.vec = vec ? 1 : 0;
                 pc.ccw = 0;
+                p->slot[p->npieces - 1] = b;
                 pc.begin = pos;
                 pc.end = stop;
                 pos = stop;

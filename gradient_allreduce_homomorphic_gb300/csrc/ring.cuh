@@ -29,10 +29,11 @@ struct FoldParams {
     int32_t mode;     // kMode*
     float inv_p;      // 1/P (exact when P is a power of two)
     float fp;         // P
-    int32_t pad0, pad1;
+    float *range;     // [slot][2] min / max of the inputs, or NULL
     int64_t total_tiles;
     int64_t tile_start[NPIECE + 1];  // first tile of each piece; [npieces] = total
     Piece piece[NPIECE];
+    int32_t slot[NPIECE];  // range launches: fusion buffer each piece's inputs are folded into
     const void *src[NPTR];  // src[row * P + w]
     void *dst[NPTR];        // dst[row * n_out + k]
 };
@@ -51,8 +52,10 @@ struct StepParams {
 };
 
 // Plan-driven all-reduce over the workers' tensors (validated by the caller).
+// d_mM (NULL, or [n_buffers][2] device floats): also fold every fp32 input
+// into its buffer's [min, max], as the THC range of the packed buffer.
 int fused_allreduce_impl(const void *const *src, void *const *dst, int32_t P, const gar_seg *segs,
                          const int32_t *dtype, int32_t count, const int64_t *buf_numel, int32_t n_buffers,
-                         int32_t op, cudaStream_t stream);
+                         int32_t op, float *d_mM, cudaStream_t stream);
 
 }  // namespace gar

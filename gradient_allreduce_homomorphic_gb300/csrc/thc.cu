@@ -15,7 +15,9 @@
 //   (jm - (2^23 + 1)) + (1 + u), where jm - (2^23 + 1) = j - 1 is exact and
 //   1 + u is the float with mantissa r mod 2^23.
 // No integer<->float conversion is needed per element.
+#include <algorithm>
 #include <cstring>
+#include <vector>
 
 #include "common.cuh"
 
@@ -323,9 +325,9 @@ struct FusedParams {
 
 // One worker's contribution to a word of E = 4G elements: Philox draws,
 // indices added to the running sums s, the packed word stored if wanted.
-template <int B, bool kPacked, int G>
+template <int B, bool kPacked, int G, class Prm>
 __device__ __forceinline__ void fused_one_worker(const float4 (&v)[G], uint32_t (&s)[4 * G], int64_t e0, int64_t w,
-                                                 int wk, const FusedParams &p, float m, float sc) {
+                                                 int wk, const Prm &p, float m, float sc) {
     uint32_t word = 0;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -405,6 +407,174 @@ __global__ void __launch_bounds__(kThreads) thc_fused_kernel(const __grid_consta
                 // elements never visited above kept s = 0; only in-range ones are stored
                 p.avg[e0 + i] = __fmaf_rn(small_to_float(s[i] - bias), k, km);
             }
+        }
+    }
+}
+
+// ------------------------------------------- fused over a Tensor Fusion plan
+// THC of one fusion buffer read straight from the workers' tensors ([H]
+// "Tensor Fusion" with [T] Algorithm 1 on the fused buffer): element e of the
+// buffer is element e - begin of the tensor whose slot [begin, end) holds it,
+// or 0 in an alignment gap -- exactly the packed buffer's contents -- and its
+// Philox draw is keyed by e, so indices, index sums, packed words and
+// averages equal those of gar_thc_allreduce_fused over the packed buffer bit
+// for bit.  The average of every tensor element goes straight to the output
+// tensor (the unpack); gap elements are not written anywhere.
+constexpr int kPlanPtrs = 2048, kPlanSegs = 192;
+
+struct PlanSeg {
+    int64_t begin;  // first buffer element of the tensor
+    int64_t end;    // one past its last
+    int32_t vec;    // every worker's pointer and the output 16-byte aligned, begin a multiple of 4
+    int32_t pad;
+};
+
+struct ThcPlanParams {
+    PhiloxKeys keys;
+    int32_t wid[GAR_MAX_WORKERS];
+    uint32_t *packed[GAR_MAX_WORKERS];  // this buffer's wire vectors, all NULL when not wanted
+    const float *mM;                    // this buffer's [m, M]
+    int64_t N;                          // elements of the buffer
+    int64_t w_begin, w_end;             // words this launch covers
+    int32_t P, nseg;
+    float L, fp;
+    PlanSeg seg[kPlanSegs];             // sorted, disjoint; every tensor meeting the launch's words
+    float *out[kPlanSegs];              // output tensor of each segment
+    const float *src[kPlanPtrs];        // src[k * P + slot]: worker slot's tensor of segment k
+};
+static_assert(sizeof(ThcPlanParams) <= 32000, "plan parameters exceed the launch limit");
+
+// Segment holding buffer element e, or -1 in a gap.
+__device__ __forceinline__ int plan_find(const ThcPlanParams &p, int64_t e) {
+    int lo = 0, hi = p.nseg - 1;
+    if (hi < 0 || p.seg[0].begin > e) return -1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.seg[mid].begin <= e) lo = mid;
+        else hi = mid - 1;
+    }
+    return e < p.seg[lo].end ? lo : -1;
+}
+
+// (the element-by-element helpers stay out of line: they serve only the few
+// groups at tensor ends and gaps, and inlining them costs the vector path registers)
+__device__ __noinline__ float plan_value(const ThcPlanParams &p, int wk, int64_t e) {
+    const int k = plan_find(p, e);
+    return k < 0 ? 0.0f : p.src[k * p.P + wk][e - p.seg[k].begin];
+}
+
+__device__ __noinline__ void plan_store(const ThcPlanParams &p, int64_t e, float v) {
+    const int k = plan_find(p, e);
+    if (k >= 0) p.out[k][e - p.seg[k].begin] = v;
+}
+
+// How one group of 4 buffer elements [e, e + 4) is read: whole from one
+// tensor with a 16-byte load (k >= 0), all gap (k == -1), or element by element.
+struct GroupSrc {
+    int k;
+    int64_t off;
+};
+constexpr int kGroupGap = -1, kGroupScalar = -2;
+
+__device__ __noinline__ GroupSrc plan_group(const ThcPlanParams &p, int64_t e) {
+    const int k = plan_find(p, e);
+    if (k >= 0) {
+        const PlanSeg &sg = p.seg[k];
+        if (sg.vec && e + 4 <= sg.end) return {k, e - sg.begin};
+        return {kGroupScalar, 0};
+    }
+    // in a gap: all four are gap unless a tensor starts inside the group
+    int lo = 0, hi = p.nseg - 1, nxt = p.nseg;  // first segment beginning after e
+    while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        if (p.seg[mid].begin > e) {
+            nxt = mid;
+            hi = mid - 1;
+        } else {
+            lo = mid + 1;
+        }
+    }
+    return (nxt == p.nseg || p.seg[nxt].begin >= e + 4) ? GroupSrc{kGroupGap, 0} : GroupSrc{kGroupScalar, 0};
+}
+
+template <int G>
+__device__ __forceinline__ void plan_load(float4 (&v)[G], const GroupSrc (&gs)[G], const ThcPlanParams &p, int wk,
+                                          int64_t e0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        if (gs[g].k >= 0) {
+            v[g] = __ldcs(reinterpret_cast<const float4 *>(p.src[gs[g].k * p.P + wk] + gs[g].off));
+        } else if (gs[g].k == kGroupGap) {
+            v[g] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        } else {
+            const int64_t e = e0 + 4 * g;
+            v[g] = make_float4(plan_value(p, wk, e), plan_value(p, wk, e + 1), plan_value(p, wk, e + 2),
+                               plan_value(p, wk, e + 3));
+        }
+    }
+}
+
+template <int B, bool kPacked>
+__global__ void __launch_bounds__(kThreads) thc_fused_plan_kernel(const __grid_constant__ ThcPlanParams p) {
+    constexpr int E = 32 / B;
+    constexpr int G = E / 4;
+    const float m = p.mM[0], M = p.mM[1];
+    const float sc = range_scale(m, M, p.L);
+    float km;
+    const float k = decode_step(p.mM, p.L, p.fp, km);
+    const uint32_t bias = static_cast<uint32_t>(p.P) * 0x4B000000u;  // mod 2^32
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t w = p.w_begin + static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < p.w_end;
+         w += stride) {
+        const int64_t e0 = w * E;
+        uint32_t s[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i) s[i] = 0;
+        if (e0 + E <= p.N) {
+            GroupSrc gs[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) gs[g] = plan_group(p, e0 + 4 * g);
+            float4 va[G], vb[G];
+            plan_load(va, gs, p, 0, e0);
+            for (int wk = 0; wk < p.P; wk += 2) {
+                const bool has1 = wk + 1 < p.P;
+                if (has1) plan_load(vb, gs, p, wk + 1, e0);
+                fused_one_worker<B, kPacked>(va, s, e0, w, wk, p, m, sc);
+                if (wk + 2 < p.P) plan_load(va, gs, p, wk + 2, e0);
+                if (has1) fused_one_worker<B, kPacked>(vb, s, e0, w, wk + 1, p, m, sc);
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float4 a = make_float4(__fmaf_rn(small_to_float(s[4 * g] - bias), k, km),
+                                             __fmaf_rn(small_to_float(s[4 * g + 1] - bias), k, km),
+                                             __fmaf_rn(small_to_float(s[4 * g + 2] - bias), k, km),
+                                             __fmaf_rn(small_to_float(s[4 * g + 3] - bias), k, km));
+                if (gs[g].k >= 0) {
+                    __stcs(reinterpret_cast<float4 *>(p.out[gs[g].k] + gs[g].off), a);
+                } else if (gs[g].k == kGroupScalar) {
+                    const int64_t e = e0 + 4 * g;
+                    plan_store(p, e, a.x);
+                    plan_store(p, e + 1, a.y);
+                    plan_store(p, e + 2, a.z);
+                    plan_store(p, e + 3, a.w);
+                }
+            }
+        } else {  // the buffer's ragged last word, element by element
+            for (int wk = 0; wk < p.P; ++wk) {
+                uint32_t word = 0;
+                for (int g = 0; g < G; ++g) {
+                    const int64_t eb = e0 + 4 * g;
+                    if (eb >= p.N) break;
+                    const uint4 r = philox_block(eb >> 2, p.wid[wk], p.keys);
+                    for (int i = 0; i < 4 && eb + i < p.N; ++i) {
+                        const uint32_t a = index_biased(plan_value(p, wk, eb + i), m, sc, p.L, pick(r, i));
+                        s[4 * g + i] += a;
+                        word |= (a - 0x4B000000u) << ((4 * g + i) * B);
+                    }
+                }
+                if (kPacked) p.packed[wk][w] = word;
+            }
+            for (int i = 0; i < E && e0 + i < p.N; ++i) plan_store(p, e0 + i, __fmaf_rn(small_to_float(s[i] - bias), k, km));
         }
     }
 }
@@ -851,6 +1021,118 @@ extern "C" int gar_thc_allreduce_fused_masked(const float *const *x, int32_t P, 
                                               int32_t b, uint64_t seed, const float *d_mM, float *avg,
                                               uint32_t *const *packed, gar_stream_t stream) {
     return thc_fused_entry(x, P, arrived, N, b, seed, d_mM, avg, packed, stream);
+}
+
+// ------------------------------------------- fused over a Tensor Fusion plan
+template <int B>
+static int launch_plan(const ThcPlanParams &p, bool packed, cudaStream_t stream) {
+    const int64_t words = p.w_end - p.w_begin;
+    if (packed)
+        thc_fused_plan_kernel<B, true><<<grid_for(thc_fused_plan_kernel<B, true>, words), kThreads, 0, stream>>>(p);
+    else
+        thc_fused_plan_kernel<B, false><<<grid_for(thc_fused_plan_kernel<B, false>, words), kThreads, 0, stream>>>(p);
+    return check_launch("thc_fused_plan_kernel");
+}
+
+extern "C" int gar_thc_allreduce_fused_plan(const float *const *src, int32_t P, const gar_seg *segs,
+                                            const int32_t *dtype, int32_t count, const int64_t *buf_numel,
+                                            int32_t n_buffers, int32_t b, uint64_t seed, const float *d_mM,
+                                            float *const *out, uint32_t *const *packed, gar_stream_t stream_) {
+    if (!valid_b(b)) return fail(GAR_EINVAL, "b=%d not in {1, 2, 4, 8}", b);
+    if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
+    if (static_cast<int64_t>(P) * ((1 << b) - 1) > 65535) return fail(GAR_EOVERFLOW, "P * (2^b - 1) > 65535");
+    if (count < 0 || n_buffers < 0) return fail(GAR_EINVAL, "count or n_buffers < 0");
+    if (count == 0) return GAR_OK;
+    if (!src || !segs || !dtype || !buf_numel || !d_mM || !out) return fail(GAR_EINVAL, "NULL argument");
+    if (!aligned(d_mM, 4)) return fail(GAR_EALIGN, "d_mM not 4-byte aligned");
+    std::vector<int64_t> cursor(n_buffers, 0);
+    std::vector<std::vector<int>> members(n_buffers);
+    for (int i = 0; i < count; ++i) {
+        const gar_seg &sg = segs[i];
+        if (dtype[i] != GAR_F32) return fail(GAR_EDTYPE, "tensor %d is not fp32", i);
+        if (sg.buffer < 0 || sg.buffer >= n_buffers) return fail(GAR_EINVAL, "tensor %d has buffer id %d", i, sg.buffer);
+        if (sg.numel < 0 || sg.offset < cursor[sg.buffer] || sg.offset + sg.numel > buf_numel[sg.buffer])
+            return fail(GAR_EINVAL, "tensor %d does not lie in order inside buffer %d", i, sg.buffer);
+        cursor[sg.buffer] = sg.offset + sg.numel;
+        if (sg.numel == 0) continue;
+        if (!out[i] || !aligned(out[i], 4)) return fail(out[i] ? GAR_EALIGN : GAR_EINVAL, "output %d NULL or misaligned", i);
+        for (int w = 0; w < P; ++w) {
+            const float *sp = src[static_cast<int64_t>(w) * count + i];
+            if (!sp) return fail(GAR_EINVAL, "worker %d tensor %d pointer is NULL", w, i);
+            if (!aligned(sp, 4)) return fail(GAR_EALIGN, "worker %d tensor %d not 4-byte aligned", w, i);
+        }
+        members[sg.buffer].push_back(i);
+    }
+    ThcPlanParams *p = new ThcPlanParams;  // ~23 KB: keep it off the stack
+    std::memset(p, 0, sizeof(ThcPlanParams));
+    p->keys = philox_keys(seed);
+    p->P = P;
+    p->L = static_cast<float>((1 << b) - 1);
+    p->fp = static_cast<float>(P);
+    for (int w = 0; w < P; ++w) p->wid[w] = w;
+    const int E = 32 / b;
+    const int cap = std::min(kPlanSegs, kPlanPtrs / P);  // >= 32 >= E: a word meets at most E tensors
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int rc = GAR_OK;
+    for (int bf = 0; bf < n_buffers && rc == GAR_OK; ++bf) {
+        const std::vector<int> &mem = members[bf];
+        if (mem.empty()) continue;
+        p->mM = d_mM + 2 * bf;
+        p->N = buf_numel[bf];
+        for (int w = 0; w < P; ++w) {
+            if (packed) {
+                uint32_t *pk = packed[static_cast<int64_t>(w) * n_buffers + bf];
+                if (!pk || !aligned(pk, 4)) {
+                    rc = fail(pk ? GAR_EALIGN : GAR_EINVAL, "packed vector of worker %d buffer %d NULL or misaligned", w, bf);
+                    break;
+                }
+                p->packed[w] = pk;
+            }
+        }
+        if (rc) break;
+        const int64_t nwords = gar_thc_words(p->N, b);
+        // launches over consecutive word ranges; each one's table holds every
+        // tensor that meets its words (those before `lo` end before them, those
+        // from `hi` on begin after them)
+        int lo = 0;
+        int64_t w0 = 0;
+        const int n = static_cast<int>(mem.size());
+        while (w0 < nwords && rc == GAR_OK) {
+            while (lo < n && segs[mem[lo]].offset + segs[mem[lo]].numel <= w0 * E) ++lo;
+            const int hi = std::min(lo + cap, n);
+            const int64_t w1 = hi == n ? nwords : segs[mem[hi]].offset / E;
+            if (w1 <= w0) {
+                rc = fail(GAR_EINVAL, "more than %d tensors meet one word of buffer %d", cap, bf);
+                break;
+            }
+            p->w_begin = w0;
+            p->w_end = w1;
+            p->nseg = hi - lo;
+            for (int k = 0; k < p->nseg; ++k) {
+                const int i = mem[lo + k];
+                PlanSeg &sg = p->seg[k];
+                sg.begin = segs[i].offset;
+                sg.end = segs[i].offset + segs[i].numel;
+                bool vec = (sg.begin % 4 == 0) && aligned(out[i], 16);
+                for (int w = 0; w < P; ++w) {
+                    const float *sp = src[static_cast<int64_t>(w) * count + i];
+                    p->src[k * P + w] = sp;
+                    vec = vec && aligned(sp, 16);
+                }
+                sg.vec = vec ? 1 : 0;
+                p->out[k] = out[i];
+            }
+            switch (b) {
+                case 1: rc = launch_plan<1>(*p, packed != nullptr, stream); break;
+                case 2: rc = launch_plan<2>(*p, packed != nullptr, stream); break;
+                case 4: rc = launch_plan<4>(*p, packed != nullptr, stream); break;
+                default: rc = launch_plan<8>(*p, packed != nullptr, stream); break;
+            }
+            w0 = w1;
+        }
+    }
+    delete p;
+    return rc;
 }
 
 // ------------------------------------------------------- non-uniform THC

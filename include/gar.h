@@ -173,6 +173,19 @@ int gar_fused_allreduce(const void *const *src, void *const *dst, int32_t P,
                         const int64_t *buf_numel, int32_t n_buffers, int32_t op,
                         gar_stream_t stream);
 
+/* gar_fused_allreduce_range -- gar_fused_allreduce that also computes THC's
+ * preliminary round for the plan's buffers ([T] section 4, Algorithm 1) from
+ * the same reads: d_mM[2b], d_mM[2b+1] = min and max over the workers' inputs
+ * of fusion buffer b, the packed buffer's zero padding included -- the values
+ * gar_fusion_pack_all with a range gives for the same arguments.  Meant with
+ * dst != src, so that the original gradients stay available to THC.  Only
+ * buffers that at least one of the tensors belongs to get range entries.
+ *   d_mM  device, 2 * n_buffers floats; fp32 plans only
+ * Errors: as gar_fused_allreduce; GAR_EDTYPE for bf16 tensors. */
+int gar_fused_allreduce_range(const void *const *src, void *const *dst, int32_t P, const gar_seg *segs,
+                              const int32_t *dtype, int32_t count, const int64_t *buf_numel,
+                              int32_t n_buffers, int32_t op, float *d_mM, gar_stream_t stream);
+
 /* ===================================================================== */
 /* Ring all-reduce [H] "The Ring-Allreduce Algorithm", [R] sections 4, 5, 7 */
 /* ===================================================================== */
@@ -296,6 +309,31 @@ int gar_thc_allreduce_fused(const float *const *x, int32_t P, int64_t N, int32_t
 int gar_thc_allreduce_fused_masked(const float *const *x, int32_t P, uint64_t arrived, int64_t N,
                                    int32_t b, uint64_t seed, const float *d_mM, float *avg,
                                    uint32_t *const *packed, gar_stream_t stream);
+
+/* gar_thc_allreduce_fused_plan -- uniform THC of every fusion buffer of a
+ * plan ([H] "Tensor Fusion" feeding [T] Algorithm 1), read straight from the
+ * workers' tensors and written straight to the output tensors: for each
+ * buffer b the result is bit-identical to gar_fusion_pack_all ->
+ * gar_thc_allreduce_fused over buffer b (worker ids 0..P-1, the packed
+ * buffer's element index keying the Philox draws, zero padding encoded as
+ * zeros) -> gar_fusion_unpack of the average.
+ *   src[P * count]   host array: src[w * count + i] = worker w's tensor i
+ *   segs, dtype      the plan; every tensor fp32; buf_numel[n_buffers]
+ *   d_mM             device, [n_buffers][2]: each buffer's shared [m, M]
+ *                    (from gar_fusion_pack_all or gar_fused_allreduce_range)
+ *   out[count]       host array: device output tensor of each tensor (the
+ *                    average every worker decodes)
+ *   packed           NULL, or host array [P * n_buffers]: packed[w *
+ *                    n_buffers + b] receives worker w's indices of buffer b
+ *                    (gar_thc_words(buf_numel[b], b) words)
+ * Only buffers that at least one of the tensors belongs to are processed.
+ * Errors: GAR_EINVAL (bad b/P/plan, NULL, more than min(192, 2048 / P)
+ * tensors meeting one packed word), GAR_EDTYPE (bf16), GAR_EOVERFLOW,
+ * GAR_EALIGN, GAR_ECUDA. */
+int gar_thc_allreduce_fused_plan(const float *const *src, int32_t P, const gar_seg *segs,
+                                 const int32_t *dtype, int32_t count, const int64_t *buf_numel,
+                                 int32_t n_buffers, int32_t b, uint64_t seed, const float *d_mM,
+                                 float *const *out, uint32_t *const *packed, gar_stream_t stream);
 
 /* ===================================================================== */
 /* Non-uniform THC [T] section 5, Algorithm 2                            */
