@@ -4,15 +4,20 @@ One step = one pass of the whole path over the ResNet-101-like Tensor
 Fusion workload: P = 8 workers, 300 fp32 gradient tensors (~45M parameters,
 log-uniform sizes 256..2.4M, N(0, 0.01)), 64 MB fusion buffers:
 
-  1. fusion plan (host)                                   gar_fusion_plan
-  2. pack every worker's tensors into its fusion buffers, gar_fusion_pack_all
-     THC's per-buffer [min, max] folded into the same pass
-  3. per fusion buffer: encode + aggregate + decode       gar_thc_allreduce_fused
-     (b = 4, fresh seed each step)
-  4. THC average back into the tensors                    gar_fusion_unpack
-  5. ring all-reduce average, pack + ring + unpack fused  gar_fused_allreduce
-     (on a second stream, overlapping step 3)
-  6. NMSE of the THC estimate against the ring average    gar_nmse
+  1. fusion plan (host)                                    gar_fusion_plan
+  2. per fusion buffer: Tensor Fusion + ring all-reduce     gar_fused_allreduce_range
+     average in one pass (pack, ring, unpack), the buffer's
+     THC range [min, max] taken from the same reads
+  3. per fusion buffer: THC encode (every worker) +         gar_thc_allreduce_fused_plan
+     integer aggregate + decode, read straight from the
+     tensors, average written straight to the output
+     tensors, wire vectors written (b = 4, fresh seed each step)
+  4. NMSE of the THC estimate against the ring average     gar_nmse
+
+The fused calls give bit for bit what pack -> ring / THC -> unpack gives
+(the tests hold them to that); the fusion buffers are never materialised.
+In the default two-stream schedule THC of buffer b runs while the ring
+averages buffer b + 1.
 
 Metric: gradient bytes reduced per second = P x 45M x 4 B per step / step
 time (each step averages those bytes twice: exactly by the ring and
@@ -126,9 +131,14 @@ class ClockSampler:
 
 # ------------------------------------------------------------ GPU (ours)
 class Step:
-    """Device-resident state and the per-step call sequence."""
+    """Device-resident state and the per-step call sequence.
 
-    STAGES = ["fused_ring", "pack", "thc_fused", "unpack", "nmse"]
+    Per fusion buffer b (plan order): the ring all-reduce of b's tensors,
+    which also yields b's THC range from the same reads, then THC of b read
+    straight from the tensors.  In the two-stream schedule THC of buffer b
+    runs while the ring averages buffer b + 1."""
+
+    STAGES = ["ring", "thc", "nmse"]
 
     def __init__(self, torch, g, dev, schedule="overlap"):
         self.torch, self.g, self.dev = torch, g, dev
@@ -153,22 +163,26 @@ class Step:
         self.plan = g.gar_fusion_plan(sizes, self.dtype, CAPACITY, ALIGN)
         self.nb = self.plan.n_buffers
         bn = self.plan.buf_numel
-        self.fusion = [[torch.empty(int(bn[b]), dtype=torch.float32, device=dev) for b in range(self.nb)]
-                       for _ in range(P)]
-        self.thc_avg = [torch.empty(int(bn[b]), dtype=torch.float32, device=dev) for b in range(self.nb)]
+        self.buf_total = int(bn.sum())
         self.words = [g.gar_thc_words(int(bn[b]), B_THC) for b in range(self.nb)]
         self.packed = [[torch.empty(self.words[b], dtype=torch.int32, device=dev) for b in range(self.nb)]
                        for _ in range(P)]
         self.mM = torch.empty((self.nb, 2), dtype=torch.float32, device=dev)
         self.nmse = torch.empty(1, dtype=torch.float64, device=dev)
         self.ws = torch.empty(g.gar_nmse_workspace_bytes(self.flat_len) // 8 + 1, dtype=torch.float64, device=dev)
-        # host pointer tables built once (the tensors do not move between steps)
-        self.ring_tables = g.fused_pointer_tables(self.src, self.ring)
-        self.pack_tables = g.pack_all_tables(self.src, self.fusion)
-        self.thc_tab = g.pointer_table(self.thc)
-        self.fusion_col = [g.pointer_table([self.fusion[w][b] for w in range(P)]) for b in range(self.nb)]
-        self.packed_col = [g.pointer_table([self.packed[w][b] for w in range(P)]) for b in range(self.nb)]
-        self.buf_total = int(bn.sum())
+        # host pointer tables per fusion buffer, built once (the tensors do not move)
+        self.parts = []
+        for b in range(self.nb):
+            first, cnt = self.plan.buffer_tensors(b)
+            rows = slice(first, first + cnt)
+            src_b = [self.src[w][rows] for w in range(P)]
+            self.parts.append({
+                "first": first, "count": cnt,
+                "lo": int(self.offs[first]), "hi": int(self.offs[first + cnt]),
+                "ring": g.fused_pointer_tables(src_b, [self.ring[w][rows] for w in range(P)]),
+                "thc": g.thc_plan_tables(src_b, self.thc[rows], self.packed),
+                "ev": torch.cuda.Event(),
+            })
         self.stream_r = torch.cuda.Stream(device=dev)
         self.stream_t = torch.cuda.Stream(device=dev)
         self.stages = list(self.STAGES)
@@ -176,69 +190,25 @@ class Step:
     def _views(self, flat):
         return [flat[int(self.offs[i]):int(self.offs[i]) + int(s)] for i, s in enumerate(self.sizes)]
 
-    def setup_e2e(self):
-        """Per-buffer slices of the plan for the host-to-host pipeline."""
-        g, torch = self.g, self.torch
-        self.parts = []
-        for b in range(self.nb):
-            first, cnt = self.plan.buffer_tensors(b)
-            sub = self.plan.subplan(first, cnt)
-            rows = slice(first, first + cnt)
-            self.parts.append({
-                "sub": sub, "lo": int(self.offs[first]), "hi": int(self.offs[first + cnt]),
-                "pack": g.pack_all_tables([self.src[w][rows] for w in range(P)], self.fusion),
-                "ring": g.fused_pointer_tables([self.src[w][rows] for w in range(P)],
-                                               [self.ring[w][rows] for w in range(P)]),
-                "thc": g.pointer_table(self.thc[rows]),
-                "ev_in": torch.cuda.Event(), "ev_out": torch.cuda.Event(),
-            })
-        self.s_h2d = torch.cuda.Stream(device=self.dev)
-        self.s_d2h = torch.cuda.Stream(device=self.dev)
-        self.ev_nmse = torch.cuda.Event()
+    def _buffer_ring(self, plan, b, stream):
+        part = self.parts[b]
+        sub = plan.subplan(part["first"], part["count"])
+        self.g.gar_fused_allreduce_range([None] * P, None, sub, self.mM, op=self.g.GAR_AVG, stream=stream,
+                                         tables=part["ring"])
 
-    def run_e2e(self, step_idx, host_in, host_ring, host_thc, host_nmse):
-        """One step from pinned host gradients to host averages and NMSE,
-        pipelined by fusion buffer: buffer b+1's inputs cross the link while
-        buffer b is averaged, and b's results travel back meanwhile."""
-        g, torch = self.g, self.torch
-        seed = workloads.THC_SEED + step_idx
-        main = torch.cuda.current_stream()
-        g.gar_fusion_plan(self.sizes, self.dtype, CAPACITY, ALIGN)  # the plan, as every step computes it
-        self.s_h2d.wait_stream(main)
-        for b, part in enumerate(self.parts):
-            lo, hi = part["lo"], part["hi"]
-            with torch.cuda.stream(self.s_h2d):
-                for w in range(P):
-                    self.flat[w][lo:hi].copy_(host_in[w][lo:hi], non_blocking=True)
-                part["ev_in"].record(self.s_h2d)
-            main.wait_event(part["ev_in"])
-            sub = part["sub"]
-            g.gar_fusion_pack_all(None, sub, None, self.mM, stream=main, tables=part["pack"])
-            g.gar_thc_allreduce_fused(self.fusion_col[b], B_THC, seed, self.mM[b], self.thc_avg[b],
-                                      self.packed_col[b], stream=main)
-            g.gar_fusion_unpack(self.thc_avg[b], sub, b, part["thc"], stream=main)
-            g.gar_fused_allreduce([None] * P, None, sub, op=g.GAR_AVG, tables=part["ring"], stream=main)
-            part["ev_out"].record(main)
-            self.s_d2h.wait_event(part["ev_out"])
-            with torch.cuda.stream(self.s_d2h):
-                host_ring[lo:hi].copy_(self.ring_flat[0][lo:hi], non_blocking=True)
-                host_thc[lo:hi].copy_(self.thc_flat[lo:hi], non_blocking=True)
-        g.gar_nmse(self.ring_flat[0], self.thc_flat, self.nmse, self.ws, stream=main)
-        self.ev_nmse.record(main)
-        self.s_d2h.wait_event(self.ev_nmse)
-        with torch.cuda.stream(self.s_d2h):
-            host_nmse.copy_(self.nmse, non_blocking=True)
-        main.wait_stream(self.s_d2h)
+    def _buffer_thc(self, plan, b, seed, stream):
+        part = self.parts[b]
+        sub = plan.subplan(part["first"], part["count"])
+        self.g.gar_thc_allreduce_fused_plan(None, sub, B_THC, seed, self.mM, None, stream=stream,
+                                            tables=part["thc"])
 
     def algorithmic_bytes(self):
-        n, bt = self.n_params * 4, self.buf_total * 4
+        n = self.n_params * 4
         words = 4 * sum(self.words)
         return {
-            "fused_ring": 2 * P * n,                  # read P x n, write P x n
-            "pack": P * n + P * bt,                   # read tensors, write buffers (gaps zeroed); range on the way
-            "thc_fused": P * bt + bt + P * words,     # read P buffers, write avg + wire vectors
-            "unpack": 2 * n,                          # THC average back into one tensor set
-            "nmse": 2 * self.flat_len * 4,            # read both flat averages
+            "ring": 2 * P * n,                 # read P x n, write P x n (range from the same reads)
+            "thc": P * n + n + P * words,      # read P x n, write the average + the wire vectors
+            "nmse": 2 * self.flat_len * 4,     # read both flat averages
         }
 
     def run(self, step_idx, events=None):
@@ -256,27 +226,25 @@ class Step:
 
         plan = g.gar_fusion_plan(self.sizes, self.dtype, CAPACITY, ALIGN)
         if overlap:
-            s_thc.wait_stream(main)
             s_ring.wait_stream(main)
-        # THC path: pack every worker (range fused in), encode/aggregate/decode, unpack
-        mark("pack", 0, s_thc)
-        g.gar_fusion_pack_all(self.src, plan, self.fusion, self.mM, stream=s_thc, tables=self.pack_tables)
-        mark("pack", 1, s_thc)
-        if overlap:  # the ring (HBM-bound) runs while THC quantizes (ALU-bound)
-            s_ring.wait_stream(s_thc)
-        mark("thc_fused", 0, s_thc)
+            s_thc.wait_stream(main)
+        # exact path: Tensor Fusion + ring all-reduce average, buffer by buffer,
+        # each buffer's THC range [m, M] from the same reads
+        mark("ring", 0, s_ring)
         for b in range(self.nb):
-            g.gar_thc_allreduce_fused(self.fusion_col[b], B_THC, seed, self.mM[b], self.thc_avg[b],
-                                      self.packed_col[b], stream=s_thc)
-        mark("thc_fused", 1, s_thc)
-        mark("unpack", 0, s_thc)
+            self._buffer_ring(plan, b, s_ring)
+            if overlap:
+                self.parts[b]["ev"].record(s_ring)
+        mark("ring", 1, s_ring)
+        # compressed path: THC of each buffer once its range is known (in the
+        # two-stream schedule, while the ring averages the next buffer)
         for b in range(self.nb):
-            g.gar_fusion_unpack(self.thc_avg[b], plan, b, self.thc_tab, stream=s_thc)
-        mark("unpack", 1, s_thc)
-        # exact path: Tensor Fusion + ring all-reduce average, one pass
-        mark("fused_ring", 0, s_ring)
-        g.gar_fused_allreduce(self.src, self.ring, plan, op=g.GAR_AVG, tables=self.ring_tables, stream=s_ring)
-        mark("fused_ring", 1, s_ring)
+            if overlap:
+                s_thc.wait_event(self.parts[b]["ev"])
+            if b == 0:
+                mark("thc", 0, s_thc)
+            self._buffer_thc(plan, b, seed, s_thc)
+        mark("thc", 1, s_thc)
         if overlap:
             main.wait_stream(s_thc)
             main.wait_stream(s_ring)
@@ -284,20 +252,61 @@ class Step:
         g.gar_nmse(self.ring_flat[0], self.thc_flat, self.nmse, self.ws, stream=main)
         mark("nmse", 1, main)
 
+    # ------------------------------------------------------- end to end
+    def setup_e2e(self, n_h2d=2):
+        torch = self.torch
+        self.s_h2d = [torch.cuda.Stream(device=self.dev) for _ in range(n_h2d)]
+        self.s_d2h = torch.cuda.Stream(device=self.dev)
+        self.ev_in = [[torch.cuda.Event() for _ in self.s_h2d] for _ in range(self.nb)]
+        self.ev_out = [torch.cuda.Event() for _ in range(self.nb)]
+        self.ev_nmse = torch.cuda.Event()
 
-KERNEL_OF_STAGE = {"fused_ring": "ring_fold_kernel", "pack": "pack_all_kernel", "thc_fused": "thc_fused_kernel",
-                   "unpack": "copy_jobs_kernel", "nmse": "nmse_partial_kernel + nmse_final_kernel"}
+    def run_e2e(self, step_idx, host_in, host_ring, host_thc, host_nmse):
+        """One step from pinned host gradients to host averages and NMSE,
+        pipelined by fusion buffer: buffer b+1's inputs cross the link (the
+        workers split over the copy streams) while buffer b is averaged, and
+        b's results travel back meanwhile."""
+        g, torch = self.g, self.torch
+        seed = workloads.THC_SEED + step_idx
+        main = torch.cuda.current_stream()
+        plan = g.gar_fusion_plan(self.sizes, self.dtype, CAPACITY, ALIGN)
+        for s in self.s_h2d:
+            s.wait_stream(main)
+        k = len(self.s_h2d)
+        for b, part in enumerate(self.parts):
+            lo, hi = part["lo"], part["hi"]
+            for j, s in enumerate(self.s_h2d):
+                with torch.cuda.stream(s):
+                    for w in range(j, P, k):
+                        self.flat[w][lo:hi].copy_(host_in[w][lo:hi], non_blocking=True)
+                    self.ev_in[b][j].record(s)
+                main.wait_event(self.ev_in[b][j])
+            self._buffer_ring(plan, b, main)
+            self._buffer_thc(plan, b, seed, main)
+            self.ev_out[b].record(main)
+            self.s_d2h.wait_event(self.ev_out[b])
+            with torch.cuda.stream(self.s_d2h):
+                host_ring[lo:hi].copy_(self.ring_flat[0][lo:hi], non_blocking=True)
+                host_thc[lo:hi].copy_(self.thc_flat[lo:hi], non_blocking=True)
+        g.gar_nmse(self.ring_flat[0], self.thc_flat, self.nmse, self.ws, stream=main)
+        self.ev_nmse.record(main)
+        self.s_d2h.wait_event(self.ev_nmse)
+        with torch.cuda.stream(self.s_d2h):
+            host_nmse.copy_(self.nmse, non_blocking=True)
+        main.wait_stream(self.s_d2h)
+
+
+KERNEL_OF_STAGE = {"ring": "ring_fold_kernel", "thc": "thc_fused_plan_kernel",
+                   "nmse": "nmse_partial_kernel + nmse_final_kernel"}
 PER_OF_STAGE = {
-    "fused_ring": "all launches of one step's gar_fused_allreduce (3 launches, 300 tensors x 8 workers)",
-    "pack": "all launches of one step's gar_fusion_pack_all (8 workers x 3 fusion buffers, range fused in)",
-    "thc_fused": "all launches of one step's 3 gar_thc_allreduce_fused calls",
-    "unpack": "all launches of one step's 3 gar_fusion_unpack calls",
+    "ring": "all launches of one step's 3 gar_fused_allreduce_range calls (one per fusion buffer; "
+            "300 tensors x 8 workers in all)",
+    "thc": "all launches of one step's 3 gar_thc_allreduce_fused_plan calls (one per fusion buffer)",
     "nmse": "one step's gar_nmse over the flat averages",
 }
 # stage -> committed ncu summary holding its per-step DRAM traffic
-PROFILE_OF_STAGE = {"fused_ring": ("ring_fold_kernel_resnet_fusion", ["ring.cu", "ring.cuh", "common.cuh"]),
-                    "pack": ("pack_all_kernel_resnet_fusion", ["fusion.cu", "ring.cuh", "common.cuh"]),
-                    "thc_fused": ("thc_fused_kernel_resnet_fusion", ["thc.cu", "common.cuh"])}
+PROFILE_OF_STAGE = {"ring": ("ring_fold_kernel_range_resnet_fusion", ["ring.cu", "ring.cuh", "common.cuh"]),
+                    "thc": ("thc_fused_plan_kernel_resnet_fusion", ["thc.cu", "common.cuh"])}
 
 
 def kernel_source_hash(files):
@@ -399,7 +408,7 @@ def run_ours(args, rank, world, dist):
     host_nmse = torch.empty(1, dtype=torch.float64, pin_memory=True)
     e2e_steps = max(3, min(args.steps, 20))
 
-    st.setup_e2e()
+    st.setup_e2e(args.h2d_streams)
 
     def e2e_step(i):
         st.run_e2e(10_000 + i, host_in, host_ring, host_thc, host_nmse)
@@ -435,11 +444,11 @@ def run_ours(args, rank, world, dist):
         # ring and THC quantization share HBM: their combined bytes over the
         # span from the ring's start to the later of the two ends
         evs = overlap_evs
-        span = float(np.mean([max(evs[i]["fused_ring"][0].elapsed_time(evs[i]["fused_ring"][1]),
-                                  evs[i]["fused_ring"][0].elapsed_time(evs[i]["thc_fused"][1]))
+        span = float(np.mean([max(evs[i]["ring"][0].elapsed_time(evs[i]["ring"][1]),
+                                  evs[i]["ring"][0].elapsed_time(evs[i]["thc"][1]))
                               for i in range(args.steps)]))
-        both = algo["fused_ring"] + algo["thc_fused"]
-        overlap_region = {"stages": ["fused_ring", "thc_fused"], "ms": round(span, 4),
+        both = algo["ring"] + algo["thc"]
+        overlap_region = {"stages": ["ring", "thc"], "ms": round(span, 4),
                           "gbs": round(both / (span * 1e-3) / 1e9, 1),
                           "frac": round(both / (span * 1e-3) / 1e9 / peak, 4)}
     out = {
@@ -447,8 +456,10 @@ def run_ours(args, rank, world, dist):
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded N(0,0.01) gradients drawn on the device)",
         "config": _config(st.n_params, st.nb, parallelism=f"{world} independent replicas" if world > 1 else "single GPU",
-                          schedule=("two streams: ring all-reduce overlapped with THC quantization"
-                                    if args.schedule == "overlap" else "one stream, stages in sequence")),
+                          schedule=("two streams: THC of fusion buffer b overlapped with the ring of buffer b+1"
+                                    if args.schedule == "overlap" else "one stream, stages in sequence"),
+                          path="fused: pack + ring + unpack and pack + THC + unpack in one pass each, "
+                               "per fusion buffer"),
         "elements_per_s": round(world * P * st.n_params / (ms * 1e-3), 1),
         "hbm_fraction_of_step": round(sum(algo.values()) / (ms * 1e-3) / 1e9 / peak, 4),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
@@ -465,7 +476,7 @@ def run_ours(args, rank, world, dist):
                                else "in the timed steps")},
         "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": P * st.flat_len * 4,
-                "d2h_bytes_per_step": 2 * st.flat_len * 4 + 8},
+                "d2h_bytes_per_step": 2 * st.flat_len * 4 + 8, "h2d_streams": args.h2d_streams},
         "gpu_launches": int(launches),
         "nmse_thc_b4": round(nmse_vals[0], 6),
         "clocks": clk,
@@ -565,6 +576,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--schedule", choices=["overlap", "serial"], default="overlap")
+    ap.add_argument("--h2d-streams", type=int, default=2, help="copy streams for the end-to-end inputs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

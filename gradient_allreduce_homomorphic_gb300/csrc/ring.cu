@@ -275,21 +275,14 @@ __global__ void range_reset_kernel(const __grid_constant__ RangeResetParams p) {
     }
 }
 
-// Launch configuration: enough CTAs to fill every SM at full occupancy,
-// striding over the tiles.
+// Launch configuration: one CTA per tile.  The hardware block scheduler hands
+// the next tile to whichever SM frees a slot first, so SMs that draw less
+// bandwidth finish no later than the rest; a persistent grid striding over the
+// tiles left single SMs busy up to 13% past the average (ncu), and one CTA per
+// tile measured 6.3 TB/s against 5.7 TB/s for the fp32 ring of 8 x 2^24.
 template <typename T, class Prm, bool kRange>
 int launch_fold_as(const Prm &p, cudaStream_t stream) {
-    static int occ = 0;  // per instantiation
-    if (occ == 0) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ring_fold_kernel<T, Prm, kRange>, kThreads, 0) !=
-                cudaSuccess ||
-            n <= 0)
-            n = 4;
-        occ = n;
-    }
-    int64_t grid = static_cast<int64_t>(sm_count()) * occ;
-    if (grid > p.total_tiles) grid = p.total_tiles;
+    const int64_t grid = p.total_tiles < 0x7FFFFFFF ? p.total_tiles : 0x7FFFFFFF;
     ring_fold_kernel<T, Prm, kRange><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
     return check_launch("ring_fold_kernel");
 }

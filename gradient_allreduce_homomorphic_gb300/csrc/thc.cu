@@ -26,6 +26,17 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Resident CTAs per SM the fused kernels are compiled for (caps registers at
+// 65536 / (256 * n)): four for b >= 4, fewer where a word's registers
+// (E = 32 / b elements, two workers in flight) need more.
+#ifndef GAR_THC_MIN_BLOCKS
+#define GAR_THC_MIN_BLOCKS 4
+#endif
+template <int B>
+constexpr int fused_min_blocks() {
+    return B >= 4 ? GAR_THC_MIN_BLOCKS : (B == 2 ? 3 : 2);
+}
+
 __device__ __forceinline__ float range_scale(float m, float M, float L) {
     return (M == m) ? 0.0f : __fdiv_rn(L, __fsub_rn(M, m));
 }
@@ -323,19 +334,35 @@ struct FusedParams {
     float fp;
 };
 
+// Constants of one launch: range, quantization scale, decode step.
+struct Coder {
+    float m, sc, k, km;
+    uint32_t bias;  // P * 0x4B000000 (mod 2^32): removed once from each index sum
+};
+
+template <class Prm>
+__device__ __forceinline__ Coder make_coder(const Prm &p) {
+    Coder c;
+    c.m = p.mM[0];
+    c.sc = range_scale(c.m, p.mM[1], p.L);
+    c.k = decode_step(p.mM, p.L, p.fp, c.km);
+    c.bias = static_cast<uint32_t>(p.P) * 0x4B000000u;
+    return c;
+}
+
 // One worker's contribution to a word of E = 4G elements: Philox draws,
 // indices added to the running sums s, the packed word stored if wanted.
 template <int B, bool kPacked, int G, class Prm>
 __device__ __forceinline__ void fused_one_worker(const float4 (&v)[G], uint32_t (&s)[4 * G], int64_t e0, int64_t w,
-                                                 int wk, const Prm &p, float m, float sc) {
+                                                 int wk, const Prm &p, const Coder &c) {
     uint32_t word = 0;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         const uint4 r = philox_block((e0 >> 2) + g, p.wid[wk], p.keys);
-        const uint32_t a0 = index_biased(v[g].x, m, sc, p.L, r.x);
-        const uint32_t a1 = index_biased(v[g].y, m, sc, p.L, r.y);
-        const uint32_t a2 = index_biased(v[g].z, m, sc, p.L, r.z);
-        const uint32_t a3 = index_biased(v[g].w, m, sc, p.L, r.w);
+        const uint32_t a0 = index_biased(v[g].x, c.m, c.sc, p.L, r.x);
+        const uint32_t a1 = index_biased(v[g].y, c.m, c.sc, p.L, r.y);
+        const uint32_t a2 = index_biased(v[g].z, c.m, c.sc, p.L, r.z);
+        const uint32_t a3 = index_biased(v[g].w, c.m, c.sc, p.L, r.w);
         s[4 * g] += a0;
         s[4 * g + 1] += a1;
         s[4 * g + 2] += a2;
@@ -348,47 +375,57 @@ __device__ __forceinline__ void fused_one_worker(const float4 (&v)[G], uint32_t 
 }
 
 template <int G>
-__device__ __forceinline__ void load_worker(float4 (&v)[G], const FusedParams &p, int wk, int64_t e0) {
+__device__ __forceinline__ void load_group(float4 (&v)[G], const float *x) {
 #pragma unroll
-    for (int g = 0; g < G; ++g) v[g] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk] + e0) + g);
+    for (int g = 0; g < G; ++g) v[g] = __ldcs(reinterpret_cast<const float4 *>(x) + g);
+}
+
+// Word w (elements w*E .. w*E + E - 1) with every operand 16-byte aligned:
+// worker slot wk's E inputs start at xs[wk] + xoff, the E averages go to avg.
+// Two register buffers, the worker loop unrolled by two: one worker's loads
+// are in flight while the other is quantized, with no copies.
+template <int B, bool kPacked, class Prm>
+__device__ __forceinline__ void fused_word_vec(const Prm &p, const Coder &c, const float *const *xs, int64_t xoff,
+                                               float *avg, int64_t w) {
+    constexpr int E = 32 / B;
+    constexpr int G = E / 4;  // float4 groups (and Philox blocks) per word
+    const int64_t e0 = w * E;
+    uint32_t s[E];
+#pragma unroll
+    for (int i = 0; i < E; ++i) s[i] = 0;
+    float4 va[G], vb[G];
+    load_group(va, xs[0] + xoff);
+    for (int wk = 0; wk < p.P; wk += 2) {
+        const bool has1 = wk + 1 < p.P;
+        if (has1) load_group(vb, xs[wk + 1] + xoff);
+        fused_one_worker<B, kPacked>(va, s, e0, w, wk, p, c);
+        if (wk + 2 < p.P) load_group(va, xs[wk + 2] + xoff);
+        if (has1) fused_one_worker<B, kPacked>(vb, s, e0, w, wk + 1, p, c);
+    }
+    float4 *dst = reinterpret_cast<float4 *>(avg);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        __stcs(dst + g, make_float4(__fmaf_rn(small_to_float(s[4 * g] - c.bias), c.k, c.km),
+                                    __fmaf_rn(small_to_float(s[4 * g + 1] - c.bias), c.k, c.km),
+                                    __fmaf_rn(small_to_float(s[4 * g + 2] - c.bias), c.k, c.km),
+                                    __fmaf_rn(small_to_float(s[4 * g + 3] - c.bias), c.k, c.km)));
+    }
 }
 
 template <int B, bool kPacked>
-__global__ void __launch_bounds__(kThreads) thc_fused_kernel(const __grid_constant__ FusedParams p) {
+__global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_kernel(const __grid_constant__ FusedParams p) {
     constexpr int E = 32 / B;
-    constexpr int G = E / 4;  // float4 groups (and Philox blocks) per word
-    const float m = p.mM[0], M = p.mM[1];
-    const float sc = range_scale(m, M, p.L);
-    float km;
-    const float k = decode_step(p.mM, p.L, p.fp, km);
-    const uint32_t bias = static_cast<uint32_t>(p.P) * 0x4B000000u;  // mod 2^32
+    constexpr int G = E / 4;
+    const Coder c = make_coder(p);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < p.nwords; w += stride) {
         const int64_t e0 = w * E;
-        uint32_t s[E];
-#pragma unroll
-        for (int i = 0; i < E; ++i) s[i] = 0;
         if (p.vec && e0 + E <= p.N) {
-            // two register buffers, the worker loop unrolled by two: one worker's
-            // loads are in flight while the other is quantized, with no copies
-            float4 va[G], vb[G];
-            load_worker(va, p, 0, e0);
-            for (int wk = 0; wk < p.P; wk += 2) {
-                const bool has1 = wk + 1 < p.P;
-                if (has1) load_worker(vb, p, wk + 1, e0);
-                fused_one_worker<B, kPacked>(va, s, e0, w, wk, p, m, sc);
-                if (wk + 2 < p.P) load_worker(va, p, wk + 2, e0);
-                if (has1) fused_one_worker<B, kPacked>(vb, s, e0, w, wk + 1, p, m, sc);
-            }
-            float4 *dst = reinterpret_cast<float4 *>(p.avg + e0);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                __stcs(dst + g, make_float4(__fmaf_rn(small_to_float(s[4 * g] - bias), k, km),
-                                            __fmaf_rn(small_to_float(s[4 * g + 1] - bias), k, km),
-                                            __fmaf_rn(small_to_float(s[4 * g + 2] - bias), k, km),
-                                            __fmaf_rn(small_to_float(s[4 * g + 3] - bias), k, km)));
-            }
+            fused_word_vec<B, kPacked>(p, c, p.x, e0, p.avg + e0, w);
         } else {  // ragged last word, or unaligned inputs: element by element
+            uint32_t s[E];
+#pragma unroll
+            for (int i = 0; i < E; ++i) s[i] = 0;
             for (int wk = 0; wk < p.P; ++wk) {
                 uint32_t word = 0;
                 for (int g = 0; g < G; ++g) {
@@ -396,7 +433,7 @@ __global__ void __launch_bounds__(kThreads) thc_fused_kernel(const __grid_consta
                     if (eb >= p.N) break;
                     const uint4 r = philox_block(eb >> 2, p.wid[wk], p.keys);
                     for (int i = 0; i < 4 && eb + i < p.N; ++i) {
-                        const uint32_t a = index_biased(p.x[wk][eb + i], m, sc, p.L, pick(r, i));
+                        const uint32_t a = index_biased(p.x[wk][eb + i], c.m, c.sc, p.L, pick(r, i));
                         s[4 * g + i] += a;
                         word |= (a - 0x4B000000u) << ((4 * g + i) * B);
                     }
@@ -405,7 +442,7 @@ __global__ void __launch_bounds__(kThreads) thc_fused_kernel(const __grid_consta
             }
             for (int i = 0; i < E && e0 + i < p.N; ++i) {
                 // elements never visited above kept s = 0; only in-range ones are stored
-                p.avg[e0 + i] = __fmaf_rn(small_to_float(s[i] - bias), k, km);
+                p.avg[e0 + i] = __fmaf_rn(small_to_float(s[i] - c.bias), c.k, c.km);
             }
         }
     }
@@ -420,13 +457,27 @@ __global__ void __launch_bounds__(kThreads) thc_fused_kernel(const __grid_consta
 // averages equal those of gar_thc_allreduce_fused over the packed buffer bit
 // for bit.  The average of every tensor element goes straight to the output
 // tensor (the unpack); gap elements are not written anywhere.
-constexpr int kPlanPtrs = 2048, kPlanSegs = 192;
+//
+// Work decomposition (made on the host): the launch's words are cut into
+// pieces -- runs of whole words inside one tensor (loaded with 16-byte
+// vectors when every pointer of the tensor is 16-byte aligned), and runs of
+// the words between them (a tensor's first and last word shared with a
+// neighbour or a gap, the buffer's ragged last word) taken element by
+// element.  Pieces are cut into tiles of kThreads words that CTAs stride
+// over; the piece of a tile is found once per tile, uniform over the CTA.
+constexpr int kPlanPtrs = 2048, kPlanSegs = 128, kPlanPieces = 2 * kPlanSegs + 1;
+constexpr int kPieceVec = 0, kPieceTensor = 1, kPieceMixed = 2;
 
 struct PlanSeg {
     int64_t begin;  // first buffer element of the tensor
     int64_t end;    // one past its last
-    int32_t vec;    // every worker's pointer and the output 16-byte aligned, begin a multiple of 4
-    int32_t pad;
+};
+
+struct PlanPiece {
+    int64_t w0, w1;  // words [w0, w1) of the buffer
+    int32_t seg;     // the tensor holding every element of the words (kPieceVec, kPieceTensor), else -1
+    int32_t kind;    // kPieceVec: 16-byte vectors; kPieceTensor: one tensor, element by element;
+                     // kPieceMixed: each element looked up (tensor, gap or past the end)
 };
 
 struct ThcPlanParams {
@@ -435,12 +486,14 @@ struct ThcPlanParams {
     uint32_t *packed[GAR_MAX_WORKERS];  // this buffer's wire vectors, all NULL when not wanted
     const float *mM;                    // this buffer's [m, M]
     int64_t N;                          // elements of the buffer
-    int64_t w_begin, w_end;             // words this launch covers
-    int32_t P, nseg;
+    int64_t total_tiles;
+    int32_t P, nseg, npieces, pad;
     float L, fp;
-    PlanSeg seg[kPlanSegs];             // sorted, disjoint; every tensor meeting the launch's words
-    float *out[kPlanSegs];              // output tensor of each segment
-    const float *src[kPlanPtrs];        // src[k * P + slot]: worker slot's tensor of segment k
+    PlanSeg seg[kPlanSegs];                  // sorted, disjoint; every tensor meeting the launch's words
+    float *out[kPlanSegs];                   // output tensor of each segment
+    int64_t tile_start[kPlanPieces + 1];     // first tile of each piece; [npieces] = total
+    PlanPiece piece[kPlanPieces];
+    const float *src[kPlanPtrs];             // src[k * P + slot]: worker slot's tensor of segment k
 };
 static_assert(sizeof(ThcPlanParams) <= 32000, "plan parameters exceed the launch limit");
 
@@ -456,125 +509,97 @@ __device__ __forceinline__ int plan_find(const ThcPlanParams &p, int64_t e) {
     return e < p.seg[lo].end ? lo : -1;
 }
 
-// (the element-by-element helpers stay out of line: they serve only the few
-// groups at tensor ends and gaps, and inlining them costs the vector path registers)
-__device__ __noinline__ float plan_value(const ThcPlanParams &p, int wk, int64_t e) {
-    const int k = plan_find(p, e);
-    return k < 0 ? 0.0f : p.src[k * p.P + wk][e - p.seg[k].begin];
-}
-
-__device__ __noinline__ void plan_store(const ThcPlanParams &p, int64_t e, float v) {
-    const int k = plan_find(p, e);
-    if (k >= 0) p.out[k][e - p.seg[k].begin] = v;
-}
-
-// How one group of 4 buffer elements [e, e + 4) is read: whole from one
-// tensor with a 16-byte load (k >= 0), all gap (k == -1), or element by element.
-struct GroupSrc {
-    int k;
-    int64_t off;
-};
-constexpr int kGroupGap = -1, kGroupScalar = -2;
-
-__device__ __noinline__ GroupSrc plan_group(const ThcPlanParams &p, int64_t e) {
-    const int k = plan_find(p, e);
-    if (k >= 0) {
-        const PlanSeg &sg = p.seg[k];
-        if (sg.vec && e + 4 <= sg.end) return {k, e - sg.begin};
-        return {kGroupScalar, 0};
-    }
-    // in a gap: all four are gap unless a tensor starts inside the group
-    int lo = 0, hi = p.nseg - 1, nxt = p.nseg;  // first segment beginning after e
-    while (lo <= hi) {
-        const int mid = (lo + hi) >> 1;
-        if (p.seg[mid].begin > e) {
-            nxt = mid;
-            hi = mid - 1;
-        } else {
-            lo = mid + 1;
+// The buffer's ragged last word (e0 + E > N), element by element: the
+// missing elements pack as zero bits and get no output.
+template <int B, bool kPacked>
+__device__ __noinline__ void plan_word_ragged(const ThcPlanParams &p, const Coder &c, int64_t w) {
+    constexpr int E = 32 / B;
+    constexpr int G = E / 4;
+    const int64_t e0 = w * E;
+    uint32_t s[E];
+    for (int i = 0; i < E; ++i) s[i] = 0;
+    for (int wk = 0; wk < p.P; ++wk) {
+        uint32_t word = 0;
+        for (int g = 0; g < G; ++g) {
+            const int64_t eb = e0 + 4 * g;
+            if (eb >= p.N) break;
+            const uint4 r = philox_block(eb >> 2, p.wid[wk], p.keys);
+            for (int i = 0; i < 4 && eb + i < p.N; ++i) {
+                const int64_t e = eb + i;
+                const int k = plan_find(p, e);
+                const float x = k < 0 ? 0.0f : p.src[k * p.P + wk][e - p.seg[k].begin];
+                const uint32_t a = index_biased(x, c.m, c.sc, p.L, pick(r, i));
+                s[4 * g + i] += a;
+                word |= (a - 0x4B000000u) << ((4 * g + i) * B);
+            }
         }
+        if (kPacked) p.packed[wk][w] = word;
     }
-    return (nxt == p.nseg || p.seg[nxt].begin >= e + 4) ? GroupSrc{kGroupGap, 0} : GroupSrc{kGroupScalar, 0};
+    for (int i = 0; i < E && e0 + i < p.N; ++i) {
+        const int64_t e = e0 + i;
+        const int k = plan_find(p, e);
+        if (k >= 0) p.out[k][e - p.seg[k].begin] = __fmaf_rn(small_to_float(s[i] - c.bias), c.k, c.km);
+    }
 }
 
-template <int G>
-__device__ __forceinline__ void plan_load(float4 (&v)[G], const GroupSrc (&gs)[G], const ThcPlanParams &p, int wk,
-                                          int64_t e0) {
+// A whole word (e0 + E <= N) read element by element: a word shared by two
+// tensors or a tensor and a gap (seg < 0: each element's tensor looked up
+// once), or a word of a tensor whose pointers are not 16-byte aligned
+// (seg >= 0).  Each worker's E values are gathered with independent loads,
+// then quantized as a vector word.  Kept out of line: it serves only the few
+// words at tensor ends and gaps, and the unaligned tensors.
+template <int B, bool kPacked>
+__device__ __noinline__ void plan_word_gather(const ThcPlanParams &p, const Coder &c, int64_t w, int seg) {
+    constexpr int E = 32 / B;
+    constexpr int G = E / 4;
+    const int64_t e0 = w * E;
+    int ks[E];
+    int64_t off[E];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        if (gs[g].k >= 0) {
-            v[g] = __ldcs(reinterpret_cast<const float4 *>(p.src[gs[g].k * p.P + wk] + gs[g].off));
-        } else if (gs[g].k == kGroupGap) {
-            v[g] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        } else {
-            const int64_t e = e0 + 4 * g;
-            v[g] = make_float4(plan_value(p, wk, e), plan_value(p, wk, e + 1), plan_value(p, wk, e + 2),
-                               plan_value(p, wk, e + 3));
-        }
+    for (int i = 0; i < E; ++i) {
+        const int k = seg >= 0 ? seg : plan_find(p, e0 + i);
+        ks[i] = k;
+        off[i] = k >= 0 ? e0 + i - p.seg[k].begin : 0;
     }
+    uint32_t s[E];
+#pragma unroll
+    for (int i = 0; i < E; ++i) s[i] = 0;
+    for (int wk = 0; wk < p.P; ++wk) {
+        float x[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i) x[i] = ks[i] >= 0 ? __ldcs(p.src[ks[i] * p.P + wk] + off[i]) : 0.0f;
+        float4 v[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) v[g] = make_float4(x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]);
+        fused_one_worker<B, kPacked>(v, s, e0, w, wk, p, c);
+    }
+#pragma unroll
+    for (int i = 0; i < E; ++i)
+        if (ks[i] >= 0) __stcs(p.out[ks[i]] + off[i], __fmaf_rn(small_to_float(s[i] - c.bias), c.k, c.km));
 }
 
 template <int B, bool kPacked>
-__global__ void __launch_bounds__(kThreads) thc_fused_plan_kernel(const __grid_constant__ ThcPlanParams p) {
+__global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_plan_kernel(const __grid_constant__ ThcPlanParams p) {
     constexpr int E = 32 / B;
-    constexpr int G = E / 4;
-    const float m = p.mM[0], M = p.mM[1];
-    const float sc = range_scale(m, M, p.L);
-    float km;
-    const float k = decode_step(p.mM, p.L, p.fp, km);
-    const uint32_t bias = static_cast<uint32_t>(p.P) * 0x4B000000u;  // mod 2^32
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t w = p.w_begin + static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < p.w_end;
-         w += stride) {
-        const int64_t e0 = w * E;
-        uint32_t s[E];
-#pragma unroll
-        for (int i = 0; i < E; ++i) s[i] = 0;
-        if (e0 + E <= p.N) {
-            GroupSrc gs[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) gs[g] = plan_group(p, e0 + 4 * g);
-            float4 va[G], vb[G];
-            plan_load(va, gs, p, 0, e0);
-            for (int wk = 0; wk < p.P; wk += 2) {
-                const bool has1 = wk + 1 < p.P;
-                if (has1) plan_load(vb, gs, p, wk + 1, e0);
-                fused_one_worker<B, kPacked>(va, s, e0, w, wk, p, m, sc);
-                if (wk + 2 < p.P) plan_load(va, gs, p, wk + 2, e0);
-                if (has1) fused_one_worker<B, kPacked>(vb, s, e0, w, wk + 1, p, m, sc);
-            }
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float4 a = make_float4(__fmaf_rn(small_to_float(s[4 * g] - bias), k, km),
-                                             __fmaf_rn(small_to_float(s[4 * g + 1] - bias), k, km),
-                                             __fmaf_rn(small_to_float(s[4 * g + 2] - bias), k, km),
-                                             __fmaf_rn(small_to_float(s[4 * g + 3] - bias), k, km));
-                if (gs[g].k >= 0) {
-                    __stcs(reinterpret_cast<float4 *>(p.out[gs[g].k] + gs[g].off), a);
-                } else if (gs[g].k == kGroupScalar) {
-                    const int64_t e = e0 + 4 * g;
-                    plan_store(p, e, a.x);
-                    plan_store(p, e + 1, a.y);
-                    plan_store(p, e + 2, a.z);
-                    plan_store(p, e + 3, a.w);
-                }
-            }
-        } else {  // the buffer's ragged last word, element by element
-            for (int wk = 0; wk < p.P; ++wk) {
-                uint32_t word = 0;
-                for (int g = 0; g < G; ++g) {
-                    const int64_t eb = e0 + 4 * g;
-                    if (eb >= p.N) break;
-                    const uint4 r = philox_block(eb >> 2, p.wid[wk], p.keys);
-                    for (int i = 0; i < 4 && eb + i < p.N; ++i) {
-                        const uint32_t a = index_biased(plan_value(p, wk, eb + i), m, sc, p.L, pick(r, i));
-                        s[4 * g + i] += a;
-                        word |= (a - 0x4B000000u) << ((4 * g + i) * B);
-                    }
-                }
-                if (kPacked) p.packed[wk][w] = word;
-            }
-            for (int i = 0; i < E && e0 + i < p.N; ++i) plan_store(p, e0 + i, __fmaf_rn(small_to_float(s[i] - bias), k, km));
+    const Coder c = make_coder(p);
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        // the piece that owns tile t: largest i with tile_start[i] <= t (uniform per CTA)
+        int lo = 0, hi = p.npieces - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.tile_start[mid] <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        const PlanPiece pc = p.piece[lo];
+        const int64_t w = pc.w0 + (t - p.tile_start[lo]) * kThreads + threadIdx.x;
+        if (w >= pc.w1) continue;
+        if (pc.kind == kPieceVec) {
+            const int64_t off = w * E - p.seg[pc.seg].begin;
+            fused_word_vec<B, kPacked>(p, c, p.src + pc.seg * p.P, off, p.out[pc.seg] + off, w);
+        } else if ((w + 1) * E <= p.N) {
+            plan_word_gather<B, kPacked>(p, c, w, pc.kind == kPieceTensor ? pc.seg : -1);
+        } else {
+            plan_word_ragged<B, kPacked>(p, c, w);
         }
     }
 }
@@ -1026,12 +1051,57 @@ extern "C" int gar_thc_allreduce_fused_masked(const float *const *x, int32_t P, 
 // ------------------------------------------- fused over a Tensor Fusion plan
 template <int B>
 static int launch_plan(const ThcPlanParams &p, bool packed, cudaStream_t stream) {
-    const int64_t words = p.w_end - p.w_begin;
+    if (p.total_tiles <= 0) return GAR_OK;
+    // one CTA per tile: the block scheduler balances the SMs (see the ring kernel)
+    const unsigned grid = static_cast<unsigned>(p.total_tiles < 0x7FFFFFFF ? p.total_tiles : 0x7FFFFFFF);
     if (packed)
-        thc_fused_plan_kernel<B, true><<<grid_for(thc_fused_plan_kernel<B, true>, words), kThreads, 0, stream>>>(p);
+        thc_fused_plan_kernel<B, true><<<grid, kThreads, 0, stream>>>(p);
     else
-        thc_fused_plan_kernel<B, false><<<grid_for(thc_fused_plan_kernel<B, false>, words), kThreads, 0, stream>>>(p);
+        thc_fused_plan_kernel<B, false><<<grid, kThreads, 0, stream>>>(p);
     return check_launch("thc_fused_plan_kernel");
+}
+
+// Pieces of the words [w_begin, w_end) of one launch over segments p.seg[0 ..
+// nseg) (sorted): per tensor, its whole words (vector or element-by-element
+// piece), and between them the words shared with a neighbour, a gap or the
+// buffer's end (looked-up piece).  At most 2 nseg + 1 pieces.  The
+// element-by-element pieces come first in tile order: a word of theirs costs
+// many times a vector word, and taking them in the first round of tiles
+// lets the vector tiles even out when the CTAs finish.
+static void plan_pieces(ThcPlanParams &p, const bool *vec, int E, int64_t w_begin, int64_t w_end) {
+    PlanPiece all[kPlanPieces];
+    int n = 0;
+    int64_t cur = w_begin;
+    auto add = [&](int64_t w0, int64_t w1, int seg, int kind) {
+        all[n].w0 = w0;
+        all[n].w1 = w1;
+        all[n].seg = seg;
+        all[n].kind = kind;
+        ++n;
+    };
+    for (int k = 0; k < p.nseg; ++k) {
+        const int64_t fw0 = std::max(ceil_div(p.seg[k].begin, E), w_begin);
+        const int64_t fw1 = std::min(p.seg[k].end / E, w_end);
+        if (fw0 >= fw1) continue;
+        if (cur < fw0) add(cur, fw0, -1, kPieceMixed);
+        add(fw0, fw1, k, vec[k] ? kPieceVec : kPieceTensor);
+        cur = fw1;
+    }
+    if (cur < w_end) add(cur, w_end, -1, kPieceMixed);
+    int m = 0;
+    int64_t tiles = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int i = 0; i < n; ++i) {
+            if ((all[i].kind == kPieceVec) != (pass == 1)) continue;
+            p.piece[m] = all[i];
+            p.tile_start[m] = tiles;
+            tiles += ceil_div(all[i].w1 - all[i].w0, kThreads);
+            ++m;
+        }
+    }
+    p.npieces = m;
+    p.tile_start[m] = tiles;
+    p.total_tiles = tiles;
 }
 
 extern "C" int gar_thc_allreduce_fused_plan(const float *const *src, int32_t P, const gar_seg *segs,
@@ -1063,7 +1133,7 @@ extern "C" int gar_thc_allreduce_fused_plan(const float *const *src, int32_t P, 
         }
         members[sg.buffer].push_back(i);
     }
-    ThcPlanParams *p = new ThcPlanParams;  // ~23 KB: keep it off the stack
+    ThcPlanParams *p = new ThcPlanParams;  // ~29 KB: keep it off the stack
     std::memset(p, 0, sizeof(ThcPlanParams));
     p->keys = philox_keys(seed);
     p->P = P;
@@ -1072,6 +1142,7 @@ extern "C" int gar_thc_allreduce_fused_plan(const float *const *src, int32_t P, 
     for (int w = 0; w < P; ++w) p->wid[w] = w;
     const int E = 32 / b;
     const int cap = std::min(kPlanSegs, kPlanPtrs / P);  // >= 32 >= E: a word meets at most E tensors
+    bool vec[kPlanSegs];
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     int rc = GAR_OK;
     for (int bf = 0; bf < n_buffers && rc == GAR_OK; ++bf) {
@@ -1105,23 +1176,22 @@ extern "C" int gar_thc_allreduce_fused_plan(const float *const *src, int32_t P, 
                 rc = fail(GAR_EINVAL, "more than %d tensors meet one word of buffer %d", cap, bf);
                 break;
             }
-            p->w_begin = w0;
-            p->w_end = w1;
             p->nseg = hi - lo;
             for (int k = 0; k < p->nseg; ++k) {
                 const int i = mem[lo + k];
                 PlanSeg &sg = p->seg[k];
                 sg.begin = segs[i].offset;
                 sg.end = segs[i].offset + segs[i].numel;
-                bool vec = (sg.begin % 4 == 0) && aligned(out[i], 16);
+                bool v = (sg.begin % 4 == 0) && aligned(out[i], 16);
                 for (int w = 0; w < P; ++w) {
                     const float *sp = src[static_cast<int64_t>(w) * count + i];
                     p->src[k * P + w] = sp;
-                    vec = vec && aligned(sp, 16);
+                    v = v && aligned(sp, 16);
                 }
-                sg.vec = vec ? 1 : 0;
+                vec[k] = v;
                 p->out[k] = out[i];
             }
+            plan_pieces(*p, vec, E, w0, w1);
             switch (b) {
                 case 1: rc = launch_plan<1>(*p, packed != nullptr, stream); break;
                 case 2: rc = launch_plan<2>(*p, packed != nullptr, stream); break;

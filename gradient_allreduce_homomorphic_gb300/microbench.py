@@ -5,6 +5,8 @@
 
 Cases: ring (in-place ring all-reduce of P buffers), ring_out (reduce to one
 output), bidir (bidirectional dual ring), fused (plan-driven all-reduce of the 300-tensor ResNet-like model),
+fused_range (the same into separate outputs, each buffer's THC range from the same reads), thc_plan
+(THC b-bit of every fusion buffer of that model read straight from the tensors, wire vectors written),
 pack, unpack (per worker and buffer), pack_all, pack_all_range (every worker
 in one call, with THC's range fused in), thc_range, thc_encode, thc_aggregate, thc_decode, thc_fused,
 thc_fused_packed, nuhc_fused, nuhc_fused_packed (non-uniform THC with a
@@ -68,7 +70,7 @@ def main(argv=None):
             t, o = g.pointer_table(x), g.pointer_table(out)
             fn = lambda: g.gar_ring_allreduce_sim_out(t, o)  # noqa: E731
             nbytes = P * N * es + N * es
-    elif a.case in ("fused", "pack", "unpack", "pack_all", "pack_all_range"):
+    elif a.case in ("fused", "fused_range", "thc_plan", "pack", "unpack", "pack_all", "pack_all_range"):
         sizes = workloads.resnet_fusion_sizes()
         dt = np.zeros(sizes.size, np.int32)
         plan = g.gar_fusion_plan(sizes, dt, 64 << 20, 16)
@@ -79,6 +81,21 @@ def main(argv=None):
             tables = g.fused_pointer_tables(src, src)
             fn = lambda: g.gar_fused_allreduce(src, src, plan, tables=tables)  # noqa: E731
             nbytes = 2 * P * n * 4
+        elif a.case in ("fused_range", "thc_plan"):
+            dst = [[torch.empty_like(t) for t in row] for row in src]
+            mM = torch.empty((plan.n_buffers, 2), device=dev)
+            tables = g.fused_pointer_tables(src, dst)
+            g.gar_fused_allreduce_range(src, dst, plan, mM, tables=tables)
+            if a.case == "fused_range":
+                fn = lambda: g.gar_fused_allreduce_range(src, dst, plan, mM, tables=tables)  # noqa: E731
+                nbytes = 2 * P * n * 4
+            else:
+                out = dst[0]
+                words = [g.gar_thc_words(int(k), b) for k in plan.buf_numel]
+                packed = [[torch.empty(k, dtype=torch.int32, device=dev) for k in words] for _ in range(P)]
+                tt = g.thc_plan_tables(src, out, packed)
+                fn = lambda: g.gar_thc_allreduce_fused_plan(src, plan, b, 5, mM, out, tables=tt)  # noqa: E731
+                nbytes = P * n * 4 + n * 4 + P * sum(words) * 4
         elif a.case.startswith("pack_all"):
             fbs = [[torch.empty(int(k), device=dev) for k in plan.buf_numel] for _ in range(P)]
             mM = torch.empty((plan.n_buffers, 2), device=dev) if a.case == "pack_all_range" else None
