@@ -52,6 +52,52 @@ __device__ __forceinline__ uint32_t index_biased(float x, float m, float sc, flo
     return __float_as_uint(jm) + (__fadd_rd(j_minus_1, one_u) < t ? 1u : 0u);
 }
 
+// The same decision for two elements at once: the fp32 adds, subtracts and
+// multiplies go through the packed f32x2 instructions (two IEEE binary32
+// operations per instruction, each lane rounded exactly as the scalar
+// operation, subnormals kept), halving their issue slots; min / max stay
+// scalar.  Bit for bit equal to two index_biased calls.
+__device__ __forceinline__ uint64_t pack_f2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 unpack_f2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub_rn_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul_rn_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_rm_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rm.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ void index_biased2(float x0, float x1, uint64_t m2, uint64_t sc2, float L, uint32_t r0,
+                                              uint32_t r1, uint32_t &a0, uint32_t &a1) {
+    float2 t = unpack_f2(mul_rn_f2(sub_rn_f2(pack_f2(x0, x1), m2), sc2));
+    t.x = fminf(fmaxf(t.x, 0.0f), L);
+    t.y = fminf(fmaxf(t.y, 0.0f), L);
+    const uint64_t jm = add_rm_f2(pack_f2(t.x, t.y), pack_f2(8388608.0f, 8388608.0f));
+    const uint64_t j_minus_1 = sub_rn_f2(jm, pack_f2(8388609.0f, 8388609.0f));
+    const uint64_t one_u = pack_f2(__uint_as_float((r0 & 0x007FFFFFu) | 0x3F800000u),
+                                   __uint_as_float((r1 & 0x007FFFFFu) | 0x3F800000u));
+    const float2 c = unpack_f2(add_rm_f2(j_minus_1, one_u));
+    const float2 j = unpack_f2(jm);
+    a0 = __float_as_uint(j.x) + (c.x < t.x ? 1u : 0u);
+    a1 = __float_as_uint(j.y) + (c.y < t.y ? 1u : 0u);
+}
+
 __device__ __forceinline__ uint4 philox_block(int64_t q, int worker, const PhiloxKeys &k) {
     return philox10(make_uint4(static_cast<uint32_t>(q), static_cast<uint32_t>(static_cast<uint64_t>(q) >> 32),
                                static_cast<uint32_t>(worker), 0u),
@@ -337,7 +383,8 @@ struct FusedParams {
 // Constants of one launch: range, quantization scale, decode step.
 struct Coder {
     float m, sc, k, km;
-    uint32_t bias;  // P * 0x4B000000 (mod 2^32): removed once from each index sum
+    uint64_t m2, sc2;  // (m, m) and (sc, sc) as f32x2 operands
+    uint32_t bias;     // P * 0x4B000000 (mod 2^32): removed once from each index sum
 };
 
 template <class Prm>
@@ -347,6 +394,8 @@ __device__ __forceinline__ Coder make_coder(const Prm &p) {
     c.sc = range_scale(c.m, p.mM[1], p.L);
     c.k = decode_step(p.mM, p.L, p.fp, c.km);
     c.bias = static_cast<uint32_t>(p.P) * 0x4B000000u;
+    c.m2 = pack_f2(c.m, c.m);
+    c.sc2 = pack_f2(c.sc, c.sc);
     return c;
 }
 
@@ -359,10 +408,16 @@ __device__ __forceinline__ void fused_one_worker(const float4 (&v)[G], uint32_t 
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         const uint4 r = philox_block((e0 >> 2) + g, p.wid[wk], p.keys);
-        const uint32_t a0 = index_biased(v[g].x, c.m, c.sc, p.L, r.x);
-        const uint32_t a1 = index_biased(v[g].y, c.m, c.sc, p.L, r.y);
-        const uint32_t a2 = index_biased(v[g].z, c.m, c.sc, p.L, r.z);
-        const uint32_t a3 = index_biased(v[g].w, c.m, c.sc, p.L, r.w);
+        uint32_t a0, a1, a2, a3;
+        if constexpr (B == 1) {  // 32 elements a word: the paired form would spill registers
+            a0 = index_biased(v[g].x, c.m, c.sc, p.L, r.x);
+            a1 = index_biased(v[g].y, c.m, c.sc, p.L, r.y);
+            a2 = index_biased(v[g].z, c.m, c.sc, p.L, r.z);
+            a3 = index_biased(v[g].w, c.m, c.sc, p.L, r.w);
+        } else {
+            index_biased2(v[g].x, v[g].y, c.m2, c.sc2, p.L, r.x, r.y, a0, a1);
+            index_biased2(v[g].z, v[g].w, c.m2, c.sc2, p.L, r.z, r.w, a2, a3);
+        }
         s[4 * g] += a0;
         s[4 * g + 1] += a1;
         s[4 * g + 2] += a2;
