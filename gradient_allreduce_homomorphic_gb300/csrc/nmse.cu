@@ -3,9 +3,10 @@
 // Two launches, deterministic: (1) each CTA folds its grid-stride slice into
 // one (sum (x - x_hat)^2, sum x^2) pair of doubles in the caller's
 // workspace; (2) one CTA adds the pairs in a fixed order and divides.
-// Per-element terms are formed in fp32 (eight at a time, summed pairwise) and
-// accumulated in fp64: fp64 throughput on this part is a small fraction of
-// fp32, and the few fp32 roundings per term keep the result within 2e-6 of an
+// Per-element terms are formed in fp32 (sixteen at a time, summed pairwise)
+// and accumulated in fp64: fp64 throughput on this part is a small fraction
+// of fp32, and the few fp32 roundings per term (at most 2 + 4 on the way to
+// the fp64 sum, about 4e-7 relative) keep the result within 2e-6 of an
 // all-fp64 sum.
 #include <cstring>
 #include <mutex>
@@ -66,19 +67,27 @@ nmse_partial_kernel(const float *__restrict__ x, const float *__restrict__ xh, i
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     int64_t first = 0;
     if (vec) {
-        // two float4 pairs per iteration (i and i + stride: both loads coalesced),
-        // eight terms summed pairwise in fp32 before each fp64 accumulation
+        // four float4 pairs per iteration (i + k * stride, k < 4: every load
+        // coalesced, eight in flight), sixteen terms summed pairwise in fp32
+        // before each fp64 accumulation: fp64 adds and conversions run at a
+        // small fraction of the fp32 rate on this part, and at one per eight
+        // terms they, not HBM, bounded the kernel
         const int64_t nv = N / 4;
         const float4 *x4 = reinterpret_cast<const float4 *>(x);
         const float4 *h4 = reinterpret_cast<const float4 *>(xh);
         int64_t i = tid;
-        for (; i + stride < nv; i += 2 * stride) {
-            const float4 a0 = __ldcs(x4 + i), a1 = __ldcs(x4 + i + stride);
-            const float4 b0 = __ldcs(h4 + i), b1 = __ldcs(h4 + i + stride);
-            num += static_cast<double>(__fadd_rn(sq_diff4(a0, b0), sq_diff4(a1, b1)));
-            den += static_cast<double>(__fadd_rn(sq4(a0), sq4(a1)));
+        for (; i + 3 * stride < nv; i += 4 * stride) {
+            float4 a[4], b[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                a[k] = __ldcs(x4 + i + k * stride);
+                b[k] = __ldcs(h4 + i + k * stride);
+            }
+            num += static_cast<double>(__fadd_rn(__fadd_rn(sq_diff4(a[0], b[0]), sq_diff4(a[1], b[1])),
+                                                 __fadd_rn(sq_diff4(a[2], b[2]), sq_diff4(a[3], b[3]))));
+            den += static_cast<double>(__fadd_rn(__fadd_rn(sq4(a[0]), sq4(a[1])), __fadd_rn(sq4(a[2]), sq4(a[3]))));
         }
-        if (i < nv) {
+        for (; i < nv; i += stride) {
             const float4 a0 = __ldcs(x4 + i), b0 = __ldcs(h4 + i);
             num += static_cast<double>(sq_diff4(a0, b0));
             den += static_cast<double>(sq4(a0));

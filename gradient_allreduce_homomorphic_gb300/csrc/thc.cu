@@ -16,6 +16,7 @@
 //   1 + u is the float with mantissa r mod 2^23.
 // No integer<->float conversion is needed per element.
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <vector>
 
@@ -518,9 +519,12 @@ __global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_ker
 // vectors when every pointer of the tensor is 16-byte aligned), and runs of
 // the words between them (a tensor's first and last word shared with a
 // neighbour or a gap, the buffer's ragged last word) taken element by
-// element.  Pieces are cut into tiles of kThreads words that CTAs stride
-// over; the piece of a tile is found once per tile, uniform over the CTA.
+// element.  Pieces are cut into tiles of kPlanTileWords words, one CTA per
+// tile; the piece of a tile is found once per tile, uniform over the CTA.
 constexpr int kPlanPtrs = 2048, kPlanSegs = 128, kPlanPieces = 2 * kPlanSegs + 1;
+// Words per tile: two per thread, so that the per-CTA set-up (the range's
+// divisions, the piece search) is paid once per 2 x P x E element-workers.
+constexpr int kPlanTileWords = 2 * kThreads;
 constexpr int kPieceVec = 0, kPieceTensor = 1, kPieceMixed = 2;
 
 struct PlanSeg {
@@ -646,15 +650,19 @@ __global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_pla
             else hi = mid - 1;
         }
         const PlanPiece pc = p.piece[lo];
-        const int64_t w = pc.w0 + (t - p.tile_start[lo]) * kThreads + threadIdx.x;
-        if (w >= pc.w1) continue;
-        if (pc.kind == kPieceVec) {
-            const int64_t off = w * E - p.seg[pc.seg].begin;
-            fused_word_vec<B, kPacked>(p, c, p.src + pc.seg * p.P, off, p.out[pc.seg] + off, w);
-        } else if ((w + 1) * E <= p.N) {
-            plan_word_gather<B, kPacked>(p, c, w, pc.kind == kPieceTensor ? pc.seg : -1);
-        } else {
-            plan_word_ragged<B, kPacked>(p, c, w);
+        const int64_t w0 = pc.w0 + (t - p.tile_start[lo]) * kPlanTileWords + threadIdx.x;
+#pragma unroll 1
+        for (int u = 0; u < kPlanTileWords / kThreads; ++u) {
+            const int64_t w = w0 + u * kThreads;
+            if (w >= pc.w1) break;
+            if (pc.kind == kPieceVec) {
+                const int64_t off = w * E - p.seg[pc.seg].begin;
+                fused_word_vec<B, kPacked>(p, c, p.src + pc.seg * p.P, off, p.out[pc.seg] + off, w);
+            } else if ((w + 1) * E <= p.N) {
+                plan_word_gather<B, kPacked>(p, c, w, pc.kind == kPieceTensor ? pc.seg : -1);
+            } else {
+                plan_word_ragged<B, kPacked>(p, c, w);
+            }
         }
     }
 }
@@ -1108,7 +1116,11 @@ template <int B>
 static int launch_plan(const ThcPlanParams &p, bool packed, cudaStream_t stream) {
     if (p.total_tiles <= 0) return GAR_OK;
     // one CTA per tile: the block scheduler balances the SMs (see the ring kernel)
-    const unsigned grid = static_cast<unsigned>(p.total_tiles < 0x7FFFFFFF ? p.total_tiles : 0x7FFFFFFF);
+    unsigned grid = static_cast<unsigned>(p.total_tiles < 0x7FFFFFFF ? p.total_tiles : 0x7FFFFFFF);
+    if (const char *ev = getenv("GAR_PROBE_THC_CTAS_PER_SM")) {  // PROBE ONLY
+        const int k = atoi(ev);
+        if (k > 0 && static_cast<int64_t>(grid) > static_cast<int64_t>(sm_count()) * k) grid = sm_count() * k;
+    }
     if (packed)
         thc_fused_plan_kernel<B, true><<<grid, kThreads, 0, stream>>>(p);
     else
@@ -1150,7 +1162,7 @@ static void plan_pieces(ThcPlanParams &p, const bool *vec, int E, int64_t w_begi
             if ((all[i].kind == kPieceVec) != (pass == 1)) continue;
             p.piece[m] = all[i];
             p.tile_start[m] = tiles;
-            tiles += ceil_div(all[i].w1 - all[i].w0, kThreads);
+            tiles += ceil_div(all[i].w1 - all[i].w0, kPlanTileWords);
             ++m;
         }
     }
