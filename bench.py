@@ -79,6 +79,19 @@ def _config(n_params, n_buffers, **extra):
     return c
 
 
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The largest `value` over all ranks (every rank gets it); `value` itself
+    when running alone.  `device`: where the reduction tensor lives (a CUDA
+    device for NCCL, None for CPU backends such as gloo)."""
+    if dist is None:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
@@ -375,10 +388,7 @@ def run_ours(args, rank, world, dist):
     ms = start.elapsed_time(stop) / args.steps
     stage_ms = {s: float(np.mean([evs[i][s][0].elapsed_time(evs[i][s][1]) for i in range(args.steps)]))
                 for s in st.stages}
-    if dist is not None:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     overlap_evs = evs if args.schedule == "overlap" else None
 
     # ---- the same steps with every kernel alone on one stream: per-kernel
@@ -424,10 +434,7 @@ def run_ours(args, rank, world, dist):
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     nmse_vals = host_nmse.numpy().tolist()
     assert all(np.isfinite(nmse_vals)), nmse_vals
 
@@ -545,7 +552,7 @@ def run_reference(args, rank, world):
     import oracle
 
     oracle.build()
-    budget = 100.0  # seconds of oracle work for the whole --steps/--warmup run
+    budget = float(args.reference_budget_s)  # seconds of oracle work for the whole --steps/--warmup run
     reps = args.steps + args.warmup
     ss, host = time_oracle(budget, reps)
     for i in range(args.warmup):
@@ -577,6 +584,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--schedule", choices=["overlap", "serial"], default="overlap")
     ap.add_argument("--h2d-streams", type=int, default=2, help="copy streams for the end-to-end inputs")
+    ap.add_argument("--reference-budget-s", type=float, default=100.0,
+                    help="seconds of oracle work for the whole --impl reference run")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -95,6 +95,8 @@ def _load():
                 "oracle_rht_signs": (C.c_int, [i64, u64, vp]),
                 "oracle_rht": (C.c_int, [vp, i64, u64, C.c_int, vp]),
                 "oracle_rht_norm_range": (None, [pp, C.c_int, i64, C.c_double, vp, vp]),
+                "oracle_ef_apply": (None, [vp, vp, vp, i64]),
+                "oracle_ef_update": (None, [vp, vp, vp, i64]),
                 "oracle_nmse": (C.c_double, [vp, vp, i64]),
                 "oracle_nmse_f64": (C.c_double, [vp, vp, i64]),
             }
@@ -433,6 +435,24 @@ def rht_norm_range(xs, t_p: float):
     m, M = C.c_double(0), C.c_double(0)
     _load().oracle_rht_norm_range(_ptrs(vs), len(vs), vs[0].size, float(t_p), C.byref(m), C.byref(M))
     return m.value, M.value
+
+
+def ef_apply(grad, e) -> np.ndarray:
+    """Error feedback before compression: x = grad + e (fp32)."""
+    g = np.ascontiguousarray(grad, np.float32)
+    ev = np.ascontiguousarray(e, np.float32)
+    x = np.empty_like(g)
+    _load().oracle_ef_apply(_ptr(g), _ptr(ev), _ptr(x), g.size)
+    return x
+
+
+def ef_update(x, x_hat) -> np.ndarray:
+    """Error feedback after decompression: e = x - x_hat (fp32)."""
+    xv = np.ascontiguousarray(x, np.float32)
+    hv = np.ascontiguousarray(x_hat, np.float32)
+    e = np.empty_like(xv)
+    _load().oracle_ef_update(_ptr(e), _ptr(xv), _ptr(hv), xv.size)
+    return e
 
 
 def nmse(x, x_hat) -> float:

@@ -725,6 +725,14 @@ int oracle_rht(const double *in, int64_t n, uint64_t seed, int inverse, double *
     return 0;
 }
 
+void oracle_ef_apply(const float *grad, const float *e, float *x, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) x[i] = grad[i] + e[i];
+}
+
+void oracle_ef_update(float *e, const float *x, const float *x_hat, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) e[i] = x[i] - x_hat[i];
+}
+
 void oracle_rht_norm_range(const double *const *x, int p, int64_t n, double t_p, double *m,
                            double *M) {
     double l = 0.0;

@@ -168,6 +168,12 @@ void oracle_rht_norm_range(const double *const *x, int p, int64_t n, double t_p,
                            double *M);
 
 /* ---------------- NMSE [T] ---------------- */
+/* Error feedback ([T] section 5): x = grad + e before the rotation, and
+ * e = x - x_hat after it (x_hat: the worker's own quantized vector, decoded
+ * and rotated back).  fp32, one rounding per element. */
+void oracle_ef_apply(const float *grad, const float *e, float *x, int64_t n);
+void oracle_ef_update(float *e, const float *x, const float *x_hat, int64_t n);
+
 double oracle_nmse(const float *x, const float *x_hat, int64_t n);
 double oracle_nmse_f64(const double *x, const double *x_hat, int64_t n);
 
