@@ -109,64 +109,88 @@ struct Range {
         lo = fminf(lo, v);
         hi = fmaxf(hi, v);
     }
+    // two values per instruction: sm_100's three-input min / max (NaN
+    // inputs are skipped, as by fminf / fmaxf)
+    __device__ __forceinline__ void add2(float a, float b) {
+        asm("min.f32 %0, %0, %1, %2;" : "+f"(lo) : "f"(a), "f"(b));
+        asm("max.f32 %0, %0, %1, %2;" : "+f"(hi) : "f"(a), "f"(b));
+    }
+    template <int V>
+    __device__ __forceinline__ void add_vec(const float (&v)[V]) {
+#pragma unroll
+        for (int q = 0; q < V; q += 2) add2(v[q], v[q + 1]);
+    }
 };
 
-// Fold one 16-byte vector at element e of row `row`, ring order from worker c.
+// The workers of one tile's fold, in ring order from the piece's chunk
+// (src[k] = the input of worker (c + k) mod P, or (c - k) mod P on the
+// counter-clockwise ring), and the row's destinations: set once per tile in
+// shared memory, so that each load and store takes one broadcast shared load
+// for its pointer instead of the ring index arithmetic and an indexed
+// parameter load.
+struct TileTables {
+    const void *src[GAR_MAX_WORKERS];
+    void *dst[GAR_MAX_WORKERS];
+};
+
+// Fold one 16-byte vector at element e of the tile's row, in ring order:
+// acc = x_0 + x_1 + ... + x_{P-1} over tt.src, left to right in fp32.
 template <typename T, bool kRange, class Prm>
-__device__ __forceinline__ void fold_vec(const Prm &p, int row, int c, int ccw, int64_t e, Range &rg) {
+__device__ __forceinline__ void fold_vec(const Prm &p, const TileTables &tt, int64_t e, Range &rg) {
     constexpr int V = Elem<T>::kVec;
     const int P = p.P;
-    const void *const *src = p.src + static_cast<int64_t>(row) * P;
     float acc[V];
-    for (int k0 = 0; k0 < P; k0 += kLoadBatch) {
-        uint4 raw[kLoadBatch];
+    uint4 raw[kLoadBatch];
+    // first batch, its first worker peeled off (it starts the sum)
 #pragma unroll
-        for (int j = 0; j < kLoadBatch; ++j) {
-            if (k0 + j < P) {
-                const int w = ring_worker(c, k0 + j, ccw, P);
-                raw[j] = ld16(static_cast<const T *>(src[w]) + e);
-            }
+    for (int j = 0; j < kLoadBatch; ++j)
+        if (j < P) raw[j] = ld16(static_cast<const T *>(tt.src[j]) + e);
+    Elem<T>::unpack(raw[0], acc);
+    if (kRange) rg.add_vec(acc);
+#pragma unroll
+    for (int j = 1; j < kLoadBatch; ++j) {
+        if (j < P) {
+            float v[V];
+            Elem<T>::unpack(raw[j], v);
+            if (kRange) rg.add_vec(v);
+#pragma unroll
+            for (int q = 0; q < V; ++q) acc[q] = __fadd_rn(acc[q], v[q]);
         }
+    }
+    for (int k0 = kLoadBatch; k0 < P; k0 += kLoadBatch) {
+#pragma unroll
+        for (int j = 0; j < kLoadBatch; ++j)
+            if (k0 + j < P) raw[j] = ld16(static_cast<const T *>(tt.src[k0 + j]) + e);
 #pragma unroll
         for (int j = 0; j < kLoadBatch; ++j) {
             if (k0 + j < P) {
                 float v[V];
                 Elem<T>::unpack(raw[j], v);
-                if (kRange) {
+                if (kRange) rg.add_vec(v);
 #pragma unroll
-                    for (int q = 0; q < V; ++q) rg.add(v[q]);
-                }
-                if (k0 + j == 0) {
-#pragma unroll
-                    for (int q = 0; q < V; ++q) acc[q] = v[q];
-                } else {
-#pragma unroll
-                    for (int q = 0; q < V; ++q) acc[q] = __fadd_rn(acc[q], v[q]);
-                }
+                for (int q = 0; q < V; ++q) acc[q] = __fadd_rn(acc[q], v[q]);
             }
         }
     }
 #pragma unroll
     for (int q = 0; q < V; ++q) acc[q] = finish(p, acc[q]);
     const uint4 out = Elem<T>::pack(acc);
-    void *const *dst = p.dst + static_cast<int64_t>(row) * p.n_out;
-    for (int k = 0; k < p.n_out; ++k) st16(static_cast<T *>(dst[k]) + e, out);
+#pragma unroll 4
+    for (int k = 0; k < p.n_out; ++k) st16(static_cast<T *>(tt.dst[k]) + e, out);
 }
 
 template <typename T, bool kRange, class Prm>
-__device__ __forceinline__ void fold_one(const Prm &p, int row, int c, int ccw, int64_t e, Range &rg) {
+__device__ __forceinline__ void fold_one(const Prm &p, const TileTables &tt, int64_t e, Range &rg) {
     const int P = p.P;
-    const void *const *src = p.src + static_cast<int64_t>(row) * P;
-    float acc = Elem<T>::load1(src[c], e);
+    float acc = Elem<T>::load1(tt.src[0], e);
     if (kRange) rg.add(acc);
     for (int k = 1; k < P; ++k) {
-        const float v = Elem<T>::load1(src[ring_worker(c, k, ccw, P)], e);
+        const float v = Elem<T>::load1(tt.src[k], e);
         if (kRange) rg.add(v);
         acc = __fadd_rn(acc, v);
     }
     acc = finish(p, acc);
-    void *const *dst = p.dst + static_cast<int64_t>(row) * p.n_out;
-    for (int k = 0; k < p.n_out; ++k) Elem<T>::store1(dst[k], e, acc);
+    for (int k = 0; k < p.n_out; ++k) Elem<T>::store1(tt.dst[k], e, acc);
 }
 
 __device__ __forceinline__ void atomic_min_f(float *a, float v) {
@@ -213,6 +237,7 @@ __device__ __forceinline__ void flush_range(Range rg, float *range, int slot) {
 template <typename T, class Prm, bool kRange>
 __global__ void __launch_bounds__(kThreads, kRange ? kRangeMinBlocks : 4) ring_fold_kernel(const __grid_constant__ Prm p) {
     constexpr int V = Elem<T>::kVec;
+    __shared__ TileTables tt;
     Range rg;
     int slot = -1;
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
@@ -230,6 +255,11 @@ __global__ void __launch_bounds__(kThreads, kRange ? kRangeMinBlocks : 4) ring_f
             slot = p.slot[lo];
         }
         const int64_t lt = t - p.tile_start[lo];
+        __syncthreads();  // the previous tile's readers are done with tt
+        if (threadIdx.x < p.P)
+            tt.src[threadIdx.x] = p.src[static_cast<int64_t>(pc.row) * p.P + ring_worker(pc.chunk, threadIdx.x, pc.ccw, p.P)];
+        if (threadIdx.x < p.n_out) tt.dst[threadIdx.x] = p.dst[static_cast<int64_t>(pc.row) * p.n_out + threadIdx.x];
+        __syncthreads();
         if (pc.vec) {
             int64_t vb = (pc.begin + V - 1) / V * V;
             if (vb > pc.end) vb = pc.end;
@@ -239,20 +269,20 @@ __global__ void __launch_bounds__(kThreads, kRange ? kRangeMinBlocks : 4) ring_f
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int64_t i = lt * kTileUnits + u * kThreads + threadIdx.x;
-                if (i < nvec) fold_vec<T, kRange>(p, pc.row, pc.chunk, pc.ccw, vb + i * V, rg);
+                if (i < nvec) fold_vec<T, kRange>(p, tt, vb + i * V, rg);
             }
             if (lt == 0) {  // ragged head and tail of the piece (fewer than V each)
                 const int head = static_cast<int>(vb - pc.begin);
                 const int tail = static_cast<int>(pc.end - ve);
-                if (threadIdx.x < head) fold_one<T, kRange>(p, pc.row, pc.chunk, pc.ccw, pc.begin + threadIdx.x, rg);
+                if (threadIdx.x < head) fold_one<T, kRange>(p, tt, pc.begin + threadIdx.x, rg);
                 else if (threadIdx.x >= 32 && threadIdx.x < 32 + tail)
-                    fold_one<T, kRange>(p, pc.row, pc.chunk, pc.ccw, ve + (threadIdx.x - 32), rg);
+                    fold_one<T, kRange>(p, tt, ve + (threadIdx.x - 32), rg);
             }
         } else {
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int64_t e = pc.begin + lt * kTileUnits + u * kThreads + threadIdx.x;
-                if (e < pc.end) fold_one<T, kRange>(p, pc.row, pc.chunk, pc.ccw, e, rg);
+                if (e < pc.end) fold_one<T, kRange>(p, tt, e, rg);
             }
         }
     }
