@@ -575,6 +575,223 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------- all five workloads
+def _median_ms(torch, fn, iters, flush=None):
+    """Median device time of fn() over `iters` calls (CUDA events on the
+    current stream, 3 warm-up calls); `flush` runs untimed before each call."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(iters):
+        if flush is not None:
+            flush()
+        s.record()
+        fn()
+        e.record()
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    return float(np.median(times))
+
+
+def _gpu_line(name, ms, nbytes, inbytes, elems, peak):
+    return {"ms": round(ms, 4), "gbs_reduced": round(inbytes / (ms * 1e-3) / 1e9, 1),
+            "elements_per_s": round(elems / (ms * 1e-3), 1),
+            "algorithmic_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "hbm_frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4), "what": name}
+
+
+def _cpu_time(fn, reps=3):
+    """Median wall time of fn() (the oracle, one core) over `reps` calls."""
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        fn()
+        ts.append(time.perf_counter() - t0)
+    return float(np.median(ts))
+
+
+def run_configs(args):
+    """Every workload of the pages' configurations on this GPU through the
+    library (one JSON line each), with the oracle timed on one host core on a
+    bounded sample of the same workload."""
+    import torch
+
+    import gradient_allreduce_homomorphic_gb300 as g
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g.load()
+    peak, _ = _peaks()
+    it = args.config_iters
+    l2 = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)  # 256 MB > the 129 MB L2
+    flush = l2.zero_
+    oracle = None
+    if not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+    out = []
+    seed = workloads.THC_SEED
+    cores = 1
+
+    # C1: four workers, one 4 MB partition (fits in L2: flushed before each call)
+    P, N = 4, 1 << 20
+    cfg = workloads.CONFIG_IDS["partition_4mb"]
+    x = [workloads.device_normal(N, 1.0, 1000 * cfg + w, torch.float32, dev) for w in range(P)]
+    buf = [t.clone() for t in x]
+    tb, tx = g.pointer_table(buf), g.pointer_table(x)
+    mM = torch.empty(2, device=dev)
+    avg = torch.empty(N, device=dev)
+    words = g.gar_thc_words(N, 4)
+    packed = [torch.empty(words, dtype=torch.int32, device=dev) for _ in range(P)]
+    tp = g.pointer_table(packed)
+    ring_ms = _median_ms(torch, lambda: g.gar_ring_allreduce_sim(tb), it, flush)
+
+    def thc():
+        g.gar_thc_range(tx, mM)
+        g.gar_thc_allreduce_fused(tx, 4, seed, mM, avg, tp)
+
+    thc_ms = _median_ms(torch, thc, it, flush)
+    line = {"config": "partition_4mb: P=4, N=2^20 fp32 N(0,1); ring average + THC b=4 (range, fused)",
+            "l2": "flushed before each call (256 MB written)",
+            "gpu": {"ring": _gpu_line("gar_ring_allreduce_sim, in place", ring_ms, 2 * P * N * 4, P * N * 4,
+                                      P * N, peak),
+                    "thc": _gpu_line("gar_thc_range + gar_thc_allreduce_fused (wire vectors written)", thc_ms,
+                                     P * N * 4 + P * N * 4 + N * 4 + P * words * 4, P * N * 4, P * N, peak)}}
+    if oracle is not None:
+        n = 1 << 18
+        hx = workloads.workers_normal(P, n, 1.0, cfg)
+        t_ring = _cpu_time(lambda: oracle.ring_fold(hx))
+        t_thc = _cpu_time(lambda: oracle.thc_allreduce(hx, 4, seed))
+        line["oracle"] = {"sample": f"P=4 x 2^18", "cores": cores,
+                          "ring_gbs": round(P * n * 4 / t_ring / 1e9, 4),
+                          "thc_gbs": round(P * n * 4 / t_thc / 1e9, 4)}
+    out.append(line)
+    del x, buf, packed, avg
+    torch.cuda.empty_cache()
+
+    # C2: the main benchmark's workload and step (two streams)
+    st = Step(torch, g, dev)
+    for i in range(3):
+        st.run(i)
+    step_ms = _median_ms(torch, lambda: st.run(7), it)
+    algo = st.algorithmic_bytes()
+    line = {"config": "resnet_fusion: P=8, 300 fp32 tensors (45M params), 64 MB fusion buffers; ring average "
+                      "with range + THC b=4 over the plan + NMSE (the main benchmark step)",
+            "l2": "inputs (1.44 GB) larger than L2",
+            "gpu": {"step": _gpu_line("one bench step", step_ms, sum(algo.values()), 8 * st.n_params * 4,
+                                      8 * st.n_params, peak)}}
+    if oracle is not None:
+        ss, host = sample_workload(300_000)
+        t = _cpu_time(lambda: oracle_step(ss, host, seed), reps=1)
+        line["oracle"] = {"sample": f"first {ss.size} tensors ({int(ss.sum())} params) x 8 workers, one step",
+                          "cores": cores, "step_gbs": round(8 * int(ss.sum()) * 4 / t / 1e9, 4)}
+    out.append(line)
+    del st
+    torch.cuda.empty_cache()
+
+    # C3: VGG-16-like, communication bound: fused pack + ring + unpack, in place
+    P = 8
+    cfg = workloads.CONFIG_IDS["vgg_fusion"]
+    sizes = workloads.vgg_fusion_sizes()
+    n = int(sizes.sum())
+    dt = np.zeros(sizes.size, np.int32)
+    plan = g.gar_fusion_plan(sizes, dt, CAPACITY, ALIGN)
+    flat = [workloads.device_normal(n, 1e-3, 1000 * cfg + w, torch.float32, dev) for w in range(P)]
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    src = [[f[int(offs[i]):int(offs[i + 1])] for i in range(sizes.size)] for f in flat]
+    tables = g.fused_pointer_tables(src, src)
+    ms = _median_ms(torch, lambda: g.gar_fused_allreduce(src, src, plan, tables=tables), it)
+    line = {"config": "vgg_fusion: P=8, 16 fp32 tensors (138M params, largest 102.8M), 64 MB fusion buffers; "
+                      "fused pack + ring average + unpack, in place",
+            "l2": "inputs (4.4 GB) larger than L2",
+            "gpu": {"fused_ring": _gpu_line("gar_fused_allreduce", ms, 2 * P * n * 4, P * n * 4, P * n, peak)}}
+    if oracle is not None:
+        ss = sizes[:6]
+        hs = [workloads.tensors_normal(ss, 1e-3, cfg, w) for w in range(P)]
+
+        def vgg_oracle():
+            sb, so, bn = oracle.fusion_plan(ss, np.zeros(ss.size, np.int32), CAPACITY, ALIGN)
+            for b in range(len(bn)):
+                fbs = [oracle.fusion_pack(hs[w], sb, so, b, bn[b]) for w in range(P)]
+                oracle.fusion_unpack(oracle.ring_fold(fbs), sb, so, ss, b)
+
+        t = _cpu_time(vgg_oracle, reps=1)
+        line["oracle"] = {"sample": f"first 6 tensors ({int(ss.sum())} params) x 8 workers", "cores": cores,
+                          "fused_ring_gbs": round(P * int(ss.sum()) * 4 / t / 1e9, 4)}
+    out.append(line)
+    del flat, src, tables
+    torch.cuda.empty_cache()
+
+    # C4: THC sweep on heavy-tailed gradients, P in {4, 16, 64}, b in {2, 4, 8}
+    N = 1 << 24
+    cfg = workloads.CONFIG_IDS["thc_sweep"]
+    sweep = []
+    for P in (4, 16, 64):
+        x = [workloads.device_student_t(N, 3, 1e-3, 1000 * cfg + w, dev) for w in range(P)]
+        tx = g.pointer_table(x)
+        exact = torch.empty(N, device=dev)
+        g.gar_ring_allreduce_sim_out(tx, g.pointer_table([exact]))
+        mM = torch.empty(2, device=dev)
+        avg = torch.empty(N, device=dev)
+        nm = torch.empty(1, dtype=torch.float64, device=dev)
+        ws = torch.empty(g.gar_nmse_workspace_bytes(N) // 8 + 1, dtype=torch.float64, device=dev)
+        range_ms = _median_ms(torch, lambda: g.gar_thc_range(tx, mM), it)
+        nmse_ms = _median_ms(torch, lambda: g.gar_nmse(exact, avg, nm, ws), it)
+        for b in (2, 4, 8):
+            words = g.gar_thc_words(N, b)
+            packed = [torch.empty(words, dtype=torch.int32, device=dev) for _ in range(P)]
+            tp = g.pointer_table(packed)
+            fused_ms = _median_ms(torch, lambda: g.gar_thc_allreduce_fused(tx, b, seed, mM, avg, tp), it)
+            g.gar_nmse(exact, avg, nm, ws)
+            torch.cuda.synchronize()
+            fb = P * N * 4 + N * 4 + P * words * 4
+            sweep.append({"P": P, "b": b, "nmse": round(float(nm.item()), 6),
+                          "range": _gpu_line("gar_thc_range", range_ms, P * N * 4, P * N * 4, P * N, peak),
+                          "fused": _gpu_line("gar_thc_allreduce_fused (wire vectors written)", fused_ms, fb,
+                                             P * N * 4, P * N, peak),
+                          "nmse_kernel": _gpu_line("gar_nmse", nmse_ms, 2 * N * 4, 2 * N * 4, N, peak),
+                          "round_gbs_reduced": round(P * N * 4 / ((range_ms + fused_ms) * 1e-3) / 1e9, 1)})
+            del packed
+        del x, exact
+        torch.cuda.empty_cache()
+    line = {"config": "thc_sweep: N=2^24 fp32 Student-t(3) x 1e-3 per worker, P in {4,16,64}, b in {2,4,8}; "
+                      "range, fused encode/aggregate/decode, NMSE against the exact (ring) average",
+            "l2": "inputs (256 MB to 4 GB) larger than L2", "gpu": sweep}
+    if oracle is not None:
+        n = 1 << 16
+        o = []
+        for P in (4, 16, 64):
+            hx = [workloads.student_t_f32(n, 3, 1e-3, cfg, w) for w in range(P)]
+            t = _cpu_time(lambda: oracle.thc_allreduce(hx, 4, seed), reps=1)
+            o.append({"P": P, "b": 4, "thc_gbs": round(P * n * 4 / t / 1e9, 4)})
+        line["oracle"] = {"sample": "N=2^16 per worker", "cores": cores, "thc": o}
+    out.append(line)
+
+    # C5: large bf16 bucket: P=16 x 2^28 bf16, fp32 accumulation in ring order
+    P, N = 16, 1 << 28
+    cfg = workloads.CONFIG_IDS["large_bf16"]
+    x = [workloads.device_normal(N, 1e-2, 1000 * cfg + w, torch.bfloat16, dev) for w in range(P)]
+    tx = g.pointer_table(x)
+    ms = _median_ms(torch, lambda: g.gar_ring_allreduce_sim(tx), max(3, it // 4))
+    line = {"config": "large_bf16: P=16, N=2^28 bf16 N(0, 1e-2) per worker (8 GiB); ring average in place, "
+                      "fp32 accumulation in ring order, bf16 out",
+            "l2": "inputs (8 GiB) larger than L2",
+            "gpu": {"ring": _gpu_line("gar_ring_allreduce_sim (bf16)", ms, 2 * P * N * 2, P * N * 2, P * N, peak)}}
+    if oracle is not None:
+        n = 1 << 18
+        hx = [workloads.normal_f32(n, 1e-2, cfg, w) for w in range(P)]
+        hb = [(a.view(np.uint32) >> 16).astype(np.uint16) for a in hx]  # bf16 bits (truncated): timing input only
+        t = _cpu_time(lambda: oracle.ring_fold(hb))
+        line["oracle"] = {"sample": "P=16 x 2^18", "cores": cores, "ring_gbs": round(P * n * 2 / t / 1e9, 4)}
+    out.append(line)
+    del x
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -586,12 +803,19 @@ def main():
     ap.add_argument("--h2d-streams", type=int, default=2, help="copy streams for the end-to-end inputs")
     ap.add_argument("--reference-budget-s", type=float, default=100.0,
                     help="seconds of oracle work for the whole --impl reference run")
+    ap.add_argument("--configs", action="store_true",
+                    help="time every workload configuration (one JSON line each) instead of the benchmark step")
+    ap.add_argument("--config-iters", type=int, default=20)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     dist = None
+    if args.configs:
+        for line in run_configs(args):
+            print(json.dumps(line))
+        return
     if args.impl == "reference":
         out = run_reference(args, rank, world)
     else:

@@ -261,9 +261,10 @@ __global__ void __launch_bounds__(kThreads, kRange ? kRangeMinBlocks : 4) ring_f
         if (threadIdx.x < p.n_out) tt.dst[threadIdx.x] = p.dst[static_cast<int64_t>(pc.row) * p.n_out + threadIdx.x];
         __syncthreads();
         if (pc.vec) {
-            int64_t vb = (pc.begin + V - 1) / V * V;
+            const int sh = pc.vec - 1;  // the row's pointers' common phase
+            int64_t vb = (pc.begin + sh + V - 1) / V * V - sh;
             if (vb > pc.end) vb = pc.end;
-            int64_t ve = pc.end / V * V;
+            int64_t ve = (pc.end + sh) / V * V - sh;
             if (ve < vb) ve = vb;
             const int64_t nvec = (ve - vb) / V;
 #pragma unroll
@@ -343,13 +344,26 @@ static int64_t piece_tiles(const Piece &pc, int V) {
         const int64_t t = ceil_div(pc.end - pc.begin, kTileUnits);
         return t > 0 ? t : 1;
     }
-    int64_t vb = (pc.begin + V - 1) / V * V;
+    const int sh = pc.vec - 1;
+    int64_t vb = (pc.begin + sh + V - 1) / V * V - sh;
     if (vb > pc.end) vb = pc.end;
-    int64_t ve = pc.end / V * V;
+    int64_t ve = (pc.end + sh) / V * V - sh;
     if (ve < vb) ve = vb;
     const int64_t t = ceil_div((ve - vb) / V, kTileUnits);
     return t > 0 ? t : 1;
 }
+
+// Common phase of a row's pointers: 1 + s when every pointer lies s elements
+// (of es bytes) past a 16-byte line, the same s for all; 0 when they differ.
+struct PhaseOf {
+    int es;
+    int sh = -1;  // -1 before the first pointer, -2 once two differ
+    void add(const void *ptr) {
+        const int s = static_cast<int>((reinterpret_cast<uintptr_t>(ptr) & 15) / es);
+        sh = sh == -1 ? s : (sh == s ? sh : -2);
+    }
+    int vec() const { return sh >= 0 ? 1 + sh : 0; }
+};
 
 template <class Prm>
 static void finalize_tiles(Prm &p, int V) {
@@ -390,17 +404,17 @@ static int ring_single_impl(Prm &p, const void *const *src, void *const *dst, in
     set_mode(p, op, P);
     const int es = elem_bytes(dtype);
     if (N == 0) return GAR_OK;  // nothing is read or written: pointers may be NULL
-    bool vec = true;
+    PhaseOf phase{es};
     for (int w = 0; w < P; ++w) {
         if (!src[w]) return fail(GAR_EINVAL, "input buffer %d is NULL", w);
         if (!aligned(src[w], es)) return fail(GAR_EALIGN, "input buffer %d not aligned to %d bytes", w, es);
-        vec = vec && aligned(src[w], 16);
+        phase.add(src[w]);
         p.src[w] = src[w];
     }
     for (int k = 0; k < n_out; ++k) {
         if (!dst[k]) return fail(GAR_EINVAL, "output buffer %d is NULL", k);
         if (!aligned(dst[k], es)) return fail(GAR_EALIGN, "output buffer %d not aligned to %d bytes", k, es);
-        vec = vec && aligned(dst[k], 16);
+        phase.add(dst[k]);
         p.dst[k] = dst[k];
     }
     if (N == 0) return GAR_OK;
@@ -413,7 +427,7 @@ static int ring_single_impl(Prm &p, const void *const *src, void *const *dst, in
         Piece &pc = p.piece[p.npieces++];
         pc.row = 0;
         pc.chunk = k < P ? k : k - P;
-        pc.vec = vec ? 1 : 0;
+        pc.vec = phase.vec();
         pc.ccw = k < P ? 0 : 1;
         pc.begin = b;
         pc.end = e;
@@ -537,11 +551,12 @@ int fused_allreduce_impl(const void *const *src, void *const *dst, int32_t P, co
             const int need = static_cast<int>(last_chunk - first_chunk + 1);
             if ((rows + 1) * P > kLargePtrs || p->npieces + need > kLargePieces) rc = flush();
             if (rc) break;
-            bool vec = true;
+            PhaseOf phase{elem_bytes(pass_dtype)};
             for (int w = 0; w < P; ++w) {
                 const void *s = src[static_cast<int64_t>(w) * count + i];
                 void *d = dst[static_cast<int64_t>(w) * count + i];
-                vec = vec && aligned(s, 16) && aligned(d, 16);
+                phase.add(s);
+                phase.add(d);
                 p->src[rows * P + w] = s;
                 p->dst[rows * P + w] = d;
             }
@@ -554,7 +569,7 @@ int fused_allreduce_impl(const void *const *src, void *const *dst, int32_t P, co
                 Piece &pc = p->piece[p->npieces++];
                 pc.row = rows;
                 pc.chunk = static_cast<int32_t>(c);
-                pc.vec = vec ? 1 : 0;
+                pc.vec = phase.vec();
                 pc.ccw = 0;
                 p->slot[p->npieces - 1] = b;
                 pc.begin = pos;

@@ -12,7 +12,8 @@ namespace gar {
 struct Piece {
     int32_t row;    // row of the pointer tables (one tensor)
     int32_t chunk;  // ring chunk id = first worker of the fold
-    int32_t vec;    // 1: all of the row's pointers are 16-byte aligned
+    int32_t vec;    // 0: element by element; 1 + s: every pointer of the row lies s elements past a
+                    // 16-byte line (the same s for all), so element e is on a line iff (e + s) % V == 0
     int32_t ccw;    // 1: the fold runs x_c, x_{c-1}, ... (counter-clockwise ring)
     int64_t begin;  // first element, in the tensor's own indexing
     int64_t end;    // one past the last element

@@ -147,6 +147,38 @@ def test_fused_unaligned_tensors(env):
             same_bits(to_host(dst[w][i]), ref[w][i])
 
 
+@pytest.mark.parametrize("inplace", [False, True])
+def test_fused_common_phase_views(env, inplace):
+    """Unpadded views of one flat buffer per worker (tensor i starts at the sum
+    of the sizes before it): the tensors are not 16-byte aligned, but all of a
+    tensor's pointers share one phase, so the fold runs in 16-byte vectors
+    after a short scalar head -- with the same sums as the oracle."""
+    torch, g = env
+    P = 8
+    sizes = np.array([5, 1, 4099, 3, 70001, 2, 9, 40000, 7, 123457], np.int64)
+    dtype = np.zeros(sizes.size, np.int32)
+    plan = g.gar_fusion_plan(sizes, dtype, 256 << 10, 16)
+    sb, so, bn = oracle.fusion_plan(sizes, dtype, 256 << 10, 16)
+    host = [workloads.tensors_normal(sizes, 1.0, 94, w) for w in range(P)]
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+
+    def views(flat):
+        return [flat[int(offs[i]):int(offs[i + 1])] for i in range(sizes.size)]
+
+    src_flat = [to_dev(np.concatenate(row), torch) for row in host]
+    src = [views(f) for f in src_flat]
+    if inplace:
+        dst = src
+    else:
+        dst_flat = [torch.zeros(int(offs[-1]), device="cuda") for _ in range(P)]
+        dst = [views(f) for f in dst_flat]
+    g.gar_fused_allreduce(src, dst, plan, op=g.GAR_AVG)
+    ref = _oracle_fused(host, sizes, dtype, sb, so, bn, oracle.AVG)
+    for w in range(P):
+        for i in range(sizes.size):
+            same_bits(to_host(dst[w][i]), ref[w][i])
+
+
 def test_resnet_fusion_full_size(env):
     # 300 fp32 tensors (~45M parameters), P=8, N(0, 0.01), 64 MB fusion buffers
     torch, g = env
