@@ -16,7 +16,6 @@
 //   1 + u is the float with mantissa r mod 2^23.
 // No integer<->float conversion is needed per element.
 #include <algorithm>
-#include <cstdlib>
 #include <cstring>
 #include <vector>
 
@@ -1116,11 +1115,7 @@ template <int B>
 static int launch_plan(const ThcPlanParams &p, bool packed, cudaStream_t stream) {
     if (p.total_tiles <= 0) return GAR_OK;
     // one CTA per tile: the block scheduler balances the SMs (see the ring kernel)
-    unsigned grid = static_cast<unsigned>(p.total_tiles < 0x7FFFFFFF ? p.total_tiles : 0x7FFFFFFF);
-    if (const char *ev = getenv("GAR_PROBE_THC_CTAS_PER_SM")) {  // PROBE ONLY
-        const int k = atoi(ev);
-        if (k > 0 && static_cast<int64_t>(grid) > static_cast<int64_t>(sm_count()) * k) grid = sm_count() * k;
-    }
+    const unsigned grid = static_cast<unsigned>(p.total_tiles < 0x7FFFFFFF ? p.total_tiles : 0x7FFFFFFF);
     if (packed)
         thc_fused_plan_kernel<B, true><<<grid, kThreads, 0, stream>>>(p);
     else
