@@ -319,7 +319,7 @@ PER_OF_STAGE = {
 }
 # stage -> committed ncu summary holding its per-step DRAM traffic
 PROFILE_OF_STAGE = {"ring": ("ring_fold_kernel_range_resnet_fusion", ["ring.cu", "ring.cuh", "common.cuh"]),
-                    "thc": ("thc_fused_plan_kernel_resnet_fusion", ["thc.cu", "common.cuh"])}
+                    "thc": ("thc_fused_plan_kernel_resnet_fusion", ["thc.cu", "thc_fused.cuh", "thc_p8.cu", "common.cuh"])}
 
 
 def kernel_source_hash(files):

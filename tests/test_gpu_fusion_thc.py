@@ -141,7 +141,7 @@ def test_fused_allreduce_range_slices_and_errors(env):
 
 
 @pytest.mark.parametrize("trial", range(5))
-@pytest.mark.parametrize("P", [1, 3, 8])
+@pytest.mark.parametrize("P", [1, 3, 4, 8, 16])
 @pytest.mark.parametrize("b", [1, 2, 4, 8])
 def test_thc_plan_equals_pack_thc_unpack(env, trial, P, b):
     torch, g = env

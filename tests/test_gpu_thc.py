@@ -73,7 +73,7 @@ def test_encode(env, b, N):
 
 
 @pytest.mark.parametrize("b", [1, 2, 4, 8])
-@pytest.mark.parametrize("P,N", [(1, 77), (3, 1000), (4, 4096), (16, 5003), (64, 1027)])
+@pytest.mark.parametrize("P,N", [(1, 77), (3, 1000), (4, 4096), (8, 3001), (16, 5003), (64, 1027)])
 def test_aggregate_decode_fused(env, b, P, N):
     torch, g = env
     seed = 0x5EED + P
