@@ -76,6 +76,8 @@ _SIGNATURES = {
     "gar_nmse_workspace_bytes": (C.c_size_t, [_i64]),
     "gar_nmse": (C.c_int, [_vp, _vp, _i64, _vp, _vp, C.c_size_t, _vp]),
     "gar_nmse_noalloc": (C.c_int, [_vp, _vp, _i64, _vp, _vp]),
+    "gar_nmse_sums": (C.c_int, [_vp, _vp, _i64, _vp, _vp, C.c_size_t, _vp]),
+    "gar_nmse_combine": (C.c_int, [_vp, _i32, _vp, _vp]),
 }
 
 
@@ -413,6 +415,17 @@ def gar_nmse_workspace_bytes(N: int) -> int:
 def gar_nmse(x, x_hat, d_out, workspace, stream=None):
     nbytes = workspace.numel() * workspace.element_size()
     _call("gar_nmse", _dev(x), _dev(x_hat), x.numel(), _dev(d_out), _dev(workspace), nbytes, _stream(stream))
+
+
+def gar_nmse_sums(x, x_hat, d_pair, workspace, stream=None):
+    """(sum (x - x_hat)^2, sum x^2) of one range into d_pair (2 fp64, device)."""
+    nbytes = workspace.numel() * workspace.element_size()
+    _call("gar_nmse_sums", _dev(x), _dev(x_hat), x.numel(), _dev(d_pair), _dev(workspace), nbytes, _stream(stream))
+
+
+def gar_nmse_combine(d_pairs, d_out, stream=None):
+    """NMSE from the pairs of gar_nmse_sums (d_pairs: [n, 2] fp64, device)."""
+    _call("gar_nmse_combine", _dev(d_pairs), d_pairs.numel() // 2, _dev(d_out), _stream(stream))
 
 
 def gar_nmse_noalloc(x, x_hat, d_out, stream=None):

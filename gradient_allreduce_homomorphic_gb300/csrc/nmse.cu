@@ -116,6 +116,32 @@ __global__ void __launch_bounds__(kThreads) nmse_final_kernel(const double *ws, 
     if (threadIdx.x == 0) *out = den == 0.0 ? __longlong_as_double(0x7FF8000000000000ll) : num / den;
 }
 
+// The two sums of one range, (sum (x - x_hat)^2, sum x^2), added in the same
+// fixed order as nmse_final_kernel but not divided.
+__global__ void __launch_bounds__(kThreads) nmse_pair_kernel(const double *ws, int nblocks, double *pair) {
+    double num = 0.0, den = 0.0;
+    for (int i = threadIdx.x; i < nblocks; i += kThreads) {
+        num += ws[2 * i];
+        den += ws[2 * i + 1];
+    }
+    block_sum2(num, den);
+    if (threadIdx.x == 0) {
+        pair[0] = num;
+        pair[1] = den;
+    }
+}
+
+// NMSE from n pairs: both sums added in pair order (one thread: n is small),
+// then divided.
+__global__ void nmse_combine_kernel(const double *pairs, int n, double *out) {
+    double num = 0.0, den = 0.0;
+    for (int i = 0; i < n; ++i) {
+        num += pairs[2 * i];
+        den += pairs[2 * i + 1];
+    }
+    *out = den == 0.0 ? __longlong_as_double(0x7FF8000000000000ll) : num / den;
+}
+
 }  // namespace
 }  // namespace gar
 
@@ -142,6 +168,32 @@ extern "C" int gar_nmse(const float *x, const float *x_hat, int64_t N, double *d
     if (rc) return rc;
     nmse_final_kernel<<<1, kThreads, 0, stream>>>(ws, g, d_out);
     return check_launch("nmse_final_kernel");
+}
+
+extern "C" int gar_nmse_sums(const float *x, const float *x_hat, int64_t N, double *d_pair, void *d_workspace,
+                             size_t workspace_bytes, gar_stream_t stream_) {
+    if (N < 0 || !d_pair || !d_workspace) return fail(GAR_EINVAL, "N < 0 or NULL argument");
+    if (N > 0 && (!x || !x_hat)) return fail(GAR_EINVAL, "x or x_hat is NULL");
+    if (workspace_bytes < gar_nmse_workspace_bytes(N))
+        return fail(GAR_EINVAL, "workspace of %zu bytes < %zu needed", workspace_bytes, gar_nmse_workspace_bytes(N));
+    if (!aligned(d_workspace, 8) || !aligned(d_pair, 8)) return fail(GAR_EALIGN, "workspace or d_pair not 8-byte aligned");
+    if ((x && !aligned(x, 4)) || (x_hat && !aligned(x_hat, 4))) return fail(GAR_EALIGN, "x or x_hat not 4-byte aligned");
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const int g = nmse_blocks(N);
+    const int vec = aligned(x, 16) && aligned(x_hat, 16);
+    double *ws = static_cast<double *>(d_workspace);
+    nmse_partial_kernel<<<g, kThreads, 0, stream>>>(x, x_hat, N, vec, ws);
+    int rc = check_launch("nmse_partial_kernel");
+    if (rc) return rc;
+    nmse_pair_kernel<<<1, kThreads, 0, stream>>>(ws, g, d_pair);
+    return check_launch("nmse_pair_kernel");
+}
+
+extern "C" int gar_nmse_combine(const double *d_pairs, int32_t n, double *d_out, gar_stream_t stream_) {
+    if (n < 1 || !d_pairs || !d_out) return fail(GAR_EINVAL, "n < 1 or NULL argument");
+    if (!aligned(d_pairs, 8) || !aligned(d_out, 8)) return fail(GAR_EALIGN, "d_pairs or d_out not 8-byte aligned");
+    nmse_combine_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(d_pairs, n, d_out);
+    return check_launch("nmse_combine_kernel");
 }
 
 // ---------------------------------------------------------------------------

@@ -447,6 +447,26 @@ size_t gar_nmse_workspace_bytes(int64_t N);
 int gar_nmse(const float *x, const float *x_hat, int64_t N, double *d_out, void *d_workspace,
              size_t workspace_bytes, gar_stream_t stream);
 
+/* gar_nmse_sums -- the two sums of NMSE ([T] section 2) over one range, not
+ * divided: d_pair[0] = sum (x - x_hat)^2, d_pair[1] = sum x^2, with the
+ * per-element terms and summation order of gar_nmse (gar_nmse_combine of this
+ * one pair gives gar_nmse's result bit for bit).  NMSE over a vector held in
+ * several ranges -- the fusion buffers of a plan, averaged one after another,
+ * or the slices of a vector split across devices -- is gar_nmse_combine of
+ * their pairs.  x, x_hat: device, N fp32 (4-byte aligned).  d_pair: device,
+ * two doubles (8-byte aligned).  d_workspace: as for gar_nmse, not shared with
+ * a concurrent call.
+ * Errors: GAR_EINVAL (null, N < 0, workspace too small), GAR_EALIGN,
+ *         GAR_ECUDA. */
+int gar_nmse_sums(const float *x, const float *x_hat, int64_t N, double *d_pair, void *d_workspace,
+                  size_t workspace_bytes, gar_stream_t stream);
+
+/* gar_nmse_combine -- *d_out = (sum of d_pairs[2i]) / (sum of d_pairs[2i+1])
+ * over i < n, each sum added in index order in fp64; NaN when the second sum
+ * is 0.  d_pairs: device, n pairs from gar_nmse_sums (8-byte aligned).
+ * Errors: GAR_EINVAL (n < 1, null), GAR_EALIGN, GAR_ECUDA. */
+int gar_nmse_combine(const double *d_pairs, int32_t n, double *d_out, gar_stream_t stream);
+
 /* gar_nmse_noalloc -- no counterpart in the pages: a library convenience.
  * The same NMSE as gar_nmse (same kernels, same summation order, same result)
  * for callers that cannot provide a workspace because they may not allocate

@@ -269,3 +269,40 @@ def test_nmse(env, N):
     assert np.isnan(out.item())
     with pytest.raises(g.GarError):
         g.gar_nmse(to_dev(x, torch), to_dev(xh, torch), out, ws[:0])
+
+
+@pytest.mark.parametrize("cuts", [(0, 1000), (0, 1, 4097, 4100, 70001), (0, 3, 4, 65536, 65537, 100000)])
+def test_nmse_sums_over_ranges(env, cuts):
+    """NMSE of a vector held in several ranges (one per fusion buffer, or per
+    device): the ranges' pairs of sums, combined, match the oracle's NMSE of
+    the whole vector; one range combined alone equals gar_nmse bit for bit."""
+    torch, g = env
+    N = cuts[-1]
+    x = _xs(1, N, 8)[0]
+    xh = (x + _xs(1, N, 9, 0.05)[0]).astype(np.float32)
+    xd, hd = to_dev(x, torch), to_dev(xh, torch)
+    ws = torch.empty(g.gar_nmse_workspace_bytes(N) // 8, dtype=torch.float64, device="cuda")
+    pairs = torch.full((len(cuts) - 1, 2), float("nan"), dtype=torch.float64, device="cuda")
+    for k in range(len(cuts) - 1):
+        lo, hi = cuts[k], cuts[k + 1]
+        g.gar_nmse_sums(xd[lo:hi], hd[lo:hi], pairs[k], ws)
+    out = torch.empty(1, dtype=torch.float64, device="cuda")
+    g.gar_nmse_combine(pairs, out)
+    ref = oracle.nmse(x, xh)
+    assert abs(out.item() - ref) <= 2e-6 * ref
+    # each pair's sums against fp64 sums of the same range
+    p = pairs.cpu().numpy()
+    for k in range(len(cuts) - 1):
+        lo, hi = cuts[k], cuts[k + 1]
+        d = x[lo:hi].astype(np.float64) - xh[lo:hi].astype(np.float64)
+        assert abs(p[k, 0] - np.sum(d * d)) <= 2e-6 * np.sum(d * d) + 1e-300
+        assert abs(p[k, 1] - np.sum(x[lo:hi].astype(np.float64) ** 2)) <= 2e-6 * np.sum(x[lo:hi].astype(np.float64) ** 2)
+    # a single range, combined, is gar_nmse's result exactly
+    whole = torch.empty(1, dtype=torch.float64, device="cuda")
+    g.gar_nmse(xd, hd, whole, ws)
+    one = torch.empty((1, 2), dtype=torch.float64, device="cuda")
+    g.gar_nmse_sums(xd, hd, one[0], ws)
+    g.gar_nmse_combine(one, out)
+    assert out.item() == whole.item()
+    with pytest.raises(g.GarError):
+        g.gar_nmse_combine(pairs[:0], out)
