@@ -119,37 +119,71 @@ struct EncodeParams {
     int32_t pad;
 };
 
+// One full word of E = 32 / B elements (four per float4 group): indices
+// packed LSB first, the decision as in the fused kernels.
+template <int B>
+__device__ __forceinline__ uint32_t encode_word(const float4 (&v)[32 / B / 4], int64_t e0, const EncodeParams &p,
+                                                float m, float sc, uint64_t m2, uint64_t sc2) {
+    constexpr int G = 32 / B / 4;
+    uint32_t word = 0;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const uint4 r = philox_block((e0 >> 2) + g, p.worker, p.keys);
+        uint32_t a0, a1, a2, a3;
+        if constexpr (B == 1) {
+            a0 = index_biased(v[g].x, m, sc, p.L, r.x);
+            a1 = index_biased(v[g].y, m, sc, p.L, r.y);
+            a2 = index_biased(v[g].z, m, sc, p.L, r.z);
+            a3 = index_biased(v[g].w, m, sc, p.L, r.w);
+        } else {
+            index_biased2(v[g].x, v[g].y, m2, sc2, p.L, r.x, r.y, a0, a1);
+            index_biased2(v[g].z, v[g].w, m2, sc2, p.L, r.z, r.w, a2, a3);
+        }
+        word += (a0 << (4 * g * B)) + (a1 << ((4 * g + 1) * B)) + (a2 << ((4 * g + 2) * B)) +
+                (a3 << ((4 * g + 3) * B));
+    }
+    return word - pack_bias<B>();
+}
+
 template <int B>
 __global__ void __launch_bounds__(kThreads) thc_encode_kernel(const __grid_constant__ EncodeParams p) {
     constexpr int E = 32 / B;  // elements per packed word
+    constexpr int G = E / 4;
     const float m = p.mM[0], M = p.mM[1];
     const float sc = range_scale(m, M, p.L);
+    const uint64_t m2 = pack_f2(m, m), sc2 = pack_f2(sc, sc);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < p.nwords; w += stride) {
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    // whole words with 16-byte aligned inputs: two words a thread per step,
+    // both words' loads in flight before either is quantized
+    const int64_t nfull = p.vec ? (p.N / E < p.nwords ? p.N / E : p.nwords) : 0;
+    int64_t w = tid;
+    for (; w + stride < nfull; w += 2 * stride) {
+        float4 a[G], b[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) a[g] = __ldcs(reinterpret_cast<const float4 *>(p.x + w * E) + g);
+#pragma unroll
+        for (int g = 0; g < G; ++g) b[g] = __ldcs(reinterpret_cast<const float4 *>(p.x + (w + stride) * E) + g);
+        __stcs(p.packed + w, encode_word<B>(a, w * E, p, m, sc, m2, sc2));
+        __stcs(p.packed + w + stride, encode_word<B>(b, (w + stride) * E, p, m, sc, m2, sc2));
+    }
+    for (; w < nfull; w += stride) {
+        float4 a[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) a[g] = __ldcs(reinterpret_cast<const float4 *>(p.x + w * E) + g);
+        __stcs(p.packed + w, encode_word<B>(a, w * E, p, m, sc, m2, sc2));
+    }
+    // the ragged last word, or unaligned inputs: element by element
+    for (w = nfull + tid; w < p.nwords; w += stride) {
         const int64_t e0 = w * E;
         uint32_t word = 0;
-        if (p.vec && e0 + E <= p.N) {
-            float4 v[E / 4];
-#pragma unroll
-            for (int g = 0; g < E / 4; ++g) v[g] = __ldcs(reinterpret_cast<const float4 *>(p.x + e0) + g);
-#pragma unroll
-            for (int g = 0; g < E / 4; ++g) {
-                const uint4 r = philox_block((e0 >> 2) + g, p.worker, p.keys);
-                const uint32_t i0 = index_biased(v[g].x, m, sc, p.L, r.x) - 0x4B000000u;
-                const uint32_t i1 = index_biased(v[g].y, m, sc, p.L, r.y) - 0x4B000000u;
-                const uint32_t i2 = index_biased(v[g].z, m, sc, p.L, r.z) - 0x4B000000u;
-                const uint32_t i3 = index_biased(v[g].w, m, sc, p.L, r.w) - 0x4B000000u;
-                word |= (i0 | (i1 << B) | (i2 << (2 * B)) | (i3 << (3 * B))) << (4 * g * B);
-            }
-        } else {
-            for (int g = 0; g < E / 4; ++g) {
-                const int64_t eb = e0 + 4 * g;
-                if (eb >= p.N) break;
-                const uint4 r = philox_block(eb >> 2, p.worker, p.keys);
-                for (int i = 0; i < 4 && eb + i < p.N; ++i) {
-                    const uint32_t idx = index_biased(p.x[eb + i], m, sc, p.L, pick(r, i)) - 0x4B000000u;
-                    word |= idx << ((4 * g + i) * B);
-                }
+        for (int g = 0; g < G; ++g) {
+            const int64_t eb = e0 + 4 * g;
+            if (eb >= p.N) break;
+            const uint4 r = philox_block(eb >> 2, p.worker, p.keys);
+            for (int i = 0; i < 4 && eb + i < p.N; ++i) {
+                const uint32_t idx = index_biased(p.x[eb + i], m, sc, p.L, pick(r, i)) - 0x4B000000u;
+                word |= idx << ((4 * g + i) * B);
             }
         }
         __stcs(p.packed + w, word);
@@ -242,10 +276,11 @@ __global__ void __launch_bounds__(kThreads) thc_decode_kernel(const __grid_const
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     int64_t first = 0;
     if (p.vec) {
+        // eight sums per 16-byte load; four loads a thread in flight before
+        // the first is decoded
         const int64_t n8 = p.N / 8;
-        for (int64_t i = tid; i < n8; i += stride) {
-            const uint4 s = __ldcs(reinterpret_cast<const uint4 *>(p.sums) + i);
-            const uint32_t w[4] = {s.x, s.y, s.z, s.w};
+        auto decode8 = [&](const uint4 &sv, int64_t i) {
+            const uint32_t w[4] = {sv.x, sv.y, sv.z, sv.w};
             float o[8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -255,7 +290,16 @@ __global__ void __launch_bounds__(kThreads) thc_decode_kernel(const __grid_const
             float4 *dst = reinterpret_cast<float4 *>(p.avg) + 2 * i;
             __stcs(dst, make_float4(o[0], o[1], o[2], o[3]));
             __stcs(dst + 1, make_float4(o[4], o[5], o[6], o[7]));
+        };
+        int64_t i = tid;
+        for (; i + 3 * stride < n8; i += 4 * stride) {
+            uint4 sv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) sv[u] = __ldcs(reinterpret_cast<const uint4 *>(p.sums) + i + u * stride);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) decode8(sv[u], i + u * stride);
         }
+        for (; i < n8; i += stride) decode8(__ldcs(reinterpret_cast<const uint4 *>(p.sums) + i), i);
         first = n8 * 8;
     }
     for (int64_t e = first + tid; e < p.N; e += stride)
