@@ -272,41 +272,64 @@ class Step:
         self.s_d2h = torch.cuda.Stream(device=self.dev)
         self.ev_in = [[torch.cuda.Event() for _ in self.s_h2d] for _ in range(self.nb)]
         self.ev_out = [torch.cuda.Event() for _ in range(self.nb)]
+        self.ev_read = [torch.cuda.Event() for _ in range(self.nb)]  # buffer b's inputs consumed
+        self.ev_sent = [torch.cuda.Event() for _ in range(self.nb)]  # buffer b's outputs copied out
         self.ev_nmse = torch.cuda.Event()
+        self.ev_nmse_sent = torch.cuda.Event()
+
+    def start_e2e(self):
+        """Order the copy streams after everything queued so far (the start of
+        a timed region)."""
+        main = self.torch.cuda.current_stream()
+        for s in self.s_h2d + [self.s_d2h]:
+            s.wait_stream(main)
+
+    def finish_e2e(self):
+        """Join the copy streams into the current stream (the end of a timed
+        region: the last results are on the host)."""
+        main = self.torch.cuda.current_stream()
+        for s in self.s_h2d + [self.s_d2h]:
+            main.wait_stream(s)
 
     def run_e2e(self, step_idx, host_in, host_ring, host_thc, host_nmse):
         """One step from pinned host gradients to host averages and NMSE,
         pipelined by fusion buffer: buffer b+1's inputs cross the link (the
         workers split over the copy streams) while buffer b is averaged, and
-        b's results travel back meanwhile."""
+        b's results travel back meanwhile.  Consecutive steps overlap too: a
+        buffer's inputs for this step are copied in as soon as the previous
+        step has consumed that buffer's inputs, and its averages are
+        overwritten only once the previous step's have been copied out."""
         g, torch = self.g, self.torch
         seed = workloads.THC_SEED + step_idx
         main = torch.cuda.current_stream()
         plan = g.gar_fusion_plan(self.sizes, self.dtype, CAPACITY, ALIGN)
-        for s in self.s_h2d:
-            s.wait_stream(main)
         k = len(self.s_h2d)
         for b, part in enumerate(self.parts):
             lo, hi = part["lo"], part["hi"]
             for j, s in enumerate(self.s_h2d):
+                s.wait_event(self.ev_read[b])
                 with torch.cuda.stream(s):
                     for w in range(j, P, k):
                         self.flat[w][lo:hi].copy_(host_in[w][lo:hi], non_blocking=True)
                     self.ev_in[b][j].record(s)
                 main.wait_event(self.ev_in[b][j])
+            main.wait_event(self.ev_sent[b])
             self._buffer_ring(plan, b, main)
             self._buffer_thc(plan, b, seed, main)
+            self.ev_read[b].record(main)
             self.ev_out[b].record(main)
             self.s_d2h.wait_event(self.ev_out[b])
             with torch.cuda.stream(self.s_d2h):
                 host_ring[lo:hi].copy_(self.ring_flat[0][lo:hi], non_blocking=True)
                 host_thc[lo:hi].copy_(self.thc_flat[lo:hi], non_blocking=True)
+                self.ev_sent[b].record(self.s_d2h)
+        main.wait_event(self.ev_nmse_sent)  # the previous step's NMSE is on the host
         g.gar_nmse(self.ring_flat[0], self.thc_flat, self.nmse, self.ws, stream=main)
         self.ev_nmse.record(main)
         self.s_d2h.wait_event(self.ev_nmse)
         with torch.cuda.stream(self.s_d2h):
             host_nmse.copy_(self.nmse, non_blocking=True)
-        main.wait_stream(self.s_d2h)
+            self.ev_nmse_sent.record(self.s_d2h)
 
 
 KERNEL_OF_STAGE = {"ring": "ring_fold_kernel", "thc": "thc_fused_plan_kernel",
@@ -423,14 +446,18 @@ def run_ours(args, rank, world, dist):
     def e2e_step(i):
         st.run_e2e(10_000 + i, host_in, host_ring, host_thc, host_nmse)
 
-    for i in range(2):
+    st.start_e2e()
+    for i in range(3):
         e2e_step(i)
+    st.finish_e2e()
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
+    st.start_e2e()
     for i in range(e2e_steps):
-        e2e_step(2 + i)
+        e2e_step(3 + i)
+    st.finish_e2e()
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
