@@ -8,11 +8,13 @@ log-uniform sizes 256..2.4M, N(0, 0.01)), 64 MB fusion buffers:
   2. per fusion buffer: Tensor Fusion + ring all-reduce     gar_fused_allreduce_range
      average in one pass (pack, ring, unpack), the buffer's
      THC range [min, max] taken from the same reads
-  3. per fusion buffer: THC encode (every worker) +         gar_thc_allreduce_fused_plan
+  3. per fusion buffer: THC encode (every worker) +         gar_thc_allreduce_fused_plan_nmse
      integer aggregate + decode, read straight from the
      tensors, average written straight to the output
-     tensors, wire vectors written (b = 4, fresh seed each step)
-  4. NMSE of the THC estimate against the ring average     gar_nmse
+     tensors, wire vectors written (b = 4, fresh seed each
+     step); in the same pass the sums of NMSE of the THC
+     average against the ring average
+  4. NMSE of the whole model from the buffers' sums         gar_nmse_combine
 
 The fused calls give bit for bit what pack -> ring / THC -> unpack gives
 (the tests hold them to that); the fusion buffers are never materialised.
@@ -182,7 +184,9 @@ class Step:
                        for _ in range(P)]
         self.mM = torch.empty((self.nb, 2), dtype=torch.float32, device=dev)
         self.nmse = torch.empty(1, dtype=torch.float64, device=dev)
-        self.ws = torch.empty(g.gar_nmse_workspace_bytes(self.flat_len) // 8 + 1, dtype=torch.float64, device=dev)
+        self.pairs = torch.empty((self.nb, 2), dtype=torch.float64, device=dev)  # NMSE sums per fusion buffer
+        self.ws = torch.empty(g.gar_thc_plan_nmse_workspace_bytes(self.plan, B_THC) // 8 + 1, dtype=torch.float64,
+                              device=dev)
         # host pointer tables per fusion buffer, built once (the tensors do not move)
         self.parts = []
         for b in range(self.nb):
@@ -194,6 +198,7 @@ class Step:
                 "lo": int(self.offs[first]), "hi": int(self.offs[first + cnt]),
                 "ring": g.fused_pointer_tables(src_b, [self.ring[w][rows] for w in range(P)]),
                 "thc": g.thc_plan_tables(src_b, self.thc[rows], self.packed),
+                "ref": g.pointer_table(self.ring[0][rows]),  # NMSE reference: the exact (ring) average
                 "ev": torch.cuda.Event(),
             })
         self.stream_r = torch.cuda.Stream(device=dev)
@@ -210,18 +215,20 @@ class Step:
                                          tables=part["ring"])
 
     def _buffer_thc(self, plan, b, seed, stream):
+        """THC of buffer b, with the NMSE sums of its average against the ring
+        average taken in the same pass (into pairs[b])."""
         part = self.parts[b]
         sub = plan.subplan(part["first"], part["count"])
-        self.g.gar_thc_allreduce_fused_plan(None, sub, B_THC, seed, self.mM, None, stream=stream,
-                                            tables=part["thc"])
+        self.g.gar_thc_allreduce_fused_plan_nmse(None, sub, B_THC, seed, self.mM, None, None, self.pairs[b], self.ws,
+                                                 stream=stream, tables=part["thc"], ref_table=part["ref"])
 
     def algorithmic_bytes(self):
         n = self.n_params * 4
         words = 4 * sum(self.words)
         return {
             "ring": 2 * P * n,                 # read P x n, write P x n (range from the same reads)
-            "thc": P * n + n + P * words,      # read P x n, write the average + the wire vectors
-            "nmse": 2 * self.flat_len * 4,     # read both flat averages
+            "thc": P * n + 2 * n + P * words,  # read P x n and the reference, write the average + wire vectors
+            "nmse": 16 * self.nb,              # the per-buffer pairs of sums, combined
         }
 
     def run(self, step_idx, events=None):
@@ -262,7 +269,7 @@ class Step:
             main.wait_stream(s_thc)
             main.wait_stream(s_ring)
         mark("nmse", 0, main)
-        g.gar_nmse(self.ring_flat[0], self.thc_flat, self.nmse, self.ws, stream=main)
+        g.gar_nmse_combine(self.pairs, self.nmse, stream=main)
         mark("nmse", 1, main)
 
     # ------------------------------------------------------- end to end
@@ -324,7 +331,7 @@ class Step:
                 host_thc[lo:hi].copy_(self.thc_flat[lo:hi], non_blocking=True)
                 self.ev_sent[b].record(self.s_d2h)
         main.wait_event(self.ev_nmse_sent)  # the previous step's NMSE is on the host
-        g.gar_nmse(self.ring_flat[0], self.thc_flat, self.nmse, self.ws, stream=main)
+        g.gar_nmse_combine(self.pairs, self.nmse, stream=main)
         self.ev_nmse.record(main)
         self.s_d2h.wait_event(self.ev_nmse)
         with torch.cuda.stream(self.s_d2h):
@@ -332,13 +339,14 @@ class Step:
             self.ev_nmse_sent.record(self.s_d2h)
 
 
-KERNEL_OF_STAGE = {"ring": "ring_fold_kernel", "thc": "thc_fused_plan_kernel",
-                   "nmse": "nmse_partial_kernel + nmse_final_kernel"}
+KERNEL_OF_STAGE = {"ring": "ring_fold_kernel", "thc": "thc_fused_plan_kernel (+ thc_nmse_pair_kernel)",
+                   "nmse": "nmse_combine_kernel"}
 PER_OF_STAGE = {
     "ring": "all launches of one step's 3 gar_fused_allreduce_range calls (one per fusion buffer; "
             "300 tensors x 8 workers in all)",
-    "thc": "all launches of one step's 3 gar_thc_allreduce_fused_plan calls (one per fusion buffer)",
-    "nmse": "one step's gar_nmse over the flat averages",
+    "thc": "all launches of one step's 3 gar_thc_allreduce_fused_plan_nmse calls (one per fusion buffer; "
+           "NMSE sums against the ring average taken in the same pass)",
+    "nmse": "one step's gar_nmse_combine of the 3 buffers' NMSE sums",
 }
 # stage -> committed ncu summary holding its per-step DRAM traffic
 PROFILE_OF_STAGE = {"ring": ("ring_fold_kernel_range_resnet_fusion", ["ring.cu", "ring.cuh", "common.cuh"]),

@@ -64,6 +64,9 @@ _SIGNATURES = {
     "gar_thc_allreduce_fused_masked": (C.c_int, [_pp, _i32, _u64, _i64, _i32, _u64, _vp, _vp, _pp, _vp]),
     "gar_thc_allreduce_fused_plan": (C.c_int, [_pp, _i32, _vp, _vp, _i32, _vp, _i32, _i32, _u64, _vp, _pp, _pp,
                                                _vp]),
+    "gar_thc_plan_nmse_workspace_bytes": (C.c_size_t, [_vp, _i32, _i32, _i32]),
+    "gar_thc_allreduce_fused_plan_nmse": (C.c_int, [_pp, _i32, _vp, _vp, _i32, _vp, _i32, _i32, _u64, _vp, _pp,
+                                                    _pp, _pp, _vp, _vp, C.c_size_t, _vp]),
     "gar_nuhc_encode": (C.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _u64, _i32, _vp, _vp]),
     "gar_nuhc_aggregate": (C.c_int, [_pp, _i32, _i64, _i32, _vp, _vp, _vp]),
     "gar_nuhc_decode": (C.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _vp]),
@@ -351,6 +354,24 @@ def gar_thc_allreduce_fused_plan(src, plan: FusionPlan, b: int, seed: int, d_mM,
     _call("gar_thc_allreduce_fused_plan", s.array, P, C.addressof(plan.segs), plan.dtype.ctypes.data, plan.count,
           plan.buf_numel.ctypes.data, plan.n_buffers, b, seed, _dev(d_mM), o.array,
           pk.array if pk is not None else None, _stream(stream))
+
+
+def gar_thc_plan_nmse_workspace_bytes(plan: FusionPlan, b: int) -> int:
+    return int(load().gar_thc_plan_nmse_workspace_bytes(plan.buf_numel.ctypes.data, plan.n_buffers, plan.count, b))
+
+
+def gar_thc_allreduce_fused_plan_nmse(src, plan: FusionPlan, b: int, seed: int, d_mM, out, ref, d_pair, workspace,
+                                      packed=None, stream=None, tables=None, ref_table=None):
+    """gar_thc_allreduce_fused_plan that also writes d_pair (2 fp64, device) =
+    (sum (ref - avg)^2, sum ref^2) over the call's tensors; ref[i] is the
+    reference tensor of tensor i (e.g. the ring average)."""
+    s, o, pk = tables if tables is not None else thc_plan_tables(src, out, packed)
+    r = ref_table if ref_table is not None else PtrTable(ref)
+    P = len(s) // max(plan.count, 1)
+    nbytes = workspace.numel() * workspace.element_size()
+    _call("gar_thc_allreduce_fused_plan_nmse", s.array, P, C.addressof(plan.segs), plan.dtype.ctypes.data, plan.count,
+          plan.buf_numel.ctypes.data, plan.n_buffers, b, seed, _dev(d_mM), o.array,
+          pk.array if pk is not None else None, r.array, _dev(d_pair), _dev(workspace), nbytes, _stream(stream))
 
 
 # --------------------------------------------------------- non-uniform THC

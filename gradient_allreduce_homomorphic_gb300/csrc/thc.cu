@@ -553,14 +553,55 @@ int dispatch_fused(const FusedParams &p, int b, bool packed, cudaStream_t stream
         default: return launch_fused<0>(p, b, packed, stream);
     }
 }
-int dispatch_fused_plan(const ThcPlanParams &p, int b, bool packed, cudaStream_t stream) {
+int dispatch_fused_plan(const ThcPlanParams &p, int b, bool packed, bool nmse, cudaStream_t stream) {
     switch (p.P) {
-        case 4: return launch_fused_plan<4>(p, b, packed, stream);
-        case 8: return launch_fused_plan<8>(p, b, packed, stream);
-        case 16: return launch_fused_plan<16>(p, b, packed, stream);
-        case 64: return launch_fused_plan<64>(p, b, packed, stream);
-        default: return launch_fused_plan<0>(p, b, packed, stream);
+        case 4: return launch_fused_plan<4>(p, b, packed, nmse, stream);
+        case 8: return launch_fused_plan<8>(p, b, packed, nmse, stream);
+        case 16: return launch_fused_plan<16>(p, b, packed, nmse, stream);
+        case 64: return launch_fused_plan<64>(p, b, packed, nmse, stream);
+        default: return launch_fused_plan<0>(p, b, packed, nmse, stream);
     }
+}
+
+// The NMSE pair of a plan call: the n per-CTA pairs of its launches added in
+// index order (fp64; each thread a fixed stride, then a fixed-order tree).
+__global__ void __launch_bounds__(kThreads) thc_nmse_pair_kernel(const double *ws, int64_t n, double *pair) {
+    double num = 0.0, den = 0.0;
+    for (int64_t i = threadIdx.x; i < n; i += kThreads) {
+        num += ws[2 * i];
+        den += ws[2 * i + 1];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        num += __shfl_xor_sync(0xFFFFFFFFu, num, o);
+        den += __shfl_xor_sync(0xFFFFFFFFu, den, o);
+    }
+    __shared__ double s_num[kThreads / 32], s_den[kThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        s_num[warp] = num;
+        s_den[warp] = den;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        num = 0.0;
+        den = 0.0;
+        for (int i = 0; i < kThreads / 32; ++i) {
+            num += s_num[i];
+            den += s_den[i];
+        }
+        pair[0] = num;
+        pair[1] = den;
+    }
+}
+
+// Upper bound on the CTAs (one pair each) all launches of one plan call run:
+// every piece adds at most one partial tile, a launch has at most 2 tensors + 1
+// pieces, and a buffer at most as many launches as tensors.
+int64_t plan_nmse_pairs_bound(const int64_t *buf_numel, int32_t n_buffers, int32_t count, int32_t b) {
+    int64_t tiles = 0;
+    for (int i = 0; i < n_buffers; ++i) tiles += ceil_div(gar_thc_words(buf_numel[i] > 0 ? buf_numel[i] : 0, b), kPlanTileWords);
+    return tiles + 5 * static_cast<int64_t>(count) + 3 * static_cast<int64_t>(n_buffers) + 1;
 }
 
 
@@ -789,15 +830,30 @@ static void plan_pieces(ThcPlanParams &p, const bool *vec, int E, int64_t w_begi
     p.total_tiles = tiles;
 }
 
-extern "C" int gar_thc_allreduce_fused_plan(const float *const *src, int32_t P, const gar_seg *segs,
-                                            const int32_t *dtype, int32_t count, const int64_t *buf_numel,
-                                            int32_t n_buffers, int32_t b, uint64_t seed, const float *d_mM,
-                                            float *const *out, uint32_t *const *packed, gar_stream_t stream_) {
+// Uniform THC over a plan; with ref != NULL also the NMSE pair of the call
+// (per-CTA pairs in ws, added by one more kernel into d_pair).
+static int thc_plan_impl(const float *const *src, int32_t P, const gar_seg *segs, const int32_t *dtype,
+                         int32_t count, const int64_t *buf_numel, int32_t n_buffers, int32_t b, uint64_t seed,
+                         const float *d_mM, float *const *out, uint32_t *const *packed, const float *const *ref,
+                         double *d_pair, double *ws, size_t ws_bytes, gar_stream_t stream_) {
     if (!valid_b(b)) return fail(GAR_EINVAL, "b=%d not in {1, 2, 4, 8}", b);
     if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
     if (static_cast<int64_t>(P) * ((1 << b) - 1) > 65535) return fail(GAR_EOVERFLOW, "P * (2^b - 1) > 65535");
     if (count < 0 || n_buffers < 0) return fail(GAR_EINVAL, "count or n_buffers < 0");
-    if (count == 0) return GAR_OK;
+    const bool nmse = ref != nullptr;
+    if (nmse) {
+        if (!d_pair || !ws) return fail(GAR_EINVAL, "d_pair or the workspace is NULL");
+        if (!aligned(d_pair, 8) || !aligned(ws, 8)) return fail(GAR_EALIGN, "d_pair or the workspace not 8-byte aligned");
+        if (count > 0 && !buf_numel) return fail(GAR_EINVAL, "NULL argument");
+        const size_t need = 16 * static_cast<size_t>(plan_nmse_pairs_bound(buf_numel, n_buffers, count, b));
+        if (ws_bytes < need) return fail(GAR_EINVAL, "workspace of %zu bytes < %zu needed", ws_bytes, need);
+    }
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (count == 0) {
+        if (!nmse) return GAR_OK;
+        thc_nmse_pair_kernel<<<1, kThreads, 0, stream>>>(ws, 0, d_pair);  // no elements: (0, 0)
+        return check_launch("thc_nmse_pair_kernel");
+    }
     if (!src || !segs || !dtype || !buf_numel || !d_mM || !out) return fail(GAR_EINVAL, "NULL argument");
     if (!aligned(d_mM, 4)) return fail(GAR_EALIGN, "d_mM not 4-byte aligned");
     std::vector<int64_t> cursor(n_buffers, 0);
@@ -816,6 +872,8 @@ extern "C" int gar_thc_allreduce_fused_plan(const float *const *src, int32_t P, 
             if (!sp) return fail(GAR_EINVAL, "worker %d tensor %d pointer is NULL", w, i);
             if (!aligned(sp, 4)) return fail(GAR_EALIGN, "worker %d tensor %d not 4-byte aligned", w, i);
         }
+        if (nmse && (!ref[i] || !aligned(ref[i], 4)))
+            return fail(ref[i] ? GAR_EALIGN : GAR_EINVAL, "reference %d NULL or not 4-byte aligned", i);
         members[sg.buffer].push_back(i);
     }
     ThcPlanParams *p = new ThcPlanParams;  // ~29 KB: keep it off the stack
@@ -828,8 +886,8 @@ extern "C" int gar_thc_allreduce_fused_plan(const float *const *src, int32_t P, 
     const int E = 32 / b;
     const int cap = std::min(kPlanSegs, kPlanPtrs / P);  // >= 32 >= E: a word meets at most E tensors
     bool vec[kPlanSegs];
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     int rc = GAR_OK;
+    int64_t used = 0;  // NMSE pairs written so far (one per CTA)
     for (int bf = 0; bf < n_buffers && rc == GAR_OK; ++bf) {
         const std::vector<int> &mem = members[bf];
         if (mem.empty()) continue;
@@ -867,7 +925,7 @@ extern "C" int gar_thc_allreduce_fused_plan(const float *const *src, int32_t P, 
                 PlanSeg &sg = p->seg[k];
                 sg.begin = segs[i].offset;
                 sg.end = segs[i].offset + segs[i].numel;
-                bool v = (sg.begin % 4 == 0) && aligned(out[i], 16);
+                bool v = (sg.begin % 4 == 0) && aligned(out[i], 16) && (!nmse || aligned(ref[i], 16));
                 for (int w = 0; w < P; ++w) {
                     const float *sp = src[static_cast<int64_t>(w) * count + i];
                     p->src[k * P + w] = sp;
@@ -875,14 +933,46 @@ extern "C" int gar_thc_allreduce_fused_plan(const float *const *src, int32_t P, 
                 }
                 vec[k] = v;
                 p->out[k] = out[i];
+                p->ref[k] = nmse ? ref[i] : nullptr;
             }
             plan_pieces(*p, vec, E, w0, w1);
-            rc = dispatch_fused_plan(*p, b, packed != nullptr, stream);
+            if (nmse) p->nmse_ws = ws + 2 * used;
+            rc = dispatch_fused_plan(*p, b, packed != nullptr, nmse, stream);
+            if (p->total_tiles > 0) used += plan_grid(*p);
             w0 = w1;
         }
     }
     delete p;
+    if (rc == GAR_OK && nmse) {
+        thc_nmse_pair_kernel<<<1, kThreads, 0, stream>>>(ws, used, d_pair);
+        rc = check_launch("thc_nmse_pair_kernel");
+    }
     return rc;
+}
+
+extern "C" int gar_thc_allreduce_fused_plan(const float *const *src, int32_t P, const gar_seg *segs,
+                                            const int32_t *dtype, int32_t count, const int64_t *buf_numel,
+                                            int32_t n_buffers, int32_t b, uint64_t seed, const float *d_mM,
+                                            float *const *out, uint32_t *const *packed, gar_stream_t stream) {
+    return thc_plan_impl(src, P, segs, dtype, count, buf_numel, n_buffers, b, seed, d_mM, out, packed, nullptr,
+                         nullptr, nullptr, 0, stream);
+}
+
+extern "C" size_t gar_thc_plan_nmse_workspace_bytes(const int64_t *buf_numel, int32_t n_buffers, int32_t count,
+                                                    int32_t b) {
+    if (!valid_b(b) || n_buffers < 0 || count < 0 || (n_buffers > 0 && !buf_numel)) return 0;
+    return 16 * static_cast<size_t>(plan_nmse_pairs_bound(buf_numel, n_buffers, count, b));
+}
+
+extern "C" int gar_thc_allreduce_fused_plan_nmse(const float *const *src, int32_t P, const gar_seg *segs,
+                                                 const int32_t *dtype, int32_t count, const int64_t *buf_numel,
+                                                 int32_t n_buffers, int32_t b, uint64_t seed, const float *d_mM,
+                                                 float *const *out, uint32_t *const *packed,
+                                                 const float *const *ref, double *d_pair, void *d_workspace,
+                                                 size_t workspace_bytes, gar_stream_t stream) {
+    if (!ref) return fail(GAR_EINVAL, "ref is NULL");
+    return thc_plan_impl(src, P, segs, dtype, count, buf_numel, n_buffers, b, seed, d_mM, out, packed, ref, d_pair,
+                         static_cast<double *>(d_workspace), workspace_bytes, stream);
 }
 
 // ------------------------------------------------------- non-uniform THC

@@ -207,12 +207,27 @@ constexpr int fused_unroll() {
     return kP <= 8 ? 64 : 2;
 }
 
+// A thread's running sums for NMSE ([T] section 2) of the decoded average
+// against a reference: sum (ref - avg)^2 and sum ref^2, fp32.
+struct NmseAcc {
+    float num = 0.0f, den = 0.0f;
+};
+
+// sum (r - a)^2 and sum r^2 over four lanes, pairwise
+__device__ __forceinline__ void nmse_terms4(const float4 &r, const float4 &a, float &num, float &den) {
+    const float d0 = __fsub_rn(r.x, a.x), d1 = __fsub_rn(r.y, a.y), d2 = __fsub_rn(r.z, a.z), d3 = __fsub_rn(r.w, a.w);
+    num = __fadd_rn(__fadd_rn(__fmul_rn(d0, d0), __fmul_rn(d1, d1)), __fadd_rn(__fmul_rn(d2, d2), __fmul_rn(d3, d3)));
+    den = __fadd_rn(__fadd_rn(__fmul_rn(r.x, r.x), __fmul_rn(r.y, r.y)), __fadd_rn(__fmul_rn(r.z, r.z), __fmul_rn(r.w, r.w)));
+}
+
 // kP > 0: the worker count is kP, known at compile time (the worker loop is
 // unrolled, its pointers and worker ids taken at fixed parameter offsets);
-// kP = 0: p.P.
-template <int B, bool kPacked, int kP = 0, class Prm>
+// kP = 0: p.P.  kNmse: also add the word's NMSE terms against ref (the
+// reference values of the same E elements) to acc.
+template <int B, bool kPacked, int kP = 0, bool kNmse = false, class Prm>
 __device__ __forceinline__ void fused_word_vec(const Prm &p, const Coder &c, const float *const *xs, int64_t xoff,
-                                               float *avg, int64_t w) {
+                                               float *avg, int64_t w, const float *ref = nullptr,
+                                               NmseAcc *acc = nullptr) {
     constexpr int E = 32 / B;
     constexpr int G = E / 4;  // float4 groups (and Philox blocks) per word
     const int P = kP > 0 ? kP : p.P;
@@ -222,6 +237,8 @@ __device__ __forceinline__ void fused_word_vec(const Prm &p, const Coder &c, con
     for (int i = 0; i < E; ++i) s[i] = 0;
     float4 va[G], vb[G];
     load_group(va, xs[0] + xoff);
+    float4 rv[kNmse ? G : 1];  // the reference values, in flight while the workers are quantized
+    if constexpr (kNmse) load_group(rv, ref);
 #pragma unroll(fused_unroll<B, kP>())
     for (int wk = 0; wk < P; wk += 2) {
         const bool has1 = wk + 1 < P;
@@ -231,12 +248,24 @@ __device__ __forceinline__ void fused_word_vec(const Prm &p, const Coder &c, con
         if (has1) fused_one_worker<B, kPacked>(vb, s, e0, w, wk + 1, p, c);
     }
     float4 *dst = reinterpret_cast<float4 *>(avg);
+    float num = 0.0f, den = 0.0f;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        __stcs(dst + g, make_float4(__fmaf_rn(small_to_float(s[4 * g] - c.bias), c.k, c.km),
-                                    __fmaf_rn(small_to_float(s[4 * g + 1] - c.bias), c.k, c.km),
-                                    __fmaf_rn(small_to_float(s[4 * g + 2] - c.bias), c.k, c.km),
-                                    __fmaf_rn(small_to_float(s[4 * g + 3] - c.bias), c.k, c.km)));
+        const float4 a = make_float4(__fmaf_rn(small_to_float(s[4 * g] - c.bias), c.k, c.km),
+                                     __fmaf_rn(small_to_float(s[4 * g + 1] - c.bias), c.k, c.km),
+                                     __fmaf_rn(small_to_float(s[4 * g + 2] - c.bias), c.k, c.km),
+                                     __fmaf_rn(small_to_float(s[4 * g + 3] - c.bias), c.k, c.km));
+        __stcs(dst + g, a);
+        if constexpr (kNmse) {
+            float n4, d4;
+            nmse_terms4(rv[g], a, n4, d4);
+            num = g == 0 ? n4 : __fadd_rn(num, n4);
+            den = g == 0 ? d4 : __fadd_rn(den, d4);
+        }
+    }
+    if constexpr (kNmse) {
+        acc->num = __fadd_rn(acc->num, num);
+        acc->den = __fadd_rn(acc->den, den);
     }
 }
 
@@ -322,6 +351,8 @@ struct ThcPlanParams {
     float L, fp;
     PlanSeg seg[kPlanSegs];                  // sorted, disjoint; every tensor meeting the launch's words
     float *out[kPlanSegs];                   // output tensor of each segment
+    const float *ref[kPlanSegs];             // NMSE reference tensor of each segment (NMSE launches)
+    double *nmse_ws;                         // NMSE launches: this launch's per-CTA pairs of sums
     int64_t tile_start[kPlanPieces + 1];     // first tile of each piece; [npieces] = total
     PlanPiece piece[kPlanPieces];
     const float *src[kPlanPtrs];             // src[k * P + slot]: worker slot's tensor of segment k
@@ -342,8 +373,8 @@ __device__ __forceinline__ int plan_find(const ThcPlanParams &p, int64_t e) {
 
 // The buffer's ragged last word (e0 + E > N), element by element: the
 // missing elements pack as zero bits and get no output.
-template <int B, bool kPacked>
-__device__ __noinline__ void plan_word_ragged(const ThcPlanParams &p, const Coder &c, int64_t w) {
+template <int B, bool kPacked, bool kNmse>
+__device__ __noinline__ void plan_word_ragged(const ThcPlanParams &p, const Coder &c, int64_t w, NmseAcc &acc) {
     constexpr int E = 32 / B;
     constexpr int G = E / 4;
     const int64_t e0 = w * E;
@@ -369,7 +400,14 @@ __device__ __noinline__ void plan_word_ragged(const ThcPlanParams &p, const Code
     for (int i = 0; i < E && e0 + i < p.N; ++i) {
         const int64_t e = e0 + i;
         const int k = plan_find(p, e);
-        if (k >= 0) p.out[k][e - p.seg[k].begin] = __fmaf_rn(small_to_float(s[i] - c.bias), c.k, c.km);
+        if (k < 0) continue;
+        const float a = __fmaf_rn(small_to_float(s[i] - c.bias), c.k, c.km);
+        p.out[k][e - p.seg[k].begin] = a;
+        if (kNmse) {
+            const float r = p.ref[k][e - p.seg[k].begin], d = __fsub_rn(r, a);
+            acc.num = __fadd_rn(acc.num, __fmul_rn(d, d));
+            acc.den = __fadd_rn(acc.den, __fmul_rn(r, r));
+        }
     }
 }
 
@@ -379,8 +417,9 @@ __device__ __noinline__ void plan_word_ragged(const ThcPlanParams &p, const Code
 // (seg >= 0).  Each worker's E values are gathered with independent loads,
 // then quantized as a vector word.  Kept out of line: it serves only the few
 // words at tensor ends and gaps, and the unaligned tensors.
-template <int B, bool kPacked>
-__device__ __noinline__ void plan_word_gather(const ThcPlanParams &p, const Coder &c, int64_t w, int seg) {
+template <int B, bool kPacked, bool kNmse>
+__device__ __noinline__ void plan_word_gather(const ThcPlanParams &p, const Coder &c, int64_t w, int seg,
+                                              NmseAcc &acc) {
     constexpr int E = 32 / B;
     constexpr int G = E / 4;
     const int64_t e0 = w * E;
@@ -405,14 +444,26 @@ __device__ __noinline__ void plan_word_gather(const ThcPlanParams &p, const Code
         fused_one_worker<B, kPacked>(v, s, e0, w, wk, p, c);
     }
 #pragma unroll
-    for (int i = 0; i < E; ++i)
-        if (ks[i] >= 0) __stcs(p.out[ks[i]] + off[i], __fmaf_rn(small_to_float(s[i] - c.bias), c.k, c.km));
+    for (int i = 0; i < E; ++i) {
+        if (ks[i] < 0) continue;
+        const float a = __fmaf_rn(small_to_float(s[i] - c.bias), c.k, c.km);
+        __stcs(p.out[ks[i]] + off[i], a);
+        if (kNmse) {
+            const float r = __ldcs(p.ref[ks[i]] + off[i]), d = __fsub_rn(r, a);
+            acc.num = __fadd_rn(acc.num, __fmul_rn(d, d));
+            acc.den = __fadd_rn(acc.den, __fmul_rn(r, r));
+        }
+    }
 }
 
-template <int B, bool kPacked, int kP>
+// kNmse: every CTA also writes its pair of NMSE sums (fp32 per thread and
+// across a warp, fp64 across the warps in a fixed order) to
+// p.nmse_ws[2 * blockIdx.x], p.nmse_ws[2 * blockIdx.x + 1].
+template <int B, bool kPacked, int kP, bool kNmse>
 __global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_plan_kernel(const __grid_constant__ ThcPlanParams p) {
     constexpr int E = 32 / B;
     const Coder c = make_coder(p);
+    NmseAcc acc;
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         // the piece that owns tile t: largest i with tile_start[i] <= t (uniform per CTA)
         int lo = 0, hi = p.npieces - 1;
@@ -429,12 +480,38 @@ __global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_pla
             if (w >= pc.w1) break;
             if (pc.kind == kPieceVec) {
                 const int64_t off = w * E - p.seg[pc.seg].begin;
-                fused_word_vec<B, kPacked, kP>(p, c, p.src + pc.seg * p.P, off, p.out[pc.seg] + off, w);
+                fused_word_vec<B, kPacked, kP, kNmse>(p, c, p.src + pc.seg * p.P, off, p.out[pc.seg] + off, w,
+                                                      kNmse ? p.ref[pc.seg] + off : nullptr, &acc);
             } else if ((w + 1) * E <= p.N) {
-                plan_word_gather<B, kPacked>(p, c, w, pc.kind == kPieceTensor ? pc.seg : -1);
+                plan_word_gather<B, kPacked, kNmse>(p, c, w, pc.kind == kPieceTensor ? pc.seg : -1, acc);
             } else {
-                plan_word_ragged<B, kPacked>(p, c, w);
+                plan_word_ragged<B, kPacked, kNmse>(p, c, w, acc);
             }
+        }
+    }
+    if constexpr (kNmse) {
+        __shared__ float s_num[kThreads / 32], s_den[kThreads / 32];
+        float num = acc.num, den = acc.den;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            num = __fadd_rn(num, __shfl_xor_sync(0xFFFFFFFFu, num, o));
+            den = __fadd_rn(den, __shfl_xor_sync(0xFFFFFFFFu, den, o));
+        }
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        if (lane == 0) {
+            s_num[warp] = num;
+            s_den[warp] = den;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double dn = 0.0, dd = 0.0;
+#pragma unroll
+            for (int i = 0; i < kThreads / 32; ++i) {
+                dn += static_cast<double>(s_num[i]);
+                dd += static_cast<double>(s_den[i]);
+            }
+            p.nmse_ws[2 * blockIdx.x] = dn;
+            p.nmse_ws[2 * blockIdx.x + 1] = dd;
         }
     }
 }
@@ -474,15 +551,26 @@ int launch_fused(const FusedParams &p, int b, bool packed, cudaStream_t stream) 
     return check_launch("thc_fused_kernel");
 }
 
+// CTAs a plan launch runs (one per tile).
+inline unsigned plan_grid(const ThcPlanParams &p) {
+    return static_cast<unsigned>(p.total_tiles < 0x7FFFFFFF ? p.total_tiles : 0x7FFFFFFF);
+}
+
 template <int kP>
-int launch_fused_plan(const ThcPlanParams &p, int b, bool packed, cudaStream_t stream) {
+int launch_fused_plan(const ThcPlanParams &p, int b, bool packed, bool nmse, cudaStream_t stream) {
     if (p.total_tiles <= 0) return GAR_OK;
     // one CTA per tile: the block scheduler balances the SMs (see the ring kernel)
-    const unsigned grid = static_cast<unsigned>(p.total_tiles < 0x7FFFFFFF ? p.total_tiles : 0x7FFFFFFF);
-#define GAR_PLAN_CASE(BB)                                                                  \
-    case BB:                                                                               \
-        if (packed) thc_fused_plan_kernel<BB, true, kP><<<grid, kThreads, 0, stream>>>(p); \
-        else thc_fused_plan_kernel<BB, false, kP><<<grid, kThreads, 0, stream>>>(p);       \
+    const unsigned grid = plan_grid(p);
+#define GAR_PLAN_KERNEL(BB, PK, NM) thc_fused_plan_kernel<BB, PK, kP, NM><<<grid, kThreads, 0, stream>>>(p)
+#define GAR_PLAN_CASE(BB)                                                           \
+    case BB:                                                                        \
+        if (nmse) {                                                                 \
+            if (packed) GAR_PLAN_KERNEL(BB, true, true);                            \
+            else GAR_PLAN_KERNEL(BB, false, true);                                  \
+        } else {                                                                    \
+            if (packed) GAR_PLAN_KERNEL(BB, true, false);                           \
+            else GAR_PLAN_KERNEL(BB, false, false);                                 \
+        }                                                                           \
         break;
     switch (b) {
         GAR_PLAN_CASE(1)
@@ -491,6 +579,7 @@ int launch_fused_plan(const ThcPlanParams &p, int b, bool packed, cudaStream_t s
         GAR_PLAN_CASE(8)
     }
 #undef GAR_PLAN_CASE
+#undef GAR_PLAN_KERNEL
     return check_launch("thc_fused_plan_kernel");
 }
 
@@ -499,10 +588,10 @@ extern template int launch_fused<4>(const FusedParams &, int, bool, cudaStream_t
 extern template int launch_fused<8>(const FusedParams &, int, bool, cudaStream_t);
 extern template int launch_fused<16>(const FusedParams &, int, bool, cudaStream_t);
 extern template int launch_fused<64>(const FusedParams &, int, bool, cudaStream_t);
-extern template int launch_fused_plan<4>(const ThcPlanParams &, int, bool, cudaStream_t);
-extern template int launch_fused_plan<8>(const ThcPlanParams &, int, bool, cudaStream_t);
-extern template int launch_fused_plan<16>(const ThcPlanParams &, int, bool, cudaStream_t);
-extern template int launch_fused_plan<64>(const ThcPlanParams &, int, bool, cudaStream_t);
+extern template int launch_fused_plan<4>(const ThcPlanParams &, int, bool, bool, cudaStream_t);
+extern template int launch_fused_plan<8>(const ThcPlanParams &, int, bool, bool, cudaStream_t);
+extern template int launch_fused_plan<16>(const ThcPlanParams &, int, bool, bool, cudaStream_t);
+extern template int launch_fused_plan<64>(const ThcPlanParams &, int, bool, bool, cudaStream_t);
 
 }  // namespace thc
 }  // namespace gar

@@ -4,6 +4,6 @@
 namespace gar {
 namespace thc {
 template int launch_fused<16>(const FusedParams &, int, bool, cudaStream_t);
-template int launch_fused_plan<16>(const ThcPlanParams &, int, bool, cudaStream_t);
+template int launch_fused_plan<16>(const ThcPlanParams &, int, bool, bool, cudaStream_t);
 }  // namespace thc
 }  // namespace gar

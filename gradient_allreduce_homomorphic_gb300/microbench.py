@@ -7,6 +7,7 @@ Cases: ring (in-place ring all-reduce of P buffers), ring_out (reduce to one
 output), bidir (bidirectional dual ring), fused (plan-driven all-reduce of the 300-tensor ResNet-like model),
 fused_range (the same into separate outputs, each buffer's THC range from the same reads), thc_plan
 (THC b-bit of every fusion buffer of that model read straight from the tensors, wire vectors written),
+thc_plan_nmse (the same with the NMSE sums against a reference taken in the pass),
 pack, unpack (per worker and buffer), pack_all, pack_all_range (every worker
 in one call, with THC's range fused in), thc_range, thc_encode, thc_aggregate, thc_decode, thc_fused,
 thc_fused_packed, nuhc_fused, nuhc_fused_packed (non-uniform THC with a
@@ -70,7 +71,8 @@ def main(argv=None):
             t, o = g.pointer_table(x), g.pointer_table(out)
             fn = lambda: g.gar_ring_allreduce_sim_out(t, o)  # noqa: E731
             nbytes = P * N * es + N * es
-    elif a.case in ("fused", "fused_range", "thc_plan", "pack", "unpack", "pack_all", "pack_all_range"):
+    elif a.case in ("fused", "fused_range", "thc_plan", "thc_plan_nmse", "pack", "unpack", "pack_all",
+                    "pack_all_range"):
         sizes = workloads.resnet_fusion_sizes()
         dt = np.zeros(sizes.size, np.int32)
         plan = g.gar_fusion_plan(sizes, dt, 64 << 20, 16)
@@ -81,7 +83,7 @@ def main(argv=None):
             tables = g.fused_pointer_tables(src, src)
             fn = lambda: g.gar_fused_allreduce(src, src, plan, tables=tables)  # noqa: E731
             nbytes = 2 * P * n * 4
-        elif a.case in ("fused_range", "thc_plan"):
+        elif a.case in ("fused_range", "thc_plan", "thc_plan_nmse"):
             dst = [[torch.empty_like(t) for t in row] for row in src]
             mM = torch.empty((plan.n_buffers, 2), device=dev)
             tables = g.fused_pointer_tables(src, dst)
@@ -94,8 +96,17 @@ def main(argv=None):
                 words = [g.gar_thc_words(int(k), b) for k in plan.buf_numel]
                 packed = [[torch.empty(k, dtype=torch.int32, device=dev) for k in words] for _ in range(P)]
                 tt = g.thc_plan_tables(src, out, packed)
-                fn = lambda: g.gar_thc_allreduce_fused_plan(src, plan, b, 5, mM, out, tables=tt)  # noqa: E731
-                nbytes = P * n * 4 + n * 4 + P * sum(words) * 4
+                if a.case == "thc_plan":
+                    fn = lambda: g.gar_thc_allreduce_fused_plan(src, plan, b, 5, mM, out, tables=tt)  # noqa: E731
+                    nbytes = P * n * 4 + n * 4 + P * sum(words) * 4
+                else:  # with the NMSE sums against worker 1's ring output as reference
+                    ws = torch.empty(g.gar_thc_plan_nmse_workspace_bytes(plan, b) // 8 + 1, dtype=torch.float64,
+                                     device=dev)
+                    pair = torch.empty(2, dtype=torch.float64, device=dev)
+                    rt = g.pointer_table(dst[1])
+                    fn = lambda: g.gar_thc_allreduce_fused_plan_nmse(  # noqa: E731
+                        src, plan, b, 5, mM, out, None, pair, ws, tables=tt, ref_table=rt)
+                    nbytes = P * n * 4 + 2 * n * 4 + P * sum(words) * 4
         elif a.case.startswith("pack_all"):
             fbs = [[torch.empty(int(k), device=dev) for k in plan.buf_numel] for _ in range(P)]
             mM = torch.empty((plan.n_buffers, 2), device=dev) if a.case == "pack_all_range" else None

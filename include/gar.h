@@ -335,6 +335,38 @@ int gar_thc_allreduce_fused_plan(const float *const *src, int32_t P, const gar_s
                                  int32_t n_buffers, int32_t b, uint64_t seed, const float *d_mM,
                                  float *const *out, uint32_t *const *packed, gar_stream_t stream);
 
+/* Bytes of device workspace gar_thc_allreduce_fused_plan_nmse needs for a
+ * plan with these buffers and `count` tensors at b bits (0 for bad b or
+ * counts).  An upper bound: one pair of doubles per CTA the call can run. */
+size_t gar_thc_plan_nmse_workspace_bytes(const int64_t *buf_numel, int32_t n_buffers, int32_t count,
+                                         int32_t b);
+
+/* gar_thc_allreduce_fused_plan_nmse -- gar_thc_allreduce_fused_plan (same
+ * outputs and wire vectors, bit for bit) that also takes, in the same pass,
+ * the two sums of NMSE ([T] section 2) of the decoded average against a
+ * reference -- the exact average, e.g. the ring all-reduce's output:
+ *   d_pair[0] = sum (ref - avg)^2,  d_pair[1] = sum ref^2
+ * over every element of the call's tensors (alignment gaps excluded), so
+ * that no second pass over the averages is needed.  Terms in fp32, summed
+ * pairwise over a word and over a thread's words and across a warp in fp32,
+ * then across warps and CTAs in fp64 in a fixed order: deterministic, within
+ * 2e-6 relative of all-fp64 sums.  gar_nmse_combine of the pairs of several
+ * calls (e.g. one per fusion buffer) gives the NMSE over all of them.
+ *   ref[count]     host array: device reference tensor of each tensor (fp32,
+ *                  the tensor's numel, 4-byte aligned)
+ *   d_pair         device, two doubles, 8-byte aligned
+ *   d_workspace    device, at least gar_thc_plan_nmse_workspace_bytes(...)
+ *                  bytes, 8-byte aligned, caller-owned, not shared with a
+ *                  concurrent call
+ * Other arguments and errors as gar_thc_allreduce_fused_plan; GAR_EINVAL
+ * also for a NULL ref, d_pair or workspace, or a workspace too small. */
+int gar_thc_allreduce_fused_plan_nmse(const float *const *src, int32_t P, const gar_seg *segs,
+                                      const int32_t *dtype, int32_t count, const int64_t *buf_numel,
+                                      int32_t n_buffers, int32_t b, uint64_t seed, const float *d_mM,
+                                      float *const *out, uint32_t *const *packed,
+                                      const float *const *ref, double *d_pair, void *d_workspace,
+                                      size_t workspace_bytes, gar_stream_t stream);
+
 /* ===================================================================== */
 /* Non-uniform THC [T] section 5, Algorithm 2                            */
 /* ===================================================================== */

@@ -226,3 +226,91 @@ def test_resnet_plan_full_size(env):
     for w in range(P):
         for bf in range(plan.n_buffers):
             assert torch.equal(pk[w][bf], ref[2][w][bf])
+
+
+def _nmse_run(g, torch, src, plan, b, seed, mM, refs):
+    P = len(src)
+    out = [torch.full_like(t, 1234.5) for t in src[0]]
+    packed = [[torch.zeros(max(g.gar_thc_words(int(n), b), 1), dtype=torch.int32, device="cuda")
+               for n in plan.buf_numel] for _ in range(P)]
+    ws = torch.empty(g.gar_thc_plan_nmse_workspace_bytes(plan, b) // 8 + 1, dtype=torch.float64, device="cuda")
+    pair = torch.full((2,), float("nan"), dtype=torch.float64, device="cuda")
+    g.gar_thc_allreduce_fused_plan_nmse(src, plan, b, seed, mM, out, refs, pair, ws, packed)
+    return out, packed, pair
+
+
+@pytest.mark.parametrize("trial", range(4))
+@pytest.mark.parametrize("P", [1, 3, 8, 16])
+@pytest.mark.parametrize("b", [2, 4, 8])
+def test_thc_plan_nmse(env, trial, P, b):
+    """The NMSE variant gives the plain call's outputs and wire words bit for
+    bit, and sums of (ref - avg)^2 and ref^2 within 2e-6 of fp64 sums over
+    the tensors (gap elements excluded), the same on a second call."""
+    torch, g = env
+    sizes, src = _plan_inputs(trial, P, torch, offset=1 if trial == 3 else 0)
+    align = 16 if trial % 2 == 0 else 4
+    plan = g.gar_fusion_plan(sizes, np.zeros(len(sizes), np.int32), 16 << 10, align)
+    seed = 0x5EED + 7 * trial
+    ref = _reference(g, torch, src, plan, b, seed)
+    refs = [torch.from_numpy(np.random.default_rng([143, trial, i]).standard_normal(int(n)).astype(np.float32)).cuda()
+            for i, n in enumerate(sizes)]
+    out, packed, pair = _nmse_run(g, torch, src, plan, b, seed, ref[0], refs)
+    _compare(g, plan, ref, (out, packed), P)
+    num = sum(float(np.sum((to_host(r).astype(np.float64) - to_host(o).astype(np.float64)) ** 2))
+              for r, o in zip(refs, out))
+    den = sum(float(np.sum(to_host(r).astype(np.float64) ** 2)) for r in refs)
+    got = pair.cpu().numpy()
+    assert abs(got[0] - num) <= 2e-6 * num + 1e-30 and abs(got[1] - den) <= 2e-6 * den + 1e-30
+    _, _, pair2 = _nmse_run(g, torch, src, plan, b, seed, ref[0], refs)
+    assert pair2.cpu().numpy().tobytes() == got.tobytes()
+
+
+def test_thc_plan_nmse_resnet_combined(env):
+    """The ResNet-like plan, one call per fusion buffer with the ring average
+    as reference, pairs combined: the NMSE of the oracle over the whole model."""
+    torch, g = env
+    P, b, seed = 8, 4, 0x5EED
+    cfg = workloads.CONFIG_IDS["resnet_fusion"]
+    sizes = workloads.resnet_fusion_sizes()
+    dt = np.zeros(sizes.size, np.int32)
+    plan = g.gar_fusion_plan(sizes, dt, 64 << 20, 16)
+    src = [[workloads.device_normal(int(s), 0.01, 7000 + 1000 * w + i, torch.float32, "cuda")
+            for i, s in enumerate(sizes)] for w in range(P)]
+    ring = [[torch.empty_like(t) for t in row] for row in src]
+    mM = torch.empty((plan.n_buffers, 2), device="cuda")
+    g.gar_fused_allreduce_range(src, ring, plan, mM)
+    out = [torch.empty_like(t) for t in src[0]]
+    pairs = torch.empty((plan.n_buffers, 2), dtype=torch.float64, device="cuda")
+    ws = torch.empty(g.gar_thc_plan_nmse_workspace_bytes(plan, b) // 8 + 1, dtype=torch.float64, device="cuda")
+    for bf in range(plan.n_buffers):
+        first, cnt = plan.buffer_tensors(bf)
+        sub = plan.subplan(first, cnt)
+        rows = slice(first, first + cnt)
+        g.gar_thc_allreduce_fused_plan_nmse([row[rows] for row in src], sub, b, seed, mM, out[rows], ring[0][rows],
+                                            pairs[bf], ws)
+    nm = torch.empty(1, dtype=torch.float64, device="cuda")
+    g.gar_nmse_combine(pairs, nm)
+    ref = oracle.nmse(np.concatenate([to_host(t) for t in ring[0]]), np.concatenate([to_host(t) for t in out]))
+    assert abs(nm.item() - ref) <= 2e-6 * ref
+
+
+def test_thc_plan_nmse_edges(env):
+    import ctypes
+
+    torch, g = env
+    lib = g.load()
+    pair = torch.full((2,), float("nan"), dtype=torch.float64, device="cuda")
+    ws = torch.empty(16, dtype=torch.float64, device="cuda")
+    no_refs = (ctypes.c_void_p * 1)()
+    # no tensors: the pair is (0, 0)
+    rc = lib.gar_thc_allreduce_fused_plan_nmse(None, 3, None, None, 0, None, 0, 4, 1, None, None, None, no_refs,
+                                               pair.data_ptr(), ws.data_ptr(), 128, None)
+    assert rc == 0
+    assert pair.cpu().numpy().tolist() == [0.0, 0.0]
+    sizes, src = _plan_inputs(0, 3, torch)
+    plan = g.gar_fusion_plan(sizes, np.zeros(len(sizes), np.int32), 16 << 10, 16)
+    refs = [torch.zeros_like(t) for t in src[0]]
+    out = [torch.empty_like(t) for t in src[0]]
+    mM = torch.zeros((plan.n_buffers, 2), device="cuda")
+    with pytest.raises(g.GarError):  # workspace too small
+        g.gar_thc_allreduce_fused_plan_nmse(src, plan, 4, 1, mM, out, refs, pair, ws[:1])
