@@ -81,14 +81,18 @@ __device__ __forceinline__ void index_biased2(float x0, float x1, uint64_t m2, u
     float2 t = unpack_f2(mul_rn_f2(sub_rn_f2(pack_f2(x0, x1), m2), sc2));
     t.x = fminf(fmaxf(t.x, 0.0f), L);
     t.y = fminf(fmaxf(t.y, 0.0f), L);
-    const uint64_t jm = add_rm_f2(pack_f2(t.x, t.y), pack_f2(8388608.0f, 8388608.0f));
+    const uint64_t t2 = pack_f2(t.x, t.y);
+    const uint64_t jm = add_rm_f2(t2, pack_f2(8388608.0f, 8388608.0f));
     const uint64_t j_minus_1 = sub_rn_f2(jm, pack_f2(8388609.0f, 8388609.0f));
     const uint64_t one_u = pack_f2(__uint_as_float((r0 & 0x007FFFFFu) | 0x3F800000u),
                                    __uint_as_float((r1 & 0x007FFFFFu) | 0x3F800000u));
-    const float2 c = unpack_f2(add_rm_f2(j_minus_1, one_u));
+    // up iff c = (j - 1) + (1 + u) rounded down is below t: the sign of the
+    // rounded difference c - t, which is exact (a nonzero difference of two
+    // binary32 values never rounds to zero, and c == t gives +0)
+    const float2 diff = unpack_f2(sub_rn_f2(add_rm_f2(j_minus_1, one_u), t2));
     const float2 j = unpack_f2(jm);
-    a0 = __float_as_uint(j.x) + (c.x < t.x ? 1u : 0u);
-    a1 = __float_as_uint(j.y) + (c.y < t.y ? 1u : 0u);
+    a0 = __float_as_uint(j.x) + (__float_as_uint(diff.x) >> 31);
+    a1 = __float_as_uint(j.y) + (__float_as_uint(diff.y) >> 31);
 }
 
 __device__ __forceinline__ uint4 philox_block(int64_t q, int worker, const PhiloxKeys &k) {
