@@ -13,7 +13,8 @@
 //   up iff u < f = t - j with u = (r mod 2^23) / 2^23.  Since t is a float,
 //   j + u < t exactly iff (j + u rounded down) < t; j + u is formed as
 //   (jm - (2^23 + 1)) + (1 + u), where jm - (2^23 + 1) = j - 1 is exact and
-//   1 + u is the float with mantissa r mod 2^23.
+//   1 + u is the float with mantissa r mod 2^23.  The fused kernels read the
+//   comparison from the sign bit of the rounded difference, which is exact.
 // No integer<->float conversion is needed per element.
 #include <algorithm>
 #include <cstring>
