@@ -8,13 +8,13 @@ log-uniform sizes 256..2.4M, N(0, 0.01)), 64 MB fusion buffers:
   2. per fusion buffer: Tensor Fusion + ring all-reduce     gar_fused_allreduce_range
      average in one pass (pack, ring, unpack), the buffer's
      THC range [min, max] taken from the same reads
-  3. per fusion buffer: THC encode (every worker) +         gar_thc_allreduce_fused_plan_nmse
+  3. per fusion buffer: THC encode (every worker) +         gar_thc_allreduce_fused_plan
      integer aggregate + decode, read straight from the
      tensors, average written straight to the output
-     tensors, wire vectors written (b = 4, fresh seed each
-     step); in the same pass the sums of NMSE of the THC
-     average against the ring average
-  4. NMSE of the whole model from the buffers' sums         gar_nmse_combine
+     tensors, wire vectors written (b = 4, fresh seed each step)
+  4. NMSE of the THC average against the ring average       gar_nmse
+     (--nmse fused: its sums taken inside step 3,           gar_thc_allreduce_fused_plan_nmse,
+     then combined)                                         gar_nmse_combine
 
 The fused calls give bit for bit what pack -> ring / THC -> unpack gives
 (the tests hold them to that); the fusion buffers are never materialised.
@@ -155,9 +155,10 @@ class Step:
 
     STAGES = ["ring", "thc", "nmse"]
 
-    def __init__(self, torch, g, dev, schedule="overlap"):
+    def __init__(self, torch, g, dev, schedule="overlap", nmse="separate"):
         self.torch, self.g, self.dev = torch, g, dev
         self.schedule = schedule
+        self.nmse_mode = nmse  # "fused": NMSE sums inside the THC pass; "separate": one NMSE pass at the end
         sizes = workloads.resnet_fusion_sizes()
         self.sizes = sizes
         self.n_params = int(sizes.sum())
@@ -187,6 +188,7 @@ class Step:
         self.pairs = torch.empty((self.nb, 2), dtype=torch.float64, device=dev)  # NMSE sums per fusion buffer
         self.ws = torch.empty(g.gar_thc_plan_nmse_workspace_bytes(self.plan, B_THC) // 8 + 1, dtype=torch.float64,
                               device=dev)
+        self.ws_nmse = torch.empty(g.gar_nmse_workspace_bytes(self.flat_len) // 8 + 1, dtype=torch.float64, device=dev)
         # host pointer tables per fusion buffer, built once (the tensors do not move)
         self.parts = []
         for b in range(self.nb):
@@ -219,16 +221,31 @@ class Step:
         average taken in the same pass (into pairs[b])."""
         part = self.parts[b]
         sub = plan.subplan(part["first"], part["count"])
-        self.g.gar_thc_allreduce_fused_plan_nmse(None, sub, B_THC, seed, self.mM, None, None, self.pairs[b], self.ws,
-                                                 stream=stream, tables=part["thc"], ref_table=part["ref"])
+        if self.nmse_mode == "fused":
+            self.g.gar_thc_allreduce_fused_plan_nmse(None, sub, B_THC, seed, self.mM, None, None, self.pairs[b],
+                                                     self.ws, stream=stream, tables=part["thc"],
+                                                     ref_table=part["ref"])
+        else:
+            self.g.gar_thc_allreduce_fused_plan(None, sub, B_THC, seed, self.mM, None, stream=stream,
+                                                tables=part["thc"])
+
+    def _nmse(self, stream):
+        """The NMSE of the whole model: from the buffers' sums (fused), or one
+        pass over both flat averages (separate)."""
+        if self.nmse_mode == "fused":
+            self.g.gar_nmse_combine(self.pairs, self.nmse, stream=stream)
+        else:
+            self.g.gar_nmse(self.ring_flat[0], self.thc_flat, self.nmse, self.ws_nmse, stream=stream)
 
     def algorithmic_bytes(self):
         n = self.n_params * 4
         words = 4 * sum(self.words)
         return {
             "ring": 2 * P * n,                 # read P x n, write P x n (range from the same reads)
-            "thc": P * n + 2 * n + P * words,  # read P x n and the reference, write the average + wire vectors
-            "nmse": 16 * self.nb,              # the per-buffer pairs of sums, combined
+            # read P x n (and the reference, fused NMSE), write the average + the wire vectors
+            "thc": P * n + (2 if self.nmse_mode == "fused" else 1) * n + P * words,
+            # the per-buffer pairs of sums, combined; or one pass over both flat averages
+            "nmse": 16 * self.nb if self.nmse_mode == "fused" else 2 * self.flat_len * 4,
         }
 
     def run(self, step_idx, events=None):
@@ -269,7 +286,7 @@ class Step:
             main.wait_stream(s_thc)
             main.wait_stream(s_ring)
         mark("nmse", 0, main)
-        g.gar_nmse_combine(self.pairs, self.nmse, stream=main)
+        self._nmse(main)
         mark("nmse", 1, main)
 
     # ------------------------------------------------------- end to end
@@ -331,7 +348,7 @@ class Step:
                 host_thc[lo:hi].copy_(self.thc_flat[lo:hi], non_blocking=True)
                 self.ev_sent[b].record(self.s_d2h)
         main.wait_event(self.ev_nmse_sent)  # the previous step's NMSE is on the host
-        g.gar_nmse_combine(self.pairs, self.nmse, stream=main)
+        self._nmse(main)
         self.ev_nmse.record(main)
         self.s_d2h.wait_event(self.ev_nmse)
         with torch.cuda.stream(self.s_d2h):
@@ -339,16 +356,26 @@ class Step:
             self.ev_nmse_sent.record(self.s_d2h)
 
 
-KERNEL_OF_STAGE = {"ring": "ring_fold_kernel", "thc": "thc_fused_plan_kernel (+ thc_nmse_pair_kernel)",
-                   "nmse": "nmse_combine_kernel"}
-PER_OF_STAGE = {
-    "ring": "all launches of one step's 3 gar_fused_allreduce_range calls (one per fusion buffer; "
-            "300 tensors x 8 workers in all)",
-    "thc": "all launches of one step's 3 gar_thc_allreduce_fused_plan_nmse calls (one per fusion buffer; "
-           "NMSE sums against the ring average taken in the same pass)",
-    "nmse": "one step's gar_nmse_combine of the 3 buffers' NMSE sums",
+KERNEL_OF_STAGE = {
+    "separate": {"ring": "ring_fold_kernel", "thc": "thc_fused_plan_kernel",
+                 "nmse": "nmse_partial_kernel + nmse_final_kernel"},
+    "fused": {"ring": "ring_fold_kernel", "thc": "thc_fused_plan_kernel (NMSE sums in the pass) + thc_nmse_pair_kernel",
+              "nmse": "nmse_combine_kernel"},
 }
-# stage -> committed ncu summary holding its per-step DRAM traffic
+PER_OF_STAGE = {
+    "separate": {
+        "ring": "all launches of one step's 3 gar_fused_allreduce_range calls (one per fusion buffer; "
+                "300 tensors x 8 workers in all)",
+        "thc": "all launches of one step's 3 gar_thc_allreduce_fused_plan calls (one per fusion buffer)",
+        "nmse": "one step's gar_nmse over the flat averages"},
+    "fused": {
+        "ring": "all launches of one step's 3 gar_fused_allreduce_range calls (one per fusion buffer; "
+                "300 tensors x 8 workers in all)",
+        "thc": "all launches of one step's 3 gar_thc_allreduce_fused_plan_nmse calls (one per fusion buffer; "
+               "NMSE sums against the ring average taken in the same pass)",
+        "nmse": "one step's gar_nmse_combine of the 3 buffers' NMSE sums"},
+}
+# stage -> committed ncu summary holding its per-step DRAM traffic (the default, separate-NMSE step)
 PROFILE_OF_STAGE = {"ring": ("ring_fold_kernel_range_resnet_fusion", ["ring.cu", "ring.cuh", "common.cuh"]),
                     "thc": ("thc_fused_plan_kernel_resnet_fusion", ["thc.cu", "thc_fused.cuh", "thc_p8.cu", "common.cuh"])}
 
@@ -387,7 +414,7 @@ def run_ours(args, rank, world, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     g.load()
-    st = Step(torch, g, dev, schedule=args.schedule)
+    st = Step(torch, g, dev, schedule=args.schedule, nmse=args.nmse)
     nbytes = P * st.n_params * 4
 
     def barrier():
@@ -479,7 +506,7 @@ def run_ours(args, rank, world, dist):
     algo = st.algorithmic_bytes()
     dom = max(serial_stage_ms, key=lambda s: serial_stage_ms[s])
     achieved = algo[dom] / (serial_stage_ms[dom] * 1e-3) / 1e9
-    traffic = _profile_traffic(dom)
+    traffic = _profile_traffic(dom) if args.nmse == "separate" or dom == "ring" else None
     value = world * nbytes / (ms * 1e-3) / 1e9
     overlap_region = None
     if overlap_evs is not None:
@@ -501,18 +528,19 @@ def run_ours(args, rank, world, dist):
                           schedule=("two streams: THC of fusion buffer b overlapped with the ring of buffer b+1"
                                     if args.schedule == "overlap" else "one stream, stages in sequence"),
                           path="fused: pack + ring + unpack and pack + THC + unpack in one pass each, "
-                               "per fusion buffer"),
+                               "per fusion buffer", nmse=("sums inside the THC pass" if args.nmse == "fused"
+                                                          else "one pass over both averages")),
         "elements_per_s": round(world * P * st.n_params / (ms * 1e-3), 1),
         "hbm_fraction_of_step": round(sum(algo.values()) / (ms * 1e-3) / 1e9 / peak, 4),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "stage_ms_alone": {k: round(v, 4) for k, v in serial_stage_ms.items()},
         "stage_gbs_alone": {k: round(algo[k] / (serial_stage_ms[k] * 1e-3) / 1e9, 1) for k in serial_stage_ms},
         "overlap_region": overlap_region,
-        "roofline": {"kernel": KERNEL_OF_STAGE[dom],
+        "roofline": {"kernel": KERNEL_OF_STAGE[args.nmse][dom],
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-                     "per": PER_OF_STAGE[dom], "stage": dom,
+                     "per": PER_OF_STAGE[args.nmse][dom], "stage": dom,
                      "timed": ("alone: the same steps run once more on one stream in this run, so the kernel "
                                "does not share HBM with a concurrent one" if args.schedule == "overlap"
                                else "in the timed steps")},
@@ -836,6 +864,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--schedule", choices=["overlap", "serial"], default="overlap")
     ap.add_argument("--h2d-streams", type=int, default=2, help="copy streams for the end-to-end inputs")
+    ap.add_argument("--nmse", choices=["fused", "separate"], default="separate",
+                    help="NMSE sums inside the THC pass, or one NMSE pass over both averages at the end")
     ap.add_argument("--reference-budget-s", type=float, default=100.0,
                     help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--configs", action="store_true",

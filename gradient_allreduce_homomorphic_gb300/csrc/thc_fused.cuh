@@ -241,11 +241,13 @@ __device__ __forceinline__ void fused_word_vec(const Prm &p, const Coder &c, con
     for (int i = 0; i < E; ++i) s[i] = 0;
     float4 va[G], vb[G];
     load_group(va, xs[0] + xoff);
-    float4 rv[kNmse ? G : 1];  // the reference values, in flight while the workers are quantized
-    if constexpr (kNmse) load_group(rv, ref);
+    float4 rv[kNmse ? G : 1];  // the reference values, in flight while the last workers are quantized
 #pragma unroll(fused_unroll<B, kP>())
     for (int wk = 0; wk < P; wk += 2) {
         const bool has1 = wk + 1 < P;
+        if constexpr (kNmse) {
+            if (wk + 2 >= P) load_group(rv, ref);
+        }
         if (has1) load_group(vb, xs[wk + 1] + xoff);
         fused_one_worker<B, kPacked>(va, s, e0, w, wk, p, c);
         if (wk + 2 < P) load_group(va, xs[wk + 2] + xoff);
