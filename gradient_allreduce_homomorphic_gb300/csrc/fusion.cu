@@ -4,8 +4,8 @@
 //
 // Copies run as a list of byte-range jobs (a tensor into its slot, a slot
 // back into a tensor, or a zero fill of an alignment gap).  Jobs are cut
-// into tiles of 512 x 16-byte vectors and CTAs stride over the tiles, so a
-// launch moves hundreds of tensors of any size mix at streaming bandwidth.
+// into tiles of 512 x 16-byte vectors, one CTA per tile, so a launch moves
+// hundreds of tensors of any size mix at streaming bandwidth.
 #include <cstring>
 #include <vector>
 
@@ -140,15 +140,8 @@ class CopyBatch {
         }
         p_->tile_start[p_->njobs] = tiles;
         p_->total_tiles = tiles;
-        static int occ = 0;
-        if (occ == 0) {
-            int n = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, copy_jobs_kernel, kThreads, 0) != cudaSuccess || n <= 0)
-                n = 4;
-            occ = n;
-        }
-        int64_t grid = static_cast<int64_t>(sm_count()) * occ;
-        if (grid > tiles) grid = tiles;
+        // one CTA per tile: the block scheduler balances the SMs (as for the ring fold)
+        const int64_t grid = tiles < 0x7FFFFFFF ? tiles : 0x7FFFFFFF;
         copy_jobs_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream_>>>(*p_);
         p_->njobs = 0;
         return check_launch("copy_jobs_kernel");
@@ -345,15 +338,8 @@ int launch_pack_all(PackAllParams &p, cudaStream_t stream) {
     }
     p.tile_start[p.nrows] = tiles;
     p.total_tiles = tiles;
-    static int occ = 0;
-    if (occ == 0) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pack_all_kernel<T>, kThreads, 0) != cudaSuccess || n <= 0)
-            n = 4;
-        occ = n;
-    }
-    int64_t grid = static_cast<int64_t>(sm_count()) * occ;
-    if (grid > tiles) grid = tiles;
+    // one CTA per tile: the block scheduler balances the SMs (as for the ring fold)
+    const int64_t grid = tiles < 0x7FFFFFFF ? tiles : 0x7FFFFFFF;
     pack_all_kernel<T><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
     return check_launch("pack_all_kernel");
 }
