@@ -102,8 +102,87 @@ def load(path: str = LIB_PATH):
     return _lib
 
 
+class _StreamArg(C.c_void_p):
+    """The cudaStream_t argument of a device call (marks the call for the timeline)."""
+
+
+class Timeline:
+    """Horovod-Timeline-like trace of the library's device calls ([H]
+    "Horovod Timeline"): with the environment variable GAR_TIMELINE set to a
+    path, every call that enqueues device work is bracketed by a pair of CUDA
+    events on its own stream, and at exit (or on ``dump()``) the calls are
+    written as Chrome Trace Event JSON (chrome://tracing): one complete event
+    per call, named after the entry point, timestamps in microseconds from
+    the first call, one track per stream.  Events cost a few microseconds of
+    host time per call, so the timeline is off unless asked for."""
+
+    def __init__(self, path: str):
+        import atexit
+
+        self.path = path
+        self.records = []  # (name, stream handle, start event, end event)
+        self._lock = threading.Lock()
+        atexit.register(self.dump)
+
+    def begin(self, name, stream_handle):
+        import torch
+
+        ext = torch.cuda.ExternalStream(stream_handle) if stream_handle else torch.cuda.default_stream()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(ext)
+        return (name, stream_handle or 0, start, end, ext)
+
+    def end(self, token):
+        name, handle, start, end, ext = token
+        end.record(ext)
+        with self._lock:
+            self.records.append((name, handle, start, end))
+
+    def events(self):
+        """The recorded calls as Chrome trace events (synchronises the device)."""
+        import torch
+
+        with self._lock:
+            recs = list(self.records)
+        if not recs:
+            return []
+        torch.cuda.synchronize()
+        t0 = recs[0][2]
+        tracks = {}
+        out = []
+        for name, handle, start, end in recs:
+            tid = tracks.setdefault(handle, len(tracks))
+            out.append({"name": name, "cat": "gar", "ph": "X", "pid": 0, "tid": tid,
+                        "ts": round(t0.elapsed_time(start) * 1e3, 3), "dur": round(start.elapsed_time(end) * 1e3, 3),
+                        "args": {"stream": hex(handle)}})
+        return out
+
+    def dump(self):
+        import json
+
+        try:
+            ev = self.events()
+        except Exception:  # the CUDA context may be gone at interpreter exit
+            return
+        with open(self.path, "w") as f:
+            json.dump({"traceEvents": ev, "displayTimeUnit": "ms"}, f)
+
+
+_timeline = Timeline(os.environ["GAR_TIMELINE"]) if os.environ.get("GAR_TIMELINE") else None
+
+
+def timeline():
+    """The active Timeline, or None when GAR_TIMELINE is not set."""
+    return _timeline
+
+
 def _call(name, *args):
+    token = None
+    if _timeline is not None and args and isinstance(args[-1], _StreamArg):
+        token = _timeline.begin(name, args[-1].value)
     rc = getattr(load(), name)(*args)
+    if token is not None:
+        _timeline.end(token)
     if rc != GAR_OK:
         raise GarError(rc, load().gar_last_error().decode(errors="replace"))
 
@@ -113,7 +192,7 @@ def _stream(stream):
 
     if stream is None:
         stream = torch.cuda.current_stream()
-    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return _StreamArg(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
 def _dev(t):
@@ -456,4 +535,5 @@ def gar_nmse_noalloc(x, x_hat, d_out, stream=None):
 
 
 __all__ = [n for n in dir() if n.startswith(("gar_", "GAR_"))] + ["GarError", "FusionPlan", "PtrTable", "load",
-                                                                    "pointer_table", "fused_pointer_tables", "thc_plan_tables"]
+                                                                    "pointer_table", "fused_pointer_tables", "thc_plan_tables",
+                                                                    "Timeline", "timeline"]
