@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kThreads) thc_decode_kernel(const __grid_const
 // k is a table value T[z].  Decision in fp32, one rounding per op:
 //   t = clamp((x - m) * (g / (M - m)), 0, g)
 //   z = the largest z <= L - 1 with T[z] <= t  (= inv[min(floor(t), g - 1)])
-//   p = (t - T[z]) / (T[z + 1] - T[z]);  up iff u < p  (u as in uniform THC)
+//   up iff u < (t - T[z]) / (T[z + 1] - T[z]) exactly  (u as in uniform THC)
 //   index = z + up; the PS sums T[index].
 constexpr int kMaxGranularity = 16383;
 
@@ -350,9 +350,12 @@ __device__ __forceinline__ uint32_t nuhc_index(float x, float m, float sc, float
     const uint32_t lo_i = s_t[z], hi_i = s_t[z + 1];
     const float lo = __uint_as_float(0x4B000000u | lo_i) - 8388608.0f;  // exact: < 2^23
     const float hi = __uint_as_float(0x4B000000u | hi_i) - 8388608.0f;
-    const float p = __fdiv_rn(__fsub_rn(t, lo), __fsub_rn(hi, lo));
-    const float one_u = __uint_as_float((r & 0x007FFFFFu) | 0x3F800000u);
-    const bool up = one_u < __fadd_ru(p, 1.0f);
+    // up iff u < (t - lo) / (hi - lo) exactly, i.e. u * (hi - lo) < t - lo: t - lo and
+    // hi - lo are exact (integer lo, hi below 2^14, t >= lo), u = (r mod 2^23) 2^-23 is
+    // exact, and the sign of the once-rounded fma(-u, hi - lo, t - lo) is the sign of
+    // the exact difference (a nonzero one is a multiple of 2^-149: never rounds to 0)
+    const float u = __fsub_rn(__uint_as_float((r & 0x007FFFFFu) | 0x3F800000u), 1.0f);
+    const bool up = __fmaf_rn(-u, __fsub_rn(hi, lo), __fsub_rn(t, lo)) > 0.0f;
     *tv = up ? hi_i : lo_i;
     return static_cast<uint32_t>(z) + (up ? 1u : 0u);
 }
@@ -463,6 +466,31 @@ struct NuhcFusedParams {
     int32_t vec;
 };
 
+// One worker's contribution to a whole word of E = 4 G4 elements: Philox
+// draws, indices, the table values added to the running sums s, the packed
+// word stored if wanted.
+template <int B, bool kPacked, int G4>
+__device__ __forceinline__ void nuhc_one_worker(const float4 (&v)[G4], uint32_t (&s)[4 * G4], int64_t e0, int64_t w,
+                                                int wk, const NuhcFusedParams &p, float m, float sc, float G,
+                                                const uint16_t *s_t, const uint8_t *s_inv) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int g4 = 0; g4 < G4; ++g4) {
+        const uint4 r = philox_block((e0 >> 2) + g4, wk, p.keys);
+        uint32_t t0, t1, t2, t3;
+        const uint32_t i0 = nuhc_index(v[g4].x, m, sc, G, p.tab.g, s_t, s_inv, r.x, &t0);
+        const uint32_t i1 = nuhc_index(v[g4].y, m, sc, G, p.tab.g, s_t, s_inv, r.y, &t1);
+        const uint32_t i2 = nuhc_index(v[g4].z, m, sc, G, p.tab.g, s_t, s_inv, r.z, &t2);
+        const uint32_t i3 = nuhc_index(v[g4].w, m, sc, G, p.tab.g, s_t, s_inv, r.w, &t3);
+        s[4 * g4] += t0;
+        s[4 * g4 + 1] += t1;
+        s[4 * g4 + 2] += t2;
+        s[4 * g4 + 3] += t3;
+        if (kPacked) word |= (i0 | (i1 << B) | (i2 << (2 * B)) | (i3 << (3 * B))) << (4 * g4 * B);
+    }
+    if (kPacked) __stcs(p.packed[wk] + w, word);
+}
+
 template <int B, bool kPacked>
 __global__ void __launch_bounds__(kThreads) nuhc_fused_kernel(const __grid_constant__ NuhcFusedParams p) {
     constexpr int E = 32 / B;
@@ -479,44 +507,28 @@ __global__ void __launch_bounds__(kThreads) nuhc_fused_kernel(const __grid_const
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < p.nwords; w += stride) {
         const int64_t e0 = w * E;
-        const bool full = p.vec && e0 + E <= p.N;
         uint32_t s[E];
 #pragma unroll
         for (int i = 0; i < E; ++i) s[i] = 0;
-        for (int wk = 0; wk < p.P; ++wk) {
-            uint32_t word = 0;
+        if (p.vec && e0 + E <= p.N) {
+            // two register buffers, the worker loop unrolled by two: one worker's
+            // loads are in flight while the other is quantized
+            float4 va[G4], vb[G4];
 #pragma unroll
-            for (int g4 = 0; g4 < G4; ++g4) {
-                const int64_t eb = e0 + 4 * g4;
-                float4 v = make_float4(m, m, m, m);
-                if (full) {
-                    v = __ldcs(reinterpret_cast<const float4 *>(p.x[wk] + eb));
-                } else {
-                    if (eb < p.N) v.x = p.x[wk][eb];
-                    if (eb + 1 < p.N) v.y = p.x[wk][eb + 1];
-                    if (eb + 2 < p.N) v.z = p.x[wk][eb + 2];
-                    if (eb + 3 < p.N) v.w = p.x[wk][eb + 3];
+            for (int g4 = 0; g4 < G4; ++g4) va[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[0] + e0) + g4);
+            for (int wk = 0; wk < p.P; wk += 2) {
+                const bool has1 = wk + 1 < p.P;
+                if (has1) {
+#pragma unroll
+                    for (int g4 = 0; g4 < G4; ++g4) vb[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk + 1] + e0) + g4);
                 }
-                const uint4 r = philox_block(eb >> 2, wk, p.keys);
-                uint32_t t0, t1, t2, t3;
-                const uint32_t i0 = nuhc_index(v.x, m, sc, G, p.tab.g, s_t, s_inv, r.x, &t0);
-                const uint32_t i1 = nuhc_index(v.y, m, sc, G, p.tab.g, s_t, s_inv, r.y, &t1);
-                const uint32_t i2 = nuhc_index(v.z, m, sc, G, p.tab.g, s_t, s_inv, r.z, &t2);
-                const uint32_t i3 = nuhc_index(v.w, m, sc, G, p.tab.g, s_t, s_inv, r.w, &t3);
-                s[4 * g4] += t0;
-                s[4 * g4 + 1] += t1;
-                s[4 * g4 + 2] += t2;
-                s[4 * g4 + 3] += t3;
-                if (kPacked) {
-                    uint32_t q = i0 | (i1 << B) | (i2 << (2 * B)) | (i3 << (3 * B));
-                    const int64_t valid = p.N - eb;
-                    if (valid < 4) q = valid <= 0 ? 0u : q & ((1u << (B * valid)) - 1u);
-                    word |= q << (4 * g4 * B);
+                nuhc_one_worker<B, kPacked>(va, s, e0, w, wk, p, m, sc, G, s_t, s_inv);
+                if (wk + 2 < p.P) {
+#pragma unroll
+                    for (int g4 = 0; g4 < G4; ++g4) va[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk + 2] + e0) + g4);
                 }
+                if (has1) nuhc_one_worker<B, kPacked>(vb, s, e0, w, wk + 1, p, m, sc, G, s_t, s_inv);
             }
-            if (kPacked) __stcs(p.packed[wk] + w, word);
-        }
-        if (full) {
             float4 *dst = reinterpret_cast<float4 *>(p.avg + e0);
 #pragma unroll
             for (int g4 = 0; g4 < G4; ++g4)
@@ -524,7 +536,23 @@ __global__ void __launch_bounds__(kThreads) nuhc_fused_kernel(const __grid_const
                                              __fmaf_rn(small_to_float(s[4 * g4 + 1]), k, km),
                                              __fmaf_rn(small_to_float(s[4 * g4 + 2]), k, km),
                                              __fmaf_rn(small_to_float(s[4 * g4 + 3]), k, km)));
-        } else {
+        } else {  // ragged last word, or unaligned pointers: element by element
+            for (int wk = 0; wk < p.P; ++wk) {
+                uint32_t word = 0;
+                for (int g4 = 0; g4 < G4; ++g4) {
+                    const int64_t eb = e0 + 4 * g4;
+                    if (eb >= p.N) break;
+                    const uint4 r = philox_block(eb >> 2, wk, p.keys);
+                    for (int i = 0; i < 4 && eb + i < p.N; ++i) {
+                        uint32_t tv;
+                        const uint32_t idx = nuhc_index(p.x[wk][eb + i], m, sc, G, p.tab.g, s_t, s_inv,
+                                                        pick(r, i), &tv);
+                        s[4 * g4 + i] += tv;
+                        word |= idx << ((4 * g4 + i) * B);
+                    }
+                }
+                if (kPacked) p.packed[wk][w] = word;
+            }
             for (int i = 0; i < E && e0 + i < p.N; ++i) p.avg[e0 + i] = __fmaf_rn(small_to_float(s[i]), k, km);
         }
     }

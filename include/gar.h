@@ -377,8 +377,9 @@ int gar_thc_allreduce_fused_plan_nmse(const float *const *src, int32_t P, const 
  * caller's).  Encoding in fp32, one rounding per operation:
  *     t = clamp((x - m) * (g / (M - m)), 0, g)        (t = 0 when M == m)
  *     z = the largest z <= 2^b - 2 with T[z] <= t
- *     p = (t - T[z]) / (T[z + 1] - T[z])
- *     index = z + (u < p ? 1 : 0)    (u: the Philox draw of uniform THC)
+ *     index = z + 1 if u < (t - T[z]) / (T[z + 1] - T[z]) exactly, else z
+ *             (u: the Philox draw of uniform THC; decided as
+ *              u (T[z + 1] - T[z]) < t - T[z], whose sides are exact)
  * Packing as for uniform THC.  The PS looks every index up in T and sums the
  * table values; each worker decodes avg = fma(S, ((M - m)/g)/P, m).  With
  * g = 2^b - 1 and T the identity this is exactly uniform THC. */

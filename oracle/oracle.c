@@ -634,14 +634,17 @@ uint32_t oracle_nuhc_index(float x, float m, float M, int b, int g, const uint16
     int z = 0;
     while (z < L - 1 && t >= (float)table[z + 1]) ++z;
     float lo = (float)table[z], hi = (float)table[z + 1];
-    float p = (t - lo) / (hi - lo); /* probability of rounding up to table[z + 1] */
+    /* rounds up to table[z + 1] with probability (t - lo) / (hi - lo): up iff
+     * u (hi - lo) < t - lo, compared exactly in double (t - lo is exact in
+     * float, the product has at most 37 significant bits) */
     uint64_t q = (uint64_t)e >> 2;
     uint32_t ctr[4] = {(uint32_t)q, (uint32_t)(q >> 32), (uint32_t)worker, 0u};
     uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
     uint32_t r[4];
     oracle_philox4x32(ctr, key, 10, r);
     float u = (float)(r[e & 3] & 0x7FFFFFu) / 8388608.0f;
-    return (uint32_t)z + (u < p ? 1u : 0u);
+    double a = (double)(t - lo), d = (double)(hi - lo);
+    return (uint32_t)z + ((double)u * d < a ? 1u : 0u);
 }
 
 int oracle_nuhc_encode(const float *x, int64_t n, float m, float M, int b, int g,
