@@ -324,14 +324,18 @@ struct NuhcTable {
 };
 
 // Shared-memory copies of T and of its inverse on the integers 0..g-1.
-__device__ __forceinline__ void nuhc_load_tables(const NuhcTable &tab, uint16_t *s_t, uint8_t *s_inv) {
-    for (int z = threadIdx.x; z <= tab.L; z += blockDim.x) s_t[z] = tab.t[z];
-    __syncthreads();
+// Shared-memory tables: the pairs (T[z], T[z + 1]) as floats for z < L (one
+// 8-byte load gives both neighbours), and the inverse of T on the integers
+// 0..g-1 (z of the interval holding k).
+constexpr int kNuhcPairBytes = 256 * 8;  // float2[255], rounded up
+__device__ __forceinline__ void nuhc_load_tables(const NuhcTable &tab, float2 *s_pair, uint8_t *s_inv) {
+    for (int z = threadIdx.x; z < tab.L; z += blockDim.x)
+        s_pair[z] = make_float2(static_cast<float>(tab.t[z]), static_cast<float>(tab.t[z + 1]));
     for (int k = threadIdx.x; k < tab.g; k += blockDim.x) {
         int lo = 0, hi = tab.L - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (s_t[mid] <= k) lo = mid;
+            if (tab.t[mid] <= k) lo = mid;
             else hi = mid - 1;
         }
         s_inv[k] = static_cast<uint8_t>(lo);
@@ -339,24 +343,23 @@ __device__ __forceinline__ void nuhc_load_tables(const NuhcTable &tab, uint16_t 
     __syncthreads();
 }
 
-// Returns the index; *tv receives the table value it stands for.
-__device__ __forceinline__ uint32_t nuhc_index(float x, float m, float sc, float G, int g, const uint16_t *s_t,
-                                               const uint8_t *s_inv, uint32_t r, uint32_t *tv) {
+// Returns the index; tv receives the table value it stands for (an integer
+// below 2^14, as a float).
+__device__ __forceinline__ uint32_t nuhc_index(float x, float m, float sc, float G, int g, const float2 *s_pair,
+                                               const uint8_t *s_inv, uint32_t r, float &tv) {
     float t = __fmul_rn(__fsub_rn(x, m), sc);
     t = fminf(fmaxf(t, 0.0f), G);
     int k = __float_as_int(__fadd_rd(t, 8388608.0f)) - 0x4B000000;  // floor(t)
     k = k < g - 1 ? k : g - 1;
     const int z = s_inv[k];
-    const uint32_t lo_i = s_t[z], hi_i = s_t[z + 1];
-    const float lo = __uint_as_float(0x4B000000u | lo_i) - 8388608.0f;  // exact: < 2^23
-    const float hi = __uint_as_float(0x4B000000u | hi_i) - 8388608.0f;
+    const float2 lh = s_pair[z];  // T[z], T[z + 1]
     // up iff u < (t - lo) / (hi - lo) exactly, i.e. u * (hi - lo) < t - lo: t - lo and
     // hi - lo are exact (integer lo, hi below 2^14, t >= lo), u = (r mod 2^23) 2^-23 is
     // exact, and the sign of the once-rounded fma(-u, hi - lo, t - lo) is the sign of
     // the exact difference (a nonzero one is a multiple of 2^-149: never rounds to 0)
     const float u = __fsub_rn(__uint_as_float((r & 0x007FFFFFu) | 0x3F800000u), 1.0f);
-    const bool up = __fmaf_rn(-u, __fsub_rn(hi, lo), __fsub_rn(t, lo)) > 0.0f;
-    *tv = up ? hi_i : lo_i;
+    const bool up = __fmaf_rn(-u, __fsub_rn(lh.y, lh.x), __fsub_rn(t, lh.x)) > 0.0f;
+    tv = up ? lh.y : lh.x;
     return static_cast<uint32_t>(z) + (up ? 1u : 0u);
 }
 
@@ -376,16 +379,17 @@ template <int B>
 __global__ void __launch_bounds__(kThreads) nuhc_encode_kernel(const __grid_constant__ NuhcEncodeParams p) {
     constexpr int E = 32 / B;
     extern __shared__ unsigned char s_mem[];
-    uint16_t *s_t = reinterpret_cast<uint16_t *>(s_mem);
-    uint8_t *s_inv = s_mem + 512;
-    nuhc_load_tables(p.tab, s_t, s_inv);
+    float2 *s_pair = reinterpret_cast<float2 *>(s_mem);
+    uint8_t *s_inv = s_mem + kNuhcPairBytes;
+    nuhc_load_tables(p.tab, s_pair, s_inv);
     const float m = p.mM[0], M = p.mM[1];
     const float G = static_cast<float>(p.tab.g);
     const float sc = range_scale(m, M, G);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < p.nwords; w += stride) {
         const int64_t e0 = w * E;
-        uint32_t word = 0, tv;
+        uint32_t word = 0;
+        float tv;
         for (int g4 = 0; g4 < E / 4; ++g4) {
             const int64_t eb = e0 + 4 * g4;
             if (eb >= p.N) break;
@@ -400,10 +404,10 @@ __global__ void __launch_bounds__(kThreads) nuhc_encode_kernel(const __grid_cons
                 if (eb + 2 < p.N) v.z = p.x[eb + 2];
                 if (eb + 3 < p.N) v.w = p.x[eb + 3];
             }
-            const uint32_t i0 = nuhc_index(v.x, m, sc, G, p.tab.g, s_t, s_inv, r.x, &tv);
-            const uint32_t i1 = nuhc_index(v.y, m, sc, G, p.tab.g, s_t, s_inv, r.y, &tv);
-            const uint32_t i2 = nuhc_index(v.z, m, sc, G, p.tab.g, s_t, s_inv, r.z, &tv);
-            const uint32_t i3 = nuhc_index(v.w, m, sc, G, p.tab.g, s_t, s_inv, r.w, &tv);
+            const uint32_t i0 = nuhc_index(v.x, m, sc, G, p.tab.g, s_pair, s_inv, r.x, tv);
+            const uint32_t i1 = nuhc_index(v.y, m, sc, G, p.tab.g, s_pair, s_inv, r.y, tv);
+            const uint32_t i2 = nuhc_index(v.z, m, sc, G, p.tab.g, s_pair, s_inv, r.z, tv);
+            const uint32_t i3 = nuhc_index(v.w, m, sc, G, p.tab.g, s_pair, s_inv, r.w, tv);
             uint32_t q = i0 | (i1 << B) | (i2 << (2 * B)) | (i3 << (3 * B));
             const int64_t valid = p.N - eb;  // elements of this group inside N
             if (valid < 4) q &= (1u << (B * valid)) - 1u;
@@ -469,23 +473,24 @@ struct NuhcFusedParams {
 // One worker's contribution to a whole word of E = 4 G4 elements: Philox
 // draws, indices, the table values added to the running sums s, the packed
 // word stored if wanted.
+// (The sums of table values are integers below 2^24: exact in fp32.)
 template <int B, bool kPacked, int G4>
-__device__ __forceinline__ void nuhc_one_worker(const float4 (&v)[G4], uint32_t (&s)[4 * G4], int64_t e0, int64_t w,
+__device__ __forceinline__ void nuhc_one_worker(const float4 (&v)[G4], float (&s)[4 * G4], int64_t e0, int64_t w,
                                                 int wk, const NuhcFusedParams &p, float m, float sc, float G,
-                                                const uint16_t *s_t, const uint8_t *s_inv) {
+                                                const float2 *s_pair, const uint8_t *s_inv) {
     uint32_t word = 0;
 #pragma unroll
     for (int g4 = 0; g4 < G4; ++g4) {
         const uint4 r = philox_block((e0 >> 2) + g4, wk, p.keys);
-        uint32_t t0, t1, t2, t3;
-        const uint32_t i0 = nuhc_index(v[g4].x, m, sc, G, p.tab.g, s_t, s_inv, r.x, &t0);
-        const uint32_t i1 = nuhc_index(v[g4].y, m, sc, G, p.tab.g, s_t, s_inv, r.y, &t1);
-        const uint32_t i2 = nuhc_index(v[g4].z, m, sc, G, p.tab.g, s_t, s_inv, r.z, &t2);
-        const uint32_t i3 = nuhc_index(v[g4].w, m, sc, G, p.tab.g, s_t, s_inv, r.w, &t3);
-        s[4 * g4] += t0;
-        s[4 * g4 + 1] += t1;
-        s[4 * g4 + 2] += t2;
-        s[4 * g4 + 3] += t3;
+        float t0, t1, t2, t3;
+        const uint32_t i0 = nuhc_index(v[g4].x, m, sc, G, p.tab.g, s_pair, s_inv, r.x, t0);
+        const uint32_t i1 = nuhc_index(v[g4].y, m, sc, G, p.tab.g, s_pair, s_inv, r.y, t1);
+        const uint32_t i2 = nuhc_index(v[g4].z, m, sc, G, p.tab.g, s_pair, s_inv, r.z, t2);
+        const uint32_t i3 = nuhc_index(v[g4].w, m, sc, G, p.tab.g, s_pair, s_inv, r.w, t3);
+        s[4 * g4] = __fadd_rn(s[4 * g4], t0);
+        s[4 * g4 + 1] = __fadd_rn(s[4 * g4 + 1], t1);
+        s[4 * g4 + 2] = __fadd_rn(s[4 * g4 + 2], t2);
+        s[4 * g4 + 3] = __fadd_rn(s[4 * g4 + 3], t3);
         if (kPacked) word |= (i0 | (i1 << B) | (i2 << (2 * B)) | (i3 << (3 * B))) << (4 * g4 * B);
     }
     if (kPacked) __stcs(p.packed[wk] + w, word);
@@ -496,9 +501,9 @@ __global__ void __launch_bounds__(kThreads) nuhc_fused_kernel(const __grid_const
     constexpr int E = 32 / B;
     constexpr int G4 = E / 4;
     extern __shared__ unsigned char s_mem[];
-    uint16_t *s_t = reinterpret_cast<uint16_t *>(s_mem);
-    uint8_t *s_inv = s_mem + 512;
-    nuhc_load_tables(p.tab, s_t, s_inv);
+    float2 *s_pair = reinterpret_cast<float2 *>(s_mem);
+    uint8_t *s_inv = s_mem + kNuhcPairBytes;
+    nuhc_load_tables(p.tab, s_pair, s_inv);
     const float m = p.mM[0], M = p.mM[1];
     const float G = static_cast<float>(p.tab.g);
     const float sc = range_scale(m, M, G);
@@ -507,9 +512,9 @@ __global__ void __launch_bounds__(kThreads) nuhc_fused_kernel(const __grid_const
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < p.nwords; w += stride) {
         const int64_t e0 = w * E;
-        uint32_t s[E];
+        float s[E];
 #pragma unroll
-        for (int i = 0; i < E; ++i) s[i] = 0;
+        for (int i = 0; i < E; ++i) s[i] = 0.0f;
         if (p.vec && e0 + E <= p.N) {
             // two register buffers, the worker loop unrolled by two: one worker's
             // loads are in flight while the other is quantized
@@ -522,20 +527,18 @@ __global__ void __launch_bounds__(kThreads) nuhc_fused_kernel(const __grid_const
 #pragma unroll
                     for (int g4 = 0; g4 < G4; ++g4) vb[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk + 1] + e0) + g4);
                 }
-                nuhc_one_worker<B, kPacked>(va, s, e0, w, wk, p, m, sc, G, s_t, s_inv);
+                nuhc_one_worker<B, kPacked>(va, s, e0, w, wk, p, m, sc, G, s_pair, s_inv);
                 if (wk + 2 < p.P) {
 #pragma unroll
                     for (int g4 = 0; g4 < G4; ++g4) va[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk + 2] + e0) + g4);
                 }
-                if (has1) nuhc_one_worker<B, kPacked>(vb, s, e0, w, wk + 1, p, m, sc, G, s_t, s_inv);
+                if (has1) nuhc_one_worker<B, kPacked>(vb, s, e0, w, wk + 1, p, m, sc, G, s_pair, s_inv);
             }
             float4 *dst = reinterpret_cast<float4 *>(p.avg + e0);
 #pragma unroll
             for (int g4 = 0; g4 < G4; ++g4)
-                __stcs(dst + g4, make_float4(__fmaf_rn(small_to_float(s[4 * g4]), k, km),
-                                             __fmaf_rn(small_to_float(s[4 * g4 + 1]), k, km),
-                                             __fmaf_rn(small_to_float(s[4 * g4 + 2]), k, km),
-                                             __fmaf_rn(small_to_float(s[4 * g4 + 3]), k, km)));
+                __stcs(dst + g4, make_float4(__fmaf_rn(s[4 * g4], k, km), __fmaf_rn(s[4 * g4 + 1], k, km),
+                                             __fmaf_rn(s[4 * g4 + 2], k, km), __fmaf_rn(s[4 * g4 + 3], k, km)));
         } else {  // ragged last word, or unaligned pointers: element by element
             for (int wk = 0; wk < p.P; ++wk) {
                 uint32_t word = 0;
@@ -544,16 +547,16 @@ __global__ void __launch_bounds__(kThreads) nuhc_fused_kernel(const __grid_const
                     if (eb >= p.N) break;
                     const uint4 r = philox_block(eb >> 2, wk, p.keys);
                     for (int i = 0; i < 4 && eb + i < p.N; ++i) {
-                        uint32_t tv;
-                        const uint32_t idx = nuhc_index(p.x[wk][eb + i], m, sc, G, p.tab.g, s_t, s_inv,
-                                                        pick(r, i), &tv);
-                        s[4 * g4 + i] += tv;
+                        float tv;
+                        const uint32_t idx = nuhc_index(p.x[wk][eb + i], m, sc, G, p.tab.g, s_pair, s_inv,
+                                                        pick(r, i), tv);
+                        s[4 * g4 + i] = __fadd_rn(s[4 * g4 + i], tv);
                         word |= idx << ((4 * g4 + i) * B);
                     }
                 }
                 if (kPacked) p.packed[wk][w] = word;
             }
-            for (int i = 0; i < E && e0 + i < p.N; ++i) p.avg[e0 + i] = __fmaf_rn(small_to_float(s[i]), k, km);
+            for (int i = 0; i < E && e0 + i < p.N; ++i) p.avg[e0 + i] = __fmaf_rn(s[i], k, km);
         }
     }
 }
@@ -1026,7 +1029,7 @@ extern "C" int gar_nuhc_encode(const float *x, int64_t N, const float *d_mM, int
     p.nwords = gar_thc_words(N, b);
     p.worker = worker;
     p.vec = aligned(x, 16) ? 1 : 0;
-    const size_t smem = 512 + static_cast<size_t>(g);
+    const size_t smem = kNuhcPairBytes + static_cast<size_t>(g);
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     switch (b) {
         case 1: nuhc_encode_kernel<1><<<grid_for(nuhc_encode_kernel<1>, p.nwords), kThreads, smem, stream>>>(p); break;
@@ -1125,7 +1128,7 @@ extern "C" int gar_nuhc_allreduce_fused(const float *const *x, int32_t P, int64_
             p.packed[w] = packed[w];
         }
     }
-    const size_t smem = 512 + static_cast<size_t>(g);
+    const size_t smem = kNuhcPairBytes + static_cast<size_t>(g);
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 #define GAR_NUHC_CASE(BB)                                                                                    \
     case BB:                                                                                                 \
