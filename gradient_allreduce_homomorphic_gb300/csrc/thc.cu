@@ -307,274 +307,6 @@ __global__ void __launch_bounds__(kThreads) thc_decode_kernel(const __grid_const
         p.avg[e] = __fmaf_rn(small_to_float(p.sums[e]), k, m);
 }
 
-// ------------------------------------------------------- non-uniform THC
-// ([T] section 5, Algorithm 2.)  Granularity g >= 2^b - 1: the grid is
-// m + k (M - m)/g, k = 0..g, and a worker may only send the 2^b points whose
-// k is a table value T[z].  Decision in fp32, one rounding per op:
-//   t = clamp((x - m) * (g / (M - m)), 0, g)
-//   z = the largest z <= L - 1 with T[z] <= t  (= inv[min(floor(t), g - 1)])
-//   up iff u < (t - T[z]) / (T[z + 1] - T[z]) exactly  (u as in uniform THC)
-//   index = z + up; the PS sums T[index].
-constexpr int kMaxGranularity = 16383;
-
-struct NuhcTable {
-    uint16_t t[256];
-    int32_t L;
-    int32_t g;
-};
-
-// Shared-memory copies of T and of its inverse on the integers 0..g-1.
-// Shared-memory tables: the pairs (T[z], T[z + 1]) as floats for z < L (one
-// 8-byte load gives both neighbours), and the inverse of T on the integers
-// 0..g-1 (z of the interval holding k).
-constexpr int kNuhcPairBytes = 256 * 8;  // float2[255], rounded up
-__device__ __forceinline__ void nuhc_load_tables(const NuhcTable &tab, float2 *s_pair, uint8_t *s_inv) {
-    for (int z = threadIdx.x; z < tab.L; z += blockDim.x)
-        s_pair[z] = make_float2(static_cast<float>(tab.t[z]), static_cast<float>(tab.t[z + 1]));
-    for (int k = threadIdx.x; k < tab.g; k += blockDim.x) {
-        int lo = 0, hi = tab.L - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (tab.t[mid] <= k) lo = mid;
-            else hi = mid - 1;
-        }
-        s_inv[k] = static_cast<uint8_t>(lo);
-    }
-    __syncthreads();
-}
-
-// Returns the index; tv receives the table value it stands for (an integer
-// below 2^14, as a float).
-__device__ __forceinline__ uint32_t nuhc_index(float x, float m, float sc, float G, int g, const float2 *s_pair,
-                                               const uint8_t *s_inv, uint32_t r, float &tv) {
-    float t = __fmul_rn(__fsub_rn(x, m), sc);
-    t = fminf(fmaxf(t, 0.0f), G);
-    int k = __float_as_int(__fadd_rd(t, 8388608.0f)) - 0x4B000000;  // floor(t)
-    k = k < g - 1 ? k : g - 1;
-    const int z = s_inv[k];
-    const float2 lh = s_pair[z];  // T[z], T[z + 1]
-    // up iff u < (t - lo) / (hi - lo) exactly, i.e. u * (hi - lo) < t - lo: t - lo and
-    // hi - lo are exact (integer lo, hi below 2^14, t >= lo), u = (r mod 2^23) 2^-23 is
-    // exact, and the sign of the once-rounded fma(-u, hi - lo, t - lo) is the sign of
-    // the exact difference (a nonzero one is a multiple of 2^-149: never rounds to 0)
-    const float u = __fsub_rn(__uint_as_float((r & 0x007FFFFFu) | 0x3F800000u), 1.0f);
-    const bool up = __fmaf_rn(-u, __fsub_rn(lh.y, lh.x), __fsub_rn(t, lh.x)) > 0.0f;
-    tv = up ? lh.y : lh.x;
-    return static_cast<uint32_t>(z) + (up ? 1u : 0u);
-}
-
-struct NuhcEncodeParams {
-    PhiloxKeys keys;
-    NuhcTable tab;
-    const float *x;
-    const float *mM;
-    uint32_t *packed;
-    int64_t N;
-    int64_t nwords;
-    int32_t worker;
-    int32_t vec;
-};
-
-template <int B>
-__global__ void __launch_bounds__(kThreads) nuhc_encode_kernel(const __grid_constant__ NuhcEncodeParams p) {
-    constexpr int E = 32 / B;
-    extern __shared__ unsigned char s_mem[];
-    float2 *s_pair = reinterpret_cast<float2 *>(s_mem);
-    uint8_t *s_inv = s_mem + kNuhcPairBytes;
-    nuhc_load_tables(p.tab, s_pair, s_inv);
-    const float m = p.mM[0], M = p.mM[1];
-    const float G = static_cast<float>(p.tab.g);
-    const float sc = range_scale(m, M, G);
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < p.nwords; w += stride) {
-        const int64_t e0 = w * E;
-        uint32_t word = 0;
-        float tv;
-        for (int g4 = 0; g4 < E / 4; ++g4) {
-            const int64_t eb = e0 + 4 * g4;
-            if (eb >= p.N) break;
-            const uint4 r = philox_block(eb >> 2, p.worker, p.keys);
-            float4 v;
-            if (p.vec && eb + 4 <= p.N) {
-                v = __ldcs(reinterpret_cast<const float4 *>(p.x + eb));
-            } else {
-                v = make_float4(m, m, m, m);  // past N: index 0, masked out below
-                if (eb < p.N) v.x = p.x[eb];
-                if (eb + 1 < p.N) v.y = p.x[eb + 1];
-                if (eb + 2 < p.N) v.z = p.x[eb + 2];
-                if (eb + 3 < p.N) v.w = p.x[eb + 3];
-            }
-            const uint32_t i0 = nuhc_index(v.x, m, sc, G, p.tab.g, s_pair, s_inv, r.x, tv);
-            const uint32_t i1 = nuhc_index(v.y, m, sc, G, p.tab.g, s_pair, s_inv, r.y, tv);
-            const uint32_t i2 = nuhc_index(v.z, m, sc, G, p.tab.g, s_pair, s_inv, r.z, tv);
-            const uint32_t i3 = nuhc_index(v.w, m, sc, G, p.tab.g, s_pair, s_inv, r.w, tv);
-            uint32_t q = i0 | (i1 << B) | (i2 << (2 * B)) | (i3 << (3 * B));
-            const int64_t valid = p.N - eb;  // elements of this group inside N
-            if (valid < 4) q &= (1u << (B * valid)) - 1u;
-            word |= q << (4 * g4 * B);
-        }
-        __stcs(p.packed + w, word);
-    }
-}
-
-struct NuhcAggParams {
-    NuhcTable tab;
-    const uint32_t *packed[GAR_MAX_WORKERS];
-    uint16_t *sums;
-    int64_t N;
-    int32_t P;
-    int32_t pad;
-};
-
-// One packed word of every worker per thread: the PS looks each index up
-// and adds the table values.
-template <int B>
-__global__ void __launch_bounds__(kThreads) nuhc_aggregate_kernel(const __grid_constant__ NuhcAggParams p) {
-    constexpr int E = 32 / B;
-    constexpr uint32_t kMask = (1u << B) - 1u;
-    __shared__ uint16_t s_t[256];
-    for (int z = threadIdx.x; z <= p.tab.L; z += blockDim.x) s_t[z] = p.tab.t[z];
-    __syncthreads();
-    const int64_t nwords = (p.N + E - 1) / E;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < nwords; w += stride) {
-        uint32_t s[E];
-#pragma unroll
-        for (int i = 0; i < E; ++i) s[i] = 0;
-        for (int k = 0; k < p.P; ++k) {
-            const uint32_t word = __ldcs(p.packed[k] + w);
-#pragma unroll
-            for (int i = 0; i < E; ++i) s[i] += s_t[(word >> (B * i)) & kMask];
-        }
-        const int64_t e0 = w * E;
-        if (e0 + E <= p.N && (E % 2 == 0)) {
-#pragma unroll
-            for (int i = 0; i < E; i += 2)
-                *reinterpret_cast<uint32_t *>(p.sums + e0 + i) = (s[i] & 0xFFFFu) | (s[i + 1] << 16);
-        } else {
-            for (int i = 0; i < E && e0 + i < p.N; ++i) p.sums[e0 + i] = static_cast<uint16_t>(s[i]);
-        }
-    }
-}
-
-struct NuhcFusedParams {
-    PhiloxKeys keys;
-    NuhcTable tab;
-    const float *x[GAR_MAX_WORKERS];
-    uint32_t *packed[GAR_MAX_WORKERS];
-    const float *mM;
-    float *avg;
-    int64_t N;
-    int64_t nwords;
-    int32_t P;
-    int32_t vec;
-};
-
-// One worker's contribution to a whole word of E = 4 G4 elements: Philox
-// draws, indices, the table values added to the running sums s, the packed
-// word stored if wanted.
-// (The sums of table values are integers below 2^24: exact in fp32.)
-template <int B, bool kPacked, int G4>
-__device__ __forceinline__ void nuhc_one_worker(const float4 (&v)[G4], float (&s)[4 * G4], int64_t e0, int64_t w,
-                                                int wk, const NuhcFusedParams &p, float m, float sc, float G,
-                                                const float2 *s_pair, const uint8_t *s_inv) {
-    uint32_t word = 0;
-#pragma unroll
-    for (int g4 = 0; g4 < G4; ++g4) {
-        const uint4 r = philox_block((e0 >> 2) + g4, wk, p.keys);
-        float t0, t1, t2, t3;
-        const uint32_t i0 = nuhc_index(v[g4].x, m, sc, G, p.tab.g, s_pair, s_inv, r.x, t0);
-        const uint32_t i1 = nuhc_index(v[g4].y, m, sc, G, p.tab.g, s_pair, s_inv, r.y, t1);
-        const uint32_t i2 = nuhc_index(v[g4].z, m, sc, G, p.tab.g, s_pair, s_inv, r.z, t2);
-        const uint32_t i3 = nuhc_index(v[g4].w, m, sc, G, p.tab.g, s_pair, s_inv, r.w, t3);
-        s[4 * g4] = __fadd_rn(s[4 * g4], t0);
-        s[4 * g4 + 1] = __fadd_rn(s[4 * g4 + 1], t1);
-        s[4 * g4 + 2] = __fadd_rn(s[4 * g4 + 2], t2);
-        s[4 * g4 + 3] = __fadd_rn(s[4 * g4 + 3], t3);
-        if (kPacked) word |= (i0 | (i1 << B) | (i2 << (2 * B)) | (i3 << (3 * B))) << (4 * g4 * B);
-    }
-    if (kPacked) __stcs(p.packed[wk] + w, word);
-}
-
-template <int B, bool kPacked>
-__global__ void __launch_bounds__(kThreads) nuhc_fused_kernel(const __grid_constant__ NuhcFusedParams p) {
-    constexpr int E = 32 / B;
-    constexpr int G4 = E / 4;
-    extern __shared__ unsigned char s_mem[];
-    float2 *s_pair = reinterpret_cast<float2 *>(s_mem);
-    uint8_t *s_inv = s_mem + kNuhcPairBytes;
-    nuhc_load_tables(p.tab, s_pair, s_inv);
-    const float m = p.mM[0], M = p.mM[1];
-    const float G = static_cast<float>(p.tab.g);
-    const float sc = range_scale(m, M, G);
-    float km;
-    const float k = decode_step(p.mM, G, static_cast<float>(p.P), km);
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < p.nwords; w += stride) {
-        const int64_t e0 = w * E;
-        float s[E];
-#pragma unroll
-        for (int i = 0; i < E; ++i) s[i] = 0.0f;
-        if (p.vec && e0 + E <= p.N) {
-            // two register buffers, the worker loop unrolled by two: one worker's
-            // loads are in flight while the other is quantized
-            float4 va[G4], vb[G4];
-#pragma unroll
-            for (int g4 = 0; g4 < G4; ++g4) va[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[0] + e0) + g4);
-            for (int wk = 0; wk < p.P; wk += 2) {
-                const bool has1 = wk + 1 < p.P;
-                if (has1) {
-#pragma unroll
-                    for (int g4 = 0; g4 < G4; ++g4) vb[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk + 1] + e0) + g4);
-                }
-                nuhc_one_worker<B, kPacked>(va, s, e0, w, wk, p, m, sc, G, s_pair, s_inv);
-                if (wk + 2 < p.P) {
-#pragma unroll
-                    for (int g4 = 0; g4 < G4; ++g4) va[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk + 2] + e0) + g4);
-                }
-                if (has1) nuhc_one_worker<B, kPacked>(vb, s, e0, w, wk + 1, p, m, sc, G, s_pair, s_inv);
-            }
-            float4 *dst = reinterpret_cast<float4 *>(p.avg + e0);
-#pragma unroll
-            for (int g4 = 0; g4 < G4; ++g4)
-                __stcs(dst + g4, make_float4(__fmaf_rn(s[4 * g4], k, km), __fmaf_rn(s[4 * g4 + 1], k, km),
-                                             __fmaf_rn(s[4 * g4 + 2], k, km), __fmaf_rn(s[4 * g4 + 3], k, km)));
-        } else {  // ragged last word, or unaligned pointers: element by element
-            for (int wk = 0; wk < p.P; ++wk) {
-                uint32_t word = 0;
-                for (int g4 = 0; g4 < G4; ++g4) {
-                    const int64_t eb = e0 + 4 * g4;
-                    if (eb >= p.N) break;
-                    const uint4 r = philox_block(eb >> 2, wk, p.keys);
-                    for (int i = 0; i < 4 && eb + i < p.N; ++i) {
-                        float tv;
-                        const uint32_t idx = nuhc_index(p.x[wk][eb + i], m, sc, G, p.tab.g, s_pair, s_inv,
-                                                        pick(r, i), tv);
-                        s[4 * g4 + i] = __fadd_rn(s[4 * g4 + i], tv);
-                        word |= idx << ((4 * g4 + i) * B);
-                    }
-                }
-                if (kPacked) p.packed[wk][w] = word;
-            }
-            for (int i = 0; i < E && e0 + i < p.N; ++i) p.avg[e0 + i] = __fmaf_rn(s[i], k, km);
-        }
-    }
-}
-
-int nuhc_table(const uint16_t *table, int b, int g, NuhcTable &tab) {
-    if (!table) return fail(GAR_EINVAL, "table is NULL");
-    const int L = (1 << b) - 1;
-    if (g < L || g > kMaxGranularity) return fail(GAR_EINVAL, "granularity %d outside [%d, %d]", g, L, kMaxGranularity);
-    if (table[0] != 0 || table[L] != g) return fail(GAR_EINVAL, "table must start at 0 and end at g=%d", g);
-    for (int z = 0; z < L; ++z)
-        if (table[z + 1] <= table[z]) return fail(GAR_EINVAL, "table not strictly increasing at %d", z);
-    std::memset(&tab, 0, sizeof(tab));
-    for (int z = 0; z <= L; ++z) tab.t[z] = table[z];
-    tab.L = L;
-    tab.g = g;
-    return GAR_OK;
-}
-
 // The launch for p.P workers: the build fixed to that count when there is one.
 int dispatch_fused(const FusedParams &p, int b, bool packed, cudaStream_t stream) {
     switch (p.P) {
@@ -636,8 +368,6 @@ int64_t plan_nmse_pairs_bound(const int64_t *buf_numel, int32_t n_buffers, int32
     return tiles + 5 * static_cast<int64_t>(count) + 3 * static_cast<int64_t>(n_buffers) + 1;
 }
 
-
-bool valid_b(int b) { return b == 1 || b == 2 || b == 4 || b == 8; }
 
 }  // namespace
 }  // namespace gar
@@ -742,6 +472,26 @@ extern "C" int gar_thc_aggregate(const uint32_t *const *packed, int32_t P, int64
     return check_launch("thc_aggregate_kernel");
 }
 
+namespace gar {
+namespace thc {
+int launch_grid_decode(const uint16_t *sums, int64_t N, const float *d_mM, int steps, int P, float *avg,
+                       cudaStream_t stream) {
+    DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.sums = sums;
+    p.mM = d_mM;
+    p.avg = avg;
+    p.N = N;
+    p.L = static_cast<float>(steps);
+    p.fp = static_cast<float>(P);
+    p.vec = aligned(sums, 16) && aligned(avg, 16);
+    const int64_t items = p.vec ? ceil_div(N, 8) : N;
+    thc_decode_kernel<<<grid_for(thc_decode_kernel, items), kThreads, 0, stream>>>(p);
+    return check_launch("thc_decode_kernel");
+}
+}  // namespace thc
+}  // namespace gar
+
 extern "C" int gar_thc_decode(const uint16_t *sums, int64_t N, const float *d_mM, int32_t b, int32_t P, float *avg,
                               gar_stream_t stream_) {
     if (!valid_b(b)) return fail(GAR_EINVAL, "b=%d not in {1, 2, 4, 8}", b);
@@ -750,18 +500,7 @@ extern "C" int gar_thc_decode(const uint16_t *sums, int64_t N, const float *d_mM
     if (N == 0) return GAR_OK;
     if (!sums || !avg) return fail(GAR_EINVAL, "sums or avg is NULL");
     if (!aligned(sums, 2) || !aligned(avg, 4) || !aligned(d_mM, 4)) return fail(GAR_EALIGN, "misaligned pointer");
-    DecodeParams p;
-    std::memset(&p, 0, sizeof(p));
-    p.sums = sums;
-    p.mM = d_mM;
-    p.avg = avg;
-    p.N = N;
-    p.L = static_cast<float>((1 << b) - 1);
-    p.fp = static_cast<float>(P);
-    p.vec = aligned(sums, 16) && aligned(avg, 16);
-    const int64_t items = p.vec ? ceil_div(N, 8) : N;
-    thc_decode_kernel<<<grid_for(thc_decode_kernel, items), kThreads, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(p);
-    return check_launch("thc_decode_kernel");
+    return launch_grid_decode(sums, N, d_mM, (1 << b) - 1, P, avg, reinterpret_cast<cudaStream_t>(stream_));
 }
 
 // Shared by the plain and the straggler-masked fused entry points: the
@@ -1005,144 +744,4 @@ extern "C" int gar_thc_allreduce_fused_plan_nmse(const float *const *src, int32_
     if (!ref) return fail(GAR_EINVAL, "ref is NULL");
     return thc_plan_impl(src, P, segs, dtype, count, buf_numel, n_buffers, b, seed, d_mM, out, packed, ref, d_pair,
                          static_cast<double *>(d_workspace), workspace_bytes, stream);
-}
-
-// ------------------------------------------------------- non-uniform THC
-extern "C" int gar_nuhc_encode(const float *x, int64_t N, const float *d_mM, int32_t b, int32_t g,
-                               const uint16_t *table, uint64_t seed, int32_t worker, uint32_t *packed,
-                               gar_stream_t stream_) {
-    if (!valid_b(b)) return fail(GAR_EINVAL, "b=%d not in {1, 2, 4, 8}", b);
-    NuhcEncodeParams p;
-    std::memset(&p, 0, sizeof(p));
-    int rc = nuhc_table(table, b, g, p.tab);
-    if (rc) return rc;
-    if (N < 0 || !d_mM) return fail(GAR_EINVAL, "N < 0 or d_mM NULL");
-    if (N == 0) return GAR_OK;
-    if (!x || !packed) return fail(GAR_EINVAL, "x or packed is NULL");
-    if (worker < 0) return fail(GAR_EINVAL, "worker %d < 0", worker);
-    if (!aligned(x, 4) || !aligned(packed, 4) || !aligned(d_mM, 4)) return fail(GAR_EALIGN, "misaligned pointer");
-    p.keys = philox_keys(seed);
-    p.x = x;
-    p.mM = d_mM;
-    p.packed = packed;
-    p.N = N;
-    p.nwords = gar_thc_words(N, b);
-    p.worker = worker;
-    p.vec = aligned(x, 16) ? 1 : 0;
-    const size_t smem = kNuhcPairBytes + static_cast<size_t>(g);
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    switch (b) {
-        case 1: nuhc_encode_kernel<1><<<grid_for(nuhc_encode_kernel<1>, p.nwords), kThreads, smem, stream>>>(p); break;
-        case 2: nuhc_encode_kernel<2><<<grid_for(nuhc_encode_kernel<2>, p.nwords), kThreads, smem, stream>>>(p); break;
-        case 4: nuhc_encode_kernel<4><<<grid_for(nuhc_encode_kernel<4>, p.nwords), kThreads, smem, stream>>>(p); break;
-        default: nuhc_encode_kernel<8><<<grid_for(nuhc_encode_kernel<8>, p.nwords), kThreads, smem, stream>>>(p); break;
-    }
-    return check_launch("nuhc_encode_kernel");
-}
-
-extern "C" int gar_nuhc_aggregate(const uint32_t *const *packed, int32_t P, int64_t N, int32_t b,
-                                  const uint16_t *table, uint16_t *sums, gar_stream_t stream_) {
-    if (!valid_b(b)) return fail(GAR_EINVAL, "b=%d not in {1, 2, 4, 8}", b);
-    if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
-    NuhcAggParams p;
-    std::memset(&p, 0, sizeof(p));
-    if (!table) return fail(GAR_EINVAL, "table is NULL");
-    const int L = (1 << b) - 1;
-    int rc = nuhc_table(table, b, table[L], p.tab);
-    if (rc) return rc;
-    if (static_cast<int64_t>(P) * p.tab.g > 65535) return fail(GAR_EOVERFLOW, "P * g > 65535");
-    if (N < 0) return fail(GAR_EINVAL, "N < 0");
-    if (N == 0) return GAR_OK;
-    if (!packed || !sums) return fail(GAR_EINVAL, "packed or sums is NULL");
-    if (!aligned(sums, 4)) return fail(GAR_EALIGN, "sums not 4-byte aligned");
-    p.sums = sums;
-    p.N = N;
-    p.P = P;
-    for (int w = 0; w < P; ++w) {
-        if (!packed[w]) return fail(GAR_EINVAL, "packed vector %d is NULL", w);
-        if (!aligned(packed[w], 4)) return fail(GAR_EALIGN, "packed vector %d not 4-byte aligned", w);
-        p.packed[w] = packed[w];
-    }
-    const int64_t words = gar_thc_words(N, b);
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    switch (b) {
-        case 1: nuhc_aggregate_kernel<1><<<grid_for(nuhc_aggregate_kernel<1>, words), kThreads, 0, stream>>>(p); break;
-        case 2: nuhc_aggregate_kernel<2><<<grid_for(nuhc_aggregate_kernel<2>, words), kThreads, 0, stream>>>(p); break;
-        case 4: nuhc_aggregate_kernel<4><<<grid_for(nuhc_aggregate_kernel<4>, words), kThreads, 0, stream>>>(p); break;
-        default: nuhc_aggregate_kernel<8><<<grid_for(nuhc_aggregate_kernel<8>, words), kThreads, 0, stream>>>(p); break;
-    }
-    return check_launch("nuhc_aggregate_kernel");
-}
-
-extern "C" int gar_nuhc_decode(const uint16_t *sums, int64_t N, const float *d_mM, int32_t g, int32_t P,
-                               float *avg, gar_stream_t stream_) {
-    if (g < 1 || g > kMaxGranularity) return fail(GAR_EINVAL, "granularity %d outside [1, %d]", g, kMaxGranularity);
-    if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
-    if (N < 0 || !d_mM) return fail(GAR_EINVAL, "N < 0 or d_mM NULL");
-    if (N == 0) return GAR_OK;
-    if (!sums || !avg) return fail(GAR_EINVAL, "sums or avg is NULL");
-    if (!aligned(sums, 2) || !aligned(avg, 4) || !aligned(d_mM, 4)) return fail(GAR_EALIGN, "misaligned pointer");
-    DecodeParams p;  // the uniform decode with the step (M - m) / g
-    std::memset(&p, 0, sizeof(p));
-    p.sums = sums;
-    p.mM = d_mM;
-    p.avg = avg;
-    p.N = N;
-    p.L = static_cast<float>(g);
-    p.fp = static_cast<float>(P);
-    p.vec = aligned(sums, 16) && aligned(avg, 16);
-    const int64_t items = p.vec ? ceil_div(N, 8) : N;
-    thc_decode_kernel<<<grid_for(thc_decode_kernel, items), kThreads, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(p);
-    return check_launch("thc_decode_kernel");
-}
-
-extern "C" int gar_nuhc_allreduce_fused(const float *const *x, int32_t P, int64_t N, int32_t b, int32_t g,
-                                        const uint16_t *table, uint64_t seed, const float *d_mM, float *avg,
-                                        uint32_t *const *packed, gar_stream_t stream_) {
-    if (!valid_b(b)) return fail(GAR_EINVAL, "b=%d not in {1, 2, 4, 8}", b);
-    if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
-    NuhcFusedParams p;
-    std::memset(&p, 0, sizeof(p));
-    int rc = nuhc_table(table, b, g, p.tab);
-    if (rc) return rc;
-    if (static_cast<int64_t>(P) * g > 65535) return fail(GAR_EOVERFLOW, "P * g > 65535");
-    if (N < 0 || !d_mM || !x) return fail(GAR_EINVAL, "N < 0 or NULL argument");
-    if (N == 0) return GAR_OK;
-    if (!avg) return fail(GAR_EINVAL, "avg is NULL");
-    if (!aligned(avg, 4) || !aligned(d_mM, 4)) return fail(GAR_EALIGN, "misaligned pointer");
-    p.keys = philox_keys(seed);
-    p.mM = d_mM;
-    p.avg = avg;
-    p.N = N;
-    p.nwords = gar_thc_words(N, b);
-    p.P = P;
-    p.vec = aligned(avg, 16) ? 1 : 0;
-    for (int w = 0; w < P; ++w) {
-        if (!x[w]) return fail(GAR_EINVAL, "input %d is NULL", w);
-        if (!aligned(x[w], 4)) return fail(GAR_EALIGN, "input %d not 4-byte aligned", w);
-        p.x[w] = x[w];
-        p.vec = p.vec && aligned(x[w], 16);
-        if (packed) {
-            if (!packed[w]) return fail(GAR_EINVAL, "packed vector %d is NULL", w);
-            if (!aligned(packed[w], 4)) return fail(GAR_EALIGN, "packed vector %d not 4-byte aligned", w);
-            p.packed[w] = packed[w];
-        }
-    }
-    const size_t smem = kNuhcPairBytes + static_cast<size_t>(g);
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-#define GAR_NUHC_CASE(BB)                                                                                    \
-    case BB:                                                                                                 \
-        if (packed)                                                                                          \
-            nuhc_fused_kernel<BB, true><<<grid_for(nuhc_fused_kernel<BB, true>, p.nwords), kThreads, smem, stream>>>(p); \
-        else                                                                                                 \
-            nuhc_fused_kernel<BB, false><<<grid_for(nuhc_fused_kernel<BB, false>, p.nwords), kThreads, smem, stream>>>(p); \
-        break;
-    switch (b) {
-        GAR_NUHC_CASE(1)
-        GAR_NUHC_CASE(2)
-        GAR_NUHC_CASE(4)
-        GAR_NUHC_CASE(8)
-    }
-#undef GAR_NUHC_CASE
-    return check_launch("nuhc_fused_kernel");
 }

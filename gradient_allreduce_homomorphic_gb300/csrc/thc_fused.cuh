@@ -599,5 +599,14 @@ extern template int launch_fused_plan<8>(const ThcPlanParams &, int, bool, bool,
 extern template int launch_fused_plan<16>(const ThcPlanParams &, int, bool, bool, cudaStream_t);
 extern template int launch_fused_plan<64>(const ThcPlanParams &, int, bool, bool, cudaStream_t);
 
+// Index widths the packing supports.
+inline bool valid_b(int b) { return b == 1 || b == 2 || b == 4 || b == 8; }
+
+// The decode avg = m + (M - m)/steps * sums/P on a grid of `steps` steps
+// (uniform THC: steps = 2^b - 1; non-uniform: the granularity g); arguments
+// already checked by the caller.
+int launch_grid_decode(const uint16_t *sums, int64_t N, const float *d_mM, int steps, int P, float *avg,
+                       cudaStream_t stream);
+
 }  // namespace thc
 }  // namespace gar
