@@ -67,6 +67,13 @@ def _load():
                 "oracle_bidir_schedule_f32": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, vp]),
                 "oracle_bidir_fold_f32": (C.c_int, [pp, C.c_int, i64, C.c_int, vp]),
                 "oracle_bidir_fold_f32_samples": (C.c_int, [vp, C.c_int, i64, C.c_int, vp, i64, vp]),
+                "oracle_dbtree_build": (C.c_int, [C.c_int, C.c_int, vp, vp, vp]),
+                "oracle_dbtree_half": (i64, [i64]),
+                "oracle_dbtree_schedule_f32": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, vp]),
+                "oracle_dbtree_fold_f32": (C.c_int, [pp, C.c_int, i64, C.c_int, vp]),
+                "oracle_dbtree_fold_bf16": (C.c_int, [pp, C.c_int, i64, C.c_int, vp]),
+                "oracle_dbtree_fold_f32_samples": (C.c_int, [vp, C.c_int, i64, C.c_int, vp, i64, vp]),
+                "oracle_dbtree_fold_bf16_samples": (C.c_int, [vp, C.c_int, i64, C.c_int, vp, i64, vp]),
                 "oracle_ring_fold_f32_samples": (C.c_int, [vp, C.c_int, i64, C.c_int, vp, i64, vp]),
                 "oracle_ring_fold_bf16_samples": (C.c_int, [vp, C.c_int, i64, C.c_int, vp, i64, vp]),
                 "oracle_thc_allreduce_samples": (C.c_int, [vp, C.c_int, vp, i64, C.c_int, u64, C.c_float,
@@ -235,6 +242,58 @@ def bf16_to_f32(h: int) -> float:
 
 def f32_to_bf16(f: float) -> int:
     return int(_load().oracle_f32_to_bf16(float(np.float32(f))))
+
+
+# ------------------------------------------------------ double binary tree
+def dbtree_build(p: int, tree: int):
+    """(root, parent[p], left[p], right[p]) of tree 0 or 1 (-1: none)."""
+    par, lc, rc = (np.zeros(p, np.int32) for _ in range(3))
+    root = _load().oracle_dbtree_build(p, tree, _ptr(par), _ptr(lc), _ptr(rc))
+    _check(0 if root >= 0 else -1, "dbtree_build")
+    return root, par, lc, rc
+
+
+def dbtree_half(n: int) -> int:
+    return int(_load().oracle_dbtree_half(n))
+
+
+def dbtree_schedule(bufs, op: int = AVG):
+    """Literal two-tree reduce + broadcast in place (fp32); returns (steps, sent_elems[p])."""
+    p, n = len(bufs), bufs[0].size
+    sent = np.zeros(p, np.int64)
+    steps = C.c_int(0)
+    _check(_load().oracle_dbtree_schedule_f32(_ptrs(bufs), p, n, op, _ptr(sent), C.byref(steps)),
+           "dbtree_schedule")
+    return steps.value, sent
+
+
+def dbtree_fold(xs, op: int = AVG):
+    """Closed-form two-tree fold; fp32 arrays -> fp32, uint16 (bf16 bits) -> uint16."""
+    p, n = len(xs), xs[0].size
+    lib = _load()
+    if xs[0].dtype == np.float32:
+        out = np.empty(n, np.float32)
+        _check(lib.oracle_dbtree_fold_f32(_ptrs(xs), p, n, op, _ptr(out)), "dbtree_fold")
+    else:
+        out = np.empty(n, np.uint16)
+        _check(lib.oracle_dbtree_fold_bf16(_ptrs(xs), p, n, op, _ptr(out)), "dbtree_fold")
+    return out
+
+
+def dbtree_fold_samples(vals, n: int, idx, op: int = AVG):
+    """vals[w, k] = worker w's value (fp32, or bf16 bits as uint16) at element idx[k]."""
+    idx = np.ascontiguousarray(idx, np.int64)
+    lib = _load()
+    if vals.dtype == np.float32:
+        vals = np.ascontiguousarray(vals)
+        out = np.empty(idx.size, np.float32)
+        rc = lib.oracle_dbtree_fold_f32_samples(_ptr(vals), vals.shape[0], n, op, _ptr(idx), idx.size, _ptr(out))
+    else:
+        vals = np.ascontiguousarray(vals, np.uint16)
+        out = np.empty(idx.size, np.uint16)
+        rc = lib.oracle_dbtree_fold_bf16_samples(_ptr(vals), vals.shape[0], n, op, _ptr(idx), idx.size, _ptr(out))
+    _check(rc, "dbtree_samples")
+    return out
 
 
 # ----------------------------------------------------------------- fusion

@@ -362,6 +362,224 @@ int oracle_bidir_fold_f32_samples(const float *vals, int p, int64_t n, int op, c
 }
 
 /* ===================================================================== */
+/* Double binary tree [R] "Design Alternatives & Collective Comparison    */
+/* Matrix: Ring vs. Tree vs. NVLS"; construction [ST]                     */
+/* ===================================================================== */
+/* The tutorial compares the ring with the double-binary-tree all-reduce
+ * (two complementary trees, each carrying half the data; about 2 log2(p)
+ * latency steps; about 2M bytes sent per rank) but prints no construction.
+ * Reading: the two-tree scheme of [ST].  Tree 1 is the in-order binary tree
+ * on the labels 1..p: the root of a run of labels is the label in it with
+ * the most trailing zero bits, and its left and right subtrees are built
+ * the same way on the labels below and above it.  Label l hosts rank l - 1.
+ * Tree 2 has the same shape; label l hosts rank p - l when p is even (the
+ * mirror image) and rank (l - 2) mod p when p is odd (shifted by one).
+ * Elements [0, ceil(n/2)) are reduced on tree 1, the rest on tree 2.  A
+ * node's partial sum is its own value plus its left child's partial sum,
+ * then plus its right child's (fp32); the root divides by p for AVG and the
+ * value is broadcast down the same tree.                                  */
+static int low_zeros(int v) {
+    int k = 0;
+    while ((v & 1) == 0) {
+        v >>= 1;
+        ++k;
+    }
+    return k;
+}
+
+/* Builds the run lo..hi of labels; returns its root label (0: empty run). */
+static int build_run(int lo, int hi, int up, int *par, int *lc, int *rc) {
+    if (lo > hi) return 0;
+    int root = lo;
+    for (int l = lo + 1; l <= hi; ++l)
+        if (low_zeros(l) > low_zeros(root)) root = l;
+    par[root] = up;
+    lc[root] = build_run(lo, root - 1, root, par, lc, rc);
+    rc[root] = build_run(root + 1, hi, root, par, lc, rc);
+    return root;
+}
+
+static int host_rank(int p, int tree, int label) {
+    if (tree == 0) return label - 1;
+    if (p % 2 == 0) return p - label;
+    return ((label - 2) % p + p) % p;
+}
+
+int oracle_dbtree_build(int p, int tree, int32_t *parent, int32_t *left, int32_t *right) {
+    if (p < 1 || p > 64 || (tree != 0 && tree != 1)) return -1;
+    int par[65], lc[65], rc[65];
+    int root = build_run(1, p, 0, par, lc, rc);
+    for (int l = 1; l <= p; ++l) {
+        int r = host_rank(p, tree, l);
+        parent[r] = par[l] ? host_rank(p, tree, par[l]) : -1;
+        left[r] = lc[l] ? host_rank(p, tree, lc[l]) : -1;
+        right[r] = rc[l] ? host_rank(p, tree, rc[l]) : -1;
+    }
+    return host_rank(p, tree, root);
+}
+
+int64_t oracle_dbtree_half(int64_t n) { return (n + 1) / 2; }
+
+/* partial sum of the subtree under rank r; v[w] = worker w's value */
+static float subtree_sum(const float *v, const int32_t *left, const int32_t *right, int r) {
+    float s = v[r];
+    if (left[r] >= 0) s = s + subtree_sum(v, left, right, left[r]);
+    if (right[r] >= 0) s = s + subtree_sum(v, left, right, right[r]);
+    return s;
+}
+
+struct dbtrees {
+    int32_t parent[2][64], left[2][64], right[2][64];
+    int root[2];
+};
+
+static int dbtrees_make(int p, struct dbtrees *t) {
+    for (int k = 0; k < 2; ++k) {
+        t->root[k] = oracle_dbtree_build(p, k, t->parent[k], t->left[k], t->right[k]);
+        if (t->root[k] < 0) return -1;
+    }
+    return 0;
+}
+
+static float dbtree_value(const struct dbtrees *t, int p, int64_t n, int op, int64_t k, const float *v) {
+    int tr = k < oracle_dbtree_half(n) ? 0 : 1;
+    float s = subtree_sum(v, t->left[tr], t->right[tr], t->root[tr]);
+    if (op == ORACLE_AVG) s = s / (float)p;
+    return s;
+}
+
+int oracle_dbtree_fold_f32(const float *const *x, int p, int64_t n, int op, float *out) {
+    struct dbtrees t;
+    if (n < 0 || (op != ORACLE_SUM && op != ORACLE_AVG) || dbtrees_make(p, &t)) return -1;
+    float v[64];
+    for (int64_t k = 0; k < n; ++k) {
+        for (int w = 0; w < p; ++w) v[w] = x[w][k];
+        out[k] = dbtree_value(&t, p, n, op, k, v);
+    }
+    return 0;
+}
+
+int oracle_dbtree_fold_bf16(const uint16_t *const *x, int p, int64_t n, int op, uint16_t *out) {
+    struct dbtrees t;
+    if (n < 0 || (op != ORACLE_SUM && op != ORACLE_AVG) || dbtrees_make(p, &t)) return -1;
+    float v[64];
+    for (int64_t k = 0; k < n; ++k) {
+        for (int w = 0; w < p; ++w) v[w] = oracle_bf16_to_f32(x[w][k]);
+        out[k] = oracle_f32_to_bf16(dbtree_value(&t, p, n, op, k, v));
+    }
+    return 0;
+}
+
+/* sampled forms: vals[w * count + j] = worker w's value at element e[j] */
+int oracle_dbtree_fold_f32_samples(const float *vals, int p, int64_t n, int op, const int64_t *e,
+                                   int64_t count, float *out) {
+    struct dbtrees t;
+    if (n < 0 || (op != ORACLE_SUM && op != ORACLE_AVG) || dbtrees_make(p, &t)) return -1;
+    float v[64];
+    for (int64_t j = 0; j < count; ++j) {
+        if (e[j] < 0 || e[j] >= n) return -1;
+        for (int w = 0; w < p; ++w) v[w] = vals[(int64_t)w * count + j];
+        out[j] = dbtree_value(&t, p, n, op, e[j], v);
+    }
+    return 0;
+}
+
+int oracle_dbtree_fold_bf16_samples(const uint16_t *vals, int p, int64_t n, int op, const int64_t *e,
+                                    int64_t count, uint16_t *out) {
+    struct dbtrees t;
+    if (n < 0 || (op != ORACLE_SUM && op != ORACLE_AVG) || dbtrees_make(p, &t)) return -1;
+    float v[64];
+    for (int64_t j = 0; j < count; ++j) {
+        if (e[j] < 0 || e[j] >= n) return -1;
+        for (int w = 0; w < p; ++w) v[w] = oracle_bf16_to_f32(vals[(int64_t)w * count + j]);
+        out[j] = oracle_f32_to_bf16(dbtree_value(&t, p, n, op, e[j], v));
+    }
+    return 0;
+}
+
+/* Literal schedule, in place on p fp32 buffers, the two trees side by side
+ * in synchronous steps.  Reduce: a rank whose children have all delivered
+ * adds their partial sums into its own half (left child's first), and sends
+ * the result to its parent at the next step.  The root divides by p (AVG).
+ * Broadcast: a rank that holds the result copies it to its children at the
+ * next step.  *steps: synchronous steps taken; sent_elems[w]: elements rank
+ * w put on the wire. */
+int oracle_dbtree_schedule_f32(float *const *bufs, int p, int64_t n, int op, int64_t *sent_elems,
+                               int *steps) {
+    struct dbtrees t;
+    if (n < 0 || (op != ORACLE_SUM && op != ORACLE_AVG) || dbtrees_make(p, &t)) return -1;
+    const int64_t h = oracle_dbtree_half(n);
+    const int64_t beg[2] = {0, h}, len[2] = {h, n - h};
+    const size_t slot = (size_t)(h > 0 ? h : 1);
+    float *inbox = (float *)malloc(sizeof(float) * slot * 2 * 2 * (size_t)p); /* [tree][rank][side] */
+    if (!inbox) return -1;
+    int got[2][64][2], ready[2][64], sent[2][64];
+    for (int w = 0; w < p; ++w)
+        if (sent_elems) sent_elems[w] = 0;
+    for (int k = 0; k < 2; ++k)
+        for (int r = 0; r < p; ++r) {
+            got[k][r][0] = got[k][r][1] = 0;
+            ready[k][r] = t.left[k][r] < 0 && t.right[k][r] < 0; /* a leaf's partial is its own value */
+            sent[k][r] = 0;
+        }
+    int nsteps = 0;
+    while (!ready[0][t.root[0]] || !ready[1][t.root[1]]) {
+        for (int k = 0; k < 2; ++k) /* every send of this step, then every receive */
+            for (int r = 0; r < p; ++r) {
+                if (r == t.root[k] || !ready[k][r] || sent[k][r]) continue;
+                int up = t.parent[k][r], side = t.left[k][up] == r ? 0 : 1;
+                float *box = inbox + (((size_t)k * (size_t)p + (size_t)up) * 2 + (size_t)side) * slot;
+                memcpy(box, bufs[r] + beg[k], sizeof(float) * (size_t)len[k]);
+                got[k][up][side] = 1;
+                sent[k][r] = 1;
+                if (sent_elems) sent_elems[r] += len[k];
+            }
+        for (int k = 0; k < 2; ++k)
+            for (int r = 0; r < p; ++r) {
+                if (ready[k][r]) continue;
+                if ((t.left[k][r] >= 0 && !got[k][r][0]) || (t.right[k][r] >= 0 && !got[k][r][1])) continue;
+                for (int side = 0; side < 2; ++side) {
+                    if ((side == 0 ? t.left[k][r] : t.right[k][r]) < 0) continue;
+                    const float *box = inbox + (((size_t)k * (size_t)p + (size_t)r) * 2 + (size_t)side) * slot;
+                    for (int64_t j = 0; j < len[k]; ++j) bufs[r][beg[k] + j] = bufs[r][beg[k] + j] + box[j];
+                }
+                ready[k][r] = 1;
+            }
+        ++nsteps;
+    }
+    free(inbox);
+    for (int k = 0; k < 2; ++k)
+        if (op == ORACLE_AVG)
+            for (int64_t j = 0; j < len[k]; ++j)
+                bufs[t.root[k]][beg[k] + j] = bufs[t.root[k]][beg[k] + j] / (float)p;
+    int have[2][64], pending = 0;
+    for (int k = 0; k < 2; ++k)
+        for (int r = 0; r < p; ++r) {
+            have[k][r] = r == t.root[k];
+            pending += !have[k][r];
+        }
+    while (pending > 0) {
+        int had[2][64];
+        memcpy(had, have, sizeof(had));
+        for (int k = 0; k < 2; ++k)
+            for (int r = 0; r < p; ++r) {
+                if (!had[k][r]) continue;
+                for (int side = 0; side < 2; ++side) {
+                    int c = side == 0 ? t.left[k][r] : t.right[k][r];
+                    if (c < 0 || have[k][c]) continue;
+                    memcpy(bufs[c] + beg[k], bufs[r] + beg[k], sizeof(float) * (size_t)len[k]);
+                    have[k][c] = 1;
+                    --pending;
+                    if (sent_elems) sent_elems[r] += len[k];
+                }
+            }
+        ++nsteps;
+    }
+    if (steps) *steps = nsteps;
+    return 0;
+}
+
+/* ===================================================================== */
 /* Tensor Fusion [H] "Tensor Fusion", steps 1-6                           */
 /* ===================================================================== */
 static int dtype_bytes(int32_t dt) {

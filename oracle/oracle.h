@@ -18,6 +18,11 @@
  *       (stochastic quantization, uniform SQ, Uniform THC / Algorithm 1).
  *  [S]  Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
  *       1, 2, 3", SC'11 -- definition of the Philox4x32 generator.
+ *  [ST] Sanders, Speck, Traff, "Two-tree algorithms for full bandwidth
+ *       broadcast, reduction and scan", Parallel Computing 35 (2009) --
+ *       the two complementary binary trees read into the tutorial's
+ *       double-binary-tree all-reduce ([R], "Design Alternatives &
+ *       Collective Comparison Matrix: Ring vs. Tree vs. NVLS").
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math), so
  * every float expression is evaluated as written, one IEEE rounding per op.
@@ -90,6 +95,29 @@ int oracle_bidir_fold_f32(const float *const *x, int p, int64_t n, int op, float
 /* sampled form: vals[w * count + k] = worker w's value at element e[k] */
 int oracle_bidir_fold_f32_samples(const float *vals, int p, int64_t n, int op, const int64_t *e,
                                   int64_t count, float *out);
+
+/* Double binary tree ([R] "Design Alternatives & Collective Comparison
+ * Matrix"; construction [ST]).  Tree 1: the in-order binary tree on labels
+ * 1..p (a run's root is its label with the most trailing zero bits), label l
+ * on rank l - 1; tree 2: the same shape, label l on rank p - l (p even) or
+ * (l - 2) mod p (p odd).  Elements [0, ceil(n/2)) go over tree 1, the rest
+ * over tree 2; a node's partial sum is (own + left child's) + right child's
+ * in fp32; the root's sum (/ p for AVG) is broadcast.
+ * oracle_dbtree_build fills parent/left/right[rank] (-1: none) for tree 0 or
+ * 1 and returns the root rank (-1: bad arguments). */
+int oracle_dbtree_build(int p, int tree, int32_t *parent, int32_t *left, int32_t *right);
+int64_t oracle_dbtree_half(int64_t n);
+/* literal schedule (fp32, in place): reduce up both trees, then broadcast */
+int oracle_dbtree_schedule_f32(float *const *bufs, int p, int64_t n, int op, int64_t *sent_elems,
+                               int *steps);
+/* closed forms; bf16 inputs are widened, summed in fp32, rounded once */
+int oracle_dbtree_fold_f32(const float *const *x, int p, int64_t n, int op, float *out);
+int oracle_dbtree_fold_bf16(const uint16_t *const *x, int p, int64_t n, int op, uint16_t *out);
+/* sampled forms: vals[w * count + k] = worker w's value at element e[k] */
+int oracle_dbtree_fold_f32_samples(const float *vals, int p, int64_t n, int op, const int64_t *e,
+                                   int64_t count, float *out);
+int oracle_dbtree_fold_bf16_samples(const uint16_t *vals, int p, int64_t n, int op, const int64_t *e,
+                                    int64_t count, uint16_t *out);
 
 /* ---------------- Tensor Fusion [H] ---------------- */
 /* Next-fit plan.  dtype[i] is ORACLE_F32 or ORACLE_BF16.  Outputs per tensor:
