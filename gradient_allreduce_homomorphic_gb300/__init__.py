@@ -55,6 +55,8 @@ _SIGNATURES = {
     "gar_ring_allreduce_sim_out": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _pp, _i32, _vp]),
     "gar_ring_allreduce_bidir": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _vp]),
     "gar_ring_allreduce_steps": (C.c_int, [_pp, _i32, _i64, _i32, C.POINTER(_i32), _vp, _vp]),
+    "gar_dbtree_allreduce": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _vp]),
+    "gar_dbtree_parents": (C.c_int, [_i32, _i32, _vp]),
     "gar_thc_words": (_i64, [_i64, _i32]),
     "gar_thc_range": (C.c_int, [_pp, _i32, _i64, _vp, _vp]),
     "gar_thc_encode": (C.c_int, [_vp, _i64, _vp, _i32, _u64, _i32, _vp, _vp]),
@@ -358,6 +360,19 @@ def gar_ring_allreduce_bidir(bufs, op: int = GAR_AVG, stream=None):
     """Bidirectional dual ring (in place): first half clockwise, second half counter-clockwise."""
     t = pointer_table(bufs)
     _call("gar_ring_allreduce_bidir", t.array, len(t), t.numel, _dtype_code(t.first), op, _stream(stream))
+
+
+def gar_dbtree_allreduce(bufs, op: int = GAR_AVG, stream=None):
+    """Double-binary-tree all-reduce (in place): first half over tree 1, the rest over tree 2."""
+    t = pointer_table(bufs)
+    _call("gar_dbtree_allreduce", t.array, len(t), t.numel, _dtype_code(t.first), op, _stream(stream))
+
+
+def gar_dbtree_parents(P: int, tree: int):
+    """Host only: parent rank of every rank in tree 0 or 1 (-1: the root)."""
+    out = np.zeros(P, np.int32)
+    _call("gar_dbtree_parents", P, tree, out.ctypes.data)
+    return out
 
 
 def gar_ring_allreduce_sim_out(bufs, out, op: int = GAR_AVG, stream=None):

@@ -4,7 +4,7 @@
            [--b 4] [--iters 20] [--warmup 3] [--dtype f32|bf16]
 
 Cases: ring (in-place ring all-reduce of P buffers), ring_out (reduce to one
-output), bidir (bidirectional dual ring), fused (plan-driven all-reduce of the 300-tensor ResNet-like model),
+output), bidir (bidirectional dual ring), dbtree (double-binary-tree all-reduce), fused (plan-driven all-reduce of the 300-tensor ResNet-like model),
 fused_range (the same into separate outputs, each buffer's THC range from the same reads), thc_plan
 (THC b-bit of every fusion buffer of that model read straight from the tensors, wire vectors written),
 thc_plan_nmse (the same with the NMSE sums against a reference taken in the pass),
@@ -56,7 +56,7 @@ def main(argv=None):
     def bufs(n, k, dt=tdt, seed=0):
         return [workloads.device_normal(n, 1.0, 77_000 + seed + i, dt, dev) for i in range(k)]
 
-    if a.case in ("ring", "ring_out", "bidir"):
+    if a.case in ("ring", "ring_out", "bidir", "dbtree"):
         x = bufs(N, P)
         if a.case == "ring":
             t = g.pointer_table(x)
@@ -65,6 +65,10 @@ def main(argv=None):
         elif a.case == "bidir":
             t = g.pointer_table(x)
             fn = lambda: g.gar_ring_allreduce_bidir(t)  # noqa: E731
+            nbytes = 2 * P * N * es
+        elif a.case == "dbtree":
+            t = g.pointer_table(x)
+            fn = lambda: g.gar_dbtree_allreduce(t)  # noqa: E731
             nbytes = 2 * P * N * es
         else:
             out = [torch.empty(N, dtype=tdt, device=dev)]

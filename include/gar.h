@@ -27,6 +27,11 @@
  *       Algorithm 1), section 5 (index vectors summed at the PS).
  *   [S] Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3"
  *       (SC'11): Philox4x32-10.
+ *   [ST] Sanders, Speck, Traff, "Two-tree algorithms for full bandwidth
+ *       broadcast, reduction and scan" (Parallel Computing, 2009): the two
+ *       complementary trees of the double-binary-tree all-reduce that [R]
+ *       compares with the ring ("Design Alternatives & Collective
+ *       Comparison Matrix: Ring vs. Tree vs. NVLS").
  *
  * Conventions shared by every call
  *   - Ownership: the caller owns every buffer.  "device" pointers are CUDA
@@ -234,6 +239,28 @@ int gar_ring_allreduce_bidir(void *const *bufs, int32_t P, int64_t N, int32_t dt
  * Errors: GAR_EINVAL, GAR_EDTYPE (bf16), GAR_EALIGN, GAR_ECUDA. */
 int gar_ring_allreduce_steps(void *const *bufs, int32_t P, int64_t N, int32_t op,
                              int32_t *steps, int64_t *sent_elems, gar_stream_t stream);
+
+/* gar_dbtree_allreduce -- the double-binary-tree all-reduce ([R] "Design
+ * Alternatives & Collective Comparison Matrix"; trees of [ST]) as a fold
+ * order, in place: afterwards every bufs[w] holds the result.  Both trees
+ * have the shape of the in-order binary tree on the labels 1..P (a run of
+ * labels is rooted at its label with the most trailing zero bits).  Elements
+ * [0, ceil(N/2)) are reduced over tree 1, label l on rank l - 1; the rest
+ * over tree 2, label l on rank P - l (P even) or (l - 2) mod P (P odd).  A
+ * node's partial sum is its own value plus its left child's partial sum,
+ * then plus its right child's, in fp32; the root's sum (divided by P for
+ * GAR_AVG, round to nearest even) is what every rank receives.  bf16
+ * buffers are widened exactly, folded in fp32 and rounded to bf16 once.
+ *   bufs[P]  host array of distinct device pointers, N elements of `dtype`
+ * Errors: GAR_EINVAL, GAR_EDTYPE, GAR_EALIGN, GAR_ECUDA. */
+int gar_dbtree_allreduce(void *const *bufs, int32_t P, int64_t N, int32_t dtype, int32_t op,
+                         gar_stream_t stream);
+
+/* gar_dbtree_parents -- host only: parent[w] = the parent rank of rank w in
+ * tree 0 or 1 of gar_dbtree_allreduce, -1 for the root.
+ *   parent  host, out: P entries
+ * Errors: GAR_EINVAL. */
+int gar_dbtree_parents(int32_t P, int32_t tree, int32_t *parent);
 
 /* ===================================================================== */
 /* Uniform THC [T] section 4 (Algorithm 1) and section 5                 */

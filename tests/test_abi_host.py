@@ -92,6 +92,24 @@ def test_status_codes_without_launch(gar):
     assert lib.gar_nmse(C.c_void_p(0x1000), C.c_void_p(0x2000), 1000, C.c_void_p(0x3000), C.c_void_p(0x4000), 8,
                         null) == gar.GAR_EINVAL
     assert lib.gar_fusion_plan(None, None, -1, 100, 16, None, None, None) == gar.GAR_EINVAL
+    assert lib.gar_dbtree_allreduce(ptrs, 0, 10, 0, 1, null) == gar.GAR_EINVAL
+    assert lib.gar_dbtree_allreduce(ptrs, 65, 10, 0, 1, null) == gar.GAR_EINVAL
+    assert lib.gar_dbtree_allreduce(ptrs, 2, 10, 7, 1, null) == gar.GAR_EDTYPE
+    assert lib.gar_dbtree_allreduce(ptrs, 2, 10, 0, 9, null) == gar.GAR_EINVAL
+    assert lib.gar_dbtree_allreduce(same, 2, 10, 0, 1, null) == gar.GAR_EINVAL
+    assert lib.gar_dbtree_allreduce(odd, 2, 10, 0, 1, null) == gar.GAR_EALIGN
+    assert lib.gar_dbtree_allreduce(None, 2, 0, 0, 1, null) == gar.GAR_OK  # N = 0: nothing touched
+    assert lib.gar_dbtree_parents(0, 0, C.c_void_p(0x1000)) == gar.GAR_EINVAL
+    assert lib.gar_dbtree_parents(4, 2, C.c_void_p(0x1000)) == gar.GAR_EINVAL
+
+
+@pytest.mark.parametrize("tree", [0, 1])
+def test_dbtree_parents_match_oracle(gar, tree):
+    """The library's trees (parent links from bit arithmetic on the labels)
+    against the oracle's (recursive split of the label run)."""
+    for P in range(1, 65):
+        _, par, _, _ = oracle.dbtree_build(P, tree)
+        np.testing.assert_array_equal(gar.gar_dbtree_parents(P, tree), par, err_msg=f"P={P} tree={tree}")
 
 
 def test_thc_words(gar):
