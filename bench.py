@@ -838,17 +838,26 @@ def run_configs(args):
     cfg = workloads.CONFIG_IDS["large_bf16"]
     x = [workloads.device_normal(N, 1e-2, 1000 * cfg + w, torch.bfloat16, dev) for w in range(P)]
     tx = g.pointer_table(x)
-    ms = _median_ms(torch, lambda: g.gar_ring_allreduce_sim(tx), max(3, it // 4))
+    reps = max(3, it // 4)
+    ms = _median_ms(torch, lambda: g.gar_ring_allreduce_sim(tx), reps)
+    bidir_ms = _median_ms(torch, lambda: g.gar_ring_allreduce_bidir(tx), reps)
+    tree_ms = _median_ms(torch, lambda: g.gar_dbtree_allreduce(tx), reps)
+    ab = 2 * P * N * 2  # every input read, every buffer written
     line = {"config": "large_bf16: P=16, N=2^28 bf16 N(0, 1e-2) per worker (8 GiB); ring average in place, "
-                      "fp32 accumulation in ring order, bf16 out",
+                      "fp32 accumulation in ring order, bf16 out; the bidirectional ring and the double binary "
+                      "tree (other fold orders) on the same buffers",
             "l2": "inputs (8 GiB) larger than L2",
-            "gpu": {"ring": _gpu_line("gar_ring_allreduce_sim (bf16)", ms, 2 * P * N * 2, P * N * 2, P * N, peak)}}
+            "gpu": {"ring": _gpu_line("gar_ring_allreduce_sim (bf16)", ms, ab, P * N * 2, P * N, peak),
+                    "bidir": _gpu_line("gar_ring_allreduce_bidir (bf16)", bidir_ms, ab, P * N * 2, P * N, peak),
+                    "dbtree": _gpu_line("gar_dbtree_allreduce (bf16)", tree_ms, ab, P * N * 2, P * N, peak)}}
     if oracle is not None:
         n = 1 << 18
         hx = [workloads.normal_f32(n, 1e-2, cfg, w) for w in range(P)]
         hb = [(a.view(np.uint32) >> 16).astype(np.uint16) for a in hx]  # bf16 bits (truncated): timing input only
         t = _cpu_time(lambda: oracle.ring_fold(hb))
-        line["oracle"] = {"sample": "P=16 x 2^18", "cores": cores, "ring_gbs": round(P * n * 2 / t / 1e9, 4)}
+        t_tree = _cpu_time(lambda: oracle.dbtree_fold(hb))
+        line["oracle"] = {"sample": "P=16 x 2^18", "cores": cores, "ring_gbs": round(P * n * 2 / t / 1e9, 4),
+                          "dbtree_gbs": round(P * n * 2 / t_tree / 1e9, 4)}
     out.append(line)
     del x
     torch.cuda.empty_cache()
