@@ -460,7 +460,13 @@ def run_ours(args, rank, world, dist):
         sevs = [{s: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for s in st.stages}
                 for _ in range(args.steps)]
         torch.cuda.synchronize()
+        # the stage events time the GPU only if the launches are already
+        # queued when it gets there: hold the stream with a spin (outside
+        # every stage's events) while the host queues the next steps
+        hold = int(0.015 * 2.07e9)  # about 15 ms of SM cycles
         for i in range(args.steps):
+            if i % 10 == 0:
+                torch.cuda._sleep(hold)
             st.run(20_003 + i, sevs[i])
         torch.cuda.synchronize()
         serial_stage_ms = {s: float(np.mean([sevs[i][s][0].elapsed_time(sevs[i][s][1]) for i in range(args.steps)]))

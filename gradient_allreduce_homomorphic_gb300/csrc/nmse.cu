@@ -1,6 +1,7 @@
 // nmse.cu -- NMSE(x, x_hat) = ||x - x_hat||^2 / ||x||^2 ([T] section 2).
 //
-// Two launches, deterministic: (1) each CTA folds its grid-stride slice into
+// Two launches, deterministic on a given GPU (the grid is one wave of it):
+// (1) each CTA folds its grid-stride slice into
 // one (sum (x - x_hat)^2, sum x^2) pair of doubles in the caller's
 // workspace; (2) one CTA adds the pairs in a fixed order and divides.
 // Per-element terms are formed in fp32 (sixteen at a time, summed pairwise)
@@ -8,6 +9,7 @@
 // of fp32, and the few fp32 roundings per term (at most 2 + 4 on the way to
 // the fp64 sum, about 4e-7 relative) keep the result within 2e-6 of an
 // all-fp64 sum.
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -106,6 +108,33 @@ nmse_partial_kernel(const float *__restrict__ x, const float *__restrict__ xh, i
     }
 }
 
+// Grid of the partial kernel: one wave of the CTAs that fit on the GPU at once
+// (a whole number per SM, so that every SM gets the same share of the
+// grid-stride loop), never more than the workspace bound nmse_blocks(N).
+// Cached per device.
+int nmse_grid(int64_t N) {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    int wave = kMaxBlocks;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+        wave = cached[dev].load(std::memory_order_relaxed);
+        if (wave == 0) {
+            int per_sm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nmse_partial_kernel, kThreads, 0) !=
+                    cudaSuccess ||
+                per_sm < 1)
+                per_sm = 1;
+            const int sms = sm_count();
+            const int fit = kMaxBlocks / sms;  // whole CTAs per SM within the bound
+            wave = sms * (per_sm < fit ? per_sm : (fit > 0 ? fit : 1));
+            if (wave > kMaxBlocks) wave = kMaxBlocks;
+            cached[dev].store(wave, std::memory_order_relaxed);
+        }
+    }
+    const int cap = nmse_blocks(N);
+    return cap < wave ? cap : wave;
+}
+
 __global__ void __launch_bounds__(kThreads) nmse_final_kernel(const double *ws, int nblocks, double *out) {
     double num = 0.0, den = 0.0;
     for (int i = threadIdx.x; i < nblocks; i += kThreads) {
@@ -160,7 +189,7 @@ extern "C" int gar_nmse(const float *x, const float *x_hat, int64_t N, double *d
     if (!aligned(d_workspace, 8) || !aligned(d_out, 8)) return fail(GAR_EALIGN, "workspace or d_out not 8-byte aligned");
     if ((x && !aligned(x, 4)) || (x_hat && !aligned(x_hat, 4))) return fail(GAR_EALIGN, "x or x_hat not 4-byte aligned");
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    const int g = nmse_blocks(N);
+    const int g = nmse_grid(N);
     const int vec = aligned(x, 16) && aligned(x_hat, 16);
     double *ws = static_cast<double *>(d_workspace);
     nmse_partial_kernel<<<g, kThreads, 0, stream>>>(x, x_hat, N, vec, ws);
@@ -179,7 +208,7 @@ extern "C" int gar_nmse_sums(const float *x, const float *x_hat, int64_t N, doub
     if (!aligned(d_workspace, 8) || !aligned(d_pair, 8)) return fail(GAR_EALIGN, "workspace or d_pair not 8-byte aligned");
     if ((x && !aligned(x, 4)) || (x_hat && !aligned(x_hat, 4))) return fail(GAR_EALIGN, "x or x_hat not 4-byte aligned");
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    const int g = nmse_blocks(N);
+    const int g = nmse_grid(N);
     const int vec = aligned(x, 16) && aligned(x_hat, 16);
     double *ws = static_cast<double *>(d_workspace);
     nmse_partial_kernel<<<g, kThreads, 0, stream>>>(x, x_hat, N, vec, ws);
@@ -241,8 +270,8 @@ int static_scratch(double **out) {
 extern "C" int gar_nmse_noalloc(const float *x, const float *x_hat, int64_t N, double *d_out, gar_stream_t stream_) {
     if (N < 0 || !d_out) return fail(GAR_EINVAL, "N < 0 or d_out is NULL");
     if (N > 0 && (!x || !x_hat)) return fail(GAR_EINVAL, "x or x_hat is NULL");
-    const int g = nmse_blocks(N);
-    if (g > kStaticPairs)  // cannot happen while nmse_blocks caps the grid at kMaxBlocks
+    const int g = nmse_grid(N);
+    if (g > kStaticPairs)  // cannot happen while nmse_grid caps the grid at kMaxBlocks
         return fail(GAR_EINVAL, "N=%lld needs %d partial sums, the static scratch holds %d",
                     static_cast<long long>(N), g, kStaticPairs);
     if (!aligned(d_out, 8)) return fail(GAR_EALIGN, "d_out not 8-byte aligned");

@@ -498,8 +498,9 @@ size_t gar_nmse_workspace_bytes(int64_t N);
 
 /* gar_nmse -- *d_out (device, one double) = sum (x - x_hat)^2 / sum x^2,
  * NaN when sum x^2 = 0.  Per-element terms are formed in fp32 and summed in
- * fp64 in a fixed order (deterministic; within 2e-6 relative of an all-fp64
- * sum).  x, x_hat: device, N fp32.  d_workspace: device, at least
+ * fp64 in a fixed order (deterministic on a given GPU model: the order
+ * follows the grid, one wave of the device's SMs; within 2e-6 relative of
+ * an all-fp64 sum).  x, x_hat: device, N fp32.  d_workspace: device, at least
  * gar_nmse_workspace_bytes(N) bytes, 8-byte aligned, caller-owned, not
  * shared with a concurrent call.
  * Errors: GAR_EINVAL (null, N < 0, workspace too small), GAR_EALIGN,
