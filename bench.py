@@ -785,6 +785,7 @@ def _median_ms(torch, fn, iters, flush=None):
     for _ in range(iters):
         if flush is not None:
             flush()
+        torch.cuda._sleep(100_000)  # the call is queued before the start event: the events time the GPU
         s.record()
         fn()
         e.record()
@@ -824,7 +825,13 @@ def run_configs(args):
     peak, _ = _peaks()
     it = args.config_iters
     l2 = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)  # 256 MB > the 129 MB L2
-    flush = l2.zero_
+    l2_clean = torch.ones_like(l2)
+
+    def flush():
+        # 256 MB written (the inputs leave L2), then 256 MB read, so that the
+        # dirty lines are written back before the timed call starts
+        l2.zero_()
+        l2_clean.sum()
     oracle = None
     if not args.no_cpu_baseline:
         import oracle
@@ -853,7 +860,7 @@ def run_configs(args):
 
     thc_ms = _median_ms(torch, thc, it, flush)
     line = {"config": "partition_4mb: P=4, N=2^20 fp32 N(0,1); ring average + THC b=4 (range, fused)",
-            "l2": "flushed before each call (256 MB written)",
+            "l2": "flushed before each call (256 MB written, then 256 MB read)",
             "gpu": {"ring": _gpu_line("gar_ring_allreduce_sim, in place", ring_ms, 2 * P * N * 4, P * N * 4,
                                       P * N, peak),
                     "thc": _gpu_line("gar_thc_range + gar_thc_allreduce_fused (wire vectors written)", thc_ms,

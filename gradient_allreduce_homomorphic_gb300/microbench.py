@@ -45,6 +45,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--dtype", default="f32")
     ap.add_argument("--g", type=int, default=0, help="granularity for the nuhc cases")
+    ap.add_argument("--flush", action="store_true",
+                    help="write then read 256 MB (more than L2) before every timed call")
     a = ap.parse_args(argv)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -200,10 +202,21 @@ def main(argv=None):
     for _ in range(a.warmup):
         fn()
     torch.cuda.synchronize()
+    flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev) if a.flush else None
+    clean = torch.ones((256 << 20) // 4, dtype=torch.float32, device=dev) if a.flush else None
     launches0 = g.gar_launch_count()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     times = []
     for _ in range(a.iters):
+        if flush is not None:
+            # 256 MB written (nothing of the inputs left in L2), then 256 MB read:
+            # the dirty lines are written back before the timed call, which
+            # starts with an L2 of clean lines
+            flush.zero_()
+            clean.sum()
+        # hold the stream briefly so that the call is queued before the start
+        # event: the events then time the GPU, not the host's enqueue
+        torch.cuda._sleep(100_000)
         s.record()
         fn()
         e.record()
