@@ -364,7 +364,8 @@ __global__ void __launch_bounds__(kThreads) thc_nmse_pair_kernel(const double *w
 // pieces, and a buffer at most as many launches as tensors.
 int64_t plan_nmse_pairs_bound(const int64_t *buf_numel, int32_t n_buffers, int32_t count, int32_t b) {
     int64_t tiles = 0;
-    for (int i = 0; i < n_buffers; ++i) tiles += ceil_div(gar_thc_words(buf_numel[i] > 0 ? buf_numel[i] : 0, b), kPlanTileWords);
+    for (int i = 0; i < n_buffers; ++i)
+        tiles += ceil_div(thc_units(gar_thc_words(buf_numel[i] > 0 ? buf_numel[i] : 0, b), b), kPlanTileWords);
     return tiles + 5 * static_cast<int64_t>(count) + 3 * static_cast<int64_t>(n_buffers) + 1;
 }
 
@@ -523,7 +524,7 @@ static int thc_fused_entry(const float *const *x, int32_t P, uint64_t arrived, i
     p.mM = d_mM;
     p.avg = avg;
     p.N = N;
-    p.nwords = gar_thc_words(N, b);
+    p.nunits = thc_units(gar_thc_words(N, b), b);
     p.P = p_eff;
     p.L = static_cast<float>((1 << b) - 1);
     p.fp = static_cast<float>(p_eff);
@@ -654,8 +655,8 @@ static int thc_plan_impl(const float *const *src, int32_t P, const gar_seg *segs
     p->L = static_cast<float>((1 << b) - 1);
     p->fp = static_cast<float>(P);
     for (int w = 0; w < P; ++w) p->wid[w] = w;
-    const int E = 32 / b;
-    const int cap = std::min(kPlanSegs, kPlanPtrs / P);  // >= 32 >= E: a word meets at most E tensors
+    const int E = unit_elems_of(b);                     // elements of a unit of work
+    const int cap = std::min(kPlanSegs, kPlanPtrs / P);  // >= 32 >= E: a unit meets at most E tensors
     bool vec[kPlanSegs];
     int rc = GAR_OK;
     int64_t used = 0;  // NMSE pairs written so far (one per CTA)
@@ -675,7 +676,7 @@ static int thc_plan_impl(const float *const *src, int32_t P, const gar_seg *segs
             }
         }
         if (rc) break;
-        const int64_t nwords = gar_thc_words(p->N, b);
+        const int64_t nwords = thc_units(gar_thc_words(p->N, b), b);  // in units
         // launches over consecutive word ranges; each one's table holds every
         // tensor that meets its words (those before `lo` end before them, those
         // from `hi` on begin after them)
@@ -687,7 +688,7 @@ static int thc_plan_impl(const float *const *src, int32_t P, const gar_seg *segs
             const int hi = std::min(lo + cap, n);
             const int64_t w1 = hi == n ? nwords : segs[mem[hi]].offset / E;
             if (w1 <= w0) {
-                rc = fail(GAR_EINVAL, "more than %d tensors meet one word of buffer %d", cap, bf);
+                rc = fail(GAR_EINVAL, "more than %d tensors meet one unit of buffer %d", cap, bf);
                 break;
             }
             p->nseg = hi - lo;

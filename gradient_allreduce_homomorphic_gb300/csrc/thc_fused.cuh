@@ -11,6 +11,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -19,15 +20,29 @@ namespace thc {
 
 constexpr int kThreads = 256;
 
+// The fused kernels' unit of work: E elements whose b-bit indices fill one
+// store -- a whole 32-bit wire word for b >= 4 (E = 32 / b), 16 bits for
+// b = 2 and 8 bits for b = 1 (E = 8, the registers of a b = 4 word).  The
+// wire vectors keep their layout: unit u is bits [j E b, (j + 1) E b) of
+// word u / (32 / (E b)), j = u mod (32 / (E b)), written as its own 8-, 16-
+// or 32-bit slice (little endian); adjacent threads write the slices of one
+// word.
+template <int B>
+constexpr int unit_elems() {
+    return B >= 4 ? 32 / B : 8;
+}
+template <int B>
+using UnitT = std::conditional_t<(B >= 4), uint32_t, std::conditional_t<(B == 2), uint16_t, uint8_t>>;
+inline int unit_elems_of(int b) { return b >= 4 ? 32 / b : 8; }
+// Units of the wire words of N elements (the last word's spare units too).
+inline int64_t thc_units(int64_t words, int b) { return words * (32 / (unit_elems_of(b) * b)); }
+
 // Resident CTAs per SM the fused kernels are compiled for (caps registers at
-// 65536 / (256 * n)): four for b >= 4, fewer where a word's registers
-// (E = 32 / b elements, two workers in flight) need more.
-#ifndef GAR_THC_MIN_BLOCKS
-#define GAR_THC_MIN_BLOCKS 4
-#endif
+// 65536 / (256 * n)).
+constexpr int kFusedMinBlocks = 4;
 template <int B>
 constexpr int fused_min_blocks() {
-    return B >= 4 ? GAR_THC_MIN_BLOCKS : (B == 2 ? 3 : 2);
+    return kFusedMinBlocks;
 }
 
 __device__ __forceinline__ float range_scale(float m, float M, float L) {
@@ -104,10 +119,10 @@ __device__ __forceinline__ uint4 philox_block(int64_t q, int worker, const Philo
 // Sum over the 32/B fields of a packed word of (0x4B000000 << field shift),
 // mod 2^32: packing the biased indices with plain shifted adds and removing
 // this once leaves the exact word (the fields never overlap).
-template <int B>
+template <int B, int E = 32 / B>
 __host__ __device__ constexpr uint32_t pack_bias() {
     uint32_t s = 0;
-    for (int i = 0; i < 32 / B; ++i) s += 0x4B000000u << (i * B);
+    for (int i = 0; i < E; ++i) s += 0x4B000000u << (i * B);
     return s;
 }
 
@@ -135,7 +150,7 @@ struct FusedParams {
     const float *mM;
     float *avg;
     int64_t N;
-    int64_t nwords;
+    int64_t nunits;  // units of work: the wire words' units (see unit_elems)
     int32_t P;    // contributing workers (the decode divides by this)
     int32_t vec;  // inputs and avg 16-byte aligned
     float L;
@@ -161,8 +176,8 @@ __device__ __forceinline__ Coder make_coder(const Prm &p) {
     return c;
 }
 
-// One worker's contribution to a word of E = 4G elements: Philox draws,
-// indices added to the running sums s, the packed word stored if wanted.
+// One worker's contribution to a unit of E = 4G elements: Philox draws,
+// indices added to the running sums s, the packed slice stored if wanted.
 template <int B, bool kPacked, int G, class Prm>
 __device__ __forceinline__ void fused_one_worker(const float4 (&v)[G], uint32_t (&s)[4 * G], int64_t e0, int64_t w,
                                                  int wk, const Prm &p, const Coder &c) {
@@ -171,15 +186,8 @@ __device__ __forceinline__ void fused_one_worker(const float4 (&v)[G], uint32_t 
     for (int g = 0; g < G; ++g) {
         const uint4 r = philox_block((e0 >> 2) + g, p.wid[wk], p.keys);
         uint32_t a0, a1, a2, a3;
-        if constexpr (B == 1) {  // 32 elements a word: the paired form would spill registers
-            a0 = index_biased(v[g].x, c.m, c.sc, p.L, r.x);
-            a1 = index_biased(v[g].y, c.m, c.sc, p.L, r.y);
-            a2 = index_biased(v[g].z, c.m, c.sc, p.L, r.z);
-            a3 = index_biased(v[g].w, c.m, c.sc, p.L, r.w);
-        } else {
-            index_biased2(v[g].x, v[g].y, c.m2, c.sc2, p.L, r.x, r.y, a0, a1);
-            index_biased2(v[g].z, v[g].w, c.m2, c.sc2, p.L, r.z, r.w, a2, a3);
-        }
+        index_biased2(v[g].x, v[g].y, c.m2, c.sc2, p.L, r.x, r.y, a0, a1);
+        index_biased2(v[g].z, v[g].w, c.m2, c.sc2, p.L, r.z, r.w, a2, a3);
         s[4 * g] += a0;
         s[4 * g + 1] += a1;
         s[4 * g + 2] += a2;
@@ -188,7 +196,8 @@ __device__ __forceinline__ void fused_one_worker(const float4 (&v)[G], uint32_t 
             word += (a0 << (4 * g * B)) + (a1 << ((4 * g + 1) * B)) + (a2 << ((4 * g + 2) * B)) +
                     (a3 << ((4 * g + 3) * B));
     }
-    if (kPacked) __stcs(p.packed[wk] + w, word - pack_bias<B>());
+    if (kPacked)
+        __stcs(reinterpret_cast<UnitT<B> *>(p.packed[wk]) + w, static_cast<UnitT<B>>(word - pack_bias<B, 4 * G>()));
 }
 
 template <int G>
@@ -197,18 +206,16 @@ __device__ __forceinline__ void load_group(float4 (&v)[G], const float *x) {
     for (int g = 0; g < G; ++g) v[g] = __ldcs(reinterpret_cast<const float4 *>(x) + g);
 }
 
-// Word w (elements w*E .. w*E + E - 1) with every operand 16-byte aligned:
+// Unit w (elements w*E .. w*E + E - 1) with every operand 16-byte aligned:
 // worker slot wk's E inputs start at xs[wk] + xoff, the E averages go to avg.
 // Two register buffers, the worker loop unrolled by two: one worker's loads
 // are in flight while the other is quantized, with no copies.
 // How far the worker loop (two workers an iteration) is unrolled: fully for
-// a fixed count of up to 16 workers, partly for 64; less where a word holds
-// 16 or 32 elements and the registers would spill.
+// a fixed count of up to 16 workers, partly for 64.
 template <int B, int kP>
 constexpr int fused_unroll() {
     if (kP == 0) return 1;
-    if (B >= 4) return kP <= 16 ? 64 : 8;
-    return kP <= 8 ? 64 : 2;
+    return kP <= 16 ? 64 : 8;
 }
 
 // A thread's running sums for NMSE ([T] section 2) of the decoded average
@@ -232,8 +239,8 @@ template <int B, bool kPacked, int kP = 0, bool kNmse = false, class Prm>
 __device__ __forceinline__ void fused_word_vec(const Prm &p, const Coder &c, const float *const *xs, int64_t xoff,
                                                float *avg, int64_t w, const float *ref = nullptr,
                                                NmseAcc *acc = nullptr) {
-    constexpr int E = 32 / B;
-    constexpr int G = E / 4;  // float4 groups (and Philox blocks) per word
+    constexpr int E = unit_elems<B>();
+    constexpr int G = E / 4;  // float4 groups (and Philox blocks) per unit
     const int P = kP > 0 ? kP : p.P;
     const int64_t e0 = w * E;
     uint32_t s[E];
@@ -275,13 +282,20 @@ __device__ __forceinline__ void fused_word_vec(const Prm &p, const Coder &c, con
     }
 }
 
+// One CTA per tile of 2 * kThreads units (two per thread): the block
+// scheduler hands tiles to the SMs as they free up, which left fewer SMs idle
+// than a resident grid striding over the units (P=16, b=4, 2^24: 0.265 ->
+// 0.232 ms).
 template <int B, bool kPacked, int kP>
 __global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_kernel(const __grid_constant__ FusedParams p) {
-    constexpr int E = 32 / B;
+    constexpr int E = unit_elems<B>();
     constexpr int G = E / 4;
     const Coder c = make_coder(p);
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < p.nwords; w += stride) {
+    const int64_t w_first = static_cast<int64_t>(blockIdx.x) * (2 * kThreads) + threadIdx.x;
+#pragma unroll 1
+    for (int u = 0; u < 2; ++u) {
+        const int64_t w = w_first + u * kThreads;
+        if (w >= p.nunits) break;
         const int64_t e0 = w * E;
         if (p.vec && e0 + E <= p.N) {
             fused_word_vec<B, kPacked, kP>(p, c, p.x, e0, p.avg + e0, w);
@@ -301,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_ker
                         word |= (a - 0x4B000000u) << ((4 * g + i) * B);
                     }
                 }
-                if (kPacked) p.packed[wk][w] = word;
+                if (kPacked) reinterpret_cast<UnitT<B> *>(p.packed[wk])[w] = static_cast<UnitT<B>>(word);
             }
             for (int i = 0; i < E && e0 + i < p.N; ++i) {
                 // elements never visited above kept s = 0; only in-range ones are stored
@@ -377,11 +391,11 @@ __device__ __forceinline__ int plan_find(const ThcPlanParams &p, int64_t e) {
     return e < p.seg[lo].end ? lo : -1;
 }
 
-// The buffer's ragged last word (e0 + E > N), element by element: the
+// The buffer's ragged last unit (e0 + E > N), element by element: the
 // missing elements pack as zero bits and get no output.
 template <int B, bool kPacked, bool kNmse>
 __device__ __noinline__ void plan_word_ragged(const ThcPlanParams &p, const Coder &c, int64_t w, NmseAcc &acc) {
-    constexpr int E = 32 / B;
+    constexpr int E = unit_elems<B>();
     constexpr int G = E / 4;
     const int64_t e0 = w * E;
     uint32_t s[E];
@@ -401,7 +415,7 @@ __device__ __noinline__ void plan_word_ragged(const ThcPlanParams &p, const Code
                 word |= (a - 0x4B000000u) << ((4 * g + i) * B);
             }
         }
-        if (kPacked) p.packed[wk][w] = word;
+        if (kPacked) reinterpret_cast<UnitT<B> *>(p.packed[wk])[w] = static_cast<UnitT<B>>(word);
     }
     for (int i = 0; i < E && e0 + i < p.N; ++i) {
         const int64_t e = e0 + i;
@@ -426,7 +440,7 @@ __device__ __noinline__ void plan_word_ragged(const ThcPlanParams &p, const Code
 template <int B, bool kPacked, bool kNmse>
 __device__ __noinline__ void plan_word_gather(const ThcPlanParams &p, const Coder &c, int64_t w, int seg,
                                               NmseAcc &acc) {
-    constexpr int E = 32 / B;
+    constexpr int E = unit_elems<B>();
     constexpr int G = E / 4;
     const int64_t e0 = w * E;
     int ks[E];
@@ -467,7 +481,7 @@ __device__ __noinline__ void plan_word_gather(const ThcPlanParams &p, const Code
 // p.nmse_ws[2 * blockIdx.x], p.nmse_ws[2 * blockIdx.x + 1].
 template <int B, bool kPacked, int kP, bool kNmse>
 __global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_plan_kernel(const __grid_constant__ ThcPlanParams p) {
-    constexpr int E = 32 / B;
+    constexpr int E = unit_elems<B>();
     const Coder c = make_coder(p);
     NmseAcc acc;
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
@@ -534,17 +548,18 @@ int grid_for(K kernel, int64_t work_items) {
 }
 
 
-// Launchers: kernel grid, dispatch on b and on whether wire vectors are
-// written.  kP = 0: any worker count; kP > 0: p.P == kP.
+// Launchers: kernel grid (one CTA per tile of 2 * kThreads words), dispatch
+// on b and on whether wire vectors are written.  kP = 0: any worker count;
+// kP > 0: p.P == kP.
 template <int kP>
 int launch_fused(const FusedParams &p, int b, bool packed, cudaStream_t stream) {
 #define GAR_FUSED_CASE(BB)                                                                                \
     case BB:                                                                                              \
         if (packed)                                                                                       \
-            thc_fused_kernel<BB, true, kP><<<grid_for(thc_fused_kernel<BB, true, kP>, p.nwords), kThreads, 0, \
+            thc_fused_kernel<BB, true, kP><<<static_cast<unsigned>(ceil_div(p.nunits, 2 * kThreads)), kThreads, 0, \
                                              stream>>>(p);                                                \
         else                                                                                              \
-            thc_fused_kernel<BB, false, kP><<<grid_for(thc_fused_kernel<BB, false, kP>, p.nwords), kThreads, \
+            thc_fused_kernel<BB, false, kP><<<static_cast<unsigned>(ceil_div(p.nunits, 2 * kThreads)), kThreads, \
                                               0, stream>>>(p);                                            \
         break;
     switch (b) {

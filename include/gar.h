@@ -355,7 +355,8 @@ int gar_thc_allreduce_fused_masked(const float *const *x, int32_t P, uint64_t ar
  *                    (gar_thc_words(buf_numel[b], b) words)
  * Only buffers that at least one of the tensors belongs to are processed.
  * Errors: GAR_EINVAL (bad b/P/plan, NULL, more than min(128, 2048 / P)
- * tensors meeting one packed word), GAR_EDTYPE (bf16), GAR_EOVERFLOW,
+ * tensors meeting one packed word -- for b <= 2 one 8-element part of a
+ * word), GAR_EDTYPE (bf16), GAR_EOVERFLOW,
  * GAR_EALIGN, GAR_ECUDA. */
 int gar_thc_allreduce_fused_plan(const float *const *src, int32_t P, const gar_seg *segs,
                                  const int32_t *dtype, int32_t count, const int64_t *buf_numel,
