@@ -45,6 +45,7 @@ _SIGNATURES = {
     "gar_version": (C.c_int, []),
     "gar_last_error": (C.c_char_p, []),
     "gar_launch_count": (C.c_uint64, []),
+    "gar_sync_status": (C.c_int, [_vp, _vp, _i32]),
     "gar_fusion_plan": (C.c_int, [_vp, _vp, _i32, _i64, _i32, _vp, C.POINTER(_i32), _vp]),
     "gar_fusion_pack": (C.c_int, [_pp, _vp, _vp, _i32, _i32, _vp, _i64, _vp]),
     "gar_fusion_unpack": (C.c_int, [_vp, _vp, _vp, _i32, _i32, _pp, _vp]),
@@ -348,6 +349,17 @@ def gar_fused_allreduce_range(src, dst, plan: FusionPlan, d_mM, op: int = GAR_AV
     s, d = tables if tables is not None else fused_pointer_tables(src, dst)
     _call("gar_fused_allreduce_range", s.array, d.array, P, C.addressof(plan.segs), plan.dtype.ctypes.data,
           plan.count, plan.buf_numel.ctypes.data, plan.n_buffers, op, _dev(d_mM), _stream(stream))
+
+
+GAR_STATUS_NONFINITE = 1
+
+
+def gar_sync_status(stream=None, clear: bool = True) -> int:
+    """Wait for `stream`, then return the device status word (GAR_STATUS_*
+    bits: conditions the kernels found on the device), clearing it if asked."""
+    out = C.c_uint32(0)
+    _call("gar_sync_status", _stream(stream), C.byref(out), 1 if clear else 0)
+    return int(out.value)
 
 
 # ----------------------------------------------------------- ring all-reduce

@@ -2,6 +2,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -39,7 +40,37 @@ int sm_count() {
     return cached[dev];
 }
 
+namespace {
+__device__ unsigned int g_device_status;  // per device: GAR_STATUS_* bits, zero at load
+std::mutex g_status_mutex;
+unsigned int *g_status_addr[64] = {};
+}  // namespace
+
+unsigned int *device_status() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_status_mutex);
+    if (!g_status_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        g_status_addr[dev] = static_cast<unsigned int *>(p);
+    }
+    return g_status_addr[dev];
+}
+
 }  // namespace gar
+
+extern "C" int gar_sync_status(gar_stream_t stream, uint32_t *status, int32_t clear) {
+    if (!status) return gar::fail(GAR_EINVAL, "status is NULL");
+    unsigned int *d = gar::device_status();
+    if (!d) return gar::fail(GAR_ECUDA, "the device status word is not available");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemcpy(status, d, sizeof(unsigned int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && clear) e = cudaMemset(d, 0, sizeof(unsigned int));
+    if (e != cudaSuccess) return gar::fail(GAR_ECUDA, "gar_sync_status: %s", cudaGetErrorString(e));
+    return GAR_OK;
+}
 
 extern "C" int gar_version(void) { return 100; }
 

@@ -20,12 +20,26 @@ int fail(int status, const char *fmt, ...);
 int check_launch(const char *what);
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
+// Device address of the library's status word on the current device (bits
+// that kernels set for conditions found on the device, GAR_STATUS_*), or
+// NULL if it cannot be had; looked up once per device.
+unsigned int *device_status();
 
 inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 inline int elem_bytes(int32_t dtype) { return dtype == GAR_F32 ? 4 : (dtype == GAR_BF16 ? 2 : -1); }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ---------------------------------------------------------------- device
+// Non-finite check at one FMA per value: chk = fma(v, 0, chk) stays 0 for
+// finite values and becomes NaN for good once a NaN or an infinity is seen.
+__device__ __forceinline__ float nonfinite_acc(float chk, float v) { return __fmaf_rn(v, 0.0f, chk); }
+// Raise GAR_STATUS_NONFINITE if any lane of the warp saw a non-finite value
+// (call with every lane of the warp; one atomic per warp at most).
+__device__ __forceinline__ void flag_nonfinite_warp(unsigned int *status, float chk) {
+    if (__any_sync(0xFFFFFFFFu, chk != chk) && (threadIdx.x & 31) == 0 && status)
+        atomicOr(status, static_cast<unsigned int>(GAR_STATUS_NONFINITE));
+}
+
 // 16-byte loads and stores with the streaming ("evict first") cache hint:
 // every byte of the hot path is touched once per pass.
 __device__ __forceinline__ uint4 ld16(const void *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }

@@ -173,6 +173,7 @@ struct PackAllParams {
     int32_t pad0;
     int32_t pad1;
     float *mM;  // [n_buffers][2] or NULL
+    unsigned int *status;  // with a range: GAR_STATUS_NONFINITE raised here
     int64_t total_tiles;
     int64_t tile_start[kPackRows + 1];
     PackRow row[kPackRows];
@@ -188,17 +189,18 @@ struct PackElem;
 template <>
 struct PackElem<float> {
     static constexpr int kVec = 4;
-    __device__ static void range(const uint4 &r, float &lo, float &hi) {
+    __device__ static void range(const uint4 &r, float &lo, float &hi, float &chk) {
         const float a = __uint_as_float(r.x), b = __uint_as_float(r.y), c = __uint_as_float(r.z),
                     d = __uint_as_float(r.w);
         lo = fminf(lo, fminf(fminf(a, b), fminf(c, d)));
         hi = fmaxf(hi, fmaxf(fmaxf(a, b), fmaxf(c, d)));
+        chk = nonfinite_acc(nonfinite_acc(nonfinite_acc(nonfinite_acc(chk, a), b), c), d);
     }
 };
 template <>
 struct PackElem<uint16_t> {
     static constexpr int kVec = 8;
-    __device__ static void range(const uint4 &, float &, float &) {}
+    __device__ static void range(const uint4 &, float &, float &, float &) {}
 };
 
 __device__ __forceinline__ void atomic_min_f(float *a, float v) {
@@ -240,6 +242,7 @@ __global__ void __launch_bounds__(kThreads) pack_all_kernel(const __grid_constan
         const void *const *src = p.src + static_cast<int64_t>(lo_i) * p.P;
         void *const *dst = p.dst + static_cast<int64_t>(lo_i) * p.P;
         float lo = __int_as_float(0x7F800000), hi = __int_as_float(0xFF800000u);
+        float chk = 0.0f;  // NaN once a non-finite input is seen
         const int64_t nvec = r.vec ? r.numel / V : 0;
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -254,7 +257,7 @@ __global__ void __launch_bounds__(kThreads) pack_all_kernel(const __grid_constan
                     for (int j = 0; j < kPackBatch; ++j) {
                         if (w0 + j < p.P) {
                             st16(static_cast<T *>(dst[w0 + j]) + i * V, v[j]);
-                            if (want_range) PackElem<T>::range(v[j], lo, hi);
+                            if (want_range) PackElem<T>::range(v[j], lo, hi, chk);
                         }
                     }
                 }
@@ -271,6 +274,7 @@ __global__ void __launch_bounds__(kThreads) pack_all_kernel(const __grid_constan
                         if constexpr (sizeof(T) == 4) {
                             lo = fminf(lo, v);
                             hi = fmaxf(hi, v);
+                            chk = nonfinite_acc(chk, v);
                         }
                     }
                 }
@@ -292,11 +296,13 @@ __global__ void __launch_bounds__(kThreads) pack_all_kernel(const __grid_constan
                     if constexpr (sizeof(T) == 4) {
                         lo = fminf(lo, static_cast<float>(v));
                         hi = fmaxf(hi, static_cast<float>(v));
+                        chk = nonfinite_acc(chk, static_cast<float>(v));
                     }
                 }
             }
         }
         if (want_range) {  // uniform branch: one pair of atomics per tile
+            flag_nonfinite_warp(p.status, chk);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
@@ -513,6 +519,7 @@ extern "C" int gar_fusion_pack_all(const void *const *src, int32_t P, const gar_
         std::memset(p, 0, sizeof(PackAllParams));
         p->P = P;
         p->mM = d_mM;
+        p->status = d_mM ? device_status() : nullptr;
         const int es = elem_bytes(pass_dtype);
         auto flush = [&]() -> int {
             if (p->nrows == 0) return GAR_OK;

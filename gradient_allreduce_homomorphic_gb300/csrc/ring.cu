@@ -101,19 +101,23 @@ __device__ __forceinline__ int ring_worker(int c, int k, int ccw, int P) {
 // (fminf / fmaxf: NaN inputs are skipped, as in the packing kernel)
 struct Range {
     float lo, hi;
+    float chk;  // NaN once a non-finite input is seen
     __device__ __forceinline__ Range() {
         lo = __int_as_float(0x7F800000);   // +inf
         hi = __int_as_float(0xFF800000u);  // -inf
+        chk = 0.0f;
     }
     __device__ __forceinline__ void add(float v) {
         lo = fminf(lo, v);
         hi = fmaxf(hi, v);
+        chk = nonfinite_acc(chk, v);
     }
     // two values per instruction: sm_100's three-input min / max (NaN
     // inputs are skipped, as by fminf / fmaxf)
     __device__ __forceinline__ void add2(float a, float b) {
         asm("min.f32 %0, %0, %1, %2;" : "+f"(lo) : "f"(a), "f"(b));
         asm("max.f32 %0, %0, %1, %2;" : "+f"(hi) : "f"(a), "f"(b));
+        chk = nonfinite_acc(nonfinite_acc(chk, a), b);
     }
     template <int V>
     __device__ __forceinline__ void add_vec(const float (&v)[V]) {
@@ -203,8 +207,9 @@ __device__ __forceinline__ void atomic_max_f(float *a, float v) {
 }
 
 // Block-wide min / max of rg merged into range[slot] (one pair of atomics).
-__device__ __forceinline__ void flush_range(Range rg, float *range, int slot) {
+__device__ __forceinline__ void flush_range(Range rg, float *range, int slot, unsigned int *status) {
     __shared__ float s_lo[kThreads / 32], s_hi[kThreads / 32];
+    flag_nonfinite_warp(status, rg.chk);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         rg.lo = fminf(rg.lo, __shfl_xor_sync(0xFFFFFFFFu, rg.lo, o));
@@ -250,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, kRange ? kRangeMinBlocks : 4) ring_f
         }
         const Piece pc = p.piece[lo];
         if (kRange && p.slot[lo] != slot) {
-            if (slot >= 0) flush_range(rg, p.range, slot);
+            if (slot >= 0) flush_range(rg, p.range, slot, p.status);
             rg = Range();
             slot = p.slot[lo];
         }
@@ -287,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, kRange ? kRangeMinBlocks : 4) ring_f
             }
         }
     }
-    if (kRange && slot >= 0) flush_range(rg, p.range, slot);
+    if (kRange && slot >= 0) flush_range(rg, p.range, slot, p.status);
 }
 
 // Range entries of the buffers a call covers start at (+inf, -inf), or at
@@ -532,6 +537,7 @@ int fused_allreduce_impl(const void *const *src, void *const *dst, int32_t P, co
         p->P = P;
         p->n_out = P;
         p->range = pass_dtype == GAR_F32 ? d_mM : nullptr;
+        p->status = p->range ? device_status() : nullptr;
         set_mode(*p, op, P);
         int rows = 0;
         auto flush = [&]() -> int {

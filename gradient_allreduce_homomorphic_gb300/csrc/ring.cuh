@@ -31,6 +31,7 @@ struct FoldParams {
     float inv_p;      // 1/P (exact when P is a power of two)
     float fp;         // P
     float *range;     // [slot][2] min / max of the inputs, or NULL
+    unsigned int *status;  // range launches: GAR_STATUS_NONFINITE raised here
     int64_t total_tiles;
     int64_t tile_start[NPIECE + 1];  // first tile of each piece; [npieces] = total
     Piece piece[NPIECE];

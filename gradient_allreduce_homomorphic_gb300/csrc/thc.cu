@@ -46,6 +46,7 @@ struct RangeParams {
     const float *x[GAR_MAX_WORKERS];
     int64_t N;
     float *mM;
+    unsigned int *status;  // GAR_STATUS_NONFINITE raised here
     int32_t vec;  // all inputs 16-byte aligned
     int32_t pad;
 };
@@ -53,6 +54,7 @@ struct RangeParams {
 __global__ void __launch_bounds__(kThreads) thc_range_kernel(const __grid_constant__ RangeParams p) {
     const float *x = p.x[blockIdx.y];
     float lo = __int_as_float(0x7F800000), hi = __int_as_float(0xFF800000u);
+    float chk = 0.0f;  // NaN once a non-finite input is seen
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     int64_t scalar_from = 0;
@@ -66,11 +68,14 @@ __global__ void __launch_bounds__(kThreads) thc_range_kernel(const __grid_consta
             hi = fmaxf(hi, fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)));
             lo = fminf(lo, fminf(fminf(b.x, b.y), fminf(b.z, b.w)));
             hi = fmaxf(hi, fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w)));
+            chk = nonfinite_acc(nonfinite_acc(nonfinite_acc(nonfinite_acc(chk, a.x), a.y), a.z), a.w);
+            chk = nonfinite_acc(nonfinite_acc(nonfinite_acc(nonfinite_acc(chk, b.x), b.y), b.z), b.w);
         }
         if (i < nv) {
             const float4 a = __ldcs(xv + i);
             lo = fminf(lo, fminf(fminf(a.x, a.y), fminf(a.z, a.w)));
             hi = fmaxf(hi, fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)));
+            chk = nonfinite_acc(nonfinite_acc(nonfinite_acc(nonfinite_acc(chk, a.x), a.y), a.z), a.w);
         }
         scalar_from = nv * 4;
     }
@@ -78,7 +83,9 @@ __global__ void __launch_bounds__(kThreads) thc_range_kernel(const __grid_consta
         const float v = __ldcs(x + k);
         lo = fminf(lo, v);
         hi = fmaxf(hi, v);
+        chk = nonfinite_acc(chk, v);
     }
+    flag_nonfinite_warp(p.status, chk);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
@@ -390,6 +397,7 @@ extern "C" int gar_thc_range(const float *const *x, int32_t P, int64_t N, float 
     std::memset(&p, 0, sizeof(p));
     p.N = N;
     p.mM = d_mM;
+    p.status = device_status();
     p.vec = 1;
     for (int w = 0; w < P; ++w) {
         if (!x[w] && N > 0) return fail(GAR_EINVAL, "input %d is NULL", w);

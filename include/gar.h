@@ -73,6 +73,11 @@ typedef enum {
 } gar_status;
 
 typedef enum { GAR_F32 = 0, GAR_BF16 = 1 } gar_dtype;
+
+/* Bits of the device status word (gar_sync_status). */
+typedef enum {
+    GAR_STATUS_NONFINITE = 1 /* a THC range pass saw a NaN or an infinite input */
+} gar_device_status;
 typedef enum { GAR_SUM = 0, GAR_AVG = 1 } gar_op;
 
 #define GAR_MAX_WORKERS 64
@@ -190,6 +195,18 @@ int gar_fused_allreduce(const void *const *src, void *const *dst, int32_t P,
 int gar_fused_allreduce_range(const void *const *src, void *const *dst, int32_t P, const gar_seg *segs,
                               const int32_t *dtype, int32_t count, const int64_t *buf_numel,
                               int32_t n_buffers, int32_t op, float *d_mM, gar_stream_t stream);
+
+/* gar_sync_status -- waits for `stream`, then *status (host) = the device
+ * status word of the current device: bits that kernels set for conditions
+ * they find on the device.  GAR_STATUS_NONFINITE: a THC range pass
+ * (gar_thc_range, gar_fusion_pack_all or gar_fused_allreduce_range with a
+ * range) saw a NaN or an infinite input; the range skips NaN and takes
+ * infinities in, so the quantization of such a round is meaningless.  The
+ * word is set to 0 when clear != 0.  Kernels queued on other streams may set
+ * bits at any time.  No kernel of this library waits on a flag or a peer, so
+ * there is no timeout condition to report.
+ * Errors: GAR_EINVAL (status NULL), GAR_ECUDA. */
+int gar_sync_status(gar_stream_t stream, uint32_t *status, int32_t clear);
 
 /* ===================================================================== */
 /* Ring all-reduce [H] "The Ring-Allreduce Algorithm", [R] sections 4, 5, 7 */

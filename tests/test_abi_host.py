@@ -100,6 +100,7 @@ def test_status_codes_without_launch(gar):
     assert lib.gar_dbtree_allreduce(odd, 2, 10, 0, 1, null) == gar.GAR_EALIGN
     assert lib.gar_dbtree_allreduce(None, 2, 0, 0, 1, null) == gar.GAR_OK  # N = 0: nothing touched
     assert lib.gar_dbtree_parents(0, 0, C.c_void_p(0x1000)) == gar.GAR_EINVAL
+    assert lib.gar_sync_status(null, None, 1) == gar.GAR_EINVAL
     assert lib.gar_dbtree_parents(4, 2, C.c_void_p(0x1000)) == gar.GAR_EINVAL
 
 
