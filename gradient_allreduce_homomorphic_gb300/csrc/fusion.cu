@@ -7,6 +7,7 @@
 // into tiles of 512 x 16-byte vectors, one CTA per tile, so a launch moves
 // hundreds of tensors of any size mix at streaming bandwidth.
 #include <cstring>
+#include <memory>
 #include <vector>
 
 #include "common.cuh"
@@ -513,10 +514,10 @@ extern "C" int gar_fusion_pack_all(const void *const *src, int32_t P, const gar_
             }
         }
     }
-    PackAllParams *p = new PackAllParams;
+    std::unique_ptr<PackAllParams> p(new PackAllParams);  // ~30 KB: keep it off the stack
     int rc = GAR_OK;
     for (int pass_dtype = 0; pass_dtype < 2 && rc == GAR_OK; ++pass_dtype) {
-        std::memset(p, 0, sizeof(PackAllParams));
+        std::memset(p.get(), 0, sizeof(PackAllParams));
         p->P = P;
         p->mM = d_mM;
         p->status = d_mM ? device_status() : nullptr;
@@ -580,7 +581,6 @@ extern "C" int gar_fusion_pack_all(const void *const *src, int32_t P, const gar_
         }
         if (rc == GAR_OK) rc = flush();
     }
-    delete p;
     return rc;
 }
 

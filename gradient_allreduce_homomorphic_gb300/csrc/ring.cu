@@ -20,6 +20,7 @@
 // at that buffer's chunk boundaries), where it reads the workers' tensors and
 // writes their results directly: pack, all-reduce and unpack in one pass.
 #include <cstring>
+#include <memory>
 #include <vector>
 
 #include "common.cuh"
@@ -33,10 +34,7 @@ constexpr int kThreads = 256;
 constexpr int kUnroll = 2;
 constexpr int kTileUnits = kThreads * kUnroll;
 constexpr int kLoadBatch = 8;  // worker vectors in flight per thread before folding
-#ifndef GAR_RING_RANGE_MIN_BLOCKS
-#define GAR_RING_RANGE_MIN_BLOCKS 4
-#endif
-constexpr int kRangeMinBlocks = GAR_RING_RANGE_MIN_BLOCKS;  // CTAs per SM the range variant is built for
+constexpr int kRangeMinBlocks = 4;  // CTAs per SM the range variant is built for
 
 template <typename T>
 struct Elem;
@@ -447,10 +445,8 @@ static int ring_single(const void *const *src, void *const *dst, int n_out, int3
         FoldParamsSmall p;
         return ring_single_impl(p, src, dst, n_out, P, N, dtype, op, rings, stream);
     }
-    FoldParamsLarge *p = new FoldParamsLarge;  // ~25 KB: keep it off the stack
-    const int rc = ring_single_impl(*p, src, dst, n_out, P, N, dtype, op, rings, stream);
-    delete p;
-    return rc;
+    std::unique_ptr<FoldParamsLarge> p(new FoldParamsLarge);  // ~25 KB: keep it off the stack
+    return ring_single_impl(*p, src, dst, n_out, P, N, dtype, op, rings, stream);
 }
 
 extern "C" int gar_ring_allreduce_sim(void *const *bufs, int32_t P, int64_t N, int32_t dtype, int32_t op,
@@ -530,10 +526,10 @@ int fused_allreduce_impl(const void *const *src, void *const *dst, int32_t P, co
         rc = reset_ranges(segs, count, buf_numel, n_buffers, d_mM, stream);
         if (rc) return rc;
     }
-    Prm *p = new Prm;  // ~25 KB: keep it off the stack
+    std::unique_ptr<Prm> p(new Prm);  // ~25 KB: keep it off the stack
     for (int pass_dtype = 0; pass_dtype < 2 && rc == GAR_OK; ++pass_dtype) {
         const int es = elem_bytes(pass_dtype);
-        std::memset(p, 0, sizeof(Prm));
+        std::memset(p.get(), 0, sizeof(Prm));
         p->P = P;
         p->n_out = P;
         p->range = pass_dtype == GAR_F32 ? d_mM : nullptr;
@@ -586,7 +582,6 @@ int fused_allreduce_impl(const void *const *src, void *const *dst, int32_t P, co
         }
         if (rc == GAR_OK) rc = flush();
     }
-    delete p;
     return rc;
 }
 

@@ -18,6 +18,7 @@
 // No integer<->float conversion is needed per element.
 #include <algorithm>
 #include <cstring>
+#include <memory>
 #include <vector>
 
 #include "common.cuh"
@@ -656,8 +657,8 @@ static int thc_plan_impl(const float *const *src, int32_t P, const gar_seg *segs
             return fail(ref[i] ? GAR_EALIGN : GAR_EINVAL, "reference %d NULL or not 4-byte aligned", i);
         members[sg.buffer].push_back(i);
     }
-    ThcPlanParams *p = new ThcPlanParams;  // ~29 KB: keep it off the stack
-    std::memset(p, 0, sizeof(ThcPlanParams));
+    std::unique_ptr<ThcPlanParams> p(new ThcPlanParams);  // ~29 KB: keep it off the stack
+    std::memset(p.get(), 0, sizeof(ThcPlanParams));
     p->keys = philox_keys(seed);
     p->P = P;
     p->L = static_cast<float>((1 << b) - 1);
@@ -722,7 +723,6 @@ static int thc_plan_impl(const float *const *src, int32_t P, const gar_seg *segs
             w0 = w1;
         }
     }
-    delete p;
     if (rc == GAR_OK && nmse) {
         thc_nmse_pair_kernel<<<1, kThreads, 0, stream>>>(ws, used, d_pair);
         rc = check_launch("thc_nmse_pair_kernel");
