@@ -161,30 +161,35 @@ __global__ void __launch_bounds__(kThreads) thc_encode_kernel(const __grid_const
     const float m = p.mM[0], M = p.mM[1];
     const float sc = range_scale(m, M, p.L);
     const uint64_t m2 = pack_f2(m, m), sc2 = pack_f2(sc, sc);
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-    // whole words with 16-byte aligned inputs: two words a thread per step,
-    // both words' loads in flight before either is quantized
+    // one CTA per tile of 2 * kThreads words: words w and w + kThreads of a
+    // thread, both words' loads in flight before either is quantized
+    const int64_t w = static_cast<int64_t>(blockIdx.x) * (2 * kThreads) + threadIdx.x;
+    const int64_t w2 = w + kThreads;
     const int64_t nfull = p.vec ? (p.N / E < p.nwords ? p.N / E : p.nwords) : 0;
-    int64_t w = tid;
-    for (; w + stride < nfull; w += 2 * stride) {
+    if (w2 < nfull) {
         float4 a[G], b[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) a[g] = __ldcs(reinterpret_cast<const float4 *>(p.x + w * E) + g);
 #pragma unroll
-        for (int g = 0; g < G; ++g) b[g] = __ldcs(reinterpret_cast<const float4 *>(p.x + (w + stride) * E) + g);
+        for (int g = 0; g < G; ++g) b[g] = __ldcs(reinterpret_cast<const float4 *>(p.x + w2 * E) + g);
         __stcs(p.packed + w, encode_word<B>(a, w * E, p, m, sc, m2, sc2));
-        __stcs(p.packed + w + stride, encode_word<B>(b, (w + stride) * E, p, m, sc, m2, sc2));
+        __stcs(p.packed + w2, encode_word<B>(b, w2 * E, p, m, sc, m2, sc2));
+        return;
     }
-    for (; w < nfull; w += stride) {
+    for (int u = 0; u < 2; ++u) {
+        const int64_t wu = u == 0 ? w : w2;
+        if (wu >= nfull) break;
         float4 a[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) a[g] = __ldcs(reinterpret_cast<const float4 *>(p.x + w * E) + g);
-        __stcs(p.packed + w, encode_word<B>(a, w * E, p, m, sc, m2, sc2));
+        for (int g = 0; g < G; ++g) a[g] = __ldcs(reinterpret_cast<const float4 *>(p.x + wu * E) + g);
+        __stcs(p.packed + wu, encode_word<B>(a, wu * E, p, m, sc, m2, sc2));
     }
     // the ragged last word, or unaligned inputs: element by element
-    for (w = nfull + tid; w < p.nwords; w += stride) {
-        const int64_t e0 = w * E;
+    for (int u = 0; u < 2; ++u) {
+        const int64_t wr = u == 0 ? w : w2;
+        if (wr < nfull || wr >= p.nwords) continue;
+        const int64_t ww = wr;
+        const int64_t e0 = ww * E;
         uint32_t word = 0;
         for (int g = 0; g < G; ++g) {
             const int64_t eb = e0 + 4 * g;
@@ -195,7 +200,7 @@ __global__ void __launch_bounds__(kThreads) thc_encode_kernel(const __grid_const
                 word |= idx << ((4 * g + i) * B);
             }
         }
-        __stcs(p.packed + w, word);
+        __stcs(p.packed + ww, word);
     }
 }
 
@@ -437,14 +442,15 @@ extern "C" int gar_thc_encode(const float *x, int64_t N, const float *d_mM, int3
     p.N = N;
     p.nwords = gar_thc_words(N, b);
     p.worker = worker;
+    const unsigned enc_grid = static_cast<unsigned>(ceil_div(p.nwords, 2 * kThreads));
     p.vec = aligned(x, 16) ? 1 : 0;
     p.L = static_cast<float>((1 << b) - 1);
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     switch (b) {
-        case 1: thc_encode_kernel<1><<<grid_for(thc_encode_kernel<1>, p.nwords), kThreads, 0, stream>>>(p); break;
-        case 2: thc_encode_kernel<2><<<grid_for(thc_encode_kernel<2>, p.nwords), kThreads, 0, stream>>>(p); break;
-        case 4: thc_encode_kernel<4><<<grid_for(thc_encode_kernel<4>, p.nwords), kThreads, 0, stream>>>(p); break;
-        default: thc_encode_kernel<8><<<grid_for(thc_encode_kernel<8>, p.nwords), kThreads, 0, stream>>>(p); break;
+        case 1: thc_encode_kernel<1><<<enc_grid, kThreads, 0, stream>>>(p); break;
+        case 2: thc_encode_kernel<2><<<enc_grid, kThreads, 0, stream>>>(p); break;
+        case 4: thc_encode_kernel<4><<<enc_grid, kThreads, 0, stream>>>(p); break;
+        default: thc_encode_kernel<8><<<enc_grid, kThreads, 0, stream>>>(p); break;
     }
     return check_launch("thc_encode_kernel");
 }
