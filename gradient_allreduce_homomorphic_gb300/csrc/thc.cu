@@ -305,18 +305,23 @@ __global__ void __launch_bounds__(kThreads) thc_decode_kernel(const __grid_const
             __stcs(dst, make_float4(o[0], o[1], o[2], o[3]));
             __stcs(dst + 1, make_float4(o[4], o[5], o[6], o[7]));
         };
-        int64_t i = tid;
-        for (; i + 3 * stride < n8; i += 4 * stride) {
+        // one CTA per tile of 4 * kThreads groups of eight: a thread's four
+        // groups i, i + kThreads, ... loaded before the first is decoded
+        const int64_t i = static_cast<int64_t>(blockIdx.x) * (4 * kThreads) + threadIdx.x;
+        if (i + 3 * kThreads < n8) {
             uint4 sv[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) sv[u] = __ldcs(reinterpret_cast<const uint4 *>(p.sums) + i + u * stride);
+            for (int u = 0; u < 4; ++u) sv[u] = __ldcs(reinterpret_cast<const uint4 *>(p.sums) + i + u * kThreads);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) decode8(sv[u], i + u * stride);
+            for (int u = 0; u < 4; ++u) decode8(sv[u], i + u * kThreads);
+        } else {
+            for (int u = 0; u < 4; ++u)
+                if (i + u * kThreads < n8) decode8(__ldcs(reinterpret_cast<const uint4 *>(p.sums) + i + u * kThreads),
+                                                   i + u * kThreads);
         }
-        for (; i < n8; i += stride) decode8(__ldcs(reinterpret_cast<const uint4 *>(p.sums) + i), i);
         first = n8 * 8;
     }
-    for (int64_t e = first + tid; e < p.N; e += stride)
+    for (int64_t e = first + tid; e < p.N; e += stride)  // the tail past the groups, or unaligned
         p.avg[e] = __fmaf_rn(small_to_float(p.sums[e]), k, m);
 }
 
@@ -501,8 +506,10 @@ int launch_grid_decode(const uint16_t *sums, int64_t N, const float *d_mM, int s
     p.L = static_cast<float>(steps);
     p.fp = static_cast<float>(P);
     p.vec = aligned(sums, 16) && aligned(avg, 16);
-    const int64_t items = p.vec ? ceil_div(N, 8) : N;
-    thc_decode_kernel<<<grid_for(thc_decode_kernel, items), kThreads, 0, stream>>>(p);
+    // vector path: one CTA per 4 * kThreads groups of eight; else a resident grid
+    const int64_t grid = p.vec ? std::max<int64_t>(ceil_div(ceil_div(N, 8), 4 * kThreads), 1)
+                               : grid_for(thc_decode_kernel, N);
+    thc_decode_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
     return check_launch("thc_decode_kernel");
 }
 }  // namespace thc
