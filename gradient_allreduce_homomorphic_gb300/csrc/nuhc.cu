@@ -71,6 +71,42 @@ __device__ __forceinline__ uint32_t nuhc_index(float x, float m, float sc, float
     return static_cast<uint32_t>(z) + (up ? 1u : 0u);
 }
 
+// The same decision for two elements at once: the subtracts, the multiply,
+// the rounded-down add and the FMA go through the packed f32x2 instructions
+// (each lane rounded exactly as the scalar operation, subnormals kept); the
+// clamp, the table lookups and the comparisons stay per element.  Bit for bit
+// equal to two nuhc_index calls.
+__device__ __forceinline__ uint64_t fma_rn_f2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ void nuhc_index2(float x0, float x1, uint64_t m2, uint64_t sc2, float G, int g,
+                                            const float2 *s_pair, const uint8_t *s_inv, uint32_t r0, uint32_t r1,
+                                            uint32_t &i0, uint32_t &i1, float &tv0, float &tv1) {
+    float2 t = unpack_f2(mul_rn_f2(sub_rn_f2(pack_f2(x0, x1), m2), sc2));
+    t.x = fminf(fmaxf(t.x, 0.0f), G);
+    t.y = fminf(fmaxf(t.y, 0.0f), G);
+    const uint64_t t2 = pack_f2(t.x, t.y);
+    const float2 jm = unpack_f2(add_rm_f2(t2, pack_f2(8388608.0f, 8388608.0f)));  // floor(t) + 2^23
+    int k0 = __float_as_int(jm.x) - 0x4B000000, k1 = __float_as_int(jm.y) - 0x4B000000;
+    k0 = k0 < g - 1 ? k0 : g - 1;
+    k1 = k1 < g - 1 ? k1 : g - 1;
+    const int z0 = s_inv[k0], z1 = s_inv[k1];
+    const float2 p0 = s_pair[z0], p1 = s_pair[z1];  // (T[z], T[z + 1]) of each
+    const uint64_t lo = pack_f2(p0.x, p1.x), hi = pack_f2(p0.y, p1.y);
+    // -u = 1 - (1 + u), exact; then fma(-u, hi - lo, t - lo) as in nuhc_index
+    const uint64_t one_u = pack_f2(__uint_as_float((r0 & 0x007FFFFFu) | 0x3F800000u),
+                                   __uint_as_float((r1 & 0x007FFFFFu) | 0x3F800000u));
+    const uint64_t neg_u = sub_rn_f2(pack_f2(1.0f, 1.0f), one_u);
+    const float2 f = unpack_f2(fma_rn_f2(neg_u, sub_rn_f2(hi, lo), sub_rn_f2(t2, lo)));
+    const bool up0 = f.x > 0.0f, up1 = f.y > 0.0f;
+    tv0 = up0 ? p0.y : p0.x;
+    tv1 = up1 ? p1.y : p1.x;
+    i0 = static_cast<uint32_t>(z0) + (up0 ? 1u : 0u);
+    i1 = static_cast<uint32_t>(z1) + (up1 ? 1u : 0u);
+}
+
 struct NuhcEncodeParams {
     PhiloxKeys keys;
     NuhcTable tab;
@@ -93,6 +129,7 @@ __global__ void __launch_bounds__(kThreads) nuhc_encode_kernel(const __grid_cons
     const float m = p.mM[0], M = p.mM[1];
     const float G = static_cast<float>(p.tab.g);
     const float sc = range_scale(m, M, G);
+    const uint64_t m2 = pack_f2(m, m), sc2 = pack_f2(sc, sc);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < p.nwords; w += stride) {
         const int64_t e0 = w * E;
@@ -112,10 +149,10 @@ __global__ void __launch_bounds__(kThreads) nuhc_encode_kernel(const __grid_cons
                 if (eb + 2 < p.N) v.z = p.x[eb + 2];
                 if (eb + 3 < p.N) v.w = p.x[eb + 3];
             }
-            const uint32_t i0 = nuhc_index(v.x, m, sc, G, p.tab.g, s_pair, s_inv, r.x, tv);
-            const uint32_t i1 = nuhc_index(v.y, m, sc, G, p.tab.g, s_pair, s_inv, r.y, tv);
-            const uint32_t i2 = nuhc_index(v.z, m, sc, G, p.tab.g, s_pair, s_inv, r.z, tv);
-            const uint32_t i3 = nuhc_index(v.w, m, sc, G, p.tab.g, s_pair, s_inv, r.w, tv);
+            uint32_t i0, i1, i2, i3;
+            float tv1;
+            nuhc_index2(v.x, v.y, m2, sc2, G, p.tab.g, s_pair, s_inv, r.x, r.y, i0, i1, tv, tv1);
+            nuhc_index2(v.z, v.w, m2, sc2, G, p.tab.g, s_pair, s_inv, r.z, r.w, i2, i3, tv, tv1);
             uint32_t q = i0 | (i1 << B) | (i2 << (2 * B)) | (i3 << (3 * B));
             const int64_t valid = p.N - eb;  // elements of this group inside N
             if (valid < 4) q &= (1u << (B * valid)) - 1u;
@@ -184,17 +221,16 @@ struct NuhcFusedParams {
 // (The sums of table values are integers below 2^24: exact in fp32.)
 template <int B, bool kPacked, int G4>
 __device__ __forceinline__ void nuhc_one_worker(const float4 (&v)[G4], float (&s)[4 * G4], int64_t e0, int64_t w,
-                                                int wk, const NuhcFusedParams &p, float m, float sc, float G,
+                                                int wk, const NuhcFusedParams &p, uint64_t m2, uint64_t sc2, float G,
                                                 const float2 *s_pair, const uint8_t *s_inv) {
     uint32_t word = 0;
 #pragma unroll
     for (int g4 = 0; g4 < G4; ++g4) {
         const uint4 r = philox_block((e0 >> 2) + g4, wk, p.keys);
         float t0, t1, t2, t3;
-        const uint32_t i0 = nuhc_index(v[g4].x, m, sc, G, p.tab.g, s_pair, s_inv, r.x, t0);
-        const uint32_t i1 = nuhc_index(v[g4].y, m, sc, G, p.tab.g, s_pair, s_inv, r.y, t1);
-        const uint32_t i2 = nuhc_index(v[g4].z, m, sc, G, p.tab.g, s_pair, s_inv, r.z, t2);
-        const uint32_t i3 = nuhc_index(v[g4].w, m, sc, G, p.tab.g, s_pair, s_inv, r.w, t3);
+        uint32_t i0, i1, i2, i3;
+        nuhc_index2(v[g4].x, v[g4].y, m2, sc2, G, p.tab.g, s_pair, s_inv, r.x, r.y, i0, i1, t0, t1);
+        nuhc_index2(v[g4].z, v[g4].w, m2, sc2, G, p.tab.g, s_pair, s_inv, r.z, r.w, i2, i3, t2, t3);
         s[4 * g4] = __fadd_rn(s[4 * g4], t0);
         s[4 * g4 + 1] = __fadd_rn(s[4 * g4 + 1], t1);
         s[4 * g4 + 2] = __fadd_rn(s[4 * g4 + 2], t2);
@@ -217,6 +253,7 @@ __global__ void __launch_bounds__(kThreads) nuhc_fused_kernel(const __grid_const
     const float sc = range_scale(m, M, G);
     float km;
     const float k = decode_step(p.mM, G, static_cast<float>(p.P), km);
+    const uint64_t m2 = pack_f2(m, m), sc2 = pack_f2(sc, sc);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t w = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; w < p.nwords; w += stride) {
         const int64_t e0 = w * E;
@@ -235,12 +272,12 @@ __global__ void __launch_bounds__(kThreads) nuhc_fused_kernel(const __grid_const
 #pragma unroll
                     for (int g4 = 0; g4 < G4; ++g4) vb[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk + 1] + e0) + g4);
                 }
-                nuhc_one_worker<B, kPacked>(va, s, e0, w, wk, p, m, sc, G, s_pair, s_inv);
+                nuhc_one_worker<B, kPacked>(va, s, e0, w, wk, p, m2, sc2, G, s_pair, s_inv);
                 if (wk + 2 < p.P) {
 #pragma unroll
                     for (int g4 = 0; g4 < G4; ++g4) va[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk + 2] + e0) + g4);
                 }
-                if (has1) nuhc_one_worker<B, kPacked>(vb, s, e0, w, wk + 1, p, m, sc, G, s_pair, s_inv);
+                if (has1) nuhc_one_worker<B, kPacked>(vb, s, e0, w, wk + 1, p, m2, sc2, G, s_pair, s_inv);
             }
             float4 *dst = reinterpret_cast<float4 *>(p.avg + e0);
 #pragma unroll
