@@ -161,14 +161,14 @@ __global__ void __launch_bounds__(kThreads) rht_pass_kernel(const __grid_constan
     const int64_t hi = bid >> cb_bits;
     float *x = p.out + ((hi << (p.s + 8)) | (cb << 4) | c);
     float v[16];
-    // round 1: rows (mh << 4) | j
+    // first stage: rows (mh << 4) | j
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = __ldcs(x + (static_cast<int64_t>((mh << 4) | j) << p.s));
     butterfly16(v, p.lo_bit);
 #pragma unroll
     for (int j = 0; j < 16; ++j) s[pass_swz((mh << 8) | (j << 4) | c)] = v[j];
     __syncthreads();
-    // round 2: rows (j << 4) | mh
+    // second stage: rows (j << 4) | mh
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = s[pass_swz((j << 8) | (mh << 4) | c)];
     butterfly16(v, p.lo_bit > 4 ? p.lo_bit - 4 : 0);
