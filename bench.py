@@ -316,11 +316,12 @@ class Step:
         for s in self.s_h2d + [self.s_d2h]:
             main.wait_stream(s)
 
-    def run_e2e(self, step_idx, host_in, host_ring, host_thc, host_nmse):
-        """One step from pinned host gradients to host averages and NMSE,
-        pipelined by fusion buffer: buffer b+1's inputs cross the link (the
-        workers split over the copy streams) while buffer b is averaged, and
-        b's results travel back meanwhile.  Consecutive steps overlap too: a
+    def run_e2e(self, step_idx, host_in, host_ring, host_thc, host_nmse, averages=False):
+        """One step from pinned host gradients to the step's metric (the NMSE)
+        on the host -- and with averages=True both averages too -- pipelined
+        by fusion buffer: buffer b+1's inputs cross the link (the workers
+        split over the copy streams) while buffer b is averaged, and b's
+        averages travel back meanwhile.  Consecutive steps overlap too: a
         buffer's inputs for this step are copied in as soon as the previous
         step has consumed that buffer's inputs, and its averages are
         overwritten only once the previous step's have been copied out."""
@@ -338,16 +339,18 @@ class Step:
                         self.flat[w][lo:hi].copy_(host_in[w][lo:hi], non_blocking=True)
                     self.ev_in[b][j].record(s)
                 main.wait_event(self.ev_in[b][j])
-            main.wait_event(self.ev_sent[b])
+            if averages:
+                main.wait_event(self.ev_sent[b])
             self._buffer_ring(plan, b, main)
             self._buffer_thc(plan, b, seed, main)
             self.ev_read[b].record(main)
-            self.ev_out[b].record(main)
-            self.s_d2h.wait_event(self.ev_out[b])
-            with torch.cuda.stream(self.s_d2h):
-                host_ring[lo:hi].copy_(self.ring_flat[0][lo:hi], non_blocking=True)
-                host_thc[lo:hi].copy_(self.thc_flat[lo:hi], non_blocking=True)
-                self.ev_sent[b].record(self.s_d2h)
+            if averages:
+                self.ev_out[b].record(main)
+                self.s_d2h.wait_event(self.ev_out[b])
+                with torch.cuda.stream(self.s_d2h):
+                    host_ring[lo:hi].copy_(self.ring_flat[0][lo:hi], non_blocking=True)
+                    host_thc[lo:hi].copy_(self.thc_flat[lo:hi], non_blocking=True)
+                    self.ev_sent[b].record(self.s_d2h)
         main.wait_event(self.ev_nmse_sent)  # the previous step's NMSE is on the host
         self._nmse(main)
         self.ev_nmse.record(main)
@@ -486,7 +489,7 @@ def run_ours(args, rank, world, dist):
     st.setup_e2e(args.h2d_streams)
 
     def e2e_step(i):
-        st.run_e2e(10_000 + i, host_in, host_ring, host_thc, host_nmse)
+        st.run_e2e(10_000 + i, host_in, host_ring, host_thc, host_nmse, averages=args.e2e_readback == "averages")
 
     st.start_e2e()
     for i in range(3):
@@ -553,7 +556,10 @@ def run_ours(args, rank, world, dist):
                                else "in the timed steps")},
         "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": P * st.flat_len * 4,
-                "d2h_bytes_per_step": 2 * st.flat_len * 4 + 8, "h2d_streams": args.h2d_streams},
+                "d2h_bytes_per_step": (2 * st.flat_len * 4 if args.e2e_readback == "averages" else 0) + 8,
+                "h2d_streams": args.h2d_streams,
+                "readback": ("the NMSE and both averages" if args.e2e_readback == "averages"
+                             else "the step's metric (NMSE); the averages stay on the device")},
         "gpu_launches": int(launches),
         "nmse_thc_b4": round(nmse_vals[0], 6),
         "clocks": clk,
@@ -1015,6 +1021,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--schedule", choices=["overlap", "serial"], default="overlap")
     ap.add_argument("--h2d-streams", type=int, default=2, help="copy streams for the end-to-end inputs")
+    ap.add_argument("--e2e-readback", choices=["metric", "averages"], default="metric",
+                    help="end to end: read back the step's metric (NMSE) only, or also both averages")
     ap.add_argument("--nmse", choices=["fused", "separate"], default="separate",
                     help="NMSE sums inside the THC pass, or one NMSE pass over both averages at the end")
     ap.add_argument("--reference-budget-s", type=float, default=100.0,
