@@ -141,7 +141,8 @@ __global__ void __launch_bounds__(kThreads) rht_tile_kernel(const __grid_constan
             if (signs_out && ((s_sign[e >> 5] >> (e & 31)) & 1u)) y = -y;
             y = __fmul_rn(y, p.scale);
         }
-        __stcs(dst + e, y);
+        if (p.last) __stcs(dst + e, y);
+        else dst[e] = y;  // the next pass reads it: normal priority, so that it can stay in L2
     }
 }
 
@@ -163,7 +164,7 @@ __global__ void __launch_bounds__(kThreads) rht_pass_kernel(const __grid_constan
     float v[16];
     // first stage: rows (mh << 4) | j
 #pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __ldcs(x + (static_cast<int64_t>((mh << 4) | j) << p.s));
+    for (int j = 0; j < 16; ++j) v[j] = x[static_cast<int64_t>((mh << 4) | j) << p.s];  // written by the launch before
     butterfly16(v, p.lo_bit);
 #pragma unroll
     for (int j = 0; j < 16; ++j) s[pass_swz((mh << 8) | (j << 4) | c)] = v[j];
@@ -192,7 +193,10 @@ __global__ void __launch_bounds__(kThreads) rht_pass_kernel(const __grid_constan
         for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], p.scale);
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) __stcs(x + (static_cast<int64_t>((j << 4) | mh) << p.s), v[j]);
+    for (int j = 0; j < 16; ++j) {
+        if (p.last) __stcs(x + (static_cast<int64_t>((j << 4) | mh) << p.s), v[j]);
+        else x[static_cast<int64_t>((j << 4) | mh) << p.s] = v[j];
+    }
 }
 
 // n < 4096: one CTA, every stage in shared memory.
