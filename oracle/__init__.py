@@ -105,6 +105,7 @@ def _load():
                 "oracle_ef_apply": (None, [vp, vp, vp, i64]),
                 "oracle_ef_update": (None, [vp, vp, vp, i64]),
                 "oracle_nmse": (C.c_double, [vp, vp, i64]),
+                "oracle_checksum": (C.c_uint64, [vp, i64]),
                 "oracle_nmse_f64": (C.c_double, [vp, vp, i64]),
             }
             for name, (res, args) in sig.items():
@@ -519,3 +520,10 @@ def nmse(x, x_hat) -> float:
         return float(_load().oracle_nmse_f64(_ptr(x), _ptr(x_hat), x.size))
     return float(_load().oracle_nmse(_ptr(np.ascontiguousarray(x, np.float32)),
                                      _ptr(np.ascontiguousarray(x_hat, np.float32)), x.size))
+
+
+# --------------------------------------------------------------- checksum
+def checksum(words) -> int:
+    """(s2 << 32) | s1 with s1 = sum w_i, s2 = sum (i + 1) w_i (mod 2^32) over uint32 words."""
+    w = np.ascontiguousarray(words, np.uint32)
+    return int(_load().oracle_checksum(_ptr(w), w.size))

@@ -990,3 +990,17 @@ double oracle_nmse_f64(const double *x, const double *x_hat, int64_t n) {
     if (den == 0.0) return NAN;
     return num / den;
 }
+
+/* ===================================================================== */
+/* Wire-vector checksum (silent data corruption check of the packed       */
+/* indices): s1 = sum w_i, s2 = sum (i + 1) w_i over the 32-bit words,    */
+/* both mod 2^32; returns (s2 << 32) | s1.                                */
+/* ===================================================================== */
+uint64_t oracle_checksum(const uint32_t *w, int64_t n) {
+    uint32_t s1 = 0, s2 = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        s1 += w[i];
+        s2 += (uint32_t)(i + 1) * w[i];
+    }
+    return ((uint64_t)s2 << 32) | s1;
+}

@@ -205,6 +205,13 @@ void oracle_ef_update(float *e, const float *x, const float *x_hat, int64_t n);
 double oracle_nmse(const float *x, const float *x_hat, int64_t n);
 double oracle_nmse_f64(const double *x, const double *x_hat, int64_t n);
 
+/* ---------------- wire-vector checksum ---------------- */
+/* Silent-data-corruption check of the packed indices (the survey's plan for
+ * failure detection; the pages fix no checksum): s1 = sum w_i and
+ * s2 = sum (i + 1) w_i over the n 32-bit words, both mod 2^32; returns
+ * (s2 << 32) | s1.  s1 changes with any flipped bit, s2 with swapped words. */
+uint64_t oracle_checksum(const uint32_t *w, int64_t n);
+
 #ifdef __cplusplus
 }
 #endif
