@@ -46,6 +46,7 @@ _SIGNATURES = {
     "gar_last_error": (C.c_char_p, []),
     "gar_launch_count": (C.c_uint64, []),
     "gar_sync_status": (C.c_int, [_vp, _vp, _i32]),
+    "gar_checksum": (C.c_int, [_vp, _i64, _vp, _vp]),
     "gar_fusion_plan": (C.c_int, [_vp, _vp, _i32, _i64, _i32, _vp, C.POINTER(_i32), _vp]),
     "gar_fusion_pack": (C.c_int, [_pp, _vp, _vp, _i32, _i32, _vp, _i64, _vp]),
     "gar_fusion_unpack": (C.c_int, [_vp, _vp, _vp, _i32, _i32, _pp, _vp]),
@@ -352,6 +353,13 @@ def gar_fused_allreduce_range(src, dst, plan: FusionPlan, d_mM, op: int = GAR_AV
 
 
 GAR_STATUS_NONFINITE = 1
+
+
+def gar_checksum(words, d_out, stream=None):
+    """(s2 << 32) | s1 of the 32-bit words (a CUDA tensor of 4-byte elements)
+    into d_out (one int64/uint64 element on the device)."""
+    n = words.numel() * words.element_size() // 4
+    _call("gar_checksum", _dev(words), n, _dev(d_out), _stream(stream))
 
 
 def gar_sync_status(stream=None, clear: bool = True) -> int:

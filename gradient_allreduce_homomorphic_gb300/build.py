@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgar.so")
 
 SOURCES = ["common.cu", "ring.cu", "fusion.cu", "thc.cu", "nuhc.cu", "thc_p4.cu", "thc_p8.cu", "thc_p16.cu", "thc_p64.cu",
-           "rht.cu", "nmse.cu", "dbtree.cu"]
+           "rht.cu", "nmse.cu", "dbtree.cu", "checksum.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
               "--expt-relaxed-constexpr"]

@@ -196,6 +196,12 @@ def main(argv=None):
             inv = a.case == "rht_inv"
             fn = lambda: g.gar_rht(src, dst, 7, inverse=inv)  # noqa: E731
             nbytes = 2 * N * 4
+    elif a.case == "checksum":
+        # algorithmic bytes: one read of N 32-bit words
+        w = bufs(N, 1, torch.float32)[0].view(torch.int32)
+        out = torch.empty(1, dtype=torch.int64, device=dev)
+        fn = lambda: g.gar_checksum(w, out)  # noqa: E731
+        nbytes = N * 4
     else:
         raise SystemExit(f"unknown case {a.case}")
 

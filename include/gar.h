@@ -196,6 +196,16 @@ int gar_fused_allreduce_range(const void *const *src, void *const *dst, int32_t 
                               const int32_t *dtype, int32_t count, const int64_t *buf_numel,
                               int32_t n_buffers, int32_t op, float *d_mM, gar_stream_t stream);
 
+/* gar_checksum -- *d_out (device, one uint64) = (s2 << 32) | s1 with
+ * s1 = sum w_i and s2 = sum (i + 1) w_i over the n 32-bit words d_words
+ * (device, 4-byte aligned), both mod 2^32: a check against silent data
+ * corruption of THC's wire vectors (a worker's packed indices as sent and
+ * as the parameter server receives them).  A flipped bit changes s1, two
+ * swapped words change s2; the value does not depend on the order of the
+ * device's partial sums.  n = 0 gives 0.
+ * Errors: GAR_EINVAL (n < 0, NULL), GAR_EALIGN, GAR_ECUDA. */
+int gar_checksum(const uint32_t *d_words, int64_t n, uint64_t *d_out, gar_stream_t stream);
+
 /* gar_sync_status -- waits for `stream`, then *status (host) = the device
  * status word of the current device: bits that kernels set for conditions
  * they find on the device.  GAR_STATUS_NONFINITE: a THC range pass

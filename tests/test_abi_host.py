@@ -101,6 +101,11 @@ def test_status_codes_without_launch(gar):
     assert lib.gar_dbtree_allreduce(None, 2, 0, 0, 1, null) == gar.GAR_OK  # N = 0: nothing touched
     assert lib.gar_dbtree_parents(0, 0, C.c_void_p(0x1000)) == gar.GAR_EINVAL
     assert lib.gar_sync_status(null, None, 1) == gar.GAR_EINVAL
+    assert lib.gar_checksum(C.c_void_p(0x1000), -1, C.c_void_p(0x2000), null) == gar.GAR_EINVAL
+    assert lib.gar_checksum(None, 10, C.c_void_p(0x2000), null) == gar.GAR_EINVAL
+    assert lib.gar_checksum(C.c_void_p(0x1000), 10, None, null) == gar.GAR_EINVAL
+    assert lib.gar_checksum(C.c_void_p(0x1002), 10, C.c_void_p(0x2000), null) == gar.GAR_EALIGN
+    assert lib.gar_checksum(C.c_void_p(0x1000), 10, C.c_void_p(0x2004), null) == gar.GAR_EALIGN
     assert lib.gar_dbtree_parents(4, 2, C.c_void_p(0x1000)) == gar.GAR_EINVAL
 
 
