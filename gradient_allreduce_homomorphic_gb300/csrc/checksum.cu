@@ -11,7 +11,6 @@ namespace gar {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTileWords = 4 * 4 * kThreads;  // four 16-byte groups per thread
 
 __global__ void checksum_init(unsigned long long *out) { *out = 0ull; }
 
@@ -20,17 +19,23 @@ __device__ __forceinline__ void sum_word(uint32_t w, uint64_t i, uint32_t &s1, u
     s2 += static_cast<uint32_t>(i + 1) * w;
 }
 
-// One CTA per tile of kTileWords words; vec: the words are 16-byte aligned.
+// One CTA per tile of 4 * U * kThreads words (U 16-byte groups per thread);
+// vec: the words are 16-byte aligned.  Every CTA ends in two same-address
+// atomics, whose serial rate bounds a grid of many small tiles (at 1 GB,
+// 4096-word tiles ran at half the copy rate, 16384-word tiles at the copy
+// rate), so large vectors take U = 16.
+template <int U>
 __global__ void __launch_bounds__(kThreads) checksum_kernel(const uint32_t *w, int64_t n, int vec,
                                                             unsigned long long *out) {
+    constexpr int kTileWords = 4 * U * kThreads;
     uint32_t s1 = 0, s2 = 0;
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTileWords;
     if (vec && t0 + kTileWords <= n) {
-        uint4 g[4];
+        uint4 g[U];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) g[u] = ld16(w + t0 + 4 * (u * kThreads + threadIdx.x));
+        for (int u = 0; u < U; ++u) g[u] = ld16(w + t0 + 4 * (u * kThreads + threadIdx.x));
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < U; ++u) {
             const uint64_t i = static_cast<uint64_t>(t0 + 4 * (u * kThreads + threadIdx.x));
             sum_word(g[u].x, i, s1, s2);
             sum_word(g[u].y, i + 1, s1, s2);
@@ -78,9 +83,14 @@ extern "C" int gar_checksum(const uint32_t *d_words, int64_t n, uint64_t *d_out,
     checksum_init<<<1, 1, 0, stream>>>(out);
     int rc = check_launch("checksum_init");
     if (rc || n == 0) return rc;
-    const int64_t blocks = ceil_div(n, kTileWords);
-    if (blocks > 0x7FFFFFFF) return fail(GAR_EINVAL, "n=%lld too large", static_cast<long long>(n));
-    checksum_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(d_words, n, aligned(d_words, 16) ? 1 : 0,
-                                                                           out);
+    const int vec = aligned(d_words, 16) ? 1 : 0;
+    if (n <= (int64_t{1} << 26)) {  // up to 256 MB: 8192-word tiles keep more CTAs in flight
+        checksum_kernel<8><<<static_cast<unsigned>(ceil_div(n, int64_t{4 * 8 * kThreads})), kThreads, 0, stream>>>(
+            d_words, n, vec, out);
+    } else {
+        const int64_t blocks = ceil_div(n, int64_t{4 * 16 * kThreads});
+        if (blocks > 0x7FFFFFFF) return fail(GAR_EINVAL, "n=%lld too large", static_cast<long long>(n));
+        checksum_kernel<16><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(d_words, n, vec, out);
+    }
     return check_launch("checksum_kernel");
 }

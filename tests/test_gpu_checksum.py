@@ -22,7 +22,7 @@ def _sum(torch, g, t):
     return int(to_host(out).view(np.uint64)[0])
 
 
-@pytest.mark.parametrize("n", [0, 1, 3, 4095, 4096, 4097, 100003, 1 << 22])
+@pytest.mark.parametrize("n", [0, 1, 3, 4095, 4096, 4097, 100003, 1 << 22, (1 << 26) + 16385])
 def test_random_words(env, n):
     torch, g = env
     w = np.random.default_rng([7, n]).integers(0, 2**32, size=n, dtype=np.uint64).astype(np.uint32)

@@ -47,7 +47,8 @@ def _words(g, N, b, P, torch):
     return [torch.empty(max(g.gar_thc_words(N, b), 1), dtype=torch.int32, device="cuda") for _ in range(P)]
 
 
-CASES = [(1, 1), (1, 5), (2, 3), (2, 4), (2, 17), (4, 15), (4, 36), (4, 51), (8, 255), (8, 1000)]
+CASES = [(1, 1), (1, 5), (2, 3), (2, 4), (2, 17), (4, 15), (4, 36), (4, 51), (4, 4000), (8, 255), (8, 1000),
+         (8, 1023), (8, 1024)]
 
 
 @pytest.mark.parametrize("b,g", CASES)
