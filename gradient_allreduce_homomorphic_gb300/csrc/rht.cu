@@ -14,12 +14,16 @@
 // its registers.  Higher bits go in passes of up to eight: a CTA holds 256
 // rows of 16 consecutive elements, the rows 2^s apart (64-byte segments:
 // whole DRAM sectors), and does the row bits in two register rounds around
-// one transpose.  n = 2^24 takes three kernels, n = 2^20 two.
+// one transpose.  For n = 2^21 .. 2^24 one cluster pass does all the bits
+// above 11 (clusters of up to 16 CTAs exchanging rows through distributed
+// shared memory), so these sizes take two kernels, as does n = 2^20; larger
+// n take the passes of eight (2^28: three kernels).
 //
 // The Rademacher signs D come from their own Philox stream (worker slot
 // 0xFFFFFFFF): one 128-bit block per 128 elements, bit i mod 128 for
 // element i.  The forward transform applies them as the first tile kernel
 // loads; the inverse applies them as the last kernel stores.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -197,6 +201,173 @@ __global__ void __launch_bounds__(kThreads) rht_pass_kernel(const __grid_constan
         if (p.last) __stcs(x + (static_cast<int64_t>((j << 4) | mh) << p.s), v[j]);
         else x[static_cast<int64_t>((j << 4) | mh) << p.s] = v[j];
     }
+}
+
+// Row bits [0, 8 + RB) of 2^(8+RB) rows 2^s apart (s >= 12), 16 columns each,
+// in place on p.out, by a cluster of K = 2^RB CTAs: the CTA of cluster rank q
+// holds rows (q << 8) | m (m < 256) and does their bits 0..7 as
+// rht_pass_kernel does, keeping the result in its shared memory; after a
+// cluster barrier every thread takes positions (m, c) and reads that
+// position from all K CTAs' shared memory (distributed shared memory), does
+// the stages of row bits 8.. on the K values and stores rows (r << 8) | m.
+// Cluster id -> (hi, column block cb): element of (row m, column c) =
+// (hi << (s + 8 + RB)) | (m << s) | (cb << 4) | c.  With 16-CTA clusters one
+// launch covers twelve index bits, so n = 2^21 .. 2^24 take two kernels.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The exit barrier orders nothing but the other CTAs' reads of this CTA's
+// shared memory, which completed when their values arrived in registers: a
+// relaxed arrive, so that the thread need not wait for its global stores.
+__device__ __forceinline__ void cluster_sync_exit() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_cluster(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    return remote;
+}
+__device__ __forceinline__ float ld_cluster(uint32_t cluster_addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+template <int RB>
+__global__ void __launch_bounds__(kThreads) rht_cluster_pass_kernel(const __grid_constant__ RhtParams p) {
+    constexpr int K = 1 << RB;
+    __shared__ float s[kTile];
+    const int t = threadIdx.x;
+    const int c = t & 15, mh = t >> 4;
+    const uint32_t q = cluster_rank();
+    const int64_t cid = static_cast<int64_t>(blockIdx.x) >> RB;
+    const int cb_bits = p.s - 4;
+    const int64_t cb = cid & ((int64_t{1} << cb_bits) - 1);
+    const int64_t hi = cid >> cb_bits;
+    const int64_t base = (hi << (p.s + 8 + RB)) | (cb << 4);  // row 0, column 0 of the cluster's block
+    const float *x = p.out + base + (static_cast<int64_t>(q) << (p.s + 8)) + c;
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = x[static_cast<int64_t>((mh << 4) | j) << p.s];  // written by the launch before
+    butterfly16(v);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) s[pass_swz((mh << 8) | (j << 4) | c)] = v[j];
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = s[pass_swz((j << 8) | (mh << 4) | c)];
+    butterfly16(v);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) s[pass_swz((j << 8) | (mh << 4) | c)] = v[j];
+    cluster_sync_all();  // every CTA's rows are done and visible to the cluster
+    // the cluster-window address of every CTA's array; an offset within the
+    // array adds to it as to a local address
+    uint32_t rbase[K];
+    {
+        const uint32_t s_addr = static_cast<uint32_t>(__cvta_generic_to_shared(s));
+#pragma unroll
+        for (int r = 0; r < K; ++r) rbase[r] = map_cluster(s_addr, r);
+    }
+    const int lane = t & 31;
+#pragma unroll 1
+    for (int i = 0; i < 16 / K; ++i) {
+        const int pos = i * (K * 256) + static_cast<int>(q) * 256 + t;  // (m, c) = (pos >> 4, pos & 15)
+        const int m = pos >> 4;
+        float w[K];
+#pragma unroll
+        for (int r = 0; r < K; ++r) w[r] = ld_cluster(rbase[r] + 4u * static_cast<uint32_t>(pass_swz(pos)));
+#pragma unroll
+        for (int h = 1; h < K; h <<= 1) {
+#pragma unroll
+            for (int r = 0; r < K; ++r) {
+                if ((r & h) == 0) {
+                    const float a = w[r], b = w[r + h];
+                    w[r] = __fadd_rn(a, b);
+                    w[r + h] = __fsub_rn(a, b);
+                }
+            }
+        }
+        if (p.last) {
+            if (p.inverse) {
+                // the 16 columns of a half-warp share one sign word per row: lane L
+                // draws the word of row ((L mod K) << 8) | m, the others read it
+                const int64_t e_lane = base | (static_cast<int64_t>(((lane & (K - 1)) << 8) | m) << p.s);
+                const uint32_t mine = word_of(sign_block(e_lane >> 7, p.keys), static_cast<int>((e_lane >> 5) & 3));
+                const int bit = static_cast<int>(((cb & 1) << 4) | c);
+#pragma unroll
+                for (int r = 0; r < K; ++r) {
+                    const uint32_t word = __shfl_sync(0xFFFFFFFFu, mine, r | (lane & 16));
+                    if ((word >> bit) & 1u) w[r] = -w[r];
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < K; ++r) w[r] = __fmul_rn(w[r], p.scale);
+        }
+        float *y = p.out + base + c;
+#pragma unroll
+        for (int r = 0; r < K; ++r) {
+            float *dst = y + (static_cast<int64_t>((r << 8) | m) << p.s);
+            if (p.last) __stcs(dst, w[r]);
+            else *dst = w[r];
+        }
+    }
+    cluster_sync_exit();  // no CTA leaves while another still reads its shared memory
+}
+
+// The cluster pass saves a launch where the vector stays in L2 between the
+// launches (2^21: 0.0205 -> 0.0167 ms, 2^22: 0.027 -> 0.021, 2^24: equal);
+// for vectors larger than L2 its barrier waits cost more than the extra plain
+// pass (2^26: 0.25 -> 0.30 ms), so it serves n <= 2^24 only.
+constexpr int kClusterMaxBits = 24;
+
+// Launches the cluster pass with 2^RB-CTA clusters and sets *launched; where
+// clusters of that size cannot be scheduled on this device (probed once) it
+// launches nothing and returns GAR_OK with *launched false, and the caller
+// takes the plain passes instead.
+template <int RB>
+int launch_cluster_pass(const RhtParams &p, unsigned blocks, cudaStream_t stream, bool *launched) {
+    static std::atomic<int> ok[64];  // 0: not probed, 1: schedulable, 2: not
+    int dev = 0;
+    *launched = false;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GAR_OK;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1u << RB;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int state = ok[dev].load(std::memory_order_relaxed);
+    if (state == 0) {
+        int clusters = 0;
+        bool good = true;
+        if (RB > 3)  // 16 CTAs: above the portable cluster size
+            good = cudaFuncSetAttribute(rht_cluster_pass_kernel<RB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                   cudaSuccess;
+        good = good && cudaOccupancyMaxActiveClusters(&clusters, rht_cluster_pass_kernel<RB>, &cfg) == cudaSuccess &&
+               clusters > 0;
+        cudaGetLastError();  // a refused probe leaves no error behind
+        state = good ? 1 : 2;
+        ok[dev].store(state, std::memory_order_relaxed);
+    }
+    if (state != 1) return GAR_OK;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, rht_cluster_pass_kernel<RB>, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(GAR_ECUDA, "rht_cluster_pass_kernel: %s", cudaGetErrorString(e));
+    }
+    *launched = true;
+    return check_launch("rht_cluster_pass_kernel");
 }
 
 // n < 4096: one CTA, every stage in shared memory.
@@ -383,9 +554,29 @@ extern "C" int gar_rht(const float *in, float *out, int64_t n, uint64_t seed, in
     p.last = k == 12 ? 1 : 0;
     rht_tile_kernel<<<blocks, kThreads, 0, stream>>>(p);
     int rc = check_launch("rht_tile_kernel");
-    // bits 12.. in passes of eight; a pass that would run past bit k-1 is
-    // moved down (s = k - 8) and skips the row bits already done
+    // bits 12..: for n <= 2^24, nine to twelve of them at once by a cluster
+    // pass where the clusters can be scheduled; else (and for the last eight
+    // or fewer) in passes of eight.  A plain pass that would run past bit k-1
+    // is moved down (s = k - 8) and skips the row bits already done.
     for (int done = 12; done < k && rc == GAR_OK;) {
+        const int left = k - done;
+        if (left > 8 && k <= kClusterMaxBits) {
+            const int rb = left >= 12 ? 4 : left - 8;
+            p.s = done;
+            p.lo_bit = 0;
+            p.last = done + 8 + rb >= k ? 1 : 0;
+            bool launched = false;
+            switch (rb) {
+                case 1: rc = launch_cluster_pass<1>(p, blocks, stream, &launched); break;
+                case 2: rc = launch_cluster_pass<2>(p, blocks, stream, &launched); break;
+                case 3: rc = launch_cluster_pass<3>(p, blocks, stream, &launched); break;
+                default: rc = launch_cluster_pass<4>(p, blocks, stream, &launched); break;
+            }
+            if (launched || rc != GAR_OK) {
+                done += 8 + rb;
+                continue;
+            }
+        }
         p.s = done < k - 8 ? done : k - 8;
         p.lo_bit = done - p.s;
         p.last = p.s + 8 >= k ? 1 : 0;

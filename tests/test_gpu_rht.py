@@ -50,8 +50,9 @@ def check_rht(got, x, seed, inverse):
 
 
 # k = 0..11 use the one-CTA kernel, 12 the tile kernel alone, 13..20 one strided
-# pass (moved down below bit 12 when fewer than eight bits remain), 21..23 two
-@pytest.mark.parametrize("k", [0, 1, 2, 5, 7, 11, 12, 13, 15, 16, 17, 19, 20, 21, 23])
+# pass (moved down below bit 12 when fewer than eight bits remain), 21..24 one
+# cluster pass of 2, 4, 8 or 16 CTAs (bits 12..k-1), 25 two strided passes
+@pytest.mark.parametrize("k", [0, 1, 2, 5, 7, 11, 12, 13, 15, 16, 17, 19, 20, 21, 22, 23, 24, 25])
 @pytest.mark.parametrize("inverse", [False, True])
 def test_rht_matches_oracle(env, k, inverse):
     torch, gar = env
@@ -62,7 +63,7 @@ def test_rht_matches_oracle(env, k, inverse):
     check_rht(to_host(out), x, 0xC0FFEE + k, inverse)
 
 
-@pytest.mark.parametrize("k", [12, 18, 22])
+@pytest.mark.parametrize("k", [12, 18, 22, 24])
 def test_rht_heavy_tailed_and_round_trip(env, k):
     torch, gar = env
     n = 1 << k
@@ -80,7 +81,7 @@ def test_rht_heavy_tailed_and_round_trip(env, k):
     assert abs(np.mean(yy ** 4) / np.mean(yy ** 2) ** 2 - 3.0) < 0.3
 
 
-@pytest.mark.parametrize("k", [3, 12, 16, 21])
+@pytest.mark.parametrize("k", [3, 12, 16, 21, 24])
 def test_rht_in_place_equals_out_of_place(env, k):
     torch, gar = env
     n = 1 << k
