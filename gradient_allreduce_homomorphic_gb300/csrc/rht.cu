@@ -485,6 +485,29 @@ int norm_blocks(int64_t n) {
     return static_cast<int>(b < 1 ? 1 : b);
 }
 
+// CTAs per worker of a launch: at most norm_blocks(n) (the workspace bound),
+// and at most one resident wave over all P workers, so that no SM idles in a
+// partial second wave (P=8, 2^24: 256 per worker were 1.7 waves).
+int norm_grid(int64_t n, int P) {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    int wave = kNormBlocksMax * 8;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+        wave = cached[dev].load(std::memory_order_relaxed);
+        if (wave == 0) {
+            int per_sm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rht_norm_partial, kThreads, 0) != cudaSuccess ||
+                per_sm < 1)
+                per_sm = 1;
+            wave = sm_count() * per_sm;
+            cached[dev].store(wave, std::memory_order_relaxed);
+        }
+    }
+    const int per_worker = wave / P > 1 ? wave / P : 1;
+    const int cap = norm_blocks(n);
+    return cap < per_worker ? cap : per_worker;
+}
+
 // ---------------------------------------------------------- error feedback
 // out = a + b (Sub = false) or a - b (Sub = true), one rounding each.
 template <bool Sub>
@@ -612,7 +635,7 @@ extern "C" int gar_rht_norm_range(const float *const *x, int32_t P, int64_t n, d
     p.mM = d_mM;
     p.n = n;
     p.P = P;
-    p.blocks = norm_blocks(n);
+    p.blocks = norm_grid(n, P);
     p.t_over_sqrt_n = t_p / std::sqrt(static_cast<double>(n));
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     rht_norm_partial<<<dim3(static_cast<unsigned>(p.blocks), static_cast<unsigned>(P)), kThreads, 0, stream>>>(p);
