@@ -342,10 +342,14 @@ __device__ __forceinline__ void nuhc_one_worker(const float4 (&v)[G4], float (&s
 // resident grid); else the interval tables (a larger g would not leave room
 // for the direct ones).  The grid-stride loop serves a resident grid and one
 // CTA per tile alike.
-template <int B, bool kPacked, bool kDirect>
+// kP > 0: built for exactly kP workers (the worker loop unrolls; pointers and
+// worker ids come from fixed parameter offsets); 0: any P.
+template <int B, bool kPacked, bool kDirect, int kP = 0>
 __global__ void __launch_bounds__(kThreads, B == 4 ? 4 : 1) nuhc_fused_kernel(const __grid_constant__ NuhcFusedParams p) {
     constexpr int E = 32 / B;
     constexpr int G4 = E / 4;
+    constexpr int kUnroll = kP > 0 ? kP : 1;
+    const int P = kP > 0 ? kP : p.P;
     extern __shared__ unsigned char s_mem[];
     float2 *s_pair;
     uint8_t *s_inv;
@@ -376,14 +380,15 @@ __global__ void __launch_bounds__(kThreads, B == 4 ? 4 : 1) nuhc_fused_kernel(co
             float4 va[G4], vb[G4];
 #pragma unroll
             for (int g4 = 0; g4 < G4; ++g4) va[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[0] + e0) + g4);
-            for (int wk = 0; wk < p.P; wk += 2) {
-                const bool has1 = wk + 1 < p.P;
+#pragma unroll(kUnroll)
+            for (int wk = 0; wk < P; wk += 2) {
+                const bool has1 = wk + 1 < P;
                 if (has1) {
 #pragma unroll
                     for (int g4 = 0; g4 < G4; ++g4) vb[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk + 1] + e0) + g4);
                 }
                 nuhc_one_worker<B, kPacked, kDirect>(va, s, e0, w, wk, p, m2, sc2, G, s_pair, s_inv);
-                if (wk + 2 < p.P) {
+                if (wk + 2 < P) {
 #pragma unroll
                     for (int g4 = 0; g4 < G4; ++g4) va[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk + 2] + e0) + g4);
                 }
@@ -415,6 +420,33 @@ __global__ void __launch_bounds__(kThreads, B == 4 ? 4 : 1) nuhc_fused_kernel(co
             }
             for (int i = 0; i < E && e0 + i < p.N; ++i) p.avg[e0 + i] = __fmaf_rn(s[i], k, km);
         }
+    }
+}
+
+// The fused kernel for one b and output kind.  b = 4 with the direct tables:
+// one CTA per 2 x kThreads words (the grid-stride loop runs twice; P=8,
+// 2^24: 0.190 -> 0.184 ms), and for 4, 8 or 16 workers the kernel built for
+// that P (0.184 -> 0.166 ms with wire vectors, 0.162 -> 0.150 without).  The
+// other widths, with 1.5 to 4 times the registers per thread or 8 words per
+// worker and thread, ran faster on a resident grid (b = 2, P = 16: 0.413 ms
+// resident, 0.440 ms one CTA per tile), and unrolling their worker loop
+// raised their registers further (b = 2, P = 16: 255 and spills).
+template <int BB, bool PK>
+void launch_nuhc_fused(const NuhcFusedParams &p, bool direct, int P, unsigned tiles, size_t smem,
+                       cudaStream_t stream) {
+    if (!direct) {
+        nuhc_fused_kernel<BB, PK, false><<<grid_for(nuhc_fused_kernel<BB, PK, false>, p.nwords), kThreads, smem,
+                                           stream>>>(p);
+    } else if constexpr (BB == 4) {
+        switch (P) {
+            case 4: nuhc_fused_kernel<BB, PK, true, 4><<<tiles, kThreads, smem, stream>>>(p); break;
+            case 8: nuhc_fused_kernel<BB, PK, true, 8><<<tiles, kThreads, smem, stream>>>(p); break;
+            case 16: nuhc_fused_kernel<BB, PK, true, 16><<<tiles, kThreads, smem, stream>>>(p); break;
+            default: nuhc_fused_kernel<BB, PK, true><<<tiles, kThreads, smem, stream>>>(p); break;
+        }
+    } else {
+        nuhc_fused_kernel<BB, PK, true><<<grid_for(nuhc_fused_kernel<BB, PK, true>, p.nwords), kThreads, smem,
+                                          stream>>>(p);
     }
 }
 
@@ -560,21 +592,8 @@ extern "C" int gar_nuhc_allreduce_fused(const float *const *x, int32_t P, int64_
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     const bool direct = g <= kDirectMaxG;
     const size_t smem = direct ? kDirectBytes : kNuhcPairBytes + static_cast<size_t>(g);
-    // b = 4 with the direct tables: one CTA per 2 x kThreads words (the
-    // grid-stride loop runs twice; P=8, 2^24: 0.190 -> 0.184 ms); the other
-    // widths, with 1.5 to 4 times the registers per thread or 8 words per
-    // worker and thread, ran faster on a resident grid (b = 2, P = 16:
-    // 0.413 ms resident, 0.440 ms one CTA per tile)
     const unsigned tiles = static_cast<unsigned>(ceil_div(p.nwords, int64_t{2 * kThreads}));
-#define GAR_NUHC_LAUNCH(BB, PK)                                                                          \
-    if (direct && BB == 4)                                                                               \
-        nuhc_fused_kernel<BB, PK, true><<<tiles, kThreads, smem, stream>>>(p);                           \
-    else if (direct)                                                                                     \
-        nuhc_fused_kernel<BB, PK, true><<<grid_for(nuhc_fused_kernel<BB, PK, true>, p.nwords), kThreads, \
-                                          smem, stream>>>(p);                                            \
-    else                                                                                                 \
-        nuhc_fused_kernel<BB, PK, false><<<grid_for(nuhc_fused_kernel<BB, PK, false>, p.nwords), kThreads, \
-                                           smem, stream>>>(p);
+#define GAR_NUHC_LAUNCH(BB, PK) launch_nuhc_fused<BB, PK>(p, direct, P, tiles, smem, stream);
 #define GAR_NUHC_CASE(BB)                 \
     case BB:                              \
         if (packed) {                     \
