@@ -1,0 +1,104 @@
+"""The averaging step captured in a CUDA graph: every call of the path is
+asynchronous on the caller's stream, allocates nothing and waits for nothing,
+so one step (the ring with each fusion buffer's THC range, THC b=4 over the
+plan, the wire-vector checksum and the NMSE) can be captured once and replayed.
+A replay must give the eager step's results bit for bit, and a replay after
+the inputs were overwritten in place must follow the new values."""
+import numpy as np
+import pytest
+
+import workloads
+from helpers import need_cuda
+
+pytestmark = pytest.mark.gpu
+
+P, B_THC, SEED = 8, 4, 0x5EED
+
+
+@pytest.fixture(scope="module")
+def env():
+    return need_cuda()
+
+
+def _setup(torch, g):
+    sizes = workloads.log_uniform_sizes(40, 256, 200_000, 1_000_000, [11, 999]).astype(np.int64)
+    dt = np.zeros(sizes.size, np.int32)
+    plan = g.gar_fusion_plan(sizes, dt, capacity_bytes=1 << 20, align_bytes=16)
+    n = int(sizes.sum())
+    flat_src = [torch.empty(n, device="cuda") for _ in range(P)]
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    src = [[f[offs[i]:offs[i + 1]] for i in range(sizes.size)] for f in flat_src]
+    flat_ring = [torch.empty(n, device="cuda") for _ in range(P)]
+    ring = [[f[offs[i]:offs[i + 1]] for i in range(sizes.size)] for f in flat_ring]
+    flat_thc = torch.empty(n, device="cuda")
+    thc = [flat_thc[offs[i]:offs[i + 1]] for i in range(sizes.size)]
+    st = dict(plan=plan, n=n, flat_src=flat_src, src=src, flat_ring=flat_ring, ring=ring, flat_thc=flat_thc, thc=thc)
+    st["mM"] = torch.empty((plan.n_buffers, 2), device="cuda")
+    st["ws"] = torch.empty(g.gar_nmse_workspace_bytes(n) // 8 + 1, dtype=torch.float64, device="cuda")
+    st["nmse"] = torch.empty(1, dtype=torch.float64, device="cuda")
+    st["ck"] = torch.empty(1, dtype=torch.int64, device="cuda")
+    return st
+
+
+def _fill(torch, st, seed):
+    for w, f in enumerate(st["flat_src"]):
+        f.copy_(torch.from_numpy(workloads.normal_f32(st["n"], 0.01, seed, w)))
+
+
+def _step(g, st):
+    g.gar_fused_allreduce_range(st["src"], st["ring"], st["plan"], st["mM"])
+    g.gar_thc_allreduce_fused_plan(st["src"], st["plan"], B_THC, SEED, st["mM"], st["thc"])
+    g.gar_checksum(st["flat_thc"], st["ck"])
+    g.gar_nmse(st["flat_ring"][0], st["flat_thc"], st["nmse"], st["ws"])
+
+
+def _results(st):
+    return ([f.cpu().numpy().view(np.uint32).copy() for f in st["flat_ring"]],
+            st["flat_thc"].cpu().numpy().view(np.uint32).copy(), st["mM"].cpu().numpy().view(np.uint32).copy(),
+            int(st["ck"].cpu().numpy()[0]), st["nmse"].cpu().numpy().view(np.uint64).copy())
+
+
+def _same(a, b):
+    for x, y in zip(a[0], b[0]):
+        assert np.array_equal(x, y), "ring average"
+    assert np.array_equal(a[1], b[1]), "THC average"
+    assert np.array_equal(a[2], b[2]), "THC range"
+    assert a[3] == b[3], "checksum"
+    assert np.array_equal(a[4], b[4]), "NMSE"
+
+
+def test_graph_replay_equals_eager(env):
+    torch, g = env
+    st = _setup(torch, g)
+    _fill(torch, st, 301)
+    _step(g, st)  # eager, also warms the library up before the capture
+    torch.cuda.synchronize()
+    eager = _results(st)
+
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            _step(g, st)
+    torch.cuda.synchronize()
+    for f in st["flat_ring"]:
+        f.zero_()
+    st["flat_thc"].zero_()
+    st["nmse"].zero_()
+    launches0 = g.gar_launch_count()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert g.gar_launch_count() == launches0  # a replay issues no library call
+    _same(_results(st), eager)
+
+    # new gradients written into the same buffers: the replay reads them
+    _fill(torch, st, 302)
+    _step(g, st)
+    torch.cuda.synchronize()
+    eager2 = _results(st)
+    assert not np.array_equal(eager2[1], eager[1])
+    _fill(torch, st, 302)
+    graph.replay()
+    torch.cuda.synchronize()
+    _same(_results(st), eager2)
