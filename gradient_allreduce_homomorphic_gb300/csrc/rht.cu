@@ -354,9 +354,12 @@ int launch_cluster_pass(const RhtParams &p, unsigned blocks, cudaStream_t stream
         if (RB > 3)  // 16 CTAs: above the portable cluster size
             good = cudaFuncSetAttribute(rht_cluster_pass_kernel<RB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
                    cudaSuccess;
-        good = good && cudaOccupancyMaxActiveClusters(&clusters, rht_cluster_pass_kernel<RB>, &cfg) == cudaSuccess &&
-               clusters > 0;
-        cudaGetLastError();  // a refused probe leaves no error behind
+        bool refused = !good;
+        if (good) {
+            refused = cudaOccupancyMaxActiveClusters(&clusters, rht_cluster_pass_kernel<RB>, &cfg) != cudaSuccess;
+            good = !refused && clusters > 0;
+        }
+        if (refused) cudaGetLastError();  // a refused probe leaves no error behind
         state = good ? 1 : 2;
         ok[dev].store(state, std::memory_order_relaxed);
     }
