@@ -30,9 +30,10 @@ CASES = [
     ("thc_range", []), ("thc_encode", []), ("thc_aggregate", []), ("thc_decode", []), ("thc_fused", []),
     ("thc_fused_packed", []), ("thc_plan", []), ("thc_plan_nmse", []), ("nuhc_fused", []),
     ("nuhc_fused_packed", []), ("nmse", []), ("rht", []), ("rht_inv", []), ("rht_norm", []), ("ef_apply", []),
+    ("checksum", ["--N", "268435456"]),
 ]
 LIB_KERNEL = re.compile(r"(ring_fold|ring_step|ring_divide|copy_jobs|pack_all|pack_range_init|range_reset|thc_|"
-                        r"nuhc_|nmse_|rht_|ef_kernel|dbtree_)")
+                        r"nuhc_|nmse_|rht_|ef_kernel|dbtree_|checksum_)")
 METRICS = "gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum"
 UNIT = {"ns": 1e-3, "us": 1.0, "usecond": 1.0, "nsecond": 1e-3, "ms": 1e3, "msecond": 1e3,
         "byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
