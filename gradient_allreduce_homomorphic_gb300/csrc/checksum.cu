@@ -1,8 +1,10 @@
 // checksum.cu -- checksum of a vector of 32-bit words, for silent-data-
 // corruption checks of THC's wire vectors (the packed indices a worker sends
 // and the parameter server receives): s1 = sum w_i and s2 = sum (i + 1) w_i,
-// both mod 2^32, returned as (s2 << 32) | s1.  A flipped bit changes s1,
-// two swapped words change s2.  Both sums are associative and commutative
+// both mod 2^32, returned as (s2 << 32) | s1.  A flipped bit changes s1; a
+// swap of words i and j changes s2 by (j - i)(w_i - w_j) mod 2^32, so it goes
+// unseen only when that product is 0 mod 2^32 (e.g. words 2^16 apart whose
+// values differ by a multiple of 2^16).  Both sums are associative and commutative
 // mod 2^32, so the CTAs' partial sums are added with atomics and the result
 // does not depend on the order.
 #include "common.cuh"

@@ -3,15 +3,25 @@
     python -m gradient_allreduce_homomorphic_gb300.kernel_table --out DIR [--cases c1,c2,...]
 
 For each microbench case (default: all of them) the case first runs on its
-own (it must exit 0), then once more under ``ncu --metrics
-gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum
---clock-control none`` (a few passes per launch, small inputs: each case
-holds at most a few GB).  Of the library's launches the last
-``launches_per_call`` are the timed call; their summed ncu duration gives the
-call's algorithmic GB/s (the case's algorithmic bytes over that time), and
-their DRAM bytes the traffic.  ncu runs every launch alone with cold caches,
-so the durations are serialised, cold-cache figures.  Writes DIR/<case>.csv
-(ncu's rows) and prints one markdown table.
+own (it must exit 0; it reports how many launches the library made in all
+and how many one timed call makes).  Then two ncu runs, both restricted to
+the library's kernels (``-k regex:``) and with ``--clock-control none``:
+
+1. durations: ``--metrics gpu__time_duration.sum`` (one pass per launch,
+   nothing saved or restored), skipping to the timed call (``-s``) and
+   capturing its launches (``-c``);
+2. DRAM traffic: ``dram__bytes_read.sum,dram__bytes_write.sum`` on at most
+   the first three launches of the timed call (``-s``, ``-c`` <= 3), inputs
+   of a few GB at most.  Where the call makes more than three launches the
+   traffic column covers only those and is left out of the ratio.
+
+The timed call's summed ncu duration gives its algorithmic GB/s (the case's
+algorithmic bytes over that time).  ncu runs every launch alone with cold
+caches, so the durations are serialised, cold-cache figures.  The peak is
+the measured copy rate (MEASURED_PEAKS.json), not a bound: a kernel that
+leaves part of its writes in L2 reads a little above 1.0.  Writes
+DIR/<case>_time.csv and DIR/<case>_dram.csv (ncu's rows) and prints one
+markdown table.
 """
 from __future__ import annotations
 
@@ -34,7 +44,10 @@ CASES = [
 ]
 LIB_KERNEL = re.compile(r"(ring_fold|ring_step|ring_divide|copy_jobs|pack_all|pack_range_init|range_reset|thc_|"
                         r"nuhc_|nmse_|rht_|ef_kernel|dbtree_|checksum_)")
-METRICS = "gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum"
+TIME_METRICS = "gpu__time_duration.sum"
+DRAM_METRICS = "dram__bytes_read.sum,dram__bytes_write.sum"
+KERNEL_FILTER = "regex:" + LIB_KERNEL.pattern
+MAX_DRAM_LAUNCHES = 3
 UNIT = {"ns": 1e-3, "us": 1.0, "usecond": 1.0, "nsecond": 1e-3, "ms": 1e3, "msecond": 1e3,
         "byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
 
@@ -88,20 +101,34 @@ def main(argv=None):
             rows.append((tag, "plain run failed", plain.stderr.strip().splitlines()[-1:]))
             continue
         info = json.loads(plain.stdout.strip().splitlines()[-1])
-        log = os.path.join(a.out, tag + ".csv")
-        prof = subprocess.run(["ncu", "--metrics", METRICS, "--clock-control", "none", "--csv", "--log-file", log,
-                               *cmd], capture_output=True, text=True)
-        if prof.returncode != 0:
-            rows.append((tag, "ncu run failed", prof.stderr.strip().splitlines()[-1:]))
+        per_call, total = info["launches_per_call"], info["launches_total"]
+        if per_call < 1:
+            rows.append((tag, "no library launch in the timed call", []))
             continue
-        lib = [(n, m) for n, m in _launches(log) if LIB_KERNEL.search(n)]
-        timed = lib[-info["launches_per_call"]:] if info["launches_per_call"] else []
+        skip = total - per_call  # the timed call's launches are the library's last ones
+
+        def ncu(metrics, count, suffix):
+            log = os.path.join(a.out, f"{tag}_{suffix}.csv")
+            r = subprocess.run(["ncu", "--metrics", metrics, "--clock-control", "none", "-k", KERNEL_FILTER,
+                                "-s", str(skip), "-c", str(count), "--csv", "--log-file", log, *cmd],
+                               capture_output=True, text=True)
+            return (_launches(log), None) if r.returncode == 0 else (None, r.stderr.strip().splitlines()[-1:])
+
+        timed, err = ncu(TIME_METRICS, per_call, "time")
+        if err is not None:
+            rows.append((tag, "ncu run failed", err))
+            continue
+        n_dram = min(per_call, MAX_DRAM_LAUNCHES)
+        dram_l, err = ncu(DRAM_METRICS, n_dram, "dram")
+        dram = (sum(m.get("dram__bytes_read.sum", 0.0) + m.get("dram__bytes_write.sum", 0.0) for _, m in dram_l)
+                if dram_l else float("nan"))
+        whole = dram_l is not None and n_dram == per_call
         us = sum(m.get("gpu__time_duration.sum", 0.0) for _, m in timed)
-        dram = sum(m.get("dram__bytes_read.sum", 0.0) + m.get("dram__bytes_write.sum", 0.0) for _, m in timed)
         names = sorted({_base(n) for n, _ in timed})
         gbs = info["bytes"] / (us * 1e-6) / 1e9 if us else 0.0
         rows.append((tag, ", ".join(names), len(timed), us, info["bytes"], gbs, gbs / peak, dram,
-                     dram / info["bytes"] if info["bytes"] else 0.0, info["ms"] * 1e3))
+                     dram / info["bytes"] if whole and info["bytes"] else float("nan"), info["ms"] * 1e3,
+                     "" if whole else f" (first {n_dram} launches)"))
     print(f"| case | kernels | launches | ncu time (us) | algorithmic bytes | GB/s (ncu) | of peak "
           f"| DRAM bytes | DRAM / algorithmic | events (us) |")
     print("|---|---|---:|---:|---:|---:|---:|---:|---:|---:|")
@@ -109,7 +136,7 @@ def main(argv=None):
         if len(r) == 3:
             print(f"| {r[0]} | {r[1]}: {r[2]} | | | | | | | | |")
         else:
-            print(f"| {r[0]} | {r[1]} | {r[2]} | {r[3]:.1f} | {r[4]:,} | {r[5]:.0f} | {r[6]:.3f} | {r[7]:,.0f} "
+            print(f"| {r[0]} | {r[1]} | {r[2]} | {r[3]:.1f} | {r[4]:,} | {r[5]:.0f} | {r[6]:.3f} | {r[7]:,.0f}{r[10]} "
                   f"| {r[8]:.3f} | {r[9]:.1f} |")
 
 

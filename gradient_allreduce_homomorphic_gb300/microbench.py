@@ -232,7 +232,8 @@ def main(argv=None):
     ms = float(np.median(times))
     print(json.dumps({"case": a.case, "P": P, "N": N, "b": b, "dtype": a.dtype, "ms": round(ms, 4),
                       "ms_min": round(float(np.min(times)), 4), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
-                      "bytes": int(nbytes), "launches_per_call": int(launches)}))
+                      "bytes": int(nbytes), "launches_per_call": int(launches),
+                      "launches_total": int(g.gar_launch_count())}))
 
 
 if __name__ == "__main__":

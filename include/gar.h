@@ -200,9 +200,10 @@ int gar_fused_allreduce_range(const void *const *src, void *const *dst, int32_t 
  * s1 = sum w_i and s2 = sum (i + 1) w_i over the n 32-bit words d_words
  * (device, 4-byte aligned), both mod 2^32: a check against silent data
  * corruption of THC's wire vectors (a worker's packed indices as sent and
- * as the parameter server receives them).  A flipped bit changes s1, two
- * swapped words change s2; the value does not depend on the order of the
- * device's partial sums.  n = 0 gives 0.
+ * as the parameter server receives them).  A flipped bit changes s1; a swap
+ * of words i and j changes s2 unless (j - i)(w_i - w_j) = 0 mod 2^32 (e.g.
+ * words 2^16 apart whose values differ by a multiple of 2^16).  The value
+ * does not depend on the order of the device's partial sums.  n = 0 gives 0.
  * Errors: GAR_EINVAL (n < 0, NULL), GAR_EALIGN, GAR_ECUDA. */
 int gar_checksum(const uint32_t *d_words, int64_t n, uint64_t *d_out, gar_stream_t stream);
 
@@ -334,7 +335,7 @@ int gar_thc_aggregate(const uint32_t *const *packed, int32_t P, int64_t N, int32
 /* gar_thc_decode -- each worker's last step: the index sum divided by the
  * number of workers, mapped back onto the grid:
  *     avg[e] = fma(sums[e], ((M - m) / L) / P, m)      (fp32, one rounding
- * per operation; within 1e-6 (|m| + |M|) of the exact value).
+ * per operation; within 1e-6 max(|m|, |M|) of the exact value).
  *   sums  device, N uint16;  d_mM  device [m, M];  avg  device, N fp32
  * Errors: GAR_EINVAL, GAR_EALIGN, GAR_ECUDA. */
 int gar_thc_decode(const uint16_t *sums, int64_t N, const float *d_mM, int32_t b, int32_t P,
@@ -570,7 +571,10 @@ int gar_nmse_combine(const double *d_pairs, int32_t n, double *d_out, gar_stream
  * blocks; a size needing more partial sums than the array holds would be
  * rejected with GAR_EINVAL.  The first call on a device looks up that array's
  * device address (cudaGetSymbolAddress) with the device current; make that
- * first call before any stream capture.  All calls on a device share the
+ * first call before any stream capture.  The address is kept for the life of
+ * the process: after cudaDeviceReset() on a device the library's image is
+ * loaded anew and the kept address is stale, so do not call this entry point
+ * on that device again.  All calls on a device share the
  * array and it keeps the last call's contents (nothing in it needs to start
  * at zero); calls that overlap on the GPU, e.g. on two streams, race.
  * Errors: GAR_EINVAL (null, N < 0), GAR_EALIGN, GAR_ECUDA. */

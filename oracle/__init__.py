@@ -60,6 +60,7 @@ def _load():
                 "oracle_ring_fold_f32_at": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, i64, vp]),
                 "oracle_bf16_to_f32": (C.c_float, [C.c_uint16]),
                 "oracle_f32_to_bf16": (C.c_uint16, [C.c_float]),
+                "oracle_f32_to_bf16_n": (None, [vp, i64, vp]),
                 "oracle_ring_fold_bf16": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, vp]),
                 "oracle_ring_fold_bf16_at": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, i64, vp]),
                 "oracle_ring_schedule_bf16": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, vp]),
@@ -243,6 +244,14 @@ def bf16_to_f32(h: int) -> float:
 
 def f32_to_bf16(f: float) -> int:
     return int(_load().oracle_f32_to_bf16(float(np.float32(f))))
+
+
+def f32_to_bf16_array(a) -> np.ndarray:
+    """f32_to_bf16 of every value of an fp32 array (bf16 bits as uint16)."""
+    a = np.ascontiguousarray(a, np.float32)
+    out = np.empty(a.size, np.uint16)
+    _load().oracle_f32_to_bf16_n(_ptr(a), a.size, _ptr(out))
+    return out
 
 
 # ------------------------------------------------------ double binary tree

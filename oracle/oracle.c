@@ -177,6 +177,11 @@ uint16_t oracle_f32_to_bf16(float f) {
     return (uint16_t)upper;
 }
 
+/* The same rounding over n values (out[k] = oracle_f32_to_bf16(in[k])). */
+void oracle_f32_to_bf16_n(const float *in, int64_t n, uint16_t *out) {
+    for (int64_t k = 0; k < n; ++k) out[k] = oracle_f32_to_bf16(in[k]);
+}
+
 static float fold_one_bf16(const uint16_t *const *x, int p, int64_t n, int op, int64_t k) {
     int c = (int)(k / oracle_ring_chunk_len(n, p));
     float s = oracle_bf16_to_f32(x[c][k]);

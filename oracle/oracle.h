@@ -70,6 +70,7 @@ int oracle_ring_fold_f32_at(const float *const *x, int p, int64_t n, int op,
  * out_f32 (may be NULL) receives the fp32 value before that rounding. */
 float oracle_bf16_to_f32(uint16_t h);
 uint16_t oracle_f32_to_bf16(float f);
+void oracle_f32_to_bf16_n(const float *in, int64_t n, uint16_t *out);
 int oracle_ring_fold_bf16(const uint16_t *const *x, int p, int64_t n, int op, uint16_t *out,
                           float *out_f32);
 int oracle_ring_fold_bf16_at(const uint16_t *const *x, int p, int64_t n, int op,
@@ -209,7 +210,9 @@ double oracle_nmse_f64(const double *x, const double *x_hat, int64_t n);
 /* Silent-data-corruption check of the packed indices (the survey's plan for
  * failure detection; the pages fix no checksum): s1 = sum w_i and
  * s2 = sum (i + 1) w_i over the n 32-bit words, both mod 2^32; returns
- * (s2 << 32) | s1.  s1 changes with any flipped bit, s2 with swapped words. */
+ * (s2 << 32) | s1.  s1 changes with any flipped bit; a swap of words i and j
+ * changes s2 by (j - i)(w_i - w_j) mod 2^32, so only swaps where that product
+ * is 0 mod 2^32 go unseen. */
 uint64_t oracle_checksum(const uint32_t *w, int64_t n);
 
 #ifdef __cplusplus

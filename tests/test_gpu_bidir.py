@@ -14,6 +14,7 @@ import pytest
 
 import oracle
 import workloads
+from oracle_par import bidir_fold_range_bf16
 from helpers import bf16_bits, need_cuda, same_bits, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
@@ -76,22 +77,22 @@ def test_bidir_order_golden(env, golden_dir):
         assert to_host(b).tolist() == d["sum"]
 
 
-def test_bidir_large_bf16_sampled(env):
-    # P=16, N = 2^28 bf16 per worker: sampled elements in both halves and at sub-chunk edges
+def test_bidir_large_bf16_full_size(env):
+    # P=16, N = 2^28 bf16 per worker, in place: every element against the
+    # oracle's two-ring fold (worker 0 on the host, every other worker equal
+    # to worker 0 on the device)
     torch, g = env
     P, N = 16, 1 << 28
     bufs = [workloads.device_normal(N, 1e-2, 6000 + w, torch.bfloat16, "cuda") for w in range(P)]
-    slen = -(-N // (2 * P))
-    edges = [k * slen + d for k in range(2 * P + 1) for d in (-1, 0, 1) if 0 <= k * slen + d < N]
-    idx = np.unique(np.concatenate([np.array(edges), np.random.default_rng(144).integers(0, N, 2048), [0, N - 1]]))
-    it = torch.from_numpy(idx).cuda()
-    vals = np.stack([to_host(b.index_select(0, it)) for b in bufs])
+    host = [to_host(b) for b in bufs]
     g.gar_ring_allreduce_bidir(bufs, op=g.GAR_AVG)
     torch.cuda.synchronize()
-    wide = (vals.astype(np.uint32) << 16).view(np.float32)  # exact widening
-    ref32 = oracle.bidir_fold_samples(wide, N, idx, op=oracle.AVG)
-    ref = np.array([oracle.f32_to_bf16(v) for v in ref32], np.uint16)
-    for w in (0, 7, 15):
-        same_bits(to_host(bufs[w].index_select(0, it)), ref)
+    for w in range(1, P):
+        assert torch.equal(bufs[w].view(torch.int16), bufs[0].view(torch.int16)), f"worker {w} differs from 0"
+    chunk = 1 << 24
+    for lo in range(0, N, chunk):
+        hi = min(N, lo + chunk)
+        ref = bidir_fold_range_bf16(np.stack([h[lo:hi] for h in host]), N, lo, op=oracle.AVG)
+        same_bits(to_host(bufs[0][lo:hi]), ref)
     del bufs
     torch.cuda.empty_cache()

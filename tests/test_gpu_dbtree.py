@@ -11,6 +11,7 @@ import pytest
 
 import oracle
 import workloads
+from oracle_par import dbtree_fold_range
 from helpers import bf16_bits, need_cuda, same_bits, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
@@ -110,22 +111,23 @@ def test_dbtree_f32_mid_size(env):
         same_bits(out[w], ref)
 
 
-def test_dbtree_large_bf16_sampled(env):
-    """P=16, N = 2^28 bf16 per worker (the launch the benchmark times):
-    sampled elements in both halves and around the split."""
+def test_dbtree_large_bf16_full_size(env):
+    """P=16, N = 2^28 bf16 per worker, in place (the launch the benchmark
+    times): every element against the oracle's two-tree fold (worker 0 on
+    the host, every other worker equal to worker 0 on the device)."""
     torch, g = env
     P, N = 16, 1 << 28
     bufs = [workloads.device_normal(N, 1e-2, 6100 + w, torch.bfloat16, "cuda") for w in range(P)]
-    h = (N + 1) // 2
-    idx = np.unique(np.concatenate([np.arange(h - 9, h + 9), np.random.default_rng(157).integers(0, N, 4096),
-                                    [0, 1, N - 2, N - 1]]))
-    it = torch.from_numpy(idx).cuda()
-    vals = np.stack([to_host(b.index_select(0, it)) for b in bufs])
+    host = [to_host(b) for b in bufs]
     g.gar_dbtree_allreduce(bufs, op=g.GAR_AVG)
     torch.cuda.synchronize()
-    ref = oracle.dbtree_fold_samples(vals, N, idx, op=oracle.AVG)
-    for w in (0, 5, 15):
-        same_bits(to_host(bufs[w].index_select(0, it)), ref)
+    for w in range(1, P):
+        assert torch.equal(bufs[w].view(torch.int16), bufs[0].view(torch.int16)), f"worker {w} differs from 0"
+    chunk = 1 << 24
+    for lo in range(0, N, chunk):
+        hi = min(N, lo + chunk)
+        ref = dbtree_fold_range(np.stack([h[lo:hi] for h in host]), N, lo, op=oracle.AVG)
+        same_bits(to_host(bufs[0][lo:hi]), ref)
     del bufs
     torch.cuda.empty_cache()
 

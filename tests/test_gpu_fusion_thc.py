@@ -16,6 +16,7 @@ import pytest
 import oracle
 import workloads
 from helpers import need_cuda, same_bits, to_dev, to_host
+from oracle_par import fusion_step
 
 pytestmark = pytest.mark.gpu
 
@@ -207,7 +208,11 @@ def test_thc_plan_against_oracle(env):
 
 
 def test_resnet_plan_full_size(env):
-    """The bench's workload: P=8, 300 tensors (45M parameters), b=4."""
+    """The bench's workload and kernel builds (the ring fold with the range,
+    the plan THC kernel built for 8 workers): P=8, 300 tensors (45M
+    parameters), b=4, against the oracle's pack -> ring fold / range / THC
+    round -> unpack over every value of every worker, and against the GPU's
+    own pack -> THC -> unpack composition."""
     torch, g = env
     P, b, seed = 8, 4, workloads.THC_SEED
     sizes = workloads.resnet_fusion_sizes()
@@ -218,14 +223,28 @@ def test_resnet_plan_full_size(env):
     mM = torch.empty((plan.n_buffers, 2), device="cuda")
     dst = [[torch.empty_like(t) for t in row] for row in src]
     g.gar_fused_allreduce_range(src, dst, plan, mM)
-    ref = _reference(g, torch, src, plan, b, seed)
-    same_bits(to_host(mM), to_host(ref[0]))
     out, pk = _plan_run(g, torch, src, plan, b, seed, mM)
+    torch.cuda.synchronize()
+    host = [[to_host(t) for t in row] for row in src]
+    sb, so, bn, per = fusion_step(host, sizes, 64 << 20, 16, b, seed)
+    assert np.array_equal(sb, plan.buffers()) and np.array_equal(so, plan.offsets())
+    got_mM = to_host(mM)
+    for k in range(len(bn)):
+        m, M = per[k]["mM"]
+        assert (got_mM[k, 0], got_mM[k, 1]) == (m, M)
+        ring = oracle.fusion_unpack(per[k]["ring"], sb, so, sizes, k)
+        tol = 1e-6 * max(abs(float(m)), abs(float(M)))
+        for i in np.nonzero(sb == k)[0]:
+            for w in range(P):
+                same_bits(to_host(dst[w][i]), ring[i])
+            ref = per[k]["thc"][int(so[i]):int(so[i]) + int(sizes[i])]
+            assert np.max(np.abs(to_host(out[i]).astype(np.float64) - ref), initial=0.0) <= tol
+        for w in range(P):
+            np.testing.assert_array_equal(to_host(pk[w][k])[: per[k]["packed"][w].size], per[k]["packed"][w])
+    ref = _reference(g, torch, src, plan, b, seed)
+    same_bits(got_mM, to_host(ref[0]))
     for i in range(plan.count):
         assert torch.equal(out[i].view(torch.int32), ref[1][i].view(torch.int32))
-    for w in range(P):
-        for bf in range(plan.n_buffers):
-            assert torch.equal(pk[w][bf], ref[2][w][bf])
 
 
 def _nmse_run(g, torch, src, plan, b, seed, mM, refs):

@@ -13,6 +13,7 @@ import pytest
 import oracle
 import workloads
 from helpers import need_cuda, to_dev, to_host
+from oracle_par import thc_range_parallel, thc_range_samples
 
 pytestmark = pytest.mark.gpu
 
@@ -179,32 +180,54 @@ def test_partition_4mb_full(env):
     assert abs(out.item() - ref) <= 2e-6 * ref
 
 
-@pytest.mark.parametrize("P", [4, 16, 64])
+@pytest.fixture(scope="module")
+def sweep_inputs(env):
+    """The THC sweep's gradients for one worker count at a time: N = 2^24
+    fp32 Student-t(3) x 1e-3 per worker, on the device and on the host."""
+    torch, g = env
+    cache = {}
+
+    def get(P):
+        if P not in cache:
+            cache.clear()
+            torch.cuda.empty_cache()
+            xd = [workloads.device_student_t(1 << 24, 3, 1e-3, 40_000 + 100 * P + w, "cuda") for w in range(P)]
+            cache[P] = (xd, [to_host(x) for x in xd])
+        return cache[P]
+
+    yield get
+    cache.clear()
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("b", [2, 4, 8])
-def test_thc_sweep_full_size_sampled(env, P, b):
-    # N = 2^24 fp32 Student-t(3) x 1e-3 per worker, shared [m, M]
+@pytest.mark.parametrize("P", [4, 16, 64])
+def test_thc_sweep_full_size(env, sweep_inputs, P, b):
+    # N = 2^24 per worker, shared [m, M]: the range, every worker's every
+    # index (through its wire words) and every averaged value against the
+    # oracle, in the launches the benchmark times
     torch, g = env
     N, seed = 1 << 24, workloads.THC_SEED
-    xd = [workloads.device_student_t(N, 3, 1e-3, 40_000 + 100 * P + w, "cuda") for w in range(P)]
+    xd, xh = sweep_inputs(P)
     mM = _run_range(torch, g, xd)
-    lo = min(float(x.min()) for x in xd)
-    hi = max(float(x.max()) for x in xd)
-    assert to_host(mM).tolist() == [np.float32(lo), np.float32(hi)]
+    m, M = thc_range_parallel(xh)
+    assert to_host(mM).tolist() == [m, M]
     avg = torch.empty(N, device="cuda")
     pk = _words(g, N, b, P, torch)
     g.gar_thc_allreduce_fused(xd, b, seed, mM, avg, pk)
-    idx = np.unique(np.concatenate([np.random.default_rng([95, P, b]).integers(0, N, 2048), [0, 1, N - 1]]))
-    it = torch.from_numpy(idx).cuda()
-    vals = np.stack([to_host(x.index_select(0, it)) for x in xd])
-    ref_idx, ref_avg = oracle.thc_allreduce_samples(vals, idx, b, seed, np.float32(lo), np.float32(hi))
-    per = 32 // b
-    wsel = torch.from_numpy(idx // per).cuda()
-    for w in range(P):
-        words = to_host(pk[w].index_select(0, wsel))
-        got = (words >> ((idx % per) * b).astype(np.uint32)) & np.uint32((1 << b) - 1)
-        np.testing.assert_array_equal(got, ref_idx[w])
-    tol = 1e-6 * max(abs(lo), abs(hi))
-    assert np.max(np.abs(to_host(avg.index_select(0, it)).astype(np.float64) - ref_avg)) <= tol
+    got_avg = to_host(avg).astype(np.float64)
+    got_pk = [to_host(t) for t in pk]
+    tol = 1e-6 * max(abs(float(m)), abs(float(M)))
+    chunk = 1 << 21
+    for lo in range(0, N, chunk):
+        hi = min(N, lo + chunk)
+        ref_idx, ref_avg = thc_range_samples(np.stack([x[lo:hi] for x in xh]), lo, b, seed, m, M)
+        w0, w1 = lo * b // 32, hi * b // 32
+        for w in range(P):
+            np.testing.assert_array_equal(oracle.thc_unpack(got_pk[w][w0:w1], hi - lo, b), ref_idx[w],
+                                          err_msg=f"worker {w}, elements {lo}..{hi}")
+        err = np.max(np.abs(got_avg[lo:hi] - ref_avg))
+        assert err <= tol, (lo, err, tol)
     # separate kernels agree with the fused one everywhere
     sums = torch.empty(N, dtype=torch.int16, device="cuda")
     g.gar_thc_aggregate(pk, N, b, sums)
@@ -214,7 +237,7 @@ def test_thc_sweep_full_size_sampled(env, P, b):
     enc = torch.empty_like(pk[P - 1])
     g.gar_thc_encode(xd[P - 1], mM, b, seed, P - 1, enc)
     assert torch.equal(enc, pk[P - 1])
-    del xd, pk
+    del pk
     torch.cuda.empty_cache()
 
 

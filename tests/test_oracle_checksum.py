@@ -29,7 +29,19 @@ def test_reveals_flips_and_swaps():
             v[i] ^= np.uint32(1 << bit)
             assert oracle.checksum(v) != c
     for i, j in rng.integers(0, w.size, (50, 2)):
-        if w[i] != w[j]:
-            v = w.copy()
-            v[i], v[j] = w[j], w[i]
-            assert oracle.checksum(v) != c
+        v = w.copy()
+        v[i], v[j] = w[j], w[i]
+        seen = ((int(j) - int(i)) * (int(w[i]) - int(w[j]))) % 2**32 != 0  # the change of s2
+        assert (oracle.checksum(v) != c) == seen
+
+
+def test_swap_blind_spot():
+    """A swap changes s2 by (j - i)(w_i - w_j) mod 2^32: words 2^16 apart whose
+    values differ by 2^16 swap unseen, as the definition says they must."""
+    w = np.zeros(1 << 17, np.uint32)
+    w[5], w[5 + (1 << 16)] = 7, 7 + (1 << 16)
+    v = w.copy()
+    v[5], v[5 + (1 << 16)] = w[5 + (1 << 16)], w[5]
+    assert oracle.checksum(v) == oracle.checksum(w)
+    v[5] += 1  # any other change to either word is seen
+    assert oracle.checksum(v) != oracle.checksum(w)

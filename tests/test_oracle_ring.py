@@ -157,6 +157,7 @@ def test_bf16_rounding_matches_torch():
     ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     ours = np.array([oracle.f32_to_bf16(v) for v in vals], np.uint16)
     np.testing.assert_array_equal(ours, ref)
+    np.testing.assert_array_equal(oracle.f32_to_bf16_array(vals), ref)
     assert np.isnan(oracle.bf16_to_f32(oracle.f32_to_bf16(np.float32("nan"))))
 
 
