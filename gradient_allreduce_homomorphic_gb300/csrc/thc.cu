@@ -9,12 +9,10 @@
 //
 // Index decision in fp32 (shared by encode and fused; one rounding per op):
 //   t = clamp((x - m) * sc, 0, L),  sc = L / (M - m)  (0 when M == m)
-//   floor: jm = t + 2^23 rounded down  ->  bits(jm) = 0x4B000000 + j, j = floor(t)
-//   up iff u < f = t - j with u = (r mod 2^23) / 2^23.  Since t is a float,
-//   j + u < t exactly iff (j + u rounded down) < t; j + u is formed as
-//   (jm - (2^23 + 1)) + (1 + u), where jm - (2^23 + 1) = j - 1 is exact and
-//   1 + u is the float with mantissa r mod 2^23.  The fused kernels read the
-//   comparison from the sign bit of the rounded difference, which is exact.
+//   up iff u < f = t - j, j = min(floor t, L - 1), u = (r mod 2^23) / 2^23,
+//   so the index is ceil(t - u).  It is formed as bits((t - (1 + u) rounded
+//   up) + 1.5 * 2^23 rounded up) - (bits(1.5 * 2^23) - 1), where 1 + u is the
+//   float with mantissa r mod 2^23 (see index_biased in thc_fused.cuh).
 // No integer<->float conversion is needed per element.
 #include <algorithm>
 #include <cstring>
@@ -196,7 +194,7 @@ __global__ void __launch_bounds__(kThreads) thc_encode_kernel(const __grid_const
             if (eb >= p.N) break;
             const uint4 r = philox_block(eb >> 2, p.worker, p.keys);
             for (int i = 0; i < 4 && eb + i < p.N; ++i) {
-                const uint32_t idx = index_biased(p.x[eb + i], m, sc, p.L, pick(r, i)) - 0x4B000000u;
+                const uint32_t idx = index_biased(p.x[eb + i], m, sc, p.L, pick(r, i)) - kIndexBias;
                 word |= idx << ((4 * g + i) * B);
             }
         }

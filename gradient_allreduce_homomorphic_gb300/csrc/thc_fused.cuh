@@ -49,15 +49,27 @@ __device__ __forceinline__ float range_scale(float m, float M, float L) {
     return (M == m) ? 0.0f : __fdiv_rn(L, __fsub_rn(M, m));
 }
 
-// Index of x given the Philox word r; returns bits(jm) + up, i.e. the index
-// plus 0x4B000000 (the caller subtracts the constant once per sum).
+// The index decision.  The grid position t = clamp((x - m) sc, 0, L) rounds
+// up to j + 1 iff u < f (j = min(floor t, L - 1), f = t - j, u the 23-bit
+// uniform), i.e. the index is ceil(t - u): for t < L, t - u = j + (f - u)
+// with f - u in (-1, 1), whose ceiling is j + [u < f]; for t = L it is L.
+// With 1 + u read as the float whose mantissa is the 23 random bits, two
+// additions rounded up give it without any int <-> float conversion:
+//   z = t - (1 + u), rounded up: ceil(z) = ceil(t - u) - 1, since rounding up
+//       never passes an integer (every integer below 2^24 is a float);
+//   z + 1.5 * 2^23, rounded up, lies in [2^23, 2^24), where the floats are
+//       the integers, so it equals 1.5 * 2^23 + ceil(z) exactly.
+// Its bit pattern is bits(1.5 * 2^23) + ceil(t - u) - 1: the index plus
+// kIndexBias.  Callers sum and pack the biased values and remove the bias
+// once per sum or word.
+constexpr uint32_t kIndexBias = 0x4B3FFFFFu;  // bits(1.5 * 2^23) - 1
+constexpr float kCeilMagic = 12582912.0f;     // 1.5 * 2^23
+
 __device__ __forceinline__ uint32_t index_biased(float x, float m, float sc, float L, uint32_t r) {
     float t = __fmul_rn(__fsub_rn(x, m), sc);
     t = fminf(fmaxf(t, 0.0f), L);
-    const float jm = __fadd_rd(t, 8388608.0f);
-    const float j_minus_1 = __fsub_rn(jm, 8388609.0f);
     const float one_u = __uint_as_float((r & 0x007FFFFFu) | 0x3F800000u);
-    return __float_as_uint(jm) + (__fadd_rd(j_minus_1, one_u) < t ? 1u : 0u);
+    return __float_as_uint(__fadd_ru(__fsub_ru(t, one_u), kCeilMagic));
 }
 
 // The same decision for two elements at once: the fp32 adds, subtracts and
@@ -90,24 +102,27 @@ __device__ __forceinline__ uint64_t add_rm_f2(uint64_t a, uint64_t b) {
     asm("add.rm.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+__device__ __forceinline__ uint64_t sub_rp_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rp.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_rp_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rp.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 
 __device__ __forceinline__ void index_biased2(float x0, float x1, uint64_t m2, uint64_t sc2, float L, uint32_t r0,
                                               uint32_t r1, uint32_t &a0, uint32_t &a1) {
     float2 t = unpack_f2(mul_rn_f2(sub_rn_f2(pack_f2(x0, x1), m2), sc2));
     t.x = fminf(fmaxf(t.x, 0.0f), L);
     t.y = fminf(fmaxf(t.y, 0.0f), L);
-    const uint64_t t2 = pack_f2(t.x, t.y);
-    const uint64_t jm = add_rm_f2(t2, pack_f2(8388608.0f, 8388608.0f));
-    const uint64_t j_minus_1 = sub_rn_f2(jm, pack_f2(8388609.0f, 8388609.0f));
     const uint64_t one_u = pack_f2(__uint_as_float((r0 & 0x007FFFFFu) | 0x3F800000u),
                                    __uint_as_float((r1 & 0x007FFFFFu) | 0x3F800000u));
-    // up iff c = (j - 1) + (1 + u) rounded down is below t: the sign of the
-    // rounded difference c - t, which is exact (a nonzero difference of two
-    // binary32 values never rounds to zero, and c == t gives +0)
-    const float2 diff = unpack_f2(sub_rn_f2(add_rm_f2(j_minus_1, one_u), t2));
-    const float2 j = unpack_f2(jm);
-    a0 = __float_as_uint(j.x) + (__float_as_uint(diff.x) >> 31);
-    a1 = __float_as_uint(j.y) + (__float_as_uint(diff.y) >> 31);
+    const float2 c = unpack_f2(add_rp_f2(sub_rp_f2(pack_f2(t.x, t.y), one_u), pack_f2(kCeilMagic, kCeilMagic)));
+    a0 = __float_as_uint(c.x);
+    a1 = __float_as_uint(c.y);
 }
 
 __device__ __forceinline__ uint4 philox_block(int64_t q, int worker, const PhiloxKeys &k) {
@@ -116,13 +131,13 @@ __device__ __forceinline__ uint4 philox_block(int64_t q, int worker, const Philo
                     k);
 }
 
-// Sum over the 32/B fields of a packed word of (0x4B000000 << field shift),
+// Sum over the 32/B fields of a packed word of (kIndexBias << field shift),
 // mod 2^32: packing the biased indices with plain shifted adds and removing
 // this once leaves the exact word (the fields never overlap).
 template <int B, int E = 32 / B>
 __host__ __device__ constexpr uint32_t pack_bias() {
     uint32_t s = 0;
-    for (int i = 0; i < E; ++i) s += 0x4B000000u << (i * B);
+    for (int i = 0; i < E; ++i) s += kIndexBias << (i * B);
     return s;
 }
 
@@ -161,7 +176,7 @@ struct FusedParams {
 struct Coder {
     float m, sc, k, km;
     uint64_t m2, sc2;  // (m, m) and (sc, sc) as f32x2 operands
-    uint32_t bias;     // P * 0x4B000000 (mod 2^32): removed once from each index sum
+    uint32_t bias;     // P * kIndexBias (mod 2^32): removed once from each index sum
 };
 
 template <class Prm>
@@ -170,7 +185,7 @@ __device__ __forceinline__ Coder make_coder(const Prm &p) {
     c.m = p.mM[0];
     c.sc = range_scale(c.m, p.mM[1], p.L);
     c.k = decode_step(p.mM, p.L, p.fp, c.km);
-    c.bias = static_cast<uint32_t>(p.P) * 0x4B000000u;
+    c.bias = static_cast<uint32_t>(p.P) * kIndexBias;
     c.m2 = pack_f2(c.m, c.m);
     c.sc2 = pack_f2(c.sc, c.sc);
     return c;
@@ -312,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_ker
                     for (int i = 0; i < 4 && eb + i < p.N; ++i) {
                         const uint32_t a = index_biased(p.x[wk][eb + i], c.m, c.sc, p.L, pick(r, i));
                         s[4 * g + i] += a;
-                        word |= (a - 0x4B000000u) << ((4 * g + i) * B);
+                        word |= (a - kIndexBias) << ((4 * g + i) * B);
                     }
                 }
                 if (kPacked) reinterpret_cast<UnitT<B> *>(p.packed[wk])[w] = static_cast<UnitT<B>>(word);
@@ -412,7 +427,7 @@ __device__ __noinline__ void plan_word_ragged(const ThcPlanParams &p, const Code
                 const float x = k < 0 ? 0.0f : p.src[k * p.P + wk][e - p.seg[k].begin];
                 const uint32_t a = index_biased(x, c.m, c.sc, p.L, pick(r, i));
                 s[4 * g + i] += a;
-                word |= (a - 0x4B000000u) << ((4 * g + i) * B);
+                word |= (a - kIndexBias) << ((4 * g + i) * B);
             }
         }
         if (kPacked) reinterpret_cast<UnitT<B> *>(p.packed[wk])[w] = static_cast<UnitT<B>>(word);
