@@ -703,6 +703,33 @@ def run_configs(args):
     del x, buf, packed, avg
     torch.cuda.empty_cache()
 
+    # C1 as THC runs it on a model: a stream of 64 partitions of 4 MB per
+    # worker, each its own fusion buffer with its own range, one call each for
+    # the ring (with the ranges) and for THC over the stream (1 GB of inputs)
+    k = 64
+    sizes = np.full(k, N, np.int64)
+    plan = g.gar_fusion_plan(sizes, np.zeros(k, np.int32), N * 4, ALIGN)
+    src = [[workloads.device_normal(N, 1.0, 100_000 * (w + 1) + i, torch.float32, dev) for i in range(k)]
+           for w in range(P)]
+    dst = [[torch.empty_like(t) for t in row] for row in src]
+    smM = torch.empty((k, 2), device=dev)
+    tabs = g.fused_pointer_tables(src, dst)
+    spk = [[torch.empty(words, dtype=torch.int32, device=dev) for _ in range(k)] for _ in range(P)]
+    stt = g.thc_plan_tables(src, dst[0], spk)
+    sring_ms = _median_ms(torch, lambda: g.gar_fused_allreduce_range(src, dst, plan, smM, tables=tabs), it)
+    sthc_ms = _median_ms(torch, lambda: g.gar_thc_allreduce_fused_plan(src, plan, 4, seed, smM, dst[0], tables=stt),
+                         it)
+    out.append({"config": "partition_4mb as a stream: P=4, 64 partitions of 2^20 fp32 N(0,1) per worker, each its "
+                          "own fusion buffer and range; ring average with the ranges, then THC b=4 over the stream",
+                "l2": "inputs (1 GB) larger than L2",
+                "gpu": {"ring": _gpu_line("gar_fused_allreduce_range over the 64 partitions", sring_ms,
+                                          2 * P * N * 4 * k, P * N * 4 * k, P * N * k, peak),
+                        "thc": _gpu_line("gar_thc_allreduce_fused_plan over the 64 partitions (wire vectors written)",
+                                         sthc_ms, (P * N * 4 + N * 4 + P * words * 4) * k, P * N * 4 * k, P * N * k,
+                                         peak)}})
+    del src, dst, spk, stt, tabs
+    torch.cuda.empty_cache()
+
     # C2: the main benchmark's workload and step (two streams)
     st = make_step(dev)
     for i in range(3):

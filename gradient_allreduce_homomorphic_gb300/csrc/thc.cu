@@ -376,13 +376,17 @@ __global__ void __launch_bounds__(kThreads) thc_nmse_pair_kernel(const double *w
 }
 
 // Upper bound on the CTAs (one pair each) all launches of one plan call run:
-// every piece adds at most one partial tile, a launch has at most 2 tensors + 1
-// pieces, and a buffer at most as many launches as tensors.
+// every piece adds at most one partial tile to the buffers' whole tiles.  A
+// span of k tensors makes at most 2 k + 1 pieces; the spans hold at most
+// count + S tensors in all (a tensor appears twice only across a span
+// boundary), and there are at most S <= count + 2 n_buffers spans (every
+// launch holds a tensor, and a buffer's last span may hold none), so at most
+// 5 count + 6 n_buffers pieces.
 int64_t plan_nmse_pairs_bound(const int64_t *buf_numel, int32_t n_buffers, int32_t count, int32_t b) {
     int64_t tiles = 0;
     for (int i = 0; i < n_buffers; ++i)
         tiles += ceil_div(thc_units(gar_thc_words(buf_numel[i] > 0 ? buf_numel[i] : 0, b), b), kPlanTileWords);
-    return tiles + 5 * static_cast<int64_t>(count) + 3 * static_cast<int64_t>(n_buffers) + 1;
+    return tiles + 5 * static_cast<int64_t>(count) + 6 * static_cast<int64_t>(n_buffers) + 1;
 }
 
 
@@ -579,48 +583,127 @@ extern "C" int gar_thc_allreduce_fused_masked(const float *const *x, int32_t P, 
 }
 
 // ------------------------------------------- fused over a Tensor Fusion plan
-// Pieces of the words [w_begin, w_end) of one launch over segments p.seg[0 ..
-// nseg) (sorted): per tensor, its whole words (vector or element-by-element
-// piece), and between them the words shared with a neighbour, a gap or the
-// buffer's end (looked-up piece).  At most 2 nseg + 1 pieces.  The
-// element-by-element pieces come first in tile order: a word of theirs costs
-// many times a vector word, and taking them in the first round of tiles
-// lets the vector tiles even out when the CTAs finish.
-static void plan_pieces(ThcPlanParams &p, const bool *vec, int E, int64_t w_begin, int64_t w_end) {
-    PlanPiece all[kPlanPieces];
-    int n = 0;
-    int64_t cur = w_begin;
-    auto add = [&](int64_t w0, int64_t w1, int seg, int kind) {
-        all[n].w0 = w0;
-        all[n].w1 = w1;
-        all[n].seg = seg;
-        all[n].kind = kind;
-        ++n;
-    };
-    for (int k = 0; k < p.nseg; ++k) {
-        const int64_t fw0 = std::max(ceil_div(p.seg[k].begin, E), w_begin);
-        const int64_t fw1 = std::min(p.seg[k].end / E, w_end);
-        if (fw0 >= fw1) continue;
-        if (cur < fw0) add(cur, fw0, -1, kPieceMixed);
-        add(fw0, fw1, k, vec[k] ? kPieceVec : kPieceTensor);
-        cur = fw1;
+// Builds the launches of one plan call.  A launch holds spans -- runs of
+// words [w0, w1) of one fusion buffer with every tensor meeting them -- of
+// as many buffers as its tables allow, so that many small buffers (a stream
+// of THC partitions, each with its own range) go out in one launch, and a
+// buffer with more tensors than one table holds is cut into several spans
+// over several launches.
+class PlanLaunches {
+  public:
+    PlanLaunches(ThcPlanParams &p, int P, int E, bool nmse, bool packed, double *ws, cudaStream_t stream, int b)
+        : p_(p), P_(P), E_(E), nmse_(nmse), packed_(packed), ws_(ws), stream_(stream), b_(b) {
+        reset();
     }
-    if (cur < w_end) add(cur, w_end, -1, kPieceMixed);
-    int m = 0;
-    int64_t tiles = 0;
-    for (int pass = 0; pass < 2; ++pass) {
-        for (int i = 0; i < n; ++i) {
-            if ((all[i].kind == kPieceVec) != (pass == 1)) continue;
-            p.piece[m] = all[i];
-            p.tile_start[m] = tiles;
-            tiles += ceil_div(all[i].w1 - all[i].w0, kPlanTileWords);
-            ++m;
+
+    // Tensors that one more span of this launch may hold (0: flush first).
+    int seg_room() const {
+        if (p_.nbuf >= kPlanBufs) return 0;
+        if (packed_ && (p_.nbuf + 1) * P_ > kPlanPkPtrs) return 0;
+        int room = std::min(kPlanSegs - p_.nseg, kPlanSrcPtrs / P_ - p_.nseg);
+        room = std::min(room, (kPlanPieces - nraw_ - 1) / 2);  // a span of k tensors makes at most 2 k + 1 pieces
+        return std::max(room, 0);
+    }
+    bool empty() const { return p_.nbuf == 0; }
+
+    // One span: words [w0, w1) of buffer `bf` (N elements, wire vectors pk[slot]) and its tensors
+    // idx[0 .. k) (plan order), with their source, output and reference pointers.
+    void add_span(int bf, int64_t N, int64_t w0, int64_t w1, uint32_t *const *pk, const int *idx, int k,
+                  const gar_seg *segs, const float *const *src, int32_t count, float *const *out,
+                  const float *const *ref) {
+        PlanBuf &B = p_.buf[p_.nbuf];
+        B.N = N;
+        B.id = bf;
+        B.seg_lo = static_cast<int16_t>(p_.nseg);
+        B.seg_hi = static_cast<int16_t>(p_.nseg + k);
+        B.pk = packed_ ? p_.nbuf * P_ : 0;
+        if (packed_)
+            for (int w = 0; w < P_; ++w) p_.packed[B.pk + w] = pk[w];
+        for (int j = 0; j < k; ++j) {
+            const int i = idx[j], ks = p_.nseg + j;
+            PlanSeg &sg = p_.seg[ks];
+            sg.begin = segs[i].offset;
+            sg.end = segs[i].offset + segs[i].numel;
+            bool v = (sg.begin % 4 == 0) && aligned(out[i], 16) && (!nmse_ || aligned(ref[i], 16));
+            for (int w = 0; w < P_; ++w) {
+                const float *sp = src[static_cast<int64_t>(w) * count + i];
+                p_.src[ks * P_ + w] = sp;
+                v = v && aligned(sp, 16);
+            }
+            vec_[ks] = v;
+            p_.out[ks] = out[i];
+            p_.ref[ks] = nmse_ ? ref[i] : nullptr;
         }
+        // pieces: per tensor its whole words, and the words between them
+        int64_t cur = w0;
+        const int16_t slot = static_cast<int16_t>(p_.nbuf);
+        auto add = [&](int64_t a, int64_t z, int seg, int kind) {
+            raw_[nraw_++] = PlanPiece{a, z, seg, static_cast<int16_t>(kind), slot};
+        };
+        for (int ks = B.seg_lo; ks < B.seg_hi; ++ks) {
+            const int64_t fw0 = std::max(ceil_div(p_.seg[ks].begin, E_), w0);
+            const int64_t fw1 = std::min(p_.seg[ks].end / E_, w1);
+            if (fw0 >= fw1) continue;
+            if (cur < fw0) add(cur, fw0, -1, kPieceMixed);
+            add(fw0, fw1, ks, vec_[ks] ? kPieceVec : kPieceTensor);
+            cur = fw1;
+        }
+        if (cur < w1) add(cur, w1, -1, kPieceMixed);
+        p_.nseg += k;
+        p_.nbuf += 1;
     }
-    p.npieces = m;
-    p.tile_start[m] = tiles;
-    p.total_tiles = tiles;
-}
+
+    // Launch what has been added.  The element-by-element pieces come first
+    // in tile order: a word of theirs costs many times a vector word, and
+    // taking them in the first round of tiles lets the vector tiles even out
+    // when the CTAs finish.
+    int flush() {
+        if (empty()) return GAR_OK;
+        int m = 0;
+        int64_t tiles = 0;
+        for (int pass = 0; pass < 2; ++pass) {
+            for (int i = 0; i < nraw_; ++i) {
+                if ((raw_[i].kind == kPieceVec) != (pass == 1)) continue;
+                p_.piece[m] = raw_[i];
+                p_.tile_start[m] = tiles;
+                tiles += ceil_div(raw_[i].w1 - raw_[i].w0, kPlanTileWords);
+                ++m;
+            }
+        }
+        p_.npieces = m;
+        p_.tile_start[m] = tiles;
+        p_.total_tiles = tiles;
+        int rc = GAR_OK;
+        if (tiles > 0) {
+            if (nmse_) p_.nmse_ws = ws_ + 2 * used_;
+            rc = dispatch_fused_plan(p_, b_, packed_, nmse_, stream_);
+            used_ += plan_grid(p_);
+        }
+        reset();
+        return rc;
+    }
+
+    int64_t used() const { return used_; }  // NMSE pairs written so far (one per CTA)
+
+  private:
+    void reset() {
+        p_.nseg = 0;
+        p_.nbuf = 0;
+        p_.npieces = 0;
+        p_.total_tiles = 0;
+        nraw_ = 0;
+    }
+    ThcPlanParams &p_;
+    int P_, E_;
+    bool nmse_, packed_;
+    double *ws_;
+    cudaStream_t stream_;
+    int b_;
+    int64_t used_ = 0;
+    bool vec_[kPlanSegs];
+    PlanPiece raw_[kPlanPieces];
+    int nraw_ = 0;
+};
 
 // Uniform THC over a plan; with ref != NULL also the NMSE pair of the call
 // (per-CTA pairs in ws, added by one more kernel into d_pair).
@@ -668,36 +751,35 @@ static int thc_plan_impl(const float *const *src, int32_t P, const gar_seg *segs
             return fail(ref[i] ? GAR_EALIGN : GAR_EINVAL, "reference %d NULL or not 4-byte aligned", i);
         members[sg.buffer].push_back(i);
     }
-    std::unique_ptr<ThcPlanParams> p(new ThcPlanParams);  // ~29 KB: keep it off the stack
+    std::vector<uint32_t *> pk(P, nullptr);
+    if (packed) {
+        for (int bf = 0; bf < n_buffers; ++bf) {
+            if (members[bf].empty()) continue;
+            for (int w = 0; w < P; ++w) {
+                uint32_t *q = packed[static_cast<int64_t>(w) * n_buffers + bf];
+                if (!q || !aligned(q, 4))
+                    return fail(q ? GAR_EALIGN : GAR_EINVAL, "packed vector of worker %d buffer %d NULL or misaligned", w, bf);
+            }
+        }
+    }
+    std::unique_ptr<ThcPlanParams> p(new ThcPlanParams);  // ~30 KB: keep it off the stack
     std::memset(p.get(), 0, sizeof(ThcPlanParams));
     p->keys = philox_keys(seed);
     p->P = P;
     p->L = static_cast<float>((1 << b) - 1);
     p->fp = static_cast<float>(P);
+    p->mM = d_mM;
     for (int w = 0; w < P; ++w) p->wid[w] = w;
-    const int E = unit_elems_of(b);                     // elements of a unit of work
-    const int cap = std::min(kPlanSegs, kPlanPtrs / P);  // >= 32 >= E: a unit meets at most E tensors
-    bool vec[kPlanSegs];
+    const int E = unit_elems_of(b);  // elements of a unit of work
+    std::unique_ptr<PlanLaunches> L(new PlanLaunches(*p, P, E, nmse, packed != nullptr, ws, stream, b));
     int rc = GAR_OK;
-    int64_t used = 0;  // NMSE pairs written so far (one per CTA)
     for (int bf = 0; bf < n_buffers && rc == GAR_OK; ++bf) {
         const std::vector<int> &mem = members[bf];
         if (mem.empty()) continue;
-        p->mM = d_mM + 2 * bf;
-        p->N = buf_numel[bf];
-        for (int w = 0; w < P; ++w) {
-            if (packed) {
-                uint32_t *pk = packed[static_cast<int64_t>(w) * n_buffers + bf];
-                if (!pk || !aligned(pk, 4)) {
-                    rc = fail(pk ? GAR_EALIGN : GAR_EINVAL, "packed vector of worker %d buffer %d NULL or misaligned", w, bf);
-                    break;
-                }
-                p->packed[w] = pk;
-            }
-        }
-        if (rc) break;
-        const int64_t nwords = thc_units(gar_thc_words(p->N, b), b);  // in units
-        // launches over consecutive word ranges; each one's table holds every
+        if (packed)
+            for (int w = 0; w < P; ++w) pk[w] = packed[static_cast<int64_t>(w) * n_buffers + bf];
+        const int64_t nwords = thc_units(gar_thc_words(buf_numel[bf], b), b);  // in units
+        // spans over consecutive word ranges; each one's table holds every
         // tensor that meets its words (those before `lo` end before them, those
         // from `hi` on begin after them)
         int lo = 0;
@@ -705,37 +787,28 @@ static int thc_plan_impl(const float *const *src, int32_t P, const gar_seg *segs
         const int n = static_cast<int>(mem.size());
         while (w0 < nwords && rc == GAR_OK) {
             while (lo < n && segs[mem[lo]].offset + segs[mem[lo]].numel <= w0 * E) ++lo;
-            const int hi = std::min(lo + cap, n);
+            const int room = L->seg_room();
+            if (room == 0) {  // this launch's tables are full (never the case for an empty one)
+                rc = L->flush();
+                continue;
+            }
+            const int hi = std::min(lo + room, n);
             const int64_t w1 = hi == n ? nwords : segs[mem[hi]].offset / E;
             if (w1 <= w0) {
-                rc = fail(GAR_EINVAL, "more than %d tensors meet one unit of buffer %d", cap, bf);
+                if (!L->empty()) {  // a fresh launch has room for more tensors
+                    rc = L->flush();
+                    continue;
+                }
+                rc = fail(GAR_EINVAL, "more than %d tensors meet one unit of buffer %d", room, bf);
                 break;
             }
-            p->nseg = hi - lo;
-            for (int k = 0; k < p->nseg; ++k) {
-                const int i = mem[lo + k];
-                PlanSeg &sg = p->seg[k];
-                sg.begin = segs[i].offset;
-                sg.end = segs[i].offset + segs[i].numel;
-                bool v = (sg.begin % 4 == 0) && aligned(out[i], 16) && (!nmse || aligned(ref[i], 16));
-                for (int w = 0; w < P; ++w) {
-                    const float *sp = src[static_cast<int64_t>(w) * count + i];
-                    p->src[k * P + w] = sp;
-                    v = v && aligned(sp, 16);
-                }
-                vec[k] = v;
-                p->out[k] = out[i];
-                p->ref[k] = nmse ? ref[i] : nullptr;
-            }
-            plan_pieces(*p, vec, E, w0, w1);
-            if (nmse) p->nmse_ws = ws + 2 * used;
-            rc = dispatch_fused_plan(*p, b, packed != nullptr, nmse, stream);
-            if (p->total_tiles > 0) used += plan_grid(*p);
+            L->add_span(bf, buf_numel[bf], w0, w1, pk.data(), mem.data() + lo, hi - lo, segs, src, count, out, ref);
             w0 = w1;
         }
     }
+    if (rc == GAR_OK) rc = L->flush();
     if (rc == GAR_OK && nmse) {
-        thc_nmse_pair_kernel<<<1, kThreads, 0, stream>>>(ws, used, d_pair);
+        thc_nmse_pair_kernel<<<1, kThreads, 0, stream>>>(ws, L->used(), d_pair);
         rc = check_launch("thc_nmse_pair_kernel");
     }
     return rc;

@@ -179,23 +179,26 @@ struct Coder {
     uint32_t bias;     // P * kIndexBias (mod 2^32): removed once from each index sum
 };
 
-template <class Prm>
-__device__ __forceinline__ Coder make_coder(const Prm &p) {
+__device__ __forceinline__ Coder make_coder_at(const float *mM, float L, float fp, int P) {
     Coder c;
-    c.m = p.mM[0];
-    c.sc = range_scale(c.m, p.mM[1], p.L);
-    c.k = decode_step(p.mM, p.L, p.fp, c.km);
-    c.bias = static_cast<uint32_t>(p.P) * kIndexBias;
+    c.m = mM[0];
+    c.sc = range_scale(c.m, mM[1], L);
+    c.k = decode_step(mM, L, fp, c.km);
+    c.bias = static_cast<uint32_t>(P) * kIndexBias;
     c.m2 = pack_f2(c.m, c.m);
     c.sc2 = pack_f2(c.sc, c.sc);
     return c;
+}
+template <class Prm>
+__device__ __forceinline__ Coder make_coder(const Prm &p) {
+    return make_coder_at(p.mM, p.L, p.fp, p.P);
 }
 
 // One worker's contribution to a unit of E = 4G elements: Philox draws,
 // indices added to the running sums s, the packed slice stored if wanted.
 template <int B, bool kPacked, int G, class Prm>
 __device__ __forceinline__ void fused_one_worker(const float4 (&v)[G], uint32_t (&s)[4 * G], int64_t e0, int64_t w,
-                                                 int wk, const Prm &p, const Coder &c) {
+                                                 int wk, uint32_t *pk, const Prm &p, const Coder &c) {
     uint32_t word = 0;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -212,7 +215,7 @@ __device__ __forceinline__ void fused_one_worker(const float4 (&v)[G], uint32_t 
                     (a3 << ((4 * g + 3) * B));
     }
     if (kPacked)
-        __stcs(reinterpret_cast<UnitT<B> *>(p.packed[wk]) + w, static_cast<UnitT<B>>(word - pack_bias<B, 4 * G>()));
+        __stcs(reinterpret_cast<UnitT<B> *>(pk) + w, static_cast<UnitT<B>>(word - pack_bias<B, 4 * G>()));
 }
 
 template <int G>
@@ -252,8 +255,8 @@ __device__ __forceinline__ void nmse_terms4(const float4 &r, const float4 &a, fl
 // reference values of the same E elements) to acc.
 template <int B, bool kPacked, int kP = 0, bool kNmse = false, class Prm>
 __device__ __forceinline__ void fused_word_vec(const Prm &p, const Coder &c, const float *const *xs, int64_t xoff,
-                                               float *avg, int64_t w, const float *ref = nullptr,
-                                               NmseAcc *acc = nullptr) {
+                                               uint32_t *const *pks, float *avg, int64_t w,
+                                               const float *ref = nullptr, NmseAcc *acc = nullptr) {
     constexpr int E = unit_elems<B>();
     constexpr int G = E / 4;  // float4 groups (and Philox blocks) per unit
     const int P = kP > 0 ? kP : p.P;
@@ -271,9 +274,9 @@ __device__ __forceinline__ void fused_word_vec(const Prm &p, const Coder &c, con
             if (wk + 2 >= P) load_group(rv, ref);
         }
         if (has1) load_group(vb, xs[wk + 1] + xoff);
-        fused_one_worker<B, kPacked>(va, s, e0, w, wk, p, c);
+        fused_one_worker<B, kPacked>(va, s, e0, w, wk, kPacked ? pks[wk] : nullptr, p, c);
         if (wk + 2 < P) load_group(va, xs[wk + 2] + xoff);
-        if (has1) fused_one_worker<B, kPacked>(vb, s, e0, w, wk + 1, p, c);
+        if (has1) fused_one_worker<B, kPacked>(vb, s, e0, w, wk + 1, kPacked ? pks[wk + 1] : nullptr, p, c);
     }
     float4 *dst = reinterpret_cast<float4 *>(avg);
     float num = 0.0f, den = 0.0f;
@@ -313,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_ker
         if (w >= p.nunits) break;
         const int64_t e0 = w * E;
         if (p.vec && e0 + E <= p.N) {
-            fused_word_vec<B, kPacked, kP>(p, c, p.x, e0, p.avg + e0, w);
+            fused_word_vec<B, kPacked, kP>(p, c, p.x, e0, p.packed, p.avg + e0, w);
         } else {  // ragged last word, or unaligned inputs: element by element
             uint32_t s[E];
 #pragma unroll
@@ -350,14 +353,19 @@ __global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_ker
 // for bit.  The average of every tensor element goes straight to the output
 // tensor (the unpack); gap elements are not written anywhere.
 //
-// Work decomposition (made on the host): the launch's words are cut into
-// pieces -- runs of whole words inside one tensor (loaded with 16-byte
-// vectors when every pointer of the tensor is 16-byte aligned), and runs of
-// the words between them (a tensor's first and last word shared with a
-// neighbour or a gap, the buffer's ragged last word) taken element by
-// element.  Pieces are cut into tiles of kPlanTileWords words, one CTA per
-// tile; the piece of a tile is found once per tile, uniform over the CTA.
-constexpr int kPlanPtrs = 2048, kPlanSegs = 128, kPlanPieces = 2 * kPlanSegs + 1;
+// Work decomposition (made on the host): a launch covers runs of words
+// ("spans") of one or more fusion buffers, each with its own range and wire
+// vectors.  A span's words are cut into pieces -- runs of whole words inside
+// one tensor (loaded with 16-byte vectors when every pointer of the tensor is
+// 16-byte aligned), and runs of the words between them (a tensor's first and
+// last word shared with a neighbour or a gap, the buffer's ragged last word)
+// taken element by element.  Pieces are cut into tiles of kPlanTileWords
+// words, one CTA per tile; the piece of a tile, and so its buffer, range and
+// coder, is found once per tile, uniform over the CTA.  Several buffers in one
+// launch let a stream of small partitions (THC's 4 MB partitions, each with
+// its own range) fill the GPU in one launch.
+constexpr int kPlanSrcPtrs = 1792, kPlanPkPtrs = 256, kPlanSegs = 128, kPlanPieces = 2 * kPlanSegs + 1;
+constexpr int kPlanBufs = 64;
 // Words per tile: two per thread, so that the per-CTA set-up (the range's
 // divisions, the piece search) is paid once per 2 x P x E element-workers.
 constexpr int kPlanTileWords = 2 * kThreads;
@@ -369,35 +377,44 @@ struct PlanSeg {
 };
 
 struct PlanPiece {
-    int64_t w0, w1;  // words [w0, w1) of the buffer
+    int64_t w0, w1;  // words [w0, w1) of its buffer
     int32_t seg;     // the tensor holding every element of the words (kPieceVec, kPieceTensor), else -1
-    int32_t kind;    // kPieceVec: 16-byte vectors; kPieceTensor: one tensor, element by element;
+    int16_t kind;    // kPieceVec: 16-byte vectors; kPieceTensor: one tensor, element by element;
                      // kPieceMixed: each element looked up (tensor, gap or past the end)
+    int16_t buf;     // its span: p.buf[buf]
+};
+
+struct PlanBuf {
+    int64_t N;               // elements of the fusion buffer
+    int32_t id;              // the buffer's index in the plan: its range is mM[2 id], mM[2 id + 1]
+    int16_t seg_lo, seg_hi;  // the span's tensors: seg[seg_lo .. seg_hi), sorted by begin
+    int32_t pk;              // its wire vectors: packed[pk + slot] (packed launches)
+    int32_t pad;
 };
 
 struct ThcPlanParams {
     PhiloxKeys keys;
     int32_t wid[GAR_MAX_WORKERS];
-    uint32_t *packed[GAR_MAX_WORKERS];  // this buffer's wire vectors, all NULL when not wanted
-    const float *mM;                    // this buffer's [m, M]
-    int64_t N;                          // elements of the buffer
+    const float *mM;                         // the plan's ranges, two floats per fusion buffer
     int64_t total_tiles;
-    int32_t P, nseg, npieces, pad;
+    int32_t P, nseg, npieces, nbuf;
     float L, fp;
-    PlanSeg seg[kPlanSegs];                  // sorted, disjoint; every tensor meeting the launch's words
+    PlanBuf buf[kPlanBufs];
+    PlanSeg seg[kPlanSegs];                  // every tensor meeting the launch's words, by span
     float *out[kPlanSegs];                   // output tensor of each segment
     const float *ref[kPlanSegs];             // NMSE reference tensor of each segment (NMSE launches)
     double *nmse_ws;                         // NMSE launches: this launch's per-CTA pairs of sums
     int64_t tile_start[kPlanPieces + 1];     // first tile of each piece; [npieces] = total
     PlanPiece piece[kPlanPieces];
-    const float *src[kPlanPtrs];             // src[k * P + slot]: worker slot's tensor of segment k
+    const float *src[kPlanSrcPtrs];          // src[k * P + slot]: worker slot's tensor of segment k
+    uint32_t *packed[kPlanPkPtrs];           // packed[buf.pk + slot]: worker slot's wire vector of a span's buffer
 };
 static_assert(sizeof(ThcPlanParams) <= 32000, "plan parameters exceed the launch limit");
 
-// Segment holding buffer element e, or -1 in a gap.
-__device__ __forceinline__ int plan_find(const ThcPlanParams &p, int64_t e) {
-    int lo = 0, hi = p.nseg - 1;
-    if (hi < 0 || p.seg[0].begin > e) return -1;
+// Segment of buffer bf holding its element e, or -1 in a gap.
+__device__ __forceinline__ int plan_find(const ThcPlanParams &p, const PlanBuf &bf, int64_t e) {
+    int lo = bf.seg_lo, hi = bf.seg_hi - 1;
+    if (hi < lo || p.seg[lo].begin > e) return -1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (p.seg[mid].begin <= e) lo = mid;
@@ -409,7 +426,8 @@ __device__ __forceinline__ int plan_find(const ThcPlanParams &p, int64_t e) {
 // The buffer's ragged last unit (e0 + E > N), element by element: the
 // missing elements pack as zero bits and get no output.
 template <int B, bool kPacked, bool kNmse>
-__device__ __noinline__ void plan_word_ragged(const ThcPlanParams &p, const Coder &c, int64_t w, NmseAcc &acc) {
+__device__ __noinline__ void plan_word_ragged(const ThcPlanParams &p, const PlanBuf &bf, const Coder &c, int64_t w,
+                                              NmseAcc &acc) {
     constexpr int E = unit_elems<B>();
     constexpr int G = E / 4;
     const int64_t e0 = w * E;
@@ -419,22 +437,22 @@ __device__ __noinline__ void plan_word_ragged(const ThcPlanParams &p, const Code
         uint32_t word = 0;
         for (int g = 0; g < G; ++g) {
             const int64_t eb = e0 + 4 * g;
-            if (eb >= p.N) break;
+            if (eb >= bf.N) break;
             const uint4 r = philox_block(eb >> 2, p.wid[wk], p.keys);
-            for (int i = 0; i < 4 && eb + i < p.N; ++i) {
+            for (int i = 0; i < 4 && eb + i < bf.N; ++i) {
                 const int64_t e = eb + i;
-                const int k = plan_find(p, e);
+                const int k = plan_find(p, bf, e);
                 const float x = k < 0 ? 0.0f : p.src[k * p.P + wk][e - p.seg[k].begin];
                 const uint32_t a = index_biased(x, c.m, c.sc, p.L, pick(r, i));
                 s[4 * g + i] += a;
                 word |= (a - kIndexBias) << ((4 * g + i) * B);
             }
         }
-        if (kPacked) reinterpret_cast<UnitT<B> *>(p.packed[wk])[w] = static_cast<UnitT<B>>(word);
+        if (kPacked) reinterpret_cast<UnitT<B> *>(p.packed[bf.pk + wk])[w] = static_cast<UnitT<B>>(word);
     }
-    for (int i = 0; i < E && e0 + i < p.N; ++i) {
+    for (int i = 0; i < E && e0 + i < bf.N; ++i) {
         const int64_t e = e0 + i;
-        const int k = plan_find(p, e);
+        const int k = plan_find(p, bf, e);
         if (k < 0) continue;
         const float a = __fmaf_rn(small_to_float(s[i] - c.bias), c.k, c.km);
         p.out[k][e - p.seg[k].begin] = a;
@@ -453,8 +471,8 @@ __device__ __noinline__ void plan_word_ragged(const ThcPlanParams &p, const Code
 // then quantized as a vector word.  Kept out of line: it serves only the few
 // words at tensor ends and gaps, and the unaligned tensors.
 template <int B, bool kPacked, bool kNmse>
-__device__ __noinline__ void plan_word_gather(const ThcPlanParams &p, const Coder &c, int64_t w, int seg,
-                                              NmseAcc &acc) {
+__device__ __noinline__ void plan_word_gather(const ThcPlanParams &p, const PlanBuf &bf, const Coder &c, int64_t w,
+                                              int seg, NmseAcc &acc) {
     constexpr int E = unit_elems<B>();
     constexpr int G = E / 4;
     const int64_t e0 = w * E;
@@ -462,7 +480,7 @@ __device__ __noinline__ void plan_word_gather(const ThcPlanParams &p, const Code
     int64_t off[E];
 #pragma unroll
     for (int i = 0; i < E; ++i) {
-        const int k = seg >= 0 ? seg : plan_find(p, e0 + i);
+        const int k = seg >= 0 ? seg : plan_find(p, bf, e0 + i);
         ks[i] = k;
         off[i] = k >= 0 ? e0 + i - p.seg[k].begin : 0;
     }
@@ -476,7 +494,7 @@ __device__ __noinline__ void plan_word_gather(const ThcPlanParams &p, const Code
         float4 v[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) v[g] = make_float4(x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]);
-        fused_one_worker<B, kPacked>(v, s, e0, w, wk, p, c);
+        fused_one_worker<B, kPacked>(v, s, e0, w, wk, kPacked ? p.packed[bf.pk + wk] : nullptr, p, c);
     }
 #pragma unroll
     for (int i = 0; i < E; ++i) {
@@ -497,7 +515,7 @@ __device__ __noinline__ void plan_word_gather(const ThcPlanParams &p, const Code
 template <int B, bool kPacked, int kP, bool kNmse>
 __global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_plan_kernel(const __grid_constant__ ThcPlanParams p) {
     constexpr int E = unit_elems<B>();
-    const Coder c = make_coder(p);
+    const int P = kP > 0 ? kP : p.P;
     NmseAcc acc;
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         // the piece that owns tile t: largest i with tile_start[i] <= t (uniform per CTA)
@@ -508,6 +526,8 @@ __global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_pla
             else hi = mid - 1;
         }
         const PlanPiece pc = p.piece[lo];
+        const PlanBuf &bf = p.buf[pc.buf];
+        const Coder c = make_coder_at(p.mM + 2 * bf.id, p.L, p.fp, P);
         const int64_t w0 = pc.w0 + (t - p.tile_start[lo]) * kPlanTileWords + threadIdx.x;
 #pragma unroll 1
         for (int u = 0; u < kPlanTileWords / kThreads; ++u) {
@@ -515,12 +535,13 @@ __global__ void __launch_bounds__(kThreads, fused_min_blocks<B>()) thc_fused_pla
             if (w >= pc.w1) break;
             if (pc.kind == kPieceVec) {
                 const int64_t off = w * E - p.seg[pc.seg].begin;
-                fused_word_vec<B, kPacked, kP, kNmse>(p, c, p.src + pc.seg * p.P, off, p.out[pc.seg] + off, w,
-                                                      kNmse ? p.ref[pc.seg] + off : nullptr, &acc);
-            } else if ((w + 1) * E <= p.N) {
-                plan_word_gather<B, kPacked, kNmse>(p, c, w, pc.kind == kPieceTensor ? pc.seg : -1, acc);
+                fused_word_vec<B, kPacked, kP, kNmse>(p, c, p.src + pc.seg * P, off, p.packed + bf.pk,
+                                                      p.out[pc.seg] + off, w, kNmse ? p.ref[pc.seg] + off : nullptr,
+                                                      &acc);
+            } else if ((w + 1) * E <= bf.N) {
+                plan_word_gather<B, kPacked, kNmse>(p, bf, c, w, pc.kind == kPieceTensor ? pc.seg : -1, acc);
             } else {
-                plan_word_ragged<B, kPacked, kNmse>(p, c, w, acc);
+                plan_word_ragged<B, kPacked, kNmse>(p, bf, c, w, acc);
             }
         }
     }

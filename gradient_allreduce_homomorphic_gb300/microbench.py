@@ -4,7 +4,9 @@
            [--b 4] [--iters 20] [--warmup 3] [--dtype f32|bf16]
 
 Cases: ring (in-place ring all-reduce of P buffers), ring_out (reduce to one
-output), bidir (bidirectional dual ring), dbtree (double-binary-tree all-reduce), fused (plan-driven all-reduce of the 300-tensor ResNet-like model),
+output), stream_ring, stream_thc (a stream of --k partitions of N values per
+worker, each its own fusion buffer and range: the ring with the ranges, or
+THC with wire vectors, one call over the stream), bidir (bidirectional dual ring), dbtree (double-binary-tree all-reduce), fused (plan-driven all-reduce of the 300-tensor ResNet-like model),
 fused_range (the same into separate outputs, each buffer's THC range from the same reads), thc_plan
 (THC b-bit of every fusion buffer of that model read straight from the tensors, wire vectors written),
 thc_plan_nmse (the same with the NMSE sums against a reference taken in the pass),
@@ -45,6 +47,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--dtype", default="f32")
     ap.add_argument("--g", type=int, default=0, help="granularity for the nuhc cases")
+    ap.add_argument("--k", type=int, default=64, help="partitions of the stream cases")
     ap.add_argument("--flush", action="store_true",
                     help="write then read 256 MB (more than L2) before every timed call")
     a = ap.parse_args(argv)
@@ -77,6 +80,28 @@ def main(argv=None):
             t, o = g.pointer_table(x), g.pointer_table(out)
             fn = lambda: g.gar_ring_allreduce_sim_out(t, o)  # noqa: E731
             nbytes = P * N * es + N * es
+    elif a.case in ("stream_ring", "stream_thc"):
+        # a stream of k partitions of N fp32 per worker, each its own fusion
+        # buffer with its own range: the ring with the ranges (stream_ring),
+        # or THC b-bit of every partition with wire vectors (stream_thc), one
+        # call over the whole stream
+        sizes = np.full(a.k, N, np.int64)
+        plan = g.gar_fusion_plan(sizes, np.zeros(a.k, np.int32), N * 4, 16)
+        src = [[workloads.device_normal(N, 1.0, 3000 * w + i, torch.float32, dev) for i in range(a.k)]
+               for w in range(P)]
+        dst = [[torch.empty_like(t) for t in row] for row in src]
+        mM = torch.empty((a.k, 2), device=dev)
+        tables = g.fused_pointer_tables(src, dst)
+        g.gar_fused_allreduce_range(src, dst, plan, mM, tables=tables)
+        if a.case == "stream_ring":
+            fn = lambda: g.gar_fused_allreduce_range(src, dst, plan, mM, tables=tables)  # noqa: E731
+            nbytes = 2 * P * N * 4 * a.k
+        else:
+            words = g.gar_thc_words(N, b)
+            packed = [[torch.empty(words, dtype=torch.int32, device=dev) for _ in range(a.k)] for _ in range(P)]
+            tt = g.thc_plan_tables(src, dst[0], packed)
+            fn = lambda: g.gar_thc_allreduce_fused_plan(src, plan, b, 5, mM, dst[0], tables=tt)  # noqa: E731
+            nbytes = (P * N * 4 + N * 4 + P * words * 4) * a.k
     elif a.case in ("fused", "fused_range", "thc_plan", "thc_plan_nmse", "pack", "unpack", "pack_all",
                     "pack_all_range"):
         sizes = workloads.resnet_fusion_sizes()

@@ -333,3 +333,41 @@ def test_thc_plan_nmse_edges(env):
     mM = torch.zeros((plan.n_buffers, 2), device="cuda")
     with pytest.raises(g.GarError):  # workspace too small
         g.gar_thc_allreduce_fused_plan_nmse(src, plan, 4, 1, mM, out, refs, pair, ws[:1])
+
+
+@pytest.mark.parametrize("P,b,k", [(4, 4, 64), (8, 2, 40), (64, 4, 9), (3, 8, 70)])
+def test_partition_stream(env, P, b, k):
+    """A stream of THC partitions ([T] section 2: the model cut into 4 MB
+    partitions, each with its own range), small here: k partitions per
+    worker, each its own fusion buffer, averaged by the ring with the range
+    and by THC over the plan -- several buffers per launch -- against the
+    oracle partition by partition."""
+    torch, g = env
+    rng = np.random.default_rng([151, P, b, k])
+    n = 4096
+    sizes = np.full(k, n, np.int64)
+    sizes[rng.integers(0, k, 3)] = [1, 4093, 777]  # a few ragged partitions
+    dt = np.zeros(k, np.int32)
+    plan = g.gar_fusion_plan(sizes, dt, n * 4, 16)
+    assert plan.n_buffers == k
+    host = [[(rng.standard_normal(int(s)) * rng.uniform(0.1, 10)).astype(np.float32) for s in sizes]
+            for _ in range(P)]
+    src = [[to_dev(x, torch) for x in row] for row in host]
+    ring = [[torch.empty_like(t) for t in row] for row in src]
+    mM = torch.full((k, 2), 7.0, device="cuda")
+    g.gar_fused_allreduce_range(src, ring, plan, mM)
+    seed = 0x5EED + k
+    out, pk = _plan_run(g, torch, src, plan, b, seed, mM)
+    torch.cuda.synchronize()
+    got_mM = to_host(mM)
+    for i in range(k):
+        xs = [host[w][i] for w in range(P)]
+        m, M = oracle.thc_range(xs)
+        assert (got_mM[i, 0], got_mM[i, 1]) == (m, M), i
+        for w in range(P):
+            same_bits(to_host(ring[w][i]), oracle.ring_fold(xs, op=oracle.AVG))
+        avg, ref_pk = oracle.thc_allreduce(xs, b, seed, m, M, want_packed=True)
+        for w in range(P):
+            np.testing.assert_array_equal(to_host(pk[w][i])[: ref_pk[w].size], ref_pk[w], err_msg=f"{i} {w}")
+        tol = 1e-6 * max(abs(float(m)), abs(float(M)))
+        assert np.max(np.abs(to_host(out[i]).astype(np.float64) - avg)) <= tol
