@@ -98,6 +98,8 @@ def _load():
                                             i64]),
                 "oracle_nuhc_encode": (C.c_int, [vp, i64, C.c_float, C.c_float, C.c_int, C.c_int, vp, u64,
                                                  C.c_int, vp]),
+                "oracle_nuhc_encode_at": (C.c_int, [vp, i64, i64, C.c_float, C.c_float, C.c_int, C.c_int, vp, u64,
+                                                    C.c_int, vp]),
                 "oracle_nuhc_aggregate": (C.c_int, [pp, C.c_int, i64, C.c_int, vp, vp]),
                 "oracle_nuhc_decode": (C.c_int, [vp, i64, C.c_float, C.c_float, C.c_int, C.c_int, vp]),
                 "oracle_rht_signs": (C.c_int, [i64, u64, vp]),
@@ -457,6 +459,16 @@ def nuhc_encode(x, m, M, b: int, g: int, table, seed: int, worker: int) -> np.nd
     out = np.empty(max(thc_words(x.size, b), 1), np.uint32)
     _check(_load().oracle_nuhc_encode(_ptr(x), x.size, float(m), float(M), b, g, _ptr(_table(table)), seed, worker,
                                       _ptr(out)), "nuhc_encode")
+    return out[:thc_words(x.size, b)]
+
+
+def nuhc_encode_at(x, e0: int, m, M, b: int, g: int, table, seed: int, worker: int) -> np.ndarray:
+    """nuhc_encode of elements e0 .. e0 + x.size - 1 of a longer vector (e0 a
+    multiple of 32 / b): that vector's packed words from word e0 / (32 / b) on."""
+    x = np.ascontiguousarray(x, np.float32)
+    out = np.empty(max(thc_words(x.size, b), 1), np.uint32)
+    _check(_load().oracle_nuhc_encode_at(_ptr(x), x.size, int(e0), float(m), float(M), b, g, _ptr(_table(table)),
+                                         seed, worker, _ptr(out)), "nuhc_encode_at")
     return out[:thc_words(x.size, b)]
 
 

@@ -883,6 +883,24 @@ int oracle_nuhc_encode(const float *x, int64_t n, float m, float M, int b, int g
     return 0;
 }
 
+/* The same encoding of a run of a longer vector: x[k] is element e0 + k
+ * (e0 a whole number of packed words into the vector), so the draws are
+ * those of the whole vector's encoding and packed[j] is its word
+ * e0 / (32 / b) + j. */
+int oracle_nuhc_encode_at(const float *x, int64_t n, int64_t e0, float m, float M, int b, int g,
+                          const uint16_t *table, uint64_t seed, int worker, uint32_t *packed) {
+    if (oracle_nuhc_check_table(table, b, g) != 0 || n < 0 || e0 < 0) return -1;
+    int per_word = 32 / b;
+    if (e0 % per_word != 0) return -1;
+    int64_t nwords = (n + per_word - 1) / per_word;
+    for (int64_t k = 0; k < nwords; ++k) packed[k] = 0u;
+    for (int64_t k = 0; k < n; ++k) {
+        uint32_t idx = oracle_nuhc_index(x[k], m, M, b, g, table, seed, worker, e0 + k);
+        packed[k / per_word] |= idx << ((k % per_word) * b);
+    }
+    return 0;
+}
+
 int oracle_nuhc_aggregate(const uint32_t *const *packed, int p, int64_t n, int b,
                           const uint16_t *table, uint16_t *sums) {
     if (!valid_bits(b) || n < 0 || p < 1) return -1;

@@ -177,6 +177,11 @@ uint32_t oracle_nuhc_index(float x, float m, float M, int b, int g, const uint16
 int oracle_nuhc_encode(const float *x, int64_t n, float m, float M, int b, int g,
                        const uint16_t *table, uint64_t seed, int worker, uint32_t *packed);
 /* the PS: sums[e] = sum over workers of table[index] */
+/* oracle_nuhc_encode of elements e0 .. e0 + n - 1 of a longer vector (x[k] =
+ * element e0 + k; e0 a multiple of 32 / b): the whole vector's words
+ * e0 / (32 / b) onwards. */
+int oracle_nuhc_encode_at(const float *x, int64_t n, int64_t e0, float m, float M, int b, int g,
+                          const uint16_t *table, uint64_t seed, int worker, uint32_t *packed);
 int oracle_nuhc_aggregate(const uint32_t *const *packed, int p, int64_t n, int b,
                           const uint16_t *table, uint16_t *sums);
 int oracle_nuhc_decode(const uint16_t *sums, int64_t n, float m, float M, int g, int p,

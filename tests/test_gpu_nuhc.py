@@ -4,7 +4,8 @@ Indices and table-value sums bit-exact; decoded averages within
 1e-6 * max(|m|, |M|) of the oracle's fp64 decode; the fused kernel equals
 decode(aggregate(encode)) bit for bit; the identity table with g = 2^b - 1
 equals the uniform THC kernels bit for bit; the page's T2 example; a
-full-size sampled run with the page's simulation setting (b = 4, g = 36).
+full-size run with the page's simulation setting (b = 4, g = 36), every
+element against the oracle.
 """
 import json
 import os
@@ -15,6 +16,7 @@ import pytest
 
 import oracle
 import workloads
+from oracle_par import pmap, runs, thc_range_parallel
 from helpers import need_cuda, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
@@ -138,33 +140,37 @@ def test_degenerate_and_errors(env):
 
 
 @pytest.mark.parametrize("P", [4, 16])
-def test_sweep_shape_full_size_sampled(env, P):
-    # N = 2^24 Student-t(3) x 1e-3, b = 4 with granularity 36 (the page's simulation setting)
+def test_sweep_shape_full_size(env, P):
+    # N = 2^24 Student-t(3) x 1e-3, b = 4 with granularity 36 (the page's
+    # simulation setting): every worker's every index (through its wire
+    # words) and every averaged value against the oracle
     torch, gar = env
     b, g, N, seed = 4, 36, 1 << 24, workloads.THC_SEED
     T = s_curve_table(b, g)
     xd = [workloads.device_student_t(N, 3, 1e-3, 50_000 + 100 * P + w, "cuda") for w in range(P)]
+    xh = [to_host(x) for x in xd]
     mM = torch.empty(2, device="cuda")
     gar.gar_thc_range(xd, mM)
-    lo = min(float(x.min()) for x in xd)
-    hi = max(float(x.max()) for x in xd)
+    m, M = thc_range_parallel(xh)
+    assert to_host(mM).tolist() == [m, M]
     avg = torch.empty(N, device="cuda")
     pk = _words(gar, N, b, P, torch)
     gar.gar_nuhc_allreduce_fused(xd, b, g, T, seed, mM, avg, pk)
-    idx = np.unique(np.concatenate([np.random.default_rng([123, P]).integers(0, N, 1024), [0, N - 1]]))
-    it = torch.from_numpy(idx).cuda()
-    vals = np.stack([to_host(x.index_select(0, it)) for x in xd])
+    got_avg = to_host(avg).astype(np.float64)
+    got_pk = [to_host(t) for t in pk]
+    tol = 1e-6 * max(abs(float(m)), abs(float(M)))
     per = 32 // b
-    wsel = torch.from_numpy(idx // per).cuda()
-    ref_idx = np.stack([[oracle.nuhc_index(vals[w, k], lo, hi, b, g, T, seed, w, int(idx[k])) for k in range(idx.size)]
-                        for w in range(P)])
-    for w in range(P):
-        words = to_host(pk[w].index_select(0, wsel))
-        got = (words >> ((idx % per) * b).astype(np.uint32)) & np.uint32((1 << b) - 1)
-        np.testing.assert_array_equal(got, ref_idx[w])
-    Y = T[ref_idx].astype(np.int64).sum(0)
-    ref_avg = float(np.float32(lo)) + Y / P * ((float(np.float32(hi)) - float(np.float32(lo))) / g)
-    got = to_host(avg.index_select(0, it)).astype(np.float64)
-    assert np.max(np.abs(got - ref_avg)) <= 1e-6 * max(abs(lo), abs(hi))
+    chunk = 1 << 20
+    for lo in range(0, N, chunk):
+        hi = min(N, lo + chunk)
+        runs_ = [(w, a, z) for w in range(P) for a, z in runs(lo, hi, 4)]
+        words = pmap(lambda r: (r, oracle.nuhc_encode_at(xh[r[0]][r[1]:r[2]], r[1], m, M, b, g, T, seed, r[0])),
+                     runs_)
+        ref_pk = [np.concatenate([wd for (w, a, z), wd in words if w == k]) for k in range(P)]
+        for w in range(P):
+            np.testing.assert_array_equal(got_pk[w][lo // per:hi // per], ref_pk[w], err_msg=f"worker {w} at {lo}")
+        ref_avg = oracle.nuhc_decode(oracle.nuhc_aggregate(ref_pk, hi - lo, b, T), m, M, g, P)
+        err = np.max(np.abs(got_avg[lo:hi] - ref_avg))
+        assert err <= tol, (lo, err, tol)
     del xd, pk
     torch.cuda.empty_cache()

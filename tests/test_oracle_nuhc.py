@@ -149,3 +149,30 @@ def test_aggregate_rejects_overflow():
     T[255] = 300
     with pytest.raises(ValueError):
         oracle.nuhc_aggregate([np.zeros(1, np.uint32)] * 220, 4, 8, T)  # 220 * 300 > 65535
+
+
+@pytest.mark.parametrize("b", [1, 2, 4, 8])
+def test_encode_at_is_the_whole_vectors_encoding(b):
+    """A run of a longer vector, encoded with its global element indices,
+    gives that vector's words; with the identity table its indices are the
+    uniform round's at those elements."""
+    L = (1 << b) - 1
+    g = 2 * L + 3
+    T = np.rint(np.linspace(0, g, L + 1)).astype(np.uint16)
+    N, w = 4099, 3
+    x = np.random.default_rng([112, b]).standard_normal(N).astype(np.float32)
+    m, M = oracle.thc_range([x])
+    full = oracle.nuhc_encode(x, m, M, b, g, T, 91, w)
+    per = 32 // b
+    for e0 in (0, per, 37 * per, N - N % per):
+        run = oracle.nuhc_encode_at(x[e0:], e0, m, M, b, g, T, 91, w)
+        np.testing.assert_array_equal(run, full[e0 // per:])
+    with pytest.raises(ValueError):  # a run must start on a word boundary
+        oracle.nuhc_encode_at(x[1:], 1, m, M, b, g, T, 91, w)
+    ident = np.arange(L + 1, dtype=np.uint16)
+    e0 = 64 * per
+    run = oracle.nuhc_encode_at(x[e0:e0 + 500], e0, m, M, b, L, ident, 91, w)
+    vals = np.zeros((w + 1, 500), np.float32)
+    vals[w] = x[e0:e0 + 500]
+    ind, _ = oracle.thc_allreduce_samples(vals, np.arange(e0, e0 + 500), b, 91, m, M)
+    np.testing.assert_array_equal(oracle.thc_unpack(run, 500, b), ind[w])
