@@ -78,6 +78,10 @@ _SIGNATURES = {
     "gar_rht": (C.c_int, [_vp, _vp, _i64, _u64, _i32, _vp]),
     "gar_rht_norm_range_workspace_bytes": (C.c_size_t, [_i32, _i64]),
     "gar_rht_norm_range": (C.c_int, [_pp, _i32, _i64, C.c_double, _vp, _vp, C.c_size_t, _vp]),
+    "gar_rht_tiles": (_i64, [_i64]),
+    "gar_rht_ef_forward": (C.c_int, [_vp, _vp, _vp, _i64, _u64, _vp, _vp]),
+    "gar_rht_norm_range_from_sums": (C.c_int, [_pp, _i32, _i64, C.c_double, _vp, _vp]),
+    "gar_rht_ef_update": (C.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i64, _u64, _vp]),
     "gar_ef_apply": (C.c_int, [_vp, _vp, _vp, _i64, _vp]),
     "gar_ef_update": (C.c_int, [_vp, _vp, _vp, _i64, _vp]),
     "gar_nmse_workspace_bytes": (C.c_size_t, [_i64]),
@@ -532,6 +536,32 @@ def gar_rht_norm_range(x, t_p: float, d_mM, workspace, stream=None):
     nbytes = workspace.numel() * workspace.element_size()
     _call("gar_rht_norm_range", t.array, len(t), t.numel, float(t_p), _dev(d_mM), _dev(workspace), nbytes,
           _stream(stream))
+
+
+def gar_rht_tiles(n: int) -> int:
+    return int(load().gar_rht_tiles(n))
+
+
+def gar_rht_ef_forward(grad, e, y, seed: int, sumsq=None, stream=None):
+    """y = (1/sqrt n) H D (grad + e); sumsq (fp64, gar_rht_tiles(n)) receives
+    the per-tile sums of squares of grad + e if given."""
+    _call("gar_rht_ef_forward", _dev(grad), _dev(e), _dev(y), grad.numel(), seed,
+          _dev(sumsq) if sumsq is not None else None, _stream(stream))
+
+
+def gar_rht_norm_range_from_sums(sumsq, n: int, t_p: float, d_mM, stream=None):
+    """The norm-based range from the workers' per-tile sums (a list of fp64 tensors)."""
+    t = pointer_table(sumsq)
+    _call("gar_rht_norm_range_from_sums", t.array, len(t), n, float(t_p), _dev(d_mM), _stream(stream))
+
+
+def gar_rht_ef_update(packed, b: int, steps: int, table, d_mM, grad, e, tmp, seed: int, stream=None):
+    """e = (grad + e) - (1/sqrt n) D H decode(packed); table None for uniform THC (steps = 2^b - 1)."""
+    tp = None
+    if table is not None:
+        t, tp = _table(table)
+    _call("gar_rht_ef_update", _dev(packed), b, steps, tp, _dev(d_mM), _dev(grad), _dev(e), _dev(tmp), e.numel(),
+          seed, _stream(stream))
 
 
 def gar_ef_apply(grad, e, x, stream=None):

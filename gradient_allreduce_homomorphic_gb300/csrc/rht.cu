@@ -26,6 +26,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <memory>
 
 #include "common.cuh"
 
@@ -72,30 +73,128 @@ struct RhtParams {
     int32_t s;        // pass: log2 of the row stride
     int32_t lo_bit;   // pass: row bits below this were done by an earlier launch
     float scale;      // 1/sqrt(n) rounded to fp32
+    // fused error feedback and decode (see the kIn / kEfOut kernel variants)
+    const float *grad;       // kInEf: the input is grad + in; kEfOut: e = (grad + e) - result
+    float *ef;               // kEfOut: the error vector e, read and rewritten
+    const uint32_t *packed;  // kInPacked: a worker's b-bit indices
+    const float *mM;         // kInPacked: their range [m, M]
+    double *sumsq;           // kNorm: one sum of squares of the input per tile
+    int32_t b;               // kInPacked: bits per index
+    int32_t has_tab;         // kInPacked: index z stands for tab[z] (non-uniform THC), else for z
+    float steps;             // kInPacked: grid steps between m and M (2^b - 1, or the granularity g)
+    int32_t pad;
+    uint16_t tab[256];       // kInPacked with has_tab: the table T
 };
+
+// What the first launch of a transform reads: the vector itself; grad + e
+// (error feedback applied on the way in); or a worker's packed indices,
+// decoded on the grid (its own quantized vector).
+constexpr int kInPlain = 0, kInEf = 1, kInPacked = 2;
+
+// Per-CTA set-up of the kInPacked decode: the table values as floats, and
+// the decode step (M - m) / steps divided by one worker, as the grid decode
+// takes them.
+struct Decoder {
+    float m, k;
+};
+__device__ __forceinline__ Decoder make_decoder(const RhtParams &p, float *s_tab) {
+    if (p.has_tab)
+        for (int z = threadIdx.x; z <= (1 << p.b) - 1; z += blockDim.x) s_tab[z] = static_cast<float>(p.tab[z]);
+    Decoder d;
+    d.m = p.mM[0];
+    d.k = __fdiv_rn(__fdiv_rn(__fsub_rn(p.mM[1], d.m), p.steps), 1.0f);
+    return d;
+}
+// The decoded value of index z: fma(S, k, m), S = tab[z] or z (exact floats).
+__device__ __forceinline__ float decode_one(const RhtParams &p, const Decoder &d, const float *s_tab, uint32_t z) {
+    const float S = p.has_tab ? s_tab[z] : static_cast<float>(z);
+    return __fmaf_rn(S, d.k, d.m);
+}
+// Elements e .. e + 3 (e a multiple of 4) decoded from the packed indices.
+__device__ __forceinline__ float4 decode4(const RhtParams &p, const Decoder &d, const float *s_tab, int64_t e) {
+    const int per = 32 / p.b;
+    const uint32_t w = __ldcs(p.packed + e / per);
+    const uint32_t mask = (1u << p.b) - 1u;
+    const int sh = static_cast<int>(e % per) * p.b;
+    return make_float4(decode_one(p, d, s_tab, (w >> sh) & mask), decode_one(p, d, s_tab, (w >> (sh + p.b)) & mask),
+                       decode_one(p, d, s_tab, (w >> (sh + 2 * p.b)) & mask),
+                       decode_one(p, d, s_tab, (w >> (sh + 3 * p.b)) & mask));
+}
+// e = (grad + e) - y for one element: the error-feedback update with x
+// recomputed as gar_ef_apply forms it.
+__device__ __forceinline__ void ef_out(const RhtParams &p, int64_t i, float y) {
+    p.ef[i] = __fsub_rn(__fadd_rn(__ldcs(p.grad + i), p.ef[i]), y);
+}
+
+// Sum of squares of a thread's 16 values (fp32, pairwise), added over the
+// CTA in fp64 in a fixed order; written by thread 0 to p.sumsq[tile].
+__device__ __forceinline__ void tile_sumsq(const RhtParams &p, const float (&v)[16], int64_t tile) {
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = __fadd_rn(__fmul_rn(v[2 * i], v[2 * i]), __fmul_rn(v[2 * i + 1], v[2 * i + 1]));
+    const float f = __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
+                              __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
+    double a = static_cast<double>(f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+    __shared__ double s_part[kThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) s_part[warp] = a;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+#pragma unroll
+        for (int i = 0; i < kThreads / 32; ++i) t += s_part[i];
+        p.sumsq[tile] = t;
+    }
+}
 
 // Tile shared-memory layout: element i of the tile lives at i ^ (bits 6..8
 // of i moved to bits 2..4).  Every warp access below then hits 32 distinct
 // banks, and 16-byte groups stay whole for the float4 stores.
 __device__ __forceinline__ int tile_swz(int i) { return i ^ (((i >> 6) & 7) << 2); }
 
-// Index bits 0..11 of every 4096-element tile.
+// Index bits 0..11 of every 4096-element tile.  kIn: what the tile reads
+// (the vector, grad + e, or packed indices to decode); kNorm: also the sum of
+// squares of what it read, per tile; kEfOut (with p.last): instead of the
+// result y, write e = (grad + e) - y.
+template <int kIn, bool kNorm, bool kEfOut>
 __global__ void __launch_bounds__(kThreads) rht_tile_kernel(const __grid_constant__ RhtParams p) {
     __shared__ __align__(16) float s[kTile];
     __shared__ uint32_t s_sign[kTile / 32];  // bit i: sign of tile element i (1 = negative)
+    __shared__ float s_tab[kIn == kInPacked ? 256 : 1];
     const int t = threadIdx.x;
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kTile;
-    const float4 *src = reinterpret_cast<const float4 *>(p.in + base);
     float v[16];
     // v[4q + j] = tile element (q << 10) | (t << 2) | j
+    if constexpr (kIn == kInPacked) {
+        const Decoder d = make_decoder(p, s_tab);
+        __syncthreads();
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float4 a = __ldcs(src + q * 256 + t);
-        v[4 * q] = a.x;
-        v[4 * q + 1] = a.y;
-        v[4 * q + 2] = a.z;
-        v[4 * q + 3] = a.w;
+        for (int q = 0; q < 4; ++q) {
+            const float4 a = decode4(p, d, s_tab, base + (q << 10) + (t << 2));
+            v[4 * q] = a.x;
+            v[4 * q + 1] = a.y;
+            v[4 * q + 2] = a.z;
+            v[4 * q + 3] = a.w;
+        }
+    } else {
+        const float4 *src = reinterpret_cast<const float4 *>(p.in + base);
+        const float4 *gsrc = reinterpret_cast<const float4 *>(kIn == kInEf ? p.grad + base : p.in + base);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float4 a = __ldcs(src + q * 256 + t);
+            if constexpr (kIn == kInEf) {  // x = grad + e, as gar_ef_apply forms it
+                const float4 gv = __ldcs(gsrc + q * 256 + t);
+                a = make_float4(__fadd_rn(gv.x, a.x), __fadd_rn(gv.y, a.y), __fadd_rn(gv.z, a.z), __fadd_rn(gv.w, a.w));
+            }
+            v[4 * q] = a.x;
+            v[4 * q + 1] = a.y;
+            v[4 * q + 2] = a.z;
+            v[4 * q + 3] = a.w;
+        }
     }
+    if constexpr (kNorm) tile_sumsq(p, v, blockIdx.x);
     const bool signs_in = !p.inverse;
     const bool signs_out = p.inverse && p.last;
     if (signs_in || signs_out) {
@@ -145,7 +244,8 @@ __global__ void __launch_bounds__(kThreads) rht_tile_kernel(const __grid_constan
             if (signs_out && ((s_sign[e >> 5] >> (e & 31)) & 1u)) y = -y;
             y = __fmul_rn(y, p.scale);
         }
-        if (p.last) __stcs(dst + e, y);
+        if (kEfOut && p.last) ef_out(p, base + e, y);
+        else if (p.last) __stcs(dst + e, y);
         else dst[e] = y;  // the next pass reads it: normal priority, so that it can stay in L2
     }
 }
@@ -156,6 +256,7 @@ __global__ void __launch_bounds__(kThreads) rht_tile_kernel(const __grid_constan
 // m * 16 + c with bit 8 folded into bit 4 (conflict-free both rounds).
 __device__ __forceinline__ int pass_swz(int i) { return i ^ (((i >> 8) & 1) << 4); }
 
+template <bool kEfOut>
 __global__ void __launch_bounds__(kThreads) rht_pass_kernel(const __grid_constant__ RhtParams p) {
     __shared__ float s[kTile];
     const int t = threadIdx.x;
@@ -198,8 +299,10 @@ __global__ void __launch_bounds__(kThreads) rht_pass_kernel(const __grid_constan
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        if (p.last) __stcs(x + (static_cast<int64_t>((j << 4) | mh) << p.s), v[j]);
-        else x[static_cast<int64_t>((j << 4) | mh) << p.s] = v[j];
+        const int64_t off = static_cast<int64_t>((j << 4) | mh) << p.s;
+        if (kEfOut && p.last) ef_out(p, (x - p.out) + off, v[j]);
+        else if (p.last) __stcs(x + off, v[j]);
+        else x[off] = v[j];
     }
 }
 
@@ -238,7 +341,7 @@ __device__ __forceinline__ float ld_cluster(uint32_t cluster_addr) {
     return v;
 }
 
-template <int RB>
+template <int RB, bool kEfOut>
 __global__ void __launch_bounds__(kThreads) rht_cluster_pass_kernel(const __grid_constant__ RhtParams p) {
     constexpr int K = 1 << RB;
     __shared__ float s[kTile];
@@ -311,7 +414,8 @@ __global__ void __launch_bounds__(kThreads) rht_cluster_pass_kernel(const __grid
 #pragma unroll
         for (int r = 0; r < K; ++r) {
             float *dst = y + (static_cast<int64_t>((r << 8) | m) << p.s);
-            if (p.last) __stcs(dst, w[r]);
+            if (kEfOut && p.last) ef_out(p, dst - p.out, w[r]);
+            else if (p.last) __stcs(dst, w[r]);
             else *dst = w[r];
         }
     }
@@ -328,7 +432,7 @@ constexpr int kClusterMaxBits = 24;
 // clusters of that size cannot be scheduled on this device (probed once) it
 // launches nothing and returns GAR_OK with *launched false, and the caller
 // takes the plain passes instead.
-template <int RB>
+template <int RB, bool kEfOut>
 int launch_cluster_pass(const RhtParams &p, unsigned blocks, cudaStream_t stream, bool *launched) {
     static std::atomic<int> ok[64];  // 0: not probed, 1: schedulable, 2: not
     int dev = 0;
@@ -352,11 +456,12 @@ int launch_cluster_pass(const RhtParams &p, unsigned blocks, cudaStream_t stream
         int clusters = 0;
         bool good = true;
         if (RB > 3)  // 16 CTAs: above the portable cluster size
-            good = cudaFuncSetAttribute(rht_cluster_pass_kernel<RB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-                   cudaSuccess;
+            good = cudaFuncSetAttribute(rht_cluster_pass_kernel<RB, kEfOut>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
         bool refused = !good;
         if (good) {
-            refused = cudaOccupancyMaxActiveClusters(&clusters, rht_cluster_pass_kernel<RB>, &cfg) != cudaSuccess;
+            refused = cudaOccupancyMaxActiveClusters(&clusters, rht_cluster_pass_kernel<RB, kEfOut>, &cfg) !=
+                      cudaSuccess;
             good = !refused && clusters > 0;
         }
         if (refused) cudaGetLastError();  // a refused probe leaves no error behind
@@ -364,7 +469,7 @@ int launch_cluster_pass(const RhtParams &p, unsigned blocks, cudaStream_t stream
         ok[dev].store(state, std::memory_order_relaxed);
     }
     if (state != 1) return GAR_OK;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, rht_cluster_pass_kernel<RB>, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, rht_cluster_pass_kernel<RB, kEfOut>, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(GAR_ECUDA, "rht_cluster_pass_kernel: %s", cudaGetErrorString(e));
@@ -373,14 +478,45 @@ int launch_cluster_pass(const RhtParams &p, unsigned blocks, cudaStream_t stream
     return check_launch("rht_cluster_pass_kernel");
 }
 
-// n < 4096: one CTA, every stage in shared memory.
+// n < 4096: one CTA, every stage in shared memory (the same kIn, kNorm and
+// kEfOut variants as the tile kernel).
+template <int kIn, bool kNorm, bool kEfOut>
 __global__ void __launch_bounds__(kThreads) rht_small_kernel(const __grid_constant__ RhtParams p) {
     __shared__ float s[kTile];
+    __shared__ float s_tab[kIn == kInPacked ? 256 : 1];
     const int n = static_cast<int>(p.n);
+    Decoder d{0.0f, 0.0f};
+    if constexpr (kIn == kInPacked) {
+        d = make_decoder(p, s_tab);
+        __syncthreads();
+    }
+    float sq = 0.0f;  // kNorm: this thread's squares, in element order
     for (int i = threadIdx.x; i < n; i += kThreads) {
-        float x = p.in[i];
+        float x;
+        if constexpr (kIn == kInPacked) {
+            const int per = 32 / p.b;
+            x = decode_one(p, d, s_tab, (__ldcs(p.packed + i / per) >> ((i % per) * p.b)) & ((1u << p.b) - 1u));
+        } else if constexpr (kIn == kInEf) {
+            x = __fadd_rn(p.grad[i], p.in[i]);
+        } else {
+            x = p.in[i];
+        }
+        if (kNorm) sq = __fadd_rn(sq, __fmul_rn(x, x));
         if (!p.inverse && ((word_of(sign_block(i >> 7, p.keys), (i >> 5) & 3) >> (i & 31)) & 1u)) x = -x;
         s[i] = x;
+    }
+    if constexpr (kNorm) {
+        double a = static_cast<double>(sq);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+        __shared__ double s_part[kThreads / 32];
+        if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = a;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double t = 0.0;
+            for (int i = 0; i < kThreads / 32; ++i) t += s_part[i];
+            p.sumsq[0] = t;
+        }
     }
     __syncthreads();
     for (int h = 1; h < n; h <<= 1) {
@@ -395,7 +531,9 @@ __global__ void __launch_bounds__(kThreads) rht_small_kernel(const __grid_consta
     for (int i = threadIdx.x; i < n; i += kThreads) {
         float y = s[i];
         if (p.inverse && ((word_of(sign_block(i >> 7, p.keys), (i >> 5) & 3) >> (i & 31)) & 1u)) y = -y;
-        p.out[i] = __fmul_rn(y, p.scale);
+        y = __fmul_rn(y, p.scale);
+        if constexpr (kEfOut) ef_out(p, i, y);
+        else p.out[i] = y;
     }
 }
 
@@ -482,6 +620,32 @@ __global__ void __launch_bounds__(kThreads) rht_norm_final(const __grid_constant
     }
 }
 
+// The range from per-tile sums of squares (gar_rht_ef_forward's): each
+// worker's tiles added in a fixed order (fp64), the largest sum taken.
+struct SumsRangeParams {
+    const double *sums[GAR_MAX_WORKERS];
+    float *mM;
+    int64_t tiles;
+    int32_t P;
+    int32_t pad;
+    double t_over_sqrt_n;
+};
+
+__global__ void __launch_bounds__(kThreads) rht_range_from_sums(const __grid_constant__ SumsRangeParams p) {
+    double best = 0.0;
+    for (int w = 0; w < p.P; ++w) {
+        double acc = 0.0;
+        for (int64_t i = threadIdx.x; i < p.tiles; i += kThreads) acc += p.sums[w][i];
+        acc = block_sum(acc);
+        if (threadIdx.x == 0 && acc > best) best = acc;
+    }
+    if (threadIdx.x == 0) {
+        const float M = static_cast<float>(p.t_over_sqrt_n * sqrt(best));
+        p.mM[0] = -M;
+        p.mM[1] = M;
+    }
+}
+
 int norm_blocks(int64_t n) {
     int64_t b = ceil_div(n, 4 * 2048);
     if (b > kNormBlocksMax) b = kNormBlocksMax;
@@ -553,33 +717,36 @@ bool overlaps(const void *a, const void *b, int64_t bytes) {
 
 using namespace gar;
 
-extern "C" int gar_rht(const float *in, float *out, int64_t n, uint64_t seed, int32_t inverse, gar_stream_t stream_) {
-    if (n < 1 || (n & (n - 1)) != 0) return fail(GAR_EINVAL, "n=%lld is not a power of two", static_cast<long long>(n));
-    if (n > (int64_t{1} << 31)) return fail(GAR_EINVAL, "n=%lld above 2^31", static_cast<long long>(n));
-    if (!in || !out) return fail(GAR_EINVAL, "in or out is NULL");
-    if (inverse != 0 && inverse != 1) return fail(GAR_EINVAL, "inverse must be 0 or 1");
-    if (!aligned(in, 16) || !aligned(out, 16)) return fail(GAR_EALIGN, "in and out must be 16-byte aligned");
-    if (in != out && overlaps(in, out, n * 4)) return fail(GAR_EINVAL, "in and out overlap without being equal");
-    RhtParams p;
-    std::memset(&p, 0, sizeof(p));
-    p.keys = philox_keys(seed);
-    p.in = in;
-    p.out = out;
-    p.n = n;
-    p.inverse = inverse;
+namespace gar {
+namespace {
+
+template <int kIn, bool kNorm, bool kEfOut>
+int launch_first(const RhtParams &p, unsigned blocks, bool small, cudaStream_t stream) {
+    if (small) {
+        rht_small_kernel<kIn, kNorm, kEfOut><<<1, kThreads, 0, stream>>>(p);
+        return check_launch("rht_small_kernel");
+    }
+    rht_tile_kernel<kIn, kNorm, kEfOut><<<blocks, kThreads, 0, stream>>>(p);
+    return check_launch("rht_tile_kernel");
+}
+
+// The whole transform of p.n = 2^k elements: the first launch reads as kIn
+// says (and sums squares per tile if kNorm), every later one works in place
+// on p.out, and the last writes the result -- or, with kEfOut, the updated
+// error vector instead.
+template <int kIn, bool kNorm, bool kEfOut>
+int rht_run(RhtParams &p, cudaStream_t stream) {
+    const int64_t n = p.n;
     p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(n)));
     int k = 0;
     while ((int64_t{1} << k) < n) ++k;
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (n < kTile) {
         p.last = 1;
-        rht_small_kernel<<<1, kThreads, 0, stream>>>(p);
-        return check_launch("rht_small_kernel");
+        return launch_first<kIn, kNorm, kEfOut>(p, 1, true, stream);
     }
     const unsigned blocks = static_cast<unsigned>(n / kTile);
     p.last = k == 12 ? 1 : 0;
-    rht_tile_kernel<<<blocks, kThreads, 0, stream>>>(p);
-    int rc = check_launch("rht_tile_kernel");
+    int rc = launch_first<kIn, kNorm, kEfOut>(p, blocks, false, stream);
     // bits 12..: for n <= 2^24, nine to twelve of them at once by a cluster
     // pass where the clusters can be scheduled; else (and for the last eight
     // or fewer) in passes of eight.  A plain pass that would run past bit k-1
@@ -593,10 +760,10 @@ extern "C" int gar_rht(const float *in, float *out, int64_t n, uint64_t seed, in
             p.last = done + 8 + rb >= k ? 1 : 0;
             bool launched = false;
             switch (rb) {
-                case 1: rc = launch_cluster_pass<1>(p, blocks, stream, &launched); break;
-                case 2: rc = launch_cluster_pass<2>(p, blocks, stream, &launched); break;
-                case 3: rc = launch_cluster_pass<3>(p, blocks, stream, &launched); break;
-                default: rc = launch_cluster_pass<4>(p, blocks, stream, &launched); break;
+                case 1: rc = launch_cluster_pass<1, kEfOut>(p, blocks, stream, &launched); break;
+                case 2: rc = launch_cluster_pass<2, kEfOut>(p, blocks, stream, &launched); break;
+                case 3: rc = launch_cluster_pass<3, kEfOut>(p, blocks, stream, &launched); break;
+                default: rc = launch_cluster_pass<4, kEfOut>(p, blocks, stream, &launched); break;
             }
             if (launched || rc != GAR_OK) {
                 done += 8 + rb;
@@ -606,11 +773,122 @@ extern "C" int gar_rht(const float *in, float *out, int64_t n, uint64_t seed, in
         p.s = done < k - 8 ? done : k - 8;
         p.lo_bit = done - p.s;
         p.last = p.s + 8 >= k ? 1 : 0;
-        rht_pass_kernel<<<blocks, kThreads, 0, stream>>>(p);
+        rht_pass_kernel<kEfOut><<<blocks, kThreads, 0, stream>>>(p);
         rc = check_launch("rht_pass_kernel");
         done = p.s + 8;
     }
     return rc;
+}
+
+int check_n(int64_t n) {
+    if (n < 1 || (n & (n - 1)) != 0) return fail(GAR_EINVAL, "n=%lld is not a power of two", static_cast<long long>(n));
+    if (n > (int64_t{1} << 31)) return fail(GAR_EINVAL, "n=%lld above 2^31", static_cast<long long>(n));
+    return GAR_OK;
+}
+
+}  // namespace
+}  // namespace gar
+
+extern "C" int gar_rht(const float *in, float *out, int64_t n, uint64_t seed, int32_t inverse, gar_stream_t stream_) {
+    int rc = check_n(n);
+    if (rc) return rc;
+    if (!in || !out) return fail(GAR_EINVAL, "in or out is NULL");
+    if (inverse != 0 && inverse != 1) return fail(GAR_EINVAL, "inverse must be 0 or 1");
+    if (!aligned(in, 16) || !aligned(out, 16)) return fail(GAR_EALIGN, "in and out must be 16-byte aligned");
+    if (in != out && overlaps(in, out, n * 4)) return fail(GAR_EINVAL, "in and out overlap without being equal");
+    std::unique_ptr<RhtParams> p(new RhtParams);
+    std::memset(p.get(), 0, sizeof(RhtParams));
+    p->keys = philox_keys(seed);
+    p->in = in;
+    p->out = out;
+    p->n = n;
+    p->inverse = inverse;
+    return rht_run<kInPlain, false, false>(*p, reinterpret_cast<cudaStream_t>(stream_));
+}
+
+extern "C" int64_t gar_rht_tiles(int64_t n) {
+    if (check_n(n) != GAR_OK) return 0;
+    return n < kTile ? 1 : n / kTile;
+}
+
+extern "C" int gar_rht_ef_forward(const float *grad, const float *e, float *y, int64_t n, uint64_t seed,
+                                  double *d_sumsq, gar_stream_t stream_) {
+    int rc = check_n(n);
+    if (rc) return rc;
+    if (!grad || !e || !y) return fail(GAR_EINVAL, "grad, e or y is NULL");
+    if (!aligned(grad, 16) || !aligned(e, 16) || !aligned(y, 16))
+        return fail(GAR_EALIGN, "grad, e and y must be 16-byte aligned");
+    if (d_sumsq && !aligned(d_sumsq, 8)) return fail(GAR_EALIGN, "d_sumsq not 8-byte aligned");
+    if (overlaps(y, grad, n * 4) || overlaps(y, e, n * 4)) return fail(GAR_EINVAL, "y overlaps grad or e");
+    std::unique_ptr<RhtParams> p(new RhtParams);
+    std::memset(p.get(), 0, sizeof(RhtParams));
+    p->keys = philox_keys(seed);
+    p->in = e;
+    p->grad = grad;
+    p->out = y;
+    p->n = n;
+    p->sumsq = d_sumsq;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    return d_sumsq ? rht_run<kInEf, true, false>(*p, stream) : rht_run<kInEf, false, false>(*p, stream);
+}
+
+extern "C" int gar_rht_ef_update(const uint32_t *packed, int32_t b, int32_t steps, const uint16_t *table,
+                                 const float *d_mM, const float *grad, float *e, float *tmp, int64_t n,
+                                 uint64_t seed, gar_stream_t stream_) {
+    int rc = check_n(n);
+    if (rc) return rc;
+    if (b != 1 && b != 2 && b != 4 && b != 8) return fail(GAR_EINVAL, "b=%d not in {1, 2, 4, 8}", b);
+    const int L = (1 << b) - 1;
+    if (!packed || !d_mM || !grad || !e || !tmp) return fail(GAR_EINVAL, "NULL argument");
+    if (!table && steps != L) return fail(GAR_EINVAL, "without a table the grid has 2^b - 1 = %d steps, not %d", L, steps);
+    if (table) {
+        if (table[0] != 0 || table[L] != steps) return fail(GAR_EINVAL, "table must start at 0 and end at %d", steps);
+        for (int z = 0; z < L; ++z)
+            if (table[z + 1] <= table[z]) return fail(GAR_EINVAL, "table not strictly increasing at %d", z);
+    }
+    if (steps < 1) return fail(GAR_EINVAL, "steps=%d < 1", steps);
+    if (!aligned(packed, 4) || !aligned(d_mM, 4) || !aligned(grad, 16) || !aligned(e, 16) || !aligned(tmp, 16))
+        return fail(GAR_EALIGN, "misaligned pointer (grad, e and tmp: 16 bytes; packed, d_mM: 4)");
+    if (overlaps(tmp, grad, n * 4) || overlaps(tmp, e, n * 4) || overlaps(e, grad, n * 4))
+        return fail(GAR_EINVAL, "tmp, grad and e must not overlap");
+    std::unique_ptr<RhtParams> p(new RhtParams);
+    std::memset(p.get(), 0, sizeof(RhtParams));
+    p->keys = philox_keys(seed);
+    p->out = tmp;
+    p->n = n;
+    p->inverse = 1;
+    p->grad = grad;
+    p->ef = e;
+    p->packed = packed;
+    p->mM = d_mM;
+    p->b = b;
+    p->steps = static_cast<float>(steps);
+    p->has_tab = table ? 1 : 0;
+    if (table)
+        for (int z = 0; z <= L; ++z) p->tab[z] = table[z];
+    return rht_run<kInPacked, false, true>(*p, reinterpret_cast<cudaStream_t>(stream_));
+}
+
+extern "C" int gar_rht_norm_range_from_sums(const double *const *d_sumsq, int32_t P, int64_t n, double t_p,
+                                            float *d_mM, gar_stream_t stream_) {
+    if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
+    int rc = check_n(n);
+    if (rc) return rc;
+    if (!d_sumsq || !d_mM) return fail(GAR_EINVAL, "NULL argument");
+    if (!(t_p > 0.0) || !std::isfinite(t_p)) return fail(GAR_EINVAL, "t_p must be positive and finite");
+    if (!aligned(d_mM, 4)) return fail(GAR_EALIGN, "d_mM not 4-byte aligned");
+    SumsRangeParams p;
+    std::memset(&p, 0, sizeof(p));
+    for (int w = 0; w < P; ++w) {
+        if (!d_sumsq[w] || !aligned(d_sumsq[w], 8)) return fail(GAR_EINVAL, "sums of worker %d NULL or misaligned", w);
+        p.sums[w] = d_sumsq[w];
+    }
+    p.P = P;
+    p.tiles = gar_rht_tiles(n);
+    p.mM = d_mM;
+    p.t_over_sqrt_n = t_p / std::sqrt(static_cast<double>(n));
+    rht_range_from_sums<<<1, kThreads, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(p);
+    return check_launch("rht_range_from_sums");
 }
 
 extern "C" size_t gar_rht_norm_range_workspace_bytes(int32_t P, int64_t n) {

@@ -13,7 +13,10 @@ thc_plan_nmse (the same with the NMSE sums against a reference taken in the pass
 pack, unpack (per worker and buffer), pack_all, pack_all_range (every worker
 in one call, with THC's range fused in), thc_range, thc_encode, thc_aggregate, thc_decode, thc_fused,
 thc_fused_packed, nuhc_fused, nuhc_fused_packed (non-uniform THC with a
-table on a granularity-g grid), nmse.  Inputs are seeded N(0, 1) draws made on the device;
+table on a granularity-g grid), nmse, train_step, train_step_fused (one step
+of THC's training process over P workers: error feedback, rotation, range,
+non-uniform THC, inverse rotation, error-feedback update; separate or fused
+calls).  Inputs are seeded N(0, 1) draws made on the device;
 every size is chosen by the caller, so a case can be kept small enough for a
 profiler capture.  Prints one JSON line: time per call (CUDA events on the
 launching stream, after warm-up) and algorithmic GB/s.
@@ -221,6 +224,61 @@ def main(argv=None):
             inv = a.case == "rht_inv"
             fn = lambda: g.gar_rht(src, dst, 7, inverse=inv)  # noqa: E731
             nbytes = 2 * N * 4
+    elif a.case in ("train_step", "train_step_fused"):
+        # one step of THC's training process for P workers of N values (the
+        # page's section 5): error feedback, rotation, norm-based range,
+        # non-uniform THC b-bit with granularity g (36 for b = 4), inverse
+        # rotation of the average, every worker's error-feedback update from
+        # its own wire vector -- through the separate calls, or the fused ones.
+        # algorithmic bytes: per worker grad and e read, y written, y read, the
+        # wire vector written and read, grad and e read and e written again;
+        # once the average written, read and its rotation written
+        L = (1 << b) - 1
+        gr = a.g if a.g else (36 if b == 4 else 2 * L + 1)
+        tab = np.rint(np.linspace(0, gr, L + 1)).astype(np.uint16)
+        grads = bufs(N, P, torch.float32)
+        errs = [t.mul_(1e-3) for t in bufs(N, P, torch.float32, seed=500)]
+        e_work = [t.clone() for t in errs]
+        ys = [torch.empty(N, device=dev) for _ in range(P)]
+        words = g.gar_thc_words(N, b)
+        packed = [torch.empty(words, dtype=torch.int32, device=dev) for _ in range(P)]
+        pt, yt = g.pointer_table(packed), g.pointer_table(ys)
+        mM = torch.empty(2, device=dev)
+        avg, est, tmp = (torch.empty(N, device=dev) for _ in range(3))
+        t_p = 2.15
+        if a.case == "train_step_fused":
+            sums = [torch.empty(g.gar_rht_tiles(N), dtype=torch.float64, device=dev) for _ in range(P)]
+            st = g.pointer_table(sums)
+
+            def fn():
+                for w in range(P):
+                    g.gar_rht_ef_forward(grads[w], e_work[w], ys[w], 11, sums[w])
+                g.gar_rht_norm_range_from_sums(st, N, t_p, mM)
+                g.gar_nuhc_allreduce_fused(yt, b, gr, tab, 5, mM, avg, pt)
+                g.gar_rht(avg, est, 11, inverse=True)
+                for w in range(P):
+                    g.gar_rht_ef_update(packed[w], b, gr, tab, mM, grads[w], e_work[w], tmp, 11)
+        else:
+            xs = [torch.empty(N, device=dev) for _ in range(P)]
+            xt = g.pointer_table(xs)
+            ws = torch.empty(g.gar_rht_norm_range_workspace_bytes(P, N) // 8 + 1, dtype=torch.float64, device=dev)
+            own = torch.empty(N, dtype=torch.int16, device=dev)
+            y_hat, x_hat = torch.empty(N, device=dev), torch.empty(N, device=dev)
+
+            def fn():
+                for w in range(P):
+                    g.gar_ef_apply(grads[w], e_work[w], xs[w])
+                g.gar_rht_norm_range(xt, t_p, mM, ws)
+                for w in range(P):
+                    g.gar_rht(xs[w], ys[w], 11)
+                g.gar_nuhc_allreduce_fused(yt, b, gr, tab, 5, mM, avg, pt)
+                g.gar_rht(avg, est, 11, inverse=True)
+                for w in range(P):
+                    g.gar_nuhc_aggregate([packed[w]], N, b, tab, own)
+                    g.gar_nuhc_decode(own, mM, gr, 1, y_hat)
+                    g.gar_rht(y_hat, x_hat, 11, inverse=True)
+                    g.gar_ef_update(e_work[w], xs[w], x_hat)
+        nbytes = P * N * 4 * (2 + 1 + 1 + 2 + 1) + P * 2 * words * 4 + 3 * N * 4
     elif a.case == "checksum":
         # algorithmic bytes: one read of N 32-bit words
         w = bufs(N, 1, torch.float32)[0].view(torch.int32)

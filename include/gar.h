@@ -518,6 +518,58 @@ int gar_rht_norm_range(const float *const *x, int32_t P, int64_t n, double t_p, 
 int gar_ef_apply(const float *grad, const float *e, float *x, int64_t n, gar_stream_t stream);
 int gar_ef_update(float *e, const float *x, const float *x_hat, int64_t n, gar_stream_t stream);
 
+/* The same worker steps fused into the transform's own passes ([T] section
+ * 5: error feedback, the randomized Hadamard transform, the norm-based
+ * range, and the update of e from the worker's own quantized vector), so
+ * that x = grad + e, the decoded own vector and x_hat are never written to
+ * memory.  Results are bit for bit those of the separate calls named below. */
+
+/* Tiles (4096 elements; 1 when n < 4096) of a transform of n elements: the
+ * per-tile sums of squares gar_rht_ef_forward writes.  0 for a bad n. */
+int64_t gar_rht_tiles(int64_t n);
+
+/* gar_rht_ef_forward -- y = (1/sqrt(n)) H D (grad + e): bit for bit
+ * gar_ef_apply(grad, e, x) then gar_rht(x, y, n, seed, 0), reading grad and
+ * e once and writing y.  d_sumsq (device, gar_rht_tiles(n) doubles, 8-byte
+ * aligned, or NULL): the sums of squares of x = grad + e per tile (fp32
+ * squares summed pairwise, fp64 per tile), for gar_rht_norm_range_from_sums.
+ * grad, e, y: device, n fp32, 16-byte aligned; y must not overlap grad or e.
+ * n: a power of two, 1 <= n <= 2^31.
+ * Errors: GAR_EINVAL (n, NULL, overlap), GAR_EALIGN, GAR_ECUDA. */
+int gar_rht_ef_forward(const float *grad, const float *e, float *y, int64_t n, uint64_t seed,
+                       double *d_sumsq, gar_stream_t stream);
+
+/* gar_rht_norm_range_from_sums -- the norm-based range of gar_rht_norm_range
+ * from the P workers' per-tile sums of squares (d_sumsq[w]: device,
+ * gar_rht_tiles(n) doubles each, as gar_rht_ef_forward wrote them): each
+ * worker's tiles added in a fixed order in fp64, the largest sum l^2 taken,
+ * d_mM = (-M, M) with M = (t_p / sqrt(n)) l rounded to fp32.  Within 1e-6
+ * relative of the exact value (the sums are ordered differently from
+ * gar_rht_norm_range's, so the two may differ in the last bit).
+ * Errors: GAR_EINVAL (P outside [1, 64], n, NULL, t_p not positive),
+ * GAR_EALIGN, GAR_ECUDA. */
+int gar_rht_norm_range_from_sums(const double *const *d_sumsq, int32_t P, int64_t n, double t_p,
+                                 float *d_mM, gar_stream_t stream);
+
+/* gar_rht_ef_update -- the worker's error-feedback update from its own wire
+ * vector: e = (grad + e) - x_hat, x_hat = (1/sqrt(n)) D H y_hat, where
+ * y_hat[i] = fma(S_i, (M - m) / steps, m) is the worker's own index i
+ * decoded on the grid (S_i = table[idx_i] for non-uniform THC, idx_i for
+ * uniform THC with table = NULL and steps = 2^b - 1).  Bit for bit
+ * gar_nuhc_aggregate / gar_thc_aggregate of [packed] alone, then the decode
+ * with P = 1, gar_rht(inverse), and gar_ef_update(e, gar_ef_apply(grad, e),
+ * x_hat).  packed: device, the worker's gar_thc_words(n, b) words (4-byte
+ * aligned); table: host, 2^b entries from 0 to steps, strictly increasing,
+ * or NULL; d_mM: device [m, M]; grad, e: device, n fp32 (e read and
+ * rewritten in place); tmp: device scratch of n fp32 for the transform's
+ * intermediate passes (caller-owned, not shared with a concurrent call);
+ * grad, e, tmp 16-byte aligned and pairwise disjoint.
+ * Errors: GAR_EINVAL (n, b, steps, table, NULL, overlap), GAR_EALIGN,
+ * GAR_ECUDA. */
+int gar_rht_ef_update(const uint32_t *packed, int32_t b, int32_t steps, const uint16_t *table,
+                      const float *d_mM, const float *grad, float *e, float *tmp, int64_t n, uint64_t seed,
+                      gar_stream_t stream);
+
 /* ===================================================================== */
 /* NMSE [T] section 2: ||x - x_hat||^2 / ||x||^2                          */
 /* ===================================================================== */
