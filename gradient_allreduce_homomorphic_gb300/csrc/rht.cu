@@ -82,7 +82,7 @@ struct RhtParams {
     int32_t b;               // kInPacked: bits per index
     int32_t has_tab;         // kInPacked: index z stands for tab[z] (non-uniform THC), else for z
     float steps;             // kInPacked: grid steps between m and M (2^b - 1, or the granularity g)
-    int32_t pad;
+    int32_t b_log;           // kInPacked: log2 b (indices per word 32 / b = 2^(5 - b_log))
     uint16_t tab[256];       // kInPacked with has_tab: the table T
 };
 
@@ -110,16 +110,29 @@ __device__ __forceinline__ float decode_one(const RhtParams &p, const Decoder &d
     const float S = p.has_tab ? s_tab[z] : static_cast<float>(z);
     return __fmaf_rn(S, d.k, d.m);
 }
+// Word of element e and the bit offset of its index in it (b a power of two:
+// shifts, no division).
+__device__ __forceinline__ uint32_t packed_word(const RhtParams &p, int64_t e, int &sh) {
+    const int per_log = 5 - p.b_log;
+    sh = static_cast<int>(e & ((int64_t{1} << per_log) - 1)) << p.b_log;
+    return __ldcs(p.packed + (e >> per_log));
+}
 // Elements e .. e + 3 (e a multiple of 4) decoded from the packed indices.
 __device__ __forceinline__ float4 decode4(const RhtParams &p, const Decoder &d, const float *s_tab, int64_t e) {
-    const int per = 32 / p.b;
-    const uint32_t w = __ldcs(p.packed + e / per);
+    int sh;
+    const uint32_t w = packed_word(p, e, sh);
     const uint32_t mask = (1u << p.b) - 1u;
-    const int sh = static_cast<int>(e % per) * p.b;
     return make_float4(decode_one(p, d, s_tab, (w >> sh) & mask), decode_one(p, d, s_tab, (w >> (sh + p.b)) & mask),
                        decode_one(p, d, s_tab, (w >> (sh + 2 * p.b)) & mask),
                        decode_one(p, d, s_tab, (w >> (sh + 3 * p.b)) & mask));
 }
+// Element i decoded from the packed indices.
+__device__ __forceinline__ float decode_at(const RhtParams &p, const Decoder &d, const float *s_tab, int64_t i) {
+    int sh;
+    const uint32_t w = packed_word(p, i, sh);
+    return decode_one(p, d, s_tab, (w >> sh) & ((1u << p.b) - 1u));
+}
+
 // e = (grad + e) - y for one element: the error-feedback update with x
 // recomputed as gar_ef_apply forms it.
 __device__ __forceinline__ void ef_out(const RhtParams &p, int64_t i, float y) {
@@ -232,6 +245,14 @@ __global__ void __launch_bounds__(kThreads) rht_tile_kernel(const __grid_constan
     __syncthreads();
     // bits 6..9 in registers: element (t & 63) | (r << 6) | ((t >> 6) << 10)
     const int b2 = (t & 63) | ((t >> 6) << 10);
+    float xr[kEfOut ? 16 : 1];  // kEfOut: x = grad + e of the elements this thread writes, loaded early
+    if constexpr (kEfOut) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const int64_t i = base + (b2 | (r << 6));
+            xr[r] = __fadd_rn(__ldcs(p.grad + i), p.ef[i]);
+        }
+    }
 #pragma unroll
     for (int r = 0; r < 16; ++r) v[r] = s[tile_swz(b2 | (r << 6))];
     butterfly16(v);
@@ -244,32 +265,43 @@ __global__ void __launch_bounds__(kThreads) rht_tile_kernel(const __grid_constan
             if (signs_out && ((s_sign[e >> 5] >> (e & 31)) & 1u)) y = -y;
             y = __fmul_rn(y, p.scale);
         }
-        if (kEfOut && p.last) ef_out(p, base + e, y);
+        if constexpr (kEfOut) __stcs(p.ef + base + e, __fsub_rn(xr[r], y));  // e = (grad + e) - x_hat
         else if (p.last) __stcs(dst + e, y);
         else dst[e] = y;  // the next pass reads it: normal priority, so that it can stay in L2
     }
 }
 
-// Row bits [lo_bit, 8) of 256 rows 2^s apart (s >= 4), 16 columns each, in
-// place on p.out.  Block -> (hi, column block cb): element of (row m, column
-// c) = (hi << (s + 8)) | (m << s) | (cb << 4) | c.  Shared layout: row-major
+// Row bits [lo_bit, 8) of 256 rows 2^s apart (s >= 4), 16 columns each,
+// read from p.in (kIn = kInPlain; p.in == p.out in place) or decoded from
+// p.packed (kInPacked), written to p.out; with p.last scaled by 1/sqrt(n).
+// Block -> (hi, column block cb): element of (row m, column c) =
+// (hi << (s + 8)) | (m << s) | (cb << 4) | c.  Shared layout: row-major
 // m * 16 + c with bit 8 folded into bit 4 (conflict-free both rounds).
 __device__ __forceinline__ int pass_swz(int i) { return i ^ (((i >> 8) & 1) << 4); }
 
-template <bool kEfOut>
+template <int kIn>
 __global__ void __launch_bounds__(kThreads) rht_pass_kernel(const __grid_constant__ RhtParams p) {
     __shared__ float s[kTile];
+    __shared__ float s_tab[kIn == kInPacked ? 256 : 1];
     const int t = threadIdx.x;
     const int c = t & 15, mh = t >> 4;
     const int64_t bid = blockIdx.x;
     const int cb_bits = p.s - 4;
     const int64_t cb = bid & ((int64_t{1} << cb_bits) - 1);
     const int64_t hi = bid >> cb_bits;
-    float *x = p.out + ((hi << (p.s + 8)) | (cb << 4) | c);
+    const int64_t col0 = (hi << (p.s + 8)) | (cb << 4) | c;
     float v[16];
     // first stage: rows (mh << 4) | j
+    if constexpr (kIn == kInPacked) {
+        const Decoder d = make_decoder(p, s_tab);
+        __syncthreads();
 #pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = x[static_cast<int64_t>((mh << 4) | j) << p.s];  // written by the launch before
+        for (int j = 0; j < 16; ++j) v[j] = decode_at(p, d, s_tab, col0 + (static_cast<int64_t>((mh << 4) | j) << p.s));
+    } else {
+        const float *x = p.in + col0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = x[static_cast<int64_t>((mh << 4) | j) << p.s];  // may be the launch before's
+    }
     butterfly16(v, p.lo_bit);
 #pragma unroll
     for (int j = 0; j < 16; ++j) s[pass_swz((mh << 8) | (j << 4) | c)] = v[j];
@@ -278,31 +310,12 @@ __global__ void __launch_bounds__(kThreads) rht_pass_kernel(const __grid_constan
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = s[pass_swz((j << 8) | (mh << 4) | c)];
     butterfly16(v, p.lo_bit > 4 ? p.lo_bit - 4 : 0);
-    if (p.last) {
-        if (p.inverse) {
-            // a half-warp's 16 columns share one sign word; lane L draws the word
-            // of row ((L & 15) << 4) | mh for its half-warp, the others read it
-            const int lane = t & 31;
-            const int mh_lane = ((t & ~31) >> 4) | (lane >> 4);
-            const int64_t e_lane = (hi << (p.s + 8)) | (cb << 4) |
-                                   (static_cast<int64_t>(((lane & 15) << 4) | mh_lane) << p.s);
-            const uint32_t mine = word_of(sign_block(e_lane >> 7, p.keys), static_cast<int>((e_lane >> 5) & 3));
-            const int bit = static_cast<int>(((cb & 1) << 4) | c);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const uint32_t w = __shfl_sync(0xFFFFFFFFu, mine, j | (lane & 16));
-                if ((w >> bit) & 1u) v[j] = -v[j];
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], p.scale);
-    }
+    float *y = p.out + col0;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const int64_t off = static_cast<int64_t>((j << 4) | mh) << p.s;
-        if (kEfOut && p.last) ef_out(p, (x - p.out) + off, v[j]);
-        else if (p.last) __stcs(x + off, v[j]);
-        else x[off] = v[j];
+        if (p.last) __stcs(y + off, __fmul_rn(v[j], p.scale));
+        else y[off] = v[j];  // the next launch reads it: normal priority, so that it can stay in L2
     }
 }
 
@@ -341,10 +354,11 @@ __device__ __forceinline__ float ld_cluster(uint32_t cluster_addr) {
     return v;
 }
 
-template <int RB, bool kEfOut>
+template <int RB, int kIn>
 __global__ void __launch_bounds__(kThreads) rht_cluster_pass_kernel(const __grid_constant__ RhtParams p) {
     constexpr int K = 1 << RB;
     __shared__ float s[kTile];
+    __shared__ float s_tab[kIn == kInPacked ? 256 : 1];
     const int t = threadIdx.x;
     const int c = t & 15, mh = t >> 4;
     const uint32_t q = cluster_rank();
@@ -353,10 +367,18 @@ __global__ void __launch_bounds__(kThreads) rht_cluster_pass_kernel(const __grid
     const int64_t cb = cid & ((int64_t{1} << cb_bits) - 1);
     const int64_t hi = cid >> cb_bits;
     const int64_t base = (hi << (p.s + 8 + RB)) | (cb << 4);  // row 0, column 0 of the cluster's block
-    const float *x = p.out + base + (static_cast<int64_t>(q) << (p.s + 8)) + c;
+    const int64_t col0 = base + (static_cast<int64_t>(q) << (p.s + 8)) + c;
     float v[16];
+    if constexpr (kIn == kInPacked) {
+        const Decoder d = make_decoder(p, s_tab);
+        __syncthreads();
 #pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = x[static_cast<int64_t>((mh << 4) | j) << p.s];  // written by the launch before
+        for (int j = 0; j < 16; ++j) v[j] = decode_at(p, d, s_tab, col0 + (static_cast<int64_t>((mh << 4) | j) << p.s));
+    } else {
+        const float *x = p.in + col0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = x[static_cast<int64_t>((mh << 4) | j) << p.s];  // may be the launch before's
+    }
     butterfly16(v);
 #pragma unroll
     for (int j = 0; j < 16; ++j) s[pass_swz((mh << 8) | (j << 4) | c)] = v[j];
@@ -375,7 +397,6 @@ __global__ void __launch_bounds__(kThreads) rht_cluster_pass_kernel(const __grid
 #pragma unroll
         for (int r = 0; r < K; ++r) rbase[r] = map_cluster(s_addr, r);
     }
-    const int lane = t & 31;
 #pragma unroll 1
     for (int i = 0; i < 16 / K; ++i) {
         const int pos = i * (K * 256) + static_cast<int>(q) * 256 + t;  // (m, c) = (pos >> 4, pos & 15)
@@ -394,28 +415,11 @@ __global__ void __launch_bounds__(kThreads) rht_cluster_pass_kernel(const __grid
                 }
             }
         }
-        if (p.last) {
-            if (p.inverse) {
-                // the 16 columns of a half-warp share one sign word per row: lane L
-                // draws the word of row ((L mod K) << 8) | m, the others read it
-                const int64_t e_lane = base | (static_cast<int64_t>(((lane & (K - 1)) << 8) | m) << p.s);
-                const uint32_t mine = word_of(sign_block(e_lane >> 7, p.keys), static_cast<int>((e_lane >> 5) & 3));
-                const int bit = static_cast<int>(((cb & 1) << 4) | c);
-#pragma unroll
-                for (int r = 0; r < K; ++r) {
-                    const uint32_t word = __shfl_sync(0xFFFFFFFFu, mine, r | (lane & 16));
-                    if ((word >> bit) & 1u) w[r] = -w[r];
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < K; ++r) w[r] = __fmul_rn(w[r], p.scale);
-        }
         float *y = p.out + base + c;
 #pragma unroll
         for (int r = 0; r < K; ++r) {
             float *dst = y + (static_cast<int64_t>((r << 8) | m) << p.s);
-            if (kEfOut && p.last) ef_out(p, dst - p.out, w[r]);
-            else if (p.last) __stcs(dst, w[r]);
+            if (p.last) __stcs(dst, __fmul_rn(w[r], p.scale));
             else *dst = w[r];
         }
     }
@@ -432,7 +436,7 @@ constexpr int kClusterMaxBits = 24;
 // clusters of that size cannot be scheduled on this device (probed once) it
 // launches nothing and returns GAR_OK with *launched false, and the caller
 // takes the plain passes instead.
-template <int RB, bool kEfOut>
+template <int RB, int kIn>
 int launch_cluster_pass(const RhtParams &p, unsigned blocks, cudaStream_t stream, bool *launched) {
     static std::atomic<int> ok[64];  // 0: not probed, 1: schedulable, 2: not
     int dev = 0;
@@ -456,11 +460,11 @@ int launch_cluster_pass(const RhtParams &p, unsigned blocks, cudaStream_t stream
         int clusters = 0;
         bool good = true;
         if (RB > 3)  // 16 CTAs: above the portable cluster size
-            good = cudaFuncSetAttribute(rht_cluster_pass_kernel<RB, kEfOut>,
+            good = cudaFuncSetAttribute(rht_cluster_pass_kernel<RB, kIn>,
                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
         bool refused = !good;
         if (good) {
-            refused = cudaOccupancyMaxActiveClusters(&clusters, rht_cluster_pass_kernel<RB, kEfOut>, &cfg) !=
+            refused = cudaOccupancyMaxActiveClusters(&clusters, rht_cluster_pass_kernel<RB, kIn>, &cfg) !=
                       cudaSuccess;
             good = !refused && clusters > 0;
         }
@@ -469,7 +473,7 @@ int launch_cluster_pass(const RhtParams &p, unsigned blocks, cudaStream_t stream
         ok[dev].store(state, std::memory_order_relaxed);
     }
     if (state != 1) return GAR_OK;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, rht_cluster_pass_kernel<RB, kEfOut>, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, rht_cluster_pass_kernel<RB, kIn>, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(GAR_ECUDA, "rht_cluster_pass_kernel: %s", cudaGetErrorString(e));
@@ -494,8 +498,7 @@ __global__ void __launch_bounds__(kThreads) rht_small_kernel(const __grid_consta
     for (int i = threadIdx.x; i < n; i += kThreads) {
         float x;
         if constexpr (kIn == kInPacked) {
-            const int per = 32 / p.b;
-            x = decode_one(p, d, s_tab, (__ldcs(p.packed + i / per) >> ((i % per) * p.b)) & ((1u << p.b) - 1u));
+            x = decode_at(p, d, s_tab, i);
         } else if constexpr (kIn == kInEf) {
             x = __fadd_rn(p.grad[i], p.in[i]);
         } else {
@@ -730,10 +733,65 @@ int launch_first(const RhtParams &p, unsigned blocks, bool small, cudaStream_t s
     return check_launch("rht_tile_kernel");
 }
 
-// The whole transform of p.n = 2^k elements: the first launch reads as kIn
-// says (and sums squares per tile if kNorm), every later one works in place
-// on p.out, and the last writes the result -- or, with kEfOut, the updated
-// error vector instead.
+// Passes over index bits 12..k-1: for n <= 2^24, nine to twelve of them at
+// once by a cluster pass where the clusters can be scheduled; else (and for
+// the last eight or fewer) in passes of eight.  A plain pass that would run
+// past bit k-1 is moved down (s = k - 8) and skips the row bits already
+// done.  The first of them reads as kIn says (p.in, or p.packed); the others
+// work in place on p.out.  fin: the last of them writes the final values.
+template <int kIn>
+int run_passes(const RhtParams &p0, int k, unsigned blocks, bool fin, cudaStream_t stream) {
+    std::unique_ptr<RhtParams> q(new RhtParams(p0));
+    int rc = GAR_OK;
+    bool first = true;
+    for (int done = 12; done < k && rc == GAR_OK; first = false) {
+        if (!first) q->in = q->out;
+        const int left = k - done;
+        if (left > 8 && k <= kClusterMaxBits) {
+            const int rb = left >= 12 ? 4 : left - 8;
+            q->s = done;
+            q->lo_bit = 0;
+            q->last = fin && done + 8 + rb >= k ? 1 : 0;
+            bool launched = false;
+            if (first) {
+                switch (rb) {
+                    case 1: rc = launch_cluster_pass<1, kIn>(*q, blocks, stream, &launched); break;
+                    case 2: rc = launch_cluster_pass<2, kIn>(*q, blocks, stream, &launched); break;
+                    case 3: rc = launch_cluster_pass<3, kIn>(*q, blocks, stream, &launched); break;
+                    default: rc = launch_cluster_pass<4, kIn>(*q, blocks, stream, &launched); break;
+                }
+            } else {
+                switch (rb) {
+                    case 1: rc = launch_cluster_pass<1, kInPlain>(*q, blocks, stream, &launched); break;
+                    case 2: rc = launch_cluster_pass<2, kInPlain>(*q, blocks, stream, &launched); break;
+                    case 3: rc = launch_cluster_pass<3, kInPlain>(*q, blocks, stream, &launched); break;
+                    default: rc = launch_cluster_pass<4, kInPlain>(*q, blocks, stream, &launched); break;
+                }
+            }
+            if (launched || rc != GAR_OK) {
+                done += 8 + rb;
+                continue;
+            }
+        }
+        q->s = done < k - 8 ? done : k - 8;
+        q->lo_bit = done - q->s;
+        q->last = fin && q->s + 8 >= k ? 1 : 0;
+        if (first) rht_pass_kernel<kIn><<<blocks, kThreads, 0, stream>>>(*q);
+        else rht_pass_kernel<kInPlain><<<blocks, kThreads, 0, stream>>>(*q);
+        rc = check_launch("rht_pass_kernel");
+        done = q->s + 8;
+    }
+    return rc;
+}
+
+// The whole transform of p.n = 2^k elements.  The butterfly stages of
+// different index bits commute, so the forward transform takes the
+// 4096-element tiles (bits 0..11) first -- they apply the signs as they read,
+// with error feedback (kInEf) and the norm's sums (kNorm) -- and the passes
+// over the higher bits after, the last of them scaling; the inverse takes
+// the passes first (reading p.in, or decoding p.packed) and the tiles last,
+// where the signs, the scale and, with kEfOut, the error-feedback update are
+// applied as contiguous tiles are written.
 template <int kIn, bool kNorm, bool kEfOut>
 int rht_run(RhtParams &p, cudaStream_t stream) {
     const int64_t n = p.n;
@@ -745,39 +803,27 @@ int rht_run(RhtParams &p, cudaStream_t stream) {
         return launch_first<kIn, kNorm, kEfOut>(p, 1, true, stream);
     }
     const unsigned blocks = static_cast<unsigned>(n / kTile);
-    p.last = k == 12 ? 1 : 0;
-    int rc = launch_first<kIn, kNorm, kEfOut>(p, blocks, false, stream);
-    // bits 12..: for n <= 2^24, nine to twelve of them at once by a cluster
-    // pass where the clusters can be scheduled; else (and for the last eight
-    // or fewer) in passes of eight.  A plain pass that would run past bit k-1
-    // is moved down (s = k - 8) and skips the row bits already done.
-    for (int done = 12; done < k && rc == GAR_OK;) {
-        const int left = k - done;
-        if (left > 8 && k <= kClusterMaxBits) {
-            const int rb = left >= 12 ? 4 : left - 8;
-            p.s = done;
-            p.lo_bit = 0;
-            p.last = done + 8 + rb >= k ? 1 : 0;
-            bool launched = false;
-            switch (rb) {
-                case 1: rc = launch_cluster_pass<1, kEfOut>(p, blocks, stream, &launched); break;
-                case 2: rc = launch_cluster_pass<2, kEfOut>(p, blocks, stream, &launched); break;
-                case 3: rc = launch_cluster_pass<3, kEfOut>(p, blocks, stream, &launched); break;
-                default: rc = launch_cluster_pass<4, kEfOut>(p, blocks, stream, &launched); break;
-            }
-            if (launched || rc != GAR_OK) {
-                done += 8 + rb;
-                continue;
-            }
-        }
-        p.s = done < k - 8 ? done : k - 8;
-        p.lo_bit = done - p.s;
-        p.last = p.s + 8 >= k ? 1 : 0;
-        rht_pass_kernel<kEfOut><<<blocks, kThreads, 0, stream>>>(p);
-        rc = check_launch("rht_pass_kernel");
-        done = p.s + 8;
+    if (!p.inverse) {
+        if constexpr (kEfOut) return fail(GAR_EINVAL, "the forward transform writes no error feedback");
+        p.last = k == 12 ? 1 : 0;
+        int rc = launch_first<kIn, kNorm, false>(p, blocks, false, stream);
+        if (rc || k == 12) return rc;
+        RhtParams &q = p;
+        q.in = q.out;
+        return run_passes<kInPlain>(q, k, blocks, true, stream);
     }
-    return rc;
+    if constexpr (kIn == kInEf || kNorm) return fail(GAR_EINVAL, "the inverse reads no error feedback and takes no norm");
+    if (k == 12) {
+        p.last = 1;
+        return launch_first<kIn, false, kEfOut>(p, blocks, false, stream);
+    }
+    int rc = run_passes<kIn>(p, k, blocks, false, stream);
+    if (rc) return rc;
+    p.in = p.out;
+    p.last = 1;
+    p.s = 0;
+    p.lo_bit = 0;
+    return launch_first<kInPlain, false, kEfOut>(p, blocks, false, stream);
 }
 
 int check_n(int64_t n) {
@@ -862,6 +908,7 @@ extern "C" int gar_rht_ef_update(const uint32_t *packed, int32_t b, int32_t step
     p->packed = packed;
     p->mM = d_mM;
     p->b = b;
+    p->b_log = b == 1 ? 0 : (b == 2 ? 1 : (b == 4 ? 2 : 3));
     p->steps = static_cast<float>(steps);
     p->has_tab = table ? 1 : 0;
     if (table)
