@@ -46,18 +46,42 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &b, int w) {
     return w == 0 ? b.x : (w == 1 ? b.y : (w == 2 ? b.z : b.w));
 }
 
-// Butterfly stages over v[0..15] on the register-index bits >= lo_bit.
+__device__ __forceinline__ uint64_t pair_bits(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void bits_pair(uint64_t v, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+
+// Butterfly stages over v[0..15] on the register-index bits >= lo_bit.  The
+// stages on bits 1..3 take the neighbouring registers (v[r], v[r + 1]) as
+// one f32x2 operand (each lane rounded as the scalar add or subtract), two
+// butterflies per instruction; bit 0 pairs the neighbours themselves and
+// stays scalar.
 __device__ __forceinline__ void butterfly16(float (&v)[16], int lo_bit = 0) {
+    if (lo_bit <= 0) {
 #pragma unroll
-    for (int bit = 0; bit < 4; ++bit) {
+        for (int r = 0; r < 16; r += 2) {
+            const float a = v[r], b = v[r + 1];
+            v[r] = __fadd_rn(a, b);
+            v[r + 1] = __fsub_rn(a, b);
+        }
+    }
+#pragma unroll
+    for (int bit = 1; bit < 4; ++bit) {
         if (bit < lo_bit) continue;
         const int h = 1 << bit;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
+        for (int r = 0; r < 16; r += 2) {
             if ((r & h) == 0) {
-                const float a = v[r], b = v[r + h];
-                v[r] = __fadd_rn(a, b);
-                v[r + h] = __fsub_rn(a, b);
+                const uint64_t a = pair_bits(v[r], v[r + 1]), b = pair_bits(v[r + h], v[r + h + 1]);
+                uint64_t sum, dif;
+                asm("add.rn.f32x2 %0, %1, %2;" : "=l"(sum) : "l"(a), "l"(b));
+                asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(dif) : "l"(a), "l"(b));
+                bits_pair(sum, v[r], v[r + 1]);
+                bits_pair(dif, v[r + h], v[r + h + 1]);
             }
         }
     }
@@ -404,14 +428,24 @@ __global__ void __launch_bounds__(kThreads) rht_cluster_pass_kernel(const __grid
         float w[K];
 #pragma unroll
         for (int r = 0; r < K; ++r) w[r] = ld_cluster(rbase[r] + 4u * static_cast<uint32_t>(pass_swz(pos)));
+        // the K-point butterflies, paired in f32x2 from the second stage on
 #pragma unroll
-        for (int h = 1; h < K; h <<= 1) {
+        for (int r = 0; r < K; r += 2) {
+            const float a = w[r], b = w[r + 1];
+            w[r] = __fadd_rn(a, b);
+            w[r + 1] = __fsub_rn(a, b);
+        }
 #pragma unroll
-            for (int r = 0; r < K; ++r) {
+        for (int h = 2; h < K; h <<= 1) {
+#pragma unroll
+            for (int r = 0; r < K; r += 2) {
                 if ((r & h) == 0) {
-                    const float a = w[r], b = w[r + h];
-                    w[r] = __fadd_rn(a, b);
-                    w[r + h] = __fsub_rn(a, b);
+                    const uint64_t a = pair_bits(w[r], w[r + 1]), b = pair_bits(w[r + h], w[r + h + 1]);
+                    uint64_t sum, dif;
+                    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(sum) : "l"(a), "l"(b));
+                    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(dif) : "l"(a), "l"(b));
+                    bits_pair(sum, w[r], w[r + 1]);
+                    bits_pair(dif, w[r + h], w[r + h + 1]);
                 }
             }
         }
@@ -634,16 +668,37 @@ struct SumsRangeParams {
     double t_over_sqrt_n;
 };
 
-__global__ void __launch_bounds__(kThreads) rht_range_from_sums(const __grid_constant__ SumsRangeParams p) {
+// One warp per worker (warps loop over the workers when P > 32): each lane
+// adds a fixed stride of the worker's tiles with four accumulators, the warp
+// adds the lanes' sums in a fixed order; thread 0 takes the largest.
+constexpr int kRangeThreads = 1024;
+__global__ void __launch_bounds__(kRangeThreads) rht_range_from_sums(const __grid_constant__ SumsRangeParams p) {
+    __shared__ double s_best[kRangeThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     double best = 0.0;
-    for (int w = 0; w < p.P; ++w) {
-        double acc = 0.0;
-        for (int64_t i = threadIdx.x; i < p.tiles; i += kThreads) acc += p.sums[w][i];
-        acc = block_sum(acc);
-        if (threadIdx.x == 0 && acc > best) best = acc;
+    for (int w = warp; w < p.P; w += kRangeThreads / 32) {
+        const double *x = p.sums[w];
+        double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
+        int64_t i = lane;
+        for (; i + 96 < p.tiles; i += 128) {
+            a0 += x[i];
+            a1 += x[i + 32];
+            a2 += x[i + 64];
+            a3 += x[i + 96];
+        }
+        for (; i < p.tiles; i += 32) a0 += x[i];
+        double acc = (a0 + a1) + (a2 + a3);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        if (acc > best) best = acc;
     }
+    if (lane == 0) s_best[warp] = best;
+    __syncthreads();
     if (threadIdx.x == 0) {
-        const float M = static_cast<float>(p.t_over_sqrt_n * sqrt(best));
+        double m = 0.0;
+        for (int i = 0; i < kRangeThreads / 32; ++i)
+            if (s_best[i] > m) m = s_best[i];
+        const float M = static_cast<float>(p.t_over_sqrt_n * sqrt(m));
         p.mM[0] = -M;
         p.mM[1] = M;
     }
@@ -934,7 +989,7 @@ extern "C" int gar_rht_norm_range_from_sums(const double *const *d_sumsq, int32_
     p.tiles = gar_rht_tiles(n);
     p.mM = d_mM;
     p.t_over_sqrt_n = t_p / std::sqrt(static_cast<double>(n));
-    rht_range_from_sums<<<1, kThreads, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(p);
+    rht_range_from_sums<<<1, kRangeThreads, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(p);
     return check_launch("rht_range_from_sums");
 }
 
