@@ -41,6 +41,9 @@ CASES = [
     ("thc_fused_packed", []), ("thc_plan", []), ("thc_plan_nmse", []), ("nuhc_fused", []),
     ("nuhc_fused_packed", []), ("nmse", []), ("rht", []), ("rht_inv", []), ("rht_norm", []), ("ef_apply", []),
     ("checksum", ["--N", "268435456"]),
+    ("stream_ring", ["--P", "4", "--N", "1048576", "--k", "64"]),
+    ("stream_thc", ["--P", "4", "--N", "1048576", "--k", "64"]),
+    ("train_step", []), ("train_step_fused", []),
 ]
 LIB_KERNEL = re.compile(r"(ring_fold|ring_step|ring_divide|copy_jobs|pack_all|pack_range_init|range_reset|thc_|"
                         r"nuhc_|nmse_|rht_|ef_kernel|dbtree_|checksum_)")
