@@ -668,39 +668,43 @@ struct SumsRangeParams {
     double t_over_sqrt_n;
 };
 
-// One warp per worker (warps loop over the workers when P > 32): each lane
-// adds a fixed stride of the worker's tiles with four accumulators, the warp
-// adds the lanes' sums in a fixed order; thread 0 takes the largest.
+// One CTA per worker: each thread adds a fixed stride of the worker's tiles
+// (four loads in flight), the CTA adds the threads' sums in a fixed order
+// (fp64), and the worker's M = (t_p / sqrt(n)) l goes into d_mM by atomic
+// max / min on the float bits (M >= 0: the bit patterns order as the values;
+// the result does not depend on the order of the CTAs).  rht_range_init sets
+// d_mM to (+0, +0) first.
 constexpr int kRangeThreads = 1024;
+__global__ void rht_range_init(float *mM) {
+    mM[0] = 0.0f;
+    mM[1] = 0.0f;
+}
+
 __global__ void __launch_bounds__(kRangeThreads) rht_range_from_sums(const __grid_constant__ SumsRangeParams p) {
-    __shared__ double s_best[kRangeThreads / 32];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    double best = 0.0;
-    for (int w = warp; w < p.P; w += kRangeThreads / 32) {
-        const double *x = p.sums[w];
-        double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
-        int64_t i = lane;
-        for (; i + 96 < p.tiles; i += 128) {
-            a0 += x[i];
-            a1 += x[i + 32];
-            a2 += x[i + 64];
-            a3 += x[i + 96];
-        }
-        for (; i < p.tiles; i += 32) a0 += x[i];
-        double acc = (a0 + a1) + (a2 + a3);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-        if (acc > best) best = acc;
+    __shared__ double s_part[kRangeThreads / 32];
+    const double *x = p.sums[blockIdx.x];
+    double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
+    int64_t i = threadIdx.x;
+    constexpr int T = kRangeThreads;
+    for (; i + 3 * T < p.tiles; i += 4 * T) {
+        a0 += x[i];
+        a1 += x[i + T];
+        a2 += x[i + 2 * T];
+        a3 += x[i + 3 * T];
     }
-    if (lane == 0) s_best[warp] = best;
+    for (; i < p.tiles; i += T) a0 += x[i];
+    double acc = (a0 + a1) + (a2 + a3);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) s_part[warp] = acc;
     __syncthreads();
     if (threadIdx.x == 0) {
-        double m = 0.0;
-        for (int i = 0; i < kRangeThreads / 32; ++i)
-            if (s_best[i] > m) m = s_best[i];
-        const float M = static_cast<float>(p.t_over_sqrt_n * sqrt(m));
-        p.mM[0] = -M;
-        p.mM[1] = M;
+        double l2 = 0.0;
+        for (int w = 0; w < kRangeThreads / 32; ++w) l2 += s_part[w];
+        const float M = static_cast<float>(p.t_over_sqrt_n * sqrt(l2));
+        atomicMax(reinterpret_cast<int *>(p.mM + 1), __float_as_int(M));
+        atomicMax(reinterpret_cast<unsigned int *>(p.mM), __float_as_uint(-M));  // negative floats: larger bits, smaller value
     }
 }
 
@@ -989,7 +993,11 @@ extern "C" int gar_rht_norm_range_from_sums(const double *const *d_sumsq, int32_
     p.tiles = gar_rht_tiles(n);
     p.mM = d_mM;
     p.t_over_sqrt_n = t_p / std::sqrt(static_cast<double>(n));
-    rht_range_from_sums<<<1, kRangeThreads, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(p);
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    rht_range_init<<<1, 1, 0, stream>>>(d_mM);
+    rc = check_launch("rht_range_init");
+    if (rc) return rc;
+    rht_range_from_sums<<<static_cast<unsigned>(P), kRangeThreads, 0, stream>>>(p);
     return check_launch("rht_range_from_sums");
 }
 
