@@ -55,6 +55,29 @@ __device__ __forceinline__ void bits_pair(uint64_t v, float &a, float &b) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
 }
 
+// L2 priorities of the transform's intermediate vector: the passes before the
+// last write it with an evict-last policy (the next launch reads it back, so
+// it should stay in L2 while the streams around it pass through) and the
+// next launch reads it with an evict-first one (it is read once).
+__device__ __forceinline__ uint64_t l2_keep_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_once_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void st_policy(float *a, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(a), "f"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ float ld_policy(const float *a, uint64_t pol) {
+    float v;
+    asm volatile("ld.global.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(a), "l"(pol) : "memory");
+    return v;
+}
+
 // Butterfly stages over v[0..15] on the register-index bits >= lo_bit.  The
 // stages on bits 1..3 take the neighbouring registers (v[r], v[r + 1]) as
 // one f32x2 operand (each lane rounded as the scalar add or subtract), two
@@ -281,6 +304,7 @@ __global__ void __launch_bounds__(kThreads) rht_tile_kernel(const __grid_constan
     for (int r = 0; r < 16; ++r) v[r] = s[tile_swz(b2 | (r << 6))];
     butterfly16(v);
     float *dst = p.out + base;
+    const uint64_t keep = l2_keep_policy();
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
         const int e = b2 | (r << 6);
@@ -291,7 +315,7 @@ __global__ void __launch_bounds__(kThreads) rht_tile_kernel(const __grid_constan
         }
         if constexpr (kEfOut) __stcs(p.ef + base + e, __fsub_rn(xr[r], y));  // e = (grad + e) - x_hat
         else if (p.last) __stcs(dst + e, y);
-        else dst[e] = y;  // the next pass reads it: normal priority, so that it can stay in L2
+        else st_policy(dst + e, y, keep);  // the next pass reads it back
     }
 }
 
@@ -323,8 +347,9 @@ __global__ void __launch_bounds__(kThreads) rht_pass_kernel(const __grid_constan
         for (int j = 0; j < 16; ++j) v[j] = decode_at(p, d, s_tab, col0 + (static_cast<int64_t>((mh << 4) | j) << p.s));
     } else {
         const float *x = p.in + col0;
+        const uint64_t once = l2_once_policy();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = x[static_cast<int64_t>((mh << 4) | j) << p.s];  // may be the launch before's
+        for (int j = 0; j < 16; ++j) v[j] = ld_policy(x + (static_cast<int64_t>((mh << 4) | j) << p.s), once);
     }
     butterfly16(v, p.lo_bit);
 #pragma unroll
@@ -335,11 +360,12 @@ __global__ void __launch_bounds__(kThreads) rht_pass_kernel(const __grid_constan
     for (int j = 0; j < 16; ++j) v[j] = s[pass_swz((j << 8) | (mh << 4) | c)];
     butterfly16(v, p.lo_bit > 4 ? p.lo_bit - 4 : 0);
     float *y = p.out + col0;
+    const uint64_t keep = l2_keep_policy();
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const int64_t off = static_cast<int64_t>((j << 4) | mh) << p.s;
         if (p.last) __stcs(y + off, __fmul_rn(v[j], p.scale));
-        else y[off] = v[j];  // the next launch reads it: normal priority, so that it can stay in L2
+        else st_policy(y + off, v[j], keep);  // the next launch reads it back
     }
 }
 
@@ -400,8 +426,9 @@ __global__ void __launch_bounds__(kThreads) rht_cluster_pass_kernel(const __grid
         for (int j = 0; j < 16; ++j) v[j] = decode_at(p, d, s_tab, col0 + (static_cast<int64_t>((mh << 4) | j) << p.s));
     } else {
         const float *x = p.in + col0;
+        const uint64_t once = l2_once_policy();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = x[static_cast<int64_t>((mh << 4) | j) << p.s];  // may be the launch before's
+        for (int j = 0; j < 16; ++j) v[j] = ld_policy(x + (static_cast<int64_t>((mh << 4) | j) << p.s), once);
     }
     butterfly16(v);
 #pragma unroll
@@ -450,11 +477,12 @@ __global__ void __launch_bounds__(kThreads) rht_cluster_pass_kernel(const __grid
             }
         }
         float *y = p.out + base + c;
+        const uint64_t keep = l2_keep_policy();
 #pragma unroll
         for (int r = 0; r < K; ++r) {
             float *dst = y + (static_cast<int64_t>((r << 8) | m) << p.s);
             if (p.last) __stcs(dst, __fmul_rn(w[r], p.scale));
-            else *dst = w[r];
+            else st_policy(dst, w[r], keep);  // the next launch reads it back
         }
     }
     cluster_sync_exit();  // no CTA leaves while another still reads its shared memory
