@@ -102,3 +102,66 @@ def test_graph_replay_equals_eager(env):
     graph.replay()
     torch.cuda.synchronize()
     _same(_results(st), eager2)
+
+
+def test_two_stream_step_captured(env):
+    """The bucketed step the benchmark times (gradient_allreduce_homomorphic_gb300
+    .pipeline: ring of each fusion buffer on one stream, THC of buffer b on a
+    second stream behind an event, NMSE after both) captured as one graph:
+    the side streams fork from and join the capturing stream, and a replay
+    gives the eager step's results bit for bit, following new inputs."""
+    torch, g = env
+    from gradient_allreduce_homomorphic_gb300 import pipeline
+
+    sizes = workloads.log_uniform_sizes(60, 256, 300_000, 2_000_000, [12, 999]).astype(np.int64)
+    offs = pipeline.flat_offsets(sizes)
+    grads = [torch.empty(int(offs[-1]), device="cuda") for _ in range(P)]
+
+    def fill(seed):
+        for w, f in enumerate(grads):
+            f.copy_(torch.from_numpy(workloads.normal_f32(int(offs[-1]), 0.01, seed, w)))
+
+    st = pipeline.AveragingStep(grads, sizes, offs, b=B_THC, capacity_bytes=1 << 20, align_bytes=16)
+    assert st.nb > 2
+
+    def results():
+        return ([f.cpu().numpy().view(np.uint32).copy() for f in st.ring_flat],
+                st.thc_flat.cpu().numpy().view(np.uint32).copy(), st.mM.cpu().numpy().view(np.uint32).copy(),
+                [[t.cpu().numpy().copy() for t in row] for row in st.packed], st.nmse.cpu().numpy().view(np.uint64))
+
+    def same(a, b):
+        for x, y in zip(a[0], b[0]):
+            assert np.array_equal(x, y), "ring average"
+        assert np.array_equal(a[1], b[1]), "THC average"
+        assert np.array_equal(a[2], b[2]), "ranges"
+        for ra, rb in zip(a[3], b[3]):
+            for x, y in zip(ra, rb):
+                assert np.array_equal(x, y), "wire words"
+        assert np.array_equal(a[4], b[4]), "NMSE"
+
+    fill(401)
+    st.run(SEED)
+    torch.cuda.synchronize()
+    eager = results()
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            st.run(SEED)
+    torch.cuda.synchronize()
+    for f in st.ring_flat:
+        f.zero_()
+    st.thc_flat.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    same(results(), eager)
+    fill(402)
+    st.run(SEED)
+    torch.cuda.synchronize()
+    eager2 = results()
+    assert not np.array_equal(eager2[1], eager[1])
+    fill(402)
+    graph.replay()
+    torch.cuda.synchronize()
+    same(results(), eager2)
