@@ -212,8 +212,8 @@ double oracle_nmse(const float *x, const float *x_hat, int64_t n);
 double oracle_nmse_f64(const double *x, const double *x_hat, int64_t n);
 
 /* ---------------- wire-vector checksum ---------------- */
-/* Silent-data-corruption check of the packed indices (the survey's plan for
- * failure detection; the pages fix no checksum): s1 = sum w_i and
+/* Silent-data-corruption check of the packed indices, for failure
+ * detection (the pages fix no checksum): s1 = sum w_i and
  * s2 = sum (i + 1) w_i over the n 32-bit words, both mod 2^32; returns
  * (s2 << 32) | s1.  s1 changes with any flipped bit; a swap of words i and j
  * changes s2 by (j - i)(w_i - w_j) mod 2^32, so only swaps where that product
