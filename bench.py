@@ -12,9 +12,10 @@ log-uniform sizes 256..2.4M, N(0, 0.01)), 64 MB fusion buffers:
      integer aggregate + decode, read straight from the
      tensors, average written straight to the output
      tensors, wire vectors written (b = 4, fresh seed each step)
-  4. NMSE of the THC average against the ring average       gar_nmse
-     (--nmse fused: its sums taken inside step 3,           gar_thc_allreduce_fused_plan_nmse,
-     then combined)                                         gar_nmse_combine
+  4. NMSE of the THC average against the ring average:      gar_thc_allreduce_fused_plan_nmse,
+     its sums taken inside step 3 (one more read of the     gar_nmse_combine
+     ring average), then combined (--nmse separate: one     (gar_nmse)
+     pass over both averages at the end)
 
 The fused calls give bit for bit what pack -> ring / THC -> unpack gives
 (the tests hold them to that); the fusion buffers are never materialised.
@@ -146,7 +147,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ GPU (ours)
-def make_step(dev, nmse="separate"):
+def make_step(dev, nmse="fused"):
     """The benchmark's workload on the device: every worker's 300 gradient
     tensors as 16-byte-aligned views of one flat buffer (as a framework's
     flat gradient buffer), seeded N(0, 0.01), and the bucketed averaging step
@@ -868,7 +869,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--schedule", choices=["overlap", "serial"], default="overlap")
     ap.add_argument("--h2d-streams", type=int, default=2, help="copy streams for the end-to-end inputs")
-    ap.add_argument("--nmse", choices=["fused", "separate"], default="separate",
+    ap.add_argument("--nmse", choices=["fused", "separate"], default="fused",
                     help="NMSE sums inside the THC pass, or one NMSE pass over both averages at the end")
     ap.add_argument("--reference-budget-s", type=float, default=100.0,
                     help="seconds of oracle work for the whole --impl reference run")

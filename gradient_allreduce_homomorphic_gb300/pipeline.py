@@ -11,9 +11,10 @@ The step runs every row of the path through the library's entry points:
      THC indices (the wire vectors), their integer sum and the
      decode, read straight from the tensors and written straight
      to the output tensors
-  4. the NMSE of the compressed average against the exact one   gar_nmse
-     (or its sums inside step 3, then combined)                 gar_thc_allreduce_fused_plan_nmse,
-                                                                gar_nmse_combine
+  4. the NMSE of the compressed average against the exact one:  gar_thc_allreduce_fused_plan_nmse,
+     its sums taken inside step 3 (one more read of the exact   gar_nmse_combine
+     average), then combined (nmse="separate": one pass over    (gar_nmse)
+     both averages at the end)
 
 Overlap ([R] "8. Compute-Communication Overlapping & Gradient Bucketing"):
 fusion buffers are the buckets.  The ring runs on one stream, bucket after
@@ -61,7 +62,7 @@ class AveragingStep:
     b, ``mM[b]`` that buffer's range, ``nmse`` the step's NMSE."""
 
     def __init__(self, grads, sizes, offsets=None, *, b: int = 4, capacity_bytes: int = 64 << 20,
-                 align_bytes: int = 16, nmse: str = "separate"):
+                 align_bytes: int = 16, nmse: str = "fused"):
         import torch
 
         if nmse not in ("separate", "fused"):
