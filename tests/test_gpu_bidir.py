@@ -3,8 +3,8 @@
 fp32 against the oracle's two-ring fold (itself equal to its literal
 schedule), bf16 against the same fold on the exactly widened inputs rounded
 to bf16, the hand-derived ordering example, ragged and degenerate sizes,
-P up to 64 (128 sub-chunks), and the full-size bf16 bucket on sampled
-elements.
+P up to 64 (128 sub-chunks), and the full-size bf16 bucket (P=16, 2^28
+elements per worker) on every element.
 """
 import json
 import os

@@ -4,7 +4,7 @@ fp32 and bf16 against the oracle's two-tree fold (itself equal to its literal
 reduce + broadcast schedule), the hand-derived P=4 fold expressions, every P
 from 1 to 64, ragged sizes (the group that straddles the two halves, the
 ragged last group), unaligned buffers (the element-wise path), and the
-full-size bf16 bucket (P=16, 2^28 elements per worker) on sampled elements.
+full-size bf16 bucket (P=16, 2^28 elements per worker) on every element.
 """
 import numpy as np
 import pytest

@@ -4,8 +4,8 @@ Bit-exact against the oracle: pack reproduces the oracle's fusion buffer
 (zero padding included), unpack restores the tensors, and the one-pass
 fused all-reduce equals the oracle's pack -> ring fold -> unpack and the
 library's own pack -> ring -> unpack pipeline.  Full-size ResNet-like plan
-(300 tensors, P=8) compared in full; VGG-like plan (P=8, 138M parameters)
-compared on sampled elements including every fusion buffer's chunk edges.
+(300 tensors, P=8) and VGG-like plan (P=8, 138M parameters) compared on
+every element of every worker.
 """
 import numpy as np
 import pytest

@@ -5,7 +5,7 @@ averages are within 1e-6 * max(|m|, |M|) of the oracle's fp64 decode (the
 fp32 decode takes four roundings of at most 2^-24 of the range each); the
 fused kernel equals decode(aggregate(encode)) bit for bit; NMSE is within
 2e-6 relative of the oracle's fp64 sum.  Full-size THC sweep (N = 2^24,
-P in {4, 16, 64}, b in {2, 4, 8}) checked on sampled elements.
+P in {4, 16, 64}, b in {2, 4, 8}) checked on every element.
 """
 import numpy as np
 import pytest
