@@ -76,6 +76,16 @@ __device__ __forceinline__ uint32_t nuhc_index(float x, float m, float sc, float
 // (each lane rounded exactly as the scalar operation, subnormals kept); the
 // clamp, the table lookups and the comparisons stay per element.  Bit for bit
 // equal to two nuhc_index calls.
+__device__ __forceinline__ uint64_t add_rn_f2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma_rm_f2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rm.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
 __device__ __forceinline__ uint64_t fma_rn_f2(uint64_t a, uint64_t b, uint64_t c) {
     uint64_t r;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
@@ -172,9 +182,13 @@ __device__ __forceinline__ void nuhc_direct2(float x0, float x1, uint64_t m2, ui
     const uint64_t lo = pack_f2(lo0, lo1), hi = pack_f2(hi0, hi1);
     const uint64_t one_u = pack_f2(__uint_as_float((r0 & 0x007FFFFFu) | 0x3F800000u),
                                    __uint_as_float((r1 & 0x007FFFFFu) | 0x3F800000u));
-    const uint64_t neg_u = sub_rn_f2(pack_f2(1.0f, 1.0f), one_u);
-    const float2 f = unpack_f2(fma_rn_f2(neg_u, sub_rn_f2(hi, lo), sub_rn_f2(t2, lo)));
-    const bool up0 = f.x > 0.0f, up1 = f.y > 0.0f;
+    // up iff lo + u w < t (w = hi - lo), decided exactly as (lo + u w) rounded
+    // down < t: rounding down never passes the float t.  lo + u w is formed
+    // with one rounding as fma((1 + u), w, lo - w); w and lo - w are exact
+    // (integers below 2^15).  Equal to nuhc_index's fma(-u, w, t - lo) > 0.
+    const uint64_t w = sub_rn_f2(hi, lo);
+    const float2 v = unpack_f2(fma_rm_f2(one_u, w, sub_rn_f2(lo, w)));
+    const bool up0 = v.x < t.x, up1 = v.y < t.y;
     tv0 = up0 ? hi0 : lo0;
     tv1 = up1 ? hi1 : lo1;
     if (kZ) {
@@ -328,10 +342,15 @@ __device__ __forceinline__ void nuhc_one_worker(const float4 (&v)[G4], float (&s
             nuhc_index2(v[g4].x, v[g4].y, m2, sc2, G, p.tab.g, s_pair, s_inv, r.x, r.y, i0, i1, t0, t1);
             nuhc_index2(v[g4].z, v[g4].w, m2, sc2, G, p.tab.g, s_pair, s_inv, r.z, r.w, i2, i3, t2, t3);
         }
-        s[4 * g4] = __fadd_rn(s[4 * g4], t0);
-        s[4 * g4 + 1] = __fadd_rn(s[4 * g4 + 1], t1);
-        s[4 * g4 + 2] = __fadd_rn(s[4 * g4 + 2], t2);
-        s[4 * g4 + 3] = __fadd_rn(s[4 * g4 + 3], t3);
+        // the running sums, two per f32x2 add (each lane rounded as __fadd_rn)
+        {
+            float2 a = unpack_f2(add_rn_f2(pack_f2(s[4 * g4], s[4 * g4 + 1]), pack_f2(t0, t1)));
+            float2 c = unpack_f2(add_rn_f2(pack_f2(s[4 * g4 + 2], s[4 * g4 + 3]), pack_f2(t2, t3)));
+            s[4 * g4] = a.x;
+            s[4 * g4 + 1] = a.y;
+            s[4 * g4 + 2] = c.x;
+            s[4 * g4 + 3] = c.y;
+        }
         if (kPacked) word |= (i0 | (i1 << B) | (i2 << (2 * B)) | (i3 << (3 * B))) << (4 * g4 * B);
     }
     if (kPacked) __stcs(p.packed[wk] + w, word);
