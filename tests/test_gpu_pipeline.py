@@ -77,7 +77,7 @@ def steps():
     return torch, sizes, offs, out, refs
 
 
-def _check(sizes, offs, snap, ref):
+def _check(sizes, offs, snap, ref, workers=P):
     sb, so, bn, per = ref
     flat_len = int(offs[-1])
     ring = np.zeros(flat_len, np.float32)
@@ -86,7 +86,7 @@ def _check(sizes, offs, snap, ref):
         for i, o in enumerate(outs):
             if o is not None:
                 ring[int(offs[i]):int(offs[i]) + int(sizes[i])] = o
-    for w in range(P):  # every worker's copy of the exact average, bit for bit
+    for w in range(workers):  # every worker's copy of the exact average, bit for bit
         got = to_host(snap["ring"][w])
         bad = np.nonzero(got.view(np.uint32) != ring.view(np.uint32))[0]
         assert bad.size == 0, f"worker {w}: {bad.size} ring values differ, first at flat {bad[0]}"
@@ -95,7 +95,7 @@ def _check(sizes, offs, snap, ref):
     for k in range(len(bn)):
         m, M = per[k]["mM"]
         assert (mM[k, 0], mM[k, 1]) == (m, M), f"buffer {k} range"
-        for w in range(P):
+        for w in range(workers):
             words = to_host(snap["packed"][w][k])[: per[k]["packed"][w].size]
             np.testing.assert_array_equal(words, per[k]["packed"][w], err_msg=f"buffer {k} worker {w} wire words")
         tol = 1e-6 * max(abs(float(m)), abs(float(M)))
@@ -161,3 +161,27 @@ def test_bench_step_from_host(steps):
     assert np.array_equal(host_ring.numpy().view(np.uint32), to_host(snap2["ring"][0]).view(np.uint32))
     assert np.array_equal(host_thc.numpy().view(np.uint32), to_host(snap2["thc"]).view(np.uint32))
     assert host_nmse.numpy()[0] == float(to_host(snap2["nmse"])[0])
+
+
+@pytest.mark.parametrize("P_,b,mode", [(3, 2, "separate"), (5, 8, "fused"), (1, 4, "fused")])
+def test_small_step_other_worker_counts(P_, b, mode):
+    """The bucketed step with worker counts that take the any-P kernel builds
+    (and one worker), small fusion buffers (many buckets), against the oracle."""
+    torch, g = need_cuda()
+    from gradient_allreduce_homomorphic_gb300 import pipeline
+
+    sizes = np.array([1, 4096, 77, 3000, 5, 20000, 12345, 2], np.int64)
+    offs = pipeline.flat_offsets(sizes)
+    host_flat = [np.random.default_rng([211, P_, w]).standard_normal(int(offs[-1])).astype(np.float32)
+                 for w in range(P_)]
+    grads = [torch.from_numpy(f).cuda() for f in host_flat]
+    cap = 32 << 10
+    st = pipeline.AveragingStep(grads, sizes, offs, b=b, capacity_bytes=cap, align_bytes=16, nmse=mode)
+    assert st.nb > 2
+    seed = 0x5EED + P_
+    st.run(seed)
+    st.run(seed)  # twice: the second step must give the same results
+    torch.cuda.synchronize()
+    host = [[f[int(offs[i]):int(offs[i]) + int(s)] for i, s in enumerate(sizes)] for f in host_flat]
+    ref = fusion_step(host, sizes, cap, 16, b, seed)
+    _check(sizes, offs, _snapshot(st), ref, workers=P_)
