@@ -130,6 +130,7 @@ struct RhtParams {
     int32_t has_tab;         // kInPacked: index z stands for tab[z] (non-uniform THC), else for z
     float steps;             // kInPacked: grid steps between m and M (2^b - 1, or the granularity g)
     int32_t b_log;           // kInPacked: log2 b (indices per word 32 / b = 2^(5 - b_log))
+    int32_t discard_in;      // kEfOut: the scratch p.out (128-byte aligned) may leave L2 unwritten once read
     uint16_t tab[256];       // kInPacked with has_tab: the table T
 };
 
@@ -282,6 +283,15 @@ __global__ void __launch_bounds__(kThreads) rht_tile_kernel(const __grid_constan
         *reinterpret_cast<float4 *>(&s[tile_swz((q << 10) | (t << 2))]) =
             make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     __syncthreads();
+    if constexpr (kEfOut && kIn == kInPlain) {
+        // the last kernel of the update reads the scratch intermediate
+        // (p.in == p.out == tmp) once, all of this tile by now: its dirty
+        // lines leave L2 without being written back to DRAM.  (Where the
+        // tile kernel is the only kernel, n = 4096, it decodes the packed
+        // indices and there is no intermediate.)
+        if (p.discard_in && t < kTile * 4 / 128)
+            asm volatile("discard.global.L2 [%0], 128;" ::"l"(p.in + base + 32 * t) : "memory");
+    }
     // bits 2..5 in registers: element (t & 3) | (r << 2) | ((t >> 2) << 6)
     const int b1 = (t & 3) | ((t >> 2) << 6);
 #pragma unroll
@@ -998,6 +1008,7 @@ extern "C" int gar_rht_ef_update(const uint32_t *packed, int32_t b, int32_t step
     p->b_log = b == 1 ? 0 : (b == 2 ? 1 : (b == 4 ? 2 : 3));
     p->steps = static_cast<float>(steps);
     p->has_tab = table ? 1 : 0;
+    p->discard_in = aligned(tmp, 128) ? 1 : 0;
     if (table)
         for (int z = 0; z <= L; ++z) p->tab[z] = table[z];
     return rht_run<kInPacked, false, true>(*p, reinterpret_cast<cudaStream_t>(stream_));

@@ -562,8 +562,10 @@ int gar_rht_norm_range_from_sums(const double *const *d_sumsq, int32_t P, int64_
  * aligned); table: host, 2^b entries from 0 to steps, strictly increasing,
  * or NULL; d_mM: device [m, M]; grad, e: device, n fp32 (e read and
  * rewritten in place); tmp: device scratch of n fp32 for the transform's
- * intermediate passes (caller-owned, not shared with a concurrent call);
- * grad, e, tmp 16-byte aligned and pairwise disjoint.
+ * intermediate passes (caller-owned, not shared with a concurrent call; its
+ * contents after the call are undefined: where it is 128-byte aligned its
+ * cache lines are dropped from L2 unwritten once read); grad, e, tmp
+ * 16-byte aligned and pairwise disjoint.
  * Errors: GAR_EINVAL (n, b, steps, table, NULL, overlap), GAR_EALIGN,
  * GAR_ECUDA. */
 int gar_rht_ef_update(const uint32_t *packed, int32_t b, int32_t steps, const uint16_t *table,
