@@ -127,14 +127,18 @@ __device__ __forceinline__ void nuhc_index2(float x0, float x1, uint64_t m2, uin
 // lookup clamps k to g - 1, which lies in the same last interval.
 constexpr int kDirectMaxG = 1023;
 constexpr int kDirectCap = kDirectMaxG + 1;
-// s_lo[kDirectCap], s_hi[kDirectCap] (floats), s_z[kDirectCap] (bytes), then T itself
-constexpr size_t kDirectBytes = kDirectCap * (2 * sizeof(float) + 1) + 256 * sizeof(uint16_t);
+// s_lo[kDirectCap], s_hi[kDirectCap], s_zb[kDirectCap] (floats; s_zb[k] = z + 2^23, exact),
+// s_z[kDirectCap] (bytes), then T itself
+constexpr size_t kDirectBytes = kDirectCap * (3 * sizeof(float) + 1) + 256 * sizeof(uint16_t);
+constexpr float kTwo23 = 8388608.0f;
+constexpr uint32_t kTwo23Bits = 0x4B000000u;  // the bits of 2^23; of z + 2^23: kTwo23Bits + z
 
 __device__ __forceinline__ void nuhc_load_direct(const NuhcTable &tab, unsigned char *mem, float *&s_lo,
                                                  uint8_t *&s_z) {
     s_lo = reinterpret_cast<float *>(mem);
     float *s_hi = s_lo + kDirectCap;
-    s_z = reinterpret_cast<uint8_t *>(s_hi + kDirectCap);
+    float *s_zb = s_hi + kDirectCap;
+    s_z = reinterpret_cast<uint8_t *>(s_zb + kDirectCap);
     uint16_t *s_t = reinterpret_cast<uint16_t *>(s_z + kDirectCap);
     for (int z = threadIdx.x; z <= tab.L; z += blockDim.x) s_t[z] = tab.t[z];
     __syncthreads();
@@ -147,6 +151,7 @@ __device__ __forceinline__ void nuhc_load_direct(const NuhcTable &tab, unsigned 
         }
         s_lo[k] = static_cast<float>(s_t[lo]);
         s_hi[k] = static_cast<float>(s_t[lo + 1]);
+        s_zb[k] = kTwo23 + static_cast<float>(lo);
         s_z[k] = static_cast<uint8_t>(lo);
     }
     __syncthreads();
@@ -195,6 +200,51 @@ __device__ __forceinline__ void nuhc_direct2(float x0, float x1, uint64_t m2, ui
         i0 = static_cast<uint32_t>(s_z[k0]) + (up0 ? 1u : 0u);
         i1 = static_cast<uint32_t>(s_z[k1]) + (up1 ? 1u : 0u);
     }
+}
+
+// nuhc_direct2 for the fused kernel, adding the two elements' table values
+// T[index] to their running sums (an f32x2 pair) as sum + lo + up * w, up =
+// 1.0 or 0.0 the comparison's value: one add and one FMA, exact (integers
+// below 2^24), with no select.  kZ: also the indices, biased: the bits of
+// z + up + 2^23 (z + 2^23 from s_zb, exact) are kTwo23Bits + index.
+template <bool kZ>
+__device__ __forceinline__ void nuhc_direct2_sum(float x0, float x1, uint64_t m2, uint64_t sc2, float G,
+                                                 const float *s_lo, uint32_t r0, uint32_t r1, uint64_t &sum,
+                                                 uint32_t &a0, uint32_t &a1) {
+    float2 t = unpack_f2(mul_rn_f2(sub_rn_f2(pack_f2(x0, x1), m2), sc2));
+    t.x = fminf(fmaxf(t.x, 0.0f), G);
+    t.y = fminf(fmaxf(t.y, 0.0f), G);
+    const uint64_t t2 = pack_f2(t.x, t.y);
+    const float2 jm = unpack_f2(add_rm_f2(t2, pack_f2(kTwo23, kTwo23)));  // floor(t) + 2^23
+    const int k0 = __float_as_int(jm.x) - 0x4B000000, k1 = __float_as_int(jm.y) - 0x4B000000;  // 0..g
+    const uint64_t lo = pack_f2(s_lo[k0], s_lo[k1]);
+    const uint64_t hi = pack_f2(s_lo[kDirectCap + k0], s_lo[kDirectCap + k1]);
+    const uint64_t one_u = pack_f2(__uint_as_float((r0 & 0x007FFFFFu) | 0x3F800000u),
+                                   __uint_as_float((r1 & 0x007FFFFFu) | 0x3F800000u));
+    // up iff RD(lo + u w) < t, as in nuhc_direct2
+    const uint64_t w = sub_rn_f2(hi, lo);
+    const float2 v = unpack_f2(fma_rm_f2(one_u, w, sub_rn_f2(lo, w)));
+    float u0, u1;
+    asm("set.lt.f32.f32 %0, %1, %2;" : "=f"(u0) : "f"(v.x), "f"(t.x));
+    asm("set.lt.f32.f32 %0, %1, %2;" : "=f"(u1) : "f"(v.y), "f"(t.y));
+    const uint64_t up = pack_f2(u0, u1);
+    sum = fma_rn_f2(up, w, add_rn_f2(sum, lo));
+    if (kZ) {
+        const float2 ib =
+            unpack_f2(add_rn_f2(pack_f2(s_lo[2 * kDirectCap + k0], s_lo[2 * kDirectCap + k1]), up));
+        a0 = __float_as_uint(ib.x);
+        a1 = __float_as_uint(ib.y);
+    }
+}
+
+// Sum over the fields of a packed word of (kTwo23Bits << field shift), mod
+// 2^32: the biased indices packed with plain shifted adds, minus this once,
+// leave the exact word (the fields never overlap).
+template <int B>
+__host__ __device__ constexpr uint32_t zb_pack_bias() {
+    uint32_t s = 0;
+    for (int i = 0; i < 32 / B; ++i) s += (i * B < 32 ? kTwo23Bits << (i * B) : 0u);
+    return s;
 }
 
 struct NuhcEncodeParams {
@@ -328,17 +378,34 @@ __device__ __forceinline__ void nuhc_one_worker(const float4 (&v)[G4], float (&s
                                                 int wk, const NuhcFusedParams &p, uint64_t m2, uint64_t sc2, float G,
                                                 const float2 *s_pair, const uint8_t *s_inv) {
     uint32_t word = 0;
+    if constexpr (kDirect) {
+        // direct tables: s_pair holds s_lo (then s_hi, s_zb)
+        const float *s_lo = reinterpret_cast<const float *>(s_pair);
+#pragma unroll
+        for (int g4 = 0; g4 < G4; ++g4) {
+            const uint4 r = philox_block((e0 >> 2) + g4, wk, p.keys);
+            uint64_t s01 = pack_f2(s[4 * g4], s[4 * g4 + 1]), s23 = pack_f2(s[4 * g4 + 2], s[4 * g4 + 3]);
+            uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+            nuhc_direct2_sum<kPacked>(v[g4].x, v[g4].y, m2, sc2, G, s_lo, r.x, r.y, s01, a0, a1);
+            nuhc_direct2_sum<kPacked>(v[g4].z, v[g4].w, m2, sc2, G, s_lo, r.z, r.w, s23, a2, a3);
+            const float2 f01 = unpack_f2(s01), f23 = unpack_f2(s23);
+            s[4 * g4] = f01.x;
+            s[4 * g4 + 1] = f01.y;
+            s[4 * g4 + 2] = f23.x;
+            s[4 * g4 + 3] = f23.y;
+            if (kPacked)
+                word += (a0 << (4 * g4 * B)) + (a1 << ((4 * g4 + 1) * B)) + (a2 << ((4 * g4 + 2) * B)) +
+                        (a3 << ((4 * g4 + 3) * B));
+        }
+        if (kPacked) __stcs(p.packed[wk] + w, word - zb_pack_bias<B>());
+        return;
+    }
 #pragma unroll
     for (int g4 = 0; g4 < G4; ++g4) {
         const uint4 r = philox_block((e0 >> 2) + g4, wk, p.keys);
         float t0, t1, t2, t3;
         uint32_t i0 = 0, i1 = 0, i2 = 0, i3 = 0;
-        if constexpr (kDirect) {
-            // direct tables: s_pair holds s_lo (then s_hi), s_inv holds s_z
-            const float *s_lo = reinterpret_cast<const float *>(s_pair);
-            nuhc_direct2<kPacked>(v[g4].x, v[g4].y, m2, sc2, G, s_lo, s_inv, r.x, r.y, i0, i1, t0, t1);
-            nuhc_direct2<kPacked>(v[g4].z, v[g4].w, m2, sc2, G, s_lo, s_inv, r.z, r.w, i2, i3, t2, t3);
-        } else {
+        {
             nuhc_index2(v[g4].x, v[g4].y, m2, sc2, G, p.tab.g, s_pair, s_inv, r.x, r.y, i0, i1, t0, t1);
             nuhc_index2(v[g4].z, v[g4].w, m2, sc2, G, p.tab.g, s_pair, s_inv, r.z, r.w, i2, i3, t2, t3);
         }
