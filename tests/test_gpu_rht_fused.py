@@ -147,6 +147,35 @@ def test_update_equals_separate_chain(env, k, b, g):
     assert err <= bound
 
 
+@pytest.mark.parametrize("k", [13, 21, 24])
+def test_update_scratch_alignment(env, k):
+    """Where tmp is 128-byte aligned the update's last pass drops the scratch
+    lines from L2 once read; where it is only 16-byte aligned it does not.
+    Both must give the same e, bit for bit, and both equal the separate chain."""
+    torch, gar = env
+    n, b, g, seed, q_seed = 1 << k, 4, 36, 0xA11 + k, 0xB22 + k
+    table = _table(b, g)
+    gs = workloads.student_t_f32(n, 4, 1e-2, 197, k)
+    es = workloads.normal_f32(n, 1e-6, 198, k)
+    gd, ed = to_dev(gs, torch), to_dev(es, torch)
+    y = torch.empty(n, device="cuda")
+    gar.gar_rht_ef_forward(gd, ed, y, seed)
+    mM = torch.empty(2, device="cuda")
+    gar.gar_thc_range([y], mM)
+    packed = torch.zeros(gar.gar_thc_words(n, b), dtype=torch.int32, device="cuda")
+    gar.gar_nuhc_encode(y, mM, b, g, table, q_seed, 0, packed)
+    ref_e, _, _ = _own_chain(torch, gar, packed, b, g, table, mM, gd, ed, seed)
+    base = torch.full((n + 64,), 3.0, device="cuda")
+    assert base.data_ptr() % 128 == 0
+    outs = []
+    for off in (0, 4):  # 0 B and 16 B past a 128-byte boundary
+        e = ed.clone()
+        gar.gar_rht_ef_update(packed, b, g, table, mM, gd, e, base[off:off + n], seed)
+        outs.append(to_host(e))
+    same_bits(outs[0], outs[1])
+    same_bits(outs[0], to_host(ref_e))
+
+
 def test_update_rejects_bad_tables(env):
     torch, gar = env
     n = 64
