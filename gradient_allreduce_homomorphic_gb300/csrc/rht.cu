@@ -414,31 +414,45 @@ __device__ __forceinline__ float ld_cluster(uint32_t cluster_addr) {
     return v;
 }
 
-template <int RB, int kIn>
+// The cluster pass always starts at index bit 12 (the tile pass has done bits
+// 0..11) and n <= 2^24, so its row stride 2^12 is a constant and every
+// element offset fits 32 bits: the 16 strided loads of a thread are one
+// base register and immediate offsets.  kLast: this launch writes the final
+// (scaled) values.
+constexpr int kClusterRowBit = 12;
+
+template <int RB, int kIn, bool kLast>
 __global__ void __launch_bounds__(kThreads) rht_cluster_pass_kernel(const __grid_constant__ RhtParams p) {
     constexpr int K = 1 << RB;
+    constexpr int S = kClusterRowBit;
     __shared__ float s[kTile];
     __shared__ float s_tab[kIn == kInPacked ? 256 : 1];
     const int t = threadIdx.x;
     const int c = t & 15, mh = t >> 4;
     const uint32_t q = cluster_rank();
-    const int64_t cid = static_cast<int64_t>(blockIdx.x) >> RB;
-    const int cb_bits = p.s - 4;
-    const int64_t cb = cid & ((int64_t{1} << cb_bits) - 1);
-    const int64_t hi = cid >> cb_bits;
-    const int64_t base = (hi << (p.s + 8 + RB)) | (cb << 4);  // row 0, column 0 of the cluster's block
-    const int64_t col0 = base + (static_cast<int64_t>(q) << (p.s + 8)) + c;
+    const int cid = static_cast<int>(blockIdx.x >> RB);
+    const int cb = cid & ((1 << (S - 4)) - 1);
+    const int hi = cid >> (S - 4);
+    const int base = (hi << (S + 8 + RB)) | (cb << 4);  // row 0, column 0 of the cluster's block
+    const int col0 = base + (static_cast<int>(q) << (S + 8)) + c;
     float v[16];
     if constexpr (kIn == kInPacked) {
         const Decoder d = make_decoder(p, s_tab);
         __syncthreads();
+        // rows 2^12 apart hold their indices at the same bit offset of
+        // words 2^(12 - log2(32 / b)) apart
+        const int per_log = 5 - p.b_log;
+        const int sh = (col0 & ((1 << per_log) - 1)) << p.b_log;
+        const uint32_t mask = (1u << p.b) - 1u;
+        const uint32_t *wp = p.packed + ((col0 + (mh << (S + 4))) >> per_log);
+        const int wstride = 1 << (S - per_log);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = decode_at(p, d, s_tab, col0 + (static_cast<int64_t>((mh << 4) | j) << p.s));
+        for (int j = 0; j < 16; ++j) v[j] = decode_one(p, d, s_tab, (__ldcs(wp + j * wstride) >> sh) & mask);
     } else {
-        const float *x = p.in + col0;
+        const float *x = p.in + (col0 + (mh << (S + 4)));
         const uint64_t once = l2_once_policy();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = ld_policy(x + (static_cast<int64_t>((mh << 4) | j) << p.s), once);
+        for (int j = 0; j < 16; ++j) v[j] = ld_policy(x + (j << S), once);
     }
     butterfly16(v);
 #pragma unroll
@@ -486,12 +500,12 @@ __global__ void __launch_bounds__(kThreads) rht_cluster_pass_kernel(const __grid
                 }
             }
         }
-        float *y = p.out + base + c;
+        float *y = p.out + (base + c + (m << S));
         const uint64_t keep = l2_keep_policy();
 #pragma unroll
         for (int r = 0; r < K; ++r) {
-            float *dst = y + (static_cast<int64_t>((r << 8) | m) << p.s);
-            if (p.last) __stcs(dst, __fmul_rn(w[r], p.scale));
+            float *dst = y + (r << (S + 8));
+            if constexpr (kLast) __stcs(dst, __fmul_rn(w[r], p.scale));
             else st_policy(dst, w[r], keep);  // the next launch reads it back
         }
     }
@@ -508,8 +522,8 @@ constexpr int kClusterMaxBits = 24;
 // clusters of that size cannot be scheduled on this device (probed once) it
 // launches nothing and returns GAR_OK with *launched false, and the caller
 // takes the plain passes instead.
-template <int RB, int kIn>
-int launch_cluster_pass(const RhtParams &p, unsigned blocks, cudaStream_t stream, bool *launched) {
+template <int RB, int kIn, bool kLast>
+int launch_cluster_pass_as(const RhtParams &p, unsigned blocks, cudaStream_t stream, bool *launched) {
     static std::atomic<int> ok[64];  // 0: not probed, 1: schedulable, 2: not
     int dev = 0;
     *launched = false;
@@ -532,11 +546,11 @@ int launch_cluster_pass(const RhtParams &p, unsigned blocks, cudaStream_t stream
         int clusters = 0;
         bool good = true;
         if (RB > 3)  // 16 CTAs: above the portable cluster size
-            good = cudaFuncSetAttribute(rht_cluster_pass_kernel<RB, kIn>,
+            good = cudaFuncSetAttribute(rht_cluster_pass_kernel<RB, kIn, kLast>,
                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
         bool refused = !good;
         if (good) {
-            refused = cudaOccupancyMaxActiveClusters(&clusters, rht_cluster_pass_kernel<RB, kIn>, &cfg) !=
+            refused = cudaOccupancyMaxActiveClusters(&clusters, rht_cluster_pass_kernel<RB, kIn, kLast>, &cfg) !=
                       cudaSuccess;
             good = !refused && clusters > 0;
         }
@@ -545,13 +559,25 @@ int launch_cluster_pass(const RhtParams &p, unsigned blocks, cudaStream_t stream
         ok[dev].store(state, std::memory_order_relaxed);
     }
     if (state != 1) return GAR_OK;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, rht_cluster_pass_kernel<RB, kIn>, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, rht_cluster_pass_kernel<RB, kIn, kLast>, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(GAR_ECUDA, "rht_cluster_pass_kernel: %s", cudaGetErrorString(e));
     }
     *launched = true;
     return check_launch("rht_cluster_pass_kernel");
+}
+
+// Launches the cluster pass with 2^RB-CTA clusters and sets *launched; where
+// clusters of that size cannot be scheduled on this device (probed once) it
+// launches nothing and returns GAR_OK with *launched false, and the caller
+// takes the plain passes instead.  The pass must start at index bit 12.
+template <int RB, int kIn>
+int launch_cluster_pass(const RhtParams &p, unsigned blocks, cudaStream_t stream, bool *launched) {
+    *launched = false;
+    if (p.s != kClusterRowBit || p.n > (int64_t{1} << kClusterMaxBits)) return GAR_OK;
+    return p.last ? launch_cluster_pass_as<RB, kIn, true>(p, blocks, stream, launched)
+                  : launch_cluster_pass_as<RB, kIn, false>(p, blocks, stream, launched);
 }
 
 // n < 4096: one CTA, every stage in shared memory (the same kIn, kNorm and
