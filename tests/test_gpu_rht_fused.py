@@ -23,7 +23,7 @@ from helpers import need_cuda, same_bits, to_dev, to_host
 pytestmark = pytest.mark.gpu
 
 U = 2.0 ** -24
-SIZES = [0, 5, 11, 12, 13, 17, 20, 21, 22, 24, 25]
+SIZES = [0, 5, 11, 12, 13, 17, 20, 21, 22, 23, 24, 25]
 
 
 @pytest.fixture(scope="module")
