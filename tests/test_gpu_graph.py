@@ -165,3 +165,77 @@ def test_two_stream_step_captured(env):
     graph.replay()
     torch.cuda.synchronize()
     same(results(), eager2)
+
+
+def test_training_step_captured(env):
+    """THC's section 5 training step through the fused calls -- per worker the
+    error feedback applied inside the forward rotation with the norm's sums,
+    the norm-based range, non-uniform THC (b = 4, g = 36), the inverse
+    rotation of the average, per worker the error-feedback update from its own
+    wire vector -- captured as one graph (cluster launches included; n = 2^21
+    takes the 2-CTA cluster pass, 2^22 the 4-CTA one).  Replays from the same
+    error vectors give the eager step's results bit for bit, two replays in a
+    row the two eager steps'."""
+    torch, g = env
+    P_, b, gr, t_p = 4, 4, 36, 2.15
+    tab = np.rint(np.linspace(0, gr, 16)).astype(np.uint16)
+    for k in (21, 22):
+        n = 1 << k
+        grads = [torch.from_numpy(workloads.student_t_f32(n, 4, 1e-2, 401, w)).cuda() for w in range(P_)]
+        e0 = [torch.from_numpy(workloads.normal_f32(n, 1e-6, 402, w)).cuda() for w in range(P_)]
+        e = [t.clone() for t in e0]
+        ys = [torch.empty(n, device="cuda") for _ in range(P_)]
+        packed = [torch.empty(g.gar_thc_words(n, b), dtype=torch.int32, device="cuda") for _ in range(P_)]
+        sums = [torch.empty(g.gar_rht_tiles(n), dtype=torch.float64, device="cuda") for _ in range(P_)]
+        yt, pt, st = g.pointer_table(ys), g.pointer_table(packed), g.pointer_table(sums)
+        mM = torch.empty(2, device="cuda")
+        avg, est, tmp = (torch.empty(n, device="cuda") for _ in range(3))
+
+        def step():
+            for w in range(P_):
+                g.gar_rht_ef_forward(grads[w], e[w], ys[w], 11, sums[w])
+            g.gar_rht_norm_range_from_sums(st, n, t_p, mM)
+            g.gar_nuhc_allreduce_fused(yt, b, gr, tab, 5, mM, avg, pt)
+            g.gar_rht(avg, est, 11, inverse=True)
+            for w in range(P_):
+                g.gar_rht_ef_update(packed[w], b, gr, tab, mM, grads[w], e[w], tmp, 11)
+
+        def reset():
+            for w in range(P_):
+                e[w].copy_(e0[w])
+
+        def results():
+            out = [mM, avg, est] + ys + packed + e
+            return [t.cpu().numpy().view(np.uint32 if t.dtype != torch.int32 else np.int32).copy() for t in out]
+
+        def same(a, c):
+            for x, y in zip(a, c):
+                assert np.array_equal(x, y)
+
+        reset()
+        step()
+        torch.cuda.synchronize()
+        eager1 = results()
+        step()
+        torch.cuda.synchronize()
+        eager2 = results()
+
+        graph = torch.cuda.CUDAGraph()
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                step()
+        torch.cuda.synchronize()
+        for t in [avg, est, mM] + ys:
+            t.zero_()
+        reset()
+        launches0 = g.gar_launch_count()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert g.gar_launch_count() == launches0
+        same(results(), eager1)
+        graph.replay()
+        torch.cuda.synchronize()
+        same(results(), eager2)
+        assert g.gar_sync_status() == 0
