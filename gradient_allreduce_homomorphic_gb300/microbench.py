@@ -15,8 +15,9 @@ in one call, with THC's range fused in), thc_range, thc_encode, thc_aggregate, t
 thc_fused_packed, nuhc_fused, nuhc_fused_packed (non-uniform THC with a
 table on a granularity-g grid), nmse, train_step, train_step_fused (one step
 of THC's training process over P workers: error feedback, rotation, range,
-non-uniform THC, inverse rotation, error-feedback update; separate or fused
-calls).  Inputs are seeded N(0, 1) draws made on the device;
+non-uniform THC, inverse rotation, error-feedback update; separate calls, or
+the fused ones as training.TrainingStep runs them, the workers' chains over
+--streams side streams).  Inputs are seeded N(0, 1) draws made on the device;
 every size is chosen by the caller, so a case can be kept small enough for a
 profiler capture.  Prints one JSON line: time per call (CUDA events on the
 launching stream, after warm-up) and algorithmic GB/s.
@@ -51,6 +52,8 @@ def main(argv=None):
     ap.add_argument("--dtype", default="f32")
     ap.add_argument("--g", type=int, default=0, help="granularity for the nuhc cases")
     ap.add_argument("--k", type=int, default=64, help="partitions of the stream cases")
+    ap.add_argument("--streams", type=int, default=2,
+                    help="train_step_fused: side streams the workers' chains go round-robin over")
     ap.add_argument("--flush", action="store_true",
                     help="write then read 256 MB (more than L2) before every timed call")
     a = ap.parse_args(argv)
@@ -247,17 +250,10 @@ def main(argv=None):
         avg, est, tmp = (torch.empty(N, device=dev) for _ in range(3))
         t_p = 2.15
         if a.case == "train_step_fused":
-            sums = [torch.empty(g.gar_rht_tiles(N), dtype=torch.float64, device=dev) for _ in range(P)]
-            st = g.pointer_table(sums)
+            from .training import TrainingStep
 
-            def fn():
-                for w in range(P):
-                    g.gar_rht_ef_forward(grads[w], e_work[w], ys[w], 11, sums[w])
-                g.gar_rht_norm_range_from_sums(st, N, t_p, mM)
-                g.gar_nuhc_allreduce_fused(yt, b, gr, tab, 5, mM, avg, pt)
-                g.gar_rht(avg, est, 11, inverse=True)
-                for w in range(P):
-                    g.gar_rht_ef_update(packed[w], b, gr, tab, mM, grads[w], e_work[w], tmp, 11)
+            step = TrainingStep(grads, e_work, b=b, table=tab, t_p=t_p, rht_seed=11, streams=a.streams)
+            fn = lambda: step.run(5)  # noqa: E731
         else:
             xs = [torch.empty(N, device=dev) for _ in range(P)]
             xt = g.pointer_table(xs)
