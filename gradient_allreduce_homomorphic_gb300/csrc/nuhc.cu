@@ -118,16 +118,18 @@ __device__ __forceinline__ void nuhc_index2(float x0, float x1, uint64_t m2, uin
 }
 
 // Direct tables, for granularities up to kDirectMaxG: for every k = 0..g the
-// ends T[z], T[z + 1] of the interval holding k (as floats) and z itself
+// lower end T[z] and the width T[z + 1] - T[z] of the interval holding k (as
+// floats; the decision and the sum of table values need no more) and z itself
 // (k = g belongs to the last interval).  One lookup by k replaces the two
-// dependent ones k -> z -> (T[z], T[z + 1]); the lower and upper ends sit in
-// separate arrays, so that two elements' ends load straight into the register
-// pairs of the f32x2 instructions.  The result equals nuhc_index bit for bit:
+// dependent ones k -> z -> (T[z], T[z + 1]); ends and widths sit in separate
+// arrays, so that two elements' values load straight into the register pairs
+// of the f32x2 instructions.  The result equals nuhc_index bit for bit:
 // for k <= g - 1 the interval is the same, and for k = g (t = G) the old
 // lookup clamps k to g - 1, which lies in the same last interval.
 constexpr int kDirectMaxG = 1023;
 constexpr int kDirectCap = kDirectMaxG + 1;
-// s_lo[kDirectCap], s_hi[kDirectCap], s_zb[kDirectCap] (floats; s_zb[k] = z + 2^23, exact),
+// s_lo[kDirectCap], s_w[kDirectCap], s_zb[kDirectCap] (floats: the interval's lower end T[z], its
+// width w = T[z + 1] - T[z] and z + 2^23, all exact),
 // s_z[kDirectCap] (bytes), then T itself
 constexpr size_t kDirectBytes = kDirectCap * (3 * sizeof(float) + 1) + 256 * sizeof(uint16_t);
 constexpr float kTwo23 = 8388608.0f;
@@ -136,8 +138,8 @@ constexpr uint32_t kTwo23Bits = 0x4B000000u;  // the bits of 2^23; of z + 2^23: 
 __device__ __forceinline__ void nuhc_load_direct(const NuhcTable &tab, unsigned char *mem, float *&s_lo,
                                                  uint8_t *&s_z) {
     s_lo = reinterpret_cast<float *>(mem);
-    float *s_hi = s_lo + kDirectCap;
-    float *s_zb = s_hi + kDirectCap;
+    float *s_w = s_lo + kDirectCap;
+    float *s_zb = s_w + kDirectCap;
     s_z = reinterpret_cast<uint8_t *>(s_zb + kDirectCap);
     uint16_t *s_t = reinterpret_cast<uint16_t *>(s_z + kDirectCap);
     for (int z = threadIdx.x; z <= tab.L; z += blockDim.x) s_t[z] = tab.t[z];
@@ -150,7 +152,7 @@ __device__ __forceinline__ void nuhc_load_direct(const NuhcTable &tab, unsigned 
             else hi = mid - 1;
         }
         s_lo[k] = static_cast<float>(s_t[lo]);
-        s_hi[k] = static_cast<float>(s_t[lo + 1]);
+        s_w[k] = static_cast<float>(s_t[lo + 1] - s_t[lo]);
         s_zb[k] = kTwo23 + static_cast<float>(lo);
         s_z[k] = static_cast<uint8_t>(lo);
     }
@@ -163,10 +165,10 @@ __device__ __forceinline__ uint32_t nuhc_direct(float x, float m, float sc, floa
     float t = __fmul_rn(__fsub_rn(x, m), sc);
     t = fminf(fmaxf(t, 0.0f), G);
     const int k = __float_as_int(__fadd_rd(t, 8388608.0f)) - 0x4B000000;  // floor(t), 0..g
-    const float lo = s_lo[k], hi = s_lo[kDirectCap + k];
+    const float lo = s_lo[k], w = s_lo[kDirectCap + k];
     const float u = __fsub_rn(__uint_as_float((r & 0x007FFFFFu) | 0x3F800000u), 1.0f);
-    const bool up = __fmaf_rn(-u, __fsub_rn(hi, lo), __fsub_rn(t, lo)) > 0.0f;
-    tv = up ? hi : lo;
+    const bool up = __fmaf_rn(-u, w, __fsub_rn(t, lo)) > 0.0f;
+    tv = up ? __fadd_rn(lo, w) : lo;  // T[z + 1], exact
     return static_cast<uint32_t>(s_z[k]) + (up ? 1u : 0u);
 }
 
@@ -183,15 +185,15 @@ __device__ __forceinline__ void nuhc_direct2(float x0, float x1, uint64_t m2, ui
     const float2 jm = unpack_f2(add_rm_f2(t2, pack_f2(8388608.0f, 8388608.0f)));  // floor(t) + 2^23
     const int k0 = __float_as_int(jm.x) - 0x4B000000, k1 = __float_as_int(jm.y) - 0x4B000000;  // 0..g
     const float lo0 = s_lo[k0], lo1 = s_lo[k1];
-    const float hi0 = s_lo[kDirectCap + k0], hi1 = s_lo[kDirectCap + k1];
-    const uint64_t lo = pack_f2(lo0, lo1), hi = pack_f2(hi0, hi1);
+    const uint64_t lo = pack_f2(lo0, lo1), w = pack_f2(s_lo[kDirectCap + k0], s_lo[kDirectCap + k1]);
+    const float2 hi2 = unpack_f2(add_rn_f2(lo, w));  // T[z + 1], exact
+    const float hi0 = hi2.x, hi1 = hi2.y;
     const uint64_t one_u = pack_f2(__uint_as_float((r0 & 0x007FFFFFu) | 0x3F800000u),
                                    __uint_as_float((r1 & 0x007FFFFFu) | 0x3F800000u));
     // up iff lo + u w < t (w = hi - lo), decided exactly as (lo + u w) rounded
     // down < t: rounding down never passes the float t.  lo + u w is formed
     // with one rounding as fma((1 + u), w, lo - w); w and lo - w are exact
     // (integers below 2^15).  Equal to nuhc_index's fma(-u, w, t - lo) > 0.
-    const uint64_t w = sub_rn_f2(hi, lo);
     const float2 v = unpack_f2(fma_rm_f2(one_u, w, sub_rn_f2(lo, w)));
     const bool up0 = v.x < t.x, up1 = v.y < t.y;
     tv0 = up0 ? hi0 : lo0;
@@ -218,11 +220,10 @@ __device__ __forceinline__ void nuhc_direct2_sum(float x0, float x1, uint64_t m2
     const float2 jm = unpack_f2(add_rm_f2(t2, pack_f2(kTwo23, kTwo23)));  // floor(t) + 2^23
     const int k0 = __float_as_int(jm.x) - 0x4B000000, k1 = __float_as_int(jm.y) - 0x4B000000;  // 0..g
     const uint64_t lo = pack_f2(s_lo[k0], s_lo[k1]);
-    const uint64_t hi = pack_f2(s_lo[kDirectCap + k0], s_lo[kDirectCap + k1]);
+    const uint64_t w = pack_f2(s_lo[kDirectCap + k0], s_lo[kDirectCap + k1]);  // T[z + 1] - T[z]
     const uint64_t one_u = pack_f2(__uint_as_float((r0 & 0x007FFFFFu) | 0x3F800000u),
                                    __uint_as_float((r1 & 0x007FFFFFu) | 0x3F800000u));
     // up iff RD(lo + u w) < t, as in nuhc_direct2
-    const uint64_t w = sub_rn_f2(hi, lo);
     const float2 v = unpack_f2(fma_rm_f2(one_u, w, sub_rn_f2(lo, w)));
     float u0, u1;
     asm("set.lt.f32.f32 %0, %1, %2;" : "=f"(u0) : "f"(v.x), "f"(t.x));
@@ -379,7 +380,7 @@ __device__ __forceinline__ void nuhc_one_worker(const float4 (&v)[G4], float (&s
                                                 const float2 *s_pair, const uint8_t *s_inv) {
     uint32_t word = 0;
     if constexpr (kDirect) {
-        // direct tables: s_pair holds s_lo (then s_hi, s_zb)
+        // direct tables: s_pair holds s_lo (then s_w, s_zb)
         const float *s_lo = reinterpret_cast<const float *>(s_pair);
 #pragma unroll
         for (int g4 = 0; g4 < G4; ++g4) {
