@@ -177,6 +177,7 @@ def test_training_step_captured(env):
     error vectors give the eager step's results bit for bit, two replays in a
     row the two eager steps'."""
     torch, g = env
+    g.gar_sync_status(clear=True)  # earlier tests may have left a bit set
     P_, b, gr, t_p = 4, 4, 36, 2.15
     tab = np.rint(np.linspace(0, gr, 16)).astype(np.uint16)
     for k in (21, 22):

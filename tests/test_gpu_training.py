@@ -59,6 +59,7 @@ def test_stream_counts_agree(env, k, b, g):
 
     n = 1 << k
     table = _table(b, g) if g else None
+    gar.gar_sync_status(clear=True)  # earlier tests may have left a bit set
     snaps = {}
     for streams in (1, 2, 3):
         grads, errs = _inputs(torch, n, k)
