@@ -75,6 +75,8 @@ _SIGNATURES = {
     "gar_nuhc_aggregate": (C.c_int, [_pp, _i32, _i64, _i32, _vp, _vp, _vp]),
     "gar_nuhc_decode": (C.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _vp]),
     "gar_nuhc_allreduce_fused": (C.c_int, [_pp, _i32, _i64, _i32, _i32, _vp, _u64, _vp, _vp, _pp, _vp]),
+    "gar_nuhc_allreduce_fused_masked": (C.c_int, [_pp, _i32, _u64, _i64, _i32, _i32, _vp, _u64, _vp, _vp, _pp,
+                                                  _vp]),
     "gar_rht": (C.c_int, [_vp, _vp, _i64, _u64, _i32, _vp]),
     "gar_rht_norm_range_workspace_bytes": (C.c_size_t, [_i32, _i64]),
     "gar_rht_norm_range": (C.c_int, [_pp, _i32, _i64, C.c_double, _vp, _vp, C.c_size_t, _vp]),
@@ -519,6 +521,17 @@ def gar_nuhc_allreduce_fused(x, b: int, g: int, table, seed: int, d_mM, avg, pac
     pk = pointer_table(packed).array if packed is not None else None
     _call("gar_nuhc_allreduce_fused", xt.array, len(xt), xt.numel, b, g, tp, seed, _dev(d_mM), _dev(avg), pk,
           _stream(stream))
+
+
+def gar_nuhc_allreduce_fused_masked(x, arrived: int, b: int, g: int, table, seed: int, d_mM, avg, packed=None,
+                                    stream=None):
+    """Non-uniform THC round over the workers whose bit is set in `arrived`
+    (stragglers dropped); x[w] / packed[w] of the others may be None."""
+    t, tp = _table(table)
+    xt = pointer_table(x, allow_none=True)
+    pk = pointer_table(packed, allow_none=True).array if packed is not None else None
+    _call("gar_nuhc_allreduce_fused_masked", xt.array, len(xt), arrived, xt.numel, b, g, tp, seed, _dev(d_mM),
+          _dev(avg), pk, _stream(stream))
 
 
 # ------------------------------------------- RHT, range and error feedback

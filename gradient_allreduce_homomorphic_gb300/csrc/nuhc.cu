@@ -360,13 +360,14 @@ __global__ void __launch_bounds__(kThreads) nuhc_aggregate_kernel(const __grid_c
 struct NuhcFusedParams {
     PhiloxKeys keys;
     NuhcTable tab;
-    const float *x[GAR_MAX_WORKERS];
+    const float *x[GAR_MAX_WORKERS];    // the P contributing workers, slot by slot
     uint32_t *packed[GAR_MAX_WORKERS];
+    int32_t wid[GAR_MAX_WORKERS];       // worker id of each slot (keys its Philox stream)
     const float *mM;
     float *avg;
     int64_t N;
     int64_t nwords;
-    int32_t P;
+    int32_t P;                          // contributing workers (the decode divides by this)
     int32_t vec;
 };
 
@@ -376,15 +377,15 @@ struct NuhcFusedParams {
 // (The sums of table values are integers below 2^24: exact in fp32.)
 template <int B, bool kPacked, bool kDirect, int G4>
 __device__ __forceinline__ void nuhc_one_worker(const float4 (&v)[G4], float (&s)[4 * G4], int64_t e0, int64_t w,
-                                                int wk, const NuhcFusedParams &p, uint64_t m2, uint64_t sc2, float G,
-                                                const float2 *s_pair, const uint8_t *s_inv) {
+                                                int wk, int wid, const NuhcFusedParams &p, uint64_t m2,
+                                                uint64_t sc2, float G, const float2 *s_pair, const uint8_t *s_inv) {
     uint32_t word = 0;
     if constexpr (kDirect) {
         // direct tables: s_pair holds s_lo (then s_w, s_zb)
         const float *s_lo = reinterpret_cast<const float *>(s_pair);
 #pragma unroll
         for (int g4 = 0; g4 < G4; ++g4) {
-            const uint4 r = philox_block((e0 >> 2) + g4, wk, p.keys);
+            const uint4 r = philox_block((e0 >> 2) + g4, wid, p.keys);
             uint64_t s01 = pack_f2(s[4 * g4], s[4 * g4 + 1]), s23 = pack_f2(s[4 * g4 + 2], s[4 * g4 + 3]);
             uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
             nuhc_direct2_sum<kPacked>(v[g4].x, v[g4].y, m2, sc2, G, s_lo, r.x, r.y, s01, a0, a1);
@@ -403,7 +404,7 @@ __device__ __forceinline__ void nuhc_one_worker(const float4 (&v)[G4], float (&s
     }
 #pragma unroll
     for (int g4 = 0; g4 < G4; ++g4) {
-        const uint4 r = philox_block((e0 >> 2) + g4, wk, p.keys);
+        const uint4 r = philox_block((e0 >> 2) + g4, wid, p.keys);
         float t0, t1, t2, t3;
         uint32_t i0 = 0, i1 = 0, i2 = 0, i3 = 0;
         {
@@ -474,12 +475,15 @@ __global__ void __launch_bounds__(kThreads, B == 4 ? 4 : 1) nuhc_fused_kernel(co
 #pragma unroll
                     for (int g4 = 0; g4 < G4; ++g4) vb[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk + 1] + e0) + g4);
                 }
-                nuhc_one_worker<B, kPacked, kDirect>(va, s, e0, w, wk, p, m2, sc2, G, s_pair, s_inv);
+                nuhc_one_worker<B, kPacked, kDirect>(va, s, e0, w, wk, kP > 0 ? wk : p.wid[wk], p, m2, sc2, G, s_pair,
+                                                     s_inv);
                 if (wk + 2 < P) {
 #pragma unroll
                     for (int g4 = 0; g4 < G4; ++g4) va[g4] = __ldcs(reinterpret_cast<const float4 *>(p.x[wk + 2] + e0) + g4);
                 }
-                if (has1) nuhc_one_worker<B, kPacked, kDirect>(vb, s, e0, w, wk + 1, p, m2, sc2, G, s_pair, s_inv);
+                if (has1)
+                    nuhc_one_worker<B, kPacked, kDirect>(vb, s, e0, w, wk + 1, kP > 0 ? wk + 1 : p.wid[wk + 1], p, m2,
+                                                         sc2, G, s_pair, s_inv);
             }
             float4 *dst = reinterpret_cast<float4 *>(p.avg + e0);
 #pragma unroll
@@ -492,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, B == 4 ? 4 : 1) nuhc_fused_kernel(co
                 for (int g4 = 0; g4 < G4; ++g4) {
                     const int64_t eb = e0 + 4 * g4;
                     if (eb >= p.N) break;
-                    const uint4 r = philox_block(eb >> 2, wk, p.keys);
+                    const uint4 r = philox_block(eb >> 2, kP > 0 ? wk : p.wid[wk], p.keys);
                     for (int i = 0; i < 4 && eb + i < p.N; ++i) {
                         float tv;
                         const uint32_t idx =
@@ -644,16 +648,24 @@ extern "C" int gar_nuhc_decode(const uint16_t *sums, int64_t N, const float *d_m
     return launch_grid_decode(sums, N, d_mM, g, P, avg, reinterpret_cast<cudaStream_t>(stream_));
 }
 
-extern "C" int gar_nuhc_allreduce_fused(const float *const *x, int32_t P, int64_t N, int32_t b, int32_t g,
-                                        const uint16_t *table, uint64_t seed, const float *d_mM, float *avg,
-                                        uint32_t *const *packed, gar_stream_t stream_) {
+// The fused round over the workers whose bit is set in `arrived` (all of
+// them for gar_nuhc_allreduce_fused): each arrived worker takes the next
+// slot under its own worker id.  The kernels built for 4, 8 or 16 workers key
+// Philox by the slot, so a round whose slots are not the ids 0 .. P-1 takes
+// the build for any worker count, which reads the ids.
+static int nuhc_fused_entry(const float *const *x, int32_t P, uint64_t arrived, int64_t N, int32_t b, int32_t g,
+                            const uint16_t *table, uint64_t seed, const float *d_mM, float *avg,
+                            uint32_t *const *packed, gar_stream_t stream_) {
     if (!valid_b(b)) return fail(GAR_EINVAL, "b=%d not in {1, 2, 4, 8}", b);
     if (P < 1 || P > GAR_MAX_WORKERS) return fail(GAR_EINVAL, "P=%d outside [1, %d]", P, GAR_MAX_WORKERS);
+    if (P < 64) arrived &= (uint64_t{1} << P) - 1u;
+    const int p_eff = __builtin_popcountll(arrived);
+    if (p_eff == 0) return fail(GAR_EINVAL, "no worker arrived");
     NuhcFusedParams p;
     std::memset(&p, 0, sizeof(p));
     int rc = nuhc_table(table, b, g, p.tab);
     if (rc) return rc;
-    if (static_cast<int64_t>(P) * g > 65535) return fail(GAR_EOVERFLOW, "P * g > 65535");
+    if (static_cast<int64_t>(p_eff) * g > 65535) return fail(GAR_EOVERFLOW, "P * g > 65535");
     if (N < 0 || !d_mM || !x) return fail(GAR_EINVAL, "N < 0 or NULL argument");
     if (N == 0) return GAR_OK;
     if (!avg) return fail(GAR_EINVAL, "avg is NULL");
@@ -663,24 +675,31 @@ extern "C" int gar_nuhc_allreduce_fused(const float *const *x, int32_t P, int64_
     p.avg = avg;
     p.N = N;
     p.nwords = gar_thc_words(N, b);
-    p.P = P;
+    p.P = p_eff;
     p.vec = aligned(avg, 16) ? 1 : 0;
+    bool ids_are_slots = true;
+    int slot = 0;
     for (int w = 0; w < P; ++w) {
+        if (!((arrived >> w) & 1u)) continue;
         if (!x[w]) return fail(GAR_EINVAL, "input %d is NULL", w);
         if (!aligned(x[w], 4)) return fail(GAR_EALIGN, "input %d not 4-byte aligned", w);
-        p.x[w] = x[w];
+        p.x[slot] = x[w];
+        p.wid[slot] = w;
+        ids_are_slots = ids_are_slots && w == slot;
         p.vec = p.vec && aligned(x[w], 16);
         if (packed) {
             if (!packed[w]) return fail(GAR_EINVAL, "packed vector %d is NULL", w);
             if (!aligned(packed[w], 4)) return fail(GAR_EALIGN, "packed vector %d not 4-byte aligned", w);
-            p.packed[w] = packed[w];
+            p.packed[slot] = packed[w];
         }
+        ++slot;
     }
+    const int P_build = ids_are_slots ? p_eff : 0;  // 0: the build for any worker count
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     const bool direct = g <= kDirectMaxG;
     const size_t smem = direct ? kDirectBytes : kNuhcPairBytes + static_cast<size_t>(g);
     const unsigned tiles = static_cast<unsigned>(ceil_div(p.nwords, int64_t{2 * kThreads}));
-#define GAR_NUHC_LAUNCH(BB, PK) launch_nuhc_fused<BB, PK>(p, direct, P, tiles, smem, stream);
+#define GAR_NUHC_LAUNCH(BB, PK) launch_nuhc_fused<BB, PK>(p, direct, P_build, tiles, smem, stream);
 #define GAR_NUHC_CASE(BB)                 \
     case BB:                              \
         if (packed) {                     \
@@ -698,4 +717,17 @@ extern "C" int gar_nuhc_allreduce_fused(const float *const *x, int32_t P, int64_
 #undef GAR_NUHC_CASE
 #undef GAR_NUHC_LAUNCH
     return check_launch("nuhc_fused_kernel");
+}
+
+extern "C" int gar_nuhc_allreduce_fused(const float *const *x, int32_t P, int64_t N, int32_t b, int32_t g,
+                                        const uint16_t *table, uint64_t seed, const float *d_mM, float *avg,
+                                        uint32_t *const *packed, gar_stream_t stream) {
+    return nuhc_fused_entry(x, P, ~uint64_t{0}, N, b, g, table, seed, d_mM, avg, packed, stream);
+}
+
+extern "C" int gar_nuhc_allreduce_fused_masked(const float *const *x, int32_t P, uint64_t arrived, int64_t N,
+                                               int32_t b, int32_t g, const uint16_t *table, uint64_t seed,
+                                               const float *d_mM, float *avg, uint32_t *const *packed,
+                                               gar_stream_t stream) {
+    return nuhc_fused_entry(x, P, arrived, N, b, g, table, seed, d_mM, avg, packed, stream);
 }

@@ -464,6 +464,22 @@ int gar_nuhc_allreduce_fused(const float *const *x, int32_t P, int64_t N, int32_
                              const uint16_t *table, uint64_t seed, const float *d_mM, float *avg,
                              uint32_t *const *packed, gar_stream_t stream);
 
+/* gar_nuhc_allreduce_fused_masked -- straggler dropping ([T] section 8,
+ * stragglers: the PS waits only for the workers that arrived) with
+ * non-uniform THC ([T] section 5, Algorithm 2).  Only the workers whose bit
+ * is set in `arrived` (bit w = worker w, w < P) are encoded, each under its
+ * own worker id, and their table values summed; the decode divides by their
+ * number.  x[w] and packed[w] of the other workers are not read or written
+ * (they may be NULL).  With every bit set this is gar_nuhc_allreduce_fused
+ * bit for bit; it also equals gar_nuhc_encode of the arrived workers (their
+ * own ids) -> gar_nuhc_aggregate over their vectors -> gar_nuhc_decode with
+ * their number.  Errors: as gar_nuhc_allreduce_fused (GAR_EOVERFLOW when the
+ * number arrived times g exceeds 65535), and GAR_EINVAL when no worker
+ * arrived. */
+int gar_nuhc_allreduce_fused_masked(const float *const *x, int32_t P, uint64_t arrived, int64_t N, int32_t b,
+                                    int32_t g, const uint16_t *table, uint64_t seed, const float *d_mM, float *avg,
+                                    uint32_t *const *packed, gar_stream_t stream);
+
 /* ===================================================================== */
 /* Pre- and post-processing [T] section 5 (RHT, truncation, error feedback) */
 /* ===================================================================== */

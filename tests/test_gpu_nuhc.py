@@ -174,3 +174,60 @@ def test_sweep_shape_full_size(env, P):
         assert err <= tol, (lo, err, tol)
     del xd, pk
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("P,arrived", [(8, 0b11111111), (8, 0b10110110), (8, 0b00000001), (16, 0xF0F0),
+                                       (5, 0b10110), (4, 0b1111)])
+@pytest.mark.parametrize("b,g", [(4, 36), (2, 9), (8, 300)])
+def test_straggler_masked(env, P, arrived, b, g):
+    """Stragglers dropped with non-uniform THC: only the arrived workers
+    encode, under their own ids, and their table values are summed; the
+    decode divides by their number.  Against the oracle's encode of the arrived
+    workers (own ids) -> aggregate -> decode; equal to the separate kernels
+    over their vectors; all arrived = the unmasked kernel bit for bit (the
+    kernels built for 4, 8 or 16 workers, which key Philox by the slot)."""
+    torch, gar = env
+    N, seed = 20011, 4343
+    T = s_curve_table(b, g)
+    xs = _xs(P, N, 131)
+    ids = [w for w in range(P) if (arrived >> w) & 1]
+    m, M = oracle.thc_range([xs[w] for w in ids])
+    mM = torch.tensor([m, M], dtype=torch.float32, device="cuda")
+    xd = [to_dev(x, torch) if w in ids else None for w, x in enumerate(xs)]
+    pk = [torch.zeros(max(gar.gar_thc_words(N, b), 1), dtype=torch.int32, device="cuda") if w in ids else None
+          for w in range(P)]
+    avg = torch.empty(N, device="cuda")
+    gar.gar_nuhc_allreduce_fused_masked(xd, arrived, b, g, T, seed, mM, avg, pk)
+    ref_pk = {w: oracle.nuhc_encode(xs[w], m, M, b, g, T, seed, w) for w in ids}
+    for w in ids:
+        np.testing.assert_array_equal(to_host(pk[w])[:ref_pk[w].size], ref_pk[w], err_msg=f"worker {w}")
+    ref_avg = oracle.nuhc_decode(oracle.nuhc_aggregate([ref_pk[w] for w in ids], N, b, T), m, M, g, len(ids))
+    assert np.max(np.abs(to_host(avg).astype(np.float64) - ref_avg)) <= 1e-6 * max(abs(m), abs(M))
+    sums = torch.empty(N + 1, dtype=torch.int16, device="cuda")[:N]
+    gar.gar_nuhc_aggregate([pk[w] for w in ids], N, b, T, sums)
+    avg2 = torch.empty(N, device="cuda")
+    gar.gar_nuhc_decode(sums, mM, g, len(ids), avg2)
+    assert torch.equal(avg.view(torch.int32), avg2.view(torch.int32))
+    if arrived == (1 << P) - 1:
+        avg3 = torch.empty(N, device="cuda")
+        pk3 = _words(gar, N, b, P, torch)
+        gar.gar_nuhc_allreduce_fused(xd, b, g, T, seed, mM, avg3, pk3)
+        assert torch.equal(avg.view(torch.int32), avg3.view(torch.int32))
+        for w in range(P):
+            assert torch.equal(pk[w], pk3[w])
+
+
+def test_straggler_masked_rejects(env):
+    torch, gar = env
+    T = s_curve_table(4, 36)
+    x = [torch.zeros(64, device="cuda") for _ in range(3)]
+    mM = torch.zeros(2, device="cuda")
+    with pytest.raises(gar.GarError):  # nobody arrived
+        gar.gar_nuhc_allreduce_fused_masked(x, 0, 4, 36, T, 1, mM, torch.empty(64, device="cuda"))
+    with pytest.raises(gar.GarError):  # an arrived worker without input
+        gar.gar_nuhc_allreduce_fused_masked([x[0], None, x[2]], 0b111, 4, 36, T, 1, mM,
+                                            torch.empty(64, device="cuda"))
+    big = [torch.zeros(64, device="cuda") for _ in range(64)]
+    with pytest.raises(gar.GarError):  # 64 arrived x g = 4000 overflows the 16-bit sums
+        gar.gar_nuhc_allreduce_fused_masked(big, ~0 & ((1 << 64) - 1), 4, 4000, s_curve_table(4, 4000), 1, mM,
+                                            torch.empty(64, device="cuda"))
