@@ -1,7 +1,8 @@
 """The C ABI from plain C: tests/c_abi/ring_thc.c is compiled with gcc
 against include/gar.h, libgar.so and the CUDA runtime (no Python or PyTorch
-in the program) and run on the GPU; it checks the ring average exactly and a
-THC round within its quantization step."""
+in the program) and run on the GPU; it checks the ring average exactly, a
+uniform and a non-uniform THC round within their quantization intervals and
+an RHT round trip within the transform's error bound."""
 import glob
 import os
 import shutil
