@@ -68,7 +68,7 @@ class TrainingStep:
         self.b, self.t_p, self.rht_seed = b, float(t_p), rht_seed
         self.table = None if table is None else np.asarray(table, np.uint16)
         self.g = (1 << b) - 1 if self.table is None else int(self.table[-1])
-        dev = grads[0].device
+        dev = self.device = grads[0].device
         self.ys = [torch.empty(self.n, device=dev) for _ in range(self.P)]
         self.packed = [torch.empty(max(gar_thc_words(self.n, b), 1), dtype=torch.int32, device=dev)
                        for _ in range(self.P)]
@@ -98,7 +98,7 @@ class TrainingStep:
         from it and join it); THC's draws are keyed by `seed`."""
         import torch
 
-        main = torch.cuda.current_stream()
+        main = torch.cuda.current_stream(self.device)
         self._fork(main)
         for w in range(self.P):
             gar_rht_ef_forward(self.grads[w], self.errs[w], self.ys[w], self.rht_seed, self.sums[w],
