@@ -246,7 +246,12 @@ def run_ours(args, rank, world, dist):
     torch.cuda.synchronize()
 
     # ---- device-timed region: inputs resident in HBM; no instrumentation
-    # inside it (the stage breakdown below takes its own pass)
+    # inside it (the stage breakdown below takes its own pass).  A spin
+    # before the start event holds the stream while the host queues the K
+    # steps, so that the events time the GPU's work and not the host's
+    # queueing: the clock sampler's nvidia-smi queries can stall the host's
+    # launches for tens of milliseconds (once seen: 2.45 ms a step against
+    # 0.80), and a GPU that has run out of queued work would count that.
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -254,6 +259,7 @@ def run_ours(args, rank, world, dist):
     torch.cuda.synchronize()
     launches0 = g.gar_launch_count()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(int(min(0.5e-3 * args.steps, 0.25) * 2.07e9))  # ~0.5 ms of SM cycles per step queued
     start.record()
     for i in range(args.steps):
         st.run(step_seed(args.warmup + i), args.schedule)
@@ -293,6 +299,29 @@ def run_ours(args, rank, world, dist):
             st.run(step_seed(20_003 + i), "serial", sevs[i])
         torch.cuda.synchronize()
         serial_stage_ms = mean_stage_ms(sevs)
+
+    # ---- the same step captured once in a CUDA graph and replayed K times
+    # (the graph holds the two streams' fork, events and join; its THC seed
+    # is the one it was captured with, so it is reported beside the eager
+    # steps, each with its own seed, not instead of them)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            st.run(step_seed(30_000), args.schedule)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record()
+    for _ in range(args.steps):
+        graph.replay()
+    g1.record()
+    torch.cuda.synchronize()
+    graph_ms = g0.elapsed_time(g1) / args.steps
+    del graph
 
     # ---- end to end: pinned host gradients in; both averages and the NMSE
     # out (and, beside it, the NMSE alone out)
@@ -365,6 +394,9 @@ def run_ours(args, rank, world, dist):
                 "nmse": "sums inside the THC pass" if args.nmse == "fused" else "one pass over both averages"},
         "elements_per_s": round(world * P * n_params / (ms * 1e-3), 1),
         "hbm_fraction_of_step": round(sum(algo.values()) / (ms * 1e-3) / 1e9 / peak, 4),
+        "graph": {"ms_per_step": round(graph_ms, 4),
+                  "value": round(world * P * n_params * 4 / (graph_ms * 1e-3) / 1e9, 2),
+                  "what": "the step captured once in a CUDA graph, replayed K times (one THC seed)"},
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "stage_ms_alone": {k: round(v, 4) for k, v in serial_stage_ms.items()},
         "stage_gbs_alone": {k: round(algo[k] / (serial_stage_ms[k] * 1e-3) / 1e9, 1) for k in serial_stage_ms},
